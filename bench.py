@@ -1,0 +1,410 @@
+"""Benchmark of GB300-native KDA prefill (head-tokens/s and us per call).
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
+
+One step is one kda_prefill call (chunk preparation + recurrence, and the
+varlen metadata kernel for packed input) over one batch of synthetic input
+already resident in HBM.  The default workload is B=1, H=6, T=8192, d=128
+("FlashKDA column split", section 4: the small-head tensor-parallel shard at
+8,192 tokens); a secondary line item times B=1, H=96, T=8192 the same way.
+Between timed steps a 512 MiB buffer is written to flush the 129 MB L2.
+
+Reported: `value` = head-tokens/s over the timed steps (device time, CUDA
+events on the launching stream); `e2e` = the same metric with the inputs
+copied host->device from pinned memory and the outputs copied back inside
+every timed step; `roofline` for the dominant kernel (events recorded by the
+library around its kernels during the timed steps); `cpu_baseline` = the FP64
+oracle timed on this host's cores.  `--impl reference` times that oracle
+alone on a bounded sample of the same workload (the pages name no runnable
+reference implementation).  Under torchrun every rank runs its own replica of
+the workload on its own GPU (weak scaling, no collective in the data path).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import torch  # noqa: E402
+
+from kimi_delta_attention_kda_gb300 import synthetic  # noqa: E402
+
+METRIC = "KDA prefill head-tokens/sec and us/call at T=8192, H=6 and H=96 (GB300)"
+UNIT = "head-tokens/s"
+# Page numbers for this workload (B200, both kernels, T=8192; "FlashKDA column
+# split", section 4): FlashKDA 731.7 us at H=6 and 1,032.6 us at H=96.
+FLASHKDA_B200_US = {"t8192_h6": 731.7, "t8192_h96": 1032.6}
+COLUMN_SPLIT_B200_US = {"t8192_h6": 283.4, "t8192_h96": 914.7}
+L2_FLUSH_BYTES = 512 << 20
+
+# Algorithmic bytes per head-token of each kernel:
+#   preparation: reads q, k (2 x 256 B), g (512 B), beta (2 B); writes one
+#                13,824-byte packet per 16 tokens (864 B per head-token).
+#   recurrence:  reads the packets (864 B) and v (256 B); writes O (256 B);
+#                plus 32 KB per (sequence, head) for each state read or written.
+PACKET_PER_TOKEN = 13824 / 16
+PREP_BYTES_PER_HT = 2 * 256 + 512 + 2 + PACKET_PER_TOKEN
+REC_BYTES_PER_HT = PACKET_PER_TOKEN + 256 + 256
+STATE_BYTES = 128 * 128 * 2
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+class ClockSampler:
+    """nvidia-smi samples of SM clock and throttle reasons during a region."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+
+    def __enter__(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu), "--query-gpu=" + self.FIELDS,
+                 "--format=csv,noheader,nounits", "-lms", "50"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        self.lines = []
+        if self.proc is not None:
+            time.sleep(0.1)
+            self.proc.terminate()
+            try:
+                out, _ = self.proc.communicate(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+                out, _ = self.proc.communicate()
+            self.lines = [ln for ln in out.splitlines() if ln.strip()]
+        return False
+
+    def summary(self):
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for ln in getattr(self, "lines", []):
+            parts = [p.strip() for p in ln.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for name, val in zip(names, parts[5:9]):
+                if val.lower().startswith("active"):
+                    reasons.add(name)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def device_inputs(inp, device):
+    return {k: (None if inp[k] is None else inp[k].to(device))
+            for k in ("q", "k", "v", "g", "beta", "init_state", "cu_seqlens")}
+
+
+def head_tokens(inp):
+    return int(inp["q"].shape[0] * inp["q"].shape[1] * inp["q"].shape[2])
+
+
+def time_kernel_steps(kda, d, steps, warmup, flush, stream, profile=False):
+    """Device time of `steps` kda_prefill calls (L2 flushed before each)."""
+    out = torch.empty_like(d["v"])
+    N = d["init_state"].shape[0] if d["init_state"] is not None else d["q"].shape[0]
+    if d["cu_seqlens"] is not None:
+        N = d["cu_seqlens"].numel() - 1
+    H = d["q"].shape[2]
+    fin = torch.empty((N, H, 128, 128), dtype=torch.bfloat16, device=d["q"].device)
+
+    def call():
+        kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                        cu_seqlens=d["cu_seqlens"], out=out, final_state=fin, stream=stream)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            call()
+        stream.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        if profile:
+            kda._lib.profile_begin(steps)
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            call()
+            ends[i].record(stream)
+        stream.synchronize()
+        prof = kda._lib.profile_end() if profile else None
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return ms, prof
+
+
+def time_e2e_steps(kda, inp, steps, warmup, flush, stream, device):
+    """Same metric through the public API with host buffers: every step copies
+    its inputs host->device (pinned) and its outputs device->host."""
+    host = {k: (None if inp[k] is None else inp[k].pin_memory())
+            for k in ("q", "k", "v", "g", "beta", "init_state", "cu_seqlens")}
+    dev = {k: (None if v is None else torch.empty_like(v, device=device)) for k, v in host.items()}
+    H = inp["q"].shape[2]
+    N = inp["N"]
+    out_d = torch.empty_like(dev["v"])
+    fin_d = torch.empty((N, H, 128, 128), dtype=torch.bfloat16, device=device)
+    out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
+    fin_h = torch.empty(fin_d.shape, dtype=fin_d.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
+    d2h = out_h.numel() * 2 + fin_h.numel() * 2
+
+    def step():
+        for k, t in host.items():
+            if t is not None:
+                dev[k].copy_(t, non_blocking=True)
+        kda.kda_prefill(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["init_state"],
+                        cu_seqlens=dev["cu_seqlens"], out=out_d, final_state=fin_d, stream=stream)
+        out_h.copy_(out_d, non_blocking=True)
+        fin_h.copy_(fin_d, non_blocking=True)
+
+    with torch.cuda.stream(stream):
+        for _ in range(warmup):
+            flush.zero_()
+            step()
+        stream.synchronize()
+        starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
+        for i in range(steps):
+            flush.zero_()
+            starts[i].record(stream)
+            step()
+            ends[i].record(stream)
+        stream.synchronize()
+    ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
+    return ms, h2d, d2h
+
+
+def cpu_baseline(name, min_seconds=10.0):
+    """The FP64 oracle, as it stands, on this host's cores, over the whole
+    workload repeated until about `min_seconds` of CPU work have run."""
+    import oracle
+    inp = synthetic.make_workload(name)
+    cu = inp["cu_seqlens"]
+    reps, total = 0, 0.0
+    while total < min_seconds and reps < 100:
+        t0 = time.perf_counter()
+        oracle.kda_token(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"], inp["init_state"],
+                         cu_seqlens=None if cu is None else cu.numpy())
+        total += time.perf_counter() - t0
+        reps += 1
+    ht = head_tokens(inp)
+    return {"value": ht * reps / total, "unit": UNIT, "cores": oracle.num_threads(),
+            "kind": "oracle",
+            "sample": "the whole %s workload (%d head-tokens) run %d times, FP64 token recurrence"
+                      % (inp["workload"].name, ht, reps)}
+
+
+def run_reference(args):
+    """The oracle as the reference arm: each step a bounded sample of the workload."""
+    import oracle
+    ws, rank, _ = dist_env()
+    if ws > 1 and rank != 0:
+        return
+    inp = synthetic.make_workload(args.workload)
+    tokens = min(inp["q"].shape[1], args.reference_tokens)
+    sl = {k: inp[k][:, :tokens].contiguous() for k in ("q", "k", "v", "g", "beta")}
+    if inp["cu_seqlens"] is not None:
+        sl = {k: inp[k][:, :tokens].contiguous() for k in ("q", "k", "v", "g", "beta")}
+        cu = None
+        init = inp["init_state"][:1] if inp["init_state"] is not None else None
+    else:
+        cu = None
+        init = inp["init_state"]
+    H = inp["q"].shape[2]
+    ht = sl["q"].shape[0] * tokens * H
+
+    def step():
+        oracle.kda_token(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], init, cu_seqlens=cu)
+
+    for _ in range(args.warmup):
+        step()
+    times = []
+    for _ in range(args.steps):
+        t0 = time.perf_counter()
+        step()
+        times.append(time.perf_counter() - t0)
+    total = sum(times)
+    value = ht * args.steps / total
+    sample = ("first %d tokens of every sequence of %s (%d head-tokens per step), FP64 token "
+              "recurrence" % (tokens, inp["workload"].name, ht))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic",
+        "config": {"workload": inp["workload"].name, "sample_tokens": tokens},
+        "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
+                         "kind": "oracle", "sample": sample},
+        "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 6800.0, "fallback"
+
+
+def run_ours(args):
+    import kimi_delta_attention_kda_gb300 as kda
+    ws, rank, local = dist_env()
+    if ws > 1:
+        import torch.distributed as dist
+        torch.cuda.set_device(local)
+        dist.init_process_group("nccl", device_id=torch.device("cuda", local))
+    device = torch.device("cuda", local if ws > 1 else 0)
+    torch.cuda.set_device(device)
+    kda._lib.load()   # fails loudly when the library is not built
+    stream = torch.cuda.Stream(device=device)
+    flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
+
+    inp = synthetic.make_workload(args.workload)
+    d = device_inputs(inp, device)
+    ht = head_tokens(inp)
+    nsplit = kda.auto_split(inp["N"], inp["q"].shape[2])
+
+    if ws > 1:
+        torch.distributed.barrier()
+    torch.cuda.synchronize(device)
+    cvd = [x for x in os.environ.get("CUDA_VISIBLE_DEVICES", "").split(",") if x.strip()]
+    gpu_index = cvd[device.index] if device.index < len(cvd) else str(device.index)
+    with ClockSampler(gpu_index) as clk:
+        ms, prof = time_kernel_steps(kda, d, args.steps, args.warmup, flush, stream, profile=True)
+        e2e_ms, h2d, d2h = time_e2e_steps(kda, inp, args.steps, min(args.warmup, 3), flush, stream,
+                                          device)
+    torch.cuda.synchronize(device)
+    if ws > 1:
+        torch.distributed.barrier()
+    status = kda.device_status(stream.cuda_stream)
+    if status != 0:
+        raise RuntimeError("device status %d during the benchmark" % status)
+
+    total_ms = sum(ms)
+    total_e2e = sum(e2e_ms)
+    if ws > 1:
+        t = torch.tensor([total_ms, total_e2e], dtype=torch.float64, device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        total_ms, total_e2e = float(t[0]), float(t[1])
+    value = ws * ht * args.steps / (total_ms * 1e-3)
+    e2e_value = ws * ht * args.steps / (total_e2e * 1e-3)
+
+    prep_ms, rec_ms, calls = prof
+    prep_avg, rec_avg = prep_ms / calls, rec_ms / calls
+    peak, peak_kind = measured_peaks()
+    H = inp["q"].shape[2]
+    n_states = inp["N"] * H
+    state_io = (2 if inp["init_state"] is not None else 1) * n_states * STATE_BYTES
+    rec_bytes = REC_BYTES_PER_HT * ht + state_io
+    prep_bytes = PREP_BYTES_PER_HT * ht
+    if rec_avg >= prep_avg:
+        dom, dom_bytes, dom_ms = "recurrence", rec_bytes, rec_avg
+    else:
+        dom, dom_bytes, dom_ms = "chunk_prep", prep_bytes, prep_avg
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
+                "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
+                "traffic": None,
+                "prep_us": 1e3 * prep_avg, "recurrence_us": 1e3 * rec_avg,
+                "chain_steps": int(math.ceil(inp["q"].shape[1] / 16)) if inp["cu_seqlens"] is None
+                else None}
+
+    line = {
+        "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": total_ms / args.steps,
+        "us_per_call": 1e3 * total_ms / args.steps,
+        "higher_is_better": True, "scaling": "weak",
+        "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": inp["workload"].name, "l2": "flushed (512 MiB write) before every step",
+                   "recurrence_split": nsplit, "head_tokens_per_step": ht},
+        "gpu_launches": (3 if inp["cu_seqlens"] is not None else 2) * args.steps,
+        "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "us_per_call": 1e3 * total_e2e / args.steps},
+        "roofline": roofline,
+        "clocks": clk.summary(),
+    }
+    if args.workload in FLASHKDA_B200_US:
+        ref_value = ht / (FLASHKDA_B200_US[args.workload] * 1e-6)
+        line["vs_baseline"] = value / ref_value
+        line["baseline"] = {"what": "FlashKDA prep + recurrence on a B200, %.1f us (pages, "
+                                    "FlashKDA column split section 4)" % FLASHKDA_B200_US[args.workload],
+                            "column_split_b200_us": COLUMN_SPLIT_B200_US[args.workload]}
+    if not args.no_secondary and args.workload != "t8192_h96":
+        sec = synthetic.make_workload("t8192_h96")
+        ds = device_inputs(sec, device)
+        ms2, prof2 = time_kernel_steps(kda, ds, max(10, args.steps // 10), 3, flush, stream,
+                                       profile=True)
+        ht2 = head_tokens(sec)
+        t2 = sum(ms2) / len(ms2)
+        line["secondary"] = {"workload": sec["workload"].name, "us_per_call": 1e3 * t2,
+                             "value": ht2 / (t2 * 1e-3), "unit": UNIT,
+                             "prep_us": 1e3 * prof2[0] / prof2[2],
+                             "recurrence_us": 1e3 * prof2[1] / prof2[2],
+                             "recurrence_split": kda.auto_split(1, 96),
+                             "vs_flashkda_b200": (ht2 / (t2 * 1e-3)) /
+                             (ht2 / (FLASHKDA_B200_US["t8192_h96"] * 1e-6))}
+        del ds
+    if rank == 0 and ws == 1 and not args.no_cpu_baseline:
+        line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)
+    if ws > 1:
+        torch.distributed.destroy_process_group()
+    if rank == 0:
+        print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser(description=__doc__.split("\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=200)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--workload", default="t8192_h6", choices=sorted(synthetic.WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-secondary", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=10.0)
+    ap.add_argument("--reference-tokens", type=int, default=1024)
+    args = ap.parse_args()
+    if args.warmup < 3:
+        ap.error("--warmup must be at least 3")
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

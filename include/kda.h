@@ -1,0 +1,142 @@
+/*
+ * kda.h -- C ABI of the GB300 (sm_103a) Kimi Delta Attention prefill library.
+ *
+ * The operation is the chunkwise KDA forward pass of "FlashKDA column split"
+ * (mainlymatmul.com), section 1: for every sequence and head, with the state S
+ * a 128 x 128 matrix (rows = value channels, columns = key channels), per
+ * token t
+ *     S <- S Diag(exp(g_t));  u_t = beta_t (v_t - S khat_t);
+ *     S <- S + u_t khat_t^T;  o_t = s S qhat_t,   s = 1/sqrt(128),
+ * evaluated 16 tokens at a time through the chunk quantities K^start, Q^start,
+ * K^end, D_{0:15}, A^kk = (I + R)^{-1} and A^qk of that section.  q and k are
+ * L2-normalised inside the operation, xhat = x / sqrt(sum x^2 + 1e-6)
+ * (flashinfer kda_prefill, "Optimized Blackwell prefill subset",
+ * use_qk_l2norm_in_kernel).  The log-decay g must lie in [-5, 0] ("K3's KDA
+ * precision problem", introduction: the lower bound keeps exp(+-G) of a
+ * 16-token chunk inside the FP32/BF16 range).
+ *
+ * Every pointer argument is a DEVICE pointer on the current CUDA device unless
+ * stated otherwise.  The caller owns every buffer; the library keeps no
+ * pointer after a call returns.  Calls are asynchronous on `stream` (a
+ * cudaStream_t; NULL is the legacy default stream): the host never reads
+ * device data and never synchronises.
+ */
+#ifndef KDA_H_
+#define KDA_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* Status codes returned by every entry point. */
+#define KDA_OK 0
+#define KDA_ERR_NULL (-1)      /* a required pointer is NULL */
+#define KDA_ERR_SHAPE (-2)     /* B, T or H out of range, or sizes overflow */
+#define KDA_ERR_ALIGN (-3)     /* a pointer is not suitably aligned */
+#define KDA_ERR_OVERLAP (-4)   /* an output overlaps an input or another output */
+#define KDA_ERR_DEVICE (-5)    /* no CUDA device, or not compute capability 10.3 */
+#define KDA_ERR_CUDA (-6)      /* a CUDA call (allocation, launch) failed */
+#define KDA_ERR_ARG (-7)       /* an option value is out of range */
+
+/* Device-side status bits, reported by kda_device_status(). */
+#define KDA_DEV_BAD_SEQLENS 1  /* cu_seqlens broke its contract; out/final_state untouched */
+#define KDA_DEV_PIPE_TIMEOUT 2 /* an internal pipeline wait hit its bound; results incomplete */
+
+/*
+ * KDA prefill, fixed or packed variable-length layout.
+ *
+ * Fixed layout (cu_seqlens == NULL): N = B sequences of T tokens each.
+ *   q, k, v, out : BF16 [B, T, H, 128], contiguous (head dim innermost)
+ *   g            : FP32 [B, T, H, 128], natural-log decay, alpha = exp(g), g in [-5, 0]
+ *   beta         : BF16 [B, T, H], beta in [0, 1] (already passed through a sigmoid)
+ * Packed layout (cu_seqlens != NULL): tensors are [1, T, H, ...] with T the
+ *   total number of tokens, and B is read as the number of sequences N.
+ *   cu_seqlens is a device int64 array of N + 1 offsets with cu[0] == 0,
+ *   cu[n] <= cu[n+1] and cu[N] == T (flashinfer kda_prefill, "Optimized
+ *   Blackwell prefill subset").  Equal neighbours are empty sequences, whose
+ *   final state equals their initial state.  The offsets are validated on the
+ *   device; a violation leaves out and final_state untouched and sets
+ *   KDA_DEV_BAD_SEQLENS (see kda_device_status).
+ * init_state  : BF16 [N, H, 128, 128] (value rows x key columns) or NULL for zeros.
+ * final_state : BF16 [N, H, 128, 128] or NULL (not written).  final_state may be
+ *   the same pointer as init_state (in-place update, as in flashinfer
+ *   kda_prefill "State and graph semantics"); any other overlap is refused.
+ *
+ * Alignment: q, k, v, g, out, init_state and final_state 16 bytes; beta 2
+ * bytes; cu_seqlens 8 bytes.  out must not overlap any input.
+ * Limits: B >= 1, T >= 0, H >= 1.  With no tokens (T = 0) only final_state is
+ * written (a copy of init_state, or zeros) and q, k, v, g, beta and out may be NULL.
+ *
+ * Scratch: the call takes a workspace of about 13.5 KB per (chunk, head) from
+ * a stream-ordered memory pool owned by the library (cudaMallocFromPoolAsync /
+ * cudaFreeAsync on `stream`), so it allocates and frees in stream order.
+ *
+ * Returns KDA_OK or a negative KDA_ERR_* code; on an error nothing is launched.
+ */
+int kda_prefill(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                const void* init_state, void* out, void* final_state, int64_t B, int64_t T,
+                int64_t H, const int64_t* cu_seqlens, void* stream);
+
+/* Human-readable text for a KDA_* status code (static storage). */
+const char* kda_error_string(int status);
+
+/*
+ * Synchronise `stream`, then read and clear this device's KDA_DEV_* status
+ * bits into *status (a HOST pointer).  The bits accumulate over every call on
+ * the device since the last read.
+ */
+int kda_device_status(void* stream, int* status);
+
+/*
+ * Number of CTAs that share one (sequence, head) in the recurrence: each owns
+ * 128 / nsplit value columns (value columns are independent recurrences,
+ * "FlashKDA column split" section 3.1).  nsplit is one of 1, 2, 4, 8, 16, or 0
+ * for the automatic choice (the largest split whose grid fits the SM count).
+ * Process-wide setting; returns KDA_ERR_ARG for other values.
+ */
+int kda_set_split(int nsplit);
+
+/* The split the automatic rule picks on the current device for N*H units (HOST out). */
+int kda_auto_split(int64_t n_seqs, int64_t H, int* nsplit);
+
+/*
+ * Bytes of scratch kda_prefill takes for a given shape (HOST out); `packed`
+ * is nonzero for the packed layout, where the size is an upper bound.
+ */
+int kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int packed, int64_t* bytes);
+
+/*
+ * Test hook: run only the chunk preparation and write the per-(chunk, head)
+ * packets into `packets` (device, capacity `packets_bytes`).  Packet
+ * (chunk, head) starts at byte (chunk * H + head) * kda_packet_bytes(), with
+ * chunks numbered sequence by sequence.  The packet layout is documented in
+ * kda_common.cuh.  Arguments as for kda_prefill.
+ */
+int kda_prep_only(const void* q, const void* k, const float* g, const void* beta, int64_t B,
+                  int64_t T, int64_t H, const int64_t* cu_seqlens, void* packets,
+                  int64_t packets_bytes, void* stream);
+
+/* Size in bytes of one (chunk, head) packet. */
+int64_t kda_packet_bytes(void);
+
+/*
+ * Per-kernel timing for benchmarks.  kda_profile_begin(max_calls) creates
+ * 3 * max_calls CUDA events on the current device; each of the next
+ * max_calls kda_prefill calls then records one event before its preparation
+ * kernels, one between preparation and recurrence and one after the
+ * recurrence, on its own stream.  kda_profile_end synchronises those events,
+ * writes the summed preparation and recurrence times in milliseconds and the
+ * number of calls timed (HOST pointers), and destroys the events.
+ * Process-wide; begin while active returns KDA_ERR_ARG.
+ */
+int kda_profile_begin(int max_calls);
+int kda_profile_end(double* prep_ms, double* recurrence_ms, int* calls);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KDA_H_ */

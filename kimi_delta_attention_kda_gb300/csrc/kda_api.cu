@@ -1,0 +1,374 @@
+// kda_api.cu -- the C ABI of the KDA prefill library (declared in include/kda.h).
+//
+// Host-side only: argument validation, workspace sizing, the choice of
+// recurrence split, and the launches (varlen metadata -> chunk preparation ->
+// recurrence) on the caller's stream.  No host <-> device synchronisation and
+// no host reads of device data happen here (flashinfer kda_prefill, "Optimized
+// Blackwell prefill subset": cu_seqlens is never inspected on the host).
+#include <mutex>
+
+#include "../../include/kda.h"
+#include "kda_common.cuh"
+#include "kda_launch.h"
+
+namespace kda {
+namespace {
+
+__device__ int g_device_status;   // KDA_DEV_* bits, one word per device
+
+constexpr int kMaxDevices = 64;
+
+struct DeviceState {
+    bool init = false;
+    int sms = 0;
+    int cc_major = 0, cc_minor = 0;
+    int* status = nullptr;            // device address of g_device_status
+    cudaMemPool_t pool = nullptr;     // library-owned stream-ordered pool
+};
+
+std::mutex g_mu;
+DeviceState g_dev[kMaxDevices];
+int g_split_override = 0;
+
+// Optional per-kernel timing: when active, each kda_prefill call records three
+// events on its stream (before the preparation kernels, between preparation
+// and recurrence, after the recurrence).  Events are created up front by
+// kda_profile_begin so that the calls themselves only record.
+struct Profile {
+    bool active = false;
+    int max_calls = 0;
+    int calls = 0;
+    cudaEvent_t* ev = nullptr;   // 3 per call
+};
+Profile g_prof;
+
+void prof_record(int which, cudaStream_t stream) {
+    if (!g_prof.active || g_prof.calls >= g_prof.max_calls) return;
+    cudaEventRecord(g_prof.ev[3 * g_prof.calls + which], stream);
+}
+
+int device_state(DeviceState** out) {
+    int dev = -1;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) {
+        cudaGetLastError();
+        return KDA_ERR_DEVICE;
+    }
+    std::lock_guard<std::mutex> lock(g_mu);
+    DeviceState& d = g_dev[dev];
+    if (!d.init) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+            cudaDeviceGetAttribute(&d.cc_minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+            cudaGetLastError();
+            return KDA_ERR_DEVICE;
+        }
+        if (d.cc_major != 10 || d.cc_minor != 3) return KDA_ERR_DEVICE;
+        void* sym = nullptr;
+        if (cudaGetSymbolAddress(&sym, g_device_status) != cudaSuccess) {
+            cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+        d.status = static_cast<int*>(sym);
+        cudaMemPoolProps props = {};
+        props.allocType = cudaMemAllocationTypePinned;
+        props.handleTypes = cudaMemHandleTypeNone;
+        props.location.type = cudaMemLocationTypeDevice;
+        props.location.id = dev;
+        if (cudaMemPoolCreate(&d.pool, &props) != cudaSuccess) {
+            cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+        // Keep freed blocks in the pool: repeated calls then allocate without
+        // going back to the driver.
+        uint64_t threshold = UINT64_MAX;
+        cudaMemPoolSetAttribute(d.pool, cudaMemPoolAttrReleaseThreshold, &threshold);
+        d.init = true;
+    }
+    *out = &d;
+    return KDA_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+struct Range {
+    uintptr_t lo, hi;
+};
+Range range(const void* p, int64_t bytes) {
+    uintptr_t lo = reinterpret_cast<uintptr_t>(p);
+    return Range{lo, lo + static_cast<uintptr_t>(bytes)};
+}
+bool overlap(Range a, Range b) {
+    if (a.lo == a.hi || b.lo == b.hi) return false;
+    return a.lo < b.hi && b.lo < a.hi;
+}
+
+int choose_split(int64_t units, int sms) {
+    if (g_split_override) return g_split_override;
+    const int options[] = {16, 8, 4, 2};
+    for (int ns : options)
+        if (units * ns <= sms) return ns;
+    return 1;
+}
+
+constexpr int64_t kMaxElems = int64_t(1) << 56;
+
+struct Plan {
+    bool packed;
+    int64_t N, tokens;
+    SeqGeometry geo;
+    int64_t meta_bytes;      // valid flag + cu_chunks (packed only), 256-aligned
+    int64_t packet_bytes;    // chunk_ub * H * kPacketBytes
+};
+
+int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
+    if (B < 1 || T < 0 || H < 1) return KDA_ERR_SHAPE;
+    p->packed = packed;
+    p->N = B;
+    p->tokens = packed ? T : B * T;
+    if (packed ? false : (T > 0 && B > kMaxElems / T)) return KDA_ERR_SHAPE;
+    if (p->tokens > kMaxElems / (H * kHeadDim)) return KDA_ERR_SHAPE;
+    if (B > kMaxElems / (H * kHeadDim * kHeadDim)) return KDA_ERR_SHAPE;
+    SeqGeometry& g = p->geo;
+    g = SeqGeometry{};
+    g.n_seqs = B;
+    g.tokens = p->tokens;
+    if (packed) {
+        g.chunk_ub = (T + (kChunk - 1) * B) / kChunk;
+        p->meta_bytes = 256 + ((8 * (B + 1) + 255) / 256) * 256;
+    } else {
+        g.tokens_per_seq = T;
+        g.chunks_per_seq = (T + kChunk - 1) / kChunk;
+        g.chunk_ub = B * g.chunks_per_seq;
+        p->meta_bytes = 0;
+    }
+    if (g.chunk_ub > kMaxElems / (H * kPacketBytes)) return KDA_ERR_SHAPE;
+    p->packet_bytes = g.chunk_ub * H * static_cast<int64_t>(kPacketBytes);
+    return KDA_OK;
+}
+
+// Launch metadata (packed) and preparation into `ws` (meta) and `packets`.
+int run_prep(const Plan& pl, const void* q, const void* k, const float* g, const void* beta,
+             int64_t H, const int64_t* cu_seqlens, uint8_t* meta, uint8_t* packets,
+             DeviceState* d, cudaStream_t stream, SeqGeometry* geo_out) {
+    SeqGeometry geo = pl.geo;
+    if (pl.packed) {
+        int32_t* valid = reinterpret_cast<int32_t*>(meta);
+        int64_t* cu_chunks = reinterpret_cast<int64_t*>(meta + 256);
+        if (launch_varlen_meta(cu_seqlens, pl.N, pl.tokens, valid, cu_chunks, d->status,
+                               stream) != cudaSuccess)
+            return KDA_ERR_CUDA;
+        geo.cu_seqlens = cu_seqlens;
+        geo.cu_chunks = cu_chunks;
+        geo.valid = valid;
+    }
+    const float scale = 0.08838834764831845f;   // 1 / sqrt(128)
+    if (launch_prep(q, k, g, beta, packets, geo, H, scale, d->status, stream) != cudaSuccess)
+        return KDA_ERR_CUDA;
+    *geo_out = geo;
+    return KDA_OK;
+}
+
+}  // namespace
+}  // namespace kda
+
+using namespace kda;
+
+extern "C" int kda_prefill(const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, const void* init_state, void* out,
+                           void* final_state, int64_t B, int64_t T, int64_t H,
+                           const int64_t* cu_seqlens, void* stream_ptr) {
+    const bool packed = cu_seqlens != nullptr;
+    Plan pl;
+    int rc = make_plan(B, T, H, packed, &pl);
+    if (rc != KDA_OK) return rc;
+    // Token tensors may be NULL only when there are no tokens to read or write.
+    if (pl.tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(v, 16) || !aligned(g, 16) ||
+        !aligned(out, 16) || !aligned(beta, 2) || (init_state && !aligned(init_state, 16)) ||
+        (final_state && !aligned(final_state, 16)) || (cu_seqlens && !aligned(cu_seqlens, 8)))
+        return KDA_ERR_ALIGN;
+
+    const int64_t x_bytes = pl.tokens * H * kHeadDim * 2;
+    const int64_t s_bytes = pl.N * H * kHeadDim * kHeadDim * 2;
+    const Range rq = range(q, x_bytes), rk = range(k, x_bytes), rv = range(v, x_bytes);
+    const Range rg = range(g, pl.tokens * H * kHeadDim * 4), rb = range(beta, pl.tokens * H * 2);
+    const Range ro = range(out, x_bytes);
+    const Range ri = range(init_state, init_state ? s_bytes : 0);
+    const Range rf = range(final_state, final_state ? s_bytes : 0);
+    const Range rc_ = range(cu_seqlens, cu_seqlens ? 8 * (pl.N + 1) : 0);
+    for (Range in : {rq, rk, rv, rg, rb, ri, rf, rc_})
+        if (overlap(ro, in)) return KDA_ERR_OVERLAP;
+    for (Range in : {rq, rk, rv, rg, rb, rc_})
+        if (overlap(rf, in)) return KDA_ERR_OVERLAP;
+    if (final_state && init_state && final_state != init_state && overlap(rf, ri))
+        return KDA_ERR_OVERLAP;
+
+    DeviceState* d = nullptr;
+    rc = device_state(&d);
+    if (rc != KDA_OK) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+
+    const int64_t ws_bytes = pl.meta_bytes + pl.packet_bytes;
+    uint8_t* ws = nullptr;
+    if (ws_bytes > 0) {
+        if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes),
+                                    d->pool, stream) != cudaSuccess) {
+            cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+    }
+    SeqGeometry geo;
+    prof_record(0, stream);
+    rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, ws + pl.meta_bytes, d, stream, &geo);
+    prof_record(1, stream);
+    if (rc == KDA_OK) {
+        const int nsplit = choose_split(pl.N * H, d->sms);
+        if (launch_recurrence(v, out, init_state, final_state, ws + pl.meta_bytes, geo, H, nsplit,
+                              d->status, stream) != cudaSuccess)
+            rc = KDA_ERR_CUDA;
+    }
+    prof_record(2, stream);
+    if (g_prof.active && g_prof.calls < g_prof.max_calls) g_prof.calls += 1;
+    if (ws) cudaFreeAsync(ws, stream);
+    if (rc != KDA_OK) cudaGetLastError();
+    return rc;
+}
+
+extern "C" int kda_prep_only(const void* q, const void* k, const float* g, const void* beta,
+                             int64_t B, int64_t T, int64_t H, const int64_t* cu_seqlens,
+                             void* packets, int64_t packets_bytes, void* stream_ptr) {
+    if (!q || !k || !g || !beta || !packets) return KDA_ERR_NULL;
+    const bool packed = cu_seqlens != nullptr;
+    Plan pl;
+    int rc = make_plan(B, T, H, packed, &pl);
+    if (rc != KDA_OK) return rc;
+    if (packets_bytes < pl.packet_bytes) return KDA_ERR_SHAPE;
+    if (!aligned(q, 16) || !aligned(k, 16) || !aligned(g, 16) || !aligned(beta, 2) ||
+        !aligned(packets, 16) || (cu_seqlens && !aligned(cu_seqlens, 8)))
+        return KDA_ERR_ALIGN;
+    DeviceState* d = nullptr;
+    rc = device_state(&d);
+    if (rc != KDA_OK) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    uint8_t* meta = nullptr;
+    if (pl.meta_bytes > 0 &&
+        cudaMallocFromPoolAsync(reinterpret_cast<void**>(&meta), static_cast<size_t>(pl.meta_bytes),
+                                d->pool, stream) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    SeqGeometry geo;
+    rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, meta, static_cast<uint8_t*>(packets), d,
+                  stream, &geo);
+    if (meta) cudaFreeAsync(meta, stream);
+    if (rc != KDA_OK) cudaGetLastError();
+    return rc;
+}
+
+extern "C" const char* kda_error_string(int status) {
+    switch (status) {
+        case KDA_OK: return "success";
+        case KDA_ERR_NULL: return "a required pointer is NULL";
+        case KDA_ERR_SHAPE: return "B, T or H out of range (or a size overflows)";
+        case KDA_ERR_ALIGN: return "a pointer is not suitably aligned";
+        case KDA_ERR_OVERLAP: return "an output overlaps an input or another output";
+        case KDA_ERR_DEVICE: return "no CUDA device of compute capability 10.3 is current";
+        case KDA_ERR_CUDA: return "a CUDA runtime call failed";
+        case KDA_ERR_ARG: return "an option value is out of range";
+        default: return "unknown KDA status";
+    }
+}
+
+extern "C" int kda_device_status(void* stream_ptr, int* status) {
+    if (!status) return KDA_ERR_NULL;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != KDA_OK) return rc;
+    cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
+    if (cudaStreamSynchronize(stream) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    int zero = 0;
+    if (cudaMemcpy(status, d->status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess ||
+        cudaMemcpy(d->status, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    return KDA_OK;
+}
+
+extern "C" int kda_set_split(int nsplit) {
+    if (nsplit != 0 && nsplit != 1 && nsplit != 2 && nsplit != 4 && nsplit != 8 && nsplit != 16)
+        return KDA_ERR_ARG;
+    g_split_override = nsplit;
+    return KDA_OK;
+}
+
+extern "C" int kda_auto_split(int64_t n_seqs, int64_t H, int* nsplit) {
+    if (!nsplit) return KDA_ERR_NULL;
+    if (n_seqs < 1 || H < 1) return KDA_ERR_SHAPE;
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != KDA_OK) return rc;
+    *nsplit = choose_split(n_seqs * H, d->sms);
+    return KDA_OK;
+}
+
+extern "C" int kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int packed, int64_t* bytes) {
+    if (!bytes) return KDA_ERR_NULL;
+    Plan pl;
+    int rc = make_plan(B, T, H, packed != 0, &pl);
+    if (rc != KDA_OK) return rc;
+    *bytes = pl.meta_bytes + pl.packet_bytes;
+    return KDA_OK;
+}
+
+extern "C" int64_t kda_packet_bytes(void) { return kPacketBytes; }
+
+extern "C" int kda_profile_begin(int max_calls) {
+    if (max_calls < 1 || max_calls > (1 << 20)) return KDA_ERR_ARG;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (g_prof.active) return KDA_ERR_ARG;
+    g_prof.ev = new cudaEvent_t[3 * static_cast<size_t>(max_calls)];
+    for (int i = 0; i < 3 * max_calls; ++i) {
+        if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
+            for (int j = 0; j < i; ++j) cudaEventDestroy(g_prof.ev[j]);
+            delete[] g_prof.ev;
+            g_prof.ev = nullptr;
+            cudaGetLastError();
+            return KDA_ERR_CUDA;
+        }
+    }
+    g_prof.max_calls = max_calls;
+    g_prof.calls = 0;
+    g_prof.active = true;
+    return KDA_OK;
+}
+
+extern "C" int kda_profile_end(double* prep_ms, double* recurrence_ms, int* calls) {
+    if (!prep_ms || !recurrence_ms || !calls) return KDA_ERR_NULL;
+    std::lock_guard<std::mutex> lock(g_mu);
+    if (!g_prof.active) return KDA_ERR_ARG;
+    double p = 0.0, r = 0.0;
+    int rc = KDA_OK;
+    for (int c = 0; c < g_prof.calls; ++c) {
+        float a = 0.f, b = 0.f;
+        if (cudaEventSynchronize(g_prof.ev[3 * c + 2]) != cudaSuccess ||
+            cudaEventElapsedTime(&a, g_prof.ev[3 * c], g_prof.ev[3 * c + 1]) != cudaSuccess ||
+            cudaEventElapsedTime(&b, g_prof.ev[3 * c + 1], g_prof.ev[3 * c + 2]) != cudaSuccess) {
+            rc = KDA_ERR_CUDA;
+            cudaGetLastError();
+            break;
+        }
+        p += a;
+        r += b;
+    }
+    *prep_ms = p;
+    *recurrence_ms = r;
+    *calls = g_prof.calls;
+    for (int i = 0; i < 3 * g_prof.max_calls; ++i) cudaEventDestroy(g_prof.ev[i]);
+    delete[] g_prof.ev;
+    g_prof = Profile{};
+    return rc;
+}

@@ -1,0 +1,183 @@
+// kda_common.cuh -- constants, the per-chunk packet layout and inline-PTX
+// helpers shared by the KDA prefill kernels (sm_103a).
+//
+// Notation follows "FlashKDA column split", section 1: a sequence is cut into
+// chunks of C = 16 tokens; for chunk c the preparation stage forms
+//   K^start (column i = D_{0:i} khat_i), Q^start, K^end (row i = khat_i^T D_{i+1:15}),
+//   D_{0:15}, A^kk = (I + R)^{-1} and the causal scores A^qk,
+// and the recurrence advances the 128 x 128 state S (value rows x key columns):
+//   U = (V - S K^start) B (A^kk)^T,  O = s S Q^start + U (A^qk)^T,
+//   S <- S D_{0:15} + U K^end.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+constexpr int kHeadDim = 128;   // K = V = 128 (flashinfer kda_prefill: head dimension 128)
+constexpr int kChunk = 16;      // C = 16 tokens per chunk
+
+// ---------------------------------------------------------------------------
+// Per-(chunk, head) packet written by the preparation kernel and read by the
+// recurrence kernel.  The byte image is exactly the shared-memory image the
+// recurrence consumes, so one bulk copy moves a whole packet.  Matrix tiles
+// are BF16 and "K-major" (the contraction index is contiguous in a row) with
+// the 128-byte or 32-byte XOR swizzle that both ldmatrix (conflict-free rows)
+// and tcgen05 shared-memory descriptors understand:
+//
+//  [    0,  4096)  KS   : K^start^T, 16 token rows x 128 key channels, SW128,
+//                         two 64-channel slabs of 16 x 128 B
+//  [ 4096,  8192)  QS   : s * Q^start^T, same layout (the scale s is folded in)
+//  [ 8192, 12288)  KE   : K^end^T, 128 key rows x 16 tokens (32 B rows), SW32
+//  [12288, 12800)  AKB  : A^kk B_c (A^kk with column j scaled by beta_j), 16 x 16, SW32
+//  [12800, 13312)  AQK  : A^qk (includes s), 16 x 16, SW32
+//  [13312, 13824)  DTOT : D_{0:15}, 128 FP32
+//
+// Folding beta into A^kk uses B (A^kk)^T = (A^kk B)^T, so U = (V - S K^start)(A^kk B)^T.
+// ---------------------------------------------------------------------------
+constexpr uint32_t kOffKS = 0;
+constexpr uint32_t kOffQS = 4096;
+constexpr uint32_t kOffKE = 8192;
+constexpr uint32_t kOffAKB = 12288;
+constexpr uint32_t kOffAQK = 12800;
+constexpr uint32_t kOffD = 13312;
+constexpr uint32_t kPacketBytes = 13824;
+
+// Byte offset of element (row r, 8-element group x) of a [rows][128] BF16 tile
+// stored as two 64-column SW128 slabs (slab = 16 B chunk index >> 3).
+__host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t rows, uint32_t r, uint32_t x) {
+    uint32_t slab = x >> 3, chunk = x & 7;
+    return slab * rows * 128u + r * 128u + ((chunk ^ (r & 7u)) << 4);
+}
+// Byte offset of (row r, 8-element group x in {0,1}) of a [rows][16] BF16 tile, SW32.
+__host__ __device__ __forceinline__ uint32_t sw32_off(uint32_t r, uint32_t x) {
+    return r * 32u + ((x ^ ((r >> 2) & 1u)) << 4);
+}
+
+// ---------------------------------------------------------------------------
+// Device status word (one per device and process, passed to every kernel as
+// a pointer).  Kernels OR error bits into it; the host reads and clears it
+// with kda_device_status().
+// ---------------------------------------------------------------------------
+enum DeviceStatus : int {
+    kDevOk = 0,
+    kDevBadSeqlens = 1,     // cu_seqlens violated its contract; outputs untouched
+    kDevPipeTimeout = 2,    // a pipeline wait ran past its bound; outputs incomplete
+};
+
+// Varlen metadata written by the metadata kernel at the start of the workspace.
+struct VarlenMeta {
+    int32_t valid;          // 1 when cu_seqlens passed validation
+    int32_t pad;
+    int64_t total_chunks;   // sum over sequences of ceil(len / 16)
+    // followed by int64 cu_chunks[N + 1]
+};
+
+// ---------------------------------------------------------------------------
+// Inline PTX helpers.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t* bar, uint32_t count) {
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_u32(bar)), "r"(count)
+                 : "memory");
+}
+__device__ __forceinline__ void fence_barrier_init() {
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t bytes) {
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_u32(bar)),
+                 "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+__device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// Wait for phase `parity` of an mbarrier with an upper bound on elapsed clock
+// cycles.  Returns false (and ORs kDevPipeTimeout into *status) when the bound
+// runs out, so that no wait can hang the GPU.
+constexpr long long kWaitBoundCycles = 4000000000LL;   // about 2 s at 2 GHz
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    long long t0 = clock64();
+    while (!mbar_try_wait(bar, parity)) {
+        if (clock64() - t0 > kWaitBoundCycles) {
+            atomicOr(status, kDevPipeTimeout);
+            return false;
+        }
+    }
+    return true;
+}
+
+// One-dimensional bulk copy global -> shared, completing on an mbarrier.
+__device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
+                                         uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// One-dimensional bulk copy shared -> global (bulk-group completion).
+__device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),
+                 "r"(smem_u32(src)), "r"(bytes)
+                 : "memory");
+}
+__device__ __forceinline__ void bulk_commit() {
+    asm volatile("cp.async.bulk.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_read_all() {
+    asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+}
+__device__ __forceinline__ void bulk_wait_all() {
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+}
+__device__ __forceinline__ void fence_proxy_async_smem() {
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t* r, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+// D = A * B + C for one m16n8k16 BF16 tile with FP32 accumulation.
+__device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, const uint32_t* b,
+                                         const float* c) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "f"(c[0]),
+          "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+// Two floats -> packed BF16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {
+    __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
+}
+__device__ __forceinline__ float bf16_lo(uint32_t v) {
+    return __uint_as_float(v << 16);
+}
+__device__ __forceinline__ float bf16_hi(uint32_t v) {
+    return __uint_as_float(v & 0xffff0000u);
+}
+
+}  // namespace kda

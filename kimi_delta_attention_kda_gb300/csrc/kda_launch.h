@@ -1,0 +1,39 @@
+// kda_launch.h -- host-side launch interface between the C ABI (kda_api.cu)
+// and the kernel translation units.  Internal; not part of the public header.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace kda {
+
+struct SeqGeometry {
+    // Fixed layout: n_seqs sequences of tokens_per_seq tokens each.
+    // Packed layout: cu_seqlens (device, n_seqs + 1) and metadata written by
+    // the varlen metadata kernel (cu_chunks, valid flag).
+    int64_t n_seqs;
+    int64_t tokens;           // total tokens across all sequences
+    int64_t tokens_per_seq;   // fixed layout only
+    int64_t chunks_per_seq;   // fixed layout only
+    int64_t chunk_ub;         // upper bound on the total number of chunks
+    const int64_t* cu_seqlens;   // packed only (device)
+    const int64_t* cu_chunks;    // packed only (device, n_seqs + 1)
+    const int32_t* valid;        // packed only (device)
+};
+
+cudaError_t launch_varlen_meta(const int64_t* cu_seqlens, int64_t n_seqs, int64_t total_tokens,
+                               int32_t* valid, int64_t* cu_chunks, int* status,
+                               cudaStream_t stream);
+
+cudaError_t launch_prep(const void* q, const void* k, const float* g, const void* beta,
+                        uint8_t* packets, const SeqGeometry& geo, int64_t H, float scale,
+                        int* status, cudaStream_t stream);
+
+// Recurrence variants: `nsplit` CTAs share one (sequence, head); each owns
+// 128 / nsplit value columns.
+cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
+                              void* final_state, const uint8_t* packets,
+                              const SeqGeometry& geo, int64_t H, int nsplit, int* status,
+                              cudaStream_t stream);
+
+}  // namespace kda

@@ -1,0 +1,82 @@
+// kda_meta.cu -- packed variable-length metadata for KDA prefill (sm_103a).
+//
+// flashinfer kda_prefill ("Optimized Blackwell prefill subset" and "Packed
+// scheduling") fixes the contract of cu_seqlens: int64, cu[0] == 0,
+// non-decreasing, cu[N] == total tokens, equal neighbours meaning an empty
+// sequence, and no host read of the device offsets.  This kernel checks that
+// contract on the device and turns the offsets into a compact per-sequence
+// chunk prefix cu_chunks[n] = sum_{m<n} ceil(len_m / 16), which the
+// preparation kernel binary-searches and the recurrence indexes directly.
+// On a violation it clears `valid` (every later kernel then returns without
+// touching its outputs) and records kDevBadSeqlens in the status word.
+#include "kda_common.cuh"
+#include "kda_launch.h"
+
+namespace kda {
+namespace {
+
+constexpr int kMetaThreads = 1024;
+
+__global__ void __launch_bounds__(kMetaThreads)
+varlen_meta_kernel(const int64_t* cu, int64_t N, int64_t total, int32_t* valid,
+                   int64_t* cu_chunks, int* status) {
+    __shared__ int64_t warp_sums[kMetaThreads / 32];
+    __shared__ int64_t carry;
+    __shared__ int bad;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (tid == 0) {
+        carry = 0;
+        bad = (cu[0] != 0) || (cu[N] != total);
+        cu_chunks[0] = 0;
+    }
+    __syncthreads();
+    for (int64_t base = 0; base < N; base += kMetaThreads) {
+        const int64_t n = base + tid;
+        int64_t cnt = 0;
+        if (n < N) {
+            const int64_t len = cu[n + 1] - cu[n];
+            if (len < 0) bad = 1;
+            cnt = len > 0 ? (len + kChunk - 1) / kChunk : 0;
+        }
+        // Inclusive scan: within the warp, then over warp totals.
+        int64_t x = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int64_t w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const int64_t incl = x + (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
+        if (n < N) cu_chunks[n + 1] = incl;
+        __syncthreads();
+        if (tid == kMetaThreads - 1) carry = incl;
+        __syncthreads();
+    }
+    if (tid == 0) {
+        *valid = bad ? 0 : 1;
+        if (bad) atomicOr(status, kDevBadSeqlens);
+    }
+}
+
+}  // namespace
+
+cudaError_t launch_varlen_meta(const int64_t* cu_seqlens, int64_t n_seqs, int64_t total_tokens,
+                               int32_t* valid, int64_t* cu_chunks, int* status,
+                               cudaStream_t stream) {
+    varlen_meta_kernel<<<1, kMetaThreads, 0, stream>>>(cu_seqlens, n_seqs, total_tokens, valid,
+                                                      cu_chunks, status);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -1,0 +1,123 @@
+"""Host-side tests of the C ABI (no GPU needed).
+
+The library must load and export every function that include/kda.h
+declares, and kda_prefill must refuse bad arguments on the host, before any
+CUDA call, with the documented codes.  The addresses passed here are never
+dereferenced: validation runs before the library touches the device.
+"""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+from kimi_delta_attention_kda_gb300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "kda.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    names = re.findall(r"^\s*(?:const\s+)?\w+\**\s+\**(kda_\w+)\s*\(", text, flags=re.M)
+    return sorted(set(names))
+
+
+def test_header_declares_the_entry_points():
+    names = declared_functions()
+    for n in ("kda_prefill", "kda_error_string", "kda_device_status", "kda_set_split"):
+        assert n in names
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), "libkda.so does not export %s" % name
+
+
+def test_error_strings(lib):
+    for code in range(0, -8, -1):
+        s = lib.kda_error_string(code).decode()
+        assert s and s != "unknown KDA status"
+    assert lib.kda_error_string(-99).decode() == "unknown KDA status"
+
+
+A = 1 << 20       # fake, 16-byte aligned, never dereferenced
+GB = 1 << 32
+
+
+def call(lib, q=A, k=A + GB, v=A + 2 * GB, g=A + 3 * GB, beta=A + 4 * GB, init=0,
+         out=A + 5 * GB, final=0, B=1, T=16, H=1, cu=0):
+    return _lib.prefill_raw(q, k, v, g, beta, init, out, final, B, T, H, cu, 0)
+
+
+def test_null_pointers(lib):
+    assert call(lib, q=0) == -1
+    assert call(lib, out=0) == -1
+    assert call(lib, beta=0) == -1
+    # with no tokens the token tensors may be NULL: validation passes and the
+    # call goes on to the device query
+    import torch
+    if not torch.cuda.is_available():
+        assert call(lib, q=0, k=0, v=0, g=0, beta=0, out=0, T=0) == -5
+
+
+def test_bad_shapes(lib):
+    assert call(lib, B=0) == -2
+    assert call(lib, H=0) == -2
+    assert call(lib, T=-1) == -2
+    assert call(lib, B=1 << 40, T=1 << 40) == -2
+
+
+def test_misaligned(lib):
+    assert call(lib, q=A + 2) == -3
+    assert call(lib, g=A + 3 * GB + 8) == -3
+    assert call(lib, beta=A + 4 * GB + 1) == -3
+    assert call(lib, init=A + 6 * GB + 4) == -3
+    assert call(lib, cu=A + 7 * GB + 4) == -3
+
+
+def test_overlaps(lib):
+    # out overlapping q
+    assert call(lib, out=A + 64) == -4
+    # final state overlapping an input
+    assert call(lib, final=A + 3 * GB + 16) == -4
+    # final partially overlapping init (identical pointers are allowed)
+    assert call(lib, init=A + 6 * GB, final=A + 6 * GB + 1024) == -4
+
+
+def test_no_device_here(lib):
+    """Valid arguments reach the device query; without a GPU that is KDA_ERR_DEVICE."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present")
+    assert call(lib) == -5
+    st = ctypes.c_int(0)
+    assert lib.kda_device_status(None, ctypes.byref(st)) == -5
+
+
+def test_split_option(lib):
+    for ns in (0, 1, 2, 4, 8, 16):
+        assert lib.kda_set_split(ns) == 0
+    for ns in (3, 5, 32, -1):
+        assert lib.kda_set_split(ns) == -7
+    assert lib.kda_set_split(0) == 0
+
+
+def test_workspace_bytes(lib):
+    pb = _lib.packet_bytes()
+    assert pb == 13824
+    # fixed: ceil(T/16) chunks per sequence
+    assert _lib.workspace_bytes(2, 40, 3, False) == 2 * 3 * 3 * pb
+    assert _lib.workspace_bytes(1, 0, 5, False) == 0
+    # packed: (T + 15 N) // 16 chunks at most, plus the metadata block
+    n, T, H = 4, 100, 2
+    meta = 256 + ((8 * (n + 1) + 255) // 256) * 256
+    assert _lib.workspace_bytes(n, T, H, True) == meta + ((T + 15 * n) // 16) * H * pb

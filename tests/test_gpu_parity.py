@@ -1,0 +1,269 @@
+"""GPU parity: the CUDA path (through the C ABI) against the FP64 oracle.
+
+Small cases compare every output element; the full workloads compare whole
+heads sampled from the full-size run, in the launch configuration the
+benchmark uses.  Tolerance per (sequence, head): rel-Frobenius <= 1e-2 and
+max-abs <= 3e-2 for O and for the final state (kda_testutil).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from kimi_delta_attention_kda_gb300 import synthetic
+import kda_testutil as tu
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def kda():
+    import kimi_delta_attention_kda_gb300 as m
+    from kimi_delta_attention_kda_gb300 import build
+    build.build()
+    assert torch.cuda.is_available(), "GPU tests need a CUDA device"
+    m.set_split(0)
+    m.device_status()   # clear
+    return m
+
+
+def run(kda, inp, **kw):
+    d = tu.to_device(inp)
+    out, fin = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                               cu_seqlens=d["cu_seqlens"], **kw)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    return out.cpu(), fin.cpu()
+
+
+# ----------------------------------------------------------------------------
+# Chunk preparation against the oracle's chunk quantities
+# ----------------------------------------------------------------------------
+
+def _check_prep(kda, inp):
+    d = tu.to_device(inp)
+    packets = kda.prep_only(d["q"], d["k"], d["g"], d["beta"], cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    P = tu.unpack_packets(packets.cpu().numpy())
+    cu = inp["cu_seqlens"]
+    im = oracle.chunk_intermediates(inp["q"], inp["k"], inp["g"], inp["beta"],
+                                    cu_seqlens=None if cu is None else cu.numpy())
+    nch = im["Akk"].shape[0]
+    s = 1 / np.sqrt(128)
+    beta = inp["beta"].double().numpy()
+    # Elementwise BF16 quantities: relative error of one BF16 rounding (2^-9)
+    # plus FP32 arithmetic and the fast exponential.
+    for key, ref in (("Kst", im["Kst"]), ("Qst_s", s * im["Qst"]),
+                     ("KendT", np.swapaxes(im["Kend"], -1, -2))):
+        got = P[key][:nch]
+        err = np.abs(got - ref)
+        assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-30), key
+    np.testing.assert_allclose(P["D"][:nch], im["D"], rtol=2e-5, atol=1e-37)
+    # Scores come from BF16 operands with FP32 accumulation.
+    assert np.abs(P["Aqk"][:nch] - im["Aqk"]).max() < 2e-3
+    # A^kk B_c: column j of A^kk scaled by beta_j.
+    if cu is None:
+        B, T, H = beta.shape
+        cps = (T + 15) // 16
+        starts = [(b, 16 * c) for b in range(B) for c in range(cps)]
+        lengths = [min(16, T - t0) for (_, t0) in starts]
+        bch = np.zeros((nch, H, 16))
+        for ch, (b, t0) in enumerate(starts):
+            bch[ch, :, :lengths[ch]] = beta[b, t0:t0 + lengths[ch]].T
+    else:
+        c = cu.numpy()
+        H = beta.shape[2]
+        bch = np.zeros((nch, H, 16))
+        ch = 0
+        for n in range(len(c) - 1):
+            for t0 in range(c[n], c[n + 1], 16):
+                L = min(16, c[n + 1] - t0)
+                bch[ch, :, :L] = beta[0, t0:t0 + L].T
+                ch += 1
+    ref = im["Akk"] * bch[:, :, None, :]
+    assert np.abs(P["AkkB"][:nch] - ref).max() < 2e-2
+    for ch in range(nch):
+        for h in range(ref.shape[1]):
+            den = np.linalg.norm(ref[ch, h])
+            assert np.linalg.norm(P["AkkB"][ch, h] - ref[ch, h]) <= 1e-2 * den + 1e-6
+
+
+def test_prep_fixed_with_tail(kda):
+    _check_prep(kda, synthetic.make_inputs(2, 40, 3, 101))
+
+
+def test_prep_packed(kda):
+    _check_prep(kda, synthetic.make_inputs(0, 0, 2, 102, lengths=[5, 0, 33, 16, 1]))
+
+
+@pytest.mark.parametrize("family", ["floor_e-5", "weak_decay_correlated", "model_like"])
+def test_prep_stress_families(kda, family):
+    _check_prep(kda, synthetic.stress_inputs(family, 48, 2, 7))
+
+
+# ----------------------------------------------------------------------------
+# End to end, small shapes: every element compared
+# ----------------------------------------------------------------------------
+
+SMALL = [
+    # (B, T, H, init?)
+    (1, 256, 1, False),    # the 16-chunk, one-head workload
+    (2, 40, 3, True),      # ragged last chunk
+    (1, 1, 2, True),
+    (1, 17, 1, False),
+    (3, 100, 2, True),
+    (1, 512, 4, True),
+]
+
+
+@pytest.mark.parametrize("B,T,H,init", SMALL)
+def test_small_fixed(kda, B, T, H, init):
+    inp = synthetic.make_inputs(B, T, H, 1000 + T, init_std=0.02 if init else None)
+    out, fin = run(kda, inp)
+    tu.check_against_oracle(inp, out, fin)
+
+
+def test_small_packed(kda):
+    inp = synthetic.make_inputs(0, 0, 3, 55, init_std=0.02, lengths=[5, 0, 33, 16, 1, 64, 200])
+    out, fin = run(kda, inp)
+    tu.check_against_oracle(inp, out, fin)
+
+
+@pytest.mark.parametrize("family", ["floor_e-5", "model_like"])
+def test_stress_families_end_to_end(kda, family):
+    inp = synthetic.stress_inputs(family, 300, 2, 9)
+    out, fin = run(kda, inp)
+    tu.check_against_oracle(inp, out, fin)
+
+
+def test_correlated_keys_end_to_end(kda):
+    """Every key points the same way (g = -0.01, beta = 0.5).  The delta rule
+    only ever corrects the state along that one direction, so the BF16
+    rounding of the K^end / K^start operands leaves state error orthogonal to
+    it that is never removed (only decayed, with a time constant of ~100
+    tokens), and the read-out with a random q amplifies it by 1 / (khat . qhat)
+    (about 11).  An emulation of the kernel's rounding points in FP64 gives
+    1.3e-2 for O and 1.4e-2 for the state on this input, so the bound here is
+    3e-2 (max-abs bound unchanged)."""
+    inp = synthetic.stress_inputs("weak_decay_correlated", 300, 2, 9)
+    out, fin = run(kda, inp)
+    o_ref, f_ref = oracle.kda_token(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"])
+    for rel, mx in tu.per_head_errors(out[0].double().numpy(), o_ref[0], 1):
+        assert rel <= 3e-2 and mx <= tu.MAX_ABS_TOL
+    for rel, mx in tu.per_head_errors(fin[0].double().numpy(), f_ref[0], 0):
+        assert rel <= 3e-2 and mx <= tu.MAX_ABS_TOL
+
+
+def test_split_factors_bitwise_identical(kda):
+    """Each value column runs the same arithmetic whichever CTA owns it, so every
+    split of the state over CTAs gives the same bits."""
+    inp = synthetic.make_inputs(1, 200, 2, 77, init_std=0.02)
+    outs = []
+    try:
+        for ns in (1, 2, 4, 8, 16):
+            kda.set_split(ns)
+            outs.append(run(kda, inp))
+    finally:
+        kda.set_split(0)
+    for o, f in outs[1:]:
+        assert torch.equal(o, outs[0][0]) and torch.equal(f, outs[0][1])
+
+
+def test_deterministic(kda):
+    inp = synthetic.make_inputs(2, 130, 3, 5, init_std=0.02)
+    a = run(kda, inp)
+    b = run(kda, inp)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_packed_equals_separate_bitwise(kda):
+    lengths = [33, 0, 48, 7]
+    inp = synthetic.make_inputs(0, 0, 2, 66, init_std=0.02, lengths=lengths)
+    out, fin = run(kda, inp)
+    cu = inp["cu_seqlens"].tolist()
+    for n, L in enumerate(lengths):
+        if L == 0:
+            assert torch.equal(fin[n], inp["init_state"][n])
+            continue
+        sub = {key: inp[key][:, cu[n]:cu[n + 1]].contiguous() for key in ("q", "k", "v", "g", "beta")}
+        sub["init_state"] = inp["init_state"][n:n + 1].contiguous()
+        sub["cu_seqlens"] = None
+        o1, f1 = run(kda, sub)
+        assert torch.equal(out[:, cu[n]:cu[n + 1]], o1)
+        assert torch.equal(fin[n], f1[0])
+
+
+def test_in_place_state(kda):
+    inp = synthetic.make_inputs(2, 64, 2, 12, init_std=0.02)
+    ref_out, ref_fin = run(kda, inp)
+    d = tu.to_device(inp)
+    state = d["init_state"].clone()
+    out, fin = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], state,
+                               final_state=state)
+    torch.cuda.synchronize()
+    assert fin.data_ptr() == state.data_ptr()
+    assert torch.equal(out.cpu(), ref_out) and torch.equal(state.cpu(), ref_fin)
+
+
+def test_split_and_continue(kda):
+    """Two calls with the state carried (split at a chunk boundary) equal one call."""
+    inp = synthetic.make_inputs(1, 96, 2, 31, init_std=0.02)
+    out, fin = run(kda, inp)
+    a = {key: inp[key][:, :48].contiguous() for key in ("q", "k", "v", "g", "beta")}
+    a.update(init_state=inp["init_state"], cu_seqlens=None)
+    oa, fa = run(kda, a)
+    b = {key: inp[key][:, 48:].contiguous() for key in ("q", "k", "v", "g", "beta")}
+    b.update(init_state=fa, cu_seqlens=None)
+    ob, fb = run(kda, b)
+    # The state is rounded to BF16 between the calls, so compare with the tolerance.
+    tu.assert_within_tolerance(torch.cat([oa, ob], 1)[0].double().numpy(),
+                               out[0].double().numpy(), 1, "continued O")
+    tu.assert_within_tolerance(fb.double().numpy()[0], fin.double().numpy()[0], 0, "continued S")
+
+
+def test_zero_tokens_copies_state(kda):
+    inp = synthetic.make_inputs(2, 0, 3, 3, init_std=0.02)
+    d = tu.to_device(inp)
+    out, fin = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"])
+    torch.cuda.synchronize()
+    assert torch.equal(fin.cpu(), inp["init_state"])
+    assert kda.device_status() == 0
+
+
+@pytest.mark.parametrize("cu", [[0, 10, 5, 20], [0, 10, 30], [1, 10, 20]])
+def test_bad_cu_seqlens_leaves_outputs(kda, cu):
+    T, H = 20, 2
+    inp = synthetic.make_inputs(1, T, H, 4, init_std=0.02)
+    d = tu.to_device(inp)
+    cu_t = torch.tensor(cu, dtype=torch.int64, device="cuda")
+    N = len(cu) - 1
+    init = torch.randn((N, H, 128, 128), device="cuda").to(torch.bfloat16)
+    out = torch.full_like(d["v"], 7.0)
+    fin = torch.full_like(init, 3.0)
+    kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], init, cu_seqlens=cu_t, out=out,
+                    final_state=fin)
+    assert kda.device_status() & 1
+    assert torch.all(out == 7.0) and torch.all(fin == 3.0)
+
+
+# ----------------------------------------------------------------------------
+# Full workloads (the benchmark's launch configuration), sampled heads
+# ----------------------------------------------------------------------------
+
+FULL = {
+    "t256_h1": None,
+    "t8192_h6": None,
+    "t8192_h96": [0, 37, 95],
+    "varlen8_h12": [0, 5, 11],
+    "t65536_h1": None,
+}
+
+
+@pytest.mark.parametrize("name", list(FULL))
+def test_full_workload(kda, name):
+    inp = synthetic.make_workload(name)
+    out, fin = run(kda, inp)
+    assert torch.isfinite(out.float()).all() and torch.isfinite(fin.float()).all()
+    tu.check_against_oracle(inp, out, fin, heads=FULL[name])
