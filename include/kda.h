@@ -40,6 +40,7 @@ extern "C" {
 #define KDA_ERR_DEVICE (-5)    /* no CUDA device, or not compute capability 10.3 */
 #define KDA_ERR_CUDA (-6)      /* a CUDA call (allocation, launch) failed */
 #define KDA_ERR_ARG (-7)       /* an option value is out of range */
+#define KDA_ERR_SCRATCH (-8)   /* shape too large for kda_prefill_noalloc's fixed scratch */
 
 /* Device-side status bits, reported by kda_device_status(). */
 #define KDA_DEV_BAD_SEQLENS 1  /* cu_seqlens broke its contract; out/final_state untouched */
@@ -134,6 +135,40 @@ int64_t kda_packet_bytes(void);
  */
 int kda_profile_begin(int max_calls);
 int kda_profile_end(double* prep_ms, double* recurrence_ms, int* calls);
+
+/*
+ * kda_prefill without any allocation.  The pages describe no such entry
+ * point; it exists for callers that cannot let a library allocate device
+ * memory: code running under an allocator that owns all of the GPU's memory
+ * (a serving engine that carves HBM up front, a framework whose caching
+ * allocator must account for every byte), callers that forbid driver
+ * allocations on their hot path, or processes that have already handed out
+ * nearly all HBM.
+ *
+ * Arguments, results, alignment and overlap rules and error codes are those
+ * of kda_prefill; the caller still passes every input and output.  The
+ * scratch kda_prefill would take from its pool lives instead in one fixed
+ * device array of kda_noalloc_scratch_bytes() bytes (48 MiB) inside this
+ * library, which every GPU that loads the library holds until the process
+ * exits.  A shape whose scratch does not fit -- about 13.5 KB per (chunk of
+ * 16 tokens, head), plus (N + 1) * 8 + 512 bytes for packed input -- is
+ * refused with KDA_ERR_SCRATCH before anything is launched.  No call
+ * allocates or frees device or host memory.
+ *
+ * The first call on a device, with that device current, looks up the
+ * array's device address (cudaGetSymbolAddress) once; make that first call
+ * before any stream capture.  Every call on a device shares the one array
+ * and leaves its contents behind; nothing in it has to start at zero.  Calls
+ * whose kernels overlap on the GPU (on different streams, or from different
+ * host threads) race on that array and corrupt each other's results: order
+ * them on one stream, or with events.
+ */
+int kda_prefill_noalloc(const void* q, const void* k, const void* v, const float* g,
+                        const void* beta, const void* init_state, void* out, void* final_state,
+                        int64_t B, int64_t T, int64_t H, const int64_t* cu_seqlens, void* stream);
+
+/* Size in bytes of kda_prefill_noalloc's fixed scratch array. */
+int64_t kda_noalloc_scratch_bytes(void);
 
 #ifdef __cplusplus
 }

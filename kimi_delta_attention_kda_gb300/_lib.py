@@ -60,6 +60,10 @@ def load():
         D = ctypes.POINTER(ctypes.c_double)
         lib.kda_profile_end.argtypes = [D, D, ctypes.POINTER(I)]
         lib.kda_profile_end.restype = I
+        lib.kda_prefill_noalloc.argtypes = [P] * 8 + [I64] * 3 + [P, P]
+        lib.kda_prefill_noalloc.restype = I
+        lib.kda_noalloc_scratch_bytes.argtypes = []
+        lib.kda_noalloc_scratch_bytes.restype = I64
         _lib = lib
         return lib
 
@@ -126,3 +130,16 @@ def profile_end():
     _check(load().kda_profile_end(ctypes.byref(p), ctypes.byref(r), ctypes.byref(n)),
            "kda_profile_end")
     return p.value, r.value, n.value
+
+
+def prefill_noalloc_raw(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,
+                        stream):
+    """Call ``kda_prefill_noalloc`` (no allocation; fixed in-library scratch) with
+    integer device addresses (0 for NULL); returns the status."""
+    return load().kda_prefill_noalloc(q or None, k or None, v or None, g or None, beta or None,
+                                      init_state or None, out or None, final_state or None,
+                                      int(B), int(T), int(H), cu_seqlens or None, stream or None)
+
+
+def noalloc_scratch_bytes() -> int:
+    return int(load().kda_noalloc_scratch_bytes())

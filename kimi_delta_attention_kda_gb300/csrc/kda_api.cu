@@ -169,6 +169,18 @@ int run_prep(const Plan& pl, const void* q, const void* k, const float* g, const
 }
 
 }  // namespace
+
+// Read-only view of the per-device state for other entry points in this
+// library: the device status word and the recurrence split kda_prefill uses.
+int device_context(int** status, int64_t units, int* nsplit) {
+    DeviceState* d = nullptr;
+    int rc = device_state(&d);
+    if (rc != KDA_OK) return rc;
+    *status = d->status;
+    *nsplit = choose_split(units, d->sms);
+    return KDA_OK;
+}
+
 }  // namespace kda
 
 using namespace kda;
@@ -275,6 +287,8 @@ extern "C" const char* kda_error_string(int status) {
         case KDA_ERR_DEVICE: return "no CUDA device of compute capability 10.3 is current";
         case KDA_ERR_CUDA: return "a CUDA runtime call failed";
         case KDA_ERR_ARG: return "an option value is out of range";
+        case KDA_ERR_SCRATCH:
+            return "the shape needs more scratch than the fixed no-allocation buffer holds";
         default: return "unknown KDA status";
     }
 }

@@ -36,4 +36,8 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
                               const SeqGeometry& geo, int64_t H, int nsplit, int* status,
                               cudaStream_t stream);
 
+// Per-device status word and the split kda_prefill picks for `units`
+// (sequence x head) recurrences, for entry points outside kda_api.cu.
+int device_context(int** status, int64_t units, int* nsplit);
+
 }  // namespace kda
