@@ -290,6 +290,8 @@ def run_ours(args):
     device = torch.device("cuda", local if ws > 1 else 0)
     torch.cuda.set_device(device)
     kda._lib.load()   # fails loudly when the library is not built
+    if args.split:
+        kda.set_split(args.split)
     stream = torch.cuda.Stream(device=device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
@@ -397,6 +399,8 @@ def main():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
     ap.add_argument("--reference-tokens", type=int, default=1024)
+    ap.add_argument("--split", type=int, default=0,
+                    help="CTAs per (sequence, head) in the recurrence (0 = automatic)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

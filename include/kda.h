@@ -68,7 +68,7 @@ extern "C" {
  *
  * Alignment: q, k, v, g, out, init_state and final_state 16 bytes; beta 2
  * bytes; cu_seqlens 8 bytes.  out must not overlap any input.
- * Limits: B >= 1, T >= 0, H >= 1.  With no tokens (T = 0) only final_state is
+ * Limits: B >= 1, T >= 0, H >= 1, fewer than 2^31 tokens in total.  With no tokens (T = 0) only final_state is
  * written (a copy of init_state, or zeros) and q, k, v, g, beta and out may be NULL.
  *
  * Scratch: the call takes a workspace of about 13.5 KB per (chunk, head) from

@@ -127,6 +127,7 @@ int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
     p->tokens = packed ? T : B * T;
     if (packed ? false : (T > 0 && B > kMaxElems / T)) return KDA_ERR_SHAPE;
     if (p->tokens > kMaxElems / (H * kHeadDim)) return KDA_ERR_SHAPE;
+    if (p->tokens >= (int64_t(1) << 31)) return KDA_ERR_SHAPE;   // token index fits int32
     if (B > kMaxElems / (H * kHeadDim * kHeadDim)) return KDA_ERR_SHAPE;
     SeqGeometry& g = p->geo;
     g = SeqGeometry{};

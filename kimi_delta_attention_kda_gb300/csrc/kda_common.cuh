@@ -33,7 +33,10 @@ constexpr int kChunk = 16;      // C = 16 tokens per chunk
 //  [ 8192, 12288)  KE   : K^end^T, 128 key rows x 16 tokens (32 B rows), SW32
 //  [12288, 12800)  AKB  : A^kk B_c (A^kk with column j scaled by beta_j), 16 x 16, SW32
 //  [12800, 13312)  AQK  : A^qk (includes s), 16 x 16, SW32
-//  [13312, 13824)  DTOT : D_{0:15}, 128 FP32
+//  [13312, 13824)  DTOT : D_{0:15}, 128 FP32, permuted: key c = 16 m + r + 8 h
+//                         (m < 8, r < 8, h < 2) sits at index 16 r + 2 m + h, so
+//                         the recurrence thread that owns key rows r and r + 8 of
+//                         every 16-key tile reads its 16 factors contiguously
 //
 // Folding beta into A^kk uses B (A^kk)^T = (A^kk B)^T, so U = (V - S K^start)(A^kk B)^T.
 // ---------------------------------------------------------------------------
@@ -50,6 +53,10 @@ constexpr uint32_t kPacketBytes = 13824;
 __host__ __device__ __forceinline__ uint32_t sw128_off(uint32_t rows, uint32_t r, uint32_t x) {
     uint32_t slab = x >> 3, chunk = x & 7;
     return slab * rows * 128u + r * 128u + ((chunk ^ (r & 7u)) << 4);
+}
+// Index of key channel c in the permuted D_{0:15} vector of the packet.
+__host__ __device__ __forceinline__ uint32_t dperm_index(uint32_t c) {
+    return 16u * (c & 7u) + 2u * (c >> 4) + ((c >> 3) & 1u);
 }
 // Byte offset of (row r, 8-element group x in {0,1}) of a [rows][16] BF16 tile, SW32.
 __host__ __device__ __forceinline__ uint32_t sw32_off(uint32_t r, uint32_t x) {
@@ -97,6 +104,13 @@ __device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t* bar, uint32_t by
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+// Arrive from the threads where `pred` holds, without a branch.
+__device__ __forceinline__ void mbar_arrive_if(uint64_t* bar, bool pred) {
+    asm volatile(
+        "{\n .reg .pred p;\n setp.ne.b32 p, %1, 0;\n @p mbarrier.arrive.shared::cta.b64 _, [%0];\n}\n"
+        ::"r"(smem_u32(bar)), "r"(static_cast<uint32_t>(pred))
+        : "memory");
+}
 __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
     uint32_t ok;
     asm volatile(
@@ -104,6 +118,21 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
         " selp.u32 %0, 1, 0, p;\n}\n"
         : "=r"(ok)
         : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// try_wait with a suspend-time hint: a thread whose phase is not complete is
+// descheduled until the phase completes or `ns` nanoseconds pass, instead of
+// polling the barrier (polling competes with the SM's other warps for the
+// shared-memory pipe).
+__device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t parity, uint32_t ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2, %3;\n"
+        " selp.u32 %0, 1, 0, p;\n}\n"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity), "r"(ns)
         : "memory");
     return ok != 0;
 }
@@ -123,6 +152,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
     return true;
 }
+// The same bound, for waits that are expected to be long (a producer waiting
+// for a consumer to free a stage): sleeps inside try_wait between checks.
+__device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, uint32_t parity,
+                                                        int* status) {
+    if (mbar_try_wait(bar, parity)) return true;
+    long long t0 = clock64();
+    while (!mbar_try_wait_sleep(bar, parity, 20000u)) {
+        if (clock64() - t0 > kWaitBoundCycles) {
+            atomicOr(status, kDevPipeTimeout);
+            return false;
+        }
+    }
+    return true;
+}
 
 // One-dimensional bulk copy global -> shared, completing on an mbarrier.
 __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t bytes,
@@ -130,6 +173,17 @@ __device__ __forceinline__ void bulk_g2s(void* dst, const void* src, uint32_t by
     asm volatile(
         "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
         ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar))
+        : "memory");
+}
+// Two-dimensional tiled TMA load (tensor map in kernel-parameter space),
+// completing on an mbarrier.  The innermost coordinate x times the element
+// size must be a multiple of 16 bytes.
+__device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t x, int32_t y,
+                                            uint64_t* bar) {
+    asm volatile(
+        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+        " [%0], [%1, {%2, %3}], [%4];"
+        ::"r"(smem_u32(dst)), "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
 // One-dimensional bulk copy shared -> global (bulk-group completion).

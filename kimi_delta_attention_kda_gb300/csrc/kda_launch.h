@@ -19,6 +19,7 @@ struct SeqGeometry {
     const int64_t* cu_seqlens;   // packed only (device)
     const int64_t* cu_chunks;    // packed only (device, n_seqs + 1)
     const int32_t* valid;        // packed only (device)
+    int* status;                 // device status word (set by the launchers)
 };
 
 cudaError_t launch_varlen_meta(const int64_t* cu_seqlens, int64_t n_seqs, int64_t total_tokens,

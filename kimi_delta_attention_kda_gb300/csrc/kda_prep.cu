@@ -24,35 +24,55 @@
 //
 // Tokens past the end of a sequence (a ragged last chunk) are zero: q = k = 0,
 // g = 0, beta = 0.  They then contribute nothing to any output or state.
+//
+// The kernel is persistent: every warp walks a strided list of (chunk, head)
+// items.  While it computes item i, the 2-D TMA loads of item i + 1's q, k and
+// g tiles are already in flight into the warp's other buffer; once an item's
+// inputs are in registers its buffer is reused as that item's scratch.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "kda_launch.h"
 
 namespace kda {
 namespace {
 
-constexpr int kPrepWarps = 2;
-// Per-warp shared memory: the packet image, then scratch tiles (16 x 128 BF16,
-// SW128): exp(-G) khat split into a BF16 high part and the BF16 rounding of
-// the remainder, the low parts of K^start and s Q^start (their high parts are
-// the packet tiles), K^end in token-row layout for the transpose, and R in FP32.
-constexpr uint32_t kPrepOffKinv = kPacketBytes;
-constexpr uint32_t kPrepOffKinvLo = kPacketBytes + 4096;
-constexpr uint32_t kPrepOffKsLo = kPacketBytes + 8192;
-constexpr uint32_t kPrepOffQsLo = kPacketBytes + 12288;
-constexpr uint32_t kPrepOffKen = kPacketBytes + 16384;
-constexpr uint32_t kPrepOffR = kPacketBytes + 20480;          // 16 x 16 FP32
-constexpr uint32_t kPrepWarpSmem = kPacketBytes + 20480 + 1024;
+constexpr int kPrepWarps = 8;
+// Per-warp shared memory: one 28 KB region that holds, in turn, an item's
+// TMA inputs, its scratch and its packet image:
+//   inputs  : q [16][128] BF16 at 0, k at 4096, g [16][128] FP32 at 8192
+//   scratch : [0,4K) K^start hi (packet KS) | [4K,8K) s Q^start hi (packet QS) |
+//             [8K,12K) exp(-G) khat hi | [12K,16K) exp(-G) khat lo |
+//             [16K,20K) K^start lo | [20K,24K) s Q^start lo | [24K,28K) K^end rows
+//             (tiles 16 x 128 BF16, SW128; "lo" = BF16 rounding of what the
+//             BF16 "hi" part left out)
+//   packet  : once the score MMAs are done, [8K,12K) receives K^end^T, [12K,13.5K)
+//             A^kk B, A^qk and D, and R (FP32) goes to [16K,17K): [0, 13824) is
+//             then the packet image.
+constexpr uint32_t kInQ = 0, kInK = 4096, kInG = 8192, kInBytes = 16384;
+constexpr uint32_t kPrepOffKinv = 8192;
+constexpr uint32_t kPrepOffKinvLo = 12288;
+constexpr uint32_t kPrepOffKsLo = 16384;
+constexpr uint32_t kPrepOffQsLo = 20480;
+constexpr uint32_t kPrepOffKen = 24576;
+constexpr uint32_t kPrepOffR = 16384;          // 16 x 16 FP32, after the MMAs
+constexpr uint32_t kPrepWarpSmem = 28672;
+constexpr uint32_t kPrepSmemBytes = kPrepWarps * kPrepWarpSmem + 64 + 1024;  // + barriers, align
 
 struct PrepArgs {
-    const __nv_bfloat16* q;
-    const __nv_bfloat16* k;
-    const float* g;
     const __nv_bfloat16* beta;
     uint8_t* packets;
     SeqGeometry geo;
     int64_t H;
     int64_t n_chunk_heads;
     float scale;
+};
+
+struct PrepMaps {
+    CUtensorMap q, k, g;   // [tokens][H * 128] views, boxes of 16 tokens x 128 channels
 };
 
 // Largest n in [0, N) with cu_chunks[n] <= c (cu_chunks non-decreasing,
@@ -67,21 +87,6 @@ __device__ __forceinline__ int64_t find_sequence(const int64_t* cu_chunks, int64
             hi = mid;
     }
     return lo;
-}
-
-__device__ __forceinline__ uint2 ldg_nc_u2(const void* p) {
-    uint2 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v2.u32 {%0,%1}, [%2];"
-                 : "=r"(r.x), "=r"(r.y)
-                 : "l"(p));
-    return r;
-}
-__device__ __forceinline__ float4 ldg_nc_f4(const void* p) {
-    float4 r;
-    asm volatile("ld.global.nc.L1::no_allocate.v4.f32 {%0,%1,%2,%3}, [%4];"
-                 : "=f"(r.x), "=f"(r.y), "=f"(r.z), "=f"(r.w)
-                 : "l"(p));
-    return r;
 }
 
 // Store 4 consecutive BF16 (channels 4*lane .. 4*lane+3) of token row t into a
@@ -104,65 +109,67 @@ __device__ __forceinline__ void st_row4_split(uint8_t* hi, uint8_t* lo, int t, i
     *reinterpret_cast<uint2*>(lo + off) = make_uint2(l0, l1);
 }
 
-__global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepArgs a) {
-    extern __shared__ __align__(1024) uint8_t smem[];
-    const int warp = threadIdx.x >> 5;
-    const int lane = threadIdx.x & 31;
-    const int64_t wid = static_cast<int64_t>(blockIdx.x) * kPrepWarps + warp;
-    if (wid >= a.n_chunk_heads) return;
-    const int64_t c = wid / a.H;
-    const int64_t h = wid - c * a.H;
-
-    // Token range of this chunk.
-    int64_t t0, len;
+// Token range [t0, t0 + len) of item (chunk c, head h); false when the item
+// does not exist (past the last chunk of a packed batch, or invalid offsets).
+__device__ __forceinline__ bool item_range(const PrepArgs& a, int64_t item, int64_t* t0,
+                                           int64_t* len, int64_t* c_out, int64_t* h_out) {
+    const int64_t c = item / a.H;
+    const int64_t h = item - c * a.H;
     if (a.geo.cu_chunks) {
-        if (!*a.geo.valid) return;
-        if (c >= a.geo.cu_chunks[a.geo.n_seqs]) return;
+        if (c >= a.geo.cu_chunks[a.geo.n_seqs]) return false;
         const int64_t n = find_sequence(a.geo.cu_chunks, a.geo.n_seqs, c);
-        t0 = a.geo.cu_seqlens[n] + kChunk * (c - a.geo.cu_chunks[n]);
-        len = a.geo.cu_seqlens[n + 1] - t0;
+        *t0 = a.geo.cu_seqlens[n] + kChunk * (c - a.geo.cu_chunks[n]);
+        *len = a.geo.cu_seqlens[n + 1] - *t0;
     } else {
         const int64_t n = c / a.geo.chunks_per_seq;
         const int64_t ci = c - n * a.geo.chunks_per_seq;
-        t0 = n * a.geo.tokens_per_seq + kChunk * ci;
-        len = a.geo.tokens_per_seq - kChunk * ci;
+        *t0 = n * a.geo.tokens_per_seq + kChunk * ci;
+        *len = a.geo.tokens_per_seq - kChunk * ci;
     }
-    if (len > kChunk) len = kChunk;
+    if (*len > kChunk) *len = kChunk;
+    *c_out = c;
+    *h_out = h;
+    return true;
+}
 
-    uint8_t* ws = smem + warp * kPrepWarpSmem;
+// One (chunk, head): inputs from the TMA tiles in `in`, packet image to `pk`,
+// scratch in `in` once the inputs are in registers.
+__device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t len, float scale,
+                                          int lane) {
+    const uint8_t* in = region;
+    uint8_t* ws = region;
+    uint8_t* sc = region;
     uint8_t* tKS = ws + kOffKS;
     uint8_t* tQS = ws + kOffQS;
     uint8_t* tKE = ws + kOffKE;
     uint8_t* tAKB = ws + kOffAKB;
     uint8_t* tAQK = ws + kOffAQK;
     float* tD = reinterpret_cast<float*>(ws + kOffD);
-    uint8_t* tKinv = ws + kPrepOffKinv;
-    uint8_t* tKinvLo = ws + kPrepOffKinvLo;
-    uint8_t* tKsLo = ws + kPrepOffKsLo;
-    uint8_t* tQsLo = ws + kPrepOffQsLo;
-    uint8_t* tKen = ws + kPrepOffKen;
-    float* tR = reinterpret_cast<float*>(ws + kPrepOffR);
+    uint8_t* tKinv = sc + kPrepOffKinv;
+    uint8_t* tKinvLo = sc + kPrepOffKinvLo;
+    uint8_t* tKsLo = sc + kPrepOffKsLo;
+    uint8_t* tQsLo = sc + kPrepOffQsLo;
+    uint8_t* tKen = sc + kPrepOffKen;
+    float* tR = reinterpret_cast<float*>(sc + kPrepOffR);
 
-    // ---- 1. Load q, k (BF16, 4 channels per lane), g (running sum -> G), beta.
+    // ---- 1. q, k (BF16, 4 channels per lane), g (running sum -> G) from the
+    // tiles; tokens past the end of the sequence read as zero.
     uint2 qv[kChunk], kv[kChunk];
     float G[kChunk][4];
     float red[2 * kChunk];   // partial sums of squares: q tokens 0..15, k tokens 0..15
     float run0 = 0.f, run1 = 0.f, run2 = 0.f, run3 = 0.f;
 #pragma unroll
     for (int t = 0; t < kChunk; ++t) {
-        if (t < len) {
-            const int64_t off = ((t0 + t) * a.H + h) * kHeadDim + 4 * lane;
-            qv[t] = ldg_nc_u2(a.q + off);
-            kv[t] = ldg_nc_u2(a.k + off);
-            const float4 gg = ldg_nc_f4(a.g + off);
-            run0 += gg.x;
-            run1 += gg.y;
-            run2 += gg.z;
-            run3 += gg.w;
-        } else {
-            qv[t] = make_uint2(0u, 0u);
-            kv[t] = make_uint2(0u, 0u);
-        }
+        const bool live = t < len;
+        const uint2 qq = *reinterpret_cast<const uint2*>(in + kInQ + t * 256 + 8 * lane);
+        const uint2 kq = *reinterpret_cast<const uint2*>(in + kInK + t * 256 + 8 * lane);
+        const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
+        qv[t] = live ? qq : make_uint2(0u, 0u);
+        kv[t] = live ? kq : make_uint2(0u, 0u);
+        run0 += live ? gg.x : 0.f;
+        run1 += live ? gg.y : 0.f;
+        run2 += live ? gg.z : 0.f;
+        run3 += live ? gg.w : 0.f;
         G[t][0] = run0;
         G[t][1] = run1;
         G[t][2] = run2;
@@ -174,8 +181,8 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepArgs a) {
         red[t] = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
         red[kChunk + t] = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
     }
-    float beta_f = 0.f;   // lane t < len holds beta of token t
-    if (lane < len) beta_f = __bfloat162float(a.beta[(t0 + lane) * a.H + h]);
+    // The input tiles are consumed: from here on the buffer is scratch.
+    __syncwarp();
 
     // ---- 2. Sums of squares over the 128 channels: butterfly reduce-scatter.
     // After the step with offset o, element i stands for original index
@@ -195,8 +202,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepArgs a) {
     // ---- 3. Decayed operands.
     const float e_last0 = __expf(G[kChunk - 1][0]), e_last1 = __expf(G[kChunk - 1][1]);
     const float e_last2 = __expf(G[kChunk - 1][2]), e_last3 = __expf(G[kChunk - 1][3]);
-    *reinterpret_cast<float4*>(tD + 4 * lane) = make_float4(e_last0, e_last1, e_last2, e_last3);
-    const float s = a.scale;
+    const float s = scale;
 #pragma unroll
     for (int t = 0; t < kChunk; ++t) {
         const float rq = __shfl_sync(0xffffffffu, rnorm, t);
@@ -247,6 +253,12 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepArgs a) {
             }
         }
     }
+    // The score operands are consumed; their tiles now take packet contents.
+    __syncwarp();
+    tD[dperm_index(4 * lane + 0)] = e_last0;
+    tD[dperm_index(4 * lane + 1)] = e_last1;
+    tD[dperm_index(4 * lane + 2)] = e_last2;
+    tD[dperm_index(4 * lane + 3)] = e_last3;
     const float beta_r0 = __shfl_sync(0xffffffffu, beta_f, gq);
     const float beta_r1 = __shfl_sync(0xffffffffu, beta_f, gq + 8);
 #pragma unroll
@@ -310,16 +322,93 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepArgs a) {
         }
     }
 
-    // ---- 7. Publish the packet with one bulk copy.
-    fence_proxy_async_smem();
-    __syncwarp();
+}
+
+__global__ void __launch_bounds__(kPrepWarps * 32, 1)
+    prep_kernel(PrepArgs a, const __grid_constant__ PrepMaps maps) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    uint8_t* region = smem + warp * kPrepWarpSmem;
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kPrepWarps * kPrepWarpSmem) + warp;
     if (lane == 0) {
-        uint8_t* dst = a.packets + (c * a.H + h) * static_cast<int64_t>(kPacketBytes);
-        bulk_s2g(dst, ws, kPacketBytes);
-        bulk_commit();
-        bulk_wait_read_all();
+        mbar_init(bar, 1);
+        fence_barrier_init();
     }
     __syncwarp();
+    if (a.geo.cu_chunks && !*a.geo.valid) return;
+
+    const int64_t stride = static_cast<int64_t>(gridDim.x) * kPrepWarps;
+    uint32_t phase = 0;
+    for (int64_t item = static_cast<int64_t>(blockIdx.x) * kPrepWarps + warp;
+         item < a.n_chunk_heads; item += stride) {
+        int64_t t0, len, c, h;
+        if (!item_range(a, item, &t0, &len, &c, &h)) break;   // items only grow past the end
+        if (lane == 0) {
+            // The previous packet store must have read the region before TMA
+            // overwrites it; the region's generic-proxy writes were fenced
+            // (fence.proxy.async) before that store.
+            bulk_wait_read_all();
+            mbar_arrive_expect_tx(bar, kInBytes);
+            const int32_t x = static_cast<int32_t>(h * kHeadDim), y = static_cast<int32_t>(t0);
+            tma_load_2d(region + kInQ, &maps.q, x, y, bar);
+            tma_load_2d(region + kInK, &maps.k, x, y, bar);
+            tma_load_2d(region + kInG, &maps.g, x, y, bar);
+        }
+        const float beta_f = lane < len ? __bfloat162float(a.beta[(t0 + lane) * a.H + h]) : 0.f;
+        if (!mbar_wait_bounded_sleep(bar, phase, a.geo.status)) {
+            // The loads may still land: wait for them (bounded) before leaving.
+            mbar_wait_bounded_sleep(bar, phase, a.geo.status);
+            break;
+        }
+        phase ^= 1u;
+        prep_item(region, beta_f, len, a.scale, lane);
+
+        // Publish the packet with one bulk copy.
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lane == 0) {
+            bulk_s2g(a.packets + (c * a.H + h) * static_cast<int64_t>(kPacketBytes), region,
+                     kPacketBytes);
+            bulk_commit();
+        }
+    }
+    if (lane == 0) bulk_wait_all();
+    __syncwarp();
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 prep_tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// [tokens][H * 128] view of a token-major tensor, boxes of 16 tokens x 128 channels.
+cudaError_t encode_rows_map(CUtensorMap* map, const void* base, CUtensorMapDataType dt,
+                            int64_t esize, int64_t tokens, int64_t H) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = prep_tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(H * kHeadDim),
+                                static_cast<cuuint64_t>(tokens)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(H * kHeadDim * esize)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(kHeadDim), static_cast<cuuint32_t>(kChunk)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
+                     CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
 }  // namespace
@@ -327,29 +416,38 @@ __global__ void __launch_bounds__(kPrepWarps * 32) prep_kernel(PrepArgs a) {
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const void* beta,
                         uint8_t* packets, const SeqGeometry& geo, int64_t H, float scale,
                         int* status, cudaStream_t stream) {
-    (void)status;
     PrepArgs a;
-    a.q = static_cast<const __nv_bfloat16*>(q);
-    a.k = static_cast<const __nv_bfloat16*>(k);
-    a.g = g;
     a.beta = static_cast<const __nv_bfloat16*>(beta);
     a.packets = packets;
     a.geo = geo;
+    a.geo.status = status;
     a.H = H;
     a.n_chunk_heads = geo.chunk_ub * H;
     a.scale = scale;
-    if (a.n_chunk_heads <= 0) return cudaSuccess;
-    const int64_t blocks = (a.n_chunk_heads + kPrepWarps - 1) / kPrepWarps;
-    if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    const uint32_t smem = kPrepWarps * kPrepWarpSmem;
-    static bool configured = false;   // attribute is per function; setting it twice is harmless
-    if (!configured) {
-        cudaError_t e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+    if (a.n_chunk_heads <= 0 || geo.tokens <= 0) return cudaSuccess;
+    if (geo.tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // TMA coordinates are int32
+    PrepMaps maps;
+    cudaError_t e = encode_rows_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, geo.tokens, H);
+    if (e == cudaSuccess)
+        e = encode_rows_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, geo.tokens, H);
+    if (e == cudaSuccess)
+        e = encode_rows_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, geo.tokens, H);
+    if (e != cudaSuccess) return e;
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    static bool configured[64] = {};
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kPrepSmemBytes));
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured[dev] = true;
     }
-    prep_kernel<<<static_cast<unsigned>(blocks), kPrepWarps * 32, smem, stream>>>(a);
+    e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    // One CTA per SM (persistent); fewer when there are fewer items than warps.
+    int64_t blocks = (a.n_chunk_heads + kPrepWarps - 1) / kPrepWarps;
+    if (blocks > sms) blocks = sms;
+    prep_kernel<<<static_cast<unsigned>(blocks), kPrepWarps * 32, kPrepSmemBytes, stream>>>(a, maps);
     return cudaGetLastError();
 }
 

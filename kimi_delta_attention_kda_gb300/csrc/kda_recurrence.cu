@@ -15,16 +15,20 @@
 // accumulator -> operand layout change is an 8 x 8 transpose in registers
 // (movmatrix).  No CTA ever waits on another CTA.
 //
-// A producer warp streams the per-chunk packets (kda_common.cuh) and the V
-// rows into a ring of shared-memory stages with one-dimensional bulk copies
-// (TMA), completing on mbarriers; every wait is bounded (kda_common.cuh).
+// A producer warp streams, per chunk, the packet (kda_common.cuh; one 1-D bulk
+// copy) and the CTA's 16 x (value columns) tile of V (one 2-D tensor-map TMA
+// load) into a ring of shared-memory stages, completing on mbarriers; every
+// wait is bounded (kda_common.cuh).
+#include <cuda.h>
+#include <cudaTypedefs.h>
+
+#include <mutex>
+
 #include "kda_common.cuh"
 #include "kda_launch.h"
 
 namespace kda {
 namespace {
-
-constexpr int kStages = 4;
 
 struct RecArgs {
     const __nv_bfloat16* v;
@@ -47,16 +51,117 @@ __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
 template <int NW>
 struct RecLayout {
     static constexpr int kCols = 8 * NW;                        // value columns per CTA
+    static constexpr int kStages = NW <= 4 ? 8 : (NW <= 8 ? 6 : 4);
     static constexpr uint32_t kVRowBytes = kCols * 2;           // one token row of V
     static constexpr uint32_t kStageBytes =
         ((kPacketBytes + kChunk * kVRowBytes + 1023) / 1024) * 1024;
     static constexpr uint32_t kBarOff = kStages * kStageBytes;
     static constexpr uint32_t kSmemBytes = kBarOff + 2 * kStages * 8 + 1024;  // + align slack
+    // With few warps per CTA every register is available, so each chunk's
+    // operand fragments are loaded in one burst ahead of use.
+    static constexpr bool kPrefetch = NW <= 4;
 };
 
+// Operand fragments of one chunk for one warp (m16n8k16 A-operand layout).
+struct ChunkFrags {
+    uint32_t ks[8][4];   // (K^start)^T, k-steps over keys
+    uint32_t qs[8][4];   // s (Q^start)^T
+    uint32_t ke[8][4];   // (K^end)^T, one 16-key tile each
+    uint32_t akb[4];     // A^kk B
+    uint32_t aqk[4];     // A^qk
+    float4 d[4];         // D for keys 16 m + g8 and 16 m + g8 + 8, m = 0..7
+    uint32_t v[2];       // V^T at tokens g8 and g8 + 8, values 2 t4, 2 t4 + 1
+};
+
+__device__ __forceinline__ void load_frags(const uint8_t* stage, uint32_t vrow_bytes, int warp,
+                                           int lane, ChunkFrags& f) {
+    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t hiA = lane >> 4;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const uint32_t sKS = smem_u32(stage + kOffKS);
+    const uint32_t sQS = smem_u32(stage + kOffQS);
+    const uint32_t sKE = smem_u32(stage + kOffKE);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) ldsm_x4(f.ks[kk], sKS + sw128_off(16, rowA, 2 * kk + hiA));
+    ldsm_x4(f.akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
+    const uint8_t* sV = stage + kPacketBytes + (8 * warp + 2 * t4) * 2;
+    f.v[0] = *reinterpret_cast<const uint32_t*>(sV + g8 * vrow_bytes);
+    f.v[1] = *reinterpret_cast<const uint32_t*>(sV + (g8 + 8) * vrow_bytes);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) ldsm_x4(f.qs[kk], sQS + sw128_off(16, rowA, 2 * kk + hiA));
+    const float4* dp = reinterpret_cast<const float4*>(stage + kOffD) + 4 * g8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f.d[j] = dp[j];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) ldsm_x4(f.ke[mt], sKE + sw32_off(16 * mt + rowA, hiA));
+    ldsm_x4(f.aqk, smem_u32(stage + kOffAQK + sw32_off(rowA, hiA)));
+}
+
+__device__ __forceinline__ void st_global_u32_if(void* p, uint32_t v, bool pred) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p st.global.b32 [%0], %1;\n}\n"
+                 ::"l"(p), "r"(v), "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+}
+
+__device__ __forceinline__ float dsel(const float4& a, int i) {
+    return i == 0 ? a.x : (i == 1 ? a.y : (i == 2 ? a.z : a.w));
+}
+
+// One chunk for one warp: advances Sf (FP32 S^T slice) and returns O^T in o.
+// Sb holds the BF16 B-operand fragments of the incoming state.
+__device__ __forceinline__ void chunk_step(const ChunkFrags& f, float (&Sf)[8][4],
+                                           const uint32_t (&Sb)[8][2], int64_t len, int g8,
+                                           float (&o)[4]) {
+    // W^T = (K^start)^T S^T: two accumulators halve the dependent chain.
+    float w0[4] = {0.f, 0.f, 0.f, 0.f}, w1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; kk += 2) {
+        mma_bf16(w0, f.ks[kk], Sb[kk], w0);
+        mma_bf16(w1, f.ks[kk + 1], Sb[kk + 1], w1);
+    }
+    // D S^T, in place (the BF16 copy of the old state is already in Sb).
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const float d0 = dsel(f.d[mt >> 1], 2 * (mt & 1));
+        const float d1 = dsel(f.d[mt >> 1], 2 * (mt & 1) + 1);
+        Sf[mt][0] *= d0;
+        Sf[mt][1] *= d0;
+        Sf[mt][2] *= d1;
+        Sf[mt][3] *= d1;
+    }
+    // Delta^T = V^T - W^T; tokens past the end of the sequence read as zero.
+    const float m0 = g8 < len ? 1.f : 0.f, m1 = g8 + 8 < len ? 1.f : 0.f;
+    uint32_t Db[2];
+    Db[0] = movm_t(pack_bf16(m0 * bf16_lo(f.v[0]) - (w0[0] + w1[0]),
+                             m0 * bf16_hi(f.v[0]) - (w0[1] + w1[1])));
+    Db[1] = movm_t(pack_bf16(m1 * bf16_lo(f.v[1]) - (w0[2] + w1[2]),
+                             m1 * bf16_hi(f.v[1]) - (w0[3] + w1[3])));
+    // U^T = (A^kk B) Delta^T.
+    float u[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_bf16(u, f.akb, Db, u);
+    // P^T = s (Q^start)^T S^T, off the state chain: fills the U latency.
+    float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+    for (int kk = 0; kk < 8; kk += 2) {
+        mma_bf16(p0, f.qs[kk], Sb[kk], p0);
+        mma_bf16(p1, f.qs[kk + 1], Sb[kk + 1], p1);
+    }
+    uint32_t Ub[2];
+    Ub[0] = movm_t(pack_bf16(u[0], u[1]));
+    Ub[1] = movm_t(pack_bf16(u[2], u[3]));
+    // S^T <- D S^T + (K^end)^T U^T.
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) mma_bf16(Sf[mt], f.ke[mt], Ub, Sf[mt]);
+    // O^T = P^T + A^qk U^T.
+    float pin[4] = {p0[0] + p1[0], p0[1] + p1[1], p0[2] + p1[2], p0[3] + p1[3]};
+    mma_bf16(o, f.aqk, Ub, pin);
+}
+
 template <int NW>
-__global__ void __launch_bounds__((NW + 1) * 32) recurrence_kernel(RecArgs a) {
+__global__ void __launch_bounds__((NW + 1) * 32)
+    recurrence_kernel(RecArgs a, const __grid_constant__ CUtensorMap vmap) {
     using L = RecLayout<NW>;
+    constexpr int kStages = L::kStages;
     extern __shared__ uint8_t smem_raw[];
     // 1024-byte aligned base for the stages.
     uint8_t* smem = reinterpret_cast<uint8_t*>(
@@ -97,31 +202,32 @@ __global__ void __launch_bounds__((NW + 1) * 32) recurrence_kernel(RecArgs a) {
 
     if (warp == NW) {
         // ------------------------------------------------------------ producer
-        int64_t fills[kStages] = {0, 0, 0, 0};
+        uint32_t fill_parity = 0;   // bit s: parity of the latest fill of stage s
+        uint32_t filled = 0;        // bit s: stage s has been filled at least once
         bool ok = true;
         for (int64_t c = 0; c < nch && ok; ++c) {
             const int s = static_cast<int>(c % kStages);
-            if (c >= kStages) ok = mbar_wait_bounded(&empty[s], ((c / kStages) - 1) & 1, a.status);
+            if (c >= kStages)
+                ok = mbar_wait_bounded_sleep(&empty[s], ((c / kStages) - 1) & 1, a.status);
             if (!ok) break;
-            int64_t len = seqlen - kChunk * c;
-            if (len > kChunk) len = kChunk;
             uint8_t* stage = smem + s * L::kStageBytes;
-            if (lane == 0)
-                mbar_arrive_expect_tx(&full[s], kPacketBytes + static_cast<uint32_t>(len) * L::kVRowBytes);
-            __syncwarp();
-            if (lane == 0)
+            if (lane == 0) {
+                // The V box always lands whole: rows past the last token are
+                // zero-filled, rows past this sequence are masked by the consumer.
+                mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * L::kVRowBytes);
                 bulk_g2s(stage, a.packets + ((c_begin + c) * a.H + h) * static_cast<int64_t>(kPacketBytes),
                          kPacketBytes, &full[s]);
-            if (lane < len)
-                bulk_g2s(stage + kPacketBytes + lane * L::kVRowBytes,
-                         a.v + ((tok0 + kChunk * c + lane) * a.H + h) * kHeadDim + v0,
-                         L::kVRowBytes, &full[s]);
-            fills[s] += 1;
+                tma_load_2d(stage + kPacketBytes, &vmap, static_cast<int32_t>(h * kHeadDim + v0),
+                            static_cast<int32_t>(tok0 + kChunk * c), &full[s]);
+            }
+            __syncwarp();
+            fill_parity ^= (filled >> s & 1u) << s;   // flip after the first fill
+            filled |= 1u << s;
         }
         if (!ok) {
             // Let every copy already issued land before the CTA can exit.
             for (int s = 0; s < kStages; ++s)
-                if (fills[s] > 0) mbar_wait_bounded(&full[s], (fills[s] - 1) & 1, a.status);
+                if (filled >> s & 1u) mbar_wait_bounded(&full[s], (fill_parity >> s) & 1u, a.status);
         }
         return;
     }
@@ -156,110 +262,51 @@ __global__ void __launch_bounds__((NW + 1) * 32) recurrence_kernel(RecArgs a) {
         Sb[mt][1] = movm_t(pack_bf16(Sf[mt][2], Sf[mt][3]));
     }
 
-    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;   // A-operand ldmatrix row
-    const uint32_t hiA = lane >> 4;                             // A-operand column half
     bool ok = true;
-    for (int64_t c = 0; c < nch; ++c) {
+    ChunkFrags f;
+    if (L::kPrefetch && nch > 0) {
+        ok = mbar_wait_bounded(&full[0], 0, a.status);
+        if (ok) load_frags(smem, L::kVRowBytes, warp, lane, f);
+    }
+    for (int64_t c = 0; c < nch && ok; ++c) {
         const int s = static_cast<int>(c % kStages);
-        if (!mbar_wait_bounded(&full[s], (c / kStages) & 1, a.status)) {
-            ok = false;
-            break;
-        }
         const uint8_t* stage = smem + s * L::kStageBytes;
-        const uint32_t sKS = smem_u32(stage + kOffKS);
-        const uint32_t sQS = smem_u32(stage + kOffQS);
-        const uint32_t sKE = smem_u32(stage + kOffKE);
-        const float* sD = reinterpret_cast<const float*>(stage + kOffD);
-        const uint8_t* sV = stage + kPacketBytes;
+        if (!L::kPrefetch) {
+            if (!mbar_wait_bounded(&full[s], (c / kStages) & 1, a.status)) {
+                ok = false;
+                break;
+            }
+            load_frags(stage, L::kVRowBytes, warp, lane, f);
+        }
         int64_t len = seqlen - kChunk * c;
         if (len > kChunk) len = kChunk;
 
-        // W^T = (K^start)^T S^T, two accumulators to halve the dependent chain.
-        float w0[4] = {0.f, 0.f, 0.f, 0.f}, w1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            uint32_t af[4];
-            ldsm_x4(af, sKS + sw128_off(16, rowA, 2 * kk + hiA));
-            if (kk & 1)
-                mma_bf16(w1, af, Sb[kk], w1);
-            else
-                mma_bf16(w0, af, Sb[kk], w0);
-        }
-        // Delta^T = V^T - W^T (tokens g8, g8 + 8; values 2 t4, 2 t4 + 1).
-        float vv[4] = {0.f, 0.f, 0.f, 0.f};
-        if (g8 < len) {
-            const uint32_t x = *reinterpret_cast<const uint32_t*>(sV + g8 * L::kVRowBytes + (8 * warp + 2 * t4) * 2);
-            vv[0] = bf16_lo(x);
-            vv[1] = bf16_hi(x);
-        }
-        if (g8 + 8 < len) {
-            const uint32_t x = *reinterpret_cast<const uint32_t*>(sV + (g8 + 8) * L::kVRowBytes + (8 * warp + 2 * t4) * 2);
-            vv[2] = bf16_lo(x);
-            vv[3] = bf16_hi(x);
-        }
-        uint32_t Db[2];
-        Db[0] = movm_t(pack_bf16(vv[0] - (w0[0] + w1[0]), vv[1] - (w0[1] + w1[1])));
-        Db[1] = movm_t(pack_bf16(vv[2] - (w0[2] + w1[2]), vv[3] - (w0[3] + w1[3])));
-
-        // U^T = (A^kk B) Delta^T.
-        float u[4] = {0.f, 0.f, 0.f, 0.f};
-        {
-            uint32_t af[4];
-            ldsm_x4(af, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
-            mma_bf16(u, af, Db, u);
-        }
-        // P^T = s (Q^start)^T S^T (off the state chain).
-        float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            uint32_t af[4];
-            ldsm_x4(af, sQS + sw128_off(16, rowA, 2 * kk + hiA));
-            if (kk & 1)
-                mma_bf16(p1, af, Sb[kk], p1);
-            else
-                mma_bf16(p0, af, Sb[kk], p0);
-        }
-        uint32_t Ub[2];
-        Ub[0] = movm_t(pack_bf16(u[0], u[1]));
-        Ub[1] = movm_t(pack_bf16(u[2], u[3]));
-
-        // S^T <- D S^T + (K^end)^T U^T.
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            uint32_t af[4];
-            ldsm_x4(af, sKE + sw32_off(16 * mt + rowA, hiA));
-            const float d0 = sD[16 * mt + g8];
-            const float d1 = sD[16 * mt + g8 + 8];
-            float cin[4] = {Sf[mt][0] * d0, Sf[mt][1] * d0, Sf[mt][2] * d1, Sf[mt][3] * d1};
-            mma_bf16(Sf[mt], af, Ub, cin);
-        }
-        // O^T = P^T + A^qk U^T.
         float o[4];
-        {
-            uint32_t af[4];
-            ldsm_x4(af, smem_u32(stage + kOffAQK + sw32_off(rowA, hiA)));
-            float pin[4] = {p0[0] + p1[0], p0[1] + p1[1], p0[2] + p1[2], p0[3] + p1[3]};
-            mma_bf16(o, af, Ub, pin);
-        }
-        // Every read of this stage is done: hand it back to the producer.
-        __syncwarp();
-        if (lane == 0) mbar_arrive(&empty[s]);
+        chunk_step(f, Sf, Sb, len, g8, o);
 
-        // Store O (tokens g8 and g8 + 8, values vcol + 2 t4 .. + 1).
-        const int64_t tok = tok0 + kChunk * c;
-        if (g8 < len)
-            *reinterpret_cast<uint32_t*>(a.out + ((tok + g8) * a.H + h) * kHeadDim + vcol + 2 * t4) =
-                pack_bf16(o[0], o[1]);
-        if (g8 + 8 < len)
-            *reinterpret_cast<uint32_t*>(a.out + ((tok + g8 + 8) * a.H + h) * kHeadDim + vcol + 2 * t4) =
-                pack_bf16(o[2], o[3]);
-
-        // BF16 operand copy of the new state for the next chunk.
+        // BF16 operand copy of the new state: first, since the next chunk's
+        // chain starts from it (warps issue in order).
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt) {
             Sb[mt][0] = movm_t(pack_bf16(Sf[mt][0], Sf[mt][1]));
             Sb[mt][1] = movm_t(pack_bf16(Sf[mt][2], Sf[mt][3]));
         }
+        // Every read of this stage is done: hand it back to the producer.
+        __syncwarp();
+        mbar_arrive_if(&empty[s], lane == 0);
+        // Next chunk's fragments, in flight while this chunk finishes.
+        if (L::kPrefetch && c + 1 < nch) {
+            const int s1 = static_cast<int>((c + 1) % kStages);
+            if (mbar_wait_bounded(&full[s1], ((c + 1) / kStages) & 1, a.status))
+                load_frags(smem + s1 * L::kStageBytes, L::kVRowBytes, warp, lane, f);
+            else
+                ok = false;
+        }
+
+        // Store O (tokens g8 and g8 + 8, values vcol + 2 t4 .. + 1), predicated.
+        __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + g8) * a.H + h) * kHeadDim + vcol + 2 * t4;
+        st_global_u32_if(orow, pack_bf16(o[0], o[1]), g8 < len);
+        st_global_u32_if(orow + 8 * a.H * kHeadDim, pack_bf16(o[2], o[3]), g8 + 8 < len);
     }
 
     if (ok && a.final_state) {
@@ -276,18 +323,58 @@ __global__ void __launch_bounds__((NW + 1) * 32) recurrence_kernel(RecArgs a) {
     }
 }
 
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+    static std::once_flag once;
+    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                             &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+        else
+            cudaGetLastError();
+    });
+    return fn;
+}
+
+// Tensor map of v viewed as a 2-D BF16 array [tokens][H * 128] with boxes of
+// 16 tokens x `cols` value columns.
+cudaError_t encode_v_map(CUtensorMap* map, const void* v, int64_t tokens, int64_t H, int cols) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(H * kHeadDim),
+                                static_cast<cuuint64_t>(tokens > 0 ? tokens : 1)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(H * kHeadDim * 2)};
+    const cuuint32_t box[2] = {static_cast<cuuint32_t>(cols), static_cast<cuuint32_t>(kChunk)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(v), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 template <int NW>
 cudaError_t launch_nw(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
     using L = RecLayout<NW>;
-    static bool configured = false;
-    if (!configured) {
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
         cudaError_t e = cudaFuncSetAttribute(recurrence_kernel<NW>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(L::kSmemBytes));
         if (e != cudaSuccess) return e;
-        configured = true;
+        configured[dev] = true;
     }
-    recurrence_kernel<NW><<<static_cast<unsigned>(blocks), (NW + 1) * 32, L::kSmemBytes, stream>>>(a);
+    CUtensorMap vmap;
+    alignas(64) static const char kZero[16] = {};
+    // With no tokens nothing is loaded; still hand the kernel a well-formed map.
+    const void* vbase = a.v ? static_cast<const void*>(a.v) : static_cast<const void*>(kZero);
+    cudaError_t e = encode_v_map(&vmap, vbase, a.geo.tokens, a.H, L::kCols);
+    if (e != cudaSuccess) return e;
+    recurrence_kernel<NW><<<static_cast<unsigned>(blocks), (NW + 1) * 32, L::kSmemBytes, stream>>>(a, vmap);
     return cudaGetLastError();
 }
 
@@ -309,6 +396,7 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
     a.status = status;
     const int64_t blocks = geo.n_seqs * H * nsplit;
     if (blocks <= 0) return cudaSuccess;
+    if (geo.tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // TMA coordinates are int32
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     switch (nsplit) {
         case 1: return launch_nw<16>(a, blocks, stream);

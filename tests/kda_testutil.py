@@ -50,7 +50,9 @@ def unpack_packets(packets):
     p = np.ascontiguousarray(packets)
     i128, i32 = _sw128_index(16), _sw32_index(16)
     iKE = _sw32_index(128)
-    d = p[..., OFF_D:OFF_D + 512].copy().view(np.float32).astype(np.float64)
+    dp = p[..., OFF_D:OFF_D + 512].copy().view(np.float32).astype(np.float64)
+    c = np.arange(128)
+    d = dp[..., 16 * (c & 7) + 2 * (c >> 4) + ((c >> 3) & 1)]   # undo the permutation
     return {
         "Kst": _bf16_at(p, OFF_KS, i128),          # [..., 16 tokens, 128 keys]
         "Qst_s": _bf16_at(p, OFF_QS, i128),        # s * Q^start rows
