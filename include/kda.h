@@ -95,7 +95,8 @@ int kda_device_status(void* stream, int* status);
  * Number of CTAs that share one (sequence, head) in the recurrence: each owns
  * 128 / nsplit value columns (value columns are independent recurrences,
  * "FlashKDA column split" section 3.1).  nsplit is one of 1, 2, 4, 8, 16, or 0
- * for the automatic choice (the largest split whose grid fits the SM count).
+ * for the automatic choice (the largest split up to 8 whose grid fits the SM
+ * count).
  * Process-wide setting; returns KDA_ERR_ARG for other values.
  */
 int kda_set_split(int nsplit);

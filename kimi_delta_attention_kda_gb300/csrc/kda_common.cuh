@@ -27,8 +27,8 @@ constexpr int kChunk = 16;      // C = 16 tokens per chunk
 // the 128-byte or 32-byte XOR swizzle that both ldmatrix (conflict-free rows)
 // and tcgen05 shared-memory descriptors understand:
 //
-//  [    0,  4096)  KS   : K^start^T, 16 token rows x 128 key channels, SW128,
-//                         two 64-channel slabs of 16 x 128 B
+//  [    0,  4096)  KS   : K' = -(A^kk B_c) K^start^T, 16 token rows x 128 key
+//                         channels, SW128, two 64-channel slabs of 16 x 128 B
 //  [ 4096,  8192)  QS   : s * Q^start^T, same layout (the scale s is folded in)
 //  [ 8192, 12288)  KE   : K^end^T, 128 key rows x 16 tokens (32 B rows), SW32
 //  [12288, 12800)  AKB  : A^kk B_c (A^kk with column j scaled by beta_j), 16 x 16, SW32
@@ -38,7 +38,10 @@ constexpr int kChunk = 16;      // C = 16 tokens per chunk
 //                         the recurrence thread that owns key rows r and r + 8 of
 //                         every 16-key tile reads its 16 factors contiguously
 //
-// Folding beta into A^kk uses B (A^kk)^T = (A^kk B)^T, so U = (V - S K^start)(A^kk B)^T.
+// Folding beta into A^kk uses B (A^kk)^T = (A^kk B)^T, so
+//   U = (V - S K^start)(A^kk B)^T = V (A^kk B)^T + S K'^T,
+// one contraction over the keys whose accumulator starts at V (A^kk B)^T, a
+// term that does not depend on the state.
 // ---------------------------------------------------------------------------
 constexpr uint32_t kOffKS = 0;
 constexpr uint32_t kOffQS = 4096;

@@ -50,15 +50,17 @@ constexpr int kPrepWarps = 8;
 //             (tiles 16 x 128 BF16, SW128; "lo" = BF16 rounding of what the
 //             BF16 "hi" part left out)
 //   packet  : once the score MMAs are done, [8K,12K) receives K^end^T, [12K,13.5K)
-//             A^kk B, A^qk and D, and R (FP32) goes to [16K,17K): [0, 13824) is
-//             then the packet image.
+//             A^kk B, A^qk and D; R (FP32) and the low part of A^kk B go to
+//             [20K,22.5K); finally -(A^kk B) K^start^T replaces K^start in [0,4K):
+//             [0, 13824) is then the packet image.
 constexpr uint32_t kInQ = 0, kInK = 4096, kInG = 8192, kInBytes = 16384;
 constexpr uint32_t kPrepOffKinv = 8192;
 constexpr uint32_t kPrepOffKinvLo = 12288;
 constexpr uint32_t kPrepOffKsLo = 16384;
 constexpr uint32_t kPrepOffQsLo = 20480;
 constexpr uint32_t kPrepOffKen = 24576;
-constexpr uint32_t kPrepOffR = 16384;          // 16 x 16 FP32, after the MMAs
+constexpr uint32_t kPrepOffAkbLo = 20480;     // 16 x 16 BF16 SW32, after the score MMAs
+constexpr uint32_t kPrepOffR = 21504;          // 16 x 16 FP32, after the score MMAs
 constexpr uint32_t kPrepWarpSmem = 28672;
 constexpr uint32_t kPrepSmemBytes = kPrepWarps * kPrepWarpSmem + 64 + 1024;  // + barriers, align
 
@@ -314,14 +316,62 @@ __device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t
             }
             x[i] = acc;
         }
-        // Column `lane` of A^kk B: scale by beta_lane.
+        // Column `lane` of A^kk B (scaled by beta_lane), as BF16 high and low parts.
 #pragma unroll
         for (int i = 0; i < kChunk; ++i) {
-            const __nv_bfloat16 v = __float2bfloat16_rn(x[i] * beta_f);
-            *reinterpret_cast<__nv_bfloat16*>(tAKB + sw32_off(i, lane >> 3) + 2 * (lane & 7)) = v;
+            const float a = x[i] * beta_f;
+            const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+            const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
+            const uint32_t off = sw32_off(i, lane >> 3) + 2 * (lane & 7);
+            *reinterpret_cast<__nv_bfloat16*>(tAKB + off) = hi;
+            *reinterpret_cast<__nv_bfloat16*>(sc + kPrepOffAkbLo + off) = lo;
         }
     }
+    __syncwarp();
 
+    // ---- 7. K' = -(A^kk B) K^start^T (16 tokens x 128 keys), so that the
+    // recurrence gets U^T = (A^kk B) V^T + K' S^T from one contraction over
+    // the keys: (V - S K^start)(A^kk B)^T = V (A^kk B)^T - S (K^start (A^kk B)^T).
+    // hi*hi + hi*lo + lo*hi of the split operands, FP32 accumulation; it then
+    // replaces K^start in the packet.
+    {
+        uint32_t ah[4], al[4];
+        const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+        ldsm_x4(ah, smem_u32(tAKB + sw32_off(rowA, lane >> 4)));
+        ldsm_x4(al, smem_u32(sc + kPrepOffAkbLo + sw32_off(rowA, lane >> 4)));
+        const int mi = lane >> 3;
+        const int tok = 8 * (mi & 1) + (lane & 7);
+        float acc[16][4];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            // B fragments (k = token, n = key) of two 8-key tiles from the token-row tiles.
+            uint32_t bh[4], bl[4];
+            const uint32_t off = sw128_off(16, tok, 2 * p + (mi >> 1));
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(bh[0]), "=r"(bh[1]), "=r"(bh[2]), "=r"(bh[3])
+                         : "r"(smem_u32(tKS + off)));
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(bl[0]), "=r"(bl[1]), "=r"(bl[2]), "=r"(bl[3])
+                         : "r"(smem_u32(tKsLo + off)));
+#pragma unroll
+            for (int half = 0; half < 2; ++half) {
+                float* d = acc[2 * p + half];
+                d[0] = d[1] = d[2] = d[3] = 0.f;
+                mma_bf16(d, ah, bh + 2 * half, d);
+                mma_bf16(d, ah, bl + 2 * half, d);
+                mma_bf16(d, al, bh + 2 * half, d);
+            }
+        }
+        __syncwarp();   // every lane's K^start fragments are in registers
+        const int gq2 = lane >> 2, tq2 = lane & 3;
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            *reinterpret_cast<uint32_t*>(tKS + sw128_off(16, gq2, nt) + 4 * tq2) =
+                pack_bf16(-acc[nt][0], -acc[nt][1]);
+            *reinterpret_cast<uint32_t*>(tKS + sw128_off(16, gq2 + 8, nt) + 4 * tq2) =
+                pack_bf16(-acc[nt][2], -acc[nt][3]);
+        }
+    }
 }
 
 __global__ void __launch_bounds__(kPrepWarps * 32, 1)

@@ -3,10 +3,11 @@
 // For every chunk c of one (sequence, head), in the transposed layout of
 // "FlashKDA column split", section 3.1 (one row per token, one column per
 // value channel):
-//   W^T   = (K^start)^T S^T                        (16 tokens x values)
-//   U^T   = (A^kk B)(V^T - W^T)
+//   U^T   = (A^kk B)(V^T - (K^start)^T S^T) = (A^kk B) V^T + K' S^T
 //   O^T   = s (Q^start)^T S^T + A^qk U^T
 //   S^T  <- D_{0:15} S^T + (K^end)^T U^T
+// with K' = -(A^kk B)(K^start)^T formed by the preparation kernel, so that the
+// state enters the chunk's error term through a single contraction.
 // Value columns are independent recurrences that share the per-chunk inputs
 // (section 3.1), so the 128 value columns of a head are split over `nsplit`
 // CTAs and, inside a CTA, over warps of 8 columns each.  Each warp keeps its
@@ -64,29 +65,31 @@ struct RecLayout {
 
 // Operand fragments of one chunk for one warp (m16n8k16 A-operand layout).
 struct ChunkFrags {
-    uint32_t ks[8][4];   // (K^start)^T, k-steps over keys
+    uint32_t ks[8][4];   // K' = -(A^kk B)(K^start)^T, k-steps over keys
     uint32_t qs[8][4];   // s (Q^start)^T
     uint32_t ke[8][4];   // (K^end)^T, one 16-key tile each
     uint32_t akb[4];     // A^kk B
     uint32_t aqk[4];     // A^qk
     float4 d[4];         // D for keys 16 m + g8 and 16 m + g8 + 8, m = 0..7
-    uint32_t v[2];       // V^T at tokens g8 and g8 + 8, values 2 t4, 2 t4 + 1
+    uint32_t vb[2];      // V^T as a B operand (k = token, n = this warp's 8 values)
 };
 
 __device__ __forceinline__ void load_frags(const uint8_t* stage, uint32_t vrow_bytes, int warp,
                                            int lane, ChunkFrags& f) {
     const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
     const uint32_t hiA = lane >> 4;
-    const int g8 = lane >> 2, t4 = lane & 3;
+    const int g8 = lane >> 2;
     const uint32_t sKS = smem_u32(stage + kOffKS);
     const uint32_t sQS = smem_u32(stage + kOffQS);
     const uint32_t sKE = smem_u32(stage + kOffKE);
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) ldsm_x4(f.ks[kk], sKS + sw128_off(16, rowA, 2 * kk + hiA));
     ldsm_x4(f.akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
-    const uint8_t* sV = stage + kPacketBytes + (8 * warp + 2 * t4) * 2;
-    f.v[0] = *reinterpret_cast<const uint32_t*>(sV + g8 * vrow_bytes);
-    f.v[1] = *reinterpret_cast<const uint32_t*>(sV + (g8 + 8) * vrow_bytes);
+    // V tile rows are tokens; lanes 0-7 address tokens 0-7, lanes 8-15 tokens 8-15.
+    const uint8_t* sV = stage + kPacketBytes + (lane & 15) * vrow_bytes + 16 * warp;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(f.vb[0]), "=r"(f.vb[1])
+                 : "r"(smem_u32(sV)));
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) ldsm_x4(f.qs[kk], sQS + sw128_off(16, rowA, 2 * kk + hiA));
     const float4* dp = reinterpret_cast<const float4*>(stage + kOffD) + 4 * g8;
@@ -109,15 +112,21 @@ __device__ __forceinline__ float dsel(const float4& a, int i) {
 
 // One chunk for one warp: advances Sf (FP32 S^T slice) and returns O^T in o.
 // Sb holds the BF16 B-operand fragments of the incoming state.
+//   U^T = (A^kk B) V^T + K' S^T          (K' = -(A^kk B)(K^start)^T, from the packet)
+//   O^T = s (Q^start)^T S^T + A^qk U^T
+//   S^T <- D S^T + (K^end)^T U^T
+// Token rows past the end of the sequence meet zero columns of A^kk B (beta
+// is zero there), so they need no masking.
 __device__ __forceinline__ void chunk_step(const ChunkFrags& f, float (&Sf)[8][4],
-                                           const uint32_t (&Sb)[8][2], int64_t len, int g8,
-                                           float (&o)[4]) {
-    // W^T = (K^start)^T S^T: two accumulators halve the dependent chain.
-    float w0[4] = {0.f, 0.f, 0.f, 0.f}, w1[4] = {0.f, 0.f, 0.f, 0.f};
+                                           const uint32_t (&Sb)[8][2], float (&o)[4]) {
+    // (A^kk B) V^T does not depend on the state: it seeds the accumulator.
+    float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
+    mma_bf16(u0, f.akb, f.vb, u0);
+    // U^T += K' S^T over the 128 keys, in two accumulators.
 #pragma unroll
     for (int kk = 0; kk < 8; kk += 2) {
-        mma_bf16(w0, f.ks[kk], Sb[kk], w0);
-        mma_bf16(w1, f.ks[kk + 1], Sb[kk + 1], w1);
+        mma_bf16(u0, f.ks[kk], Sb[kk], u0);
+        mma_bf16(u1, f.ks[kk + 1], Sb[kk + 1], u1);
     }
     // D S^T, in place (the BF16 copy of the old state is already in Sb).
 #pragma unroll
@@ -129,29 +138,19 @@ __device__ __forceinline__ void chunk_step(const ChunkFrags& f, float (&Sf)[8][4
         Sf[mt][2] *= d1;
         Sf[mt][3] *= d1;
     }
-    // Delta^T = V^T - W^T; tokens past the end of the sequence read as zero.
-    const float m0 = g8 < len ? 1.f : 0.f, m1 = g8 + 8 < len ? 1.f : 0.f;
-    uint32_t Db[2];
-    Db[0] = movm_t(pack_bf16(m0 * bf16_lo(f.v[0]) - (w0[0] + w1[0]),
-                             m0 * bf16_hi(f.v[0]) - (w0[1] + w1[1])));
-    Db[1] = movm_t(pack_bf16(m1 * bf16_lo(f.v[1]) - (w0[2] + w1[2]),
-                             m1 * bf16_hi(f.v[1]) - (w0[3] + w1[3])));
-    // U^T = (A^kk B) Delta^T.
-    float u[4] = {0.f, 0.f, 0.f, 0.f};
-    mma_bf16(u, f.akb, Db, u);
-    // P^T = s (Q^start)^T S^T, off the state chain: fills the U latency.
+    uint32_t Ub[2];
+    Ub[0] = movm_t(pack_bf16(u0[0] + u1[0], u0[1] + u1[1]));
+    Ub[1] = movm_t(pack_bf16(u0[2] + u1[2], u0[3] + u1[3]));
+    // S^T <- D S^T + (K^end)^T U^T.
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) mma_bf16(Sf[mt], f.ke[mt], Ub, Sf[mt]);
+    // P^T = s (Q^start)^T S^T, off the state chain.
     float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int kk = 0; kk < 8; kk += 2) {
         mma_bf16(p0, f.qs[kk], Sb[kk], p0);
         mma_bf16(p1, f.qs[kk + 1], Sb[kk + 1], p1);
     }
-    uint32_t Ub[2];
-    Ub[0] = movm_t(pack_bf16(u[0], u[1]));
-    Ub[1] = movm_t(pack_bf16(u[2], u[3]));
-    // S^T <- D S^T + (K^end)^T U^T.
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt) mma_bf16(Sf[mt], f.ke[mt], Ub, Sf[mt]);
     // O^T = P^T + A^qk U^T.
     float pin[4] = {p0[0] + p1[0], p0[1] + p1[1], p0[2] + p1[2], p0[3] + p1[3]};
     mma_bf16(o, f.aqk, Ub, pin);
@@ -282,7 +281,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         if (len > kChunk) len = kChunk;
 
         float o[4];
-        chunk_step(f, Sf, Sb, len, g8, o);
+        chunk_step(f, Sf, Sb, o);
 
         // BF16 operand copy of the new state: first, since the next chunk's
         // chain starts from it (warps issue in order).

@@ -54,7 +54,7 @@ def unpack_packets(packets):
     c = np.arange(128)
     d = dp[..., 16 * (c & 7) + 2 * (c >> 4) + ((c >> 3) & 1)]   # undo the permutation
     return {
-        "Kst": _bf16_at(p, OFF_KS, i128),          # [..., 16 tokens, 128 keys]
+        "Kprime": _bf16_at(p, OFF_KS, i128),       # -(A^kk B) K^start^T [..., 16 tokens, 128 keys]
         "Qst_s": _bf16_at(p, OFF_QS, i128),        # s * Q^start rows
         "KendT": _bf16_at(p, OFF_KE, iKE),         # [..., 128 keys, 16 tokens]
         "AkkB": _bf16_at(p, OFF_AKB, i32),         # A^kk with column j scaled by beta_j

@@ -55,8 +55,7 @@ def _check_prep(kda, inp):
     beta = inp["beta"].double().numpy()
     # Elementwise BF16 quantities: relative error of one BF16 rounding (2^-9)
     # plus FP32 arithmetic and the fast exponential.
-    for key, ref in (("Kst", im["Kst"]), ("Qst_s", s * im["Qst"]),
-                     ("KendT", np.swapaxes(im["Kend"], -1, -2))):
+    for key, ref in (("Qst_s", s * im["Qst"]), ("KendT", np.swapaxes(im["Kend"], -1, -2))):
         got = P[key][:nch]
         err = np.abs(got - ref)
         assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-30), key
@@ -88,6 +87,12 @@ def _check_prep(kda, inp):
         for h in range(ref.shape[1]):
             den = np.linalg.norm(ref[ch, h])
             assert np.linalg.norm(P["AkkB"][ch, h] - ref[ch, h]) <= 1e-2 * den + 1e-6
+    # K' = -(A^kk B) K^start^T: a sum of signed terms, so compared per tile.
+    kp_ref = -np.einsum("chij,chjk->chik", ref, im["Kst"])
+    for ch in range(nch):
+        for h in range(ref.shape[1]):
+            den = np.linalg.norm(kp_ref[ch, h])
+            assert np.linalg.norm(P["Kprime"][ch, h] - kp_ref[ch, h]) <= 4e-3 * den + 1e-6
 
 
 def test_prep_fixed_with_tail(kda):
