@@ -292,6 +292,8 @@ def run_ours(args):
     kda._lib.load()   # fails loudly when the library is not built
     if args.split:
         kda.set_split(args.split)
+    if args.engine:
+        kda.set_engine(args.engine)
     stream = torch.cuda.Stream(device=device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
@@ -352,7 +354,8 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": inp["workload"].name, "l2": "flushed (512 MiB write) before every step",
-                   "recurrence_split": nsplit, "head_tokens_per_step": ht},
+                   "recurrence_split": nsplit, "recurrence_engine": args.engine,
+                   "head_tokens_per_step": ht},
         "gpu_launches": (3 if inp["cu_seqlens"] is not None else 2) * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "us_per_call": 1e3 * total_e2e / args.steps},
@@ -401,6 +404,8 @@ def main():
     ap.add_argument("--reference-tokens", type=int, default=1024)
     ap.add_argument("--split", type=int, default=0,
                     help="CTAs per (sequence, head) in the recurrence (0 = automatic)")
+    ap.add_argument("--engine", type=int, default=0,
+                    help="recurrence engine: 0 automatic, 1 column-split warp MMA, 2 tcgen05")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

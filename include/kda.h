@@ -101,6 +101,16 @@ int kda_device_status(void* stream, int* status);
  */
 int kda_set_split(int nsplit);
 
+/*
+ * Recurrence engine.  0 (default) and 1: the column-split kernel (warp-level
+ * m16n8k16 MMAs, state in registers, `nsplit` CTAs per head).  2: the tcgen05
+ * kernel (one CTA per (sequence, head); the value rows are the MMA's M = 128,
+ * operands are read by the tensor cores straight from shared memory,
+ * accumulators live in tensor memory; the split setting is ignored).
+ * Process-wide; returns KDA_ERR_ARG for other values.
+ */
+int kda_set_engine(int engine);
+
 /* The split the automatic rule picks on the current device for N*H units (HOST out). */
 int kda_auto_split(int64_t n_seqs, int64_t H, int* nsplit);
 

@@ -47,6 +47,8 @@ def load():
         lib.kda_device_status.restype = I
         lib.kda_set_split.argtypes = [I]
         lib.kda_set_split.restype = I
+        lib.kda_set_engine.argtypes = [I]
+        lib.kda_set_engine.restype = I
         lib.kda_auto_split.argtypes = [I64, I64, ctypes.POINTER(I)]
         lib.kda_auto_split.restype = I
         lib.kda_workspace_bytes.argtypes = [I64, I64, I64, I, ctypes.POINTER(I64)]
@@ -95,6 +97,11 @@ def device_status(stream=0) -> int:
 
 def set_split(nsplit: int):
     _check(load().kda_set_split(int(nsplit)), "kda_set_split")
+
+
+def set_engine(engine: int):
+    """0 automatic, 1 column-split warp-MMA kernel, 2 tcgen05 kernel."""
+    _check(load().kda_set_engine(int(engine)), "kda_set_engine")
 
 
 def auto_split(n_seqs: int, H: int) -> int:

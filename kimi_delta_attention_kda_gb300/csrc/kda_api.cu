@@ -29,6 +29,7 @@ struct DeviceState {
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_split_override = 0;
+int g_engine = 0;
 
 // Optional per-kernel timing: when active, each kda_prefill call records three
 // events on its stream (before the preparation kernels, between preparation
@@ -173,6 +174,8 @@ int run_prep(const Plan& pl, const void* q, const void* k, const float* g, const
 }
 
 }  // namespace
+
+int recurrence_engine() { return g_engine; }
 
 // Read-only view of the per-device state for other entry points in this
 // library: the device status word and the recurrence split kda_prefill uses.
@@ -320,6 +323,12 @@ extern "C" int kda_set_split(int nsplit) {
     if (nsplit != 0 && nsplit != 1 && nsplit != 2 && nsplit != 4 && nsplit != 8 && nsplit != 16)
         return KDA_ERR_ARG;
     g_split_override = nsplit;
+    return KDA_OK;
+}
+
+extern "C" int kda_set_engine(int engine) {
+    if (engine < 0 || engine > 2) return KDA_ERR_ARG;
+    g_engine = engine;
     return KDA_OK;
 }
 

@@ -155,6 +155,12 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
     }
     return true;
 }
+// Warp-uniform bounded wait: every lane of the warp gets the same answer, so a
+// timeout can never leave a warp diverged before a warp-collective instruction.
+__device__ __forceinline__ bool mbar_wait_warp(uint64_t* bar, uint32_t parity, int* status) {
+    const bool ok = mbar_wait_bounded(bar, parity, status);
+    return __all_sync(0xffffffffu, ok);
+}
 // The same bound, for waits that are expected to be long (a producer waiting
 // for a consumer to free a stage): sleeps inside try_wait between checks.
 __device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, uint32_t parity,
@@ -168,6 +174,11 @@ __device__ __forceinline__ bool mbar_wait_bounded_sleep(uint64_t* bar, uint32_t 
         }
     }
     return true;
+}
+
+__device__ __forceinline__ bool mbar_wait_warp_sleep(uint64_t* bar, uint32_t parity, int* status) {
+    const bool ok = mbar_wait_bounded_sleep(bar, parity, status);
+    return __all_sync(0xffffffffu, ok);
 }
 
 // One-dimensional bulk copy global -> shared, completing on an mbarrier.

@@ -2,6 +2,7 @@
 // and the kernel translation units.  Internal; not part of the public header.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -36,6 +37,18 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
                               void* final_state, const uint8_t* packets,
                               const SeqGeometry& geo, int64_t H, int nsplit, int* status,
                               cudaStream_t stream);
+
+// The tcgen05 recurrence: one CTA per (sequence, head).
+cudaError_t launch_recurrence_tc(const void* v, void* out, const void* init_state,
+                                 void* final_state, const uint8_t* packets, const SeqGeometry& geo,
+                                 int64_t H, int* status, cudaStream_t stream);
+
+// Tensor map of v viewed as a 2-D BF16 array [tokens][H * 128], boxes of
+// 16 tokens x `cols` value columns.
+cudaError_t encode_v_map(CUtensorMap* map, const void* v, int64_t tokens, int64_t H, int cols);
+
+// Recurrence engine: 0 automatic, 1 column-split warp MMA, 2 tcgen05.
+int recurrence_engine();
 
 // Per-device status word and the split kda_prefill picks for `units`
 // (sequence x head) recurrences, for entry points outside kda_api.cu.

@@ -408,7 +408,7 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 1)
             tma_load_2d(region + kInG, &maps.g, x, y, bar);
         }
         const float beta_f = lane < len ? __bfloat162float(a.beta[(t0 + lane) * a.H + h]) : 0.f;
-        if (!mbar_wait_bounded_sleep(bar, phase, a.geo.status)) {
+        if (!mbar_wait_warp_sleep(bar, phase, a.geo.status)) {
             // The loads may still land: wait for them (bounded) before leaving.
             mbar_wait_bounded_sleep(bar, phase, a.geo.status);
             break;

@@ -207,7 +207,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         for (int64_t c = 0; c < nch && ok; ++c) {
             const int s = static_cast<int>(c % kStages);
             if (c >= kStages)
-                ok = mbar_wait_bounded_sleep(&empty[s], ((c / kStages) - 1) & 1, a.status);
+                ok = mbar_wait_warp_sleep(&empty[s], ((c / kStages) - 1) & 1, a.status);
             if (!ok) break;
             uint8_t* stage = smem + s * L::kStageBytes;
             if (lane == 0) {
@@ -264,14 +264,14 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     bool ok = true;
     ChunkFrags f;
     if (L::kPrefetch && nch > 0) {
-        ok = mbar_wait_bounded(&full[0], 0, a.status);
+        ok = mbar_wait_warp(&full[0], 0, a.status);
         if (ok) load_frags(smem, L::kVRowBytes, warp, lane, f);
     }
     for (int64_t c = 0; c < nch && ok; ++c) {
         const int s = static_cast<int>(c % kStages);
         const uint8_t* stage = smem + s * L::kStageBytes;
         if (!L::kPrefetch) {
-            if (!mbar_wait_bounded(&full[s], (c / kStages) & 1, a.status)) {
+            if (!mbar_wait_warp(&full[s], (c / kStages) & 1, a.status)) {
                 ok = false;
                 break;
             }
@@ -296,7 +296,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         // Next chunk's fragments, in flight while this chunk finishes.
         if (L::kPrefetch && c + 1 < nch) {
             const int s1 = static_cast<int>((c + 1) % kStages);
-            if (mbar_wait_bounded(&full[s1], ((c + 1) / kStages) & 1, a.status))
+            if (mbar_wait_warp(&full[s1], ((c + 1) / kStages) & 1, a.status))
                 load_frags(smem + s1 * L::kStageBytes, L::kVRowBytes, warp, lane, f);
             else
                 ok = false;
@@ -322,7 +322,32 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     }
 }
 
-PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+template <int NW>
+cudaError_t launch_nw(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
+    using L = RecLayout<NW>;
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(recurrence_kernel<NW>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(L::kSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    CUtensorMap vmap;
+    alignas(64) static const char kZero[16] = {};
+    // With no tokens nothing is loaded; still hand the kernel a well-formed map.
+    const void* vbase = a.v ? static_cast<const void*>(a.v) : static_cast<const void*>(kZero);
+    cudaError_t e = encode_v_map(&vmap, vbase, a.geo.tokens, a.H, L::kCols);
+    if (e != cudaSuccess) return e;
+    recurrence_kernel<NW><<<static_cast<unsigned>(blocks), (NW + 1) * 32, L::kSmemBytes, stream>>>(a, vmap);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+static PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
     static std::once_flag once;
     static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
     std::call_once(once, [] {
@@ -354,31 +379,6 @@ cudaError_t encode_v_map(CUtensorMap* map, const void* v, int64_t tokens, int64_
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
-template <int NW>
-cudaError_t launch_nw(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
-    using L = RecLayout<NW>;
-    static bool configured[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(recurrence_kernel<NW>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(L::kSmemBytes));
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
-    CUtensorMap vmap;
-    alignas(64) static const char kZero[16] = {};
-    // With no tokens nothing is loaded; still hand the kernel a well-formed map.
-    const void* vbase = a.v ? static_cast<const void*>(a.v) : static_cast<const void*>(kZero);
-    cudaError_t e = encode_v_map(&vmap, vbase, a.geo.tokens, a.H, L::kCols);
-    if (e != cudaSuccess) return e;
-    recurrence_kernel<NW><<<static_cast<unsigned>(blocks), (NW + 1) * 32, L::kSmemBytes, stream>>>(a, vmap);
-    return cudaGetLastError();
-}
-
-}  // namespace
-
 cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
                               void* final_state, const uint8_t* packets,
                               const SeqGeometry& geo, int64_t H, int nsplit, int* status,
@@ -393,6 +393,10 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
     a.H = H;
     a.nsplit = nsplit;
     a.status = status;
+    // Engine 2 (opt-in): the tcgen05 kernel, one CTA per head.  Otherwise the
+    // column-split kernel with `nsplit` CTAs per head.
+    if (recurrence_engine() == 2)
+        return launch_recurrence_tc(v, out, init_state, final_state, packets, geo, H, status, stream);
     const int64_t blocks = geo.n_seqs * H * nsplit;
     if (blocks <= 0) return cudaSuccess;
     if (geo.tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // TMA coordinates are int32

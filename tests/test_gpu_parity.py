@@ -272,3 +272,57 @@ def test_full_workload(kda, name):
     out, fin = run(kda, inp)
     assert torch.isfinite(out.float()).all() and torch.isfinite(fin.float()).all()
     tu.check_against_oracle(inp, out, fin, heads=FULL[name])
+
+
+# ----------------------------------------------------------------------------
+# The tcgen05 recurrence engine, forced
+# ----------------------------------------------------------------------------
+
+@pytest.fixture
+def tc_engine(kda):
+    kda.set_engine(2)
+    yield kda
+    kda.set_engine(0)
+
+
+@pytest.mark.parametrize("B,T,H,init", SMALL)
+def test_tcgen05_small_fixed(tc_engine, B, T, H, init):
+    inp = synthetic.make_inputs(B, T, H, 2000 + T, init_std=0.02 if init else None)
+    out, fin = run(tc_engine, inp)
+    tu.check_against_oracle(inp, out, fin)
+
+
+def test_tcgen05_small_packed(tc_engine):
+    inp = synthetic.make_inputs(0, 0, 3, 56, init_std=0.02, lengths=[5, 0, 33, 16, 1, 64, 200])
+    out, fin = run(tc_engine, inp)
+    tu.check_against_oracle(inp, out, fin)
+
+
+def test_tcgen05_zero_tokens_and_in_place(tc_engine):
+    inp = synthetic.make_inputs(2, 0, 2, 3, init_std=0.02)
+    d = tu.to_device(inp)
+    out, fin = tc_engine.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"])
+    torch.cuda.synchronize()
+    assert torch.equal(fin.cpu(), inp["init_state"])
+    inp = synthetic.make_inputs(1, 64, 2, 12, init_std=0.02)
+    ref_out, ref_fin = run(tc_engine, inp)
+    d = tu.to_device(inp)
+    state = d["init_state"].clone()
+    out, _ = tc_engine.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], state,
+                                   final_state=state)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), ref_out) and torch.equal(state.cpu(), ref_fin)
+
+
+def test_tcgen05_deterministic(tc_engine):
+    inp = synthetic.make_inputs(2, 130, 3, 5, init_std=0.02)
+    a = run(tc_engine, inp)
+    b = run(tc_engine, inp)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+@pytest.mark.parametrize("name", ["t8192_h6", "t65536_h1", "varlen8_h12"])
+def test_tcgen05_full_workload(tc_engine, name):
+    inp = synthetic.make_workload(name)
+    out, fin = run(tc_engine, inp)
+    tu.check_against_oracle(inp, out, fin, heads=[0, 5, 11] if name == "varlen8_h12" else None)
