@@ -103,7 +103,9 @@ int kda_set_split(int nsplit);
 
 /*
  * Recurrence engine.  0 (default) and 1: the column-split kernel (warp-level
- * m16n8k16 MMAs, state in registers, `nsplit` CTAs per head).  2: the tcgen05
+ * m16n8k16 MMAs, state in registers, `nsplit` CTAs per head); with nsplit 1,
+ * engine 0 gives each warp 16 value columns (8 warps) and engine 1 gives each
+ * warp 8 columns (16 warps).  2: the tcgen05
  * kernel (one CTA per (sequence, head); the value rows are the MMA's M = 128,
  * operands are read by the tensor cores straight from shared memory,
  * accumulators live in tensor memory; the split setting is ignored).

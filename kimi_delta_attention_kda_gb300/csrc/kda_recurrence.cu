@@ -322,6 +322,265 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     }
 }
 
+// ---------------------------------------------------------------------------
+// Wide variant for one CTA per head: 8 consumer warps of 16 value columns
+// each.  A warp's two 8-column n-tiles share every A-operand fragment, so the
+// CTA reads each chunk's K', Q^start and K^end fragments from shared memory 8
+// times instead of 16 (with 16 narrow warps the shared-memory pipe, not the
+// tensor pipe, limits a chunk step).  Fragments are loaded just before use.
+// ---------------------------------------------------------------------------
+constexpr int kWideWarps = 8;
+constexpr int kWideStages = 4;
+constexpr uint32_t kWideVRowBytes = kHeadDim * 2;
+constexpr uint32_t kWideStageBytes = ((kPacketBytes + kChunk * kWideVRowBytes + 1023) / 1024) * 1024;
+constexpr uint32_t kWideBarOff = kWideStages * kWideStageBytes;
+constexpr uint32_t kWideSmemBytes = kWideBarOff + 2 * kWideStages * 8 + 1024;
+
+__global__ void __launch_bounds__((kWideWarps + 1) * 32)
+    recurrence_wide_kernel(RecArgs a, const __grid_constant__ CUtensorMap vmap) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWideBarOff);
+    uint64_t* empty = full + kWideStages;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t n = blockIdx.x / a.H;
+    const int64_t h = blockIdx.x - n * a.H;
+
+    int64_t c_begin, nch, tok0, seqlen;
+    if (a.geo.cu_chunks) {
+        if (!*a.geo.valid) return;
+        c_begin = a.geo.cu_chunks[n];
+        nch = a.geo.cu_chunks[n + 1] - c_begin;
+        tok0 = a.geo.cu_seqlens[n];
+        seqlen = a.geo.cu_seqlens[n + 1] - tok0;
+    } else {
+        c_begin = n * a.geo.chunks_per_seq;
+        nch = a.geo.chunks_per_seq;
+        tok0 = n * a.geo.tokens_per_seq;
+        seqlen = a.geo.tokens_per_seq;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kWideStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWideWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kWideWarps) {
+        // ------------------------------------------------------------ producer
+        uint32_t fill_parity = 0, filled = 0;
+        bool ok = true;
+        for (int64_t c = 0; c < nch && ok; ++c) {
+            const int s = static_cast<int>(c % kWideStages);
+            if (c >= kWideStages)
+                ok = mbar_wait_warp_sleep(&empty[s], ((c / kWideStages) - 1) & 1, a.status);
+            if (!ok) break;
+            uint8_t* stage = smem + s * kWideStageBytes;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * kWideVRowBytes);
+                bulk_g2s(stage, a.packets + ((c_begin + c) * a.H + h) * static_cast<int64_t>(kPacketBytes),
+                         kPacketBytes, &full[s]);
+                tma_load_2d(stage + kPacketBytes, &vmap, static_cast<int32_t>(h * kHeadDim),
+                            static_cast<int32_t>(tok0 + kChunk * c), &full[s]);
+            }
+            __syncwarp();
+            fill_parity ^= (filled >> s & 1u) << s;
+            filled |= 1u << s;
+        }
+        if (!ok)
+            for (int s = 0; s < kWideStages; ++s)
+                if (filled >> s & 1u) mbar_wait_bounded(&full[s], (fill_parity >> s) & 1u, a.status);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int vcol = 16 * warp;   // first of this warp's 16 value columns
+    const int64_t state_base = (n * a.H + h) * kHeadDim * kHeadDim;
+    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t hiA = lane >> 4;
+
+    float Sf[8][2][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            if (a.init_state) {
+                const __nv_bfloat16* src = a.init_state + state_base;
+                const int key = 16 * mt + g8;
+                const int val = vcol + 8 * nt + 2 * t4;
+                Sf[mt][nt][0] = __bfloat162float(src[(int64_t)val * kHeadDim + key]);
+                Sf[mt][nt][1] = __bfloat162float(src[(int64_t)(val + 1) * kHeadDim + key]);
+                Sf[mt][nt][2] = __bfloat162float(src[(int64_t)val * kHeadDim + key + 8]);
+                Sf[mt][nt][3] = __bfloat162float(src[(int64_t)(val + 1) * kHeadDim + key + 8]);
+            } else {
+                Sf[mt][nt][0] = Sf[mt][nt][1] = Sf[mt][nt][2] = Sf[mt][nt][3] = 0.f;
+            }
+        }
+    uint32_t Sb[8][2][2];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            Sb[mt][nt][0] = movm_t(pack_bf16(Sf[mt][nt][0], Sf[mt][nt][1]));
+            Sb[mt][nt][1] = movm_t(pack_bf16(Sf[mt][nt][2], Sf[mt][nt][3]));
+        }
+
+    bool ok = true;
+    for (int64_t c = 0; c < nch; ++c) {
+        const int s = static_cast<int>(c % kWideStages);
+        if (!mbar_wait_warp(&full[s], (c / kWideStages) & 1, a.status)) {
+            ok = false;
+            break;
+        }
+        const uint8_t* stage = smem + s * kWideStageBytes;
+        const uint32_t sKS = smem_u32(stage + kOffKS);
+        const uint32_t sQS = smem_u32(stage + kOffQS);
+        const uint32_t sKE = smem_u32(stage + kOffKE);
+        int64_t len = seqlen - kChunk * c;
+        if (len > kChunk) len = kChunk;
+
+        // U^T = (A^kk B) V^T + K' S^T for both n-tiles.
+        uint32_t akb[4], vb[4];
+        ldsm_x4(akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
+        {
+            // lanes 0-7 / 8-15: tokens 0-7 / 8-15 of columns vcol..+7; lanes
+            // 16-31: the same for columns vcol+8..+15.
+            const uint8_t* sV = stage + kPacketBytes + (lane & 15) * kWideVRowBytes + (vcol + 8 * (lane >> 4)) * 2;
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(vb[0]), "=r"(vb[1]), "=r"(vb[2]), "=r"(vb[3])
+                         : "r"(smem_u32(sV)));
+        }
+        float u[2][2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) u[0][nt][j] = u[1][nt][j] = 0.f;
+        mma_bf16(u[0][0], akb, vb, u[0][0]);
+        mma_bf16(u[0][1], akb, vb + 2, u[0][1]);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t af[4];
+            ldsm_x4(af, sKS + sw128_off(16, rowA, 2 * kk + hiA));
+            mma_bf16(u[kk & 1][0], af, Sb[kk][0], u[kk & 1][0]);
+            mma_bf16(u[kk & 1][1], af, Sb[kk][1], u[kk & 1][1]);
+        }
+        // D S^T in place.
+        {
+            const float4* dp = reinterpret_cast<const float4*>(stage + kOffD) + 4 * g8;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 d = dp[j];
+#pragma unroll
+                for (int nt = 0; nt < 2; ++nt) {
+                    Sf[2 * j][nt][0] *= d.x;
+                    Sf[2 * j][nt][1] *= d.x;
+                    Sf[2 * j][nt][2] *= d.y;
+                    Sf[2 * j][nt][3] *= d.y;
+                    Sf[2 * j + 1][nt][0] *= d.z;
+                    Sf[2 * j + 1][nt][1] *= d.z;
+                    Sf[2 * j + 1][nt][2] *= d.w;
+                    Sf[2 * j + 1][nt][3] *= d.w;
+                }
+            }
+        }
+        uint32_t Ub[2][2];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            Ub[nt][0] = movm_t(pack_bf16(u[0][nt][0] + u[1][nt][0], u[0][nt][1] + u[1][nt][1]));
+            Ub[nt][1] = movm_t(pack_bf16(u[0][nt][2] + u[1][nt][2], u[0][nt][3] + u[1][nt][3]));
+        }
+        // S^T <- D S^T + (K^end)^T U^T.
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            uint32_t af[4];
+            ldsm_x4(af, sKE + sw32_off(16 * mt + rowA, hiA));
+            mma_bf16(Sf[mt][0], af, Ub[0], Sf[mt][0]);
+            mma_bf16(Sf[mt][1], af, Ub[1], Sf[mt][1]);
+        }
+        // P^T = s (Q^start)^T S^T from the incoming state, then O^T.
+        float pa[2][4], pb[2][4];
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+            for (int j = 0; j < 4; ++j) pa[nt][j] = pb[nt][j] = 0.f;
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t af[4];
+            ldsm_x4(af, sQS + sw128_off(16, rowA, 2 * kk + hiA));
+            float (*acc)[4] = (kk & 1) ? pb : pa;
+            mma_bf16(acc[0], af, Sb[kk][0], acc[0]);
+            mma_bf16(acc[1], af, Sb[kk][1], acc[1]);
+        }
+        float o[2][4];
+        {
+            uint32_t aq[4];
+            ldsm_x4(aq, smem_u32(stage + kOffAQK + sw32_off(rowA, hiA)));
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                float pin[4] = {pa[nt][0] + pb[nt][0], pa[nt][1] + pb[nt][1], pa[nt][2] + pb[nt][2],
+                                pa[nt][3] + pb[nt][3]};
+                mma_bf16(o[nt], aq, Ub[nt], pin);
+            }
+        }
+        __syncwarp();
+        mbar_arrive_if(&empty[s], lane == 0);
+        // BF16 operand copy of the new state.
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                Sb[mt][nt][0] = movm_t(pack_bf16(Sf[mt][nt][0], Sf[mt][nt][1]));
+                Sb[mt][nt][1] = movm_t(pack_bf16(Sf[mt][nt][2], Sf[mt][nt][3]));
+            }
+        __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + g8) * a.H + h) * kHeadDim + vcol + 2 * t4;
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            st_global_u32_if(orow + 8 * nt, pack_bf16(o[nt][0], o[nt][1]), g8 < len);
+            st_global_u32_if(orow + 8 * a.H * kHeadDim + 8 * nt, pack_bf16(o[nt][2], o[nt][3]), g8 + 8 < len);
+        }
+    }
+
+    if (ok && a.final_state) {
+        __nv_bfloat16* dst = a.final_state + state_base;
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+            for (int nt = 0; nt < 2; ++nt) {
+                const int key = 16 * mt + g8;
+                const int val = vcol + 8 * nt + 2 * t4;
+                dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][nt][0]);
+                dst[(int64_t)(val + 1) * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][nt][1]);
+                dst[(int64_t)val * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][nt][2]);
+                dst[(int64_t)(val + 1) * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][nt][3]);
+            }
+    }
+}
+
+cudaError_t launch_wide(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(recurrence_wide_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kWideSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    CUtensorMap vmap;
+    alignas(64) static const char kZero[16] = {};
+    const void* vbase = a.v ? static_cast<const void*>(a.v) : static_cast<const void*>(kZero);
+    cudaError_t e = encode_v_map(&vmap, vbase, a.geo.tokens, a.H, kHeadDim);
+    if (e != cudaSuccess) return e;
+    recurrence_wide_kernel<<<static_cast<unsigned>(blocks), (kWideWarps + 1) * 32, kWideSmemBytes, stream>>>(a, vmap);
+    return cudaGetLastError();
+}
+
 template <int NW>
 cudaError_t launch_nw(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
     using L = RecLayout<NW>;
@@ -402,7 +661,10 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
     if (geo.tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // TMA coordinates are int32
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     switch (nsplit) {
-        case 1: return launch_nw<16>(a, blocks, stream);
+        case 1:
+            // Engine 1 keeps 16 warps of 8 columns (for comparison).
+            return recurrence_engine() == 1 ? launch_nw<16>(a, blocks, stream)
+                                            : launch_wide(a, blocks, stream);
         case 2: return launch_nw<8>(a, blocks, stream);
         case 4: return launch_nw<4>(a, blocks, stream);
         case 8: return launch_nw<2>(a, blocks, stream);

@@ -162,15 +162,20 @@ def test_correlated_keys_end_to_end(kda):
 
 
 def test_split_factors_bitwise_identical(kda):
-    """Each value column runs the same arithmetic whichever CTA owns it, so every
-    split of the state over CTAs gives the same bits."""
+    """Each value column runs the same arithmetic whichever CTA or warp owns it,
+    so every split of the state over CTAs, and both warp widths of the
+    one-CTA-per-head kernel (16 or 8 value columns per warp), give the same bits."""
     inp = synthetic.make_inputs(1, 200, 2, 77, init_std=0.02)
     outs = []
     try:
         for ns in (1, 2, 4, 8, 16):
             kda.set_split(ns)
             outs.append(run(kda, inp))
+        kda.set_split(1)
+        kda.set_engine(1)
+        outs.append(run(kda, inp))
     finally:
+        kda.set_engine(0)
         kda.set_split(0)
     for o, f in outs[1:]:
         assert torch.equal(o, outs[0][0]) and torch.equal(f, outs[0][1])
