@@ -95,17 +95,19 @@ int kda_device_status(void* stream, int* status);
  * Number of CTAs that share one (sequence, head) in the recurrence: each owns
  * 128 / nsplit value columns (value columns are independent recurrences,
  * "FlashKDA column split" section 3.1).  nsplit is one of 1, 2, 4, 8, 16, or 0
- * for the automatic choice (the largest split up to 8 whose grid fits the SM
- * count).
+ * for the automatic choice (the largest split whose grid fits the SM count).
  * Process-wide setting; returns KDA_ERR_ARG for other values.
  */
 int kda_set_split(int nsplit);
 
 /*
  * Recurrence engine.  0 (default) and 1: the column-split kernel (warp-level
- * m16n8k16 MMAs, state in registers, `nsplit` CTAs per head); with nsplit 1,
- * engine 0 gives each warp 16 value columns (8 warps) and engine 1 gives each
- * warp 8 columns (16 warps).  2: the tcgen05
+ * m16n8k16 MMAs, state in registers, `nsplit` CTAs per head).  Engine 0 gives
+ * each warp 16 value columns at nsplit 1, 8 columns at nsplit 2, and at nsplit
+ * 4, 8 and 16 splits each 8-column group's 128 keys over a pair of warps
+ * (their partial sums over keys are added in a fixed order, so results agree
+ * with the other variants to rounding, not bit for bit).  Engine 1 gives each
+ * warp 8 columns and all 128 keys at every split.  2: the tcgen05
  * kernel (one CTA per (sequence, head); the value rows are the MMA's M = 128,
  * operands are read by the tensor cores straight from shared memory,
  * accumulators live in tensor memory; the split setting is ignored).

@@ -105,10 +105,10 @@ bool overlap(Range a, Range b) {
 
 int choose_split(int64_t units, int sms) {
     if (g_split_override) return g_split_override;
-    // Two consumer warps per CTA (split 8) share a producer and halve the
-    // packet traffic of split 16 and measure faster, so 8 is the widest split
-    // the automatic rule takes.
-    const int options[] = {8, 4, 2};
+    // The widest split whose grid still fits on the SMs: with few heads the
+    // recurrence is a per-warp latency chain, and more CTAs per head give each
+    // warp fewer value columns and keys.
+    const int options[] = {16, 8, 4, 2};
     for (int ns : options)
         if (units * ns <= sms) return ns;
     return 1;

@@ -100,6 +100,41 @@ __device__ __forceinline__ void load_frags(const uint8_t* stage, uint32_t vrow_b
     ldsm_x4(f.aqk, smem_u32(stage + kOffAQK + sw32_off(rowA, hiA)));
 }
 
+// The same loads in three groups, in the order a chunk step needs them: the
+// error-term operands, K^end, then the output operands and D.
+__device__ __forceinline__ void load_frags_u(const uint8_t* stage, uint32_t vrow_bytes, int warp,
+                                             int lane, ChunkFrags& f) {
+    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t hiA = lane >> 4;
+    const uint32_t sKS = smem_u32(stage + kOffKS);
+    ldsm_x4(f.akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
+    const uint8_t* sV = stage + kPacketBytes + (lane & 15) * vrow_bytes + 16 * warp;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(f.vb[0]), "=r"(f.vb[1])
+                 : "r"(smem_u32(sV)));
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) ldsm_x4(f.ks[kk], sKS + sw128_off(16, rowA, 2 * kk + hiA));
+}
+__device__ __forceinline__ void load_frags_ke(const uint8_t* stage, int lane, ChunkFrags& f) {
+    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t hiA = lane >> 4;
+    const uint32_t sKE = smem_u32(stage + kOffKE);
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) ldsm_x4(f.ke[mt], sKE + sw32_off(16 * mt + rowA, hiA));
+}
+__device__ __forceinline__ void load_frags_o(const uint8_t* stage, int lane, ChunkFrags& f) {
+    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t hiA = lane >> 4;
+    const int g8 = lane >> 2;
+    const uint32_t sQS = smem_u32(stage + kOffQS);
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) ldsm_x4(f.qs[kk], sQS + sw128_off(16, rowA, 2 * kk + hiA));
+    ldsm_x4(f.aqk, smem_u32(stage + kOffAQK + sw32_off(rowA, hiA)));
+    const float4* dp = reinterpret_cast<const float4*>(stage + kOffD) + 4 * g8;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) f.d[j] = dp[j];
+}
+
 __device__ __forceinline__ void st_global_u32_if(void* p, uint32_t v, bool pred) {
     asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p st.global.b32 [%0], %1;\n}\n"
                  ::"l"(p), "r"(v), "r"(static_cast<uint32_t>(pred))
@@ -263,49 +298,109 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 
     bool ok = true;
     ChunkFrags f;
-    if (L::kPrefetch && nch > 0) {
-        ok = mbar_wait_warp(&full[0], 0, a.status);
-        if (ok) load_frags(smem, L::kVRowBytes, warp, lane, f);
-    }
-    for (int64_t c = 0; c < nch && ok; ++c) {
-        const int s = static_cast<int>(c % kStages);
-        const uint8_t* stage = smem + s * L::kStageBytes;
-        if (!L::kPrefetch) {
+    if (L::kPrefetch) {
+        // Rolling prefetch: each group of chunk c+1's fragments is loaded as
+        // soon as chunk c has issued its last use of that group, so the loads
+        // are in flight behind the rest of chunk c.
+        if (nch > 0) {
+            ok = mbar_wait_warp(&full[0], 0, a.status);
+            if (ok) load_frags(smem, L::kVRowBytes, warp, lane, f);
+        }
+        for (int64_t c = 0; c < nch && ok; ++c) {
+            const int s = static_cast<int>(c % kStages);
+            const bool has_next = c + 1 < nch;
+            const int s1 = static_cast<int>((c + 1) % kStages);
+            const uint32_t par1 = static_cast<uint32_t>(((c + 1) / kStages) & 1);
+            const uint8_t* stage1 = smem + s1 * L::kStageBytes;
+            // Probe the next stage now; the answer is needed only after U.
+            bool next_ready = has_next && mbar_try_wait(&full[s1], par1);
+            int64_t len = seqlen - kChunk * c;
+            if (len > kChunk) len = kChunk;
+
+            float u0[4] = {0.f, 0.f, 0.f, 0.f}, u1[4] = {0.f, 0.f, 0.f, 0.f};
+            mma_bf16(u0, f.akb, f.vb, u0);
+#pragma unroll
+            for (int kk = 0; kk < 8; kk += 2) {
+                mma_bf16(u0, f.ks[kk], Sb[kk], u0);
+                mma_bf16(u1, f.ks[kk + 1], Sb[kk + 1], u1);
+            }
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                const float d0 = dsel(f.d[mt >> 1], 2 * (mt & 1));
+                const float d1 = dsel(f.d[mt >> 1], 2 * (mt & 1) + 1);
+                Sf[mt][0] *= d0;
+                Sf[mt][1] *= d0;
+                Sf[mt][2] *= d1;
+                Sf[mt][3] *= d1;
+            }
+            if (has_next) {
+                if (!__all_sync(0xffffffffu, next_ready))
+                    next_ready = mbar_wait_warp(&full[s1], par1, a.status);
+                if (next_ready)
+                    load_frags_u(stage1, L::kVRowBytes, warp, lane, f);
+                else
+                    ok = false;
+            }
+            uint32_t Ub[2];
+            Ub[0] = movm_t(pack_bf16(u0[0] + u1[0], u0[1] + u1[1]));
+            Ub[1] = movm_t(pack_bf16(u0[2] + u1[2], u0[3] + u1[3]));
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) mma_bf16(Sf[mt], f.ke[mt], Ub, Sf[mt]);
+            if (has_next && ok) load_frags_ke(stage1, lane, f);
+            float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+            for (int kk = 0; kk < 8; kk += 2) {
+                mma_bf16(p0, f.qs[kk], Sb[kk], p0);
+                mma_bf16(p1, f.qs[kk + 1], Sb[kk + 1], p1);
+            }
+            float o[4];
+            {
+                float pin[4] = {p0[0] + p1[0], p0[1] + p1[1], p0[2] + p1[2], p0[3] + p1[3]};
+                mma_bf16(o, f.aqk, Ub, pin);
+            }
+            if (has_next && ok) load_frags_o(stage1, lane, f);
+#pragma unroll
+            for (int mt = 0; mt < 8; ++mt) {
+                Sb[mt][0] = movm_t(pack_bf16(Sf[mt][0], Sf[mt][1]));
+                Sb[mt][1] = movm_t(pack_bf16(Sf[mt][2], Sf[mt][3]));
+            }
+            __syncwarp();
+            mbar_arrive_if(&empty[s], lane == 0);
+            __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + g8) * a.H + h) * kHeadDim + vcol + 2 * t4;
+            st_global_u32_if(orow, pack_bf16(o[0], o[1]), g8 < len);
+            st_global_u32_if(orow + 8 * a.H * kHeadDim, pack_bf16(o[2], o[3]), g8 + 8 < len);
+        }
+    } else {
+        for (int64_t c = 0; c < nch; ++c) {
+            const int s = static_cast<int>(c % kStages);
+            const uint8_t* stage = smem + s * L::kStageBytes;
             if (!mbar_wait_warp(&full[s], (c / kStages) & 1, a.status)) {
                 ok = false;
                 break;
             }
             load_frags(stage, L::kVRowBytes, warp, lane, f);
-        }
-        int64_t len = seqlen - kChunk * c;
-        if (len > kChunk) len = kChunk;
+            int64_t len = seqlen - kChunk * c;
+            if (len > kChunk) len = kChunk;
 
-        float o[4];
-        chunk_step(f, Sf, Sb, o);
+            float o[4];
+            chunk_step(f, Sf, Sb, o);
 
-        // BF16 operand copy of the new state: first, since the next chunk's
-        // chain starts from it (warps issue in order).
+            // BF16 operand copy of the new state: first, since the next chunk's
+            // chain starts from it (warps issue in order).
 #pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            Sb[mt][0] = movm_t(pack_bf16(Sf[mt][0], Sf[mt][1]));
-            Sb[mt][1] = movm_t(pack_bf16(Sf[mt][2], Sf[mt][3]));
-        }
-        // Every read of this stage is done: hand it back to the producer.
-        __syncwarp();
-        mbar_arrive_if(&empty[s], lane == 0);
-        // Next chunk's fragments, in flight while this chunk finishes.
-        if (L::kPrefetch && c + 1 < nch) {
-            const int s1 = static_cast<int>((c + 1) % kStages);
-            if (mbar_wait_warp(&full[s1], ((c + 1) / kStages) & 1, a.status))
-                load_frags(smem + s1 * L::kStageBytes, L::kVRowBytes, warp, lane, f);
-            else
-                ok = false;
-        }
+            for (int mt = 0; mt < 8; ++mt) {
+                Sb[mt][0] = movm_t(pack_bf16(Sf[mt][0], Sf[mt][1]));
+                Sb[mt][1] = movm_t(pack_bf16(Sf[mt][2], Sf[mt][3]));
+            }
+            // Every read of this stage is done: hand it back to the producer.
+            __syncwarp();
+            mbar_arrive_if(&empty[s], lane == 0);
 
-        // Store O (tokens g8 and g8 + 8, values vcol + 2 t4 .. + 1), predicated.
-        __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + g8) * a.H + h) * kHeadDim + vcol + 2 * t4;
-        st_global_u32_if(orow, pack_bf16(o[0], o[1]), g8 < len);
-        st_global_u32_if(orow + 8 * a.H * kHeadDim, pack_bf16(o[2], o[3]), g8 + 8 < len);
+            // Store O (tokens g8 and g8 + 8, values vcol + 2 t4 .. + 1), predicated.
+            __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + g8) * a.H + h) * kHeadDim + vcol + 2 * t4;
+            st_global_u32_if(orow, pack_bf16(o[0], o[1]), g8 < len);
+            st_global_u32_if(orow + 8 * a.H * kHeadDim, pack_bf16(o[2], o[3]), g8 + 8 < len);
+        }
     }
 
     if (ok && a.final_state) {
@@ -581,6 +676,298 @@ cudaError_t launch_wide(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
     return cudaGetLastError();
 }
 
+// ---------------------------------------------------------------------------
+// Key-split variant for heads that get many CTAs (a latency-bound chain per
+// warp).  Each 8-column group of S^T is held by a pair of warps, one per half
+// of the 128 keys, so a warp issues half the operand loads and MMAs of the
+// keys-major form.  Per chunk each warp forms its partial U^T (and partial
+// P^T) over its 64 keys, the pair swaps partials through shared memory behind
+// an mbarrier (bounded wait), and both add them in the same order (key half
+// 0 + key half 1), so both warps continue from identical U^T.  The sums over
+// keys are associated differently from the other variants, so results agree
+// with them to rounding, not bit for bit.
+// ---------------------------------------------------------------------------
+template <int NCG>
+struct KsLayout {
+    static constexpr int kWarps = 2 * NCG;                        // consumer warps
+    static constexpr int kCols = 8 * NCG;                         // value columns per CTA
+    static constexpr int kStages = 8;
+    static constexpr uint32_t kVRowBytes = kCols * 2;
+    static constexpr uint32_t kStageBytes = ((kPacketBytes + kChunk * kVRowBytes + 1023) / 1024) * 1024;
+    // Exchange buffers: [column group][chunk parity][key half][u, p][lane] float4.
+    static constexpr uint32_t kXOff = kStages * kStageBytes;
+    static constexpr uint32_t kXBytes = NCG * 2 * 2 * 2 * 32 * 16;
+    static constexpr uint32_t kBarOff = kXOff + kXBytes;
+    static constexpr uint32_t kSmemBytes = kBarOff + (2 * kStages + NCG) * 8 + 1024;
+};
+
+struct HalfFrags {
+    uint32_t ks[4][4];   // K' k-steps of this key half
+    uint32_t qs[4][4];   // s (Q^start)^T k-steps of this key half
+    uint32_t ke[4][4];   // (K^end)^T key tiles of this key half
+    uint32_t akb[4];
+    uint32_t aqk[4];
+    float4 d[2];         // D for the key tiles of this key half
+    uint32_t vb[2];
+};
+
+__device__ __forceinline__ void ks_load_uq(const uint8_t* stage, int kh, int lane, HalfFrags& f) {
+    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t hiA = lane >> 4;
+    const uint32_t sKS = smem_u32(stage + kOffKS);
+    const uint32_t sQS = smem_u32(stage + kOffQS);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        ldsm_x4(f.ks[i], sKS + sw128_off(16, rowA, 2 * (4 * kh + i) + hiA));
+        ldsm_x4(f.qs[i], sQS + sw128_off(16, rowA, 2 * (4 * kh + i) + hiA));
+    }
+}
+__device__ __forceinline__ void ks_load_rest(const uint8_t* stage, uint32_t vrow_bytes, int cg, int kh,
+                                             int lane, HalfFrags& f) {
+    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t hiA = lane >> 4;
+    const int g8 = lane >> 2;
+    const uint32_t sKE = smem_u32(stage + kOffKE);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ldsm_x4(f.ke[i], sKE + sw32_off(16 * (4 * kh + i) + rowA, hiA));
+    ldsm_x4(f.akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
+    ldsm_x4(f.aqk, smem_u32(stage + kOffAQK + sw32_off(rowA, hiA)));
+    const uint8_t* sV = stage + kPacketBytes + (lane & 15) * vrow_bytes + 16 * cg;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(f.vb[0]), "=r"(f.vb[1])
+                 : "r"(smem_u32(sV)));
+    const float4* dp = reinterpret_cast<const float4*>(stage + kOffD) + 4 * g8 + 2 * kh;
+    f.d[0] = dp[0];
+    f.d[1] = dp[1];
+}
+
+template <int NCG>
+__global__ void __launch_bounds__((2 * NCG + 1) * 32, 1)
+    recurrence_ks_kernel(RecArgs a, const __grid_constant__ CUtensorMap vmap) {
+    using L = KsLayout<NCG>;
+    constexpr int kStages = L::kStages;
+    constexpr int kWarps = L::kWarps;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+    uint64_t* empty = full + kStages;
+    uint64_t* xbar = empty + kStages;   // one per column group
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t nh = blockIdx.x / a.nsplit;
+    const int split = blockIdx.x - nh * a.nsplit;
+    const int64_t n = nh / a.H;
+    const int64_t h = nh - n * a.H;
+    const int v0 = split * L::kCols;
+
+    int64_t c_begin, nch, tok0, seqlen;
+    if (a.geo.cu_chunks) {
+        if (!*a.geo.valid) return;
+        c_begin = a.geo.cu_chunks[n];
+        nch = a.geo.cu_chunks[n + 1] - c_begin;
+        tok0 = a.geo.cu_seqlens[n];
+        seqlen = a.geo.cu_seqlens[n + 1] - tok0;
+    } else {
+        c_begin = n * a.geo.chunks_per_seq;
+        nch = a.geo.chunks_per_seq;
+        tok0 = n * a.geo.tokens_per_seq;
+        seqlen = a.geo.tokens_per_seq;
+    }
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kWarps);
+        }
+        for (int g = 0; g < NCG; ++g) mbar_init(&xbar[g], 64);   // every lane of the pair arrives
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kWarps) {
+        // ------------------------------------------------------------ producer
+        uint32_t fill_parity = 0, filled = 0;
+        bool ok = true;
+        for (int64_t c = 0; c < nch && ok; ++c) {
+            const int s = static_cast<int>(c % kStages);
+            if (c >= kStages)
+                ok = mbar_wait_warp_sleep(&empty[s], ((c / kStages) - 1) & 1, a.status);
+            if (!ok) break;
+            uint8_t* stage = smem + s * L::kStageBytes;
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * L::kVRowBytes);
+                bulk_g2s(stage, a.packets + ((c_begin + c) * a.H + h) * static_cast<int64_t>(kPacketBytes),
+                         kPacketBytes, &full[s]);
+                tma_load_2d(stage + kPacketBytes, &vmap, static_cast<int32_t>(h * kHeadDim + v0),
+                            static_cast<int32_t>(tok0 + kChunk * c), &full[s]);
+            }
+            __syncwarp();
+            fill_parity ^= (filled >> s & 1u) << s;
+            filled |= 1u << s;
+        }
+        if (!ok)
+            for (int s = 0; s < kStages; ++s)
+                if (filled >> s & 1u) mbar_wait_bounded(&full[s], (fill_parity >> s) & 1u, a.status);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int cg = warp >> 1;     // column group
+    const int kh = warp & 1;      // key half
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int vcol = v0 + 8 * cg;
+    const int64_t state_base = (n * a.H + h) * kHeadDim * kHeadDim;
+    float4* xb = reinterpret_cast<float4*>(smem + L::kXOff) + cg * (2 * 2 * 2 * 32);
+
+    // S^T rows (keys) of this half: tile i covers keys 16 (4 kh + i) + {g8, g8 + 8}.
+    float Sf[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (a.init_state) {
+            const __nv_bfloat16* src = a.init_state + state_base;
+            const int key = 16 * (4 * kh + i) + g8;
+            const int val = vcol + 2 * t4;
+            Sf[i][0] = __bfloat162float(src[(int64_t)val * kHeadDim + key]);
+            Sf[i][1] = __bfloat162float(src[(int64_t)(val + 1) * kHeadDim + key]);
+            Sf[i][2] = __bfloat162float(src[(int64_t)val * kHeadDim + key + 8]);
+            Sf[i][3] = __bfloat162float(src[(int64_t)(val + 1) * kHeadDim + key + 8]);
+        } else {
+            Sf[i][0] = Sf[i][1] = Sf[i][2] = Sf[i][3] = 0.f;
+        }
+    }
+    uint32_t Sb[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        Sb[i][0] = movm_t(pack_bf16(Sf[i][0], Sf[i][1]));
+        Sb[i][1] = movm_t(pack_bf16(Sf[i][2], Sf[i][3]));
+    }
+
+    bool ok = true;
+    HalfFrags f;
+    if (nch > 0) {
+        ok = mbar_wait_warp(&full[0], 0, a.status);
+        if (ok) {
+            ks_load_uq(smem, kh, lane, f);
+            ks_load_rest(smem, L::kVRowBytes, cg, kh, lane, f);
+        }
+    }
+    for (int64_t c = 0; c < nch && ok; ++c) {
+        const int s = static_cast<int>(c % kStages);
+        const bool has_next = c + 1 < nch;
+        const int s1 = static_cast<int>((c + 1) % kStages);
+        const uint32_t par1 = static_cast<uint32_t>(((c + 1) / kStages) & 1);
+        const uint8_t* stage1 = smem + s1 * L::kStageBytes;
+        bool next_ready = has_next && mbar_try_wait(&full[s1], par1);
+        int64_t len = seqlen - kChunk * c;
+        if (len > kChunk) len = kChunk;
+
+        // Partial U^T and P^T over this warp's 64 keys, from the incoming state.
+        float ua[4] = {0.f, 0.f, 0.f, 0.f}, ub[4] = {0.f, 0.f, 0.f, 0.f};
+        float pa[4] = {0.f, 0.f, 0.f, 0.f}, pb[4] = {0.f, 0.f, 0.f, 0.f};
+        if (kh == 0) mma_bf16(ua, f.akb, f.vb, ua);
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+            mma_bf16(ua, f.ks[i], Sb[i], ua);
+            mma_bf16(ub, f.ks[i + 1], Sb[i + 1], ub);
+            mma_bf16(pa, f.qs[i], Sb[i], pa);
+            mma_bf16(pb, f.qs[i + 1], Sb[i + 1], pb);
+        }
+        const int slot = static_cast<int>(c & 1);
+        float4* mine = xb + ((slot * 2 + kh) * 2) * 32 + lane;
+        const float4* theirs = xb + ((slot * 2 + (kh ^ 1)) * 2) * 32 + lane;
+        mine[0] = make_float4(ua[0] + ub[0], ua[1] + ub[1], ua[2] + ub[2], ua[3] + ub[3]);
+        mine[32] = make_float4(pa[0] + pb[0], pa[1] + pb[1], pa[2] + pb[2], pa[3] + pb[3]);
+        mbar_arrive(&xbar[cg]);
+        // D S^T for this half, in place (the BF16 copy is in Sb).
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float d0 = dsel(f.d[i >> 1], 2 * (i & 1));
+            const float d1 = dsel(f.d[i >> 1], 2 * (i & 1) + 1);
+            Sf[i][0] *= d0;
+            Sf[i][1] *= d0;
+            Sf[i][2] *= d1;
+            Sf[i][3] *= d1;
+        }
+        // The K' and Q^start fragments are dead: load the next chunk's.
+        if (has_next) {
+            if (!__all_sync(0xffffffffu, next_ready))
+                next_ready = mbar_wait_warp(&full[s1], par1, a.status);
+            if (next_ready)
+                ks_load_uq(stage1, kh, lane, f);
+            else
+                ok = false;
+        }
+        // The partner's partials (phase c of the pair barrier).
+        const bool xok = mbar_wait_warp(&xbar[cg], static_cast<uint32_t>(c & 1), a.status);
+        ok = ok && xok;
+        float u[4], pp[4];
+        {
+            const float4 tu = theirs[0], tp = theirs[32];
+            const float4 mu = mine[0], mp = mine[32];
+            // Key half 0 + key half 1, in that order, in both warps.
+            const float4 u0 = kh == 0 ? mu : tu, u1 = kh == 0 ? tu : mu;
+            const float4 p0 = kh == 0 ? mp : tp, p1 = kh == 0 ? tp : mp;
+            u[0] = u0.x + u1.x; u[1] = u0.y + u1.y; u[2] = u0.z + u1.z; u[3] = u0.w + u1.w;
+            pp[0] = p0.x + p1.x; pp[1] = p0.y + p1.y; pp[2] = p0.z + p1.z; pp[3] = p0.w + p1.w;
+        }
+        uint32_t Ub[2];
+        Ub[0] = movm_t(pack_bf16(u[0], u[1]));
+        Ub[1] = movm_t(pack_bf16(u[2], u[3]));
+        // S^T <- D S^T + (K^end)^T U^T for this half.
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mma_bf16(Sf[i], f.ke[i], Ub, Sf[i]);
+        float o[4];
+        mma_bf16(o, f.aqk, Ub, pp);
+        if (has_next && ok) ks_load_rest(stage1, L::kVRowBytes, cg, kh, lane, f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            Sb[i][0] = movm_t(pack_bf16(Sf[i][0], Sf[i][1]));
+            Sb[i][1] = movm_t(pack_bf16(Sf[i][2], Sf[i][3]));
+        }
+        __syncwarp();
+        mbar_arrive_if(&empty[s], lane == 0);
+        // Key half 0 stores tokens 0-7 of O, key half 1 tokens 8-15.
+        const int tok = 8 * kh + g8;
+        __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + tok) * a.H + h) * kHeadDim + vcol + 2 * t4;
+        st_global_u32_if(orow, kh == 0 ? pack_bf16(o[0], o[1]) : pack_bf16(o[2], o[3]), tok < len);
+    }
+
+    if (ok && a.final_state) {
+        __nv_bfloat16* dst = a.final_state + state_base;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int key = 16 * (4 * kh + i) + g8;
+            const int val = vcol + 2 * t4;
+            dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[i][0]);
+            dst[(int64_t)(val + 1) * kHeadDim + key] = __float2bfloat16_rn(Sf[i][1]);
+            dst[(int64_t)val * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[i][2]);
+            dst[(int64_t)(val + 1) * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[i][3]);
+        }
+    }
+}
+
+template <int NCG>
+cudaError_t launch_ks(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
+    using L = KsLayout<NCG>;
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(recurrence_ks_kernel<NCG>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(L::kSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    CUtensorMap vmap;
+    alignas(64) static const char kZero[16] = {};
+    const void* vbase = a.v ? static_cast<const void*>(a.v) : static_cast<const void*>(kZero);
+    cudaError_t e = encode_v_map(&vmap, vbase, a.geo.tokens, a.H, L::kCols);
+    if (e != cudaSuccess) return e;
+    recurrence_ks_kernel<NCG><<<static_cast<unsigned>(blocks), (2 * NCG + 1) * 32, L::kSmemBytes, stream>>>(a, vmap);
+    return cudaGetLastError();
+}
+
 template <int NW>
 cudaError_t launch_nw(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
     using L = RecLayout<NW>;
@@ -660,15 +1047,23 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
     if (blocks <= 0) return cudaSuccess;
     if (geo.tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // TMA coordinates are int32
     if (blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    if (recurrence_engine() == 1) {
+        // Keys-major form only, 8 value columns per warp (for comparison).
+        switch (nsplit) {
+            case 1: return launch_nw<16>(a, blocks, stream);
+            case 2: return launch_nw<8>(a, blocks, stream);
+            case 4: return launch_nw<4>(a, blocks, stream);
+            case 8: return launch_nw<2>(a, blocks, stream);
+            case 16: return launch_nw<1>(a, blocks, stream);
+            default: return cudaErrorInvalidValue;
+        }
+    }
     switch (nsplit) {
-        case 1:
-            // Engine 1 keeps 16 warps of 8 columns (for comparison).
-            return recurrence_engine() == 1 ? launch_nw<16>(a, blocks, stream)
-                                            : launch_wide(a, blocks, stream);
-        case 2: return launch_nw<8>(a, blocks, stream);
-        case 4: return launch_nw<4>(a, blocks, stream);
-        case 8: return launch_nw<2>(a, blocks, stream);
-        case 16: return launch_nw<1>(a, blocks, stream);
+        case 1: return launch_wide(a, blocks, stream);     // 8 warps x 16 columns
+        case 2: return launch_nw<8>(a, blocks, stream);    // 8 warps x 8 columns
+        case 4: return launch_ks<4>(a, blocks, stream);    // key split: 4 pairs x 8 columns
+        case 8: return launch_ks<2>(a, blocks, stream);
+        case 16: return launch_ks<1>(a, blocks, stream);
         default: return cudaErrorInvalidValue;
     }
 }

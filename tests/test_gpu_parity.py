@@ -162,23 +162,29 @@ def test_correlated_keys_end_to_end(kda):
 
 
 def test_split_factors_bitwise_identical(kda):
-    """Each value column runs the same arithmetic whichever CTA or warp owns it,
-    so every split of the state over CTAs, and both warp widths of the
-    one-CTA-per-head kernel (16 or 8 value columns per warp), give the same bits."""
+    """Each value column runs the same arithmetic whichever CTA or warp owns it.
+    Splits 1 and 2 (and the 8-column warps of engine 1) sum every product over
+    all 128 keys in one order and give the same bits; splits 4, 8 and 16 split
+    the keys over a warp pair and give the same bits among themselves.  Both
+    families match the oracle."""
     inp = synthetic.make_inputs(1, 200, 2, 77, init_std=0.02)
-    outs = []
+    outs = {}
     try:
         for ns in (1, 2, 4, 8, 16):
             kda.set_split(ns)
-            outs.append(run(kda, inp))
+            outs[ns] = run(kda, inp)
         kda.set_split(1)
         kda.set_engine(1)
-        outs.append(run(kda, inp))
+        outs["narrow"] = run(kda, inp)
     finally:
         kda.set_engine(0)
         kda.set_split(0)
-    for o, f in outs[1:]:
-        assert torch.equal(o, outs[0][0]) and torch.equal(f, outs[0][1])
+    for family in ((1, 2, "narrow"), (4, 8, 16)):
+        o0, f0 = outs[family[0]]
+        for key in family[1:]:
+            o, f = outs[key]
+            assert torch.equal(o, o0) and torch.equal(f, f0), key
+        tu.check_against_oracle(inp, o0, f0)
 
 
 def test_deterministic(kda):
@@ -331,3 +337,49 @@ def test_tcgen05_full_workload(tc_engine, name):
     inp = synthetic.make_workload(name)
     out, fin = run(tc_engine, inp)
     tu.check_against_oracle(inp, out, fin, heads=[0, 5, 11] if name == "varlen8_h12" else None)
+
+
+# ----------------------------------------------------------------------------
+# The key-split recurrence (two warps per 8-column group, one per half of the
+# keys), forced at each split it serves
+# ----------------------------------------------------------------------------
+
+@pytest.fixture
+def forced_split(kda):
+    yield kda
+    kda.set_split(0)
+
+
+@pytest.mark.parametrize("nsplit", [4, 8, 16])
+def test_keysplit_small(forced_split, nsplit):
+    forced_split.set_split(nsplit)
+    for B, T, H, init in SMALL:
+        inp = synthetic.make_inputs(B, T, H, 3000 + T, init_std=0.02 if init else None)
+        out, fin = run(forced_split, inp)
+        tu.check_against_oracle(inp, out, fin)
+    inp = synthetic.make_inputs(0, 0, 3, 57, init_std=0.02, lengths=[5, 0, 33, 16, 1, 64, 200])
+    out, fin = run(forced_split, inp)
+    tu.check_against_oracle(inp, out, fin)
+
+
+def test_keysplit_deterministic_and_in_place(forced_split):
+    forced_split.set_split(8)
+    inp = synthetic.make_inputs(2, 130, 3, 5, init_std=0.02)
+    a = run(forced_split, inp)
+    b = run(forced_split, inp)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    d = tu.to_device(inp)
+    state = d["init_state"].clone()
+    out, _ = forced_split.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], state,
+                                      final_state=state)
+    torch.cuda.synchronize()
+    assert torch.equal(out.cpu(), a[0]) and torch.equal(state.cpu(), a[1])
+
+
+@pytest.mark.parametrize("nsplit", [1, 2, 4])
+def test_forced_split_full_t8192_h6(forced_split, nsplit):
+    """The 6-head workload (auto split 16) through the other kernel variants."""
+    forced_split.set_split(nsplit)
+    inp = synthetic.make_workload("t8192_h6")
+    out, fin = run(forced_split, inp)
+    tu.check_against_oracle(inp, out, fin)
