@@ -52,18 +52,23 @@ L2_FLUSH_BYTES = 512 << 20
 #                13,824-byte packet per 16 tokens (864 B per head-token).
 #   recurrence:  reads the packets (864 B) and v (256 B); writes O (256 B);
 #                plus 32 KB per (sequence, head) for each state read or written.
+#   one launch (preparation and recurrence fused): the inputs and outputs of
+#                the whole path, q, k, g, beta, v in and O out (1,538 B per
+#                head-token) plus the states; the packets pass between the two
+#                halves of the launch and are not counted.
 PACKET_PER_TOKEN = 13824 / 16
 PREP_BYTES_PER_HT = 2 * 256 + 512 + 2 + PACKET_PER_TOKEN
 REC_BYTES_PER_HT = PACKET_PER_TOKEN + 256 + 256
+PATH_BYTES_PER_HT = 2 * 256 + 512 + 2 + 256 + 256
 STATE_BYTES = 128 * 128 * 2
 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from one ncu
 # capture each (summaries in profiles/).  A figure is reported only while the
 # kernel's sources still hash to the value they had when it was captured.
+REC_SOURCES = ("kda_recurrence.cu", "kda_rec_impl.cuh", "kda_common.cuh")
+PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
+FUSED_SOURCES = ("kda_fused.cu", "kda_prep_impl.cuh", "kda_rec_impl.cuh", "kda_common.cuh")
 PROFILED_TRAFFIC = {
-    ("recurrence", "t8192_h6"): (56.08e6, ("kda_recurrence.cu", "kda_common.cuh"), "1defd151beb3fd69"),
-    ("recurrence", "t8192_h96"): (1067.3e6, ("kda_recurrence.cu", "kda_common.cuh"), "1defd151beb3fd69"),
-    ("chunk_prep", "t8192_h96"): (1442.7e6, ("kda_prep.cu", "kda_common.cuh"), "3c1b2987a6857c0b"),
 }
 
 
@@ -316,6 +321,7 @@ def run_ours(args):
         kda.set_split(args.split)
     if args.engine:
         kda.set_engine(args.engine)
+    kda.set_fusion(bool(args.fusion))
     stream = torch.cuda.Stream(device=device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
@@ -323,6 +329,9 @@ def run_ours(args):
     d = device_inputs(inp, device)
     ht = head_tokens(inp)
     nsplit = kda.auto_split(inp["N"], inp["q"].shape[2])
+    packed = inp["cu_seqlens"] is not None
+    fused = kda.plan_fused(inp["N"] if packed else inp["q"].shape[0], inp["q"].shape[1],
+                           inp["q"].shape[2], packed)
 
     if ws > 1:
         torch.distributed.barrier()
@@ -357,7 +366,11 @@ def run_ours(args):
     state_io = (2 if inp["init_state"] is not None else 1) * n_states * STATE_BYTES
     rec_bytes = REC_BYTES_PER_HT * ht + state_io
     prep_bytes = PREP_BYTES_PER_HT * ht
-    if rec_avg >= prep_avg:
+    if fused:
+        # The profile's first interval is the reset of the ready flags, the
+        # second the one launch.
+        dom, dom_bytes, dom_ms = "fused", PATH_BYTES_PER_HT * ht + state_io, rec_avg
+    elif rec_avg >= prep_avg:
         dom, dom_bytes, dom_ms = "recurrence", rec_bytes, rec_avg
     else:
         dom, dom_bytes, dom_ms = "chunk_prep", prep_bytes, prep_avg
@@ -365,9 +378,12 @@ def run_ours(args):
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
                 "traffic": profiled_traffic(dom, args.workload, args.engine),
-                "prep_us": 1e3 * prep_avg, "recurrence_us": 1e3 * rec_avg,
                 "chain_steps": int(math.ceil(inp["q"].shape[1] / 16)) if inp["cu_seqlens"] is None
                 else None}
+    if fused:
+        roofline.update({"fused_us": 1e3 * rec_avg, "flag_reset_us": 1e3 * prep_avg})
+    else:
+        roofline.update({"prep_us": 1e3 * prep_avg, "recurrence_us": 1e3 * rec_avg})
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -377,8 +393,8 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": inp["workload"].name, "l2": "flushed (512 MiB write) before every step",
                    "recurrence_split": nsplit, "recurrence_engine": args.engine,
-                   "head_tokens_per_step": ht},
-        "gpu_launches": (3 if inp["cu_seqlens"] is not None else 2) * args.steps,
+                   "one_launch": fused, "head_tokens_per_step": ht},
+        "gpu_launches": (1 if fused else (3 if packed else 2)) * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "us_per_call": 1e3 * total_e2e / args.steps},
         "roofline": roofline,
@@ -428,6 +444,8 @@ def main():
                     help="CTAs per (sequence, head) in the recurrence (0 = automatic)")
     ap.add_argument("--engine", type=int, default=0,
                     help="recurrence engine: 0 automatic, 1 column-split warp MMA, 2 tcgen05")
+    ap.add_argument("--fusion", type=int, default=1, choices=[0, 1],
+                    help="allow preparation and recurrence as one launch (kda_set_fusion)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

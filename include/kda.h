@@ -115,12 +115,32 @@ int kda_set_split(int nsplit);
  */
 int kda_set_engine(int engine);
 
+/*
+ * Whether kda_prefill may run preparation and recurrence as one cooperative
+ * launch (1, the default) or always as two kernels (0).  One launch is used
+ * for fixed-length batches (cu_seqlens NULL) under engine 0 whose recurrence
+ * takes a split of 8 or 16 and leaves at least 16 SMs free: those SMs prepare
+ * packets while the recurrence consumes them, each packet behind a ready flag
+ * in the workspace.  The results are bit for bit those of the two-kernel path.
+ * Process-wide; returns KDA_ERR_ARG for other values.
+ */
+int kda_set_fusion(int on);
+
+/*
+ * Whether kda_prefill would run a call of this shape as one launch on the
+ * current device under the current settings (HOST out: 1 or 0).  Errors as
+ * kda_prefill's shape checks, or KDA_ERR_DEVICE / KDA_ERR_CUDA without a
+ * usable device.
+ */
+int kda_plan_fused(int64_t B, int64_t T, int64_t H, int packed, int* fused);
+
 /* The split the automatic rule picks on the current device for N*H units (HOST out). */
 int kda_auto_split(int64_t n_seqs, int64_t H, int* nsplit);
 
 /*
- * Bytes of scratch kda_prefill takes for a given shape (HOST out); `packed`
- * is nonzero for the packed layout, where the size is an upper bound.
+ * Bytes of scratch kda_prefill takes for a given shape at most (HOST out);
+ * `packed` is nonzero for the packed layout.  The ready flags of a fused
+ * launch (kda_set_fusion) are counted whether or not the call fuses.
  */
 int kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int packed, int64_t* bytes);
 
@@ -143,7 +163,9 @@ int64_t kda_packet_bytes(void);
  * 3 * max_calls CUDA events on the current device; each of the next
  * max_calls kda_prefill calls then records one event before its preparation
  * kernels, one between preparation and recurrence and one after the
- * recurrence, on its own stream.  kda_profile_end synchronises those events,
+ * recurrence, on its own stream.  When a call runs as one launch (see
+ * kda_set_fusion), the first interval holds only the reset of the ready flags
+ * and the second the fused kernel.  kda_profile_end synchronises those events,
  * writes the summed preparation and recurrence times in milliseconds and the
  * number of calls timed (HOST pointers), and destroys the events.
  * Process-wide; begin while active returns KDA_ERR_ARG.

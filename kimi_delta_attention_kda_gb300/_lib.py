@@ -49,6 +49,10 @@ def load():
         lib.kda_set_split.restype = I
         lib.kda_set_engine.argtypes = [I]
         lib.kda_set_engine.restype = I
+        lib.kda_set_fusion.argtypes = [I]
+        lib.kda_set_fusion.restype = I
+        lib.kda_plan_fused.argtypes = [I64, I64, I64, I, ctypes.POINTER(I)]
+        lib.kda_plan_fused.restype = I
         lib.kda_auto_split.argtypes = [I64, I64, ctypes.POINTER(I)]
         lib.kda_auto_split.restype = I
         lib.kda_workspace_bytes.argtypes = [I64, I64, I64, I, ctypes.POINTER(I64)]
@@ -102,6 +106,19 @@ def set_split(nsplit: int):
 def set_engine(engine: int):
     """0 automatic, 1 column-split warp-MMA kernel, 2 tcgen05 kernel."""
     _check(load().kda_set_engine(int(engine)), "kda_set_engine")
+
+
+def set_fusion(on: bool):
+    """Allow (True, the default) or forbid preparation and recurrence as one launch."""
+    _check(load().kda_set_fusion(1 if on else 0), "kda_set_fusion")
+
+
+def plan_fused(B: int, T: int, H: int, packed: bool) -> bool:
+    """Whether kda_prefill runs this shape as one launch on the current device."""
+    out = ctypes.c_int(0)
+    _check(load().kda_plan_fused(int(B), int(T), int(H), 1 if packed else 0, ctypes.byref(out)),
+           "kda_plan_fused")
+    return bool(out.value)
 
 
 def auto_split(n_seqs: int, H: int) -> int:

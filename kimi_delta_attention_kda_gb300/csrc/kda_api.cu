@@ -30,6 +30,7 @@ std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
 int g_split_override = 0;
 int g_engine = 0;
+int g_fusion = 1;
 
 // Optional per-kernel timing: when active, each kda_prefill call records three
 // events on its stream (before the preparation kernels, between preparation
@@ -115,6 +116,7 @@ int choose_split(int64_t units, int sms) {
 }
 
 constexpr int64_t kMaxElems = int64_t(1) << 56;
+constexpr float kScale = 0.08838834764831845f;   // 1 / sqrt(128)
 
 struct Plan {
     bool packed;
@@ -122,6 +124,7 @@ struct Plan {
     SeqGeometry geo;
     int64_t meta_bytes;      // valid flag + cu_chunks (packed only), 256-aligned
     int64_t packet_bytes;    // chunk_ub * H * kPacketBytes
+    int64_t ready_bytes;     // chunk_ub * H flags of the fused launch, 256-aligned
 };
 
 int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
@@ -148,7 +151,21 @@ int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
     }
     if (g.chunk_ub > kMaxElems / (H * kPacketBytes)) return KDA_ERR_SHAPE;
     p->packet_bytes = g.chunk_ub * H * static_cast<int64_t>(kPacketBytes);
+    p->ready_bytes = ((g.chunk_ub * H * 4 + 255) / 256) * 256;
     return KDA_OK;
+}
+
+// Whether kda_prefill runs preparation and recurrence as one launch: the
+// key-split recurrence on part of the SMs, with enough SMs left for the
+// preparation to stay ahead of it.  A preparing warp takes about 25 times as
+// long per packet as the recurrence takes per chunk, so the free SMs'
+// 8 warps each must have at most ~chunks / 4 packets to make.
+bool use_fusion(const Plan& pl, int64_t H, int nsplit, int sms) {
+    if (!g_fusion || g_engine != 0 || pl.packed || pl.tokens <= 0) return false;
+    if (!fused_supported(pl.N, H, nsplit, sms)) return false;
+    const int64_t free_sms = sms - pl.N * H * nsplit;
+    if (free_sms < 16) return false;
+    return pl.geo.chunk_ub * H <= free_sms * pl.geo.chunks_per_seq / 4;
 }
 
 // Launch metadata (packed) and preparation into `ws` (meta) and `packets`.
@@ -166,8 +183,7 @@ int run_prep(const Plan& pl, const void* q, const void* k, const float* g, const
         geo.cu_chunks = cu_chunks;
         geo.valid = valid;
     }
-    const float scale = 0.08838834764831845f;   // 1 / sqrt(128)
-    if (launch_prep(q, k, g, beta, packets, geo, H, scale, d->status, stream) != cudaSuccess)
+    if (launch_prep(q, k, g, beta, packets, geo, H, kScale, d->status, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
     *geo_out = geo;
     return KDA_OK;
@@ -227,7 +243,9 @@ extern "C" int kda_prefill(const void* q, const void* k, const void* v, const fl
     if (rc != KDA_OK) return rc;
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
-    const int64_t ws_bytes = pl.meta_bytes + pl.packet_bytes;
+    const int nsplit = choose_split(pl.N * H, d->sms);
+    const bool fused = use_fusion(pl, H, nsplit, d->sms);
+    const int64_t ws_bytes = pl.meta_bytes + pl.packet_bytes + (fused ? pl.ready_bytes : 0);
     uint8_t* ws = nullptr;
     if (ws_bytes > 0) {
         if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes),
@@ -238,11 +256,28 @@ extern "C" int kda_prefill(const void* q, const void* k, const void* v, const fl
     }
     SeqGeometry geo;
     prof_record(0, stream);
-    rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, ws + pl.meta_bytes, d, stream, &geo);
-    prof_record(1, stream);
-    if (rc == KDA_OK) {
-        const int nsplit = choose_split(pl.N * H, d->sms);
-        if (launch_recurrence(v, out, init_state, final_state, ws + pl.meta_bytes, geo, H, nsplit,
+    bool done = false;
+    if (fused) {
+        // Reset the ready flags, then one cooperative launch.  If the device
+        // refuses the cooperative launch (fewer SMs available to this
+        // context), fall through to the two-kernel path.
+        uint32_t* ready = reinterpret_cast<uint32_t*>(ws + pl.meta_bytes + pl.packet_bytes);
+        if (cudaMemsetAsync(ready, 0, static_cast<size_t>(pl.ready_bytes), stream) != cudaSuccess)
+            rc = KDA_ERR_CUDA;
+        prof_record(1, stream);
+        if (rc == KDA_OK) {
+            if (launch_fused(q, k, g, beta, v, out, init_state, final_state, ws + pl.meta_bytes,
+                             ready, pl.geo, H, nsplit, kScale, d->status, stream) == cudaSuccess)
+                done = true;
+            else
+                cudaGetLastError();
+        }
+    }
+    if (rc == KDA_OK && !done) {
+        rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, ws + pl.meta_bytes, d, stream, &geo);
+        prof_record(1, stream);
+        if (rc == KDA_OK &&
+            launch_recurrence(v, out, init_state, final_state, ws + pl.meta_bytes, geo, H, nsplit,
                               d->status, stream) != cudaSuccess)
             rc = KDA_ERR_CUDA;
     }
@@ -326,6 +361,24 @@ extern "C" int kda_set_split(int nsplit) {
     return KDA_OK;
 }
 
+extern "C" int kda_plan_fused(int64_t B, int64_t T, int64_t H, int packed, int* fused) {
+    if (!fused) return KDA_ERR_NULL;
+    Plan pl;
+    int rc = make_plan(B, T, H, packed != 0, &pl);
+    if (rc != KDA_OK) return rc;
+    DeviceState* d = nullptr;
+    rc = device_state(&d);
+    if (rc != KDA_OK) return rc;
+    *fused = use_fusion(pl, H, choose_split(pl.N * H, d->sms), d->sms) ? 1 : 0;
+    return KDA_OK;
+}
+
+extern "C" int kda_set_fusion(int on) {
+    if (on != 0 && on != 1) return KDA_ERR_ARG;
+    g_fusion = on;
+    return KDA_OK;
+}
+
 extern "C" int kda_set_engine(int engine) {
     if (engine < 0 || engine > 2) return KDA_ERR_ARG;
     g_engine = engine;
@@ -347,7 +400,7 @@ extern "C" int kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int packed, 
     Plan pl;
     int rc = make_plan(B, T, H, packed != 0, &pl);
     if (rc != KDA_OK) return rc;
-    *bytes = pl.meta_bytes + pl.packet_bytes;
+    *bytes = pl.meta_bytes + pl.packet_bytes + (pl.packed ? 0 : pl.ready_bytes);
     return KDA_OK;
 }
 

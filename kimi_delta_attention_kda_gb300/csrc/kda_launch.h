@@ -43,6 +43,17 @@ cudaError_t launch_recurrence_tc(const void* v, void* out, const void* init_stat
                                  void* final_state, const uint8_t* packets, const SeqGeometry& geo,
                                  int64_t H, int* status, cudaStream_t stream);
 
+// Preparation and the key-split recurrence (nsplit 8 or 16) as one
+// cooperative launch over all SMs, for fixed-length batches whose recurrence
+// grid leaves SMs free.  `ready` holds chunk_ub * H flags that must be zero
+// when the kernel starts; the packets go through `packets` as in the
+// two-kernel path.
+bool fused_supported(int64_t n_seqs, int64_t H, int nsplit, int sms);
+cudaError_t launch_fused(const void* q, const void* k, const float* g, const void* beta,
+                         const void* v, void* out, const void* init_state, void* final_state,
+                         uint8_t* packets, uint32_t* ready, const SeqGeometry& geo, int64_t H,
+                         int nsplit, float scale, int* status, cudaStream_t stream);
+
 // Tensor map of v viewed as a 2-D BF16 array [tokens][H * 128], boxes of
 // 16 tokens x `cols` value columns.
 cudaError_t encode_v_map(CUtensorMap* map, const void* v, int64_t tokens, int64_t H, int cols);

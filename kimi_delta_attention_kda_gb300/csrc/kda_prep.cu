@@ -26,9 +26,11 @@
 // g = 0, beta = 0.  They then contribute nothing to any output or state.
 //
 // The kernel is persistent: every warp walks a strided list of (chunk, head)
-// items.  While it computes item i, the 2-D TMA loads of item i + 1's q, k and
-// g tiles are already in flight into the warp's other buffer; once an item's
-// inputs are in registers its buffer is reused as that item's scratch.
+// items through one shared-memory region: 2-D TMA loads of the item's q, k
+// and g tiles, the item's work (the region turns into scratch once the inputs
+// are in registers, then into the packet image), and one bulk copy of the
+// packet to global memory, which must have read the region before the next
+// item's loads overwrite it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -36,343 +38,12 @@
 
 #include "kda_common.cuh"
 #include "kda_launch.h"
+#include "kda_prep_impl.cuh"
 
 namespace kda {
 namespace {
 
-constexpr int kPrepWarps = 8;
-// Per-warp shared memory: one 28 KB region that holds, in turn, an item's
-// TMA inputs, its scratch and its packet image:
-//   inputs  : q [16][128] BF16 at 0, k at 4096, g [16][128] FP32 at 8192
-//   scratch : [0,4K) K^start hi (packet KS) | [4K,8K) s Q^start hi (packet QS) |
-//             [8K,12K) exp(-G) khat hi | [12K,16K) exp(-G) khat lo |
-//             [16K,20K) K^start lo | [20K,24K) s Q^start lo | [24K,28K) K^end rows
-//             (tiles 16 x 128 BF16, SW128; "lo" = BF16 rounding of what the
-//             BF16 "hi" part left out)
-//   packet  : once the score MMAs are done, [8K,12K) receives K^end^T, [12K,13.5K)
-//             A^kk B, A^qk and D; R (FP32) and the low part of A^kk B go to
-//             [20K,22.5K); finally -(A^kk B) K^start^T replaces K^start in [0,4K):
-//             [0, 13824) is then the packet image.
-constexpr uint32_t kInQ = 0, kInK = 4096, kInG = 8192, kInBytes = 16384;
-constexpr uint32_t kPrepOffKinv = 8192;
-constexpr uint32_t kPrepOffKinvLo = 12288;
-constexpr uint32_t kPrepOffKsLo = 16384;
-constexpr uint32_t kPrepOffQsLo = 20480;
-constexpr uint32_t kPrepOffKen = 24576;
-constexpr uint32_t kPrepOffAkbLo = 20480;     // 16 x 16 BF16 SW32, after the score MMAs
-constexpr uint32_t kPrepOffR = 21504;          // 16 x 16 FP32, after the score MMAs
-constexpr uint32_t kPrepWarpSmem = 28672;
-constexpr uint32_t kPrepSmemBytes = kPrepWarps * kPrepWarpSmem + 64 + 1024;  // + barriers, align
-
-struct PrepArgs {
-    const __nv_bfloat16* beta;
-    uint8_t* packets;
-    SeqGeometry geo;
-    int64_t H;
-    int64_t n_chunk_heads;
-    float scale;
-};
-
-struct PrepMaps {
-    CUtensorMap q, k, g;   // [tokens][H * 128] views, boxes of 16 tokens x 128 channels
-};
-
-// Largest n in [0, N) with cu_chunks[n] <= c (cu_chunks non-decreasing,
-// cu_chunks[0] = 0 <= c < cu_chunks[N]).
-__device__ __forceinline__ int64_t find_sequence(const int64_t* cu_chunks, int64_t N, int64_t c) {
-    int64_t lo = 0, hi = N;
-    while (hi - lo > 1) {
-        int64_t mid = (lo + hi) >> 1;
-        if (cu_chunks[mid] <= c)
-            lo = mid;
-        else
-            hi = mid;
-    }
-    return lo;
-}
-
-// Store 4 consecutive BF16 (channels 4*lane .. 4*lane+3) of token row t into a
-// [16][128] SW128 tile.
-__device__ __forceinline__ void st_row4(uint8_t* tile, int t, int lane, float a, float b, float c,
-                                        float d) {
-    uint32_t off = sw128_off(16, t, (4 * lane) >> 3) + ((lane & 1) << 3);
-    uint2 v = make_uint2(pack_bf16(a, b), pack_bf16(c, d));
-    *reinterpret_cast<uint2*>(tile + off) = v;
-}
-// Same, storing the BF16 rounding in `hi` and the BF16 rounding of what it
-// left out in `lo`, so that hi + lo carries about 16 significant bits.
-__device__ __forceinline__ void st_row4_split(uint8_t* hi, uint8_t* lo, int t, int lane, float a,
-                                              float b, float c, float d) {
-    uint32_t off = sw128_off(16, t, (4 * lane) >> 3) + ((lane & 1) << 3);
-    const uint32_t h0 = pack_bf16(a, b), h1 = pack_bf16(c, d);
-    const uint32_t l0 = pack_bf16(a - bf16_lo(h0), b - bf16_hi(h0));
-    const uint32_t l1 = pack_bf16(c - bf16_lo(h1), d - bf16_hi(h1));
-    *reinterpret_cast<uint2*>(hi + off) = make_uint2(h0, h1);
-    *reinterpret_cast<uint2*>(lo + off) = make_uint2(l0, l1);
-}
-
-// Token range [t0, t0 + len) of item (chunk c, head h); false when the item
-// does not exist (past the last chunk of a packed batch, or invalid offsets).
-__device__ __forceinline__ bool item_range(const PrepArgs& a, int64_t item, int64_t* t0,
-                                           int64_t* len, int64_t* c_out, int64_t* h_out) {
-    const int64_t c = item / a.H;
-    const int64_t h = item - c * a.H;
-    if (a.geo.cu_chunks) {
-        if (c >= a.geo.cu_chunks[a.geo.n_seqs]) return false;
-        const int64_t n = find_sequence(a.geo.cu_chunks, a.geo.n_seqs, c);
-        *t0 = a.geo.cu_seqlens[n] + kChunk * (c - a.geo.cu_chunks[n]);
-        *len = a.geo.cu_seqlens[n + 1] - *t0;
-    } else {
-        const int64_t n = c / a.geo.chunks_per_seq;
-        const int64_t ci = c - n * a.geo.chunks_per_seq;
-        *t0 = n * a.geo.tokens_per_seq + kChunk * ci;
-        *len = a.geo.tokens_per_seq - kChunk * ci;
-    }
-    if (*len > kChunk) *len = kChunk;
-    *c_out = c;
-    *h_out = h;
-    return true;
-}
-
-// One (chunk, head): inputs from the TMA tiles in `in`, packet image to `pk`,
-// scratch in `in` once the inputs are in registers.
-__device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t len, float scale,
-                                          int lane) {
-    const uint8_t* in = region;
-    uint8_t* ws = region;
-    uint8_t* sc = region;
-    uint8_t* tKS = ws + kOffKS;
-    uint8_t* tQS = ws + kOffQS;
-    uint8_t* tKE = ws + kOffKE;
-    uint8_t* tAKB = ws + kOffAKB;
-    uint8_t* tAQK = ws + kOffAQK;
-    float* tD = reinterpret_cast<float*>(ws + kOffD);
-    uint8_t* tKinv = sc + kPrepOffKinv;
-    uint8_t* tKinvLo = sc + kPrepOffKinvLo;
-    uint8_t* tKsLo = sc + kPrepOffKsLo;
-    uint8_t* tQsLo = sc + kPrepOffQsLo;
-    uint8_t* tKen = sc + kPrepOffKen;
-    float* tR = reinterpret_cast<float*>(sc + kPrepOffR);
-
-    // ---- 1. q, k (BF16, 4 channels per lane), g (running sum -> G) from the
-    // tiles; tokens past the end of the sequence read as zero.
-    uint2 qv[kChunk], kv[kChunk];
-    float G[kChunk][4];
-    float red[2 * kChunk];   // partial sums of squares: q tokens 0..15, k tokens 0..15
-    float run0 = 0.f, run1 = 0.f, run2 = 0.f, run3 = 0.f;
-#pragma unroll
-    for (int t = 0; t < kChunk; ++t) {
-        const bool live = t < len;
-        const uint2 qq = *reinterpret_cast<const uint2*>(in + kInQ + t * 256 + 8 * lane);
-        const uint2 kq = *reinterpret_cast<const uint2*>(in + kInK + t * 256 + 8 * lane);
-        const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
-        qv[t] = live ? qq : make_uint2(0u, 0u);
-        kv[t] = live ? kq : make_uint2(0u, 0u);
-        run0 += live ? gg.x : 0.f;
-        run1 += live ? gg.y : 0.f;
-        run2 += live ? gg.z : 0.f;
-        run3 += live ? gg.w : 0.f;
-        G[t][0] = run0;
-        G[t][1] = run1;
-        G[t][2] = run2;
-        G[t][3] = run3;
-        const float q0 = bf16_lo(qv[t].x), q1 = bf16_hi(qv[t].x), q2 = bf16_lo(qv[t].y),
-                    q3 = bf16_hi(qv[t].y);
-        const float k0 = bf16_lo(kv[t].x), k1 = bf16_hi(kv[t].x), k2 = bf16_lo(kv[t].y),
-                    k3 = bf16_hi(kv[t].y);
-        red[t] = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
-        red[kChunk + t] = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
-    }
-    // The input tiles are consumed: from here on the buffer is scratch.
-    __syncwarp();
-
-    // ---- 2. Sums of squares over the 128 channels: butterfly reduce-scatter.
-    // After the step with offset o, element i stands for original index
-    // i + o * (bit o of lane); at the end lane l holds the total of index l.
-#pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
-        const bool up = (lane & o) != 0;
-#pragma unroll
-        for (int i = 0; i < o; ++i) {
-            const float send = up ? red[i] : red[i + o];
-            const float keep = up ? red[i + o] : red[i];
-            red[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-        }
-    }
-    const float rnorm = rsqrtf(red[0] + 1e-6f);   // lane < 16: 1/|q_lane|, else 1/|k_(lane-16)|
-
-    // ---- 3. Decayed operands.
-    const float e_last0 = __expf(G[kChunk - 1][0]), e_last1 = __expf(G[kChunk - 1][1]);
-    const float e_last2 = __expf(G[kChunk - 1][2]), e_last3 = __expf(G[kChunk - 1][3]);
-    const float s = scale;
-#pragma unroll
-    for (int t = 0; t < kChunk; ++t) {
-        const float rq = __shfl_sync(0xffffffffu, rnorm, t);
-        const float rk = __shfl_sync(0xffffffffu, rnorm, kChunk + t);
-        const float kh0 = bf16_lo(kv[t].x) * rk, kh1 = bf16_hi(kv[t].x) * rk;
-        const float kh2 = bf16_lo(kv[t].y) * rk, kh3 = bf16_hi(kv[t].y) * rk;
-        const float qh0 = bf16_lo(qv[t].x) * rq, qh1 = bf16_hi(qv[t].x) * rq;
-        const float qh2 = bf16_lo(qv[t].y) * rq, qh3 = bf16_hi(qv[t].y) * rq;
-        const float e0 = __expf(G[t][0]), e1 = __expf(G[t][1]);
-        const float e2 = __expf(G[t][2]), e3 = __expf(G[t][3]);
-        const float i0 = __expf(-G[t][0]), i1 = __expf(-G[t][1]);
-        const float i2 = __expf(-G[t][2]), i3 = __expf(-G[t][3]);
-        st_row4_split(tKS, tKsLo, t, lane, e0 * kh0, e1 * kh1, e2 * kh2, e3 * kh3);
-        st_row4_split(tQS, tQsLo, t, lane, s * e0 * qh0, s * e1 * qh1, s * e2 * qh2, s * e3 * qh3);
-        st_row4_split(tKinv, tKinvLo, t, lane, i0 * kh0, i1 * kh1, i2 * kh2, i3 * kh3);
-        st_row4(tKen, t, lane, (e_last0 * i0) * kh0, (e_last1 * i1) * kh1,
-                (e_last2 * i2) * kh2, (e_last3 * i3) * kh3);
-    }
-    __syncwarp();
-
-    // ---- 4. Scores: A^qk = (s Q^start)(K exp(-G))^T and K^start (K exp(-G))^T,
-    // each as hi*hi + hi*lo + lo*hi of the split BF16 operands (FP32 accumulate).
-    const int gq = lane >> 2, tq = lane & 3;
-    float acc_qk[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float acc_kk[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    {
-        const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
-        const uint32_t rowB = (lane & 7) + (lane >> 4) * 8;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            uint32_t aq[4], ak[4], bk[4], aql[4], akl[4], bkl[4];
-            const uint32_t offA = sw128_off(16, rowA, 2 * kk + (lane >> 4));
-            const uint32_t offB = sw128_off(16, rowB, 2 * kk + ((lane >> 3) & 1));
-            ldsm_x4(aq, smem_u32(tQS + offA));
-            ldsm_x4(ak, smem_u32(tKS + offA));
-            ldsm_x4(bk, smem_u32(tKinv + offB));
-            ldsm_x4(aql, smem_u32(tQsLo + offA));
-            ldsm_x4(akl, smem_u32(tKsLo + offA));
-            ldsm_x4(bkl, smem_u32(tKinvLo + offB));
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                mma_bf16(acc_qk[nt], aq, bk + 2 * nt, acc_qk[nt]);
-                mma_bf16(acc_qk[nt], aq, bkl + 2 * nt, acc_qk[nt]);
-                mma_bf16(acc_qk[nt], aql, bk + 2 * nt, acc_qk[nt]);
-                mma_bf16(acc_kk[nt], ak, bk + 2 * nt, acc_kk[nt]);
-                mma_bf16(acc_kk[nt], ak, bkl + 2 * nt, acc_kk[nt]);
-                mma_bf16(acc_kk[nt], akl, bk + 2 * nt, acc_kk[nt]);
-            }
-        }
-    }
-    // The score operands are consumed; their tiles now take packet contents.
-    __syncwarp();
-    tD[dperm_index(4 * lane + 0)] = e_last0;
-    tD[dperm_index(4 * lane + 1)] = e_last1;
-    tD[dperm_index(4 * lane + 2)] = e_last2;
-    tD[dperm_index(4 * lane + 3)] = e_last3;
-    const float beta_r0 = __shfl_sync(0xffffffffu, beta_f, gq);
-    const float beta_r1 = __shfl_sync(0xffffffffu, beta_f, gq + 8);
-#pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int j0 = 8 * nt + 2 * tq;
-#pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int i = gq + 8 * hh;
-            const float q0 = (j0 <= i) ? acc_qk[nt][2 * hh] : 0.f;
-            const float q1 = (j0 + 1 <= i) ? acc_qk[nt][2 * hh + 1] : 0.f;
-            *reinterpret_cast<uint32_t*>(tAQK + sw32_off(i, nt) + 4 * tq) = pack_bf16(q0, q1);
-            const float b = hh ? beta_r1 : beta_r0;
-            const float r0 = (j0 < i) ? b * acc_kk[nt][2 * hh] : 0.f;
-            const float r1 = (j0 + 1 < i) ? b * acc_kk[nt][2 * hh + 1] : 0.f;
-            *reinterpret_cast<float2*>(tR + 16 * i + j0) = make_float2(r0, r1);
-        }
-    }
-
-    // ---- 5. K^end^T (key rows x token columns) by transposing 8 x 8 blocks.
-#pragma unroll
-    for (int p = 0; p < 8; ++p) {
-        const int mi = lane >> 3;
-        const int tok = 8 * (mi & 1) + (lane & 7);
-        const int grp = 2 * p + (mi >> 1);
-        uint32_t r[4];
-        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                     : "r"(smem_u32(tKen + sw128_off(16, tok, grp))));
-#pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int key = 8 * (2 * p + (b >> 1)) + (lane >> 2);
-            const int half = b & 1;
-            *reinterpret_cast<uint32_t*>(tKE + sw32_off(key, half) + 4 * (lane & 3)) = r[b];
-        }
-    }
-    __syncwarp();
-
-    // ---- 6. A^kk = (I + R)^{-1} by forward substitution; lane m owns column m.
-    if (lane < kChunk) {
-        float x[kChunk];
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) x[i] = 0.f;
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            float acc = (i == lane) ? 1.f : 0.f;
-#pragma unroll
-            for (int jj = 0; jj < (i + 3) / 4; ++jj) {
-                const float4 rr = *reinterpret_cast<const float4*>(tR + 16 * i + 4 * jj);
-                acc -= rr.x * x[4 * jj + 0];
-                acc -= rr.y * x[4 * jj + 1];
-                acc -= rr.z * x[4 * jj + 2];
-                acc -= rr.w * x[4 * jj + 3];
-            }
-            x[i] = acc;
-        }
-        // Column `lane` of A^kk B (scaled by beta_lane), as BF16 high and low parts.
-#pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            const float a = x[i] * beta_f;
-            const __nv_bfloat16 hi = __float2bfloat16_rn(a);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
-            const uint32_t off = sw32_off(i, lane >> 3) + 2 * (lane & 7);
-            *reinterpret_cast<__nv_bfloat16*>(tAKB + off) = hi;
-            *reinterpret_cast<__nv_bfloat16*>(sc + kPrepOffAkbLo + off) = lo;
-        }
-    }
-    __syncwarp();
-
-    // ---- 7. K' = -(A^kk B) K^start^T (16 tokens x 128 keys), so that the
-    // recurrence gets U^T = (A^kk B) V^T + K' S^T from one contraction over
-    // the keys: (V - S K^start)(A^kk B)^T = V (A^kk B)^T - S (K^start (A^kk B)^T).
-    // hi*hi + hi*lo + lo*hi of the split operands, FP32 accumulation; it then
-    // replaces K^start in the packet.
-    {
-        uint32_t ah[4], al[4];
-        const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
-        ldsm_x4(ah, smem_u32(tAKB + sw32_off(rowA, lane >> 4)));
-        ldsm_x4(al, smem_u32(sc + kPrepOffAkbLo + sw32_off(rowA, lane >> 4)));
-        const int mi = lane >> 3;
-        const int tok = 8 * (mi & 1) + (lane & 7);
-        float acc[16][4];
-#pragma unroll
-        for (int p = 0; p < 8; ++p) {
-            // B fragments (k = token, n = key) of two 8-key tiles from the token-row tiles.
-            uint32_t bh[4], bl[4];
-            const uint32_t off = sw128_off(16, tok, 2 * p + (mi >> 1));
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(bh[0]), "=r"(bh[1]), "=r"(bh[2]), "=r"(bh[3])
-                         : "r"(smem_u32(tKS + off)));
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(bl[0]), "=r"(bl[1]), "=r"(bl[2]), "=r"(bl[3])
-                         : "r"(smem_u32(tKsLo + off)));
-#pragma unroll
-            for (int half = 0; half < 2; ++half) {
-                float* d = acc[2 * p + half];
-                d[0] = d[1] = d[2] = d[3] = 0.f;
-                mma_bf16(d, ah, bh + 2 * half, d);
-                mma_bf16(d, ah, bl + 2 * half, d);
-                mma_bf16(d, al, bh + 2 * half, d);
-            }
-        }
-        __syncwarp();   // every lane's K^start fragments are in registers
-        const int gq2 = lane >> 2, tq2 = lane & 3;
-#pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
-            *reinterpret_cast<uint32_t*>(tKS + sw128_off(16, gq2, nt) + 4 * tq2) =
-                pack_bf16(-acc[nt][0], -acc[nt][1]);
-            *reinterpret_cast<uint32_t*>(tKS + sw128_off(16, gq2 + 8, nt) + 4 * tq2) =
-                pack_bf16(-acc[nt][2], -acc[nt][3]);
-        }
-    }
-}
+using namespace prep;
 
 __global__ void __launch_bounds__(kPrepWarps * 32, 1)
     prep_kernel(PrepArgs a, const __grid_constant__ PrepMaps maps) {
@@ -381,52 +52,10 @@ __global__ void __launch_bounds__(kPrepWarps * 32, 1)
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    uint8_t* region = smem + warp * kPrepWarpSmem;
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kPrepWarps * kPrepWarpSmem) + warp;
-    if (lane == 0) {
-        mbar_init(bar, 1);
-        fence_barrier_init();
-    }
-    __syncwarp();
-    if (a.geo.cu_chunks && !*a.geo.valid) return;
-
-    const int64_t stride = static_cast<int64_t>(gridDim.x) * kPrepWarps;
-    uint32_t phase = 0;
-    for (int64_t item = static_cast<int64_t>(blockIdx.x) * kPrepWarps + warp;
-         item < a.n_chunk_heads; item += stride) {
-        int64_t t0, len, c, h;
-        if (!item_range(a, item, &t0, &len, &c, &h)) break;   // items only grow past the end
-        if (lane == 0) {
-            // The previous packet store must have read the region before TMA
-            // overwrites it; the region's generic-proxy writes were fenced
-            // (fence.proxy.async) before that store.
-            bulk_wait_read_all();
-            mbar_arrive_expect_tx(bar, kInBytes);
-            const int32_t x = static_cast<int32_t>(h * kHeadDim), y = static_cast<int32_t>(t0);
-            tma_load_2d(region + kInQ, &maps.q, x, y, bar);
-            tma_load_2d(region + kInK, &maps.k, x, y, bar);
-            tma_load_2d(region + kInG, &maps.g, x, y, bar);
-        }
-        const float beta_f = lane < len ? __bfloat162float(a.beta[(t0 + lane) * a.H + h]) : 0.f;
-        if (!mbar_wait_warp_sleep(bar, phase, a.geo.status)) {
-            // The loads may still land: wait for them (bounded) before leaving.
-            mbar_wait_bounded_sleep(bar, phase, a.geo.status);
-            break;
-        }
-        phase ^= 1u;
-        prep_item(region, beta_f, len, a.scale, lane);
-
-        // Publish the packet with one bulk copy.
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
-            bulk_s2g(a.packets + (c * a.H + h) * static_cast<int64_t>(kPacketBytes), region,
-                     kPacketBytes);
-            bulk_commit();
-        }
-    }
-    if (lane == 0) bulk_wait_all();
-    __syncwarp();
+    uint64_t* bar = warp_barrier(smem, warp, lane);
+    run_items(a, maps, smem + warp * kPrepWarpSmem, bar, lane,
+              static_cast<int64_t>(blockIdx.x) * kPrepWarps + warp,
+              static_cast<int64_t>(gridDim.x) * kPrepWarps, nullptr);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 prep_tensor_map_encoder() {
@@ -463,6 +92,20 @@ cudaError_t encode_rows_map(CUtensorMap* map, const void* base, CUtensorMapDataT
 
 }  // namespace
 
+namespace prep {
+cudaError_t encode_maps(PrepMaps* maps, const void* q, const void* k, const float* g,
+                        int64_t tokens, int64_t H) {
+    cudaError_t e = encode_rows_map(&maps->q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, tokens, H);
+    if (e == cudaSuccess)
+        e = encode_rows_map(&maps->k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, tokens, H);
+    if (e == cudaSuccess)
+        e = encode_rows_map(&maps->g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, tokens, H);
+    return e;
+}
+}  // namespace prep
+
+using namespace prep;
+
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const void* beta,
                         uint8_t* packets, const SeqGeometry& geo, int64_t H, float scale,
                         int* status, cudaStream_t stream) {
@@ -477,11 +120,7 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const void
     if (a.n_chunk_heads <= 0 || geo.tokens <= 0) return cudaSuccess;
     if (geo.tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // TMA coordinates are int32
     PrepMaps maps;
-    cudaError_t e = encode_rows_map(&maps.q, q, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, geo.tokens, H);
-    if (e == cudaSuccess)
-        e = encode_rows_map(&maps.k, k, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, geo.tokens, H);
-    if (e == cudaSuccess)
-        e = encode_rows_map(&maps.g, g, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, geo.tokens, H);
+    cudaError_t e = encode_maps(&maps, q, k, g, geo.tokens, H);
     if (e != cudaSuccess) return e;
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;

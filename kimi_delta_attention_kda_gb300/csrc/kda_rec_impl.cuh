@@ -1,0 +1,347 @@
+// kda_rec_impl.cuh -- device code of the recurrence shared by the
+// standalone recurrence kernels (kda_recurrence.cu) and the fused kernel
+// (kda_fused.cu): kernel arguments, small helpers, and the key-split variant.
+#pragma once
+
+#include <cuda.h>
+
+#include "kda_common.cuh"
+#include "kda_launch.h"
+
+namespace kda {
+namespace rec {
+
+struct RecArgs {
+    const __nv_bfloat16* v;
+    __nv_bfloat16* out;
+    const __nv_bfloat16* init_state;
+    __nv_bfloat16* final_state;
+    const uint8_t* packets;
+    SeqGeometry geo;
+    int64_t H;
+    int nsplit;
+    int* status;
+};
+
+__device__ __forceinline__ uint32_t movm_t(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ void st_global_u32_if(void* p, uint32_t v, bool pred) {
+    asm volatile("{\n .reg .pred p;\n setp.ne.b32 p, %2, 0;\n @p st.global.b32 [%0], %1;\n}\n"
+                 ::"l"(p), "r"(v), "r"(static_cast<uint32_t>(pred))
+                 : "memory");
+}
+
+__device__ __forceinline__ float dsel(const float4& a, int i) {
+    return i == 0 ? a.x : (i == 1 ? a.y : (i == 2 ? a.z : a.w));
+}
+
+// ---------------------------------------------------------------------------
+// Key-split variant for heads that get many CTAs (a latency-bound chain per
+// warp).  Each 8-column group of S^T is held by a pair of warps, one per half
+// of the 128 keys, so a warp issues half the operand loads and MMAs of the
+// keys-major form.  Per chunk each warp forms its partial U^T (and partial
+// P^T) over its 64 keys, the pair swaps partials through shared memory behind
+// an mbarrier (bounded wait), and both add them in the same order (key half
+// 0 + key half 1), so both warps continue from identical U^T.  The sums over
+// keys are associated differently from the other variants, so results agree
+// with them to rounding, not bit for bit.
+// ---------------------------------------------------------------------------
+template <int NCG>
+struct KsLayout {
+    static constexpr int kWarps = 2 * NCG;                        // consumer warps
+    static constexpr int kCols = 8 * NCG;                         // value columns per CTA
+    static constexpr int kStages = 8;
+    static constexpr uint32_t kVRowBytes = kCols * 2;
+    static constexpr uint32_t kStageBytes = ((kPacketBytes + kChunk * kVRowBytes + 1023) / 1024) * 1024;
+    // Exchange buffers: [column group][chunk parity][key half][u, p][lane] float4.
+    static constexpr uint32_t kXOff = kStages * kStageBytes;
+    static constexpr uint32_t kXBytes = NCG * 2 * 2 * 2 * 32 * 16;
+    static constexpr uint32_t kBarOff = kXOff + kXBytes;
+    static constexpr uint32_t kSmemBytes = kBarOff + (2 * kStages + NCG) * 8 + 1024;
+};
+
+struct HalfFrags {
+    uint32_t ks[4][4];   // K' k-steps of this key half
+    uint32_t qs[4][4];   // s (Q^start)^T k-steps of this key half
+    uint32_t ke[4][4];   // (K^end)^T key tiles of this key half
+    uint32_t akb[4];
+    uint32_t aqk[4];
+    float4 d[2];         // D for the key tiles of this key half
+    uint32_t vb[2];
+};
+
+__device__ __forceinline__ void ks_load_uq(const uint8_t* stage, int kh, int lane, HalfFrags& f) {
+    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t hiA = lane >> 4;
+    const uint32_t sKS = smem_u32(stage + kOffKS);
+    const uint32_t sQS = smem_u32(stage + kOffQS);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        ldsm_x4(f.ks[i], sKS + sw128_off(16, rowA, 2 * (4 * kh + i) + hiA));
+        ldsm_x4(f.qs[i], sQS + sw128_off(16, rowA, 2 * (4 * kh + i) + hiA));
+    }
+}
+__device__ __forceinline__ void ks_load_rest(const uint8_t* stage, uint32_t vrow_bytes, int cg, int kh,
+                                             int lane, HalfFrags& f) {
+    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t hiA = lane >> 4;
+    const int g8 = lane >> 2;
+    const uint32_t sKE = smem_u32(stage + kOffKE);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) ldsm_x4(f.ke[i], sKE + sw32_off(16 * (4 * kh + i) + rowA, hiA));
+    ldsm_x4(f.akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
+    ldsm_x4(f.aqk, smem_u32(stage + kOffAQK + sw32_off(rowA, hiA)));
+    const uint8_t* sV = stage + kPacketBytes + (lane & 15) * vrow_bytes + 16 * cg;
+    asm volatile("ldmatrix.sync.aligned.m8n8.x2.trans.shared.b16 {%0,%1}, [%2];"
+                 : "=r"(f.vb[0]), "=r"(f.vb[1])
+                 : "r"(smem_u32(sV)));
+    const float4* dp = reinterpret_cast<const float4*>(stage + kOffD) + 4 * g8 + 2 * kh;
+    f.d[0] = dp[0];
+    f.d[1] = dp[1];
+}
+
+template <int NCG>
+__device__ __forceinline__ void ks_setup(uint8_t* smem) {
+    using L = KsLayout<NCG>;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+    uint64_t* empty = full + L::kStages;
+    uint64_t* xbar = empty + L::kStages;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < L::kStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], L::kWarps);
+        }
+        for (int g = 0; g < NCG; ++g) mbar_init(&xbar[g], 64);   // every lane of the pair arrives
+        fence_barrier_init();
+    }
+}
+
+// The CTA's work after ks_setup and a CTA-wide barrier: CTA `block` of the
+// recurrence grid, warps 0 .. 2 NCG (the others do nothing here).  With
+// `ready` set, the producer waits for ready[(chunk) * H + head] before it
+// copies that chunk's packet (the packets are being written by the
+// preparation running in the same launch).
+template <int NCG>
+__device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap, uint8_t* smem,
+                                       int64_t block, const uint32_t* ready) {
+    using L = KsLayout<NCG>;
+    constexpr int kStages = L::kStages;
+    constexpr int kWarps = L::kWarps;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
+    uint64_t* empty = full + kStages;
+    uint64_t* xbar = empty + kStages;   // one per column group
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t nh = block / a.nsplit;
+    const int split = static_cast<int>(block - nh * a.nsplit);
+    const int64_t n = nh / a.H;
+    const int64_t h = nh - n * a.H;
+    const int v0 = split * L::kCols;
+
+    int64_t c_begin, nch, tok0, seqlen;
+    if (a.geo.cu_chunks) {
+        if (!*a.geo.valid) return;
+        c_begin = a.geo.cu_chunks[n];
+        nch = a.geo.cu_chunks[n + 1] - c_begin;
+        tok0 = a.geo.cu_seqlens[n];
+        seqlen = a.geo.cu_seqlens[n + 1] - tok0;
+    } else {
+        c_begin = n * a.geo.chunks_per_seq;
+        nch = a.geo.chunks_per_seq;
+        tok0 = n * a.geo.tokens_per_seq;
+        seqlen = a.geo.tokens_per_seq;
+    }
+
+    if (warp > kWarps) return;
+    if (warp == kWarps) {
+        // ------------------------------------------------------------ producer
+        uint32_t fill_parity = 0, filled = 0;
+        uint32_t ready_mask = 0;   // bit i: chunk ready_base + i seen ready
+        int64_t ready_base = 0;
+        bool ok = true;
+        for (int64_t c = 0; c < nch && ok; ++c) {
+            const int s = static_cast<int>(c % kStages);
+            if (c >= kStages)
+                ok = mbar_wait_warp_sleep(&empty[s], ((c / kStages) - 1) & 1, a.status);
+            if (!ok) break;
+            uint8_t* stage = smem + s * L::kStageBytes;
+            if (ready && !((c - ready_base) < 32 && (ready_mask >> (c - ready_base)) & 1u)) {
+                // Poll the flags of chunks c .. c + 31 at once (lane i: chunk
+                // c + i) until chunk c's is set; one proxy fence then orders
+                // every copy of a chunk seen ready here after its packet.
+                ready_base = c;
+                const long long t0 = clock64();
+                for (;;) {
+                    const int64_t cc = c + lane;
+                    const uint32_t flag =
+                        cc < nch ? ld_acquire_gpu(ready + (c_begin + cc) * a.H + h) : 0u;
+                    ready_mask = __ballot_sync(0xffffffffu, flag != 0u);
+                    if (ready_mask & 1u) break;
+                    if (__shfl_sync(0xffffffffu, clock64() - t0 > kWaitBoundCycles, 0)) {
+                        if (lane == 0) atomicOr(a.status, kDevPipeTimeout);
+                        ok = false;
+                        break;
+                    }
+                    __nanosleep(256);
+                }
+                if (!ok) break;
+                if (lane == 0) fence_proxy_async_global();
+            }
+            if (lane == 0) {
+                mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * L::kVRowBytes);
+                bulk_g2s(stage, a.packets + ((c_begin + c) * a.H + h) * static_cast<int64_t>(kPacketBytes),
+                         kPacketBytes, &full[s]);
+                tma_load_2d(stage + kPacketBytes, vmap, static_cast<int32_t>(h * kHeadDim + v0),
+                            static_cast<int32_t>(tok0 + kChunk * c), &full[s]);
+            }
+            __syncwarp();
+            fill_parity ^= (filled >> s & 1u) << s;
+            filled |= 1u << s;
+        }
+        if (!ok)
+            for (int s = 0; s < kStages; ++s)
+                if (filled >> s & 1u) mbar_wait_bounded(&full[s], (fill_parity >> s) & 1u, a.status);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int cg = warp >> 1;     // column group
+    const int kh = warp & 1;      // key half
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int vcol = v0 + 8 * cg;
+    const int64_t state_base = (n * a.H + h) * kHeadDim * kHeadDim;
+    float4* xb = reinterpret_cast<float4*>(smem + L::kXOff) + cg * (2 * 2 * 2 * 32);
+
+    // S^T rows (keys) of this half: tile i covers keys 16 (4 kh + i) + {g8, g8 + 8}.
+    float Sf[4][4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        if (a.init_state) {
+            const __nv_bfloat16* src = a.init_state + state_base;
+            const int key = 16 * (4 * kh + i) + g8;
+            const int val = vcol + 2 * t4;
+            Sf[i][0] = __bfloat162float(src[(int64_t)val * kHeadDim + key]);
+            Sf[i][1] = __bfloat162float(src[(int64_t)(val + 1) * kHeadDim + key]);
+            Sf[i][2] = __bfloat162float(src[(int64_t)val * kHeadDim + key + 8]);
+            Sf[i][3] = __bfloat162float(src[(int64_t)(val + 1) * kHeadDim + key + 8]);
+        } else {
+            Sf[i][0] = Sf[i][1] = Sf[i][2] = Sf[i][3] = 0.f;
+        }
+    }
+    uint32_t Sb[4][2];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        Sb[i][0] = movm_t(pack_bf16(Sf[i][0], Sf[i][1]));
+        Sb[i][1] = movm_t(pack_bf16(Sf[i][2], Sf[i][3]));
+    }
+
+    bool ok = true;
+    HalfFrags f;
+    if (nch > 0) {
+        ok = mbar_wait_warp(&full[0], 0, a.status);
+        if (ok) {
+            ks_load_uq(smem, kh, lane, f);
+            ks_load_rest(smem, L::kVRowBytes, cg, kh, lane, f);
+        }
+    }
+    for (int64_t c = 0; c < nch && ok; ++c) {
+        const int s = static_cast<int>(c % kStages);
+        const bool has_next = c + 1 < nch;
+        const int s1 = static_cast<int>((c + 1) % kStages);
+        const uint32_t par1 = static_cast<uint32_t>(((c + 1) / kStages) & 1);
+        const uint8_t* stage1 = smem + s1 * L::kStageBytes;
+        bool next_ready = has_next && mbar_try_wait(&full[s1], par1);
+        int64_t len = seqlen - kChunk * c;
+        if (len > kChunk) len = kChunk;
+
+        // Partial U^T and P^T over this warp's 64 keys, from the incoming state.
+        float ua[4] = {0.f, 0.f, 0.f, 0.f}, ub[4] = {0.f, 0.f, 0.f, 0.f};
+        float pa[4] = {0.f, 0.f, 0.f, 0.f}, pb[4] = {0.f, 0.f, 0.f, 0.f};
+        if (kh == 0) mma_bf16(ua, f.akb, f.vb, ua);
+#pragma unroll
+        for (int i = 0; i < 4; i += 2) {
+            mma_bf16(ua, f.ks[i], Sb[i], ua);
+            mma_bf16(ub, f.ks[i + 1], Sb[i + 1], ub);
+            mma_bf16(pa, f.qs[i], Sb[i], pa);
+            mma_bf16(pb, f.qs[i + 1], Sb[i + 1], pb);
+        }
+        const int slot = static_cast<int>(c & 1);
+        float4* mine = xb + ((slot * 2 + kh) * 2) * 32 + lane;
+        const float4* theirs = xb + ((slot * 2 + (kh ^ 1)) * 2) * 32 + lane;
+        mine[0] = make_float4(ua[0] + ub[0], ua[1] + ub[1], ua[2] + ub[2], ua[3] + ub[3]);
+        mine[32] = make_float4(pa[0] + pb[0], pa[1] + pb[1], pa[2] + pb[2], pa[3] + pb[3]);
+        mbar_arrive(&xbar[cg]);
+        // D S^T for this half, in place (the BF16 copy is in Sb).
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const float d0 = dsel(f.d[i >> 1], 2 * (i & 1));
+            const float d1 = dsel(f.d[i >> 1], 2 * (i & 1) + 1);
+            Sf[i][0] *= d0;
+            Sf[i][1] *= d0;
+            Sf[i][2] *= d1;
+            Sf[i][3] *= d1;
+        }
+        // The K' and Q^start fragments are dead: load the next chunk's.
+        if (has_next) {
+            if (!__all_sync(0xffffffffu, next_ready))
+                next_ready = mbar_wait_warp(&full[s1], par1, a.status);
+            if (next_ready)
+                ks_load_uq(stage1, kh, lane, f);
+            else
+                ok = false;
+        }
+        // The partner's partials (phase c of the pair barrier).
+        const bool xok = mbar_wait_warp(&xbar[cg], static_cast<uint32_t>(c & 1), a.status);
+        ok = ok && xok;
+        float u[4], pp[4];
+        {
+            const float4 tu = theirs[0], tp = theirs[32];
+            const float4 mu = mine[0], mp = mine[32];
+            // Key half 0 + key half 1, in that order, in both warps.
+            const float4 u0 = kh == 0 ? mu : tu, u1 = kh == 0 ? tu : mu;
+            const float4 p0 = kh == 0 ? mp : tp, p1 = kh == 0 ? tp : mp;
+            u[0] = u0.x + u1.x; u[1] = u0.y + u1.y; u[2] = u0.z + u1.z; u[3] = u0.w + u1.w;
+            pp[0] = p0.x + p1.x; pp[1] = p0.y + p1.y; pp[2] = p0.z + p1.z; pp[3] = p0.w + p1.w;
+        }
+        uint32_t Ub[2];
+        Ub[0] = movm_t(pack_bf16(u[0], u[1]));
+        Ub[1] = movm_t(pack_bf16(u[2], u[3]));
+        // S^T <- D S^T + (K^end)^T U^T for this half.
+#pragma unroll
+        for (int i = 0; i < 4; ++i) mma_bf16(Sf[i], f.ke[i], Ub, Sf[i]);
+        float o[4];
+        mma_bf16(o, f.aqk, Ub, pp);
+        if (has_next && ok) ks_load_rest(stage1, L::kVRowBytes, cg, kh, lane, f);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            Sb[i][0] = movm_t(pack_bf16(Sf[i][0], Sf[i][1]));
+            Sb[i][1] = movm_t(pack_bf16(Sf[i][2], Sf[i][3]));
+        }
+        __syncwarp();
+        mbar_arrive_if(&empty[s], lane == 0);
+        // Key half 0 stores tokens 0-7 of O, key half 1 tokens 8-15.
+        const int tok = 8 * kh + g8;
+        __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + tok) * a.H + h) * kHeadDim + vcol + 2 * t4;
+        st_global_u32_if(orow, kh == 0 ? pack_bf16(o[0], o[1]) : pack_bf16(o[2], o[3]), tok < len);
+    }
+
+    if (ok && a.final_state) {
+        __nv_bfloat16* dst = a.final_state + state_base;
+#pragma unroll
+        for (int i = 0; i < 4; ++i) {
+            const int key = 16 * (4 * kh + i) + g8;
+            const int val = vcol + 2 * t4;
+            dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[i][0]);
+            dst[(int64_t)(val + 1) * kHeadDim + key] = __float2bfloat16_rn(Sf[i][1]);
+            dst[(int64_t)val * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[i][2]);
+            dst[(int64_t)(val + 1) * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[i][3]);
+        }
+    }
+}
+
+}  // namespace rec
+}  // namespace kda

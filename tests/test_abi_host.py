@@ -115,7 +115,8 @@ def test_workspace_bytes(lib):
     pb = _lib.packet_bytes()
     assert pb == 13824
     # fixed: ceil(T/16) chunks per sequence
-    assert _lib.workspace_bytes(2, 40, 3, False) == 2 * 3 * 3 * pb
+    # packets, plus 256-aligned ready flags (one per chunk and head) for a fused launch
+    assert _lib.workspace_bytes(2, 40, 3, False) == 2 * 3 * 3 * pb + 256
     assert _lib.workspace_bytes(1, 0, 5, False) == 0
     # packed: (T + 15 N) // 16 chunks at most, plus the metadata block
     n, T, H = 4, 100, 2

@@ -383,3 +383,49 @@ def test_forced_split_full_t8192_h6(forced_split, nsplit):
     inp = synthetic.make_workload("t8192_h6")
     out, fin = run(forced_split, inp)
     tu.check_against_oracle(inp, out, fin)
+
+
+# ----------------------------------------------------------------------------
+# Preparation and recurrence in one launch (few heads, fixed length)
+# ----------------------------------------------------------------------------
+
+@pytest.fixture
+def fusion_toggle(kda):
+    yield kda
+    kda.set_fusion(True)
+
+
+@pytest.mark.parametrize("B,T,H", [(1, 8192, 6), (2, 300, 3), (1, 256, 1), (3, 100, 2)])
+def test_fused_matches_two_kernels_bitwise(fusion_toggle, B, T, H):
+    kda = fusion_toggle
+    assert kda.plan_fused(B, T, H, False)
+    inp = synthetic.make_inputs(B, T, H, 4000 + T, init_std=0.02)
+    kda.set_fusion(True)
+    fused = run(kda, inp)
+    kda.set_fusion(False)
+    assert not kda.plan_fused(B, T, H, False)
+    split = run(kda, inp)
+    assert torch.equal(fused[0], split[0]) and torch.equal(fused[1], split[1])
+    tu.check_against_oracle(inp, fused[0], fused[1])
+
+
+def test_fused_not_planned_where_it_cannot_run(kda):
+    assert not kda.plan_fused(1, 8192, 96, False)   # one CTA per head fills the SMs
+    assert not kda.plan_fused(1, 8192, 6, True)      # packed layout
+    assert not kda.plan_fused(1, 0, 6, False)        # no tokens
+
+
+def test_fused_repeated_calls_and_in_place(kda):
+    """Back-to-back fused calls reuse pool memory with stale ready flags in it."""
+    inp = synthetic.make_inputs(1, 2048, 4, 4100, init_std=0.02)
+    assert kda.plan_fused(1, 2048, 4, False)
+    a = run(kda, inp)
+    for _ in range(3):
+        b = run(kda, inp)
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    d = tu.to_device(inp)
+    state = d["init_state"].clone()
+    out, _ = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], state, final_state=state)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    assert torch.equal(out.cpu(), a[0]) and torch.equal(state.cpu(), a[1])
