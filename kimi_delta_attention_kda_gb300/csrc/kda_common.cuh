@@ -200,6 +200,12 @@ __device__ __forceinline__ void tma_load_2d(void* dst, const void* tmap, int32_t
         ::"r"(smem_u32(dst)), "l"(tmap), "r"(x), "r"(y), "r"(smem_u32(bar))
         : "memory");
 }
+// Prefetch of a 2-D tensor-map tile into L2 (no completion to wait for).
+__device__ __forceinline__ void tma_prefetch_l2_2d(const void* tmap, int32_t x, int32_t y) {
+    asm volatile("cp.async.bulk.prefetch.tensor.2d.L2.global.tile [%0, {%1, %2}];"
+                 ::"l"(tmap), "r"(x), "r"(y)
+                 : "memory");
+}
 // One-dimensional bulk copy shared -> global (bulk-group completion).
 __device__ __forceinline__ void bulk_s2g(void* dst, const void* src, uint32_t bytes) {
     asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst),

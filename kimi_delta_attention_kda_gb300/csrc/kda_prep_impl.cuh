@@ -62,6 +62,16 @@ __device__ __forceinline__ int64_t find_sequence(const int64_t* cu_chunks, int64
     return lo;
 }
 
+constexpr float kLog2e = 1.4426950408889634f;
+
+// 2^x by the hardware's approximate base-2 exponential (relative error about
+// 2^-22 over the range used here, |x| <= 16 * 5 * log2(e)).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
 // Store 4 consecutive BF16 (channels 4*lane .. 4*lane+3) of token row t into a
 // [16][128] SW128 tile.
 __device__ __forceinline__ void st_row4(uint8_t* tile, int t, int lane, float a, float b, float c,
@@ -139,10 +149,11 @@ __device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t
         const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
         qv[t] = live ? qq : make_uint2(0u, 0u);
         kv[t] = live ? kq : make_uint2(0u, 0u);
-        run0 += live ? gg.x : 0.f;
-        run1 += live ? gg.y : 0.f;
-        run2 += live ? gg.z : 0.f;
-        run3 += live ? gg.w : 0.f;
+        // G is kept in base-2 units (G log2(e)), so each exponential below is one ex2.
+        run0 += live ? gg.x * kLog2e : 0.f;
+        run1 += live ? gg.y * kLog2e : 0.f;
+        run2 += live ? gg.z * kLog2e : 0.f;
+        run3 += live ? gg.w * kLog2e : 0.f;
         G[t][0] = run0;
         G[t][1] = run1;
         G[t][2] = run2;
@@ -172,24 +183,24 @@ __device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t
     }
     const float rnorm = rsqrtf(red[0] + 1e-6f);   // lane < 16: 1/|q_lane|, else 1/|k_(lane-16)|
 
-    // ---- 3. Decayed operands.
-    const float e_last0 = __expf(G[kChunk - 1][0]), e_last1 = __expf(G[kChunk - 1][1]);
-    const float e_last2 = __expf(G[kChunk - 1][2]), e_last3 = __expf(G[kChunk - 1][3]);
-    const float s = scale;
+    // ---- 3. Decayed operands (the scale s rides on the q norm factor).
+    const float e_last0 = ex2_approx(G[kChunk - 1][0]), e_last1 = ex2_approx(G[kChunk - 1][1]);
+    const float e_last2 = ex2_approx(G[kChunk - 1][2]), e_last3 = ex2_approx(G[kChunk - 1][3]);
+    const float rnorm_q = lane < kChunk ? scale * rnorm : rnorm;
 #pragma unroll
     for (int t = 0; t < kChunk; ++t) {
-        const float rq = __shfl_sync(0xffffffffu, rnorm, t);
+        const float rq = __shfl_sync(0xffffffffu, rnorm_q, t);
         const float rk = __shfl_sync(0xffffffffu, rnorm, kChunk + t);
         const float kh0 = bf16_lo(kv[t].x) * rk, kh1 = bf16_hi(kv[t].x) * rk;
         const float kh2 = bf16_lo(kv[t].y) * rk, kh3 = bf16_hi(kv[t].y) * rk;
         const float qh0 = bf16_lo(qv[t].x) * rq, qh1 = bf16_hi(qv[t].x) * rq;
         const float qh2 = bf16_lo(qv[t].y) * rq, qh3 = bf16_hi(qv[t].y) * rq;
-        const float e0 = __expf(G[t][0]), e1 = __expf(G[t][1]);
-        const float e2 = __expf(G[t][2]), e3 = __expf(G[t][3]);
-        const float i0 = __expf(-G[t][0]), i1 = __expf(-G[t][1]);
-        const float i2 = __expf(-G[t][2]), i3 = __expf(-G[t][3]);
+        const float e0 = ex2_approx(G[t][0]), e1 = ex2_approx(G[t][1]);
+        const float e2 = ex2_approx(G[t][2]), e3 = ex2_approx(G[t][3]);
+        const float i0 = ex2_approx(-G[t][0]), i1 = ex2_approx(-G[t][1]);
+        const float i2 = ex2_approx(-G[t][2]), i3 = ex2_approx(-G[t][3]);
         st_row4_split(tKS, tKsLo, t, lane, e0 * kh0, e1 * kh1, e2 * kh2, e3 * kh3);
-        st_row4_split(tQS, tQsLo, t, lane, s * e0 * qh0, s * e1 * qh1, s * e2 * qh2, s * e3 * qh3);
+        st_row4_split(tQS, tQsLo, t, lane, e0 * qh0, e1 * qh1, e2 * qh2, e3 * qh3);
         st_row4_split(tKinv, tKinvLo, t, lane, i0 * kh0, i1 * kh1, i2 * kh2, i3 * kh3);
         st_row4(tKen, t, lane, (e_last0 * i0) * kh0, (e_last1 * i1) * kh1,
                 (e_last2 * i2) * kh2, (e_last3 * i3) * kh3);
@@ -381,6 +392,15 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
             tma_load_2d(region + kInQ, &maps.q, x, y, bar);
             tma_load_2d(region + kInK, &maps.k, x, y, bar);
             tma_load_2d(region + kInG, &maps.g, x, y, bar);
+            // This warp's next item: its tiles on their way to L2 while this
+            // item is worked on, so that its loads above find them there.
+            int64_t nt0, nlen, nc, nh;
+            if (item + stride < a.n_chunk_heads && item_range(a, item + stride, &nt0, &nlen, &nc, &nh)) {
+                const int32_t nx = static_cast<int32_t>(nh * kHeadDim), ny = static_cast<int32_t>(nt0);
+                tma_prefetch_l2_2d(&maps.q, nx, ny);
+                tma_prefetch_l2_2d(&maps.k, nx, ny);
+                tma_prefetch_l2_2d(&maps.g, nx, ny);
+            }
             if (ready && pending >= 0) {
                 // The previous packet is complete in global memory: publish it.
                 bulk_wait_all();
