@@ -69,13 +69,16 @@ REC_SOURCES = ("kda_recurrence.cu", "kda_rec_impl.cuh", "kda_common.cuh")
 PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
 FUSED_SOURCES = ("kda_fused.cu", "kda_prep_impl.cuh", "kda_rec_impl.cuh", "kda_common.cuh")
 PROFILED_TRAFFIC = {
+    ("fused", "t8192_h6"): (75.876e6, FUSED_SOURCES, "47d2052912ab1610"),
+    ("recurrence", "t8192_h96"): (1068.165e6, REC_SOURCES, "cd39cd347978aee2"),
+    ("chunk_prep", "t8192_h96"): (1445.243e6, PREP_SOURCES, "223d2dc525b8082b"),
 }
 
 
 def profiled_traffic(kernel, workload, engine):
     import hashlib
     entry = PROFILED_TRAFFIC.get((kernel, workload))
-    if entry is None or (kernel == "recurrence" and engine == 2):
+    if entry is None or engine != 0:   # the figures are for the default kernels
         return None
     nbytes, files, digest = entry
     h = hashlib.sha256()
