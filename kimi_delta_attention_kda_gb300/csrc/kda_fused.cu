@@ -53,11 +53,12 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         __syncthreads();
         ks_run<NCG>(f.r, &vmap, smem, blockIdx.x, f.ready);
     } else {
-        uint64_t* bar = prep::warp_barrier(smem, warp, lane);
+        const int pair = warp >> 1, hw = warp & 1, bid = 1 + pair;
+        uint64_t* bar = prep::pair_barrier(smem, pair, hw, lane, bid);
         const int64_t pb = static_cast<int64_t>(blockIdx.x) - f.rec_blocks;
         const int64_t pgrid = static_cast<int64_t>(gridDim.x) - f.rec_blocks;
-        prep::run_items(f.p, maps, smem + warp * prep::kPrepWarpSmem, bar, lane,
-                        pb * prep::kPrepWarps + warp, pgrid * prep::kPrepWarps, f.ready);
+        prep::run_items(f.p, maps, smem + pair * prep::kPrepRegion, bar, bid, hw, lane,
+                        pb * prep::kPrepPairs + pair, pgrid * prep::kPrepPairs, f.ready);
     }
 }
 

@@ -1,7 +1,7 @@
 // kda_prep.cu -- chunk preparation for KDA prefill (sm_103a).
 //
-// One warp prepares one (chunk, head): 16 tokens of q, k, g and beta in, one
-// packet (kda_common.cuh) out.  Following "FlashKDA column split", section 1,
+// A pair of warps prepares one (chunk, head): 16 tokens of q, k, g and beta
+// in, one packet (kda_common.cuh) out.  Following "FlashKDA column split", section 1,
 // for tokens i = 0..15 of the chunk and key channel c:
 //   qhat, khat    per-token L2 normalisation (flashinfer kda_prefill,
 //                 use_qk_l2norm_in_kernel): x / sqrt(sum x^2 + 1e-6)
@@ -25,12 +25,13 @@
 // Tokens past the end of a sequence (a ragged last chunk) are zero: q = k = 0,
 // g = 0, beta = 0.  They then contribute nothing to any output or state.
 //
-// The kernel is persistent: every warp walks a strided list of (chunk, head)
-// items through one shared-memory region: 2-D TMA loads of the item's q, k
-// and g tiles, the item's work (the region turns into scratch once the inputs
-// are in registers, then into the packet image), and one bulk copy of the
-// packet to global memory, which must have read the region before the next
-// item's loads overwrite it.
+// The kernel is persistent (two CTAs of 4 warp pairs per SM): every pair walks
+// a strided list of (chunk, head) items through one shared-memory region
+// (kda_prep_impl.cuh has the split of the work between the two warps): 2-D
+// TMA loads of the item's q, k and g tiles, the item's work (the region turns
+// into scratch once the inputs are in registers, then into the packet image),
+// and one bulk copy of the packet to global memory, which must have read the
+// region before the next item's loads overwrite it.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -45,17 +46,18 @@ namespace {
 
 using namespace prep;
 
-__global__ void __launch_bounds__(kPrepWarps * 32, 1)
+__global__ void __launch_bounds__(kPrepWarps * 32, 2)
     prep_kernel(PrepArgs a, const __grid_constant__ PrepMaps maps) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+        (reinterpret_cast<uintptr_t>(smem_raw) + 127) & ~static_cast<uintptr_t>(127));
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    uint64_t* bar = warp_barrier(smem, warp, lane);
-    run_items(a, maps, smem + warp * kPrepWarpSmem, bar, lane,
-              static_cast<int64_t>(blockIdx.x) * kPrepWarps + warp,
-              static_cast<int64_t>(gridDim.x) * kPrepWarps, nullptr);
+    const int pair = warp >> 1, hw = warp & 1, bid = 1 + pair;
+    uint64_t* bar = pair_barrier(smem, pair, hw, lane, bid);
+    run_items(a, maps, smem + pair * kPrepRegion, bar, bid, hw, lane,
+              static_cast<int64_t>(blockIdx.x) * kPrepPairs + pair,
+              static_cast<int64_t>(gridDim.x) * kPrepPairs, nullptr);
 }
 
 PFN_cuTensorMapEncodeTiled_v12000 prep_tensor_map_encoder() {
@@ -133,9 +135,9 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const void
     }
     e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    // One CTA per SM (persistent); fewer when there are fewer items than warps.
-    int64_t blocks = (a.n_chunk_heads + kPrepWarps - 1) / kPrepWarps;
-    if (blocks > sms) blocks = sms;
+    // Two CTAs per SM (persistent); fewer when there are fewer items than pairs.
+    int64_t blocks = (a.n_chunk_heads + kPrepPairs - 1) / kPrepPairs;
+    if (blocks > 2 * sms) blocks = 2 * sms;
     prep_kernel<<<static_cast<unsigned>(blocks), kPrepWarps * 32, kPrepSmemBytes, stream>>>(a, maps);
     return cudaGetLastError();
 }

@@ -11,8 +11,14 @@
 namespace kda {
 namespace prep {
 
+// A CTA has 8 warps: 4 pairs.  Each (chunk, head) is prepared by one pair:
+// warp h (0 or 1) of the pair builds the operands of tokens 8 h .. 8 h + 7,
+// and the pair splits the rest (step comments below).  The pair synchronises on its own
+// named barrier at fixed points of the item, so both warps always pass the
+// same barriers.
 constexpr int kPrepWarps = 8;
-// Per-warp shared memory: one 28 KB region that holds, in turn, an item's
+constexpr int kPrepPairs = kPrepWarps / 2;
+// Per-pair shared memory: one 28 KB region that holds, in turn, an item's
 // TMA inputs, its scratch and its packet image:
 //   inputs  : q [16][128] BF16 at 0, k at 4096, g [16][128] FP32 at 8192
 //   scratch : [0,4K) K^start hi (packet KS) | [4K,8K) s Q^start hi (packet QS) |
@@ -32,8 +38,10 @@ constexpr uint32_t kPrepOffQsLo = 20480;
 constexpr uint32_t kPrepOffKen = 24576;
 constexpr uint32_t kPrepOffAkbLo = 20480;     // 16 x 16 BF16 SW32, after the score MMAs
 constexpr uint32_t kPrepOffR = 21504;          // 16 x 16 FP32, after the score MMAs
-constexpr uint32_t kPrepWarpSmem = 28672;
-constexpr uint32_t kPrepSmemBytes = kPrepWarps * kPrepWarpSmem + 64 + 1024;  // + barriers, align
+constexpr uint32_t kPrepRegion = 28672;
+// Regions, then one mbarrier per pair; + slack to align the base to 128 bytes
+// (TMA destinations).  Two CTAs fit on an SM.
+constexpr uint32_t kPrepSmemBytes = kPrepPairs * kPrepRegion + kPrepPairs * 8 + 128;
 
 struct PrepArgs {
     const __nv_bfloat16* beta;
@@ -72,24 +80,42 @@ __device__ __forceinline__ float ex2_approx(float x) {
     return y;
 }
 
-// Store 4 consecutive BF16 (channels 4*lane .. 4*lane+3) of token row t into a
-// [16][128] SW128 tile.
+// Byte offset of channels 4 lane .. 4 lane + 3 of token row t in a [16][128]
+// BF16 SW128 tile.
+__device__ __forceinline__ uint32_t row4_off(int t, int lane) {
+    return sw128_off(16, t, (4 * lane) >> 3) + ((lane & 1) << 3);
+}
+// Store 4 BF16 (channels 4 lane .. 4 lane + 3) of token row t.
 __device__ __forceinline__ void st_row4(uint8_t* tile, int t, int lane, float a, float b, float c,
                                         float d) {
-    uint32_t off = sw128_off(16, t, (4 * lane) >> 3) + ((lane & 1) << 3);
-    uint2 v = make_uint2(pack_bf16(a, b), pack_bf16(c, d));
-    *reinterpret_cast<uint2*>(tile + off) = v;
+    *reinterpret_cast<uint2*>(tile + row4_off(t, lane)) = make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
 // Same, storing the BF16 rounding in `hi` and the BF16 rounding of what it
 // left out in `lo`, so that hi + lo carries about 16 significant bits.
 __device__ __forceinline__ void st_row4_split(uint8_t* hi, uint8_t* lo, int t, int lane, float a,
                                               float b, float c, float d) {
-    uint32_t off = sw128_off(16, t, (4 * lane) >> 3) + ((lane & 1) << 3);
+    const uint32_t off = row4_off(t, lane);
     const uint32_t h0 = pack_bf16(a, b), h1 = pack_bf16(c, d);
     const uint32_t l0 = pack_bf16(a - bf16_lo(h0), b - bf16_hi(h0));
     const uint32_t l1 = pack_bf16(c - bf16_lo(h1), d - bf16_hi(h1));
     *reinterpret_cast<uint2*>(hi + off) = make_uint2(h0, h1);
     *reinterpret_cast<uint2*>(lo + off) = make_uint2(l0, l1);
+}
+
+// Named barrier of a warp pair (64 threads).
+__device__ __forceinline__ void pair_sync(int id) {
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+// The same barrier, returning whether `p` holds in every thread of the pair.
+__device__ __forceinline__ bool pair_all(int id, bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred q, a;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred a, %2, 64, q;\n"
+        " selp.u32 %0, 1, 0, a;\n}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(p)), "r"(id)
+        : "memory");
+    return r != 0;
 }
 
 // Token range [t0, t0 + len) of item (chunk c, head h); false when the item
@@ -115,10 +141,11 @@ __device__ __forceinline__ bool item_range(const PrepArgs& a, int64_t item, int6
     return true;
 }
 
-// One (chunk, head): inputs from the TMA tiles in `in`, packet image to `pk`,
-// scratch in `in` once the inputs are in registers.
-__device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t len, float scale,
-                                          int lane) {
+// One (chunk, head) by warp `hw` of a pair (named barrier `bid`): inputs from
+// the TMA tiles in `region`, scratch in `region` once the inputs are in
+// registers, packet image in `region` at the end.
+__device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, float beta_f,
+                                          int64_t len, float scale, int lane) {
     const uint8_t* in = region;
     uint8_t* ws = region;
     uint8_t* sc = region;
@@ -134,45 +161,76 @@ __device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t
     uint8_t* tQsLo = sc + kPrepOffQsLo;
     uint8_t* tKen = sc + kPrepOffKen;
     float* tR = reinterpret_cast<float*>(sc + kPrepOffR);
+    const int tb = 8 * hw;   // this warp's tokens in steps 1-3: tb .. tb + 7
 
-    // ---- 1. q, k (BF16, 4 channels per lane), g (running sum -> G) from the
-    // tiles; tokens past the end of the sequence read as zero.
-    uint2 qv[kChunk], kv[kChunk];
-    float G[kChunk][4];
-    float red[2 * kChunk];   // partial sums of squares: q tokens 0..15, k tokens 0..15
-    float run0 = 0.f, run1 = 0.f, run2 = 0.f, run3 = 0.f;
+    // ---- 1. Lane l owns key channels 4 l .. 4 l + 3.  g's running sum (G, in
+    // base-2 units so that each exponential below is one ex2) over all 16
+    // tokens, keeping this warp's 8 tokens and G_15; q and k of this warp's 8
+    // tokens.  Tokens past the end of the sequence read as zero.
+    uint2 qv[8], kv[8];
+    float G[8][4];
+    float gl[4];             // G_15
+    float red[16];           // partial sums of squares: q tokens tb..tb+7, k tokens tb..tb+7
+    {
+        float r0 = 0.f, r1 = 0.f, r2 = 0.f, r3 = 0.f;
+        if (hw == 1) {
 #pragma unroll
-    for (int t = 0; t < kChunk; ++t) {
-        const bool live = t < len;
-        const uint2 qq = *reinterpret_cast<const uint2*>(in + kInQ + t * 256 + 8 * lane);
-        const uint2 kq = *reinterpret_cast<const uint2*>(in + kInK + t * 256 + 8 * lane);
-        const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
-        qv[t] = live ? qq : make_uint2(0u, 0u);
-        kv[t] = live ? kq : make_uint2(0u, 0u);
-        // G is kept in base-2 units (G log2(e)), so each exponential below is one ex2.
-        run0 += live ? gg.x * kLog2e : 0.f;
-        run1 += live ? gg.y * kLog2e : 0.f;
-        run2 += live ? gg.z * kLog2e : 0.f;
-        run3 += live ? gg.w * kLog2e : 0.f;
-        G[t][0] = run0;
-        G[t][1] = run1;
-        G[t][2] = run2;
-        G[t][3] = run3;
-        const float q0 = bf16_lo(qv[t].x), q1 = bf16_hi(qv[t].x), q2 = bf16_lo(qv[t].y),
-                    q3 = bf16_hi(qv[t].y);
-        const float k0 = bf16_lo(kv[t].x), k1 = bf16_hi(kv[t].x), k2 = bf16_lo(kv[t].y),
-                    k3 = bf16_hi(kv[t].y);
-        red[t] = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
-        red[kChunk + t] = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
+            for (int t = 0; t < 8; ++t) {
+                const bool live = t < len;
+                const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
+                r0 += live ? gg.x * kLog2e : 0.f;
+                r1 += live ? gg.y * kLog2e : 0.f;
+                r2 += live ? gg.z * kLog2e : 0.f;
+                r3 += live ? gg.w * kLog2e : 0.f;
+            }
+        }
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+            const int t = tb + j;
+            const bool live = t < len;
+            const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
+            r0 += live ? gg.x * kLog2e : 0.f;
+            r1 += live ? gg.y * kLog2e : 0.f;
+            r2 += live ? gg.z * kLog2e : 0.f;
+            r3 += live ? gg.w * kLog2e : 0.f;
+            G[j][0] = r0;
+            G[j][1] = r1;
+            G[j][2] = r2;
+            G[j][3] = r3;
+            const uint2 qq = *reinterpret_cast<const uint2*>(in + kInQ + t * 256 + 8 * lane);
+            const uint2 kq = *reinterpret_cast<const uint2*>(in + kInK + t * 256 + 8 * lane);
+            qv[j] = live ? qq : make_uint2(0u, 0u);
+            kv[j] = live ? kq : make_uint2(0u, 0u);
+            const float q0 = bf16_lo(qv[j].x), q1 = bf16_hi(qv[j].x), q2 = bf16_lo(qv[j].y),
+                        q3 = bf16_hi(qv[j].y);
+            const float k0 = bf16_lo(kv[j].x), k1 = bf16_hi(kv[j].x), k2 = bf16_lo(kv[j].y),
+                        k3 = bf16_hi(kv[j].y);
+            red[j] = q0 * q0 + q1 * q1 + q2 * q2 + q3 * q3;
+            red[8 + j] = k0 * k0 + k1 * k1 + k2 * k2 + k3 * k3;
+        }
+        if (hw == 0) {
+#pragma unroll
+            for (int t = 8; t < kChunk; ++t) {
+                const bool live = t < len;
+                const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
+                r0 += live ? gg.x * kLog2e : 0.f;
+                r1 += live ? gg.y * kLog2e : 0.f;
+                r2 += live ? gg.z * kLog2e : 0.f;
+                r3 += live ? gg.w * kLog2e : 0.f;
+            }
+        }
+        gl[0] = r0;
+        gl[1] = r1;
+        gl[2] = r2;
+        gl[3] = r3;
     }
-    // The input tiles are consumed: from here on the buffer is scratch.
-    __syncwarp();
 
-    // ---- 2. Sums of squares over the 128 channels: butterfly reduce-scatter.
-    // After the step with offset o, element i stands for original index
-    // i + o * (bit o of lane); at the end lane l holds the total of index l.
+    // ---- 2. Sums of squares over the 128 channels: butterfly reduce-scatter
+    // over lane bits 3..0, then the two lane halves.  Lane l ends with the
+    // total of index l & 15 (q of token tb + l for l & 15 < 8, else k of
+    // token tb + (l & 7)).
 #pragma unroll
-    for (int o = 16; o >= 1; o >>= 1) {
+    for (int o = 8; o >= 1; o >>= 1) {
         const bool up = (lane & o) != 0;
 #pragma unroll
         for (int i = 0; i < o; ++i) {
@@ -181,89 +239,105 @@ __device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t
             red[i] = keep + __shfl_xor_sync(0xffffffffu, send, o);
         }
     }
-    const float rnorm = rsqrtf(red[0] + 1e-6f);   // lane < 16: 1/|q_lane|, else 1/|k_(lane-16)|
+    const float tot = red[0] + __shfl_xor_sync(0xffffffffu, red[0], 16);
+    const float rnorm = rsqrtf(tot + 1e-6f);
+    // Both warps have read the input tiles: from here on the region is scratch.
+    pair_sync(bid);
 
-    // ---- 3. Decayed operands (the scale s rides on the q norm factor).
-    const float e_last0 = ex2_approx(G[kChunk - 1][0]), e_last1 = ex2_approx(G[kChunk - 1][1]);
-    const float e_last2 = ex2_approx(G[kChunk - 1][2]), e_last3 = ex2_approx(G[kChunk - 1][3]);
-    const float rnorm_q = lane < kChunk ? scale * rnorm : rnorm;
+    // ---- 3. Decayed operands of this warp's 8 tokens (the scale s rides on
+    // the q norm factor).
+    const float e_last0 = ex2_approx(gl[0]), e_last1 = ex2_approx(gl[1]);
+    const float e_last2 = ex2_approx(gl[2]), e_last3 = ex2_approx(gl[3]);
+    const float rnorm_q = (lane & 15) < 8 ? scale * rnorm : rnorm;
 #pragma unroll
-    for (int t = 0; t < kChunk; ++t) {
-        const float rq = __shfl_sync(0xffffffffu, rnorm_q, t);
-        const float rk = __shfl_sync(0xffffffffu, rnorm, kChunk + t);
-        const float kh0 = bf16_lo(kv[t].x) * rk, kh1 = bf16_hi(kv[t].x) * rk;
-        const float kh2 = bf16_lo(kv[t].y) * rk, kh3 = bf16_hi(kv[t].y) * rk;
-        const float qh0 = bf16_lo(qv[t].x) * rq, qh1 = bf16_hi(qv[t].x) * rq;
-        const float qh2 = bf16_lo(qv[t].y) * rq, qh3 = bf16_hi(qv[t].y) * rq;
-        const float e0 = ex2_approx(G[t][0]), e1 = ex2_approx(G[t][1]);
-        const float e2 = ex2_approx(G[t][2]), e3 = ex2_approx(G[t][3]);
-        const float i0 = ex2_approx(-G[t][0]), i1 = ex2_approx(-G[t][1]);
-        const float i2 = ex2_approx(-G[t][2]), i3 = ex2_approx(-G[t][3]);
+    for (int j = 0; j < 8; ++j) {
+        const int t = tb + j;
+        const float rq = __shfl_sync(0xffffffffu, rnorm_q, j);
+        const float rk = __shfl_sync(0xffffffffu, rnorm, 8 + j);
+        const float kh0 = bf16_lo(kv[j].x) * rk, kh1 = bf16_hi(kv[j].x) * rk;
+        const float kh2 = bf16_lo(kv[j].y) * rk, kh3 = bf16_hi(kv[j].y) * rk;
+        const float qh0 = bf16_lo(qv[j].x) * rq, qh1 = bf16_hi(qv[j].x) * rq;
+        const float qh2 = bf16_lo(qv[j].y) * rq, qh3 = bf16_hi(qv[j].y) * rq;
+        const float e0 = ex2_approx(G[j][0]), e1 = ex2_approx(G[j][1]);
+        const float e2 = ex2_approx(G[j][2]), e3 = ex2_approx(G[j][3]);
+        const float i0 = ex2_approx(-G[j][0]), i1 = ex2_approx(-G[j][1]);
+        const float i2 = ex2_approx(-G[j][2]), i3 = ex2_approx(-G[j][3]);
         st_row4_split(tKS, tKsLo, t, lane, e0 * kh0, e1 * kh1, e2 * kh2, e3 * kh3);
         st_row4_split(tQS, tQsLo, t, lane, e0 * qh0, e1 * qh1, e2 * qh2, e3 * qh3);
         st_row4_split(tKinv, tKinvLo, t, lane, i0 * kh0, i1 * kh1, i2 * kh2, i3 * kh3);
-        st_row4(tKen, t, lane, (e_last0 * i0) * kh0, (e_last1 * i1) * kh1,
-                (e_last2 * i2) * kh2, (e_last3 * i3) * kh3);
+        st_row4(tKen, t, lane, (e_last0 * i0) * kh0, (e_last1 * i1) * kh1, (e_last2 * i2) * kh2,
+                (e_last3 * i3) * kh3);
     }
-    __syncwarp();
+    // Every operand tile is complete.
+    pair_sync(bid);
 
-    // ---- 4. Scores: A^qk = (s Q^start)(K exp(-G))^T and K^start (K exp(-G))^T,
-    // each as hi*hi + hi*lo + lo*hi of the split BF16 operands (FP32 accumulate).
+    // ---- 4. Scores, each as hi*hi + hi*lo + lo*hi of the split BF16 operands
+    // (FP32 accumulate): warp 0 forms K^start (K exp(-G))^T (for R), warp 1
+    // A^qk = (s Q^start)(K exp(-G))^T.
     const int gq = lane >> 2, tq = lane & 3;
-    float acc_qk[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
-    float acc_kk[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
+    float acc[2][4] = {{0.f, 0.f, 0.f, 0.f}, {0.f, 0.f, 0.f, 0.f}};
     {
+        const uint8_t* tA = hw == 0 ? tKS : tQS;
+        const uint8_t* tAlo = hw == 0 ? tKsLo : tQsLo;
         const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
         const uint32_t rowB = (lane & 7) + (lane >> 4) * 8;
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            uint32_t aq[4], ak[4], bk[4], aql[4], akl[4], bkl[4];
+            uint32_t a4[4], b4[4], al4[4], bl4[4];
             const uint32_t offA = sw128_off(16, rowA, 2 * kk + (lane >> 4));
             const uint32_t offB = sw128_off(16, rowB, 2 * kk + ((lane >> 3) & 1));
-            ldsm_x4(aq, smem_u32(tQS + offA));
-            ldsm_x4(ak, smem_u32(tKS + offA));
-            ldsm_x4(bk, smem_u32(tKinv + offB));
-            ldsm_x4(aql, smem_u32(tQsLo + offA));
-            ldsm_x4(akl, smem_u32(tKsLo + offA));
-            ldsm_x4(bkl, smem_u32(tKinvLo + offB));
+            ldsm_x4(a4, smem_u32(tA + offA));
+            ldsm_x4(b4, smem_u32(tKinv + offB));
+            ldsm_x4(al4, smem_u32(tAlo + offA));
+            ldsm_x4(bl4, smem_u32(tKinvLo + offB));
 #pragma unroll
             for (int nt = 0; nt < 2; ++nt) {
-                mma_bf16(acc_qk[nt], aq, bk + 2 * nt, acc_qk[nt]);
-                mma_bf16(acc_qk[nt], aq, bkl + 2 * nt, acc_qk[nt]);
-                mma_bf16(acc_qk[nt], aql, bk + 2 * nt, acc_qk[nt]);
-                mma_bf16(acc_kk[nt], ak, bk + 2 * nt, acc_kk[nt]);
-                mma_bf16(acc_kk[nt], ak, bkl + 2 * nt, acc_kk[nt]);
-                mma_bf16(acc_kk[nt], akl, bk + 2 * nt, acc_kk[nt]);
+                mma_bf16(acc[nt], a4, b4 + 2 * nt, acc[nt]);
+                mma_bf16(acc[nt], a4, bl4 + 2 * nt, acc[nt]);
+                mma_bf16(acc[nt], al4, b4 + 2 * nt, acc[nt]);
             }
         }
     }
-    // The score operands are consumed; their tiles now take packet contents.
-    __syncwarp();
-    tD[dperm_index(4 * lane + 0)] = e_last0;
-    tD[dperm_index(4 * lane + 1)] = e_last1;
-    tD[dperm_index(4 * lane + 2)] = e_last2;
-    tD[dperm_index(4 * lane + 3)] = e_last3;
-    const float beta_r0 = __shfl_sync(0xffffffffu, beta_f, gq);
-    const float beta_r1 = __shfl_sync(0xffffffffu, beta_f, gq + 8);
+    // Every read of the score operands is done; their tiles now take packet contents.
+    pair_sync(bid);
+    if (hw == 0) {
+        tD[dperm_index(4 * lane + 0)] = e_last0;
+        tD[dperm_index(4 * lane + 1)] = e_last1;
+        tD[dperm_index(4 * lane + 2)] = e_last2;
+        tD[dperm_index(4 * lane + 3)] = e_last3;
+        const float beta_r0 = __shfl_sync(0xffffffffu, beta_f, gq);
+        const float beta_r1 = __shfl_sync(0xffffffffu, beta_f, gq + 8);
 #pragma unroll
-    for (int nt = 0; nt < 2; ++nt) {
-        const int j0 = 8 * nt + 2 * tq;
+        for (int nt = 0; nt < 2; ++nt) {
+            const int j0 = 8 * nt + 2 * tq;
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-            const int i = gq + 8 * hh;
-            const float q0 = (j0 <= i) ? acc_qk[nt][2 * hh] : 0.f;
-            const float q1 = (j0 + 1 <= i) ? acc_qk[nt][2 * hh + 1] : 0.f;
-            *reinterpret_cast<uint32_t*>(tAQK + sw32_off(i, nt) + 4 * tq) = pack_bf16(q0, q1);
-            const float b = hh ? beta_r1 : beta_r0;
-            const float r0 = (j0 < i) ? b * acc_kk[nt][2 * hh] : 0.f;
-            const float r1 = (j0 + 1 < i) ? b * acc_kk[nt][2 * hh + 1] : 0.f;
-            *reinterpret_cast<float2*>(tR + 16 * i + j0) = make_float2(r0, r1);
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = gq + 8 * hh;
+                const float b = hh ? beta_r1 : beta_r0;
+                const float r0 = (j0 < i) ? b * acc[nt][2 * hh] : 0.f;
+                const float r1 = (j0 + 1 < i) ? b * acc[nt][2 * hh + 1] : 0.f;
+                *reinterpret_cast<float2*>(tR + 16 * i + j0) = make_float2(r0, r1);
+            }
+        }
+    } else {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt) {
+            const int j0 = 8 * nt + 2 * tq;
+#pragma unroll
+            for (int hh = 0; hh < 2; ++hh) {
+                const int i = gq + 8 * hh;
+                const float q0 = (j0 <= i) ? acc[nt][2 * hh] : 0.f;
+                const float q1 = (j0 + 1 <= i) ? acc[nt][2 * hh + 1] : 0.f;
+                *reinterpret_cast<uint32_t*>(tAQK + sw32_off(i, nt) + 4 * tq) = pack_bf16(q0, q1);
+            }
         }
     }
 
-    // ---- 5. K^end^T (key rows x token columns) by transposing 8 x 8 blocks.
+    // ---- 5. K^end^T (key rows x token columns) of this warp's 64 keys by
+    // transposing 8 x 8 blocks.
 #pragma unroll
-    for (int p = 0; p < 8; ++p) {
+    for (int pp = 0; pp < 4; ++pp) {
+        const int p = 4 * hw + pp;
         const int mi = lane >> 3;
         const int tok = 8 * (mi & 1) + (lane & 7);
         const int grp = 2 * p + (mi >> 1);
@@ -278,44 +352,49 @@ __device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t
             *reinterpret_cast<uint32_t*>(tKE + sw32_off(key, half) + 4 * (lane & 3)) = r[b];
         }
     }
-    __syncwarp();
 
-    // ---- 6. A^kk = (I + R)^{-1} by forward substitution; lane m owns column m.
-    if (lane < kChunk) {
-        float x[kChunk];
+    // ---- 6. A^kk = (I + R)^{-1} by forward substitution (warp 0, which wrote
+    // R; lane m owns column m).
+    if (hw == 0) {
+        __syncwarp();
+        if (lane < kChunk) {
+            float x[kChunk];
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) x[i] = 0.f;
+            for (int i = 0; i < kChunk; ++i) x[i] = 0.f;
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            float acc = (i == lane) ? 1.f : 0.f;
+            for (int i = 0; i < kChunk; ++i) {
+                float a = (i == lane) ? 1.f : 0.f;
 #pragma unroll
-            for (int jj = 0; jj < (i + 3) / 4; ++jj) {
-                const float4 rr = *reinterpret_cast<const float4*>(tR + 16 * i + 4 * jj);
-                acc -= rr.x * x[4 * jj + 0];
-                acc -= rr.y * x[4 * jj + 1];
-                acc -= rr.z * x[4 * jj + 2];
-                acc -= rr.w * x[4 * jj + 3];
+                for (int jj = 0; jj < (i + 3) / 4; ++jj) {
+                    const float4 rr = *reinterpret_cast<const float4*>(tR + 16 * i + 4 * jj);
+                    a -= rr.x * x[4 * jj + 0];
+                    a -= rr.y * x[4 * jj + 1];
+                    a -= rr.z * x[4 * jj + 2];
+                    a -= rr.w * x[4 * jj + 3];
+                }
+                x[i] = a;
             }
-            x[i] = acc;
-        }
-        // Column `lane` of A^kk B (scaled by beta_lane), as BF16 high and low parts.
+            // Column `lane` of A^kk B (scaled by beta_lane), as BF16 high and low parts.
 #pragma unroll
-        for (int i = 0; i < kChunk; ++i) {
-            const float a = x[i] * beta_f;
-            const __nv_bfloat16 hi = __float2bfloat16_rn(a);
-            const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
-            const uint32_t off = sw32_off(i, lane >> 3) + 2 * (lane & 7);
-            *reinterpret_cast<__nv_bfloat16*>(tAKB + off) = hi;
-            *reinterpret_cast<__nv_bfloat16*>(sc + kPrepOffAkbLo + off) = lo;
+            for (int i = 0; i < kChunk; ++i) {
+                const float a = x[i] * beta_f;
+                const __nv_bfloat16 hi = __float2bfloat16_rn(a);
+                const __nv_bfloat16 lo = __float2bfloat16_rn(a - __bfloat162float(hi));
+                const uint32_t off = sw32_off(i, lane >> 3) + 2 * (lane & 7);
+                *reinterpret_cast<__nv_bfloat16*>(tAKB + off) = hi;
+                *reinterpret_cast<__nv_bfloat16*>(sc + kPrepOffAkbLo + off) = lo;
+            }
         }
     }
-    __syncwarp();
+    // A^kk B and K^end^T are complete.
+    pair_sync(bid);
 
-    // ---- 7. K' = -(A^kk B) K^start^T (16 tokens x 128 keys), so that the
-    // recurrence gets U^T = (A^kk B) V^T + K' S^T from one contraction over
-    // the keys: (V - S K^start)(A^kk B)^T = V (A^kk B)^T - S (K^start (A^kk B)^T).
-    // hi*hi + hi*lo + lo*hi of the split operands, FP32 accumulation; it then
-    // replaces K^start in the packet.
+    // ---- 7. K' = -(A^kk B) K^start^T (16 tokens x 128 keys; this warp's 64
+    // keys), so that the recurrence gets U^T = (A^kk B) V^T + K' S^T from one
+    // contraction over the keys: (V - S K^start)(A^kk B)^T = V (A^kk B)^T -
+    // S (K^start (A^kk B)^T).  hi*hi + hi*lo + lo*hi of the split operands,
+    // FP32 accumulation; it then replaces K^start in the packet (each warp
+    // reads and writes only its own 64 key columns).
     {
         uint32_t ah[4], al[4];
         const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
@@ -323,12 +402,12 @@ __device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t
         ldsm_x4(al, smem_u32(sc + kPrepOffAkbLo + sw32_off(rowA, lane >> 4)));
         const int mi = lane >> 3;
         const int tok = 8 * (mi & 1) + (lane & 7);
-        float acc[16][4];
+        float kacc[8][4];
 #pragma unroll
-        for (int p = 0; p < 8; ++p) {
+        for (int pp = 0; pp < 4; ++pp) {
             // B fragments (k = token, n = key) of two 8-key tiles from the token-row tiles.
             uint32_t bh[4], bl[4];
-            const uint32_t off = sw128_off(16, tok, 2 * p + (mi >> 1));
+            const uint32_t off = sw128_off(16, tok, 2 * (4 * hw + pp) + (mi >> 1));
             asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                          : "=r"(bh[0]), "=r"(bh[1]), "=r"(bh[2]), "=r"(bh[3])
                          : "r"(smem_u32(tKS + off)));
@@ -337,7 +416,7 @@ __device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t
                          : "r"(smem_u32(tKsLo + off)));
 #pragma unroll
             for (int half = 0; half < 2; ++half) {
-                float* d = acc[2 * p + half];
+                float* d = kacc[2 * pp + half];
                 d[0] = d[1] = d[2] = d[3] = 0.f;
                 mma_bf16(d, ah, bh + 2 * half, d);
                 mma_bf16(d, ah, bl + 2 * half, d);
@@ -347,42 +426,49 @@ __device__ __forceinline__ void prep_item(uint8_t* region, float beta_f, int64_t
         __syncwarp();   // every lane's K^start fragments are in registers
         const int gq2 = lane >> 2, tq2 = lane & 3;
 #pragma unroll
-        for (int nt = 0; nt < 16; ++nt) {
+        for (int n = 0; n < 8; ++n) {
+            const int nt = 8 * hw + n;
             *reinterpret_cast<uint32_t*>(tKS + sw128_off(16, gq2, nt) + 4 * tq2) =
-                pack_bf16(-acc[nt][0], -acc[nt][1]);
+                pack_bf16(-kacc[n][0], -kacc[n][1]);
             *reinterpret_cast<uint32_t*>(tKS + sw128_off(16, gq2 + 8, nt) + 4 * tq2) =
-                pack_bf16(-acc[nt][2], -acc[nt][3]);
+                pack_bf16(-kacc[n][2], -kacc[n][3]);
         }
     }
+    // The packet image is complete; make it visible to the bulk copy.
+    fence_proxy_async_smem();
+    pair_sync(bid);
 }
 
-
-// Initialise warp `warp`'s mbarrier (lane 0; the warp then syncs).
-__device__ __forceinline__ uint64_t* warp_barrier(uint8_t* smem, int warp, int lane) {
-    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kPrepWarps * kPrepWarpSmem) + warp;
-    if (lane == 0) {
+// Initialise pair `pair`'s mbarrier; both warps of the pair pass its named
+// barrier `bid` afterwards.
+__device__ __forceinline__ uint64_t* pair_barrier(uint8_t* smem, int pair, int hw, int lane,
+                                                  int bid) {
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kPrepPairs * kPrepRegion) + pair;
+    if (hw == 0 && lane == 0) {
         mbar_init(bar, 1);
         fence_barrier_init();
     }
-    __syncwarp();
+    pair_sync(bid);
     return bar;
 }
 
-// One warp's share of the items: items first, first + stride, ... .  With
-// `ready` set, ready[item] becomes 1 (release, GPU scope) once the item's
-// packet is in global memory; the flag of an item is published when the warp
-// has issued the next item's loads, or at the end.
+// A pair's share of the items: items first, first + stride, ... .  Both warps
+// run this loop; warp 0's lane 0 issues the copies.  With `ready` set,
+// ready[item] becomes 1 (release, GPU scope) once the item's packet is in
+// global memory; the flag of an item is published when the pair has issued
+// the next item's loads, or at the end.
 __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& maps, uint8_t* region,
-                                          uint64_t* bar, int lane, int64_t first, int64_t stride,
-                                          uint32_t* ready) {
+                                          uint64_t* bar, int bid, int hw, int lane, int64_t first,
+                                          int64_t stride, uint32_t* ready) {
     int64_t pending = -1;   // item whose packet store is in flight, not yet published
     if (a.geo.cu_chunks && !*a.geo.valid) return;
+    const bool issuer = hw == 0 && lane == 0;
 
     uint32_t phase = 0;
     for (int64_t item = first; item < a.n_chunk_heads; item += stride) {
         int64_t t0, len, c, h;
         if (!item_range(a, item, &t0, &len, &c, &h)) break;   // items only grow past the end
-        if (lane == 0) {
+        if (issuer) {
             // The previous packet store must have read the region before TMA
             // overwrites it; the region's generic-proxy writes were fenced
             // (fence.proxy.async) before that store.
@@ -392,7 +478,7 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
             tma_load_2d(region + kInQ, &maps.q, x, y, bar);
             tma_load_2d(region + kInK, &maps.k, x, y, bar);
             tma_load_2d(region + kInG, &maps.g, x, y, bar);
-            // This warp's next item: its tiles on their way to L2 while this
+            // This pair's next item: its tiles on their way to L2 while this
             // item is worked on, so that its loads above find them there.
             int64_t nt0, nlen, nc, nh;
             if (item + stride < a.n_chunk_heads && item_range(a, item + stride, &nt0, &nlen, &nc, &nh)) {
@@ -410,25 +496,24 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
             }
         }
         const float beta_f = lane < len ? __bfloat162float(a.beta[(t0 + lane) * a.H + h]) : 0.f;
-        if (!mbar_wait_warp_sleep(bar, phase, a.geo.status)) {
+        const bool got = mbar_wait_warp_sleep(bar, phase, a.geo.status);
+        if (!pair_all(bid, got)) {
             // The loads may still land: wait for them (bounded) before leaving.
-            mbar_wait_bounded_sleep(bar, phase, a.geo.status);
+            if (!got) mbar_wait_bounded_sleep(bar, phase, a.geo.status);
             break;
         }
         phase ^= 1u;
-        prep_item(region, beta_f, len, a.scale, lane);
+        prep_item(region, bid, hw, beta_f, len, a.scale, lane);
 
         // Publish the packet with one bulk copy.
-        fence_proxy_async_smem();
-        __syncwarp();
-        if (lane == 0) {
+        if (issuer) {
             bulk_s2g(a.packets + (c * a.H + h) * static_cast<int64_t>(kPacketBytes), region,
                      kPacketBytes);
             bulk_commit();
             pending = item;
         }
     }
-    if (lane == 0) {
+    if (issuer) {
         bulk_wait_all();
         if (ready && pending >= 0) {
             fence_proxy_async_global();
