@@ -103,7 +103,7 @@ int kda_set_split(int nsplit);
 /*
  * Recurrence engine.  0 (default) and 1: the column-split kernel (warp-level
  * m16n8k16 MMAs, state in registers, `nsplit` CTAs per head).  Engine 0 gives
- * each warp 16 value columns at nsplit 1, 8 columns at nsplit 2, and at nsplit
+ * each warp 32 value columns at nsplit 1, 8 columns at nsplit 2, and at nsplit
  * 4, 8 and 16 splits each 8-column group's 128 keys over a pair of warps
  * (their partial sums over keys are added in a fixed order, so results agree
  * with the other variants to rounding, not bit for bit).  Engine 1 gives each

@@ -393,26 +393,29 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 }
 
 // ---------------------------------------------------------------------------
-// Wide variant for one CTA per head: 8 consumer warps of 16 value columns
-// each.  A warp's two 8-column n-tiles share every A-operand fragment, so the
-// CTA reads each chunk's K', Q^start and K^end fragments from shared memory 8
-// times instead of 16 (with 16 narrow warps the shared-memory pipe, not the
-// tensor pipe, limits a chunk step).  Fragments are loaded just before use.
+// Quad-width variant for one CTA per head: 4 consumer warps of 32 value
+// columns (four 8-column n-tiles sharing every A fragment), so the CTA reads
+// each chunk's K', Q^start and K^end fragments from shared memory 4 times
+// rather than once per 8 columns (with 16 warps of 8 columns the
+// shared-memory pipe, not the tensor pipe, limits a chunk step).  The BF16
+// copy of the state is not kept: each k-step converts its slice of the
+// incoming FP32 state just before the U and P MMAs that use it (the same
+// conversions as the other variants, so the results are bitwise theirs).
 // ---------------------------------------------------------------------------
-constexpr int kWideWarps = 8;
-constexpr int kWideStages = 4;
-constexpr uint32_t kWideVRowBytes = kHeadDim * 2;
-constexpr uint32_t kWideStageBytes = ((kPacketBytes + kChunk * kWideVRowBytes + 1023) / 1024) * 1024;
-constexpr uint32_t kWideBarOff = kWideStages * kWideStageBytes;
-constexpr uint32_t kWideSmemBytes = kWideBarOff + 2 * kWideStages * 8 + 1024;
+constexpr uint32_t kQuadVRowBytes = kHeadDim * 2;
+constexpr uint32_t kQuadStageBytes = ((kPacketBytes + kChunk * kQuadVRowBytes + 1023) / 1024) * 1024;
+constexpr int kQuadWarps = 4;
+constexpr int kQuadStages = 6;
+constexpr uint32_t kQuadBarOff = kQuadStages * kQuadStageBytes;
+constexpr uint32_t kQuadSmemBytes = kQuadBarOff + 2 * kQuadStages * 8 + 1024;
 
-__global__ void __launch_bounds__((kWideWarps + 1) * 32)
-    recurrence_wide_kernel(RecArgs a, const __grid_constant__ CUtensorMap vmap) {
+__global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
+    recurrence_quad_kernel(RecArgs a, const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(
         (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kWideBarOff);
-    uint64_t* empty = full + kWideStages;
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQuadBarOff);
+    uint64_t* empty = full + kQuadStages;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t n = blockIdx.x / a.H;
@@ -432,26 +435,26 @@ __global__ void __launch_bounds__((kWideWarps + 1) * 32)
         seqlen = a.geo.tokens_per_seq;
     }
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kWideStages; ++s) {
+        for (int s = 0; s < kQuadStages; ++s) {
             mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kWideWarps);
+            mbar_init(&empty[s], kQuadWarps);
         }
         fence_barrier_init();
     }
     __syncthreads();
 
-    if (warp == kWideWarps) {
+    if (warp == kQuadWarps) {
         // ------------------------------------------------------------ producer
         uint32_t fill_parity = 0, filled = 0;
         bool ok = true;
         for (int64_t c = 0; c < nch && ok; ++c) {
-            const int s = static_cast<int>(c % kWideStages);
-            if (c >= kWideStages)
-                ok = mbar_wait_warp_sleep(&empty[s], ((c / kWideStages) - 1) & 1, a.status);
+            const int s = static_cast<int>(c % kQuadStages);
+            if (c >= kQuadStages)
+                ok = mbar_wait_warp_sleep(&empty[s], ((c / kQuadStages) - 1) & 1, a.status);
             if (!ok) break;
-            uint8_t* stage = smem + s * kWideStageBytes;
+            uint8_t* stage = smem + s * kQuadStageBytes;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * kWideVRowBytes);
+                mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * kQuadVRowBytes);
                 bulk_g2s(stage, a.packets + ((c_begin + c) * a.H + h) * static_cast<int64_t>(kPacketBytes),
                          kPacketBytes, &full[s]);
                 tma_load_2d(stage + kPacketBytes, &vmap, static_cast<int32_t>(h * kHeadDim),
@@ -462,23 +465,23 @@ __global__ void __launch_bounds__((kWideWarps + 1) * 32)
             filled |= 1u << s;
         }
         if (!ok)
-            for (int s = 0; s < kWideStages; ++s)
+            for (int s = 0; s < kQuadStages; ++s)
                 if (filled >> s & 1u) mbar_wait_bounded(&full[s], (fill_parity >> s) & 1u, a.status);
         return;
     }
 
     // ---------------------------------------------------------------- consumers
     const int g8 = lane >> 2, t4 = lane & 3;
-    const int vcol = 16 * warp;   // first of this warp's 16 value columns
+    const int vcol = 32 * warp;   // first of this warp's 32 value columns
     const int64_t state_base = (n * a.H + h) * kHeadDim * kHeadDim;
     const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
     const uint32_t hiA = lane >> 4;
 
-    float Sf[8][2][4];
+    float Sf[8][4][4];
 #pragma unroll
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 4; ++nt) {
             if (a.init_state) {
                 const __nv_bfloat16* src = a.init_state + state_base;
                 const int key = 16 * mt + g8;
@@ -491,53 +494,58 @@ __global__ void __launch_bounds__((kWideWarps + 1) * 32)
                 Sf[mt][nt][0] = Sf[mt][nt][1] = Sf[mt][nt][2] = Sf[mt][nt][3] = 0.f;
             }
         }
-    uint32_t Sb[8][2][2];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
-            Sb[mt][nt][0] = movm_t(pack_bf16(Sf[mt][nt][0], Sf[mt][nt][1]));
-            Sb[mt][nt][1] = movm_t(pack_bf16(Sf[mt][nt][2], Sf[mt][nt][3]));
-        }
 
     bool ok = true;
     for (int64_t c = 0; c < nch; ++c) {
-        const int s = static_cast<int>(c % kWideStages);
-        if (!mbar_wait_warp(&full[s], (c / kWideStages) & 1, a.status)) {
+        const int s = static_cast<int>(c % kQuadStages);
+        if (!mbar_wait_warp(&full[s], (c / kQuadStages) & 1, a.status)) {
             ok = false;
             break;
         }
-        const uint8_t* stage = smem + s * kWideStageBytes;
+        const uint8_t* stage = smem + s * kQuadStageBytes;
         const uint32_t sKS = smem_u32(stage + kOffKS);
         const uint32_t sQS = smem_u32(stage + kOffQS);
         const uint32_t sKE = smem_u32(stage + kOffKE);
         int64_t len = seqlen - kChunk * c;
         if (len > kChunk) len = kChunk;
 
-        // U^T = (A^kk B) V^T + K' S^T for both n-tiles.
-        uint32_t akb[4], vb[4];
-        ldsm_x4(akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
+        // U^T = (A^kk B) V^T + K' S^T and P^T = s (Q^start)^T S^T from the
+        // incoming state, four n-tiles, two accumulators each.
+        float u[2][4][4], p[2][4][4];
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) u[x][nt][j] = p[x][nt][j] = 0.f;
         {
-            // lanes 0-7 / 8-15: tokens 0-7 / 8-15 of columns vcol..+7; lanes
-            // 16-31: the same for columns vcol+8..+15.
-            const uint8_t* sV = stage + kPacketBytes + (lane & 15) * kWideVRowBytes + (vcol + 8 * (lane >> 4)) * 2;
-            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                         : "=r"(vb[0]), "=r"(vb[1]), "=r"(vb[2]), "=r"(vb[3])
-                         : "r"(smem_u32(sV)));
+            uint32_t akb[4];
+            ldsm_x4(akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+                // lanes 0-15: tokens of columns vcol + 16 hp .. + 7; lanes 16-31: + 8.
+                uint32_t vb[4];
+                const uint8_t* sV = stage + kPacketBytes + (lane & 15) * kQuadVRowBytes +
+                                    (vcol + 16 * hp + 8 * (lane >> 4)) * 2;
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(vb[0]), "=r"(vb[1]), "=r"(vb[2]), "=r"(vb[3])
+                             : "r"(smem_u32(sV)));
+                mma_bf16(u[0][2 * hp], akb, vb, u[0][2 * hp]);
+                mma_bf16(u[0][2 * hp + 1], akb, vb + 2, u[0][2 * hp + 1]);
+            }
         }
-        float u[2][2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) u[0][nt][j] = u[1][nt][j] = 0.f;
-        mma_bf16(u[0][0], akb, vb, u[0][0]);
-        mma_bf16(u[0][1], akb, vb + 2, u[0][1]);
 #pragma unroll
         for (int kk = 0; kk < 8; ++kk) {
-            uint32_t af[4];
-            ldsm_x4(af, sKS + sw128_off(16, rowA, 2 * kk + hiA));
-            mma_bf16(u[kk & 1][0], af, Sb[kk][0], u[kk & 1][0]);
-            mma_bf16(u[kk & 1][1], af, Sb[kk][1], u[kk & 1][1]);
+            uint32_t kf[4], qf[4];
+            ldsm_x4(kf, sKS + sw128_off(16, rowA, 2 * kk + hiA));
+            ldsm_x4(qf, sQS + sw128_off(16, rowA, 2 * kk + hiA));
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const uint32_t sb[2] = {movm_t(pack_bf16(Sf[kk][nt][0], Sf[kk][nt][1])),
+                                        movm_t(pack_bf16(Sf[kk][nt][2], Sf[kk][nt][3]))};
+                mma_bf16(u[kk & 1][nt], kf, sb, u[kk & 1][nt]);
+                mma_bf16(p[kk & 1][nt], qf, sb, p[kk & 1][nt]);
+            }
         }
         // D S^T in place.
         {
@@ -546,7 +554,7 @@ __global__ void __launch_bounds__((kWideWarps + 1) * 32)
             for (int j = 0; j < 4; ++j) {
                 const float4 d = dp[j];
 #pragma unroll
-                for (int nt = 0; nt < 2; ++nt) {
+                for (int nt = 0; nt < 4; ++nt) {
                     Sf[2 * j][nt][0] *= d.x;
                     Sf[2 * j][nt][1] *= d.x;
                     Sf[2 * j][nt][2] *= d.y;
@@ -558,9 +566,9 @@ __global__ void __launch_bounds__((kWideWarps + 1) * 32)
                 }
             }
         }
-        uint32_t Ub[2][2];
+        uint32_t Ub[4][2];
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 4; ++nt) {
             Ub[nt][0] = movm_t(pack_bf16(u[0][nt][0] + u[1][nt][0], u[0][nt][1] + u[1][nt][1]));
             Ub[nt][1] = movm_t(pack_bf16(u[0][nt][2] + u[1][nt][2], u[0][nt][3] + u[1][nt][3]));
         }
@@ -569,47 +577,26 @@ __global__ void __launch_bounds__((kWideWarps + 1) * 32)
         for (int mt = 0; mt < 8; ++mt) {
             uint32_t af[4];
             ldsm_x4(af, sKE + sw32_off(16 * mt + rowA, hiA));
-            mma_bf16(Sf[mt][0], af, Ub[0], Sf[mt][0]);
-            mma_bf16(Sf[mt][1], af, Ub[1], Sf[mt][1]);
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) mma_bf16(Sf[mt][nt], af, Ub[nt], Sf[mt][nt]);
         }
-        // P^T = s (Q^start)^T S^T from the incoming state, then O^T.
-        float pa[2][4], pb[2][4];
-#pragma unroll
-        for (int nt = 0; nt < 2; ++nt)
-#pragma unroll
-            for (int j = 0; j < 4; ++j) pa[nt][j] = pb[nt][j] = 0.f;
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            uint32_t af[4];
-            ldsm_x4(af, sQS + sw128_off(16, rowA, 2 * kk + hiA));
-            float (*acc)[4] = (kk & 1) ? pb : pa;
-            mma_bf16(acc[0], af, Sb[kk][0], acc[0]);
-            mma_bf16(acc[1], af, Sb[kk][1], acc[1]);
-        }
-        float o[2][4];
+        // O^T = P^T + A^qk U^T.
+        float o[4][4];
         {
             uint32_t aq[4];
             ldsm_x4(aq, smem_u32(stage + kOffAQK + sw32_off(rowA, hiA)));
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                float pin[4] = {pa[nt][0] + pb[nt][0], pa[nt][1] + pb[nt][1], pa[nt][2] + pb[nt][2],
-                                pa[nt][3] + pb[nt][3]};
+            for (int nt = 0; nt < 4; ++nt) {
+                float pin[4] = {p[0][nt][0] + p[1][nt][0], p[0][nt][1] + p[1][nt][1],
+                                p[0][nt][2] + p[1][nt][2], p[0][nt][3] + p[1][nt][3]};
                 mma_bf16(o[nt], aq, Ub[nt], pin);
             }
         }
         __syncwarp();
         mbar_arrive_if(&empty[s], lane == 0);
-        // BF16 operand copy of the new state.
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
-                Sb[mt][nt][0] = movm_t(pack_bf16(Sf[mt][nt][0], Sf[mt][nt][1]));
-                Sb[mt][nt][1] = movm_t(pack_bf16(Sf[mt][nt][2], Sf[mt][nt][3]));
-            }
         __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + g8) * a.H + h) * kHeadDim + vcol + 2 * t4;
 #pragma unroll
-        for (int nt = 0; nt < 2; ++nt) {
+        for (int nt = 0; nt < 4; ++nt) {
             st_global_u32_if(orow + 8 * nt, pack_bf16(o[nt][0], o[nt][1]), g8 < len);
             st_global_u32_if(orow + 8 * a.H * kHeadDim + 8 * nt, pack_bf16(o[nt][2], o[nt][3]), g8 + 8 < len);
         }
@@ -620,7 +607,7 @@ __global__ void __launch_bounds__((kWideWarps + 1) * 32)
 #pragma unroll
         for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
-            for (int nt = 0; nt < 2; ++nt) {
+            for (int nt = 0; nt < 4; ++nt) {
                 const int key = 16 * mt + g8;
                 const int val = vcol + 8 * nt + 2 * t4;
                 dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][nt][0]);
@@ -631,14 +618,14 @@ __global__ void __launch_bounds__((kWideWarps + 1) * 32)
     }
 }
 
-cudaError_t launch_wide(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
+cudaError_t launch_quad(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(recurrence_wide_kernel,
+        cudaError_t e = cudaFuncSetAttribute(recurrence_quad_kernel,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kWideSmemBytes));
+                                             static_cast<int>(kQuadSmemBytes));
         if (e != cudaSuccess) return e;
         configured[dev] = true;
     }
@@ -647,7 +634,7 @@ cudaError_t launch_wide(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
     const void* vbase = a.v ? static_cast<const void*>(a.v) : static_cast<const void*>(kZero);
     cudaError_t e = encode_v_map(&vmap, vbase, a.geo.tokens, a.H, kHeadDim);
     if (e != cudaSuccess) return e;
-    recurrence_wide_kernel<<<static_cast<unsigned>(blocks), (kWideWarps + 1) * 32, kWideSmemBytes, stream>>>(a, vmap);
+    recurrence_quad_kernel<<<static_cast<unsigned>(blocks), (kQuadWarps + 1) * 32, kQuadSmemBytes, stream>>>(a, vmap);
     return cudaGetLastError();
 }
 
@@ -775,7 +762,7 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
         }
     }
     switch (nsplit) {
-        case 1: return launch_wide(a, blocks, stream);     // 8 warps x 16 columns
+        case 1: return launch_quad(a, blocks, stream);     // 4 warps x 32 columns
         case 2: return launch_nw<8>(a, blocks, stream);    // 8 warps x 8 columns
         case 4: return launch_ks<4>(a, blocks, stream);    // key split: 4 pairs x 8 columns
         case 8: return launch_ks<2>(a, blocks, stream);
