@@ -45,6 +45,7 @@ extern "C" {
 /* Device-side status bits, reported by kda_device_status(). */
 #define KDA_DEV_BAD_SEQLENS 1  /* cu_seqlens broke its contract; out/final_state untouched */
 #define KDA_DEV_PIPE_TIMEOUT 2 /* an internal pipeline wait hit its bound; results incomplete */
+#define KDA_DEV_BAD_CHECKPOINTS 4 /* a checkpoint had no valid row in checkpoint_cu_starts; skipped */
 
 /*
  * KDA prefill, fixed or packed variable-length layout.
@@ -114,6 +115,36 @@ int kda_set_split(int nsplit);
  * Process-wide; returns KDA_ERR_ARG for other values.
  */
 int kda_set_engine(int engine);
+
+/*
+ * kda_prefill plus native state checkpoints ("flashinfer kda_prefill", Native
+ * checkpoints): the recurrent state before each interval of
+ * checkpoint_every_n_tokens tokens (a positive multiple of 16).  Every
+ * non-empty sequence n contributes ceil(len_n / interval) rows: its initial
+ * state (init_state, or zeros), then the states after one, two, ... intervals
+ * that strictly precede its end; empty sequences contribute none.
+ *
+ *   state_checkpoints     BF16 [checkpoint_rows, H, 128 (value), 128 (key)], DEVICE,
+ *                         written; 16-byte aligned; must not overlap any other
+ *                         argument.
+ *   checkpoint_cu_starts  int64 [N + 1], DEVICE, read: sequence n's rows are
+ *                         checkpoint_cu_starts[n] ..; N = B (fixed layout) or the
+ *                         number of sequences (packed).  Caller-provided and not
+ *                         scanned at launch: a checkpoint whose row falls outside
+ *                         [cu_starts[n], cu_starts[n + 1]) or [0, checkpoint_rows)
+ *                         is not written and sets KDA_DEV_BAD_CHECKPOINTS.
+ *
+ * Everything else, including results and errors, is as kda_prefill; in
+ * addition KDA_ERR_ARG for an interval that is not a positive multiple of 16
+ * or negative checkpoint_rows, KDA_ERR_NULL for NULL checkpoint pointers.
+ * Under engine 2 (kda_set_engine) such calls run on the column-split kernels.
+ */
+int kda_prefill_checkpointed(const void* q, const void* k, const void* v, const float* g,
+                             const void* beta, const void* init_state, void* out,
+                             void* final_state, int64_t B, int64_t T, int64_t H,
+                             const int64_t* cu_seqlens, int64_t checkpoint_every_n_tokens,
+                             void* state_checkpoints, const int64_t* checkpoint_cu_starts,
+                             int64_t checkpoint_rows, void* stream);
 
 /*
  * Whether kda_prefill may run preparation and recurrence as one cooperative

@@ -36,15 +36,22 @@ def _stream_handle(stream):
 
 
 def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
-                final_state=None, output_final_state=True, stream=None):
-    """KDA prefill on CUDA tensors; returns ``(out, final_state)``.
+                final_state=None, output_final_state=True, stream=None,
+                checkpoint_every_n_tokens=None, state_checkpoints=None,
+                checkpoint_cu_starts=None):
+    """KDA prefill on CUDA tensors; returns ``(out, final_state)``, or
+    ``(out, final_state, state_checkpoints)`` with checkpoints.
 
     q, k, v: bf16 ``[B, T, H, 128]``; g: fp32 ``[B, T, H, 128]`` (log-decay in
     [-5, 0]); beta: bf16 ``[B, T, H]``; init_state: bf16 ``[N, H, 128, 128]`` or
     None; cu_seqlens: int64 ``[N + 1]`` on the device for the packed layout
     (then ``B == 1``).  ``final_state`` may be ``init_state`` for an in-place
-    update.  The call is asynchronous on ``stream`` (default: the current
-    PyTorch stream).
+    update.  With ``checkpoint_every_n_tokens`` (a positive multiple of 16),
+    ``state_checkpoints`` (bf16 ``[C, H, 128, 128]``) receives the state before
+    every interval of each sequence at rows ``checkpoint_cu_starts[n]`` ..
+    (int64 ``[N + 1]`` on the device; see ``kda_prefill_checkpointed`` in
+    include/kda.h).  The call is asynchronous on ``stream`` (default: the
+    current PyTorch stream).
     """
     import torch
     _require(q.dim() == 4 and q.shape[-1] == HEAD_DIM, "q must be [B, T, H, 128]")
@@ -77,12 +84,30 @@ def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, HEAD_DIM, HEAD_DIM), dtype=torch.bfloat16,
                                   device=q.device)
-    rc = _lib.prefill_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
-                          _ptr(out), _ptr(final_state), n_arg, T, H, _ptr(cu_seqlens),
-                          _stream_handle(stream))
+    if checkpoint_every_n_tokens is None:
+        rc = _lib.prefill_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                              _ptr(out), _ptr(final_state), n_arg, T, H, _ptr(cu_seqlens),
+                              _stream_handle(stream))
+        if rc != 0:
+            raise KdaError(rc, "kda_prefill")
+        return out, final_state
+    _require(state_checkpoints is not None and checkpoint_cu_starts is not None,
+             "checkpoints need state_checkpoints and checkpoint_cu_starts")
+    _require(state_checkpoints.is_cuda and state_checkpoints.dtype == torch.bfloat16
+             and state_checkpoints.is_contiguous() and state_checkpoints.dim() == 4
+             and tuple(state_checkpoints.shape[1:]) == (H, HEAD_DIM, HEAD_DIM),
+             "state_checkpoints must be a contiguous bf16 [C, H, 128, 128] CUDA tensor")
+    _require(checkpoint_cu_starts.is_cuda and checkpoint_cu_starts.dtype == torch.int64
+             and checkpoint_cu_starts.is_contiguous() and checkpoint_cu_starts.numel() == N + 1,
+             "checkpoint_cu_starts must be a contiguous int64 [N + 1] CUDA vector")
+    rc = _lib.prefill_checkpointed_raw(
+        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(out),
+        _ptr(final_state), n_arg, T, H, _ptr(cu_seqlens), checkpoint_every_n_tokens,
+        _ptr(state_checkpoints), _ptr(checkpoint_cu_starts), state_checkpoints.shape[0],
+        _stream_handle(stream))
     if rc != 0:
-        raise KdaError(rc, "kda_prefill")
-    return out, final_state
+        raise KdaError(rc, "kda_prefill_checkpointed")
+    return out, final_state, state_checkpoints
 
 
 def prep_only(q, k, g, beta, cu_seqlens=None, stream=None):

@@ -41,6 +41,8 @@ def load():
         P, I64, I = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
         lib.kda_prefill.argtypes = [P] * 8 + [I64] * 3 + [P, P]
         lib.kda_prefill.restype = I
+        lib.kda_prefill_checkpointed.argtypes = [P] * 8 + [I64] * 3 + [P, I64, P, P, I64, P]
+        lib.kda_prefill_checkpointed.restype = I
         lib.kda_error_string.argtypes = [I]
         lib.kda_error_string.restype = ctypes.c_char_p
         lib.kda_device_status.argtypes = [P, ctypes.POINTER(I)]
@@ -91,6 +93,15 @@ def prefill_raw(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seql
     return load().kda_prefill(q or None, k or None, v or None, g or None, beta or None,
                               init_state or None, out or None, final_state or None,
                               int(B), int(T), int(H), cu_seqlens or None, stream or None)
+
+
+def prefill_checkpointed_raw(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,
+                             every, states, cu_starts, rows, stream):
+    """Call ``kda_prefill_checkpointed`` with integer device addresses (0 for NULL)."""
+    return load().kda_prefill_checkpointed(
+        q or None, k or None, v or None, g or None, beta or None, init_state or None, out or None,
+        final_state or None, int(B), int(T), int(H), cu_seqlens or None, int(every),
+        states or None, cu_starts or None, int(rows), stream or None)
 
 
 def device_status(stream=0) -> int:

@@ -208,10 +208,14 @@ int device_context(int** status, int64_t units, int* nsplit) {
 
 using namespace kda;
 
-extern "C" int kda_prefill(const void* q, const void* k, const void* v, const float* g,
-                           const void* beta, const void* init_state, void* out,
-                           void* final_state, int64_t B, int64_t T, int64_t H,
-                           const int64_t* cu_seqlens, void* stream_ptr) {
+namespace kda {
+namespace {
+
+// kda_prefill and kda_prefill_checkpointed; `ck` null for no checkpoints.
+int prefill_impl(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                 const void* init_state, void* out, void* final_state, int64_t B, int64_t T,
+                 int64_t H, const int64_t* cu_seqlens, void* stream_ptr, const Checkpoints* ck,
+                 const void* ck_cu_starts) {
     const bool packed = cu_seqlens != nullptr;
     Plan pl;
     int rc = make_plan(B, T, H, packed, &pl);
@@ -237,6 +241,12 @@ extern "C" int kda_prefill(const void* q, const void* k, const void* v, const fl
         if (overlap(rf, in)) return KDA_ERR_OVERLAP;
     if (final_state && init_state && final_state != init_state && overlap(rf, ri))
         return KDA_ERR_OVERLAP;
+    if (ck) {
+        const Range rs = range(ck->states, ck->rows * H * kHeadDim * kHeadDim * 2);
+        const Range rcs = range(ck_cu_starts, 8 * (pl.N + 1));
+        for (Range in : {rq, rk, rv, rg, rb, ro, ri, rf, rc_, rcs})
+            if (overlap(rs, in)) return KDA_ERR_OVERLAP;
+    }
 
     DeviceState* d = nullptr;
     rc = device_state(&d);
@@ -267,7 +277,7 @@ extern "C" int kda_prefill(const void* q, const void* k, const void* v, const fl
         prof_record(1, stream);
         if (rc == KDA_OK) {
             if (launch_fused(q, k, g, beta, v, out, init_state, final_state, ws + pl.meta_bytes,
-                             ready, pl.geo, H, nsplit, kScale, d->status, stream) == cudaSuccess)
+                             ready, pl.geo, H, nsplit, kScale, d->status, stream, ck) == cudaSuccess)
                 done = true;
             else
                 cudaGetLastError();
@@ -278,7 +288,7 @@ extern "C" int kda_prefill(const void* q, const void* k, const void* v, const fl
         prof_record(1, stream);
         if (rc == KDA_OK &&
             launch_recurrence(v, out, init_state, final_state, ws + pl.meta_bytes, geo, H, nsplit,
-                              d->status, stream) != cudaSuccess)
+                              d->status, stream, ck) != cudaSuccess)
             rc = KDA_ERR_CUDA;
     }
     prof_record(2, stream);
@@ -287,6 +297,40 @@ extern "C" int kda_prefill(const void* q, const void* k, const void* v, const fl
     if (rc != KDA_OK) cudaGetLastError();
     return rc;
 }
+
+}  // namespace
+}  // namespace kda
+
+extern "C" int kda_prefill(const void* q, const void* k, const void* v, const float* g,
+                           const void* beta, const void* init_state, void* out,
+                           void* final_state, int64_t B, int64_t T, int64_t H,
+                           const int64_t* cu_seqlens, void* stream_ptr) {
+    return prefill_impl(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,
+                        stream_ptr, nullptr, nullptr);
+}
+
+extern "C" int kda_prefill_checkpointed(const void* q, const void* k, const void* v,
+                                        const float* g, const void* beta, const void* init_state,
+                                        void* out, void* final_state, int64_t B, int64_t T,
+                                        int64_t H, const int64_t* cu_seqlens,
+                                        int64_t checkpoint_every_n_tokens, void* state_checkpoints,
+                                        const int64_t* checkpoint_cu_starts,
+                                        int64_t checkpoint_rows, void* stream_ptr) {
+    if (checkpoint_every_n_tokens <= 0 || checkpoint_every_n_tokens % kChunk != 0 ||
+        checkpoint_rows < 0)
+        return KDA_ERR_ARG;
+    if (!checkpoint_cu_starts || !state_checkpoints) return KDA_ERR_NULL;
+    if (!aligned(state_checkpoints, 16) || !aligned(checkpoint_cu_starts, 8)) return KDA_ERR_ALIGN;
+    if (H > 0 && checkpoint_rows > kMaxElems / (H * kHeadDim * kHeadDim)) return KDA_ERR_SHAPE;
+    Checkpoints ck;
+    ck.states = static_cast<__nv_bfloat16*>(state_checkpoints);
+    ck.cu_starts = checkpoint_cu_starts;
+    ck.every = checkpoint_every_n_tokens / kChunk;
+    ck.rows = checkpoint_rows;
+    return prefill_impl(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,
+                        stream_ptr, &ck, checkpoint_cu_starts);
+}
+
 
 extern "C" int kda_prep_only(const void* q, const void* k, const float* g, const void* beta,
                              int64_t B, int64_t T, int64_t H, const int64_t* cu_seqlens,

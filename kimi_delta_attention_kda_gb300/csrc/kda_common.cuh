@@ -75,6 +75,7 @@ enum DeviceStatus : int {
     kDevOk = 0,
     kDevBadSeqlens = 1,     // cu_seqlens violated its contract; outputs untouched
     kDevPipeTimeout = 2,    // a pipeline wait ran past its bound; outputs incomplete
+    kDevBadCheckpoints = 4, // a checkpoint had no valid row in the caller's offsets; not written
 };
 
 // Varlen metadata written by the metadata kernel at the start of the workspace.

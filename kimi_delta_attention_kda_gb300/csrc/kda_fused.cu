@@ -93,7 +93,8 @@ bool fused_supported(int64_t n_seqs, int64_t H, int nsplit, int sms) {
 cudaError_t launch_fused(const void* q, const void* k, const float* g, const void* beta,
                          const void* v, void* out, const void* init_state, void* final_state,
                          uint8_t* packets, uint32_t* ready, const SeqGeometry& geo, int64_t H,
-                         int nsplit, float scale, int* status, cudaStream_t stream) {
+                         int nsplit, float scale, int* status, cudaStream_t stream,
+                         const Checkpoints* ck) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -119,6 +120,7 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
     f.r.H = H;
     f.r.nsplit = nsplit;
     f.r.status = status;
+    f.r.ck = ck ? *ck : Checkpoints{nullptr, nullptr, 1, 0};
     f.rec_blocks = geo.n_seqs * H * nsplit;
     f.ready = ready;
 

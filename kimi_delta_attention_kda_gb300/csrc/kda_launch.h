@@ -31,12 +31,22 @@ cudaError_t launch_prep(const void* q, const void* k, const float* g, const void
                         uint8_t* packets, const SeqGeometry& geo, int64_t H, float scale,
                         int* status, cudaStream_t stream);
 
+// Native state checkpoints: the state before every `every`-chunk interval of
+// each sequence (its initial state first), in rows cu_starts[n] ..
+// cu_starts[n + 1] - 1 of states [rows, H, 128, 128] (BF16, DEVICE).
+struct Checkpoints {
+    __nv_bfloat16* states;       // null: no checkpoints
+    const int64_t* cu_starts;    // [N + 1], DEVICE
+    int64_t every;               // chunks per interval (>= 1)
+    int64_t rows;                // rows of `states`
+};
+
 // Recurrence variants: `nsplit` CTAs share one (sequence, head); each owns
-// 128 / nsplit value columns.
+// 128 / nsplit value columns.  `ck` may be null (no checkpoints).
 cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
                               void* final_state, const uint8_t* packets,
                               const SeqGeometry& geo, int64_t H, int nsplit, int* status,
-                              cudaStream_t stream);
+                              cudaStream_t stream, const Checkpoints* ck = nullptr);
 
 // The tcgen05 recurrence: one CTA per (sequence, head).
 cudaError_t launch_recurrence_tc(const void* v, void* out, const void* init_state,
@@ -52,7 +62,8 @@ bool fused_supported(int64_t n_seqs, int64_t H, int nsplit, int sms);
 cudaError_t launch_fused(const void* q, const void* k, const float* g, const void* beta,
                          const void* v, void* out, const void* init_state, void* final_state,
                          uint8_t* packets, uint32_t* ready, const SeqGeometry& geo, int64_t H,
-                         int nsplit, float scale, int* status, cudaStream_t stream);
+                         int nsplit, float scale, int* status, cudaStream_t stream,
+                         const Checkpoints* ck = nullptr);
 
 // Tensor map of v viewed as a 2-D BF16 array [tokens][H * 128], boxes of
 // 16 tokens x `cols` value columns.

@@ -21,7 +21,21 @@ struct RecArgs {
     int64_t H;
     int nsplit;
     int* status;
+    Checkpoints ck;   // ck.states null: none
 };
+
+// Where sequence n's checkpoint j of head h goes, or null (with the
+// kDevBadCheckpoints status bit) when the caller's row offsets give it no
+// row inside the buffer and inside the sequence's own range.
+__device__ __forceinline__ __nv_bfloat16* checkpoint_dst(const RecArgs& a, int64_t n, int64_t h,
+                                                         int64_t j) {
+    const int64_t row = a.ck.cu_starts[n] + j;
+    if (row < 0 || row >= a.ck.rows || row >= a.ck.cu_starts[n + 1]) {
+        atomicOr(a.status, kDevBadCheckpoints);
+        return nullptr;
+    }
+    return a.ck.states + (row * a.H + h) * kHeadDim * kHeadDim;
+}
 
 __device__ __forceinline__ uint32_t movm_t(uint32_t x) {
     uint32_t y;
@@ -102,6 +116,21 @@ __device__ __forceinline__ void ks_load_rest(const uint8_t* stage, uint32_t vrow
     const float4* dp = reinterpret_cast<const float4*>(stage + kOffD) + 4 * g8 + 2 * kh;
     f.d[0] = dp[0];
     f.d[1] = dp[1];
+}
+
+// This warp's slice of a state (its 64 keys of 8 value columns), BF16, into a
+// [128 value][128 key] state at dst.
+__device__ __forceinline__ void ks_store_state(__nv_bfloat16* dst, const float (&Sf)[4][4], int kh,
+                                               int vcol, int g8, int t4) {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+        const int key = 16 * (4 * kh + i) + g8;
+        const int val = vcol + 2 * t4;
+        dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[i][0]);
+        dst[(int64_t)(val + 1) * kHeadDim + key] = __float2bfloat16_rn(Sf[i][1]);
+        dst[(int64_t)val * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[i][2]);
+        dst[(int64_t)(val + 1) * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[i][3]);
+    }
 }
 
 template <int NCG>
@@ -248,7 +277,13 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
             ks_load_rest(smem, L::kVRowBytes, cg, kh, lane, f);
         }
     }
+    int64_t ck_next = 0;   // next chunk whose incoming state is a checkpoint
     for (int64_t c = 0; c < nch && ok; ++c) {
+        if (a.ck.states && c == ck_next) {
+            ck_next += a.ck.every;
+            __nv_bfloat16* dst = checkpoint_dst(a, n, h, c / a.ck.every);
+            if (dst) ks_store_state(dst, Sf, kh, vcol, g8, t4);
+        }
         const int s = static_cast<int>(c % kStages);
         const bool has_next = c + 1 < nch;
         const int s1 = static_cast<int>((c + 1) % kStages);
@@ -329,18 +364,7 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
         st_global_u32_if(orow, kh == 0 ? pack_bf16(o[0], o[1]) : pack_bf16(o[2], o[3]), tok < len);
     }
 
-    if (ok && a.final_state) {
-        __nv_bfloat16* dst = a.final_state + state_base;
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-            const int key = 16 * (4 * kh + i) + g8;
-            const int val = vcol + 2 * t4;
-            dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[i][0]);
-            dst[(int64_t)(val + 1) * kHeadDim + key] = __float2bfloat16_rn(Sf[i][1]);
-            dst[(int64_t)val * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[i][2]);
-            dst[(int64_t)(val + 1) * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[i][3]);
-        }
-    }
+    if (ok && a.final_state) ks_store_state(a.final_state + state_base, Sf, kh, vcol, g8, t4);
 }
 
 }  // namespace rec

@@ -166,6 +166,21 @@ __device__ __forceinline__ void chunk_step(const ChunkFrags& f, float (&Sf)[8][4
     mma_bf16(o, f.aqk, Ub, pin);
 }
 
+// A warp's slice of a state (all 128 keys of 8 value columns), BF16, into a
+// [128 value][128 key] state at dst.
+__device__ __forceinline__ void narrow_store_state(__nv_bfloat16* dst, const float (&Sf)[8][4],
+                                                   int vcol, int g8, int t4) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt) {
+        const int key = 16 * mt + g8;
+        const int val = vcol + 2 * t4;
+        dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][0]);
+        dst[(int64_t)(val + 1) * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][1]);
+        dst[(int64_t)val * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][2]);
+        dst[(int64_t)(val + 1) * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][3]);
+    }
+}
+
 template <int NW>
 __global__ void __launch_bounds__((NW + 1) * 32)
     recurrence_kernel(RecArgs a, const __grid_constant__ CUtensorMap vmap) {
@@ -273,6 +288,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 
     bool ok = true;
     ChunkFrags f;
+    int64_t ck_next = 0;   // next chunk whose incoming state is a checkpoint
     if (L::kPrefetch) {
         // Rolling prefetch: each group of chunk c+1's fragments is loaded as
         // soon as chunk c has issued its last use of that group, so the loads
@@ -282,6 +298,11 @@ __global__ void __launch_bounds__((NW + 1) * 32)
             if (ok) load_frags(smem, L::kVRowBytes, warp, lane, f);
         }
         for (int64_t c = 0; c < nch && ok; ++c) {
+            if (a.ck.states && c == ck_next) {
+                ck_next += a.ck.every;
+                __nv_bfloat16* dst = checkpoint_dst(a, n, h, c / a.ck.every);
+                if (dst) narrow_store_state(dst, Sf, vcol, g8, t4);
+            }
             const int s = static_cast<int>(c % kStages);
             const bool has_next = c + 1 < nch;
             const int s1 = static_cast<int>((c + 1) % kStages);
@@ -347,6 +368,11 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         }
     } else {
         for (int64_t c = 0; c < nch; ++c) {
+            if (a.ck.states && c == ck_next) {
+                ck_next += a.ck.every;
+                __nv_bfloat16* dst = checkpoint_dst(a, n, h, c / a.ck.every);
+                if (dst) narrow_store_state(dst, Sf, vcol, g8, t4);
+            }
             const int s = static_cast<int>(c % kStages);
             const uint8_t* stage = smem + s * L::kStageBytes;
             if (!mbar_wait_warp(&full[s], (c / kStages) & 1, a.status)) {
@@ -378,18 +404,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
         }
     }
 
-    if (ok && a.final_state) {
-        __nv_bfloat16* dst = a.final_state + state_base;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            const int key = 16 * mt + g8;
-            const int val = vcol + 2 * t4;
-            dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][0]);
-            dst[(int64_t)(val + 1) * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][1]);
-            dst[(int64_t)val * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][2]);
-            dst[(int64_t)(val + 1) * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][3]);
-        }
-    }
+    if (ok && a.final_state) narrow_store_state(a.final_state + state_base, Sf, vcol, g8, t4);
 }
 
 // ---------------------------------------------------------------------------
@@ -408,6 +423,23 @@ constexpr int kQuadWarps = 4;
 constexpr int kQuadStages = 6;
 constexpr uint32_t kQuadBarOff = kQuadStages * kQuadStageBytes;
 constexpr uint32_t kQuadSmemBytes = kQuadBarOff + 2 * kQuadStages * 8 + 1024;
+
+// A warp's slice of a state (all 128 keys of 32 value columns), BF16, into a
+// [128 value][128 key] state at dst.
+__device__ __forceinline__ void quad_store_state(__nv_bfloat16* dst, const float (&Sf)[8][4][4],
+                                                 int vcol, int g8, int t4) {
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const int key = 16 * mt + g8;
+            const int val = vcol + 8 * nt + 2 * t4;
+            dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][nt][0]);
+            dst[(int64_t)(val + 1) * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][nt][1]);
+            dst[(int64_t)val * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][nt][2]);
+            dst[(int64_t)(val + 1) * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][nt][3]);
+        }
+}
 
 __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     recurrence_quad_kernel(RecArgs a, const __grid_constant__ CUtensorMap vmap) {
@@ -496,7 +528,13 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
         }
 
     bool ok = true;
+    int64_t ck_next = 0;   // next chunk whose incoming state is a checkpoint
     for (int64_t c = 0; c < nch; ++c) {
+        if (a.ck.states && c == ck_next) {
+            ck_next += a.ck.every;
+            __nv_bfloat16* dst = checkpoint_dst(a, n, h, c / a.ck.every);
+            if (dst) quad_store_state(dst, Sf, vcol, g8, t4);
+        }
         const int s = static_cast<int>(c % kQuadStages);
         if (!mbar_wait_warp(&full[s], (c / kQuadStages) & 1, a.status)) {
             ok = false;
@@ -602,20 +640,7 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
         }
     }
 
-    if (ok && a.final_state) {
-        __nv_bfloat16* dst = a.final_state + state_base;
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const int key = 16 * mt + g8;
-                const int val = vcol + 8 * nt + 2 * t4;
-                dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][nt][0]);
-                dst[(int64_t)(val + 1) * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][nt][1]);
-                dst[(int64_t)val * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][nt][2]);
-                dst[(int64_t)(val + 1) * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][nt][3]);
-            }
-    }
+    if (ok && a.final_state) quad_store_state(a.final_state + state_base, Sf, vcol, g8, t4);
 }
 
 cudaError_t launch_quad(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
@@ -731,7 +756,7 @@ cudaError_t encode_v_map(CUtensorMap* map, const void* v, int64_t tokens, int64_
 cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
                               void* final_state, const uint8_t* packets,
                               const SeqGeometry& geo, int64_t H, int nsplit, int* status,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, const Checkpoints* ck) {
     RecArgs a;
     a.v = static_cast<const __nv_bfloat16*>(v);
     a.out = static_cast<__nv_bfloat16*>(out);
@@ -742,9 +767,11 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
     a.H = H;
     a.nsplit = nsplit;
     a.status = status;
-    // Engine 2 (opt-in): the tcgen05 kernel, one CTA per head.  Otherwise the
-    // column-split kernel with `nsplit` CTAs per head.
-    if (recurrence_engine() == 2)
+    a.ck = ck ? *ck : Checkpoints{nullptr, nullptr, 1, 0};
+    // Engine 2 (opt-in): the tcgen05 kernel, one CTA per head (it writes no
+    // checkpoints, so calls that ask for them take the column-split kernels).
+    // Otherwise the column-split kernel with `nsplit` CTAs per head.
+    if (recurrence_engine() == 2 && !a.ck.states)
         return launch_recurrence_tc(v, out, init_state, final_state, packets, geo, H, status, stream);
     const int64_t blocks = geo.n_seqs * H * nsplit;
     if (blocks <= 0) return cudaSuccess;

@@ -122,3 +122,29 @@ def test_workspace_bytes(lib):
     n, T, H = 4, 100, 2
     meta = 256 + ((8 * (n + 1) + 255) // 256) * 256
     assert _lib.workspace_bytes(n, T, H, True) == meta + ((T + 15 * n) // 16) * H * pb
+
+
+def call_ck(lib, every=64, states=A + 9 * GB, cu_starts=A + 10 * GB, rows=4, **kw):
+    args = dict(q=A, k=A + GB, v=A + 2 * GB, g=A + 3 * GB, beta=A + 4 * GB, init=0,
+                out=A + 5 * GB, final=0, B=1, T=16, H=1, cu=0)
+    args.update(kw)
+    return _lib.prefill_checkpointed_raw(args["q"], args["k"], args["v"], args["g"], args["beta"],
+                                         args["init"], args["out"], args["final"], args["B"],
+                                         args["T"], args["H"], args["cu"], every, states,
+                                         cu_starts, rows, 0)
+
+
+def test_checkpoint_arguments(lib):
+    """Checked on the host before anything launches (no GPU needed)."""
+    for every in (0, -16, 8, 24, 100):
+        assert call_ck(lib, every=every) == -7       # not a positive multiple of 16
+    assert call_ck(lib, rows=-1) == -7
+    assert call_ck(lib, cu_starts=0) == -1
+    assert call_ck(lib, states=0) == -1
+    assert call_ck(lib, states=A + 9 * GB + 8) == -3   # 16-byte alignment
+    assert call_ck(lib, cu_starts=A + 10 * GB + 4) == -3
+    # the checkpoint buffer must not overlap an input, an output or its offsets
+    assert call_ck(lib, states=A + 64) == -4                      # q
+    assert call_ck(lib, states=A + 5 * GB) == -4                  # out
+    assert call_ck(lib, states=A + 10 * GB - 1024) == -4          # the offsets
+    assert call_ck(lib, B=0) == -2                                # ordinary shape checks still apply
