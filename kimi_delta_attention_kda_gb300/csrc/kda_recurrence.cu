@@ -441,6 +441,9 @@ __device__ __forceinline__ void quad_store_state(__nv_bfloat16* dst, const float
         }
 }
 
+// kCkpt: this instantiation writes checkpoints (a separate one keeps the
+// check out of the loop of the plain call, which is at the register limit).
+template <bool kCkpt>
 __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     recurrence_quad_kernel(RecArgs a, const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ uint8_t smem_raw[];
@@ -530,7 +533,7 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     bool ok = true;
     int64_t ck_next = 0;   // next chunk whose incoming state is a checkpoint
     for (int64_t c = 0; c < nch; ++c) {
-        if (a.ck.states && c == ck_next) {
+        if (kCkpt && c == ck_next) {
             ck_next += a.ck.every;
             __nv_bfloat16* dst = checkpoint_dst(a, n, h, c / a.ck.every);
             if (dst) quad_store_state(dst, Sf, vcol, g8, t4);
@@ -643,12 +646,13 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     if (ok && a.final_state) quad_store_state(a.final_state + state_base, Sf, vcol, g8, t4);
 }
 
-cudaError_t launch_quad(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
+template <bool kCkpt>
+cudaError_t launch_quad_t(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(recurrence_quad_kernel,
+        cudaError_t e = cudaFuncSetAttribute(recurrence_quad_kernel<kCkpt>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kQuadSmemBytes));
         if (e != cudaSuccess) return e;
@@ -659,8 +663,13 @@ cudaError_t launch_quad(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
     const void* vbase = a.v ? static_cast<const void*>(a.v) : static_cast<const void*>(kZero);
     cudaError_t e = encode_v_map(&vmap, vbase, a.geo.tokens, a.H, kHeadDim);
     if (e != cudaSuccess) return e;
-    recurrence_quad_kernel<<<static_cast<unsigned>(blocks), (kQuadWarps + 1) * 32, kQuadSmemBytes, stream>>>(a, vmap);
+    recurrence_quad_kernel<kCkpt>
+        <<<static_cast<unsigned>(blocks), (kQuadWarps + 1) * 32, kQuadSmemBytes, stream>>>(a, vmap);
     return cudaGetLastError();
+}
+
+cudaError_t launch_quad(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
+    return a.ck.states ? launch_quad_t<true>(a, blocks, stream) : launch_quad_t<false>(a, blocks, stream);
 }
 
 template <int NCG>
