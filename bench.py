@@ -69,9 +69,9 @@ REC_SOURCES = ("kda_recurrence.cu", "kda_rec_impl.cuh", "kda_common.cuh")
 PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
 FUSED_SOURCES = ("kda_fused.cu", "kda_prep_impl.cuh", "kda_rec_impl.cuh", "kda_common.cuh")
 PROFILED_TRAFFIC = {
-    ("fused", "t8192_h6"): (75.876e6, FUSED_SOURCES, "47d2052912ab1610"),
-    ("recurrence", "t8192_h96"): (1068.165e6, REC_SOURCES, "cd39cd347978aee2"),
-    ("chunk_prep", "t8192_h96"): (1445.243e6, PREP_SOURCES, "223d2dc525b8082b"),
+    ("fused", "t8192_h6"): (77.900e6, FUSED_SOURCES, "ec2a6931cf32a73c"),
+    ("recurrence", "t8192_h96"): (1066.989e6, REC_SOURCES, "369416dc86b00a10"),
+    ("chunk_prep", "t8192_h96"): (1466.940e6, PREP_SOURCES, "c2cf1618b34710a2"),
 }
 
 
