@@ -240,6 +240,22 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
 }
 
 
+// Named barrier of a warp pair (64 threads).
+__device__ __forceinline__ void pair_sync(int id) {
+    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
+}
+// The same barrier, returning whether `p` holds in every thread of the pair.
+__device__ __forceinline__ bool pair_all(int id, bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred q, a;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred a, %2, 64, q;\n"
+        " selp.u32 %0, 1, 0, a;\n}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(p)), "r"(id)
+        : "memory");
+    return r != 0;
+}
+
 __device__ __forceinline__ void ldsm_x4(uint32_t* r, uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])

@@ -102,21 +102,6 @@ __device__ __forceinline__ void st_row4_split(uint8_t* hi, uint8_t* lo, int t, i
     *reinterpret_cast<uint2*>(lo + off) = make_uint2(l0, l1);
 }
 
-// Named barrier of a warp pair (64 threads).
-__device__ __forceinline__ void pair_sync(int id) {
-    asm volatile("bar.sync %0, 64;" ::"r"(id) : "memory");
-}
-// The same barrier, returning whether `p` holds in every thread of the pair.
-__device__ __forceinline__ bool pair_all(int id, bool p) {
-    uint32_t r;
-    asm volatile(
-        "{\n .reg .pred q, a;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred a, %2, 64, q;\n"
-        " selp.u32 %0, 1, 0, a;\n}\n"
-        : "=r"(r)
-        : "r"(static_cast<uint32_t>(p)), "r"(id)
-        : "memory");
-    return r != 0;
-}
 
 // Token range [t0, t0 + len) of item (chunk c, head h); false when the item
 // does not exist (past the last chunk of a packed batch, or invalid offsets).

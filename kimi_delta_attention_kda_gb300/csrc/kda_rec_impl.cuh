@@ -58,9 +58,9 @@ __device__ __forceinline__ float dsel(const float4& a, int i) {
 // warp).  Each 8-column group of S^T is held by a pair of warps, one per half
 // of the 128 keys, so a warp issues half the operand loads and MMAs of the
 // keys-major form.  Per chunk each warp forms its partial U^T (and partial
-// P^T) over its 64 keys, the pair swaps partials through shared memory behind
-// an mbarrier (bounded wait), and both add them in the same order (key half
-// 0 + key half 1), so both warps continue from identical U^T.  The sums over
+// P^T) over its 64 keys, the pair swaps partials through shared memory across
+// its named barrier, and both add them in the same order (key half 0 + key
+// half 1), so both warps continue from identical U^T.  The sums over
 // keys are associated differently from the other variants, so results agree
 // with them to rounding, not bit for bit.
 // ---------------------------------------------------------------------------
@@ -75,7 +75,7 @@ struct KsLayout {
     static constexpr uint32_t kXOff = kStages * kStageBytes;
     static constexpr uint32_t kXBytes = NCG * 2 * 2 * 2 * 32 * 16;
     static constexpr uint32_t kBarOff = kXOff + kXBytes;
-    static constexpr uint32_t kSmemBytes = kBarOff + (2 * kStages + NCG) * 8 + 1024;
+    static constexpr uint32_t kSmemBytes = kBarOff + 2 * kStages * 8 + 1024;
 };
 
 struct HalfFrags {
@@ -138,13 +138,11 @@ __device__ __forceinline__ void ks_setup(uint8_t* smem) {
     using L = KsLayout<NCG>;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
     uint64_t* empty = full + L::kStages;
-    uint64_t* xbar = empty + L::kStages;
     if (threadIdx.x == 0) {
         for (int s = 0; s < L::kStages; ++s) {
             mbar_init(&full[s], 1);
             mbar_init(&empty[s], L::kWarps);
         }
-        for (int g = 0; g < NCG; ++g) mbar_init(&xbar[g], 64);   // every lane of the pair arrives
         fence_barrier_init();
     }
 }
@@ -162,7 +160,6 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
     constexpr int kWarps = L::kWarps;
     uint64_t* full = reinterpret_cast<uint64_t*>(smem + L::kBarOff);
     uint64_t* empty = full + kStages;
-    uint64_t* xbar = empty + kStages;   // one per column group
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     const int64_t nh = block / a.nsplit;
@@ -270,12 +267,16 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
 
     bool ok = true;
     HalfFrags f;
+    // The pair's named barrier (ids 1 .. NCG) also carries whether every wait
+    // of both warps succeeded, so the two always leave the loop together.
+    const int xbid = 1 + cg;
     if (nch > 0) {
         ok = mbar_wait_warp(&full[0], 0, a.status);
         if (ok) {
             ks_load_uq(smem, kh, lane, f);
             ks_load_rest(smem, L::kVRowBytes, cg, kh, lane, f);
         }
+        ok = pair_all(xbid, ok);
     }
     int64_t ck_next = 0;   // next chunk whose incoming state is a checkpoint
     for (int64_t c = 0; c < nch && ok; ++c) {
@@ -309,7 +310,6 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
         const float4* theirs = xb + ((slot * 2 + (kh ^ 1)) * 2) * 32 + lane;
         mine[0] = make_float4(ua[0] + ub[0], ua[1] + ub[1], ua[2] + ub[2], ua[3] + ub[3]);
         mine[32] = make_float4(pa[0] + pb[0], pa[1] + pb[1], pa[2] + pb[2], pa[3] + pb[3]);
-        mbar_arrive(&xbar[cg]);
         // D S^T for this half, in place (the BF16 copy is in Sb).
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -329,9 +329,9 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
             else
                 ok = false;
         }
-        // The partner's partials (phase c of the pair barrier).
-        const bool xok = mbar_wait_warp(&xbar[cg], static_cast<uint32_t>(c & 1), a.status);
-        ok = ok && xok;
+        // The partner's partials (the pair barrier orders the stores above
+        // before the loads below).
+        ok = pair_all(xbid, ok);
         float u[4], pp[4];
         {
             const float4 tu = theirs[0], tp = theirs[32];
