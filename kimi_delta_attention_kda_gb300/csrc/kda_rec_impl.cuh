@@ -308,8 +308,14 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
         const int slot = static_cast<int>(c & 1);
         float4* mine = xb + ((slot * 2 + kh) * 2) * 32 + lane;
         const float4* theirs = xb + ((slot * 2 + (kh ^ 1)) * 2) * 32 + lane;
-        mine[0] = make_float4(ua[0] + ub[0], ua[1] + ub[1], ua[2] + ub[2], ua[3] + ub[3]);
-        mine[32] = make_float4(pa[0] + pb[0], pa[1] + pb[1], pa[2] + pb[2], pa[3] + pb[3]);
+        // Own partials: all of U^T; of P^T the token rows the partner stores
+        // (key half 0 stores tokens 0-7, i.e. fragment rows g8; half 1 rows g8 + 8).
+        const float4 uh = make_float4(ua[0] + ub[0], ua[1] + ub[1], ua[2] + ub[2], ua[3] + ub[3]);
+        const float2 ph_own = kh == 0 ? make_float2(pa[0] + pb[0], pa[1] + pb[1])
+                                      : make_float2(pa[2] + pb[2], pa[3] + pb[3]);
+        mine[0] = uh;
+        *reinterpret_cast<float2*>(mine + 32) = kh == 0 ? make_float2(pa[2] + pb[2], pa[3] + pb[3])
+                                                        : make_float2(pa[0] + pb[0], pa[1] + pb[1]);
         // D S^T for this half, in place (the BF16 copy is in Sb).
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
@@ -332,15 +338,19 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
         // The partner's partials (the pair barrier orders the stores above
         // before the loads below).
         ok = pair_all(xbid, ok);
+        // Key half 0 + key half 1 (addition commutes, so both warps get the
+        // same bits whichever half is their own).
         float u[4], pp[4];
         {
-            const float4 tu = theirs[0], tp = theirs[32];
-            const float4 mu = mine[0], mp = mine[32];
-            // Key half 0 + key half 1, in that order, in both warps.
-            const float4 u0 = kh == 0 ? mu : tu, u1 = kh == 0 ? tu : mu;
-            const float4 p0 = kh == 0 ? mp : tp, p1 = kh == 0 ? tp : mp;
-            u[0] = u0.x + u1.x; u[1] = u0.y + u1.y; u[2] = u0.z + u1.z; u[3] = u0.w + u1.w;
-            pp[0] = p0.x + p1.x; pp[1] = p0.y + p1.y; pp[2] = p0.z + p1.z; pp[3] = p0.w + p1.w;
+            const float4 tu = theirs[0];
+            const float2 tp = *reinterpret_cast<const float2*>(theirs + 32);
+            u[0] = uh.x + tu.x; u[1] = uh.y + tu.y; u[2] = uh.z + tu.z; u[3] = uh.w + tu.w;
+            // P^T rows this warp stores; the other two entries are not used.
+            const float2 pr = make_float2(ph_own.x + tp.x, ph_own.y + tp.y);
+            pp[0] = kh == 0 ? pr.x : 0.f;
+            pp[1] = kh == 0 ? pr.y : 0.f;
+            pp[2] = kh == 0 ? 0.f : pr.x;
+            pp[3] = kh == 0 ? 0.f : pr.y;
         }
         uint32_t Ub[2];
         Ub[0] = movm_t(pack_bf16(u[0], u[1]));
