@@ -318,23 +318,24 @@ __device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, floa
         }
     }
 
-    // ---- 5. K^end^T (key rows x token columns) of this warp's 64 keys by
-    // transposing 8 x 8 blocks.
+    // ---- 5. K^end^T (key rows x token columns) by transposing 8 x 8 blocks:
+    // warp 1, while warp 0 runs the forward substitution.
+    if (hw == 1) {
 #pragma unroll
-    for (int pp = 0; pp < 4; ++pp) {
-        const int p = 4 * hw + pp;
-        const int mi = lane >> 3;
-        const int tok = 8 * (mi & 1) + (lane & 7);
-        const int grp = 2 * p + (mi >> 1);
-        uint32_t r[4];
-        asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                     : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
-                     : "r"(smem_u32(tKen + sw128_off(16, tok, grp))));
+        for (int p = 0; p < 8; ++p) {
+            const int mi = lane >> 3;
+            const int tok = 8 * (mi & 1) + (lane & 7);
+            const int grp = 2 * p + (mi >> 1);
+            uint32_t r[4];
+            asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                         : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                         : "r"(smem_u32(tKen + sw128_off(16, tok, grp))));
 #pragma unroll
-        for (int b = 0; b < 4; ++b) {
-            const int key = 8 * (2 * p + (b >> 1)) + (lane >> 2);
-            const int half = b & 1;
-            *reinterpret_cast<uint32_t*>(tKE + sw32_off(key, half) + 4 * (lane & 3)) = r[b];
+            for (int b = 0; b < 4; ++b) {
+                const int key = 8 * (2 * p + (b >> 1)) + (lane >> 2);
+                const int half = b & 1;
+                *reinterpret_cast<uint32_t*>(tKE + sw32_off(key, half) + 4 * (lane & 3)) = r[b];
+            }
         }
     }
 
