@@ -122,7 +122,7 @@ struct Plan {
     bool packed;
     int64_t N, tokens;
     SeqGeometry geo;
-    int64_t meta_bytes;      // valid flag + cu_chunks (packed only), 256-aligned
+    int64_t meta_bytes;      // valid flag + cu_chunks + order (packed only), 256-aligned
     int64_t packet_bytes;    // chunk_ub * H * kPacketBytes
     int64_t ready_bytes;     // chunk_ub * H flags of the fused launch, 256-aligned
 };
@@ -142,7 +142,8 @@ int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
     g.tokens = p->tokens;
     if (packed) {
         g.chunk_ub = (T + (kChunk - 1) * B) / kChunk;
-        p->meta_bytes = 256 + ((8 * (B + 1) + 255) / 256) * 256;
+        p->meta_bytes = 256 + ((8 * (B + 1) + 255) / 256) * 256 +
+                        (B <= kMaxOrdered ? ((4 * B + 255) / 256) * 256 : 0);
     } else {
         g.tokens_per_seq = T;
         g.chunks_per_seq = (T + kChunk - 1) / kChunk;
@@ -169,19 +170,24 @@ bool use_fusion(const Plan& pl, int64_t H, int nsplit, int sms) {
 }
 
 // Launch metadata (packed) and preparation into `ws` (meta) and `packets`.
+// `ordered`: also have the metadata kernel order the sequences longest-first.
 int run_prep(const Plan& pl, const void* q, const void* k, const float* g, const void* beta,
              int64_t H, const int64_t* cu_seqlens, uint8_t* meta, uint8_t* packets,
-             DeviceState* d, cudaStream_t stream, SeqGeometry* geo_out) {
+             DeviceState* d, cudaStream_t stream, SeqGeometry* geo_out, bool ordered = false) {
     SeqGeometry geo = pl.geo;
     if (pl.packed) {
         int32_t* valid = reinterpret_cast<int32_t*>(meta);
         int64_t* cu_chunks = reinterpret_cast<int64_t*>(meta + 256);
-        if (launch_varlen_meta(cu_seqlens, pl.N, pl.tokens, valid, cu_chunks, d->status,
+        int32_t* order = ordered && pl.N <= kMaxOrdered
+                             ? reinterpret_cast<int32_t*>(meta + 256 + ((8 * (pl.N + 1) + 255) / 256) * 256)
+                             : nullptr;
+        if (launch_varlen_meta(cu_seqlens, pl.N, pl.tokens, valid, cu_chunks, order, d->status,
                                stream) != cudaSuccess)
             return KDA_ERR_CUDA;
         geo.cu_seqlens = cu_seqlens;
         geo.cu_chunks = cu_chunks;
         geo.valid = valid;
+        geo.order = order;
     }
     if (launch_prep(q, k, g, beta, packets, geo, H, kScale, d->status, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
@@ -284,7 +290,11 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         }
     }
     if (rc == KDA_OK && !done) {
-        rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, ws + pl.meta_bytes, d, stream, &geo);
+        // A recurrence grid of more than one wave starts the longest
+        // sequences first (packed layout).
+        const bool ordered = pl.packed && pl.N * H * nsplit > d->sms;
+        rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, ws + pl.meta_bytes, d, stream, &geo,
+                      ordered);
         prof_record(1, stream);
         if (rc == KDA_OK &&
             launch_recurrence(v, out, init_state, final_state, ws + pl.meta_bytes, geo, H, nsplit,

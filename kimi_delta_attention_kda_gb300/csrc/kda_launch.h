@@ -20,11 +20,18 @@ struct SeqGeometry {
     const int64_t* cu_seqlens;   // packed only (device)
     const int64_t* cu_chunks;    // packed only (device, n_seqs + 1)
     const int32_t* valid;        // packed only (device)
+    // Packed only, may be null: the recurrence's sequence slots in
+    // longest-first order (slot i runs sequence order[i]), from the metadata
+    // kernel, so that the longest sequences start in the first wave.
+    const int32_t* order;
     int* status;                 // device status word (set by the launchers)
 };
 
+// Validates cu_seqlens, writes cu_chunks and, when `order` is not null
+// (n_seqs <= kMaxOrdered), the longest-first order of the sequences.
+constexpr int64_t kMaxOrdered = 1024;
 cudaError_t launch_varlen_meta(const int64_t* cu_seqlens, int64_t n_seqs, int64_t total_tokens,
-                               int32_t* valid, int64_t* cu_chunks, int* status,
+                               int32_t* valid, int64_t* cu_chunks, int32_t* order, int* status,
                                cudaStream_t stream);
 
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const void* beta,

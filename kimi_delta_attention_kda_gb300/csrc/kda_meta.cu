@@ -9,6 +9,10 @@
 // preparation kernel binary-searches and the recurrence indexes directly.
 // On a violation it clears `valid` (every later kernel then returns without
 // touching its outputs) and records kDevBadSeqlens in the status word.
+// For up to kMaxOrdered sequences it can also write the longest-first order
+// of the sequences (by chunk count, ties by index; "flashinfer kda_prefill",
+// Packed scheduling, seq_order), which the recurrence uses to start the
+// longest sequences in its first wave.
 #include "kda_common.cuh"
 #include "kda_launch.h"
 
@@ -19,8 +23,9 @@ constexpr int kMetaThreads = 1024;
 
 __global__ void __launch_bounds__(kMetaThreads)
 varlen_meta_kernel(const int64_t* cu, int64_t N, int64_t total, int32_t* valid,
-                   int64_t* cu_chunks, int* status) {
+                   int64_t* cu_chunks, int32_t* order, int* status) {
     __shared__ int64_t warp_sums[kMetaThreads / 32];
+    __shared__ int64_t counts[kMaxOrdered];
     __shared__ int64_t carry;
     __shared__ int bad;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -37,6 +42,7 @@ varlen_meta_kernel(const int64_t* cu, int64_t N, int64_t total, int32_t* valid,
             const int64_t len = cu[n + 1] - cu[n];
             if (len < 0) bad = 1;
             cnt = len > 0 ? (len + kChunk - 1) / kChunk : 0;
+            if (order && n < kMaxOrdered) counts[n] = cnt;
         }
         // Inclusive scan: within the warp, then over warp totals.
         int64_t x = cnt;
@@ -67,15 +73,30 @@ varlen_meta_kernel(const int64_t* cu, int64_t N, int64_t total, int32_t* valid,
         *valid = bad ? 0 : 1;
         if (bad) atomicOr(status, kDevBadSeqlens);
     }
+    if (order && N <= kMaxOrdered) {
+        // Rank of sequence n: sequences with more chunks, or as many and a
+        // smaller index, come first.
+        __syncthreads();
+        for (int64_t n = tid; n < N; n += kMetaThreads) {
+            const int64_t cn = counts[n];
+            int32_t rank = 0;
+            for (int64_t m = 0; m < N; ++m) {
+                const int64_t cm = counts[m];
+                rank += (cm > cn || (cm == cn && m < n)) ? 1 : 0;
+            }
+            order[rank] = static_cast<int32_t>(n);
+        }
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_varlen_meta(const int64_t* cu_seqlens, int64_t n_seqs, int64_t total_tokens,
-                               int32_t* valid, int64_t* cu_chunks, int* status,
+                               int32_t* valid, int64_t* cu_chunks, int32_t* order, int* status,
                                cudaStream_t stream) {
+    if (n_seqs > kMaxOrdered) order = nullptr;
     varlen_meta_kernel<<<1, kMetaThreads, 0, stream>>>(cu_seqlens, n_seqs, total_tokens, valid,
-                                                      cu_chunks, status);
+                                                      cu_chunks, order, status);
     return cudaGetLastError();
 }
 

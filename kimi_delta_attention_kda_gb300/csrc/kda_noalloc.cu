@@ -140,7 +140,7 @@ extern "C" int kda_prefill_noalloc(const void* q, const void* k, const void* v, 
     if (packed) {
         int32_t* valid = reinterpret_cast<int32_t*>(scratch);
         int64_t* cu_chunks = reinterpret_cast<int64_t*>(scratch + 256);
-        if (launch_varlen_meta(cu_seqlens, B, tokens, valid, cu_chunks, status, stream) !=
+        if (launch_varlen_meta(cu_seqlens, B, tokens, valid, cu_chunks, nullptr, status, stream) !=
             cudaSuccess) {
             cudaGetLastError();
             return KDA_ERR_CUDA;

@@ -164,8 +164,9 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
     const int lane = threadIdx.x & 31;
     const int64_t nh = block / a.nsplit;
     const int split = static_cast<int>(block - nh * a.nsplit);
-    const int64_t n = nh / a.H;
-    const int64_t h = nh - n * a.H;
+    const int64_t n_slot = nh / a.H;
+    const int64_t h = nh - n_slot * a.H;
+    const int64_t n = a.geo.order ? a.geo.order[n_slot] : n_slot;   // longest-first (packed)
     const int v0 = split * L::kCols;
 
     int64_t c_begin, nch, tok0, seqlen;

@@ -197,8 +197,9 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     const int lane = threadIdx.x & 31;
     const int64_t nh = blockIdx.x / a.nsplit;
     const int split = blockIdx.x - nh * a.nsplit;
-    const int64_t n = nh / a.H;
-    const int64_t h = nh - n * a.H;
+    const int64_t n_slot = nh / a.H;
+    const int64_t h = nh - n_slot * a.H;
+    const int64_t n = a.geo.order ? a.geo.order[n_slot] : n_slot;   // longest-first (packed)
     const int v0 = split * L::kCols;
 
     int64_t c_begin, nch, tok0, seqlen;
@@ -453,8 +454,9 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     uint64_t* empty = full + kQuadStages;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t n = blockIdx.x / a.H;
-    const int64_t h = blockIdx.x - n * a.H;
+    const int64_t n_slot = blockIdx.x / a.H;
+    const int64_t h = blockIdx.x - n_slot * a.H;
+    const int64_t n = a.geo.order ? a.geo.order[n_slot] : n_slot;   // longest-first (packed)
 
     int64_t c_begin, nch, tok0, seqlen;
     if (a.geo.cu_chunks) {

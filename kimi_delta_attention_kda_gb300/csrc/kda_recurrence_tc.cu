@@ -97,8 +97,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
 
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t n = blockIdx.x / a.H;
-    const int64_t h = blockIdx.x - n * a.H;
+    const int64_t n_slot = blockIdx.x / a.H;
+    const int64_t h = blockIdx.x - n_slot * a.H;
+    const int64_t n = a.geo.order ? a.geo.order[n_slot] : n_slot;   // longest-first (packed)
 
     int64_t c_begin, nch, tok0, seqlen;
     if (a.geo.cu_chunks) {

@@ -118,9 +118,10 @@ def test_workspace_bytes(lib):
     # packets, plus 256-aligned ready flags (one per chunk and head) for a fused launch
     assert _lib.workspace_bytes(2, 40, 3, False) == 2 * 3 * 3 * pb + 256
     assert _lib.workspace_bytes(1, 0, 5, False) == 0
-    # packed: (T + 15 N) // 16 chunks at most, plus the metadata block
+    # packed: (T + 15 N) // 16 chunks at most, plus the metadata block (valid
+    # flag, chunk offsets and, for up to 1024 sequences, their longest-first order)
     n, T, H = 4, 100, 2
-    meta = 256 + ((8 * (n + 1) + 255) // 256) * 256
+    meta = 256 + ((8 * (n + 1) + 255) // 256) * 256 + ((4 * n + 255) // 256) * 256
     assert _lib.workspace_bytes(n, T, H, True) == meta + ((T + 15 * n) // 16) * H * pb
 
 

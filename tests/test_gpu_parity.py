@@ -429,3 +429,31 @@ def test_fused_repeated_calls_and_in_place(kda):
     torch.cuda.synchronize()
     assert kda.device_status() == 0
     assert torch.equal(out.cpu(), a[0]) and torch.equal(state.cpu(), a[1])
+
+
+def test_packed_many_sequences_longest_first(kda):
+    """300 packed sequences (0-400 tokens) at H=2 and split 1: 600 one-CTA-per-head
+    units are more than one wave, so the recurrence takes the sequences longest
+    first.  The order changes no arithmetic: each sequence equals, bit for bit,
+    a call with that sequence alone, and all of them match the oracle."""
+    rng = np.random.default_rng(7)
+    lengths = rng.integers(0, 401, size=300).tolist()
+    inp = synthetic.make_inputs(0, 0, 2, 6100, init_std=0.02, lengths=lengths)
+    kda.set_split(1)
+    try:
+        out, fin = run(kda, inp)
+        cu = inp["cu_seqlens"].tolist()
+        longest = int(np.argmax(lengths))
+        for n in sorted({0, 1, 2, 150, 299, longest, int(np.argmin(lengths))}):
+            t0, t1 = cu[n], cu[n + 1]
+            one = dict(inp)
+            for key in ("q", "k", "v", "g", "beta"):
+                one[key] = inp[key][:, t0:t1].contiguous()
+            one["init_state"] = inp["init_state"][n:n + 1].contiguous()
+            one["cu_seqlens"] = torch.tensor([0, t1 - t0], dtype=torch.int64)
+            one["N"] = 1
+            o1, f1 = run(kda, one)
+            assert torch.equal(o1[0], out[0, t0:t1]) and torch.equal(f1[0], fin[n]), n
+    finally:
+        kda.set_split(0)
+    tu.check_against_oracle(inp, out, fin)
