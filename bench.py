@@ -335,6 +335,7 @@ def run_ours(args):
     packed = inp["cu_seqlens"] is not None
     fused = kda.plan_fused(inp["N"] if packed else inp["q"].shape[0], inp["q"].shape[1],
                            inp["q"].shape[2], packed)
+    long_split = kda.plan_long_split(inp["N"], inp["q"].shape[1], inp["q"].shape[2]) if packed else 0
 
     if ws > 1:
         torch.distributed.barrier()
@@ -396,8 +397,9 @@ def run_ours(args):
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": inp["workload"].name, "l2": "flushed (512 MiB write) before every step",
                    "recurrence_split": nsplit, "recurrence_engine": args.engine,
-                   "one_launch": fused, "head_tokens_per_step": ht},
-        "gpu_launches": (1 if fused else (3 if packed else 2)) * args.steps,
+                   "one_launch": fused, "long_sequences_at_split_2": long_split,
+                   "head_tokens_per_step": ht},
+        "gpu_launches": (1 if fused else (3 + (1 if long_split else 0) if packed else 2)) * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "us_per_call": 1e3 * total_e2e / args.steps},
         "roofline": roofline,

@@ -165,6 +165,16 @@ int kda_set_fusion(int on);
  */
 int kda_plan_fused(int64_t B, int64_t T, int64_t H, int packed, int* fused);
 
+/*
+ * For a packed call of n_seqs sequences (T tokens in all) and H heads: how
+ * many of its longest sequences kda_prefill runs at split 2 in a second,
+ * concurrent recurrence launch on a library-owned stream (HOST out; 0 when
+ * the call uses a single launch).  That happens under engine 0 with the
+ * automatic split when the one-CTA-per-head grid leaves SMs free and
+ * n_seqs <= 1024; the results are bitwise those of split 1.
+ */
+int kda_plan_long_split(int64_t n_seqs, int64_t T, int64_t H, int64_t* k);
+
 /* The split the automatic rule picks on the current device for N*H units (HOST out). */
 int kda_auto_split(int64_t n_seqs, int64_t H, int* nsplit);
 

@@ -9,13 +9,13 @@ streams.  There is no CPU path.
 from __future__ import annotations
 
 from . import _lib
-from ._lib import (KdaError, auto_split, device_status, packet_bytes, plan_fused, set_engine,
-                   set_fusion, set_split, workspace_bytes)
+from ._lib import (KdaError, auto_split, device_status, packet_bytes, plan_fused,
+                   plan_long_split, set_engine, set_fusion, set_split, workspace_bytes)
 
 HEAD_DIM = 128
 
 __all__ = ["kda_prefill", "prep_only", "KdaError", "device_status", "set_split", "set_engine",
-           "set_fusion", "plan_fused", "auto_split",
+           "set_fusion", "plan_fused", "plan_long_split", "auto_split",
            "workspace_bytes", "packet_bytes", "HEAD_DIM"]
 
 

@@ -55,6 +55,8 @@ def load():
         lib.kda_set_fusion.restype = I
         lib.kda_plan_fused.argtypes = [I64, I64, I64, I, ctypes.POINTER(I)]
         lib.kda_plan_fused.restype = I
+        lib.kda_plan_long_split.argtypes = [I64, I64, I64, ctypes.POINTER(I64)]
+        lib.kda_plan_long_split.restype = I
         lib.kda_auto_split.argtypes = [I64, I64, ctypes.POINTER(I)]
         lib.kda_auto_split.restype = I
         lib.kda_workspace_bytes.argtypes = [I64, I64, I64, I, ctypes.POINTER(I64)]
@@ -130,6 +132,14 @@ def plan_fused(B: int, T: int, H: int, packed: bool) -> bool:
     _check(load().kda_plan_fused(int(B), int(T), int(H), 1 if packed else 0, ctypes.byref(out)),
            "kda_plan_fused")
     return bool(out.value)
+
+
+def plan_long_split(n_seqs: int, T: int, H: int) -> int:
+    """How many longest sequences of a packed call run at split 2 in a second launch."""
+    out = ctypes.c_int64(0)
+    _check(load().kda_plan_long_split(int(n_seqs), int(T), int(H), ctypes.byref(out)),
+           "kda_plan_long_split")
+    return int(out.value)
 
 
 def auto_split(n_seqs: int, H: int) -> int:

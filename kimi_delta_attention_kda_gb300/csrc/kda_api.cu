@@ -24,6 +24,10 @@ struct DeviceState {
     int cc_major = 0, cc_minor = 0;
     int* status = nullptr;            // device address of g_device_status
     cudaMemPool_t pool = nullptr;     // library-owned stream-ordered pool
+    // Second stream and fork/join events for a concurrent second recurrence
+    // launch (long packed sequences at split 2); created on first use.
+    cudaStream_t side = nullptr;
+    cudaEvent_t fork = nullptr, join = nullptr;
 };
 
 std::mutex g_mu;
@@ -161,6 +165,32 @@ int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
 // preparation to stay ahead of it.  A preparing warp takes about 25 times as
 // long per packet as the recurrence takes per chunk, so the free SMs'
 // 8 warps each must have at most ~chunks / 4 packets to make.
+// Packed batches whose one-CTA-per-head recurrence fits one wave with SMs
+// to spare: the k longest sequences (the first k of the metadata kernel's
+// longest-first order) run at split 2 in a second, concurrent launch, the
+// rest at split 1.  Returns k (0: no second launch).
+int64_t long_split_count(const Plan& pl, int64_t H, int nsplit, int sms) {
+    if (!pl.packed || g_engine != 0 || g_split_override || nsplit != 1 || pl.N > kMaxOrdered ||
+        pl.tokens <= 0)
+        return 0;
+    const int64_t units = pl.N * H;
+    if (units >= sms) return 0;
+    const int64_t k = (sms - units) / H;
+    return k < pl.N ? k : pl.N;
+}
+
+// The side stream and events of device state d (under g_mu).
+bool ensure_side(DeviceState* d) {
+    if (d->side) return true;
+    if (cudaStreamCreateWithFlags(&d->side, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d->fork, cudaEventDisableTiming) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d->join, cudaEventDisableTiming) != cudaSuccess) {
+        cudaGetLastError();
+        return false;
+    }
+    return true;
+}
+
 bool use_fusion(const Plan& pl, int64_t H, int nsplit, int sms) {
     if (!g_fusion || g_engine != 0 || pl.packed || pl.tokens <= 0) return false;
     if (!fused_supported(pl.N, H, nsplit, sms)) return false;
@@ -291,15 +321,35 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
     }
     if (rc == KDA_OK && !done) {
         // A recurrence grid of more than one wave starts the longest
-        // sequences first (packed layout).
-        const bool ordered = pl.packed && pl.N * H * nsplit > d->sms;
+        // sequences first; a grid of less than one wave gives the longest
+        // sequences more CTAs (packed layout).
+        const int64_t k_long = long_split_count(pl, H, nsplit, d->sms);
+        const bool ordered = pl.packed && (pl.N * H * nsplit > d->sms || k_long > 0);
         rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, ws + pl.meta_bytes, d, stream, &geo,
                       ordered);
         prof_record(1, stream);
-        if (rc == KDA_OK &&
-            launch_recurrence(v, out, init_state, final_state, ws + pl.meta_bytes, geo, H, nsplit,
-                              d->status, stream, ck) != cudaSuccess)
+        if (rc == KDA_OK && k_long > 0) {
+            // Fork: slots 0 .. k_long-1 (the longest) at split 2 on the side
+            // stream, the rest at split 1 on the caller's stream; join.
+            std::lock_guard<std::mutex> lock(g_mu);
+            SeqGeometry g_long = geo, g_rest = geo;
+            g_long.n_seqs = k_long;
+            g_rest.first_slot = k_long;
+            uint8_t* packets = ws + pl.meta_bytes;
+            if (!ensure_side(d) || cudaEventRecord(d->fork, stream) != cudaSuccess ||
+                cudaStreamWaitEvent(d->side, d->fork, 0) != cudaSuccess ||
+                launch_recurrence(v, out, init_state, final_state, packets, g_long, H, 2, d->status,
+                                  d->side, ck) != cudaSuccess ||
+                launch_recurrence(v, out, init_state, final_state, packets, g_rest, H, 1, d->status,
+                                  stream, ck) != cudaSuccess ||
+                cudaEventRecord(d->join, d->side) != cudaSuccess ||
+                cudaStreamWaitEvent(stream, d->join, 0) != cudaSuccess)
+                rc = KDA_ERR_CUDA;
+        } else if (rc == KDA_OK &&
+                   launch_recurrence(v, out, init_state, final_state, ws + pl.meta_bytes, geo, H,
+                                     nsplit, d->status, stream, ck) != cudaSuccess) {
             rc = KDA_ERR_CUDA;
+        }
     }
     prof_record(2, stream);
     if (g_prof.active && g_prof.calls < g_prof.max_calls) g_prof.calls += 1;
@@ -424,6 +474,18 @@ extern "C" int kda_plan_fused(int64_t B, int64_t T, int64_t H, int packed, int* 
     rc = device_state(&d);
     if (rc != KDA_OK) return rc;
     *fused = use_fusion(pl, H, choose_split(pl.N * H, d->sms), d->sms) ? 1 : 0;
+    return KDA_OK;
+}
+
+extern "C" int kda_plan_long_split(int64_t n_seqs, int64_t T, int64_t H, int64_t* k) {
+    if (!k) return KDA_ERR_NULL;
+    Plan pl;
+    int rc = make_plan(n_seqs, T, H, true, &pl);
+    if (rc != KDA_OK) return rc;
+    DeviceState* d = nullptr;
+    rc = device_state(&d);
+    if (rc != KDA_OK) return rc;
+    *k = long_split_count(pl, H, choose_split(pl.N * H, d->sms), d->sms);
     return KDA_OK;
 }
 

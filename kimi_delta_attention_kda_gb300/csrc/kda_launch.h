@@ -24,6 +24,9 @@ struct SeqGeometry {
     // longest-first order (slot i runs sequence order[i]), from the metadata
     // kernel, so that the longest sequences start in the first wave.
     const int32_t* order;
+    // Recurrence CTAs whose sequence slot is below first_slot return at once
+    // (those sequences run in a second, concurrent launch).
+    int64_t first_slot;
     int* status;                 // device status word (set by the launchers)
 };
 

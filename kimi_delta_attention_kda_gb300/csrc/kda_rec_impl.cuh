@@ -166,6 +166,7 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
     const int split = static_cast<int>(block - nh * a.nsplit);
     const int64_t n_slot = nh / a.H;
     const int64_t h = nh - n_slot * a.H;
+    if (n_slot < a.geo.first_slot) return;   // runs in the other launch
     const int64_t n = a.geo.order ? a.geo.order[n_slot] : n_slot;   // longest-first (packed)
     const int v0 = split * L::kCols;
 

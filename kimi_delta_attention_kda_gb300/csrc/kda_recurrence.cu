@@ -199,6 +199,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
     const int split = blockIdx.x - nh * a.nsplit;
     const int64_t n_slot = nh / a.H;
     const int64_t h = nh - n_slot * a.H;
+    if (n_slot < a.geo.first_slot) return;   // runs in the other launch
     const int64_t n = a.geo.order ? a.geo.order[n_slot] : n_slot;   // longest-first (packed)
     const int v0 = split * L::kCols;
 
@@ -456,6 +457,7 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     const int lane = threadIdx.x & 31;
     const int64_t n_slot = blockIdx.x / a.H;
     const int64_t h = blockIdx.x - n_slot * a.H;
+    if (n_slot < a.geo.first_slot) return;   // runs in the other launch
     const int64_t n = a.geo.order ? a.geo.order[n_slot] : n_slot;   // longest-first (packed)
 
     int64_t c_begin, nch, tok0, seqlen;

@@ -457,3 +457,22 @@ def test_packed_many_sequences_longest_first(kda):
     finally:
         kda.set_split(0)
     tu.check_against_oracle(inp, out, fin)
+
+
+def test_long_sequences_at_split_two_bitwise(kda):
+    """The packed 12-head workload (8 sequences, 96 one-CTA-per-head units on
+    152 SMs): its 4 longest sequences run at split 2 in a second, concurrent
+    launch.  Splits 1 and 2 sum in the same order, so the call equals the
+    single-launch split-1 call bit for bit."""
+    inp = synthetic.make_workload("varlen8_h12")
+    N, T = inp["N"], inp["q"].shape[1]
+    props = torch.cuda.get_device_properties(0)
+    assert kda.plan_long_split(N, T, 12) == min(N, (props.multi_processor_count - N * 12) // 12)
+    a = run(kda, inp)
+    kda.set_split(1)
+    try:
+        assert kda.plan_long_split(N, T, 12) == 0
+        b = run(kda, inp)
+    finally:
+        kda.set_split(0)
+    assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
