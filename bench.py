@@ -69,9 +69,9 @@ REC_SOURCES = ("kda_recurrence.cu", "kda_rec_impl.cuh", "kda_common.cuh")
 PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
 FUSED_SOURCES = ("kda_fused.cu", "kda_prep_impl.cuh", "kda_rec_impl.cuh", "kda_common.cuh")
 PROFILED_TRAFFIC = {
-    ("fused", "t8192_h6"): (77.900e6, FUSED_SOURCES, "ec2a6931cf32a73c"),
-    ("recurrence", "t8192_h96"): (1066.989e6, REC_SOURCES, "369416dc86b00a10"),
-    ("chunk_prep", "t8192_h96"): (1466.940e6, PREP_SOURCES, "c2cf1618b34710a2"),
+    ("fused", "t8192_h6"): (77.884e6, FUSED_SOURCES, "aa0f826f6b03cd6a"),
+    ("recurrence", "t8192_h96"): (1067.049e6, REC_SOURCES, "806d87c2bfa734e7"),
+    ("chunk_prep", "t8192_h96"): (1460.424e6, PREP_SOURCES, "f4ed658ee797cb7a"),
 }
 
 
