@@ -56,10 +56,16 @@ L2_FLUSH_BYTES = 512 << 20
 #                the whole path, q, k, g, beta, v in and O out (1,538 B per
 #                head-token) plus the states; the packets pass between the two
 #                halves of the launch and are not counted.
+#   segmented scan: the transition pass reads the packets twice and v once
+#                (1,984 B per head-token) and writes two states per (segment,
+#                head); the segment chain reads two states and writes one per
+#                (segment, head); the rerun is the recurrence above plus one
+#                state read per (segment, head).
 PACKET_PER_TOKEN = 13824 / 16
 PREP_BYTES_PER_HT = 2 * 256 + 512 + 2 + PACKET_PER_TOKEN
 REC_BYTES_PER_HT = PACKET_PER_TOKEN + 256 + 256
 PATH_BYTES_PER_HT = 2 * 256 + 512 + 2 + 256 + 256
+TRANSITION_BYTES_PER_HT = 2 * PACKET_PER_TOKEN + 256
 STATE_BYTES = 128 * 128 * 2
 
 # DRAM bytes (read + write) of one launch of the dominant kernel, from one ncu
@@ -188,7 +194,7 @@ def time_kernel_steps(kda, d, steps, warmup, flush, stream, profile=False):
             call()
             ends[i].record(stream)
         stream.synchronize()
-        prof = kda._lib.profile_end() if profile else None
+        prof = kda._lib.profile_end_detail() if profile else None
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
     return ms, prof
 
@@ -325,6 +331,7 @@ def run_ours(args):
     if args.engine:
         kda.set_engine(args.engine)
     kda.set_fusion(bool(args.fusion))
+    kda.set_segments(bool(args.segments))
     stream = torch.cuda.Stream(device=device)
     flush = torch.empty(L2_FLUSH_BYTES // 4, dtype=torch.float32, device=device)
 
@@ -335,6 +342,8 @@ def run_ours(args):
     packed = inp["cu_seqlens"] is not None
     fused = kda.plan_fused(inp["N"] if packed else inp["q"].shape[0], inp["q"].shape[1],
                            inp["q"].shape[2], packed)
+    segs = kda.plan_segments(inp["N"] if packed else inp["q"].shape[0], inp["q"].shape[1],
+                             inp["q"].shape[2], packed)
     long_split = kda.plan_long_split(inp["N"], inp["q"].shape[1], inp["q"].shape[2]) if packed else 0
 
     if ws > 1:
@@ -362,22 +371,28 @@ def run_ours(args):
     value = ws * ht * args.steps / (total_ms * 1e-3)
     e2e_value = ws * ht * args.steps / (total_e2e * 1e-3)
 
-    prep_ms, rec_ms, calls = prof
-    prep_avg, rec_avg = prep_ms / calls, rec_ms / calls
+    intervals, calls = prof
+    prep_avg, trans_avg, chain_avg, rec_avg = (t / calls for t in intervals)
     peak, peak_kind = measured_peaks()
     H = inp["q"].shape[2]
     n_states = inp["N"] * H
     state_io = (2 if inp["init_state"] is not None else 1) * n_states * STATE_BYTES
-    rec_bytes = REC_BYTES_PER_HT * ht + state_io
+    seg_states = n_states * segs * STATE_BYTES
     prep_bytes = PREP_BYTES_PER_HT * ht
     if fused:
         # The profile's first interval is the reset of the ready flags, the
-        # second the one launch.
-        dom, dom_bytes, dom_ms = "fused", PATH_BYTES_PER_HT * ht + state_io, rec_avg
-    elif rec_avg >= prep_avg:
-        dom, dom_bytes, dom_ms = "recurrence", rec_bytes, rec_avg
+        # last the one launch.
+        kernels = {"fused": (PATH_BYTES_PER_HT * ht + state_io, rec_avg)}
+    elif segs:
+        kernels = {"chunk_prep": (prep_bytes, prep_avg),
+                   "transition": (TRANSITION_BYTES_PER_HT * ht + 2 * seg_states, trans_avg),
+                   "segment_chain": (3 * seg_states + state_io, chain_avg),
+                   "recurrence": (REC_BYTES_PER_HT * ht + seg_states, rec_avg)}
     else:
-        dom, dom_bytes, dom_ms = "chunk_prep", prep_bytes, prep_avg
+        kernels = {"chunk_prep": (prep_bytes, prep_avg),
+                   "recurrence": (REC_BYTES_PER_HT * ht + state_io, rec_avg)}
+    dom = max(kernels, key=lambda k: kernels[k][1])
+    dom_bytes, dom_ms = kernels[dom]
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
                 "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
@@ -388,6 +403,8 @@ def run_ours(args):
         roofline.update({"fused_us": 1e3 * rec_avg, "flag_reset_us": 1e3 * prep_avg})
     else:
         roofline.update({"prep_us": 1e3 * prep_avg, "recurrence_us": 1e3 * rec_avg})
+    if segs:
+        roofline.update({"transition_us": 1e3 * trans_avg, "segment_chain_us": 1e3 * chain_avg})
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -396,10 +413,11 @@ def run_ours(args):
         "higher_is_better": True, "scaling": "weak",
         "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": {"workload": inp["workload"].name, "l2": "flushed (512 MiB write) before every step",
-                   "recurrence_split": nsplit, "recurrence_engine": args.engine,
+                   "recurrence_split": 1 if segs else nsplit, "recurrence_engine": args.engine,
                    "one_launch": fused, "long_sequences_at_split_2": long_split,
-                   "head_tokens_per_step": ht},
-        "gpu_launches": (1 if fused else (3 + (1 if long_split else 0) if packed else 2)) * args.steps,
+                   "segments_per_sequence": segs, "head_tokens_per_step": ht},
+        "gpu_launches": (1 if fused else 4 if segs else
+                         (3 + (1 if long_split else 0) if packed else 2)) * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "us_per_call": 1e3 * total_e2e / args.steps},
         "roofline": roofline,
@@ -420,8 +438,8 @@ def run_ours(args):
         t2 = sum(ms2) / len(ms2)
         line["secondary"] = {"workload": sec["workload"].name, "us_per_call": 1e3 * t2,
                              "value": ht2 / (t2 * 1e-3), "unit": UNIT,
-                             "prep_us": 1e3 * prof2[0] / prof2[2],
-                             "recurrence_us": 1e3 * prof2[1] / prof2[2],
+                             "prep_us": 1e3 * prof2[0][0] / prof2[1],
+                             "recurrence_us": 1e3 * sum(prof2[0][1:]) / prof2[1],
                              "recurrence_split": kda.auto_split(1, 96),
                              "vs_flashkda_b200": (ht2 / (t2 * 1e-3)) /
                              (ht2 / (FLASHKDA_B200_US["t8192_h96"] * 1e-6))}
@@ -451,6 +469,8 @@ def main():
                     help="recurrence engine: 0 automatic, 1 column-split warp MMA, 2 tcgen05")
     ap.add_argument("--fusion", type=int, default=1, choices=[0, 1],
                     help="allow preparation and recurrence as one launch (kda_set_fusion)")
+    ap.add_argument("--segments", type=int, default=1, choices=[0, 1],
+                    help="allow the segmented scan over chunks (kda_set_segments)")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be at least 3")

@@ -175,13 +175,41 @@ int kda_plan_fused(int64_t B, int64_t T, int64_t H, int packed, int* fused);
  */
 int kda_plan_long_split(int64_t n_seqs, int64_t T, int64_t H, int64_t* k);
 
+/*
+ * Whether kda_prefill may use the segmented scan over chunks (1, the default)
+ * or always runs each (sequence, head) as one serial chain of chunk steps (0).
+ * The chunkwise state update is affine in the incoming state, so over a run
+ * of chunks it is S -> S F + Z ("Kimi Linear" technical report, chunkwise
+ * KDA: S_{c+1} = S_c D_c + U_c K^end_c with U_c affine in S_c).  When there
+ * are too few (sequence, head) chains to fill the GPU (fixed-length batches,
+ * engine 0, automatic split, no checkpoints), each sequence is cut into
+ * segments: one launch forms every segment's F and Z, a short chain over the
+ * segments forms each segment's incoming state, and one launch reruns every
+ * segment from its incoming state and writes O.  The results agree with the
+ * serial chain to rounding (the incoming states are rounded to BF16), not bit
+ * for bit.  seg_chunks 0 lets a cost estimate decide whether and how to cut;
+ * seg_chunks > 0 cuts every eligible call into segments of that many chunks
+ * (for tests).  Process-wide; returns KDA_ERR_ARG for on not 0 or 1 or
+ * seg_chunks negative or above 2^26.
+ */
+int kda_set_segments(int on, int64_t seg_chunks);
+
+/*
+ * Segments per sequence kda_prefill would use for a call of this shape on the
+ * current device under the current settings (HOST out; 0: no segmented scan).
+ * Errors as kda_plan_fused.
+ */
+int kda_plan_segments(int64_t B, int64_t T, int64_t H, int packed, int64_t* segs);
+
 /* The split the automatic rule picks on the current device for N*H units (HOST out). */
 int kda_auto_split(int64_t n_seqs, int64_t H, int* nsplit);
 
 /*
  * Bytes of scratch kda_prefill takes for a given shape at most (HOST out);
  * `packed` is nonzero for the packed layout.  The ready flags of a fused
- * launch (kda_set_fusion) are counted whether or not the call fuses.
+ * launch (kda_set_fusion) are counted whether or not the call fuses; the
+ * segmented scan's three state buffers (kda_set_segments) when the current
+ * device (a 152-SM one when there is none) would use it.
  */
 int kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int packed, int64_t* bytes);
 
@@ -201,18 +229,23 @@ int64_t kda_packet_bytes(void);
 
 /*
  * Per-kernel timing for benchmarks.  kda_profile_begin(max_calls) creates
- * 3 * max_calls CUDA events on the current device; each of the next
- * max_calls kda_prefill calls then records one event before its preparation
- * kernels, one between preparation and recurrence and one after the
- * recurrence, on its own stream.  When a call runs as one launch (see
- * kda_set_fusion), the first interval holds only the reset of the ready flags
- * and the second the fused kernel.  kda_profile_end synchronises those events,
- * writes the summed preparation and recurrence times in milliseconds and the
- * number of calls timed (HOST pointers), and destroys the events.
- * Process-wide; begin while active returns KDA_ERR_ARG.
+ * 5 * max_calls CUDA events on the current device; each of the next
+ * max_calls kda_prefill calls then records, on its own stream, one event
+ * before its preparation kernels, one after them, one after the transition
+ * pass and one after the segment chain of a segmented scan (see
+ * kda_set_segments; recorded right after the second otherwise), and one after
+ * the recurrence.  When a call runs as one launch (see kda_set_fusion), the
+ * first interval holds only the reset of the ready flags and the last the
+ * fused kernel.  kda_profile_end synchronises those events, writes the summed
+ * preparation time and recurrence time (the last three intervals) in
+ * milliseconds and the number of calls timed (HOST pointers), and destroys
+ * the events; kda_profile_end_detail does the same but writes the four
+ * summed intervals to intervals_ms[0..3].  Process-wide; begin while active
+ * returns KDA_ERR_ARG.
  */
 int kda_profile_begin(int max_calls);
 int kda_profile_end(double* prep_ms, double* recurrence_ms, int* calls);
+int kda_profile_end_detail(double* intervals_ms, int* calls);
 
 /*
  * kda_prefill without any allocation.  The pages describe no such entry

@@ -10,12 +10,14 @@ from __future__ import annotations
 
 from . import _lib
 from ._lib import (KdaError, auto_split, device_status, packet_bytes, plan_fused,
-                   plan_long_split, set_engine, set_fusion, set_split, workspace_bytes)
+                   plan_long_split, plan_segments, set_engine, set_fusion, set_segments,
+                   set_split, workspace_bytes)
 
 HEAD_DIM = 128
 
 __all__ = ["kda_prefill", "prep_only", "KdaError", "device_status", "set_split", "set_engine",
-           "set_fusion", "plan_fused", "plan_long_split", "auto_split",
+           "set_fusion", "plan_fused", "plan_long_split", "set_segments", "plan_segments",
+           "auto_split",
            "workspace_bytes", "packet_bytes", "HEAD_DIM"]
 
 

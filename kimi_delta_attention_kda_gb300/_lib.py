@@ -53,6 +53,10 @@ def load():
         lib.kda_set_engine.restype = I
         lib.kda_set_fusion.argtypes = [I]
         lib.kda_set_fusion.restype = I
+        lib.kda_set_segments.argtypes = [I, I64]
+        lib.kda_set_segments.restype = I
+        lib.kda_plan_segments.argtypes = [I64, I64, I64, I, ctypes.POINTER(I64)]
+        lib.kda_plan_segments.restype = I
         lib.kda_plan_fused.argtypes = [I64, I64, I64, I, ctypes.POINTER(I)]
         lib.kda_plan_fused.restype = I
         lib.kda_plan_long_split.argtypes = [I64, I64, I64, ctypes.POINTER(I64)]
@@ -70,6 +74,8 @@ def load():
         D = ctypes.POINTER(ctypes.c_double)
         lib.kda_profile_end.argtypes = [D, D, ctypes.POINTER(I)]
         lib.kda_profile_end.restype = I
+        lib.kda_profile_end_detail.argtypes = [D, ctypes.POINTER(I)]
+        lib.kda_profile_end_detail.restype = I
         lib.kda_prefill_noalloc.argtypes = [P] * 8 + [I64] * 3 + [P, P]
         lib.kda_prefill_noalloc.restype = I
         lib.kda_noalloc_scratch_bytes.argtypes = []
@@ -126,6 +132,20 @@ def set_fusion(on: bool):
     _check(load().kda_set_fusion(1 if on else 0), "kda_set_fusion")
 
 
+def set_segments(on: bool, seg_chunks: int = 0):
+    """Allow (True, the default) or forbid the segmented scan over chunks;
+    seg_chunks > 0 forces segments of that many chunks on every eligible call."""
+    _check(load().kda_set_segments(1 if on else 0, int(seg_chunks)), "kda_set_segments")
+
+
+def plan_segments(B: int, T: int, H: int, packed: bool) -> int:
+    """Segments per sequence kda_prefill uses for this shape (0: serial chain)."""
+    out = ctypes.c_int64(0)
+    _check(load().kda_plan_segments(int(B), int(T), int(H), 1 if packed else 0, ctypes.byref(out)),
+           "kda_plan_segments")
+    return int(out.value)
+
+
 def plan_fused(B: int, T: int, H: int, packed: bool) -> bool:
     """Whether kda_prefill runs this shape as one launch on the current device."""
     out = ctypes.c_int(0)
@@ -175,6 +195,14 @@ def profile_end():
     _check(load().kda_profile_end(ctypes.byref(p), ctypes.byref(r), ctypes.byref(n)),
            "kda_profile_end")
     return p.value, r.value, n.value
+
+
+def profile_end_detail():
+    """Returns ([prep, transition, segment chain, recurrence] ms totals, calls)."""
+    t = (ctypes.c_double * 4)()
+    n = ctypes.c_int(0)
+    _check(load().kda_profile_end_detail(t, ctypes.byref(n)), "kda_profile_end_detail")
+    return [t[i] for i in range(4)], n.value
 
 
 def prefill_noalloc_raw(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,

@@ -35,6 +35,8 @@ DeviceState g_dev[kMaxDevices];
 int g_split_override = 0;
 int g_engine = 0;
 int g_fusion = 1;
+int g_segments = 1;
+int64_t g_seg_chunks = 0;   // > 0: forced segment length (kda_set_segments)
 
 // Optional per-kernel timing: when active, each kda_prefill call records three
 // events on its stream (before the preparation kernels, between preparation
@@ -48,9 +50,14 @@ struct Profile {
 };
 Profile g_prof;
 
+// Events per call: 0 before the preparation, 1 after it, 2 after the
+// transition pass and 3 after the segment chain of a segmented scan (else
+// recorded right after 1), 4 after the recurrence.
+constexpr int kProfEvents = 5;
+
 void prof_record(int which, cudaStream_t stream) {
     if (!g_prof.active || g_prof.calls >= g_prof.max_calls) return;
-    cudaEventRecord(g_prof.ev[3 * g_prof.calls + which], stream);
+    cudaEventRecord(g_prof.ev[kProfEvents * g_prof.calls + which], stream);
 }
 
 int device_state(DeviceState** out) {
@@ -179,6 +186,53 @@ int64_t long_split_count(const Plan& pl, int64_t H, int nsplit, int sms) {
     return k < pl.N ? k : pl.N;
 }
 
+// Segmented scan over chunks (kda_segments.cu): with few (sequence, head)
+// chains the serial recurrence leaves most SMs idle, so each sequence is cut
+// into `segs` segments of seg_chunks chunks and run in three launches (every
+// segment's zero-start state and state map; a short chain over the segments;
+// every segment again from its true incoming state).  The choice compares
+// rough costs in microseconds, measured on GB300 at T = 8192: a chunk step
+// of the serial chain at split 8-16, of the one-CTA-per-head kernel, and of
+// its transition pass; a step of the segment chain; the launches' fixed cost.
+constexpr double kSerialChunkUs = 0.35;
+constexpr double kQuadChunkUs = 1.0;
+constexpr double kTransChunkUs = 0.7;
+constexpr double kScanStepUs = 0.3;
+constexpr double kSegFixedUs = 25.0;
+
+struct SegChoice {
+    int64_t segs = 0;         // segments per sequence (0: no segmented scan)
+    int64_t seg_chunks = 0;   // chunks per segment (the last one of a sequence shorter)
+    int64_t state_bytes = 0;  // bytes of each of the three [N * segs][H][128][128] BF16 buffers
+};
+
+SegChoice plan_segments(const Plan& pl, int64_t H, int sms, bool checkpoints) {
+    SegChoice sc;
+    if (!g_segments || g_engine != 0 || g_split_override || pl.packed || checkpoints ||
+        pl.tokens <= 0)
+        return sc;
+    const int64_t units = pl.N * H;
+    const int64_t chunks = pl.geo.chunks_per_seq;
+    if (g_seg_chunks > 0) {
+        sc.seg_chunks = g_seg_chunks;
+        sc.segs = (chunks + g_seg_chunks - 1) / g_seg_chunks;
+        sc.state_bytes = pl.N * sc.segs * H * kHeadDim * kHeadDim * 2;
+        return sc;
+    }
+    const int64_t target = sms / units;   // segments per sequence: one wave in the last pass
+    if (target < 4) return sc;
+    const int64_t L = (chunks + target - 1) / target;
+    const int64_t segs = (chunks + L - 1) / L;
+    if (segs < 4) return sc;
+    const double waves = static_cast<double>((2 * segs * units + sms - 1) / sms);
+    const double seg_us = kSegFixedUs + L * (waves * kTransChunkUs + kQuadChunkUs) + segs * kScanStepUs;
+    if (seg_us >= chunks * kSerialChunkUs) return sc;
+    sc.segs = segs;
+    sc.seg_chunks = L;
+    sc.state_bytes = pl.N * segs * H * kHeadDim * kHeadDim * 2;
+    return sc;
+}
+
 // The side stream and events of device state d (under g_mu).
 bool ensure_side(DeviceState* d) {
     if (d->side) return true;
@@ -290,8 +344,10 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
     cudaStream_t stream = static_cast<cudaStream_t>(stream_ptr);
 
     const int nsplit = choose_split(pl.N * H, d->sms);
-    const bool fused = use_fusion(pl, H, nsplit, d->sms);
-    const int64_t ws_bytes = pl.meta_bytes + pl.packet_bytes + (fused ? pl.ready_bytes : 0);
+    const SegChoice sc = plan_segments(pl, H, d->sms, ck != nullptr);
+    const bool fused = sc.segs == 0 && use_fusion(pl, H, nsplit, d->sms);
+    const int64_t ws_bytes =
+        pl.meta_bytes + pl.packet_bytes + (fused ? pl.ready_bytes : 0) + 3 * sc.state_bytes;
     uint8_t* ws = nullptr;
     if (ws_bytes > 0) {
         if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes),
@@ -311,6 +367,8 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         if (cudaMemsetAsync(ready, 0, static_cast<size_t>(pl.ready_bytes), stream) != cudaSuccess)
             rc = KDA_ERR_CUDA;
         prof_record(1, stream);
+        prof_record(2, stream);
+        prof_record(3, stream);
         if (rc == KDA_OK) {
             if (launch_fused(q, k, g, beta, v, out, init_state, final_state, ws + pl.meta_bytes,
                              ready, pl.geo, H, nsplit, kScale, d->status, stream, ck) == cudaSuccess)
@@ -318,6 +376,32 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
             else
                 cudaGetLastError();
         }
+    }
+    if (rc == KDA_OK && !done && sc.segs > 0) {
+        // Segmented scan: preparation, then the three recurrence passes.
+        uint8_t* packets = ws + pl.meta_bytes;
+        uint8_t* zstates = packets + pl.packet_bytes;
+        uint8_t* maps = zstates + sc.state_bytes;
+        uint8_t* starts = maps + sc.state_bytes;
+        rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, packets, d, stream, &geo);
+        prof_record(1, stream);
+        SeqGeometry sg = geo;
+        sg.n_seqs = pl.N * sc.segs;
+        sg.seg_chunks = sc.seg_chunks;
+        sg.segs_per_seq = sc.segs;
+        if (rc == KDA_OK &&
+            launch_transition(v, packets, sg, H, zstates, maps, d->status, stream) != cudaSuccess)
+            rc = KDA_ERR_CUDA;
+        prof_record(2, stream);
+        if (rc == KDA_OK && launch_segment_scan(init_state, final_state, maps, zstates, starts, pl.N,
+                                                sc.segs, H, d->status, stream) != cudaSuccess)
+            rc = KDA_ERR_CUDA;
+        prof_record(3, stream);
+        if (rc == KDA_OK &&
+            launch_recurrence(v, out, starts, nullptr, packets, sg, H, 1, d->status, stream) !=
+                cudaSuccess)
+            rc = KDA_ERR_CUDA;
+        done = true;
     }
     if (rc == KDA_OK && !done) {
         // A recurrence grid of more than one wave starts the longest
@@ -328,6 +412,8 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, ws + pl.meta_bytes, d, stream, &geo,
                       ordered);
         prof_record(1, stream);
+        prof_record(2, stream);
+        prof_record(3, stream);
         if (rc == KDA_OK && k_long > 0) {
             // Fork: slots 0 .. k_long-1 (the longest) at split 2 on the side
             // stream, the rest at split 1 on the caller's stream; join.
@@ -351,7 +437,7 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
             rc = KDA_ERR_CUDA;
         }
     }
-    prof_record(2, stream);
+    prof_record(4, stream);
     if (g_prof.active && g_prof.calls < g_prof.max_calls) g_prof.calls += 1;
     if (ws) cudaFreeAsync(ws, stream);
     if (rc != KDA_OK) cudaGetLastError();
@@ -473,7 +559,10 @@ extern "C" int kda_plan_fused(int64_t B, int64_t T, int64_t H, int packed, int* 
     DeviceState* d = nullptr;
     rc = device_state(&d);
     if (rc != KDA_OK) return rc;
-    *fused = use_fusion(pl, H, choose_split(pl.N * H, d->sms), d->sms) ? 1 : 0;
+    *fused = plan_segments(pl, H, d->sms, false).segs == 0 &&
+                     use_fusion(pl, H, choose_split(pl.N * H, d->sms), d->sms)
+                 ? 1
+                 : 0;
     return KDA_OK;
 }
 
@@ -492,6 +581,25 @@ extern "C" int kda_plan_long_split(int64_t n_seqs, int64_t T, int64_t H, int64_t
 extern "C" int kda_set_fusion(int on) {
     if (on != 0 && on != 1) return KDA_ERR_ARG;
     g_fusion = on;
+    return KDA_OK;
+}
+
+extern "C" int kda_set_segments(int on, int64_t seg_chunks) {
+    if ((on != 0 && on != 1) || seg_chunks < 0 || seg_chunks > (int64_t(1) << 26)) return KDA_ERR_ARG;
+    g_segments = on;
+    g_seg_chunks = seg_chunks;
+    return KDA_OK;
+}
+
+extern "C" int kda_plan_segments(int64_t B, int64_t T, int64_t H, int packed, int64_t* segs) {
+    if (!segs) return KDA_ERR_NULL;
+    Plan pl;
+    int rc = make_plan(B, T, H, packed != 0, &pl);
+    if (rc != KDA_OK) return rc;
+    DeviceState* d = nullptr;
+    rc = device_state(&d);
+    if (rc != KDA_OK) return rc;
+    *segs = plan_segments(pl, H, d->sms, false).segs;
     return KDA_OK;
 }
 
@@ -516,7 +624,13 @@ extern "C" int kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int packed, 
     Plan pl;
     int rc = make_plan(B, T, H, packed != 0, &pl);
     if (rc != KDA_OK) return rc;
-    *bytes = pl.meta_bytes + pl.packet_bytes + (pl.packed ? 0 : pl.ready_bytes);
+    // The segmented scan's buffers as planned on the current device (on a
+    // 152-SM device when there is none).
+    int sms = 152;
+    DeviceState* d = nullptr;
+    if (device_state(&d) == KDA_OK) sms = d->sms;
+    const SegChoice sc = plan_segments(pl, H, sms, false);
+    *bytes = pl.meta_bytes + pl.packet_bytes + (pl.packed ? 0 : pl.ready_bytes) + 3 * sc.state_bytes;
     return KDA_OK;
 }
 
@@ -526,8 +640,8 @@ extern "C" int kda_profile_begin(int max_calls) {
     if (max_calls < 1 || max_calls > (1 << 20)) return KDA_ERR_ARG;
     std::lock_guard<std::mutex> lock(g_mu);
     if (g_prof.active) return KDA_ERR_ARG;
-    g_prof.ev = new cudaEvent_t[3 * static_cast<size_t>(max_calls)];
-    for (int i = 0; i < 3 * max_calls; ++i) {
+    g_prof.ev = new cudaEvent_t[kProfEvents * static_cast<size_t>(max_calls)];
+    for (int i = 0; i < kProfEvents * max_calls; ++i) {
         if (cudaEventCreate(&g_prof.ev[i]) != cudaSuccess) {
             for (int j = 0; j < i; ++j) cudaEventDestroy(g_prof.ev[j]);
             delete[] g_prof.ev;
@@ -542,29 +656,36 @@ extern "C" int kda_profile_begin(int max_calls) {
     return KDA_OK;
 }
 
-extern "C" int kda_profile_end(double* prep_ms, double* recurrence_ms, int* calls) {
-    if (!prep_ms || !recurrence_ms || !calls) return KDA_ERR_NULL;
+extern "C" int kda_profile_end_detail(double* intervals_ms, int* calls) {
+    if (!intervals_ms || !calls) return KDA_ERR_NULL;
     std::lock_guard<std::mutex> lock(g_mu);
     if (!g_prof.active) return KDA_ERR_ARG;
-    double p = 0.0, r = 0.0;
+    double t[kProfEvents - 1] = {};
     int rc = KDA_OK;
-    for (int c = 0; c < g_prof.calls; ++c) {
-        float a = 0.f, b = 0.f;
-        if (cudaEventSynchronize(g_prof.ev[3 * c + 2]) != cudaSuccess ||
-            cudaEventElapsedTime(&a, g_prof.ev[3 * c], g_prof.ev[3 * c + 1]) != cudaSuccess ||
-            cudaEventElapsedTime(&b, g_prof.ev[3 * c + 1], g_prof.ev[3 * c + 2]) != cudaSuccess) {
-            rc = KDA_ERR_CUDA;
-            cudaGetLastError();
-            break;
+    for (int c = 0; c < g_prof.calls && rc == KDA_OK; ++c) {
+        const cudaEvent_t* ev = g_prof.ev + kProfEvents * c;
+        if (cudaEventSynchronize(ev[kProfEvents - 1]) != cudaSuccess) rc = KDA_ERR_CUDA;
+        for (int i = 0; i + 1 < kProfEvents && rc == KDA_OK; ++i) {
+            float ms = 0.f;
+            if (cudaEventElapsedTime(&ms, ev[i], ev[i + 1]) != cudaSuccess)
+                rc = KDA_ERR_CUDA;
+            t[i] += ms;
         }
-        p += a;
-        r += b;
     }
-    *prep_ms = p;
-    *recurrence_ms = r;
+    if (rc != KDA_OK) cudaGetLastError();
+    for (int i = 0; i + 1 < kProfEvents; ++i) intervals_ms[i] = t[i];
     *calls = g_prof.calls;
-    for (int i = 0; i < 3 * g_prof.max_calls; ++i) cudaEventDestroy(g_prof.ev[i]);
+    for (int i = 0; i < kProfEvents * g_prof.max_calls; ++i) cudaEventDestroy(g_prof.ev[i]);
     delete[] g_prof.ev;
     g_prof = Profile{};
+    return rc;
+}
+
+extern "C" int kda_profile_end(double* prep_ms, double* recurrence_ms, int* calls) {
+    if (!prep_ms || !recurrence_ms || !calls) return KDA_ERR_NULL;
+    double t[kProfEvents - 1] = {};
+    const int rc = kda_profile_end_detail(t, calls);
+    *prep_ms = t[0];
+    *recurrence_ms = t[1] + t[2] + t[3];
     return rc;
 }

@@ -255,6 +255,18 @@ __device__ __forceinline__ bool pair_all(int id, bool p) {
         : "memory");
     return r != 0;
 }
+// The same for a group of kThreads threads (a multiple of 32) on barrier `id`.
+template <int kThreads>
+__device__ __forceinline__ bool group_all(int id, bool p) {
+    uint32_t r;
+    asm volatile(
+        "{\n .reg .pred q, a;\n setp.ne.u32 q, %1, 0;\n bar.red.and.pred a, %2, %3, q;\n"
+        " selp.u32 %0, 1, 0, a;\n}\n"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(p)), "r"(id), "n"(kThreads)
+        : "memory");
+    return r != 0;
+}
 
 __device__ __forceinline__ void ldsm_x4(uint32_t* r, uint32_t addr) {
     asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0,%1,%2,%3}, [%4];"

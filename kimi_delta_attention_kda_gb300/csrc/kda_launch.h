@@ -27,6 +27,11 @@ struct SeqGeometry {
     // Recurrence CTAs whose sequence slot is below first_slot return at once
     // (those sequences run in a second, concurrent launch).
     int64_t first_slot;
+    // Fixed layout only, 0 for none: each sequence is cut into segments of
+    // seg_chunks chunks (the last one shorter), and "sequence" n of the
+    // recurrence is segment n % segs_per_seq of sequence n / segs_per_seq.
+    int64_t seg_chunks;
+    int64_t segs_per_seq;
     int* status;                 // device status word (set by the launchers)
 };
 
@@ -58,6 +63,22 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
                               const SeqGeometry& geo, int64_t H, int nsplit, int* status,
                               cudaStream_t stream, const Checkpoints* ck = nullptr);
 
+// First pass of the segmented scan (geo: a fixed layout with seg_chunks set):
+// for every segment and head, the BF16 state the segment's chunks lead to
+// from a zero state (zero_start_states) and from the identity with V taken as
+// zero (transitions: the segment's state map S -> S F), each [segments][H][128][128].
+cudaError_t launch_transition(const void* v, const uint8_t* packets, const SeqGeometry& geo,
+                              int64_t H, void* zero_start_states, void* transitions, int* status,
+                              cudaStream_t stream);
+
+// Second pass: per sequence and head, the segments' incoming states in order,
+// S_0 = init (zero when null), S_{j+1} = S_j F_j + Z_j, written as BF16 to
+// starts[(n * segs + j) * H + h] for j < segs, and S_segs to final_state
+// (when not null).
+cudaError_t launch_segment_scan(const void* init_state, void* final_state, const void* transitions,
+                                const void* zero_start_states, void* starts, int64_t n_seqs,
+                                int64_t segs, int64_t H, int* status, cudaStream_t stream);
+
 // The tcgen05 recurrence: one CTA per (sequence, head).
 cudaError_t launch_recurrence_tc(const void* v, void* out, const void* init_state,
                                  void* final_state, const uint8_t* packets, const SeqGeometry& geo,
@@ -78,6 +99,7 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
 // Tensor map of v viewed as a 2-D BF16 array [tokens][H * 128], boxes of
 // 16 tokens x `cols` value columns.
 cudaError_t encode_v_map(CUtensorMap* map, const void* v, int64_t tokens, int64_t H, int cols);
+cudaError_t encode_state_map(CUtensorMap* map, const void* base, int64_t rows, int box_rows);
 
 // Recurrence engine: 0 automatic, 1 column-split warp MMA, 2 tcgen05.
 int recurrence_engine();

@@ -22,6 +22,10 @@ struct RecArgs {
     int nsplit;
     int* status;
     Checkpoints ck;   // ck.states null: none
+    // Transition launches only (segmented scan): blocks from ident_from on
+    // run the identity-state pass and write their final states to final_ident.
+    int64_t ident_from;
+    __nv_bfloat16* final_ident;
 };
 
 // Where sequence n's checkpoint j of head h goes, or null (with the

@@ -443,9 +443,18 @@ __device__ __forceinline__ void quad_store_state(__nv_bfloat16* dst, const float
         }
 }
 
-// kCkpt: this instantiation writes checkpoints (a separate one keeps the
-// check out of the loop of the plain call, which is at the register limit).
-template <bool kCkpt>
+// Modes of the quad kernel: kQuadPlain; kQuadCkpt writes checkpoints (a
+// separate instantiation keeps the check out of the loop of the plain call,
+// which is at the register limit); kQuadTransition is the first pass of the
+// segmented scan: per segment, the state reached from a zero state (blocks
+// below a.ident_from, final state to a.final_state) and from the identity
+// with V taken as zero (the segment's state transition, to a.final_ident).
+// That pass forms no P^T and stores no O.
+constexpr int kQuadPlain = 0;
+constexpr int kQuadCkpt = 1;
+constexpr int kQuadTransition = 2;
+
+template <int kMode>
 __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     recurrence_quad_kernel(RecArgs a, const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ uint8_t smem_raw[];
@@ -455,8 +464,12 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     uint64_t* empty = full + kQuadStages;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    const int64_t n_slot = blockIdx.x / a.H;
-    const int64_t h = blockIdx.x - n_slot * a.H;
+    constexpr bool kCkpt = kMode == kQuadCkpt;
+    constexpr bool kTrans = kMode == kQuadTransition;
+    const bool ident = kTrans && static_cast<int64_t>(blockIdx.x) >= a.ident_from;
+    const int64_t blk = ident ? blockIdx.x - a.ident_from : blockIdx.x;
+    const int64_t n_slot = blk / a.H;
+    const int64_t h = blk - n_slot * a.H;
     if (n_slot < a.geo.first_slot) return;   // runs in the other launch
     const int64_t n = a.geo.order ? a.geo.order[n_slot] : n_slot;   // longest-first (packed)
 
@@ -467,6 +480,19 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
         nch = a.geo.cu_chunks[n + 1] - c_begin;
         tok0 = a.geo.cu_seqlens[n];
         seqlen = a.geo.cu_seqlens[n + 1] - tok0;
+    } else if (a.geo.seg_chunks) {
+        // Segment j of sequence sq.
+        const int64_t sq = n / a.geo.segs_per_seq;
+        const int64_t j = n - sq * a.geo.segs_per_seq;
+        const int64_t c0 = j * a.geo.seg_chunks;
+        c_begin = sq * a.geo.chunks_per_seq + c0;
+        nch = a.geo.chunks_per_seq - c0;
+        if (nch > a.geo.seg_chunks) nch = a.geo.seg_chunks;
+        if (nch < 0) nch = 0;
+        tok0 = sq * a.geo.tokens_per_seq + kChunk * c0;
+        seqlen = a.geo.tokens_per_seq - kChunk * c0;
+        if (seqlen > kChunk * a.geo.seg_chunks) seqlen = kChunk * a.geo.seg_chunks;
+        if (seqlen < 0) seqlen = 0;
     } else {
         c_begin = n * a.geo.chunks_per_seq;
         nch = a.geo.chunks_per_seq;
@@ -493,11 +519,13 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
             if (!ok) break;
             uint8_t* stage = smem + s * kQuadStageBytes;
             if (lane == 0) {
-                mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * kQuadVRowBytes);
+                // The identity pass takes V as zero: no V tile.
+                mbar_arrive_expect_tx(&full[s], kPacketBytes + (ident ? 0u : kChunk * kQuadVRowBytes));
                 bulk_g2s(stage, a.packets + ((c_begin + c) * a.H + h) * static_cast<int64_t>(kPacketBytes),
                          kPacketBytes, &full[s]);
-                tma_load_2d(stage + kPacketBytes, &vmap, static_cast<int32_t>(h * kHeadDim),
-                            static_cast<int32_t>(tok0 + kChunk * c), &full[s]);
+                if (!ident)
+                    tma_load_2d(stage + kPacketBytes, &vmap, static_cast<int32_t>(h * kHeadDim),
+                                static_cast<int32_t>(tok0 + kChunk * c), &full[s]);
             }
             __syncwarp();
             fill_parity ^= (filled >> s & 1u) << s;
@@ -521,7 +549,15 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-            if (a.init_state) {
+            if (kTrans) {
+                // Zero, or the identity (S[v][key] = 1 where v == key).
+                const int key = 16 * mt + g8;
+                const int val = vcol + 8 * nt + 2 * t4;
+                Sf[mt][nt][0] = ident && val == key ? 1.f : 0.f;
+                Sf[mt][nt][1] = ident && val + 1 == key ? 1.f : 0.f;
+                Sf[mt][nt][2] = ident && val == key + 8 ? 1.f : 0.f;
+                Sf[mt][nt][3] = ident && val + 1 == key + 8 ? 1.f : 0.f;
+            } else if (a.init_state) {
                 const __nv_bfloat16* src = a.init_state + state_base;
                 const int key = 16 * mt + g8;
                 const int val = vcol + 8 * nt + 2 * t4;
@@ -563,7 +599,7 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
             for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) u[x][nt][j] = p[x][nt][j] = 0.f;
-        {
+        if (!ident) {
             uint32_t akb[4];
             ldsm_x4(akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
 #pragma unroll
@@ -583,13 +619,13 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
         for (int kk = 0; kk < 8; ++kk) {
             uint32_t kf[4], qf[4];
             ldsm_x4(kf, sKS + sw128_off(16, rowA, 2 * kk + hiA));
-            ldsm_x4(qf, sQS + sw128_off(16, rowA, 2 * kk + hiA));
+            if (!kTrans) ldsm_x4(qf, sQS + sw128_off(16, rowA, 2 * kk + hiA));
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const uint32_t sb[2] = {movm_t(pack_bf16(Sf[kk][nt][0], Sf[kk][nt][1])),
                                         movm_t(pack_bf16(Sf[kk][nt][2], Sf[kk][nt][3]))};
                 mma_bf16(u[kk & 1][nt], kf, sb, u[kk & 1][nt]);
-                mma_bf16(p[kk & 1][nt], qf, sb, p[kk & 1][nt]);
+                if (!kTrans) mma_bf16(p[kk & 1][nt], qf, sb, p[kk & 1][nt]);
             }
         }
         // D S^T in place.
@@ -625,6 +661,11 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) mma_bf16(Sf[mt][nt], af, Ub[nt], Sf[mt][nt]);
         }
+        if (kTrans) {
+            __syncwarp();
+            mbar_arrive_if(&empty[s], lane == 0);
+            continue;
+        }
         // O^T = P^T + A^qk U^T.
         float o[4][4];
         {
@@ -647,16 +688,17 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
         }
     }
 
-    if (ok && a.final_state) quad_store_state(a.final_state + state_base, Sf, vcol, g8, t4);
+    __nv_bfloat16* fin = ident ? a.final_ident : a.final_state;
+    if (ok && fin) quad_store_state(fin + state_base, Sf, vcol, g8, t4);
 }
 
-template <bool kCkpt>
+template <int kMode>
 cudaError_t launch_quad_t(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
     static bool configured[64] = {};
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(recurrence_quad_kernel<kCkpt>,
+        cudaError_t e = cudaFuncSetAttribute(recurrence_quad_kernel<kMode>,
                                              cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(kQuadSmemBytes));
         if (e != cudaSuccess) return e;
@@ -667,13 +709,14 @@ cudaError_t launch_quad_t(const RecArgs& a, int64_t blocks, cudaStream_t stream)
     const void* vbase = a.v ? static_cast<const void*>(a.v) : static_cast<const void*>(kZero);
     cudaError_t e = encode_v_map(&vmap, vbase, a.geo.tokens, a.H, kHeadDim);
     if (e != cudaSuccess) return e;
-    recurrence_quad_kernel<kCkpt>
+    recurrence_quad_kernel<kMode>
         <<<static_cast<unsigned>(blocks), (kQuadWarps + 1) * 32, kQuadSmemBytes, stream>>>(a, vmap);
     return cudaGetLastError();
 }
 
 cudaError_t launch_quad(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
-    return a.ck.states ? launch_quad_t<true>(a, blocks, stream) : launch_quad_t<false>(a, blocks, stream);
+    return a.ck.states ? launch_quad_t<kQuadCkpt>(a, blocks, stream)
+                       : launch_quad_t<kQuadPlain>(a, blocks, stream);
 }
 
 template <int NCG>
@@ -766,6 +809,21 @@ cudaError_t encode_v_map(CUtensorMap* map, const void* v, int64_t tokens, int64_
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// Tensor map of BF16 states viewed as a 2-D array [rows][128], boxes of
+// `box_rows` rows x 64 columns with the 128-byte swizzle.
+cudaError_t encode_state_map(CUtensorMap* map, const void* base, int64_t rows, int box_rows) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(kHeadDim), static_cast<cuuint64_t>(rows)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(kHeadDim * 2)};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(box_rows)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
                               void* final_state, const uint8_t* packets,
                               const SeqGeometry& geo, int64_t H, int nsplit, int* status,
@@ -781,6 +839,8 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
     a.nsplit = nsplit;
     a.status = status;
     a.ck = ck ? *ck : Checkpoints{nullptr, nullptr, 1, 0};
+    a.ident_from = 0;
+    a.final_ident = nullptr;
     // Engine 2 (opt-in): the tcgen05 kernel, one CTA per head (it writes no
     // checkpoints, so calls that ask for them take the column-split kernels).
     // Otherwise the column-split kernel with `nsplit` CTAs per head.
@@ -809,6 +869,28 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
         case 16: return launch_ks<1>(a, blocks, stream);
         default: return cudaErrorInvalidValue;
     }
+}
+
+cudaError_t launch_transition(const void* v, const uint8_t* packets, const SeqGeometry& geo,
+                              int64_t H, void* zero_start_states, void* transitions, int* status,
+                              cudaStream_t stream) {
+    RecArgs a;
+    a.v = static_cast<const __nv_bfloat16*>(v);
+    a.out = nullptr;
+    a.init_state = nullptr;
+    a.final_state = static_cast<__nv_bfloat16*>(zero_start_states);
+    a.packets = packets;
+    a.geo = geo;
+    a.H = H;
+    a.nsplit = 1;
+    a.status = status;
+    a.ck = Checkpoints{nullptr, nullptr, 1, 0};
+    a.ident_from = geo.n_seqs * H;
+    a.final_ident = static_cast<__nv_bfloat16*>(transitions);
+    const int64_t blocks = 2 * a.ident_from;
+    if (blocks <= 0) return cudaSuccess;
+    if (geo.tokens >= (int64_t(1) << 31) || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    return launch_quad_t<kQuadTransition>(a, blocks, stream);
 }
 
 }  // namespace kda

@@ -1,0 +1,263 @@
+// kda_segments.cu -- the middle pass of the segmented scan over chunks.
+//
+// The chunkwise recurrence ("Kimi Linear" technical report, section on the
+// chunkwise KDA algorithm) maps the state of one chunk to the next by
+//     S_{c+1} = S_c D_c + U_c K^end_c,   U_c = V_c (A^kk B)^T + S_c K'_c^T,
+// which is affine in S_c.  Over a segment of consecutive chunks the map is
+// therefore S -> S F + Z, with F the state the segment's chunks lead to from
+// the identity with V taken as zero and Z the state they lead to from zero.
+// The first pass (launch_transition) forms F and Z for every segment at
+// once; this pass walks each sequence's segments in order,
+//     S_0 = initial state,   S_{j+1} = S_j F_j + Z_j,
+// and hands S_j to the last pass, which reruns segment j from S_j and writes
+// its outputs.  With few heads this replaces one chain of all the chunks by
+// chains of one segment's chunks plus this short chain of segment steps.
+//
+// One CTA per (sequence, head, 8 value rows of S): the rows of S update
+// independently.  Four consumer warps each form 32 key columns of the new
+// rows as (S_{j+1})^T = F_j^T S_j^T + Z_j^T on the warp MMA (BF16 operands,
+// FP32 accumulation; the FP32 rows stay in registers), and swap their BF16
+// slices through shared memory for the next step's operand.  A producer warp
+// streams F_j and the CTA's rows of Z_j through a TMA ring.
+#include <cuda.h>
+
+#include "kda_common.cuh"
+#include "kda_launch.h"
+
+namespace kda {
+namespace {
+
+constexpr int kScanRows = 8;     // value rows of the state per CTA
+constexpr int kScanWarps = 4;    // consumer warps, 32 keys each
+constexpr int kScanStages = 3;
+constexpr uint32_t kScanFBytes = kHeadDim * kHeadDim * 2;      // F: two SW128 slabs [128][64]
+constexpr uint32_t kScanZBytes = kScanRows * kHeadDim * 2;     // Z rows: two SW128 slabs [8][64]
+constexpr uint32_t kScanStageBytes = ((kScanFBytes + kScanZBytes + 1023) / 1024) * 1024;
+constexpr uint32_t kScanXBytes = kScanRows * kHeadDim * 2;     // one BF16 copy of the CTA's rows
+constexpr uint32_t kScanXOff = kScanStages * kScanStageBytes;
+constexpr uint32_t kScanBarOff = kScanXOff + 2 * kScanXBytes;
+constexpr uint32_t kScanSmemBytes = kScanBarOff + 2 * kScanStages * 8 + 1024;
+
+// Byte offset of (row v, keys 8 ch .. 8 ch + 7) in a [8][128] BF16 copy of
+// the CTA's rows; the 16-byte chunks of row v are XOR-swizzled by v so that
+// the eight rows of one chunk fall in different banks.
+__device__ __forceinline__ uint32_t x_off(uint32_t v, uint32_t ch) {
+    return v * (kHeadDim * 2) + ((ch ^ v) << 4);
+}
+
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t* r, uint32_t addr) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
+__device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
+
+struct ScanArgs {
+    const __nv_bfloat16* init_state;   // [N][H][128][128] or null
+    __nv_bfloat16* final_state;        // [N][H][128][128] or null
+    __nv_bfloat16* starts;             // [N * segs][H][128][128]
+    int64_t segs, H;
+    int* status;
+};
+
+// Warp w's slice (keys 32 w .. 32 w + 31 of the CTA's 8 rows) of a state in
+// C-fragment form (m = key, n = value row), rounded to BF16, into the copy at x.
+__device__ __forceinline__ void put_rows(uint8_t* x, const float (&c)[2][4], int w, int g8, int t4) {
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+        const uint32_t lo = movm_trans(pack_bf16(c[mt][0], c[mt][1]));   // row g8, keys base + 2 t4
+        const uint32_t hi = movm_trans(pack_bf16(c[mt][2], c[mt][3]));   // keys base + 8 + 2 t4
+        const uint32_t base = 32 * w + 16 * mt;
+        *reinterpret_cast<uint32_t*>(x + x_off(g8, base / 8) + 4 * t4) = lo;
+        *reinterpret_cast<uint32_t*>(x + x_off(g8, base / 8 + 1) + 4 * t4) = hi;
+    }
+}
+
+// The CTA's 8 rows from the copy at x into rows [8][128] at dst (thread tid
+// of the 128 consumers copies 16 bytes).
+__device__ __forceinline__ void copy_rows_out(const uint8_t* x, __nv_bfloat16* dst, int tid) {
+    const int v = tid >> 4, ch = tid & 15;
+    const uint4 val = *reinterpret_cast<const uint4*>(x + x_off(v, ch));
+    *reinterpret_cast<uint4*>(dst + v * kHeadDim + 8 * ch) = val;
+}
+
+__global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
+    segment_scan_kernel(ScanArgs a, const __grid_constant__ CUtensorMap fmap,
+                        const __grid_constant__ CUtensorMap zmap) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kScanBarOff);
+    uint64_t* empty = full + kScanStages;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    constexpr int kGroups = kHeadDim / kScanRows;
+    const int64_t nh = blockIdx.x / kGroups;
+    const int v0 = kScanRows * static_cast<int>(blockIdx.x - nh * kGroups);
+    const int64_t n = nh / a.H;
+    const int64_t h = nh - n * a.H;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kScanStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kScanWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+
+    if (warp == kScanWarps) {
+        // ------------------------------------------------------------ producer
+        uint32_t fill_parity = 0, filled = 0;
+        bool ok = true;
+        for (int64_t j = 0; j < a.segs && ok; ++j) {
+            const int s = static_cast<int>(j % kScanStages);
+            if (j >= kScanStages)
+                ok = mbar_wait_warp_sleep(&empty[s], ((j / kScanStages) - 1) & 1, a.status);
+            if (!ok) break;
+            uint8_t* stage = smem + s * kScanStageBytes;
+            if (lane == 0) {
+                const int32_t row = static_cast<int32_t>(((n * a.segs + j) * a.H + h) * kHeadDim);
+                mbar_arrive_expect_tx(&full[s], kScanFBytes + kScanZBytes);
+                tma_load_2d(stage, &fmap, 0, row, &full[s]);
+                tma_load_2d(stage + kScanFBytes / 2, &fmap, 64, row, &full[s]);
+                tma_load_2d(stage + kScanFBytes, &zmap, 0, row + v0, &full[s]);
+                tma_load_2d(stage + kScanFBytes + kScanZBytes / 2, &zmap, 64, row + v0, &full[s]);
+            }
+            __syncwarp();
+            fill_parity ^= (filled >> s & 1u) << s;
+            filled |= 1u << s;
+        }
+        if (!ok)
+            for (int s = 0; s < kScanStages; ++s)
+                if (filled >> s & 1u) mbar_wait_bounded(&full[s], (fill_parity >> s) & 1u, a.status);
+        return;
+    }
+
+    // ---------------------------------------------------------------- consumers
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int tid = threadIdx.x;   // 0 .. 127
+    uint8_t* xbuf = smem + kScanXOff;
+    const int64_t rows0 = (n * a.H + h) * kHeadDim + v0;   // first row of this CTA in [N][H][128]
+
+    // S_0^T for keys 32 warp + 16 mt + {g8, g8 + 8}, rows v0 + 2 t4 + {0, 1}.
+    float c[2][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt) {
+        const int key = 32 * warp + 16 * mt + g8;
+        if (a.init_state) {
+            const __nv_bfloat16* src = a.init_state + (rows0 + 2 * t4) * kHeadDim;
+            c[mt][0] = __bfloat162float(src[key]);
+            c[mt][1] = __bfloat162float(src[kHeadDim + key]);
+            c[mt][2] = __bfloat162float(src[key + 8]);
+            c[mt][3] = __bfloat162float(src[kHeadDim + key + 8]);
+        } else {
+            c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.f;
+        }
+    }
+    put_rows(xbuf, c, warp, g8, t4);
+    bool ok = group_all<kScanWarps * 32>(1, true);
+
+    const uint32_t mi = lane >> 3, r8 = lane & 7;
+    for (int64_t j = 0; j < a.segs && ok; ++j) {
+        const uint8_t* xc = xbuf + (j & 1) * kScanXBytes;
+        // S_j is this segment's incoming state.
+        copy_rows_out(xc, a.starts + (((n * a.segs + j) * a.H + h) * kHeadDim + v0) * kHeadDim, tid);
+        // B operand: S_j^T (k = key of S_j, n = value row), all 8 k-steps.
+        uint32_t b[8][2];
+#pragma unroll
+        for (int kp = 0; kp < 4; ++kp) {
+            uint32_t r[4];
+            ldsm_x4(r, smem_u32(xc + x_off(r8, 4 * kp + mi)));
+            b[2 * kp][0] = r[0];
+            b[2 * kp][1] = r[1];
+            b[2 * kp + 1][0] = r[2];
+            b[2 * kp + 1][1] = r[3];
+        }
+        const int s = static_cast<int>(j % kScanStages);
+        if (!mbar_wait_warp(&full[s], (j / kScanStages) & 1, a.status)) ok = false;
+        if (ok) {
+            const uint8_t* stage = smem + s * kScanStageBytes;
+            // Accumulators: Z_j^T (k = 0 half) and zero (k = 1 half).
+            float acc[2][2][4];
+            {
+                uint32_t z[4];
+                ldsm_x4_trans(z, smem_u32(stage + kScanFBytes + sw128_off(8, r8, 4 * warp + mi)));
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    acc[mt][0][0] = bf_lo(z[2 * mt]);
+                    acc[mt][0][1] = bf_hi(z[2 * mt]);
+                    acc[mt][0][2] = bf_lo(z[2 * mt + 1]);
+                    acc[mt][0][3] = bf_hi(z[2 * mt + 1]);
+                    acc[mt][1][0] = acc[mt][1][1] = acc[mt][1][2] = acc[mt][1][3] = 0.f;
+                }
+            }
+            // F_j^T (m = new key, k = old key) from F_j's rows (old key) by
+            // transposing loads.
+#pragma unroll
+            for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+                for (int mt = 0; mt < 2; ++mt) {
+                    uint32_t af[4];
+                    const uint32_t row = 16 * kk + r8 + 8 * (mi >> 1);
+                    const uint32_t ch = 4 * warp + 2 * mt + (mi & 1);
+                    ldsm_x4_trans(af, smem_u32(stage + sw128_off(kHeadDim, row, ch)));
+                    mma_bf16(acc[mt][kk & 1], af, b[kk], acc[mt][kk & 1]);
+                }
+            __syncwarp();
+            mbar_arrive_if(&empty[s], lane == 0);
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+                for (int e = 0; e < 4; ++e) c[mt][e] = acc[mt][0][e] + acc[mt][1][e];
+            put_rows(xbuf + ((j + 1) & 1) * kScanXBytes, c, warp, g8, t4);
+        }
+        ok = group_all<kScanWarps * 32>(1, ok);
+    }
+    if (ok && a.final_state)
+        copy_rows_out(xbuf + (a.segs & 1) * kScanXBytes, a.final_state + rows0 * kHeadDim, tid);
+}
+
+}  // namespace
+
+cudaError_t launch_segment_scan(const void* init_state, void* final_state, const void* transitions,
+                                const void* zero_start_states, void* starts, int64_t n_seqs,
+                                int64_t segs, int64_t H, int* status, cudaStream_t stream) {
+    const int64_t blocks = n_seqs * H * (kHeadDim / kScanRows);
+    if (blocks <= 0 || segs <= 0) return cudaSuccess;
+    const int64_t rows = n_seqs * segs * H * kHeadDim;
+    if (rows >= (int64_t(1) << 31) || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(segment_scan_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kScanSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    CUtensorMap fmap, zmap;
+    cudaError_t e = encode_state_map(&fmap, transitions, rows, kHeadDim);
+    if (e == cudaSuccess) e = encode_state_map(&zmap, zero_start_states, rows, kScanRows);
+    if (e != cudaSuccess) return e;
+    ScanArgs a;
+    a.init_state = static_cast<const __nv_bfloat16*>(init_state);
+    a.final_state = static_cast<__nv_bfloat16*>(final_state);
+    a.starts = static_cast<__nv_bfloat16*>(starts);
+    a.segs = segs;
+    a.H = H;
+    a.status = status;
+    segment_scan_kernel<<<static_cast<unsigned>(blocks), (kScanWarps + 1) * 32, kScanSmemBytes,
+                          stream>>>(a, fmap, zmap);
+    return cudaGetLastError();
+}
+
+}  // namespace kda

@@ -111,6 +111,14 @@ def test_split_option(lib):
     assert lib.kda_set_split(0) == 0
 
 
+def test_segments_option(lib):
+    for on, L in ((0, 0), (1, 0), (1, 1), (1, 64), (0, 5)):
+        assert lib.kda_set_segments(on, L) == 0
+    for on, L in ((2, 0), (-1, 0), (1, -1), (1, (1 << 26) + 1)):
+        assert lib.kda_set_segments(on, L) == -7
+    assert lib.kda_set_segments(1, 0) == 0
+
+
 def test_workspace_bytes(lib):
     pb = _lib.packet_bytes()
     assert pb == 13824
@@ -123,6 +131,15 @@ def test_workspace_bytes(lib):
     n, T, H = 4, 100, 2
     meta = 256 + ((8 * (n + 1) + 255) // 256) * 256 + ((4 * n + 255) // 256) * 256
     assert _lib.workspace_bytes(n, T, H, True) == meta + ((T + 15 * n) // 16) * H * pb
+    # fixed, few heads, long sequence: the segmented scan's three state buffers
+    # as planned for a 152-SM device (B=1, H=6, T=8192: 25 segments of 21 chunks)
+    import torch
+    if not torch.cuda.is_available():
+        st = 25 * 6 * 128 * 128 * 2
+        assert _lib.workspace_bytes(1, 8192, 6, False) == 512 * 6 * pb + 12288 + 3 * st
+        lib.kda_set_segments(0, 0)
+        assert _lib.workspace_bytes(1, 8192, 6, False) == 512 * 6 * pb + 12288
+        lib.kda_set_segments(1, 0)
 
 
 def call_ck(lib, every=64, states=A + 9 * GB, cu_starts=A + 10 * GB, rows=4, **kw):

@@ -23,10 +23,14 @@ def kda():
     build.build()
     assert torch.cuda.is_available(), "GPU tests need a CUDA device"
     m.set_split(0)
+    # Checkpointed calls always run the serial chain; the plain calls they are
+    # compared with bit for bit must too.
+    m.set_segments(False)
     m.device_status()
     yield m
     m.set_split(0)
     m.set_engine(0)
+    m.set_segments(True)
 
 
 def _rows(lengths, every):

@@ -391,8 +391,10 @@ def test_forced_split_full_t8192_h6(forced_split, nsplit):
 
 @pytest.fixture
 def fusion_toggle(kda):
+    kda.set_segments(False)   # shapes the segmented scan would otherwise take
     yield kda
     kda.set_fusion(True)
+    kda.set_segments(True)
 
 
 @pytest.mark.parametrize("B,T,H", [(1, 8192, 6), (2, 300, 3), (1, 256, 1), (3, 100, 2)])
@@ -415,8 +417,9 @@ def test_fused_not_planned_where_it_cannot_run(kda):
     assert not kda.plan_fused(1, 0, 6, False)        # no tokens
 
 
-def test_fused_repeated_calls_and_in_place(kda):
+def test_fused_repeated_calls_and_in_place(fusion_toggle):
     """Back-to-back fused calls reuse pool memory with stale ready flags in it."""
+    kda = fusion_toggle
     inp = synthetic.make_inputs(1, 2048, 4, 4100, init_std=0.02)
     assert kda.plan_fused(1, 2048, 4, False)
     a = run(kda, inp)
