@@ -121,7 +121,6 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
     f.r.nsplit = nsplit;
     f.r.status = status;
     f.r.ck = ck ? *ck : Checkpoints{nullptr, nullptr, 1, 0};
-    f.r.ident_from = 0;
     f.r.final_ident = nullptr;
     f.rec_blocks = geo.n_seqs * H * nsplit;
     f.ready = ready;

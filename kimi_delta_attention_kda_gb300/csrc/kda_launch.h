@@ -99,6 +99,7 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
 // Tensor map of v viewed as a 2-D BF16 array [tokens][H * 128], boxes of
 // 16 tokens x `cols` value columns.
 cudaError_t encode_v_map(CUtensorMap* map, const void* v, int64_t tokens, int64_t H, int cols);
+cudaError_t encode_v_map_sw128(CUtensorMap* map, const void* v, int64_t tokens, int64_t H);
 cudaError_t encode_state_map(CUtensorMap* map, const void* base, int64_t rows, int box_rows);
 
 // Recurrence engine: 0 automatic, 1 column-split warp MMA, 2 tcgen05.

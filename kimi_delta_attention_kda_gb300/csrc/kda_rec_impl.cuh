@@ -22,11 +22,41 @@ struct RecArgs {
     int nsplit;
     int* status;
     Checkpoints ck;   // ck.states null: none
-    // Transition launches only (segmented scan): blocks from ident_from on
-    // run the identity-state pass and write their final states to final_ident.
-    int64_t ident_from;
+    // Transition launches only (segmented scan): where the identity-start
+    // pass writes its final states.
     __nv_bfloat16* final_ident;
 };
+
+// Chunks and tokens of recurrence sequence n: a sequence of the batch, or
+// with g.seg_chunks set, segment n % segs_per_seq of sequence
+// n / segs_per_seq.  False when the packed metadata marked the batch invalid.
+__device__ __forceinline__ bool seq_span(const SeqGeometry& g, int64_t n, int64_t& c_begin,
+                                         int64_t& nch, int64_t& tok0, int64_t& seqlen) {
+    if (g.cu_chunks) {
+        if (!*g.valid) return false;
+        c_begin = g.cu_chunks[n];
+        nch = g.cu_chunks[n + 1] - c_begin;
+        tok0 = g.cu_seqlens[n];
+        seqlen = g.cu_seqlens[n + 1] - tok0;
+    } else if (g.seg_chunks) {
+        const int64_t sq = n / g.segs_per_seq;
+        const int64_t c0 = (n - sq * g.segs_per_seq) * g.seg_chunks;
+        c_begin = sq * g.chunks_per_seq + c0;
+        nch = g.chunks_per_seq - c0;
+        if (nch > g.seg_chunks) nch = g.seg_chunks;
+        if (nch < 0) nch = 0;
+        tok0 = sq * g.tokens_per_seq + kChunk * c0;
+        seqlen = g.tokens_per_seq - kChunk * c0;
+        if (seqlen > kChunk * g.seg_chunks) seqlen = kChunk * g.seg_chunks;
+        if (seqlen < 0) seqlen = 0;
+    } else {
+        c_begin = n * g.chunks_per_seq;
+        nch = g.chunks_per_seq;
+        tok0 = n * g.tokens_per_seq;
+        seqlen = g.tokens_per_seq;
+    }
+    return true;
+}
 
 // Where sequence n's checkpoint j of head h goes, or null (with the
 // kDevBadCheckpoints status bit) when the caller's row offsets give it no

@@ -420,11 +420,24 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 // conversions as the other variants, so the results are bitwise theirs).
 // ---------------------------------------------------------------------------
 constexpr uint32_t kQuadVRowBytes = kHeadDim * 2;
-constexpr uint32_t kQuadStageBytes = ((kPacketBytes + kChunk * kQuadVRowBytes + 1023) / 1024) * 1024;
+// The V tile sits 1024-aligned after the packet as two [16][64] slabs with
+// the 128-byte swizzle (rows 256 bytes apart would put the eight rows of
+// each transposing load in the same banks).
+constexpr uint32_t kQuadVOff = ((kPacketBytes + 1023) / 1024) * 1024;
+constexpr uint32_t kQuadStageBytes = ((kQuadVOff + kChunk * kQuadVRowBytes + 1023) / 1024) * 1024;
 constexpr int kQuadWarps = 4;
 constexpr int kQuadStages = 6;
 constexpr uint32_t kQuadBarOff = kQuadStages * kQuadStageBytes;
 constexpr uint32_t kQuadSmemBytes = kQuadBarOff + 2 * kQuadStages * 8 + 1024;
+
+// V rows tok .. tok + 15 of head h into the stage's two swizzled slabs.
+__device__ __forceinline__ void quad_load_v(uint8_t* stage, const CUtensorMap* vmap, int64_t h,
+                                            int64_t tok, uint64_t* bar) {
+    tma_load_2d(stage + kQuadVOff, vmap, static_cast<int32_t>(h * kHeadDim), static_cast<int32_t>(tok),
+                bar);
+    tma_load_2d(stage + kQuadVOff + kChunk * 128, vmap, static_cast<int32_t>(h * kHeadDim + 64),
+                static_cast<int32_t>(tok), bar);
+}
 
 // A warp's slice of a state (all 128 keys of 32 value columns), BF16, into a
 // [128 value][128 key] state at dst.
@@ -445,14 +458,9 @@ __device__ __forceinline__ void quad_store_state(__nv_bfloat16* dst, const float
 
 // Modes of the quad kernel: kQuadPlain; kQuadCkpt writes checkpoints (a
 // separate instantiation keeps the check out of the loop of the plain call,
-// which is at the register limit); kQuadTransition is the first pass of the
-// segmented scan: per segment, the state reached from a zero state (blocks
-// below a.ident_from, final state to a.final_state) and from the identity
-// with V taken as zero (the segment's state transition, to a.final_ident).
-// That pass forms no P^T and stores no O.
+// which is at the register limit).
 constexpr int kQuadPlain = 0;
 constexpr int kQuadCkpt = 1;
-constexpr int kQuadTransition = 2;
 
 template <int kMode>
 __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
@@ -465,40 +473,13 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr bool kCkpt = kMode == kQuadCkpt;
-    constexpr bool kTrans = kMode == kQuadTransition;
-    const bool ident = kTrans && static_cast<int64_t>(blockIdx.x) >= a.ident_from;
-    const int64_t blk = ident ? blockIdx.x - a.ident_from : blockIdx.x;
-    const int64_t n_slot = blk / a.H;
-    const int64_t h = blk - n_slot * a.H;
+    const int64_t n_slot = blockIdx.x / a.H;
+    const int64_t h = blockIdx.x - n_slot * a.H;
     if (n_slot < a.geo.first_slot) return;   // runs in the other launch
     const int64_t n = a.geo.order ? a.geo.order[n_slot] : n_slot;   // longest-first (packed)
 
     int64_t c_begin, nch, tok0, seqlen;
-    if (a.geo.cu_chunks) {
-        if (!*a.geo.valid) return;
-        c_begin = a.geo.cu_chunks[n];
-        nch = a.geo.cu_chunks[n + 1] - c_begin;
-        tok0 = a.geo.cu_seqlens[n];
-        seqlen = a.geo.cu_seqlens[n + 1] - tok0;
-    } else if (a.geo.seg_chunks) {
-        // Segment j of sequence sq.
-        const int64_t sq = n / a.geo.segs_per_seq;
-        const int64_t j = n - sq * a.geo.segs_per_seq;
-        const int64_t c0 = j * a.geo.seg_chunks;
-        c_begin = sq * a.geo.chunks_per_seq + c0;
-        nch = a.geo.chunks_per_seq - c0;
-        if (nch > a.geo.seg_chunks) nch = a.geo.seg_chunks;
-        if (nch < 0) nch = 0;
-        tok0 = sq * a.geo.tokens_per_seq + kChunk * c0;
-        seqlen = a.geo.tokens_per_seq - kChunk * c0;
-        if (seqlen > kChunk * a.geo.seg_chunks) seqlen = kChunk * a.geo.seg_chunks;
-        if (seqlen < 0) seqlen = 0;
-    } else {
-        c_begin = n * a.geo.chunks_per_seq;
-        nch = a.geo.chunks_per_seq;
-        tok0 = n * a.geo.tokens_per_seq;
-        seqlen = a.geo.tokens_per_seq;
-    }
+    if (!seq_span(a.geo, n, c_begin, nch, tok0, seqlen)) return;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kQuadStages; ++s) {
             mbar_init(&full[s], 1);
@@ -519,13 +500,10 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
             if (!ok) break;
             uint8_t* stage = smem + s * kQuadStageBytes;
             if (lane == 0) {
-                // The identity pass takes V as zero: no V tile.
-                mbar_arrive_expect_tx(&full[s], kPacketBytes + (ident ? 0u : kChunk * kQuadVRowBytes));
+                mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * kQuadVRowBytes);
                 bulk_g2s(stage, a.packets + ((c_begin + c) * a.H + h) * static_cast<int64_t>(kPacketBytes),
                          kPacketBytes, &full[s]);
-                if (!ident)
-                    tma_load_2d(stage + kPacketBytes, &vmap, static_cast<int32_t>(h * kHeadDim),
-                                static_cast<int32_t>(tok0 + kChunk * c), &full[s]);
+                quad_load_v(stage, &vmap, h, tok0 + kChunk * c, &full[s]);
             }
             __syncwarp();
             fill_parity ^= (filled >> s & 1u) << s;
@@ -549,15 +527,7 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     for (int mt = 0; mt < 8; ++mt)
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-            if (kTrans) {
-                // Zero, or the identity (S[v][key] = 1 where v == key).
-                const int key = 16 * mt + g8;
-                const int val = vcol + 8 * nt + 2 * t4;
-                Sf[mt][nt][0] = ident && val == key ? 1.f : 0.f;
-                Sf[mt][nt][1] = ident && val + 1 == key ? 1.f : 0.f;
-                Sf[mt][nt][2] = ident && val == key + 8 ? 1.f : 0.f;
-                Sf[mt][nt][3] = ident && val + 1 == key + 8 ? 1.f : 0.f;
-            } else if (a.init_state) {
+            if (a.init_state) {
                 const __nv_bfloat16* src = a.init_state + state_base;
                 const int key = 16 * mt + g8;
                 const int val = vcol + 8 * nt + 2 * t4;
@@ -599,15 +569,15 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
             for (int nt = 0; nt < 4; ++nt)
 #pragma unroll
                 for (int j = 0; j < 4; ++j) u[x][nt][j] = p[x][nt][j] = 0.f;
-        if (!ident) {
+        {
             uint32_t akb[4];
             ldsm_x4(akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
 #pragma unroll
             for (int hp = 0; hp < 2; ++hp) {
                 // lanes 0-15: tokens of columns vcol + 16 hp .. + 7; lanes 16-31: + 8.
                 uint32_t vb[4];
-                const uint8_t* sV = stage + kPacketBytes + (lane & 15) * kQuadVRowBytes +
-                                    (vcol + 16 * hp + 8 * (lane >> 4)) * 2;
+                const uint8_t* sV = stage + kQuadVOff +
+                                    sw128_off(kChunk, lane & 15, (vcol + 16 * hp) / 8 + (lane >> 4));
                 asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                              : "=r"(vb[0]), "=r"(vb[1]), "=r"(vb[2]), "=r"(vb[3])
                              : "r"(smem_u32(sV)));
@@ -619,13 +589,13 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
         for (int kk = 0; kk < 8; ++kk) {
             uint32_t kf[4], qf[4];
             ldsm_x4(kf, sKS + sw128_off(16, rowA, 2 * kk + hiA));
-            if (!kTrans) ldsm_x4(qf, sQS + sw128_off(16, rowA, 2 * kk + hiA));
+            ldsm_x4(qf, sQS + sw128_off(16, rowA, 2 * kk + hiA));
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
                 const uint32_t sb[2] = {movm_t(pack_bf16(Sf[kk][nt][0], Sf[kk][nt][1])),
                                         movm_t(pack_bf16(Sf[kk][nt][2], Sf[kk][nt][3]))};
                 mma_bf16(u[kk & 1][nt], kf, sb, u[kk & 1][nt]);
-                if (!kTrans) mma_bf16(p[kk & 1][nt], qf, sb, p[kk & 1][nt]);
+                mma_bf16(p[kk & 1][nt], qf, sb, p[kk & 1][nt]);
             }
         }
         // D S^T in place.
@@ -661,11 +631,6 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) mma_bf16(Sf[mt][nt], af, Ub[nt], Sf[mt][nt]);
         }
-        if (kTrans) {
-            __syncwarp();
-            mbar_arrive_if(&empty[s], lane == 0);
-            continue;
-        }
         // O^T = P^T + A^qk U^T.
         float o[4][4];
         {
@@ -688,8 +653,7 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
         }
     }
 
-    __nv_bfloat16* fin = ident ? a.final_ident : a.final_state;
-    if (ok && fin) quad_store_state(fin + state_base, Sf, vcol, g8, t4);
+    if (ok && a.final_state) quad_store_state(a.final_state + state_base, Sf, vcol, g8, t4);
 }
 
 template <int kMode>
@@ -707,7 +671,7 @@ cudaError_t launch_quad_t(const RecArgs& a, int64_t blocks, cudaStream_t stream)
     CUtensorMap vmap;
     alignas(64) static const char kZero[16] = {};
     const void* vbase = a.v ? static_cast<const void*>(a.v) : static_cast<const void*>(kZero);
-    cudaError_t e = encode_v_map(&vmap, vbase, a.geo.tokens, a.H, kHeadDim);
+    cudaError_t e = encode_v_map_sw128(&vmap, vbase, a.geo.tokens, a.H);
     if (e != cudaSuccess) return e;
     recurrence_quad_kernel<kMode>
         <<<static_cast<unsigned>(blocks), (kQuadWarps + 1) * 32, kQuadSmemBytes, stream>>>(a, vmap);
@@ -717,6 +681,176 @@ cudaError_t launch_quad_t(const RecArgs& a, int64_t blocks, cudaStream_t stream)
 cudaError_t launch_quad(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
     return a.ck.states ? launch_quad_t<kQuadCkpt>(a, blocks, stream)
                        : launch_quad_t<kQuadPlain>(a, blocks, stream);
+}
+
+// ---------------------------------------------------------------------------
+// Transition pass of the segmented scan.  For segment n of the batch and head
+// h: the state the segment's chunks lead to from a zero state (Z, warps 0-3)
+// and from the identity with V taken as zero (F, warps 4-7; S -> S F is the
+// map of those chunks on the incoming state).  Both halves read the same
+// packets; each warp holds 32 value columns of its state over all 128 keys as
+// in the quad kernel and runs the U^T and S^T updates only (no P^T, no O).
+// Under the state's registers eight warps leave no room for a producer warp,
+// so warp 0 refills each stage once every warp has released it.
+// ---------------------------------------------------------------------------
+constexpr int kTransWarps = 2 * kQuadWarps;
+
+__global__ void __launch_bounds__(kTransWarps * 32, 1)
+    transition_kernel(RecArgs a, const __grid_constant__ CUtensorMap vmap) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kQuadBarOff);
+    uint64_t* empty = full + kQuadStages;
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t n = blockIdx.x / a.H;
+    const int64_t h = blockIdx.x - n * a.H;
+    int64_t c_begin, nch, tok0, seqlen;
+    if (!seq_span(a.geo, n, c_begin, nch, tok0, seqlen)) return;
+    const bool ident = warp >= kQuadWarps;
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kQuadStages; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], kTransWarps);
+        }
+        fence_barrier_init();
+    }
+    __syncthreads();
+    // Chunk c's packet and V tile into its stage (warp 0, lane 0).
+    auto load = [&](int64_t c) {
+        const int s = static_cast<int>(c % kQuadStages);
+        uint8_t* stage = smem + s * kQuadStageBytes;
+        mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * kQuadVRowBytes);
+        bulk_g2s(stage, a.packets + ((c_begin + c) * a.H + h) * static_cast<int64_t>(kPacketBytes),
+                 kPacketBytes, &full[s]);
+        quad_load_v(stage, &vmap, h, tok0 + kChunk * c, &full[s]);
+    };
+    int64_t issued = nch < kQuadStages ? nch : kQuadStages;
+    if (warp == 0 && lane == 0)
+        for (int64_t c = 0; c < issued; ++c) load(c);
+
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const int vcol = 32 * (warp % kQuadWarps);
+    const int64_t state_base = (n * a.H + h) * kHeadDim * kHeadDim;
+    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
+    const uint32_t hiA = lane >> 4;
+
+    // Zero, or the identity (S[v][key] = 1 where v == key).
+    float Sf[8][4][4];
+#pragma unroll
+    for (int mt = 0; mt < 8; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            const int key = 16 * mt + g8;
+            const int val = vcol + 8 * nt + 2 * t4;
+            Sf[mt][nt][0] = ident && val == key ? 1.f : 0.f;
+            Sf[mt][nt][1] = ident && val + 1 == key ? 1.f : 0.f;
+            Sf[mt][nt][2] = ident && val == key + 8 ? 1.f : 0.f;
+            Sf[mt][nt][3] = ident && val + 1 == key + 8 ? 1.f : 0.f;
+        }
+
+    bool ok = true;
+    int64_t c = 0;
+    for (; c < nch; ++c) {
+        const int s = static_cast<int>(c % kQuadStages);
+        if (!mbar_wait_warp(&full[s], (c / kQuadStages) & 1, a.status)) {
+            ok = false;
+            break;
+        }
+        const uint8_t* stage = smem + s * kQuadStageBytes;
+        const uint32_t sKS = smem_u32(stage + kOffKS);
+        const uint32_t sKE = smem_u32(stage + kOffKE);
+
+        // U^T = (A^kk B) V^T (zero-start half only) + K' S^T.
+        float u[2][4][4];
+#pragma unroll
+        for (int x = 0; x < 2; ++x)
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt)
+#pragma unroll
+                for (int j = 0; j < 4; ++j) u[x][nt][j] = 0.f;
+        if (!ident) {
+            uint32_t akb[4];
+            ldsm_x4(akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
+#pragma unroll
+            for (int hp = 0; hp < 2; ++hp) {
+                uint32_t vb[4];
+                const uint8_t* sV = stage + kQuadVOff +
+                                    sw128_off(kChunk, lane & 15, (vcol + 16 * hp) / 8 + (lane >> 4));
+                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
+                             : "=r"(vb[0]), "=r"(vb[1]), "=r"(vb[2]), "=r"(vb[3])
+                             : "r"(smem_u32(sV)));
+                mma_bf16(u[0][2 * hp], akb, vb, u[0][2 * hp]);
+                mma_bf16(u[0][2 * hp + 1], akb, vb + 2, u[0][2 * hp + 1]);
+            }
+        }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) {
+            uint32_t kf[4];
+            ldsm_x4(kf, sKS + sw128_off(16, rowA, 2 * kk + hiA));
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) {
+                const uint32_t sb[2] = {movm_t(pack_bf16(Sf[kk][nt][0], Sf[kk][nt][1])),
+                                        movm_t(pack_bf16(Sf[kk][nt][2], Sf[kk][nt][3]))};
+                mma_bf16(u[kk & 1][nt], kf, sb, u[kk & 1][nt]);
+            }
+        }
+        // D S^T in place.
+        {
+            const float4* dp = reinterpret_cast<const float4*>(stage + kOffD) + 4 * g8;
+#pragma unroll
+            for (int j = 0; j < 4; ++j) {
+                const float4 d = dp[j];
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    Sf[2 * j][nt][0] *= d.x;
+                    Sf[2 * j][nt][1] *= d.x;
+                    Sf[2 * j][nt][2] *= d.y;
+                    Sf[2 * j][nt][3] *= d.y;
+                    Sf[2 * j + 1][nt][0] *= d.z;
+                    Sf[2 * j + 1][nt][1] *= d.z;
+                    Sf[2 * j + 1][nt][2] *= d.w;
+                    Sf[2 * j + 1][nt][3] *= d.w;
+                }
+            }
+        }
+        uint32_t Ub[4][2];
+#pragma unroll
+        for (int nt = 0; nt < 4; ++nt) {
+            Ub[nt][0] = movm_t(pack_bf16(u[0][nt][0] + u[1][nt][0], u[0][nt][1] + u[1][nt][1]));
+            Ub[nt][1] = movm_t(pack_bf16(u[0][nt][2] + u[1][nt][2], u[0][nt][3] + u[1][nt][3]));
+        }
+        // S^T <- D S^T + (K^end)^T U^T.
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            uint32_t af[4];
+            ldsm_x4(af, sKE + sw32_off(16 * mt + rowA, hiA));
+#pragma unroll
+            for (int nt = 0; nt < 4; ++nt) mma_bf16(Sf[mt][nt], af, Ub[nt], Sf[mt][nt]);
+        }
+        __syncwarp();
+        mbar_arrive_if(&empty[s], lane == 0);
+        // Refill the stage of chunk c - 1 once every warp has released it.
+        if (warp == 0 && c >= 1 && issued < nch) {
+            const int64_t cp = c - 1;
+            if (!mbar_wait_warp(&empty[cp % kQuadStages], (cp / kQuadStages) & 1, a.status)) {
+                ok = false;
+                ++c;
+                break;
+            }
+            if (lane == 0) load(issued);
+            __syncwarp();
+            ++issued;
+        }
+    }
+    if (!ok && warp == 0) {
+        // Let the copies this warp issued and did not consume land before exiting.
+        for (int64_t cc = c; cc < issued; ++cc)
+            mbar_wait_bounded(&full[cc % kQuadStages], (cc / kQuadStages) & 1, a.status);
+    }
+    __nv_bfloat16* dst = ident ? a.final_ident : a.final_state;
+    if (ok && dst) quad_store_state(dst + state_base, Sf, vcol, g8, t4);
 }
 
 template <int NCG>
@@ -809,6 +943,22 @@ cudaError_t encode_v_map(CUtensorMap* map, const void* v, int64_t tokens, int64_
     return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
 }
 
+// The same view of v with boxes of 16 tokens x 64 value columns and the
+// 128-byte swizzle (two boxes per 128 columns).
+cudaError_t encode_v_map_sw128(CUtensorMap* map, const void* v, int64_t tokens, int64_t H) {
+    PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+    if (!enc) return cudaErrorNotSupported;
+    const cuuint64_t dims[2] = {static_cast<cuuint64_t>(H * kHeadDim),
+                                static_cast<cuuint64_t>(tokens > 0 ? tokens : 1)};
+    const cuuint64_t strides[1] = {static_cast<cuuint64_t>(H * kHeadDim * 2)};
+    const cuuint32_t box[2] = {64u, static_cast<cuuint32_t>(kChunk)};
+    const cuuint32_t estr[2] = {1, 1};
+    CUresult r = enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(v), dims, strides,
+                     box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                     CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+    return r == CUDA_SUCCESS ? cudaSuccess : cudaErrorInvalidValue;
+}
+
 // Tensor map of BF16 states viewed as a 2-D array [rows][128], boxes of
 // `box_rows` rows x 64 columns with the 128-byte swizzle.
 cudaError_t encode_state_map(CUtensorMap* map, const void* base, int64_t rows, int box_rows) {
@@ -839,7 +989,6 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
     a.nsplit = nsplit;
     a.status = status;
     a.ck = ck ? *ck : Checkpoints{nullptr, nullptr, 1, 0};
-    a.ident_from = 0;
     a.final_ident = nullptr;
     // Engine 2 (opt-in): the tcgen05 kernel, one CTA per head (it writes no
     // checkpoints, so calls that ask for them take the column-split kernels).
@@ -885,12 +1034,28 @@ cudaError_t launch_transition(const void* v, const uint8_t* packets, const SeqGe
     a.nsplit = 1;
     a.status = status;
     a.ck = Checkpoints{nullptr, nullptr, 1, 0};
-    a.ident_from = geo.n_seqs * H;
     a.final_ident = static_cast<__nv_bfloat16*>(transitions);
-    const int64_t blocks = 2 * a.ident_from;
+    const int64_t blocks = geo.n_seqs * H;
     if (blocks <= 0) return cudaSuccess;
     if (geo.tokens >= (int64_t(1) << 31) || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    return launch_quad_t<kQuadTransition>(a, blocks, stream);
+    static bool configured[64] = {};
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    if (!configured[dev]) {
+        cudaError_t e = cudaFuncSetAttribute(transition_kernel,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                             static_cast<int>(kQuadSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    CUtensorMap vmap;
+    alignas(64) static const char kZero[16] = {};
+    const void* vbase = a.v ? static_cast<const void*>(a.v) : static_cast<const void*>(kZero);
+    cudaError_t e = encode_v_map_sw128(&vmap, vbase, a.geo.tokens, a.H);
+    if (e != cudaSuccess) return e;
+    transition_kernel<<<static_cast<unsigned>(blocks), kTransWarps * 32, kQuadSmemBytes, stream>>>(a,
+                                                                                                  vmap);
+    return cudaGetLastError();
 }
 
 }  // namespace kda

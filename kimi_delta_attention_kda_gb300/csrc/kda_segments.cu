@@ -163,13 +163,34 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
         }
     }
     put_rows(xbuf, c, warp, g8, t4);
-    bool ok = group_all<kScanWarps * 32>(1, true);
+    bool ok = true;
 
     const uint32_t mi = lane >> 3, r8 = lane & 7;
+    // Step j's operands from its stage into registers: F_j^T (m = new key,
+    // k = old key) by transposing loads of F_j's rows (old key), and the C
+    // fragments of Z_j^T.  The stage is released right after.
+    uint32_t af[2][8][4], zf[4];
+    auto load_step = [&](int64_t j) -> bool {
+        const int s = static_cast<int>(j % kScanStages);
+        if (!mbar_wait_warp(&full[s], (j / kScanStages) & 1, a.status)) return false;
+        const uint8_t* stage = smem + s * kScanStageBytes;
+        ldsm_x4_trans(zf, smem_u32(stage + kScanFBytes + sw128_off(8, r8, 4 * warp + mi)));
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                const uint32_t row = 16 * kk + r8 + 8 * (mi >> 1);
+                const uint32_t ch = 4 * warp + 2 * mt + (mi & 1);
+                ldsm_x4_trans(af[mt][kk], smem_u32(stage + sw128_off(kHeadDim, row, ch)));
+            }
+        __syncwarp();
+        mbar_arrive_if(&empty[s], lane == 0);
+        return true;
+    };
+    if (a.segs > 0 && ok) ok = load_step(0);
+    ok = group_all<kScanWarps * 32>(1, ok);
     for (int64_t j = 0; j < a.segs && ok; ++j) {
         const uint8_t* xc = xbuf + (j & 1) * kScanXBytes;
-        // S_j is this segment's incoming state.
-        copy_rows_out(xc, a.starts + (((n * a.segs + j) * a.H + h) * kHeadDim + v0) * kHeadDim, tid);
         // B operand: S_j^T (k = key of S_j, n = value row), all 8 k-steps.
         uint32_t b[8][2];
 #pragma unroll
@@ -181,44 +202,29 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
             b[2 * kp + 1][0] = r[2];
             b[2 * kp + 1][1] = r[3];
         }
-        const int s = static_cast<int>(j % kScanStages);
-        if (!mbar_wait_warp(&full[s], (j / kScanStages) & 1, a.status)) ok = false;
-        if (ok) {
-            const uint8_t* stage = smem + s * kScanStageBytes;
-            // Accumulators: Z_j^T (k = 0 half) and zero (k = 1 half).
-            float acc[2][2][4];
-            {
-                uint32_t z[4];
-                ldsm_x4_trans(z, smem_u32(stage + kScanFBytes + sw128_off(8, r8, 4 * warp + mi)));
+        // Accumulators: Z_j^T (even k-steps) and zero (odd k-steps).
+        float acc[2][2][4];
 #pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    acc[mt][0][0] = bf_lo(z[2 * mt]);
-                    acc[mt][0][1] = bf_hi(z[2 * mt]);
-                    acc[mt][0][2] = bf_lo(z[2 * mt + 1]);
-                    acc[mt][0][3] = bf_hi(z[2 * mt + 1]);
-                    acc[mt][1][0] = acc[mt][1][1] = acc[mt][1][2] = acc[mt][1][3] = 0.f;
-                }
-            }
-            // F_j^T (m = new key, k = old key) from F_j's rows (old key) by
-            // transposing loads.
-#pragma unroll
-            for (int kk = 0; kk < 8; ++kk)
-#pragma unroll
-                for (int mt = 0; mt < 2; ++mt) {
-                    uint32_t af[4];
-                    const uint32_t row = 16 * kk + r8 + 8 * (mi >> 1);
-                    const uint32_t ch = 4 * warp + 2 * mt + (mi & 1);
-                    ldsm_x4_trans(af, smem_u32(stage + sw128_off(kHeadDim, row, ch)));
-                    mma_bf16(acc[mt][kk & 1], af, b[kk], acc[mt][kk & 1]);
-                }
-            __syncwarp();
-            mbar_arrive_if(&empty[s], lane == 0);
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-                for (int e = 0; e < 4; ++e) c[mt][e] = acc[mt][0][e] + acc[mt][1][e];
-            put_rows(xbuf + ((j + 1) & 1) * kScanXBytes, c, warp, g8, t4);
+        for (int mt = 0; mt < 2; ++mt) {
+            acc[mt][0][0] = bf_lo(zf[2 * mt]);
+            acc[mt][0][1] = bf_hi(zf[2 * mt]);
+            acc[mt][0][2] = bf_lo(zf[2 * mt + 1]);
+            acc[mt][0][3] = bf_hi(zf[2 * mt + 1]);
+            acc[mt][1][0] = acc[mt][1][1] = acc[mt][1][2] = acc[mt][1][3] = 0.f;
         }
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) mma_bf16(acc[mt][kk & 1], af[mt][kk], b[kk], acc[mt][kk & 1]);
+        // While the MMAs run: S_j out as this segment's incoming state, and
+        // the next step's operands in.
+        copy_rows_out(xc, a.starts + (((n * a.segs + j) * a.H + h) * kHeadDim + v0) * kHeadDim, tid);
+        if (j + 1 < a.segs && !load_step(j + 1)) ok = false;
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+            for (int e = 0; e < 4; ++e) c[mt][e] = acc[mt][0][e] + acc[mt][1][e];
+        put_rows(xbuf + ((j + 1) & 1) * kScanXBytes, c, warp, g8, t4);
         ok = group_all<kScanWarps * 32>(1, ok);
     }
     if (ok && a.final_state)
