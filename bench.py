@@ -73,11 +73,12 @@ STATE_BYTES = 128 * 128 * 2
 # kernel's sources still hash to the value they had when it was captured.
 REC_SOURCES = ("kda_recurrence.cu", "kda_rec_impl.cuh", "kda_common.cuh")
 PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
-FUSED_SOURCES = ("kda_fused.cu", "kda_prep_impl.cuh", "kda_rec_impl.cuh", "kda_common.cuh")
+SEG_SOURCES = ("kda_segments.cu", "kda_common.cuh")
 PROFILED_TRAFFIC = {
-    ("fused", "t8192_h6"): (77.884e6, FUSED_SOURCES, "aa0f826f6b03cd6a"),
-    ("recurrence", "t8192_h96"): (1067.049e6, REC_SOURCES, "806d87c2bfa734e7"),
-    ("chunk_prep", "t8192_h96"): (1460.424e6, PREP_SOURCES, "f4ed658ee797cb7a"),
+    ("transition", "t8192_h6"): (55.514e6, REC_SOURCES, "703f5024d16930e2"),
+    ("segment_chain", "t65536_h1"): (10.009e6, SEG_SOURCES, "469bcecb9ef0f87e"),
+    ("recurrence", "t8192_h96"): (1067.616e6, REC_SOURCES, "703f5024d16930e2"),
+    ("chunk_prep", "t8192_h96"): (1460.403e6, PREP_SOURCES, "983222c2baaef973"),
 }
 
 
