@@ -76,6 +76,7 @@ PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
 SEG_SOURCES = ("kda_segments.cu", "kda_common.cuh")
 PROFILED_TRAFFIC = {
     ("transition", "t8192_h6"): (55.514e6, REC_SOURCES, "703f5024d16930e2"),
+    ("chunk_prep", "t8192_h6"): (54.477e6, PREP_SOURCES, "983222c2baaef973"),
     ("segment_chain", "t65536_h1"): (10.009e6, SEG_SOURCES, "469bcecb9ef0f87e"),
     ("recurrence", "t8192_h96"): (1067.616e6, REC_SOURCES, "703f5024d16930e2"),
     ("chunk_prep", "t8192_h96"): (1460.403e6, PREP_SOURCES, "983222c2baaef973"),
