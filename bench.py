@@ -318,6 +318,44 @@ def measured_peaks():
         return 6800.0, "fallback"
 
 
+def measured_tensor_peak():
+    """Dense BF16 TFLOP/s (burst) from MEASURED_PEAKS.json, else the recipe's fallback."""
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as f:
+            return float(json.load(f)["bf16_tflops"]), "measured"
+    except (OSError, KeyError, ValueError):
+        return 1900.0, "fallback"
+
+
+# Algorithmic FLOPs per head-token of the chunkwise form at C = 16 (dense
+# 16-tiles): the three 128 x 128 x 16 state products per chunk, the A^qk and R
+# scores, U (A^kk)^T and U (A^qk)^T, and the 16 x 16 inverse, per 16 tokens.
+FLOP_PER_HT = (3 * 2 * 128 * 128 * 16 + 2 * 65536 + 2 * 65536 + 49152) / 16
+
+
+def critical_path(kda, inp, ht, state_io, us_per_call):
+    """Bounds on the call: HBM (the path's algorithmic bytes at the measured
+    copy bandwidth), tensor (its FLOPs at the measured BF16 rate) and the
+    serial chain (the longest sequence's chunk steps times the measured
+    shortest dependent chunk-step chain); `frac` = the largest over the time."""
+    t_step = kda._lib.chain_step_ns()
+    if inp["cu_seqlens"] is None:
+        steps = int(math.ceil(inp["q"].shape[1] / 16))
+    else:
+        cu = inp["cu_seqlens"].tolist()
+        steps = max((cu[i + 1] - cu[i] + 15) // 16 for i in range(len(cu) - 1))
+    hbm_gbs, _ = measured_peaks()
+    tflops, tkind = measured_tensor_peak()
+    hbm_us = (PATH_BYTES_PER_HT * ht + state_io) / (hbm_gbs * 1e3)
+    tensor_us = FLOP_PER_HT * ht / (tflops * 1e6)
+    chain_us = steps * t_step / 1e3
+    bound = max(hbm_us, tensor_us, chain_us)
+    kind = "chain" if bound == chain_us else ("hbm" if bound == hbm_us else "tensor")
+    return {"t_step_ns": t_step, "chain_steps": steps, "chain_bound_us": chain_us,
+            "hbm_bound_us": hbm_us, "tensor_bound_us": tensor_us, "tensor_peak_kind": tkind,
+            "bound_us": bound, "bound": kind, "frac": bound / us_per_call}
+
+
 def run_ours(args):
     import kimi_delta_attention_kda_gb300 as kda
     ws, rank, local = dist_env()
@@ -412,6 +450,7 @@ def run_ours(args):
         roofline.update({"prep_us": 1e3 * prep_avg, "recurrence_us": 1e3 * rec_avg})
     if segs:
         roofline.update({"transition_us": 1e3 * trans_avg, "segment_chain_us": 1e3 * chain_avg})
+    roofline["critical_path"] = critical_path(kda, inp, ht, state_io, 1e3 * total_ms / args.steps)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,

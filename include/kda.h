@@ -248,6 +248,19 @@ int kda_profile_end(double* prep_ms, double* recurrence_ms, int* calls);
 int kda_profile_end_detail(double* intervals_ms, int* calls);
 
 /*
+ * Measurement hook: nanoseconds per step of the shortest dependent chain of
+ * one chunk step on the current device (HOST out), for the critical-path
+ * bound of a serial walk over the chunks ("FlashKDA column split" section 1:
+ * chunk c + 1 needs chunk c's state).  One warp runs, 4,096 times, U^T = K'
+ * S^T over 128 keys (two interleaved MMA accumulators and an add), the BF16
+ * conversion and transpose of U^T, S^T <- D S^T + (K^end)^T U^T and the BF16
+ * conversion and transpose of the new state, with operands in registers.
+ * Synchronises the device; not for use on a hot path.  KDA_ERR_DEVICE
+ * without a compute capability 10.3 device, KDA_ERR_CUDA on a CUDA error.
+ */
+int kda_chain_step_ns(double* ns);
+
+/*
  * kda_prefill without any allocation.  The pages describe no such entry
  * point; it exists for callers that cannot let a library allocate device
  * memory: code running under an allocator that owns all of the GPU's memory

@@ -76,6 +76,8 @@ def load():
         lib.kda_profile_end.restype = I
         lib.kda_profile_end_detail.argtypes = [D, ctypes.POINTER(I)]
         lib.kda_profile_end_detail.restype = I
+        lib.kda_chain_step_ns.argtypes = [ctypes.POINTER(ctypes.c_double)]
+        lib.kda_chain_step_ns.restype = I
         lib.kda_prefill_noalloc.argtypes = [P] * 8 + [I64] * 3 + [P, P]
         lib.kda_prefill_noalloc.restype = I
         lib.kda_noalloc_scratch_bytes.argtypes = []
@@ -203,6 +205,13 @@ def profile_end_detail():
     n = ctypes.c_int(0)
     _check(load().kda_profile_end_detail(t, ctypes.byref(n)), "kda_profile_end_detail")
     return [t[i] for i in range(4)], n.value
+
+
+def chain_step_ns() -> float:
+    """Nanoseconds per step of the shortest dependent chunk-step chain (one warp)."""
+    v = ctypes.c_double(0)
+    _check(load().kda_chain_step_ns(ctypes.byref(v)), "kda_chain_step_ns")
+    return v.value
 
 
 def prefill_noalloc_raw(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,

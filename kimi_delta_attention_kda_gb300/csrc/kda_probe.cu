@@ -1,0 +1,123 @@
+// kda_probe.cu -- measurement hook: the time of the shortest dependent chain
+// of one chunk step, which bounds any serial walk over the chunks.
+//
+// The recurrence ("FlashKDA column split", section 1, with the key
+// contraction folded as U = V (A^kk B)^T + S K'^T) cannot start the
+// state-dependent part of chunk c + 1 before chunk c's state exists.  For one
+// warp's 8 value columns that part is at least: U^T = K' S^T over the 128 keys
+// (8 m16n8k16 MMAs as two interleaved accumulators, then one add), U^T to a
+// BF16 operand (convert, 8x8 transpose), S^T <- D S^T + (K^end)^T U^T (one
+// MMA per 16-key tile, independent across tiles), and the new S^T to BF16
+// operands (convert, transpose).  The probe runs exactly that chain `iters`
+// times in one warp, with operand fragments held in registers (no memory
+// traffic), and reports %globaltimer nanoseconds per step.
+#include "../../include/kda.h"
+#include "kda_common.cuh"
+
+namespace kda {
+namespace {
+
+__device__ __forceinline__ unsigned long long global_ns() {
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+__device__ __forceinline__ uint32_t movm_trans(uint32_t x) {
+    uint32_t y;
+    asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+    return y;
+}
+
+__global__ void __launch_bounds__(32, 1) chain_probe_kernel(int iters, float scale,
+                                                            unsigned long long* out) {
+    const int lane = threadIdx.x;
+    // Small constant operands keep the state bounded (MMA timing does not
+    // depend on the values).
+    const float a = scale * static_cast<float>((lane & 7) + 1);
+    uint32_t ks[8][4], ke[8][4], Sb[8][2];
+    float Sf[8][4];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            ks[i][j] = pack_bf16(a * (i + 1), -a * (j + 1));
+            ke[i][j] = pack_bf16(-a * (j + 2), a * (i + 2));
+            Sf[i][j] = a * (i - j);
+        }
+        Sb[i][0] = movm_trans(pack_bf16(Sf[i][0], Sf[i][1]));
+        Sb[i][1] = movm_trans(pack_bf16(Sf[i][2], Sf[i][3]));
+    }
+    const float d = 0.5f;
+    unsigned long long t0 = 0;
+    for (int it = 0; it < iters; ++it) {
+        if (it == 1) t0 = global_ns();   // the first step warms the pipeline
+        float ua[4] = {0.f, 0.f, 0.f, 0.f}, ub[4] = {0.f, 0.f, 0.f, 0.f};
+#pragma unroll
+        for (int i = 0; i < 8; i += 2) {
+            mma_bf16(ua, ks[i], Sb[i], ua);
+            mma_bf16(ub, ks[i + 1], Sb[i + 1], ub);
+        }
+        uint32_t Ub[2];
+        Ub[0] = movm_trans(pack_bf16(ua[0] + ub[0], ua[1] + ub[1]));
+        Ub[1] = movm_trans(pack_bf16(ua[2] + ub[2], ua[3] + ub[3]));
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+#pragma unroll
+            for (int j = 0; j < 4; ++j) Sf[i][j] *= d;
+            mma_bf16(Sf[i], ke[i], Ub, Sf[i]);
+        }
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+            Sb[i][0] = movm_trans(pack_bf16(Sf[i][0], Sf[i][1]));
+            Sb[i][1] = movm_trans(pack_bf16(Sf[i][2], Sf[i][3]));
+        }
+    }
+    const unsigned long long t1 = global_ns();
+    float acc = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc += Sf[i][0] + Sf[i][3];
+    if (lane == 0) {
+        out[0] = t1 - t0;
+        out[1] = __float_as_uint(acc);   // keeps the chain's result live
+    }
+}
+
+}  // namespace
+}  // namespace kda
+
+extern "C" int kda_chain_step_ns(double* ns) {
+    if (!ns) return KDA_ERR_NULL;
+    int dev = -1, major = 0, minor = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_DEVICE;
+    }
+    if (major != 10 || minor != 3) return KDA_ERR_DEVICE;
+    constexpr int kIters = 4097;
+    unsigned long long* d_out = nullptr;
+    unsigned long long h_out[2] = {0, 0};
+    int rc = KDA_OK;
+    if (cudaMalloc(reinterpret_cast<void**>(&d_out), sizeof(h_out)) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    // Warm-up launch, then the measured one (the first step of each is not timed).
+    for (int rep = 0; rep < 2 && rc == KDA_OK; ++rep) {
+        kda::chain_probe_kernel<<<1, 32>>>(rep == 0 ? 64 : kIters, 1.0f / 1024.f, d_out);
+        if (cudaGetLastError() != cudaSuccess || cudaDeviceSynchronize() != cudaSuccess)
+            rc = KDA_ERR_CUDA;
+    }
+    if (rc == KDA_OK &&
+        cudaMemcpy(h_out, d_out, sizeof(h_out), cudaMemcpyDeviceToHost) != cudaSuccess)
+        rc = KDA_ERR_CUDA;
+    cudaFree(d_out);
+    if (rc != KDA_OK) {
+        cudaGetLastError();
+        return rc;
+    }
+    *ns = static_cast<double>(h_out[0]) / (kIters - 1);
+    return KDA_OK;
+}

@@ -426,7 +426,7 @@ constexpr uint32_t kQuadVRowBytes = kHeadDim * 2;
 constexpr uint32_t kQuadVOff = ((kPacketBytes + 1023) / 1024) * 1024;
 constexpr uint32_t kQuadStageBytes = ((kQuadVOff + kChunk * kQuadVRowBytes + 1023) / 1024) * 1024;
 constexpr int kQuadWarps = 4;
-constexpr int kQuadStages = 6;
+constexpr int kQuadStages = 8;
 constexpr uint32_t kQuadBarOff = kQuadStages * kQuadStageBytes;
 constexpr uint32_t kQuadSmemBytes = kQuadBarOff + 2 * kQuadStages * 8 + 1024;
 

@@ -101,6 +101,9 @@ def test_no_device_here(lib):
     assert call(lib) == -5
     st = ctypes.c_int(0)
     assert lib.kda_device_status(None, ctypes.byref(st)) == -5
+    ns = ctypes.c_double(0)
+    assert lib.kda_chain_step_ns(ctypes.byref(ns)) == -5
+    assert lib.kda_chain_step_ns(None) == -1
 
 
 def test_split_option(lib):

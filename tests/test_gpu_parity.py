@@ -479,3 +479,11 @@ def test_long_sequences_at_split_two_bitwise(kda):
     finally:
         kda.set_split(0)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+
+
+def test_chain_step_probe(kda):
+    """The measurement hook behind the critical-path bound: a plausible time per
+    step of the shortest dependent chunk-step chain (a few hundred cycles)."""
+    from kimi_delta_attention_kda_gb300 import _lib
+    ns = _lib.chain_step_ns()
+    assert 20.0 < ns < 5000.0, ns
