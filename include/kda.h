@@ -181,8 +181,8 @@ int kda_plan_long_split(int64_t n_seqs, int64_t T, int64_t H, int64_t* k);
  * The chunkwise state update is affine in the incoming state, so over a run
  * of chunks it is S -> S F + Z ("Kimi Linear" technical report, chunkwise
  * KDA: S_{c+1} = S_c D_c + U_c K^end_c with U_c affine in S_c).  When there
- * are too few (sequence, head) chains to fill the GPU (fixed-length batches,
- * engine 0, automatic split, no checkpoints), each sequence is cut into
+ * are too few (sequence, head) chains to fill the GPU (engine 0, automatic
+ * split, no checkpoints; fixed or packed layout), each sequence is cut into
  * segments: one launch forms every segment's F and Z, a short chain over the
  * segments forms each segment's incoming state, and one launch reruns every
  * segment from its incoming state and writes O.  The results agree with the
@@ -195,9 +195,11 @@ int kda_plan_long_split(int64_t n_seqs, int64_t T, int64_t H, int64_t* k);
 int kda_set_segments(int on, int64_t seg_chunks);
 
 /*
- * Segments per sequence kda_prefill would use for a call of this shape on the
- * current device under the current settings (HOST out; 0: no segmented scan).
- * Errors as kda_plan_fused.
+ * Segments kda_prefill would use for a call of this shape on the current
+ * device under the current settings (HOST out; 0: no segmented scan): per
+ * sequence for the fixed layout; for the packed layout a bound on all
+ * segments (the cut itself is made on the device from cu_seqlens).  Errors as
+ * kda_plan_fused.
  */
 int kda_plan_segments(int64_t B, int64_t T, int64_t H, int packed, int64_t* segs);
 

@@ -5,6 +5,7 @@
 // recurrence) on the caller's stream.  No host <-> device synchronisation and
 // no host reads of device data happen here (flashinfer kda_prefill, "Optimized
 // Blackwell prefill subset": cu_seqlens is never inspected on the host).
+#include <cmath>
 #include <mutex>
 
 #include "../../include/kda.h"
@@ -188,48 +189,71 @@ int64_t long_split_count(const Plan& pl, int64_t H, int nsplit, int sms) {
 
 // Segmented scan over chunks (kda_segments.cu): with few (sequence, head)
 // chains the serial recurrence leaves most SMs idle, so each sequence is cut
-// into `segs` segments of seg_chunks chunks and run in three launches (every
-// segment's zero-start state and state map; a short chain over the segments;
-// every segment again from its true incoming state).  The choice compares
-// rough costs in microseconds, measured on GB300 at T = 8192: a chunk step
-// of the serial chain at split 8-16, of the one-CTA-per-head kernel, and of
-// its transition pass; a step of the segment chain; the launches' fixed cost.
-constexpr double kSerialChunkUs = 0.35;
+// into segments of seg_chunks chunks and run in three launches (every
+// segment's zero-start state and state map; a short chain over each
+// sequence's segments; every segment again from its true incoming state).
+// The choice compares rough costs in microseconds, measured on GB300: a chunk
+// step of the serial chain at the automatic split; a chunk of the transition
+// pass and of the rerun; a step of the segment chain; the passes' fixed cost.
+double serial_chunk_us(int nsplit) {
+    return nsplit >= 16 ? 0.35 : nsplit == 8 ? 0.40 : nsplit == 4 ? 0.58 : nsplit == 2 ? 0.75 : 0.9;
+}
+constexpr double kTransChunkUs = 1.25;
 constexpr double kQuadChunkUs = 1.0;
-constexpr double kTransChunkUs = 0.7;
-constexpr double kScanStepUs = 0.3;
-constexpr double kSegFixedUs = 25.0;
+constexpr double kScanStepUs = 0.6;
+constexpr double kSegFixedUs = 12.0;
 
 struct SegChoice {
-    int64_t segs = 0;         // segments per sequence (0: no segmented scan)
+    int64_t segs = 0;         // fixed: segments per sequence; packed: a bound on all segments (0: none)
     int64_t seg_chunks = 0;   // chunks per segment (the last one of a sequence shorter)
-    int64_t state_bytes = 0;  // bytes of each of the three [N * segs][H][128][128] BF16 buffers
+    int64_t total = 0;        // segments the three state buffers hold
+    int64_t state_bytes = 0;  // bytes of each of the three [total][H][128][128] BF16 buffers
+    int64_t meta_bytes = 0;   // packed: seg_begin, seg_chunks, seg_tokens (256-aligned each)
 };
+
+int64_t align256(int64_t b) { return ((b + 255) / 256) * 256; }
 
 SegChoice plan_segments(const Plan& pl, int64_t H, int sms, bool checkpoints) {
     SegChoice sc;
-    if (!g_segments || g_engine != 0 || g_split_override || pl.packed || checkpoints ||
-        pl.tokens <= 0)
-        return sc;
+    if (!g_segments || g_engine != 0 || g_split_override || checkpoints || pl.tokens <= 0) return sc;
     const int64_t units = pl.N * H;
-    const int64_t chunks = pl.geo.chunks_per_seq;
-    if (g_seg_chunks > 0) {
-        sc.seg_chunks = g_seg_chunks;
-        sc.segs = (chunks + g_seg_chunks - 1) / g_seg_chunks;
-        sc.state_bytes = pl.N * sc.segs * H * kHeadDim * kHeadDim * 2;
-        return sc;
+    const double t_serial = serial_chunk_us(choose_split(units, sms));
+    if (pl.packed) {
+        // Sequence lengths stay on the device: plan on the bound of all
+        // chunks; the longest sequence has at least the mean.
+        const int64_t C = pl.geo.chunk_ub, N = pl.N;
+        int64_t L = g_seg_chunks;
+        if (L <= 0) {
+            const int64_t budget = sms / H;   // segments per head in one wave
+            if (budget < N + 4) return sc;
+            L = (C + (budget - N) - 1) / (budget - N);
+            const double mean = static_cast<double>(C) / static_cast<double>(N);
+            const double seg_us = kSegFixedUs + L * (kTransChunkUs + kQuadChunkUs) +
+                                  std::ceil(mean / L) * kScanStepUs;
+            if (seg_us >= mean * t_serial) return sc;
+        }
+        sc.seg_chunks = L;
+        sc.segs = C / L + N;
+        sc.total = sc.segs;
+        sc.meta_bytes = align256(8 * (N + 1)) + 2 * align256(8 * (sc.segs + 1));
+    } else {
+        const int64_t chunks = pl.geo.chunks_per_seq;
+        int64_t L = g_seg_chunks;
+        if (L <= 0) {
+            const int64_t target = sms / units;   // segments per sequence: one wave
+            if (target < 4) return sc;
+            L = (chunks + target - 1) / target;
+            const int64_t segs = (chunks + L - 1) / L;
+            if (segs < 4) return sc;
+            const double seg_us =
+                kSegFixedUs + L * (kTransChunkUs + kQuadChunkUs) + segs * kScanStepUs;
+            if (seg_us >= chunks * t_serial) return sc;
+        }
+        sc.seg_chunks = L;
+        sc.segs = (chunks + L - 1) / L;
+        sc.total = pl.N * sc.segs;
     }
-    const int64_t target = sms / units;   // segments per sequence: one wave in the last pass
-    if (target < 4) return sc;
-    const int64_t L = (chunks + target - 1) / target;
-    const int64_t segs = (chunks + L - 1) / L;
-    if (segs < 4) return sc;
-    const double waves = static_cast<double>((2 * segs * units + sms - 1) / sms);
-    const double seg_us = kSegFixedUs + L * (waves * kTransChunkUs + kQuadChunkUs) + segs * kScanStepUs;
-    if (seg_us >= chunks * kSerialChunkUs) return sc;
-    sc.segs = segs;
-    sc.seg_chunks = L;
-    sc.state_bytes = pl.N * segs * H * kHeadDim * kHeadDim * 2;
+    sc.state_bytes = sc.total * H * kHeadDim * kHeadDim * 2;
     return sc;
 }
 
@@ -349,8 +373,8 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
     const int nsplit = choose_split(pl.N * H, d->sms);
     const SegChoice sc = plan_segments(pl, H, d->sms, ck != nullptr);
     const bool fused = sc.segs == 0 && use_fusion(pl, H, nsplit, d->sms);
-    const int64_t ws_bytes =
-        pl.meta_bytes + pl.packet_bytes + (fused ? pl.ready_bytes : 0) + 3 * sc.state_bytes;
+    const int64_t ws_bytes = pl.meta_bytes + pl.packet_bytes + (fused ? pl.ready_bytes : 0) +
+                             3 * sc.state_bytes + sc.meta_bytes;
     uint8_t* ws = nullptr;
     if (ws_bytes > 0) {
         if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes),
@@ -387,17 +411,36 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         uint8_t* maps = zstates + sc.state_bytes;
         uint8_t* starts = maps + sc.state_bytes;
         rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, packets, d, stream, &geo);
-        prof_record(1, stream);
         SeqGeometry sg = geo;
-        sg.n_seqs = pl.N * sc.segs;
-        sg.seg_chunks = sc.seg_chunks;
-        sg.segs_per_seq = sc.segs;
+        int64_t* seg_begin = nullptr;
+        if (pl.packed) {
+            // Segment offsets from the device-side chunk offsets.
+            seg_begin = reinterpret_cast<int64_t*>(starts + sc.state_bytes);
+            int64_t* seg_chunk0 = seg_begin + align256(8 * (pl.N + 1)) / 8;
+            int64_t* seg_tok0 = seg_chunk0 + align256(8 * (sc.segs + 1)) / 8;
+            if (rc == KDA_OK &&
+                launch_segment_meta(cu_seqlens, geo.cu_chunks, const_cast<int32_t*>(geo.valid), pl.N,
+                                    sc.seg_chunks, sc.segs, seg_begin, seg_chunk0, seg_tok0,
+                                    d->status, stream) != cudaSuccess)
+                rc = KDA_ERR_CUDA;
+            sg.n_seqs = sc.segs;
+            sg.cu_seqlens = seg_tok0;
+            sg.cu_chunks = seg_chunk0;
+            sg.order = nullptr;
+        } else {
+            sg.n_seqs = pl.N * sc.segs;
+            sg.seg_chunks = sc.seg_chunks;
+            sg.segs_per_seq = sc.segs;
+        }
+        prof_record(1, stream);
         if (rc == KDA_OK &&
             launch_transition(v, packets, sg, H, zstates, maps, d->status, stream) != cudaSuccess)
             rc = KDA_ERR_CUDA;
         prof_record(2, stream);
-        if (rc == KDA_OK && launch_segment_scan(init_state, final_state, maps, zstates, starts, pl.N,
-                                                sc.segs, H, d->status, stream) != cudaSuccess)
+        if (rc == KDA_OK &&
+            launch_segment_scan(init_state, final_state, maps, zstates, starts, pl.N, sc.segs,
+                                seg_begin, pl.packed ? geo.valid : nullptr, H, d->status,
+                                stream) != cudaSuccess)
             rc = KDA_ERR_CUDA;
         prof_record(3, stream);
         if (rc == KDA_OK &&
@@ -633,7 +676,8 @@ extern "C" int kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int packed, 
     DeviceState* d = nullptr;
     if (device_state(&d) == KDA_OK) sms = d->sms;
     const SegChoice sc = plan_segments(pl, H, sms, false);
-    *bytes = pl.meta_bytes + pl.packet_bytes + (pl.packed ? 0 : pl.ready_bytes) + 3 * sc.state_bytes;
+    *bytes = pl.meta_bytes + pl.packet_bytes + (pl.packed ? 0 : pl.ready_bytes) +
+             3 * sc.state_bytes + sc.meta_bytes;
     return KDA_OK;
 }
 

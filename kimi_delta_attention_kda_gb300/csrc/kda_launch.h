@@ -73,11 +73,24 @@ cudaError_t launch_transition(const void* v, const uint8_t* packets, const SeqGe
 
 // Second pass: per sequence and head, the segments' incoming states in order,
 // S_0 = init (zero when null), S_{j+1} = S_j F_j + Z_j, written as BF16 to
-// starts[(n * segs + j) * H + h] for j < segs, and S_segs to final_state
-// (when not null).
+// starts[segment * H + h] for the sequence's segments and the last one to
+// final_state (when not null).  Fixed layout (seg_begin null): sequence n's
+// segments are n segs .. n segs + segs - 1.  Packed layout: seg_begin[n] ..
+// seg_begin[n + 1] - 1 from launch_segment_meta, `segs` bounds the total and
+// `valid` is the metadata's verdict.
 cudaError_t launch_segment_scan(const void* init_state, void* final_state, const void* transitions,
                                 const void* zero_start_states, void* starts, int64_t n_seqs,
-                                int64_t segs, int64_t H, int* status, cudaStream_t stream);
+                                int64_t segs, const int64_t* seg_begin, const int32_t* valid,
+                                int64_t H, int* status, cudaStream_t stream);
+
+// Segments of a packed batch of n_seqs sequences (after launch_varlen_meta):
+// ceil(chunks / seg_chunks_len) per sequence, at most s_ub in all; writes
+// seg_begin [n_seqs + 1] and, per segment, its first chunk and first token
+// ([s_ub + 1] each, padded with the batch's end).
+cudaError_t launch_segment_meta(const int64_t* cu_seqlens, const int64_t* cu_chunks, int32_t* valid,
+                                int64_t n_seqs, int64_t seg_chunks_len, int64_t s_ub,
+                                int64_t* seg_begin, int64_t* seg_chunks, int64_t* seg_tokens,
+                                int* status, cudaStream_t stream);
 
 // The tcgen05 recurrence: one CTA per (sequence, head).
 cudaError_t launch_recurrence_tc(const void* v, void* out, const void* init_state,

@@ -63,7 +63,11 @@ __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 
 struct ScanArgs {
     const __nv_bfloat16* init_state;   // [N][H][128][128] or null
     __nv_bfloat16* final_state;        // [N][H][128][128] or null
-    __nv_bfloat16* starts;             // [N * segs][H][128][128]
+    __nv_bfloat16* starts;             // [segments][H][128][128]
+    // Sequence n's segments: seg_begin[n] .. seg_begin[n + 1] - 1 (packed
+    // layout), or n segs .. n segs + segs - 1 (seg_begin null: fixed layout).
+    const int64_t* seg_begin;
+    const int32_t* valid;              // packed layout: the metadata's verdict
     int64_t segs, H;
     int* status;
 };
@@ -104,6 +108,9 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
     const int v0 = kScanRows * static_cast<int>(blockIdx.x - nh * kGroups);
     const int64_t n = nh / a.H;
     const int64_t h = nh - n * a.H;
+    if (a.valid && !*a.valid) return;
+    const int64_t first = a.seg_begin ? a.seg_begin[n] : n * a.segs;
+    const int64_t nseg = a.seg_begin ? a.seg_begin[n + 1] - first : a.segs;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kScanStages; ++s) {
             mbar_init(&full[s], 1);
@@ -117,14 +124,14 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
         // ------------------------------------------------------------ producer
         uint32_t fill_parity = 0, filled = 0;
         bool ok = true;
-        for (int64_t j = 0; j < a.segs && ok; ++j) {
+        for (int64_t j = 0; j < nseg && ok; ++j) {
             const int s = static_cast<int>(j % kScanStages);
             if (j >= kScanStages)
                 ok = mbar_wait_warp_sleep(&empty[s], ((j / kScanStages) - 1) & 1, a.status);
             if (!ok) break;
             uint8_t* stage = smem + s * kScanStageBytes;
             if (lane == 0) {
-                const int32_t row = static_cast<int32_t>(((n * a.segs + j) * a.H + h) * kHeadDim);
+                const int32_t row = static_cast<int32_t>(((first + j) * a.H + h) * kHeadDim);
                 mbar_arrive_expect_tx(&full[s], kScanFBytes + kScanZBytes);
                 tma_load_2d(stage, &fmap, 0, row, &full[s]);
                 tma_load_2d(stage + kScanFBytes / 2, &fmap, 64, row, &full[s]);
@@ -187,9 +194,9 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
         mbar_arrive_if(&empty[s], lane == 0);
         return true;
     };
-    if (a.segs > 0 && ok) ok = load_step(0);
+    if (nseg > 0 && ok) ok = load_step(0);
     ok = group_all<kScanWarps * 32>(1, ok);
-    for (int64_t j = 0; j < a.segs && ok; ++j) {
+    for (int64_t j = 0; j < nseg && ok; ++j) {
         const uint8_t* xc = xbuf + (j & 1) * kScanXBytes;
         // B operand: S_j^T (k = key of S_j, n = value row), all 8 k-steps.
         uint32_t b[8][2];
@@ -218,8 +225,8 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
             for (int mt = 0; mt < 2; ++mt) mma_bf16(acc[mt][kk & 1], af[mt][kk], b[kk], acc[mt][kk & 1]);
         // While the MMAs run: S_j out as this segment's incoming state, and
         // the next step's operands in.
-        copy_rows_out(xc, a.starts + (((n * a.segs + j) * a.H + h) * kHeadDim + v0) * kHeadDim, tid);
-        if (j + 1 < a.segs && !load_step(j + 1)) ok = false;
+        copy_rows_out(xc, a.starts + (((first + j) * a.H + h) * kHeadDim + v0) * kHeadDim, tid);
+        if (j + 1 < nseg && !load_step(j + 1)) ok = false;
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
 #pragma unroll
@@ -228,17 +235,90 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
         ok = group_all<kScanWarps * 32>(1, ok);
     }
     if (ok && a.final_state)
-        copy_rows_out(xbuf + (a.segs & 1) * kScanXBytes, a.final_state + rows0 * kHeadDim, tid);
+        copy_rows_out(xbuf + (nseg & 1) * kScanXBytes, a.final_state + rows0 * kHeadDim, tid);
+}
+
+// Segments of a packed batch (one block): sequence n, of c_n chunks, gets
+// ceil(c_n / L) segments of L chunks (the last one shorter; none when empty),
+// numbered sequence by sequence.  Writes seg_begin[0..N], and for segment s
+// its first chunk seg_chunks[s] and first token seg_tokens[s]; entries from
+// the last segment to bound s_ub repeat the batch's end, so segments past the
+// real ones are empty.  Runs after the varlen metadata and exits when it found
+// the offsets invalid (every later kernel then returns at once); a count
+// above s_ub (impossible for valid offsets) invalidates the batch as well.
+constexpr int kSegMetaThreads = 1024;
+
+__global__ void __launch_bounds__(kSegMetaThreads)
+    segment_meta_kernel(const int64_t* cu, const int64_t* cu_chunks, int32_t* valid, int64_t N,
+                        int64_t L, int64_t s_ub, int64_t* seg_begin, int64_t* seg_chunks,
+                        int64_t* seg_tokens, int* status) {
+    __shared__ int64_t warp_sums[kSegMetaThreads / 32];
+    __shared__ int64_t carry;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    if (!*valid) return;
+    if (tid == 0) {
+        carry = 0;
+        seg_begin[0] = 0;
+    }
+    __syncthreads();
+    for (int64_t base = 0; base < N; base += kSegMetaThreads) {
+        const int64_t n = base + tid;
+        const int64_t cnt = n < N ? (cu_chunks[n + 1] - cu_chunks[n] + L - 1) / L : 0;
+        int64_t x = cnt;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+            const int64_t y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+        }
+        if (lane == 31) warp_sums[warp] = x;
+        __syncthreads();
+        if (warp == 0) {
+            int64_t w = warp_sums[lane];
+#pragma unroll
+            for (int o = 1; o < 32; o <<= 1) {
+                const int64_t y = __shfl_up_sync(0xffffffffu, w, o);
+                if (lane >= o) w += y;
+            }
+            warp_sums[lane] = w;
+        }
+        __syncthreads();
+        const int64_t incl = x + (warp > 0 ? warp_sums[warp - 1] : 0) + carry;
+        if (n < N) {
+            seg_begin[n + 1] = incl;
+            const int64_t s0 = incl - cnt;
+            for (int64_t j = 0; j < cnt && s0 + j < s_ub; ++j) {
+                seg_chunks[s0 + j] = cu_chunks[n] + j * L;
+                seg_tokens[s0 + j] = cu[n] + kChunk * j * L;
+            }
+        }
+        __syncthreads();
+        if (tid == kSegMetaThreads - 1) carry = incl;
+        __syncthreads();
+    }
+    const int64_t total = carry;
+    if (total > s_ub) {
+        if (tid == 0) {
+            *valid = 0;
+            atomicOr(status, kDevBadSeqlens);
+        }
+        return;
+    }
+    for (int64_t sidx = total + tid; sidx <= s_ub; sidx += kSegMetaThreads) {
+        seg_chunks[sidx] = cu_chunks[N];
+        seg_tokens[sidx] = cu[N];
+    }
 }
 
 }  // namespace
 
 cudaError_t launch_segment_scan(const void* init_state, void* final_state, const void* transitions,
                                 const void* zero_start_states, void* starts, int64_t n_seqs,
-                                int64_t segs, int64_t H, int* status, cudaStream_t stream) {
+                                int64_t segs, const int64_t* seg_begin, const int32_t* valid,
+                                int64_t H, int* status, cudaStream_t stream) {
     const int64_t blocks = n_seqs * H * (kHeadDim / kScanRows);
-    if (blocks <= 0 || segs <= 0) return cudaSuccess;
-    const int64_t rows = n_seqs * segs * H * kHeadDim;
+    if (blocks <= 0) return cudaSuccess;
+    const int64_t total_segs = seg_begin ? segs : n_seqs * segs;
+    const int64_t rows = (total_segs > 0 ? total_segs : 1) * H * kHeadDim;
     if (rows >= (int64_t(1) << 31) || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
     static bool configured[64] = {};
     int dev = 0;
@@ -259,10 +339,23 @@ cudaError_t launch_segment_scan(const void* init_state, void* final_state, const
     a.final_state = static_cast<__nv_bfloat16*>(final_state);
     a.starts = static_cast<__nv_bfloat16*>(starts);
     a.segs = segs;
+    a.seg_begin = seg_begin;
+    a.valid = valid;
     a.H = H;
     a.status = status;
     segment_scan_kernel<<<static_cast<unsigned>(blocks), (kScanWarps + 1) * 32, kScanSmemBytes,
                           stream>>>(a, fmap, zmap);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_segment_meta(const int64_t* cu_seqlens, const int64_t* cu_chunks, int32_t* valid,
+                                int64_t n_seqs, int64_t seg_chunks_len, int64_t s_ub,
+                                int64_t* seg_begin, int64_t* seg_chunks, int64_t* seg_tokens,
+                                int* status, cudaStream_t stream) {
+    if (n_seqs <= 0 || seg_chunks_len <= 0) return cudaErrorInvalidValue;
+    segment_meta_kernel<<<1, kSegMetaThreads, 0, stream>>>(cu_seqlens, cu_chunks, valid, n_seqs,
+                                                          seg_chunks_len, s_ub, seg_begin,
+                                                          seg_chunks, seg_tokens, status);
     return cudaGetLastError();
 }
 

@@ -51,8 +51,10 @@ def test_plan(kda):
     assert kda.plan_segments(1, 8192, 6, False) > 0
     assert kda.plan_segments(1, 65536, 1, False) > 0
     assert kda.plan_segments(1, 8192, 96, False) == 0
-    assert kda.plan_segments(1, 8192, 6, True) == 0
     assert kda.plan_segments(1, 256, 1, False) == 0
+    # packed: a bound on all segments, from the total tokens
+    assert kda.plan_segments(2, 16384, 6, True) > 0
+    assert kda.plan_segments(8, 34816, 12, True) == 0   # 96 chains already fill most SMs
     try:
         kda.set_split(16)
         assert kda.plan_segments(1, 8192, 6, False) == 0
@@ -148,4 +150,67 @@ def test_full_workload_close_to_serial(kda, name):
                                "segmented vs serial O")
     tu.assert_within_tolerance(fin[0].double().numpy(), fin_s[0].double().numpy(), 0,
                                "segmented vs serial S")
+    tu.check_against_oracle(inp, out, fin)
+
+
+# ----------------------------------------------------------------------------
+# Packed layout: segments cut on the device from cu_seqlens
+# ----------------------------------------------------------------------------
+
+LENGTHS = [40, 0, 17, 256, 1, 100]
+
+
+@pytest.mark.parametrize("L", [1, 3, 7])
+def test_forced_packed(forced, L):
+    forced.set_segments(True, L)
+    inp = synthetic.make_inputs(0, 0, 2, 7000 + L, init_std=0.02, lengths=LENGTHS)
+    out, fin = run(forced, inp)
+    tu.check_against_oracle(inp, out, fin)
+    # empty sequence: final state = initial state
+    assert torch.equal(fin[1], inp["init_state"][1])
+
+
+def test_forced_packed_equals_fixed(forced):
+    """Equal lengths packed and the fixed layout, cut the same way, agree bit for bit."""
+    forced.set_segments(True, 5)
+    inp = synthetic.make_inputs(3, 400, 2, 7100, init_std=0.02)
+    out_f, fin_f = run(forced, inp)
+    packed = dict(inp)
+    for key in ("q", "k", "v", "g", "beta"):
+        packed[key] = inp[key].reshape(1, 3 * 400, *inp[key].shape[2:]).contiguous()
+    packed["cu_seqlens"] = torch.tensor([0, 400, 800, 1200], dtype=torch.int64)
+    out_p, fin_p = run(forced, packed)
+    assert torch.equal(out_p.reshape(out_f.shape), out_f) and torch.equal(fin_p, fin_f)
+
+
+def test_forced_packed_bad_offsets_leave_outputs(forced):
+    forced.set_segments(True, 2)
+    H = 2
+    inp = synthetic.make_inputs(1, 64, H, 7200, init_std=0.02)
+    d = tu.to_device(inp)
+    cu = torch.tensor([0, 40, 30, 64], dtype=torch.int64, device="cuda")
+    init = torch.randn((3, H, 128, 128), device="cuda").to(torch.bfloat16)
+    out = torch.full_like(d["v"], 7.0)
+    fin = torch.full_like(init, 3.0)
+    forced.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], init, cu_seqlens=cu, out=out,
+                       final_state=fin)
+    assert forced.device_status() & 1
+    assert torch.all(out == 7.0) and torch.all(fin == 3.0)
+
+
+def test_packed_plan_against_oracle(kda):
+    """Two 8,192-token sequences at H=6: the automatic plan segments them."""
+    assert kda.plan_segments(2, 16384, 6, True) > 0
+    inp = synthetic.make_inputs(0, 0, 6, 7300, init_std=0.02, lengths=[8192, 6000])
+    out, fin = run(kda, inp)
+    kda.set_segments(False)
+    try:
+        out_s, fin_s = run(kda, inp)
+    finally:
+        kda.set_segments(True, 0)
+    tu.assert_within_tolerance(out[0].double().numpy(), out_s[0].double().numpy(), 1,
+                               "segmented vs serial O")
+    for n in range(2):
+        tu.assert_within_tolerance(fin[n].double().numpy(), fin_s[n].double().numpy(), 0,
+                                   "segmented vs serial S")
     tu.check_against_oracle(inp, out, fin)
