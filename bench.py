@@ -2,19 +2,22 @@
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl ours|reference]
 
-One step is one kda_prefill call (chunk preparation + recurrence, and the
-varlen metadata kernel for packed input) over one batch of synthetic input
-already resident in HBM.  The default workload is B=1, H=6, T=8192, d=128
-("FlashKDA column split", section 4: the small-head tensor-parallel shard at
-8,192 tokens); a secondary line item times B=1, H=96, T=8192 the same way.
-Between timed steps a 512 MiB buffer is written to flush the 129 MB L2.
+One step is one kda_prefill call (all of its kernels) over one batch of
+synthetic input already resident in HBM; by default the timed steps replay
+the call captured once in a CUDA graph (`--graph 0`: eager calls; the eager
+time is reported beside it either way).  The default workload is B=1, H=6,
+T=8192, d=128 ("FlashKDA column split", section 4: the small-head
+tensor-parallel shard at 8,192 tokens); a secondary line item times B=1,
+H=96, T=8192 the same way.  Between timed steps a 512 MiB buffer is written
+to flush the 129 MB L2.
 
 Reported: `value` = head-tokens/s over the timed steps (device time, CUDA
 events on the launching stream); `e2e` = the same metric with the inputs
 copied host->device from pinned memory and the outputs copied back inside
-every timed step; `roofline` for the dominant kernel (events recorded by the
-library around its kernels during the timed steps); `cpu_baseline` = the FP64
-oracle timed on this host's cores.  `--impl reference` times that oracle
+every timed step (eager calls); `roofline` for the dominant kernel (events
+recorded by the library between its kernels in a separate pass of eager
+calls) and `roofline.critical_path` (HBM, tensor and serial-chain bounds of
+the call); `cpu_baseline` = the FP64 oracle timed on this host's cores.  `--impl reference` times that oracle
 alone on a bounded sample of the same workload (the pages name no runnable
 reference implementation).  Under torchrun every rank runs its own replica of
 the workload on its own GPU (weak scaling, no collective in the data path).
@@ -168,8 +171,10 @@ def head_tokens(inp):
     return int(inp["q"].shape[0] * inp["q"].shape[1] * inp["q"].shape[2])
 
 
-def time_kernel_steps(kda, d, steps, warmup, flush, stream, profile=False):
-    """Device time of `steps` kda_prefill calls (L2 flushed before each)."""
+def time_kernel_steps(kda, d, steps, warmup, flush, stream, profile=False, graph=False):
+    """Device time of `steps` kda_prefill calls (L2 flushed before each).
+    With `graph`, the call is captured once into a CUDA graph after the
+    warm-up and every step replays it (the flush stays outside the graph)."""
     out = torch.empty_like(d["v"])
     N = d["init_state"].shape[0] if d["init_state"] is not None else d["q"].shape[0]
     if d["cu_seqlens"] is not None:
@@ -177,15 +182,22 @@ def time_kernel_steps(kda, d, steps, warmup, flush, stream, profile=False):
     H = d["q"].shape[2]
     fin = torch.empty((N, H, 128, 128), dtype=torch.bfloat16, device=d["q"].device)
 
-    def call():
+    def eager():
         kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
                         cu_seqlens=d["cu_seqlens"], out=out, final_state=fin, stream=stream)
 
+    call = eager
     with torch.cuda.stream(stream):
         for _ in range(warmup):
             flush.zero_()
-            call()
+            eager()
         stream.synchronize()
+        if graph:
+            g = torch.cuda.CUDAGraph()
+            with torch.cuda.graph(g, stream=stream):
+                eager()
+            stream.synchronize()
+            call = g.replay
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         if profile:
@@ -333,11 +345,14 @@ def measured_tensor_peak():
 FLOP_PER_HT = (3 * 2 * 128 * 128 * 16 + 2 * 65536 + 2 * 65536 + 49152) / 16
 
 
-def critical_path(kda, inp, ht, state_io, us_per_call):
+def critical_path(kda, inp, ht, state_io, us_per_call, segs):
     """Bounds on the call: HBM (the path's algorithmic bytes at the measured
     copy bandwidth), tensor (its FLOPs at the measured BF16 rate) and the
     serial chain (the longest sequence's chunk steps times the measured
-    shortest dependent chunk-step chain); `frac` = the largest over the time."""
+    shortest dependent chunk-step chain); `frac` = the largest over the time.
+    A segmented call is not a serial walk: its own chain bound is the two
+    walks of one segment's L chunks (`plan_*`), which the serial bound can
+    exceed."""
     t_step = kda._lib.chain_step_ns()
     if inp["cu_seqlens"] is None:
         steps = int(math.ceil(inp["q"].shape[1] / 16))
@@ -351,9 +366,22 @@ def critical_path(kda, inp, ht, state_io, us_per_call):
     chain_us = steps * t_step / 1e3
     bound = max(hbm_us, tensor_us, chain_us)
     kind = "chain" if bound == chain_us else ("hbm" if bound == hbm_us else "tensor")
-    return {"t_step_ns": t_step, "chain_steps": steps, "chain_bound_us": chain_us,
-            "hbm_bound_us": hbm_us, "tensor_bound_us": tensor_us, "tensor_peak_kind": tkind,
-            "bound_us": bound, "bound": kind, "frac": bound / us_per_call}
+    res = {"t_step_ns": t_step, "chain_steps": steps, "chain_bound_us": chain_us,
+           "hbm_bound_us": hbm_us, "tensor_bound_us": tensor_us, "tensor_peak_kind": tkind,
+           "bound_us": bound, "bound": kind, "frac": bound / us_per_call,
+           "plan": "segmented" if segs else "serial"}
+    if segs:
+        if inp["cu_seqlens"] is None:
+            L = int(math.ceil(steps / segs))
+        else:   # the planner's segment length from its bound on all segments
+            n = inp["cu_seqlens"].numel() - 1
+            c_ub = (inp["q"].shape[1] + 15 * n) // 16
+            L = int(math.ceil(c_ub / max(segs - n, 1)))
+        plan_chain = 2 * L * t_step / 1e3
+        plan_bound = max(hbm_us, tensor_us, plan_chain)
+        res.update({"plan_segment_chunks": L, "plan_chain_bound_us": plan_chain,
+                    "plan_bound_us": plan_bound, "plan_frac": plan_bound / us_per_call})
+    return res
 
 
 def run_ours(args):
@@ -393,11 +421,15 @@ def run_ours(args):
     gpu_index = cvd[device.index] if device.index < len(cvd) else str(device.index)
     prof_steps = max(10, args.steps // 4)
     with ClockSampler(gpu_index) as clk:
-        # The headline steps run without the library's profile events (an
-        # event between each pair of kernels adds a few microseconds per
-        # call); a second, shorter pass records them for the per-kernel split.
-        ms, _ = time_kernel_steps(kda, d, args.steps, args.warmup, flush, stream, profile=False)
+        # The headline steps replay the call captured in a CUDA graph (with
+        # --graph 1) and run without the library's profile events (an event
+        # between each pair of kernels adds a few microseconds per call); a
+        # second, shorter pass of eager calls records them for the per-kernel
+        # split, and a third times eager calls without them.
+        ms, _ = time_kernel_steps(kda, d, args.steps, args.warmup, flush, stream,
+                                  graph=bool(args.graph))
         _, prof = time_kernel_steps(kda, d, prof_steps, 3, flush, stream, profile=True)
+        eager_ms, _ = time_kernel_steps(kda, d, prof_steps, 3, flush, stream)
         e2e_ms, h2d, d2h = time_e2e_steps(kda, inp, args.steps, min(args.warmup, 3), flush, stream,
                                           device)
     torch.cuda.synchronize(device)
@@ -450,7 +482,8 @@ def run_ours(args):
         roofline.update({"prep_us": 1e3 * prep_avg, "recurrence_us": 1e3 * rec_avg})
     if segs:
         roofline.update({"transition_us": 1e3 * trans_avg, "segment_chain_us": 1e3 * chain_avg})
-    roofline["critical_path"] = critical_path(kda, inp, ht, state_io, 1e3 * total_ms / args.steps)
+    roofline["critical_path"] = critical_path(kda, inp, ht, state_io, 1e3 * total_ms / args.steps,
+                                              segs)
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -463,7 +496,9 @@ def run_ours(args):
                    "one_launch": fused, "long_sequences_at_split_2": long_split,
                    "segments_per_sequence": segs, "head_tokens_per_step": ht,
                    "kernel_times": "per-kernel split from a separate pass of %d steps with library "
-                                   "events between the kernels" % prof_steps},
+                                   "events between the kernels" % prof_steps,
+                   "cuda_graph": bool(args.graph)},
+        "eager_us_per_call": 1e3 * sum(eager_ms) / len(eager_ms),
         "gpu_launches": (1 if fused else 4 if segs else
                          (3 + (1 if long_split else 0) if packed else 2)) * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
@@ -480,7 +515,8 @@ def run_ours(args):
     if not args.no_secondary and args.workload != "t8192_h96":
         sec = synthetic.make_workload("t8192_h96")
         ds = device_inputs(sec, device)
-        ms2, _ = time_kernel_steps(kda, ds, max(10, args.steps // 10), 3, flush, stream)
+        ms2, _ = time_kernel_steps(kda, ds, max(10, args.steps // 10), 3, flush, stream,
+                                   graph=bool(args.graph))
         _, prof2 = time_kernel_steps(kda, ds, 10, 3, flush, stream, profile=True)
         ht2 = head_tokens(sec)
         t2 = sum(ms2) / len(ms2)
@@ -517,6 +553,8 @@ def main():
                     help="recurrence engine: 0 automatic, 1 column-split warp MMA, 2 tcgen05")
     ap.add_argument("--fusion", type=int, default=1, choices=[0, 1],
                     help="allow preparation and recurrence as one launch (kda_set_fusion)")
+    ap.add_argument("--graph", type=int, default=1, choices=[0, 1],
+                    help="time replays of the call captured in a CUDA graph (eager calls with 0)")
     ap.add_argument("--segments", type=int, default=1, choices=[0, 1],
                     help="allow the segmented scan over chunks (kda_set_segments)")
     args = ap.parse_args()
