@@ -134,9 +134,12 @@ int kda_set_engine(int engine);
  *                         [cu_starts[n], cu_starts[n + 1]) or [0, checkpoint_rows)
  *                         is not written and sets KDA_DEV_BAD_CHECKPOINTS.
  *
- * Everything else, including results and errors, is as kda_prefill; in
- * addition KDA_ERR_ARG for an interval that is not a positive multiple of 16
- * or negative checkpoint_rows, KDA_ERR_NULL for NULL checkpoint pointers.
+ * Everything else, including results and errors, is as kda_prefill (a call
+ * that takes the segmented scan, kda_set_segments, writes the checkpoints
+ * from its last pass: those at segment starts are the segments' BF16
+ * incoming states); in addition KDA_ERR_ARG for an interval that is not a
+ * positive multiple of 16 or negative checkpoint_rows, KDA_ERR_NULL for NULL
+ * checkpoint pointers.
  * Under engine 2 (kda_set_engine) such calls run on the column-split kernels.
  */
 int kda_prefill_checkpointed(const void* q, const void* k, const void* v, const float* g,
@@ -182,7 +185,8 @@ int kda_plan_long_split(int64_t n_seqs, int64_t T, int64_t H, int64_t* k);
  * of chunks it is S -> S F + Z ("Kimi Linear" technical report, chunkwise
  * KDA: S_{c+1} = S_c D_c + U_c K^end_c with U_c affine in S_c).  When there
  * are too few (sequence, head) chains to fill the GPU (engine 0, automatic
- * split, no checkpoints; fixed or packed layout), each sequence is cut into
+ * split; fixed or packed layout; with or without checkpoints, which the last
+ * pass writes), each sequence is cut into
  * segments: one launch forms every segment's F and Z, a short chain over the
  * segments forms each segment's incoming state, and one launch reruns every
  * segment from its incoming state and writes O.  The results agree with the

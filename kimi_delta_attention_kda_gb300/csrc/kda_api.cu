@@ -215,7 +215,8 @@ int64_t align256(int64_t b) { return ((b + 255) / 256) * 256; }
 
 SegChoice plan_segments(const Plan& pl, int64_t H, int sms, bool checkpoints) {
     SegChoice sc;
-    if (!g_segments || g_engine != 0 || g_split_override || checkpoints || pl.tokens <= 0) return sc;
+    if (!g_segments || g_engine != 0 || g_split_override || pl.tokens <= 0) return sc;
+    (void)checkpoints;   // the rerun writes them (per-sequence numbering)
     const int64_t units = pl.N * H;
     const double t_serial = serial_chunk_us(choose_split(units, sms));
     if (pl.packed) {
@@ -235,7 +236,7 @@ SegChoice plan_segments(const Plan& pl, int64_t H, int sms, bool checkpoints) {
         sc.seg_chunks = L;
         sc.segs = C / L + N;
         sc.total = sc.segs;
-        sc.meta_bytes = align256(8 * (N + 1)) + 2 * align256(8 * (sc.segs + 1));
+        sc.meta_bytes = align256(8 * (N + 1)) + 2 * align256(8 * (sc.segs + 1)) + align256(8 * sc.segs);
     } else {
         const int64_t chunks = pl.geo.chunks_per_seq;
         int64_t L = g_seg_chunks;
@@ -418,15 +419,18 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
             seg_begin = reinterpret_cast<int64_t*>(starts + sc.state_bytes);
             int64_t* seg_chunk0 = seg_begin + align256(8 * (pl.N + 1)) / 8;
             int64_t* seg_tok0 = seg_chunk0 + align256(8 * (sc.segs + 1)) / 8;
+            int64_t* seg_seq = seg_tok0 + align256(8 * (sc.segs + 1)) / 8;
             if (rc == KDA_OK &&
                 launch_segment_meta(cu_seqlens, geo.cu_chunks, const_cast<int32_t*>(geo.valid), pl.N,
-                                    sc.seg_chunks, sc.segs, seg_begin, seg_chunk0, seg_tok0,
+                                    sc.seg_chunks, sc.segs, seg_begin, seg_chunk0, seg_tok0, seg_seq,
                                     d->status, stream) != cudaSuccess)
                 rc = KDA_ERR_CUDA;
             sg.n_seqs = sc.segs;
             sg.cu_seqlens = seg_tok0;
             sg.cu_chunks = seg_chunk0;
             sg.order = nullptr;
+            sg.seg_seq = seg_seq;
+            sg.seq_chunks = geo.cu_chunks;
         } else {
             sg.n_seqs = pl.N * sc.segs;
             sg.seg_chunks = sc.seg_chunks;
@@ -444,7 +448,7 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
             rc = KDA_ERR_CUDA;
         prof_record(3, stream);
         if (rc == KDA_OK &&
-            launch_recurrence(v, out, starts, nullptr, packets, sg, H, 1, d->status, stream) !=
+            launch_recurrence(v, out, starts, nullptr, packets, sg, H, 1, d->status, stream, ck) !=
                 cudaSuccess)
             rc = KDA_ERR_CUDA;
         done = true;

@@ -32,6 +32,11 @@ struct SeqGeometry {
     // recurrence is segment n % segs_per_seq of sequence n / segs_per_seq.
     int64_t seg_chunks;
     int64_t segs_per_seq;
+    // Packed layout cut into segments (the segment table is cu_seqlens /
+    // cu_chunks): the sequence of each segment and each sequence's first
+    // chunk, for per-sequence checkpoint numbering.  Null otherwise.
+    const int64_t* seg_seq;
+    const int64_t* seq_chunks;
     int* status;                 // device status word (set by the launchers)
 };
 
@@ -85,12 +90,13 @@ cudaError_t launch_segment_scan(const void* init_state, void* final_state, const
 
 // Segments of a packed batch of n_seqs sequences (after launch_varlen_meta):
 // ceil(chunks / seg_chunks_len) per sequence, at most s_ub in all; writes
-// seg_begin [n_seqs + 1] and, per segment, its first chunk and first token
-// ([s_ub + 1] each, padded with the batch's end).
+// seg_begin [n_seqs + 1], per segment its first chunk and first token
+// ([s_ub + 1] each, padded with the batch's end) and its sequence
+// (seg_seq [s_ub], 0 for padding).
 cudaError_t launch_segment_meta(const int64_t* cu_seqlens, const int64_t* cu_chunks, int32_t* valid,
                                 int64_t n_seqs, int64_t seg_chunks_len, int64_t s_ub,
                                 int64_t* seg_begin, int64_t* seg_chunks, int64_t* seg_tokens,
-                                int* status, cudaStream_t stream);
+                                int64_t* seg_seq, int* status, cudaStream_t stream);
 
 // The tcgen05 recurrence: one CTA per (sequence, head).
 cudaError_t launch_recurrence_tc(const void* v, void* out, const void* init_state,

@@ -541,11 +541,24 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
         }
 
     bool ok = true;
-    int64_t ck_next = 0;   // next chunk whose incoming state is a checkpoint
+    // Checkpoints are numbered per sequence: a segment's chunks start at
+    // chunk c_off of sequence n_ck.
+    int64_t n_ck = n, c_off = 0;
+    if (kCkpt) {
+        if (a.geo.seg_chunks) {
+            n_ck = n / a.geo.segs_per_seq;
+            c_off = (n - n_ck * a.geo.segs_per_seq) * a.geo.seg_chunks;
+        } else if (a.geo.seg_seq) {
+            n_ck = a.geo.seg_seq[n];
+            c_off = c_begin - a.geo.seq_chunks[n_ck];
+        }
+    }
+    // next chunk whose incoming state is a checkpoint
+    int64_t ck_next = kCkpt ? ((c_off + a.ck.every - 1) / a.ck.every) * a.ck.every - c_off : 0;
     for (int64_t c = 0; c < nch; ++c) {
         if (kCkpt && c == ck_next) {
             ck_next += a.ck.every;
-            __nv_bfloat16* dst = checkpoint_dst(a, n, h, c / a.ck.every);
+            __nv_bfloat16* dst = checkpoint_dst(a, n_ck, h, (c_off + c) / a.ck.every);
             if (dst) quad_store_state(dst, Sf, vcol, g8, t4);
         }
         const int s = static_cast<int>(c % kQuadStages);

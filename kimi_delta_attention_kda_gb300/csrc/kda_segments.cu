@@ -251,7 +251,7 @@ constexpr int kSegMetaThreads = 1024;
 __global__ void __launch_bounds__(kSegMetaThreads)
     segment_meta_kernel(const int64_t* cu, const int64_t* cu_chunks, int32_t* valid, int64_t N,
                         int64_t L, int64_t s_ub, int64_t* seg_begin, int64_t* seg_chunks,
-                        int64_t* seg_tokens, int* status) {
+                        int64_t* seg_tokens, int64_t* seg_seq, int* status) {
     __shared__ int64_t warp_sums[kSegMetaThreads / 32];
     __shared__ int64_t carry;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -289,6 +289,7 @@ __global__ void __launch_bounds__(kSegMetaThreads)
             for (int64_t j = 0; j < cnt && s0 + j < s_ub; ++j) {
                 seg_chunks[s0 + j] = cu_chunks[n] + j * L;
                 seg_tokens[s0 + j] = cu[n] + kChunk * j * L;
+                seg_seq[s0 + j] = n;
             }
         }
         __syncthreads();
@@ -306,6 +307,7 @@ __global__ void __launch_bounds__(kSegMetaThreads)
     for (int64_t sidx = total + tid; sidx <= s_ub; sidx += kSegMetaThreads) {
         seg_chunks[sidx] = cu_chunks[N];
         seg_tokens[sidx] = cu[N];
+        if (sidx < s_ub) seg_seq[sidx] = 0;
     }
 }
 
@@ -351,11 +353,11 @@ cudaError_t launch_segment_scan(const void* init_state, void* final_state, const
 cudaError_t launch_segment_meta(const int64_t* cu_seqlens, const int64_t* cu_chunks, int32_t* valid,
                                 int64_t n_seqs, int64_t seg_chunks_len, int64_t s_ub,
                                 int64_t* seg_begin, int64_t* seg_chunks, int64_t* seg_tokens,
-                                int* status, cudaStream_t stream) {
+                                int64_t* seg_seq, int* status, cudaStream_t stream) {
     if (n_seqs <= 0 || seg_chunks_len <= 0) return cudaErrorInvalidValue;
     segment_meta_kernel<<<1, kSegMetaThreads, 0, stream>>>(cu_seqlens, cu_chunks, valid, n_seqs,
                                                           seg_chunks_len, s_ub, seg_begin,
-                                                          seg_chunks, seg_tokens, status);
+                                                          seg_chunks, seg_tokens, seg_seq, status);
     return cudaGetLastError();
 }
 

@@ -214,3 +214,74 @@ def test_packed_plan_against_oracle(kda):
         tu.assert_within_tolerance(fin[n].double().numpy(), fin_s[n].double().numpy(), 0,
                                    "segmented vs serial S")
     tu.check_against_oracle(inp, out, fin)
+
+
+# ----------------------------------------------------------------------------
+# Native checkpoints on the segmented path (the rerun writes them)
+# ----------------------------------------------------------------------------
+
+def _ck_starts(lengths, every):
+    rows = [(n + every - 1) // every for n in lengths]
+    out = [0]
+    for r in rows:
+        out.append(out[-1] + r)
+    return out
+
+
+def _ck_call(kda, inp, every, starts):
+    d = tu.to_device(inp)
+    H = inp["q"].shape[2]
+    ck = torch.full((starts[-1], H, 128, 128), 5.0, dtype=torch.bfloat16, device="cuda")
+    cu = torch.tensor(starts, dtype=torch.int64, device="cuda")
+    out, fin, ck = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                                   cu_seqlens=d["cu_seqlens"], checkpoint_every_n_tokens=every,
+                                   state_checkpoints=ck, checkpoint_cu_starts=cu)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    return out.cpu(), fin.cpu(), ck.cpu()
+
+
+def _check_rows(inp, lengths, every, starts, ck):
+    import oracle
+    cu = [0]
+    for n in lengths:
+        cu.append(cu[-1] + n)
+    packed = inp["cu_seqlens"] is not None
+    for n in range(len(lengths)):
+        for j in range(starts[n + 1] - starts[n]):
+            row = ck[starts[n] + j].double().numpy()
+            if j == 0:
+                assert torch.equal(ck[starts[n]], inp["init_state"][n])
+                continue
+            if packed:
+                sl = slice(cu[n], cu[n] + j * every)
+                args = [inp[k][:, sl] for k in ("q", "k", "v", "g", "beta")]
+            else:
+                args = [inp[k][n:n + 1, :j * every] for k in ("q", "k", "v", "g", "beta")]
+            _, st = oracle.kda_token(*args, inp["init_state"][n:n + 1])
+            tu.assert_within_tolerance(row, st[0], 0, "checkpoint seq %d row %d" % (n, j))
+
+
+@pytest.mark.parametrize("every", [32, 48, 64])
+def test_forced_checkpoints_fixed(forced, every):
+    """Segments of 4 chunks (64 tokens); intervals of 2, 3 and 4 chunks, so
+    checkpoints fall inside segments, on their boundaries and across them."""
+    forced.set_segments(True, 4)
+    inp = synthetic.make_inputs(2, 300, 3, 7600 + every, init_std=0.02)
+    starts = _ck_starts([300, 300], every)
+    out, fin, ck = _ck_call(forced, inp, every, starts)
+    plain = run(forced, inp)
+    assert torch.equal(out, plain[0]) and torch.equal(fin, plain[1])
+    _check_rows(inp, [300, 300], every, starts, ck)
+    assert forced.plan_segments(2, 300, 3, False) == 5
+
+
+def test_forced_checkpoints_packed(forced):
+    forced.set_segments(True, 3)
+    every = 32
+    inp = synthetic.make_inputs(0, 0, 2, 7700, init_std=0.02, lengths=LENGTHS)
+    starts = _ck_starts(LENGTHS, every)
+    out, fin, ck = _ck_call(forced, inp, every, starts)
+    plain = run(forced, inp)
+    assert torch.equal(out, plain[0]) and torch.equal(fin, plain[1])
+    _check_rows(inp, LENGTHS, every, starts, ck)
