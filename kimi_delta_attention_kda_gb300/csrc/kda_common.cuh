@@ -255,6 +255,26 @@ __device__ __forceinline__ bool pair_all(int id, bool p) {
         : "memory");
     return r != 0;
 }
+// (a, b) <- (a d, b d) as one packed FP32x2 multiply (sm_100 and later;
+// each lane rounds as a scalar multiply does, so results are bitwise those
+// of two multiplies).
+__device__ __forceinline__ void mul2(float& a, float& b, float d) {
+    uint64_t x, y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %1};" : "=l"(y) : "f"(d));
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(y));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+
+// (a, b) <- (a + c, b + d) as one packed FP32x2 add (bitwise two adds).
+__device__ __forceinline__ void add2(float& a, float& b, float c, float d) {
+    uint64_t x, y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(c), "f"(d));
+    asm("add.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(y));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+
 // The same for a group of kThreads threads (a multiple of 32) on barrier `id`.
 template <int kThreads>
 __device__ __forceinline__ bool group_all(int id, bool p) {

@@ -357,10 +357,8 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
         for (int i = 0; i < 4; ++i) {
             const float d0 = dsel(f.d[i >> 1], 2 * (i & 1));
             const float d1 = dsel(f.d[i >> 1], 2 * (i & 1) + 1);
-            Sf[i][0] *= d0;
-            Sf[i][1] *= d0;
-            Sf[i][2] *= d1;
-            Sf[i][3] *= d1;
+            mul2(Sf[i][0], Sf[i][1], d0);
+            mul2(Sf[i][2], Sf[i][3], d1);
         }
         // The K' and Q^start fragments are dead: load the next chunk's.
         if (has_next) {

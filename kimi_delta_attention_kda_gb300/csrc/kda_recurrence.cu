@@ -143,10 +143,8 @@ __device__ __forceinline__ void chunk_step(const ChunkFrags& f, float (&Sf)[8][4
     for (int mt = 0; mt < 8; ++mt) {
         const float d0 = dsel(f.d[mt >> 1], 2 * (mt & 1));
         const float d1 = dsel(f.d[mt >> 1], 2 * (mt & 1) + 1);
-        Sf[mt][0] *= d0;
-        Sf[mt][1] *= d0;
-        Sf[mt][2] *= d1;
-        Sf[mt][3] *= d1;
+        mul2(Sf[mt][0], Sf[mt][1], d0);
+        mul2(Sf[mt][2], Sf[mt][3], d1);
     }
     uint32_t Ub[2];
     Ub[0] = movm_t(pack_bf16(u0[0] + u1[0], u0[1] + u1[1]));
@@ -326,10 +324,8 @@ __global__ void __launch_bounds__((NW + 1) * 32)
             for (int mt = 0; mt < 8; ++mt) {
                 const float d0 = dsel(f.d[mt >> 1], 2 * (mt & 1));
                 const float d1 = dsel(f.d[mt >> 1], 2 * (mt & 1) + 1);
-                Sf[mt][0] *= d0;
-                Sf[mt][1] *= d0;
-                Sf[mt][2] *= d1;
-                Sf[mt][3] *= d1;
+                mul2(Sf[mt][0], Sf[mt][1], d0);
+                mul2(Sf[mt][2], Sf[mt][3], d1);
             }
             if (has_next) {
                 if (!__all_sync(0xffffffffu, next_ready))
@@ -619,22 +615,20 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
                 const float4 d = dp[j];
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
-                    Sf[2 * j][nt][0] *= d.x;
-                    Sf[2 * j][nt][1] *= d.x;
-                    Sf[2 * j][nt][2] *= d.y;
-                    Sf[2 * j][nt][3] *= d.y;
-                    Sf[2 * j + 1][nt][0] *= d.z;
-                    Sf[2 * j + 1][nt][1] *= d.z;
-                    Sf[2 * j + 1][nt][2] *= d.w;
-                    Sf[2 * j + 1][nt][3] *= d.w;
+                    mul2(Sf[2 * j][nt][0], Sf[2 * j][nt][1], d.x);
+                    mul2(Sf[2 * j][nt][2], Sf[2 * j][nt][3], d.y);
+                    mul2(Sf[2 * j + 1][nt][0], Sf[2 * j + 1][nt][1], d.z);
+                    mul2(Sf[2 * j + 1][nt][2], Sf[2 * j + 1][nt][3], d.w);
                 }
             }
         }
         uint32_t Ub[4][2];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-            Ub[nt][0] = movm_t(pack_bf16(u[0][nt][0] + u[1][nt][0], u[0][nt][1] + u[1][nt][1]));
-            Ub[nt][1] = movm_t(pack_bf16(u[0][nt][2] + u[1][nt][2], u[0][nt][3] + u[1][nt][3]));
+            add2(u[0][nt][0], u[0][nt][1], u[1][nt][0], u[1][nt][1]);
+            add2(u[0][nt][2], u[0][nt][3], u[1][nt][2], u[1][nt][3]);
+            Ub[nt][0] = movm_t(pack_bf16(u[0][nt][0], u[0][nt][1]));
+            Ub[nt][1] = movm_t(pack_bf16(u[0][nt][2], u[0][nt][3]));
         }
         // S^T <- D S^T + (K^end)^T U^T.
 #pragma unroll
@@ -651,9 +645,9 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
             ldsm_x4(aq, smem_u32(stage + kOffAQK + sw32_off(rowA, hiA)));
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) {
-                float pin[4] = {p[0][nt][0] + p[1][nt][0], p[0][nt][1] + p[1][nt][1],
-                                p[0][nt][2] + p[1][nt][2], p[0][nt][3] + p[1][nt][3]};
-                mma_bf16(o[nt], aq, Ub[nt], pin);
+                add2(p[0][nt][0], p[0][nt][1], p[1][nt][0], p[1][nt][1]);
+                add2(p[0][nt][2], p[0][nt][3], p[1][nt][2], p[1][nt][3]);
+                mma_bf16(o[nt], aq, Ub[nt], p[0][nt]);
             }
         }
         __syncwarp();
@@ -817,22 +811,20 @@ __global__ void __launch_bounds__(kTransWarps * 32, 1)
                 const float4 d = dp[j];
 #pragma unroll
                 for (int nt = 0; nt < 4; ++nt) {
-                    Sf[2 * j][nt][0] *= d.x;
-                    Sf[2 * j][nt][1] *= d.x;
-                    Sf[2 * j][nt][2] *= d.y;
-                    Sf[2 * j][nt][3] *= d.y;
-                    Sf[2 * j + 1][nt][0] *= d.z;
-                    Sf[2 * j + 1][nt][1] *= d.z;
-                    Sf[2 * j + 1][nt][2] *= d.w;
-                    Sf[2 * j + 1][nt][3] *= d.w;
+                    mul2(Sf[2 * j][nt][0], Sf[2 * j][nt][1], d.x);
+                    mul2(Sf[2 * j][nt][2], Sf[2 * j][nt][3], d.y);
+                    mul2(Sf[2 * j + 1][nt][0], Sf[2 * j + 1][nt][1], d.z);
+                    mul2(Sf[2 * j + 1][nt][2], Sf[2 * j + 1][nt][3], d.w);
                 }
             }
         }
         uint32_t Ub[4][2];
 #pragma unroll
         for (int nt = 0; nt < 4; ++nt) {
-            Ub[nt][0] = movm_t(pack_bf16(u[0][nt][0] + u[1][nt][0], u[0][nt][1] + u[1][nt][1]));
-            Ub[nt][1] = movm_t(pack_bf16(u[0][nt][2] + u[1][nt][2], u[0][nt][3] + u[1][nt][3]));
+            add2(u[0][nt][0], u[0][nt][1], u[1][nt][0], u[1][nt][1]);
+            add2(u[0][nt][2], u[0][nt][3], u[1][nt][2], u[1][nt][3]);
+            Ub[nt][0] = movm_t(pack_bf16(u[0][nt][0], u[0][nt][1]));
+            Ub[nt][1] = movm_t(pack_bf16(u[0][nt][2], u[0][nt][3]));
         }
         // S^T <- D S^T + (K^end)^T U^T.
 #pragma unroll
