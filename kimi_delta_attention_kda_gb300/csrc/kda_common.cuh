@@ -275,6 +275,23 @@ __device__ __forceinline__ void add2(float& a, float& b, float c, float d) {
     asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
 }
 
+// (a, b) <- (a c, b d) and (a, b) <- (a - c, b - d), packed FP32x2 (each
+// lane rounds as the scalar instruction does).
+__device__ __forceinline__ void mul2v(float& a, float& b, float c, float d) {
+    uint64_t x, y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(c), "f"(d));
+    asm("mul.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(y));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+__device__ __forceinline__ void sub2(float& a, float& b, float c, float d) {
+    uint64_t x, y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(a), "f"(b));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(c), "f"(d));
+    asm("sub.rn.f32x2 %0, %0, %1;" : "+l"(x) : "l"(y));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(a), "=f"(b) : "l"(x));
+}
+
 // The same for a group of kThreads threads (a multiple of 32) on barrier `id`.
 template <int kThreads>
 __device__ __forceinline__ bool group_all(int id, bool p) {

@@ -96,8 +96,10 @@ __device__ __forceinline__ void st_row4_split(uint8_t* hi, uint8_t* lo, int t, i
                                               float b, float c, float d) {
     const uint32_t off = row4_off(t, lane);
     const uint32_t h0 = pack_bf16(a, b), h1 = pack_bf16(c, d);
-    const uint32_t l0 = pack_bf16(a - bf16_lo(h0), b - bf16_hi(h0));
-    const uint32_t l1 = pack_bf16(c - bf16_lo(h1), d - bf16_hi(h1));
+    sub2(a, b, bf16_lo(h0), bf16_hi(h0));
+    sub2(c, d, bf16_lo(h1), bf16_hi(h1));
+    const uint32_t l0 = pack_bf16(a, b);
+    const uint32_t l1 = pack_bf16(c, d);
     *reinterpret_cast<uint2*>(hi + off) = make_uint2(h0, h1);
     *reinterpret_cast<uint2*>(lo + off) = make_uint2(l0, l1);
 }
@@ -239,19 +241,37 @@ __device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, floa
         const int t = tb + j;
         const float rq = __shfl_sync(0xffffffffu, rnorm_q, j);
         const float rk = __shfl_sync(0xffffffffu, rnorm, 8 + j);
-        const float kh0 = bf16_lo(kv[j].x) * rk, kh1 = bf16_hi(kv[j].x) * rk;
-        const float kh2 = bf16_lo(kv[j].y) * rk, kh3 = bf16_hi(kv[j].y) * rk;
-        const float qh0 = bf16_lo(qv[j].x) * rq, qh1 = bf16_hi(qv[j].x) * rq;
-        const float qh2 = bf16_lo(qv[j].y) * rq, qh3 = bf16_hi(qv[j].y) * rq;
+        // The products below in packed pairs (bitwise the scalar products).
+        float kh0 = bf16_lo(kv[j].x), kh1 = bf16_hi(kv[j].x);
+        float kh2 = bf16_lo(kv[j].y), kh3 = bf16_hi(kv[j].y);
+        float qh0 = bf16_lo(qv[j].x), qh1 = bf16_hi(qv[j].x);
+        float qh2 = bf16_lo(qv[j].y), qh3 = bf16_hi(qv[j].y);
+        mul2(kh0, kh1, rk);
+        mul2(kh2, kh3, rk);
+        mul2(qh0, qh1, rq);
+        mul2(qh2, qh3, rq);
         const float e0 = ex2_approx(G[j][0]), e1 = ex2_approx(G[j][1]);
         const float e2 = ex2_approx(G[j][2]), e3 = ex2_approx(G[j][3]);
         const float i0 = ex2_approx(-G[j][0]), i1 = ex2_approx(-G[j][1]);
         const float i2 = ex2_approx(-G[j][2]), i3 = ex2_approx(-G[j][3]);
-        st_row4_split(tKS, tKsLo, t, lane, e0 * kh0, e1 * kh1, e2 * kh2, e3 * kh3);
-        st_row4_split(tQS, tQsLo, t, lane, e0 * qh0, e1 * qh1, e2 * qh2, e3 * qh3);
-        st_row4_split(tKinv, tKinvLo, t, lane, i0 * kh0, i1 * kh1, i2 * kh2, i3 * kh3);
-        st_row4(tKen, t, lane, (e_last0 * i0) * kh0, (e_last1 * i1) * kh1, (e_last2 * i2) * kh2,
-                (e_last3 * i3) * kh3);
+        float ks0 = e0, ks1 = e1, ks2 = e2, ks3 = e3;       // K^start
+        float qs0 = e0, qs1 = e1, qs2 = e2, qs3 = e3;       // s Q^start
+        float kv0 = i0, kv1 = i1, kv2 = i2, kv3 = i3;       // exp(-G) khat
+        float ke0 = e_last0, ke1 = e_last1, ke2 = e_last2, ke3 = e_last3;   // K^end rows
+        mul2v(ks0, ks1, kh0, kh1);
+        mul2v(ks2, ks3, kh2, kh3);
+        mul2v(qs0, qs1, qh0, qh1);
+        mul2v(qs2, qs3, qh2, qh3);
+        mul2v(kv0, kv1, kh0, kh1);
+        mul2v(kv2, kv3, kh2, kh3);
+        mul2v(ke0, ke1, i0, i1);
+        mul2v(ke2, ke3, i2, i3);
+        mul2v(ke0, ke1, kh0, kh1);
+        mul2v(ke2, ke3, kh2, kh3);
+        st_row4_split(tKS, tKsLo, t, lane, ks0, ks1, ks2, ks3);
+        st_row4_split(tQS, tQsLo, t, lane, qs0, qs1, qs2, qs3);
+        st_row4_split(tKinv, tKinvLo, t, lane, kv0, kv1, kv2, kv3);
+        st_row4(tKen, t, lane, ke0, ke1, ke2, ke3);
     }
     // Every operand tile is complete.
     pair_sync(bid);
