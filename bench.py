@@ -320,6 +320,22 @@ def run_reference(args):
     print(json.dumps(line), flush=True)
 
 
+def max_over_ranks(values, device):
+    """Each value's maximum over the ranks of the default process group (the
+    values themselves with one process): the slowest replica sets the time."""
+    import torch.distributed as dist
+    if not (dist.is_available() and dist.is_initialized()) or dist.get_world_size() == 1:
+        return [float(v) for v in values]
+    t = torch.tensor([float(v) for v in values], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return [float(x) for x in t]
+
+
+def job_throughput(world_size, units_per_rank, steps, total_ms):
+    """Whole-job rate: every rank's units over the slowest rank's time."""
+    return world_size * units_per_rank * steps / (total_ms * 1e-3)
+
+
 def measured_peaks():
     path = os.path.join(ROOT, "MEASURED_PEAKS.json")
     try:
@@ -439,14 +455,9 @@ def run_ours(args):
     if status != 0:
         raise RuntimeError("device status %d during the benchmark" % status)
 
-    total_ms = sum(ms)
-    total_e2e = sum(e2e_ms)
-    if ws > 1:
-        t = torch.tensor([total_ms, total_e2e], dtype=torch.float64, device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        total_ms, total_e2e = float(t[0]), float(t[1])
-    value = ws * ht * args.steps / (total_ms * 1e-3)
-    e2e_value = ws * ht * args.steps / (total_e2e * 1e-3)
+    total_ms, total_e2e = max_over_ranks([sum(ms), sum(e2e_ms)], device)
+    value = job_throughput(ws, ht, args.steps, total_ms)
+    e2e_value = job_throughput(ws, ht, args.steps, total_e2e)
 
     intervals, calls = prof
     prep_avg, trans_avg, chain_avg, rec_avg = (t / calls for t in intervals)
