@@ -202,6 +202,11 @@ constexpr double kTransChunkUs = 1.25;
 constexpr double kQuadChunkUs = 1.0;
 constexpr double kScanStepUs = 0.6;
 constexpr double kSegFixedUs = 12.0;
+// From this many segments per sequence (fixed layout) the chain over them
+// runs in two levels: groups of about sqrt(segments), composed in parallel,
+// then a chain over the groups, then every segment's incoming state.
+constexpr int64_t kTwoLevelSegs = 48;
+constexpr double kTwoLevelFixedUs = 10.0;
 
 struct SegChoice {
     int64_t segs = 0;         // fixed: segments per sequence; packed: a bound on all segments (0: none)
@@ -209,7 +214,30 @@ struct SegChoice {
     int64_t total = 0;        // segments the three state buffers hold
     int64_t state_bytes = 0;  // bytes of each of the three [total][H][128][128] BF16 buffers
     int64_t meta_bytes = 0;   // packed: seg_begin, seg_chunks, seg_tokens (256-aligned each)
+    int64_t group_segs = 0;   // two-level chain: segments per group (0: one level)
+    int64_t groups = 0;       // two-level chain: groups per sequence
+    int64_t group_bytes = 0;  // two-level chain: prefix and group buffers in all
 };
+
+// Segments per group of a two-level chain: about sqrt(segs), but large enough
+// that the composition (32 CTAs per group and head, two per SM) fits one
+// wave; 0 when one level is better (few segments, or no such size).
+int64_t group_size(int64_t segs, int64_t units, int sms, bool forced) {
+    if (segs < kTwoLevelSegs) return 0;
+    int64_t m = static_cast<int64_t>(std::ceil(std::sqrt(static_cast<double>(segs))));
+    if (!forced) {
+        const int64_t max_groups = sms / (16 * units);
+        if (max_groups < 4) return 0;
+        const int64_t m_wave = (segs + max_groups - 1) / max_groups;
+        if (m_wave > m) m = m_wave;
+    }
+    return m;
+}
+
+double chain_us(int64_t segs, int64_t m) {
+    if (m == 0) return segs * kScanStepUs;
+    return kTwoLevelFixedUs + (m - 1 + (segs + m - 1) / m) * kScanStepUs;
+}
 
 int64_t align256(int64_t b) { return ((b + 255) / 256) * 256; }
 
@@ -246,13 +274,19 @@ SegChoice plan_segments(const Plan& pl, int64_t H, int sms, bool checkpoints) {
             L = (chunks + target - 1) / target;
             const int64_t segs = (chunks + L - 1) / L;
             if (segs < 4) return sc;
-            const double seg_us =
-                kSegFixedUs + L * (kTransChunkUs + kQuadChunkUs) + segs * kScanStepUs;
+            const double seg_us = kSegFixedUs + L * (kTransChunkUs + kQuadChunkUs) +
+                                  chain_us(segs, group_size(segs, units, sms, false));
             if (seg_us >= chunks * t_serial) return sc;
         }
         sc.seg_chunks = L;
         sc.segs = (chunks + L - 1) / L;
         sc.total = pl.N * sc.segs;
+        sc.group_segs = group_size(sc.segs, units, sms, g_seg_chunks > 0);
+        if (sc.group_segs > 0) {
+            sc.groups = (sc.segs + sc.group_segs - 1) / sc.group_segs;
+            const int64_t st = H * kHeadDim * kHeadDim * 2;
+            sc.group_bytes = (2 * sc.total + 3 * pl.N * sc.groups) * st;
+        }
     }
     sc.state_bytes = sc.total * H * kHeadDim * kHeadDim * 2;
     return sc;
@@ -375,7 +409,7 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
     const SegChoice sc = plan_segments(pl, H, d->sms, ck != nullptr);
     const bool fused = sc.segs == 0 && use_fusion(pl, H, nsplit, d->sms);
     const int64_t ws_bytes = pl.meta_bytes + pl.packet_bytes + (fused ? pl.ready_bytes : 0) +
-                             3 * sc.state_bytes + sc.meta_bytes;
+                             3 * sc.state_bytes + sc.meta_bytes + sc.group_bytes;
     uint8_t* ws = nullptr;
     if (ws_bytes > 0) {
         if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes),
@@ -441,11 +475,27 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
             launch_transition(v, packets, sg, H, zstates, maps, d->status, stream) != cudaSuccess)
             rc = KDA_ERR_CUDA;
         prof_record(2, stream);
-        if (rc == KDA_OK &&
-            launch_segment_scan(init_state, final_state, maps, zstates, starts, pl.N, sc.segs,
-                                seg_begin, pl.packed ? geo.valid : nullptr, H, d->status,
-                                stream) != cudaSuccess)
+        if (rc == KDA_OK && sc.groups > 0) {
+            // Two levels: compose inside groups, chain over the groups, apply.
+            const int64_t st = H * kHeadDim * kHeadDim * 2;
+            uint8_t* pf = starts + sc.state_bytes + sc.meta_bytes;
+            uint8_t* pz = pf + sc.total * st;
+            uint8_t* gf = pz + sc.total * st;
+            uint8_t* gz = gf + pl.N * sc.groups * st;
+            uint8_t* gs = gz + pl.N * sc.groups * st;
+            if (launch_segment_compose(maps, zstates, pf, pz, gf, gz, pl.N, sc.segs, sc.group_segs,
+                                       sc.groups, H, d->status, stream) != cudaSuccess ||
+                launch_segment_scan(init_state, final_state, gf, gz, gs, pl.N, sc.groups, nullptr,
+                                    nullptr, H, d->status, stream) != cudaSuccess ||
+                launch_segment_apply(gs, pf, pz, starts, pl.N, sc.segs, sc.group_segs, sc.groups, H,
+                                     d->status, stream) != cudaSuccess)
+                rc = KDA_ERR_CUDA;
+        } else if (rc == KDA_OK &&
+                   launch_segment_scan(init_state, final_state, maps, zstates, starts, pl.N,
+                                       sc.segs, seg_begin, pl.packed ? geo.valid : nullptr, H,
+                                       d->status, stream) != cudaSuccess) {
             rc = KDA_ERR_CUDA;
+        }
         prof_record(3, stream);
         if (rc == KDA_OK &&
             launch_recurrence(v, out, starts, nullptr, packets, sg, H, 1, d->status, stream, ck) !=
@@ -681,7 +731,7 @@ extern "C" int kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int packed, 
     if (device_state(&d) == KDA_OK) sms = d->sms;
     const SegChoice sc = plan_segments(pl, H, sms, false);
     *bytes = pl.meta_bytes + pl.packet_bytes + (pl.packed ? 0 : pl.ready_bytes) +
-             3 * sc.state_bytes + sc.meta_bytes;
+             3 * sc.state_bytes + sc.meta_bytes + sc.group_bytes;
     return KDA_OK;
 }
 

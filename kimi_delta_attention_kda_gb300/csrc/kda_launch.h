@@ -88,6 +88,21 @@ cudaError_t launch_segment_scan(const void* init_state, void* final_state, const
                                 int64_t segs, const int64_t* seg_begin, const int32_t* valid,
                                 int64_t H, int* status, cudaStream_t stream);
 
+// Two-level chain (fixed layout, segs segments per sequence in groups of
+// group_segs): first the composition inside each group — prefix maps
+// (prefix_f, prefix_z: [segments][H][128][128], entry s = the map of the
+// group's segments up to s) and the group maps (group_f, group_z:
+// [groups][H][128][128]); then launch_segment_scan over the group maps gives
+// each group's incoming state; then launch_segment_apply forms every
+// segment's incoming state from its group's and the prefix before it.
+cudaError_t launch_segment_compose(const void* transitions, const void* zero_start_states,
+                                   void* prefix_f, void* prefix_z, void* group_f, void* group_z,
+                                   int64_t n_seqs, int64_t segs, int64_t group_segs,
+                                   int64_t groups, int64_t H, int* status, cudaStream_t stream);
+cudaError_t launch_segment_apply(const void* group_starts, const void* prefix_f, const void* prefix_z,
+                                 void* starts, int64_t n_seqs, int64_t segs, int64_t group_segs,
+                                 int64_t groups, int64_t H, int* status, cudaStream_t stream);
+
 // Segments of a packed batch of n_seqs sequences (after launch_varlen_meta):
 // ceil(chunks / seg_chunks_len) per sequence, at most s_ub in all; writes
 // seg_begin [n_seqs + 1], per segment its first chunk and first token

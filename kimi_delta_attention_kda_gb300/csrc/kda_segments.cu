@@ -70,6 +70,17 @@ struct ScanArgs {
     const int32_t* valid;              // packed layout: the metadata's verdict
     int64_t segs, H;
     int* status;
+    // Composition in groups (first level of a two-level chain, fixed layout;
+    // groups 0: off).  CTA sequence n is group n % groups of sequence
+    // n / groups: segments gs = (n / groups) segs + (n % groups) group_segs
+    // and on, up to group_segs of them.  The grid's first half composes the
+    // F maps (src[0], no Z), the second half the Z maps (src[1], adding Z):
+    // state_0 = src[gs], state_j = state_{j-1} F_{gs+j} (+ Z_{gs+j}); state_j
+    // goes to prefix[p][gs + j] and the last one to gmap[p][n].
+    int64_t groups, group_segs;
+    const __nv_bfloat16* src[2];
+    __nv_bfloat16* prefix[2];
+    __nv_bfloat16* gmap[2];
 };
 
 // Warp w's slice (keys 32 w .. 32 w + 31 of the CTA's 8 rows) of a state in
@@ -104,13 +115,37 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
     constexpr int kGroups = kHeadDim / kScanRows;
-    const int64_t nh = blockIdx.x / kGroups;
-    const int v0 = kScanRows * static_cast<int>(blockIdx.x - nh * kGroups);
+    const bool compose = a.groups > 0;
+    int part = 0;
+    int64_t blk = blockIdx.x;
+    if (compose) {
+        const int64_t half = gridDim.x / 2;
+        part = blk >= half ? 1 : 0;
+        blk -= part * half;
+    }
+    const int64_t nh = blk / kGroups;
+    const int v0 = kScanRows * static_cast<int>(blk - nh * kGroups);
     const int64_t n = nh / a.H;
     const int64_t h = nh - n * a.H;
     if (a.valid && !*a.valid) return;
-    const int64_t first = a.seg_begin ? a.seg_begin[n] : n * a.segs;
-    const int64_t nseg = a.seg_begin ? a.seg_begin[n + 1] - first : a.segs;
+    // Step j reads the maps of segment step0 + j and first carries no Z (or
+    // its own when composing the Z maps); the state before step j goes to
+    // segment first + j.
+    int64_t first, nseg, step0;
+    if (compose) {
+        const int64_t sq = n / a.groups, gi = n - sq * a.groups;
+        first = sq * a.segs + gi * a.group_segs;
+        int64_t len = a.segs - gi * a.group_segs;
+        if (len > a.group_segs) len = a.group_segs;
+        nseg = len - 1;
+        step0 = first + 1;
+    } else {
+        first = a.seg_begin ? a.seg_begin[n] : n * a.segs;
+        nseg = a.seg_begin ? a.seg_begin[n + 1] - first : a.segs;
+        step0 = first;
+    }
+    const bool add_z = !compose || part == 1;
+    __nv_bfloat16* const starts = compose ? (part ? a.prefix[1] : a.prefix[0]) : a.starts;
     if (threadIdx.x == 0) {
         for (int s = 0; s < kScanStages; ++s) {
             mbar_init(&full[s], 1);
@@ -131,7 +166,7 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
             if (!ok) break;
             uint8_t* stage = smem + s * kScanStageBytes;
             if (lane == 0) {
-                const int32_t row = static_cast<int32_t>(((first + j) * a.H + h) * kHeadDim);
+                const int32_t row = static_cast<int32_t>(((step0 + j) * a.H + h) * kHeadDim);
                 mbar_arrive_expect_tx(&full[s], kScanFBytes + kScanZBytes);
                 tma_load_2d(stage, &fmap, 0, row, &full[s]);
                 tma_load_2d(stage + kScanFBytes / 2, &fmap, 64, row, &full[s]);
@@ -153,14 +188,18 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
     const int tid = threadIdx.x;   // 0 .. 127
     uint8_t* xbuf = smem + kScanXOff;
     const int64_t rows0 = (n * a.H + h) * kHeadDim + v0;   // first row of this CTA in [N][H][128]
+    // The initial state: the caller's (per sequence), or when composing the
+    // group's first segment map.
+    const __nv_bfloat16* init = compose ? (part ? a.src[1] : a.src[0]) + ((first * a.H + h) * kHeadDim + v0) * kHeadDim
+                                        : (a.init_state ? a.init_state + rows0 * kHeadDim : nullptr);
 
     // S_0^T for keys 32 warp + 16 mt + {g8, g8 + 8}, rows v0 + 2 t4 + {0, 1}.
     float c[2][4];
 #pragma unroll
     for (int mt = 0; mt < 2; ++mt) {
         const int key = 32 * warp + 16 * mt + g8;
-        if (a.init_state) {
-            const __nv_bfloat16* src = a.init_state + (rows0 + 2 * t4) * kHeadDim;
+        if (init) {
+            const __nv_bfloat16* src = init + 2 * t4 * kHeadDim;
             c[mt][0] = __bfloat162float(src[key]);
             c[mt][1] = __bfloat162float(src[kHeadDim + key]);
             c[mt][2] = __bfloat162float(src[key + 8]);
@@ -209,14 +248,15 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
             b[2 * kp + 1][0] = r[2];
             b[2 * kp + 1][1] = r[3];
         }
-        // Accumulators: Z_j^T (even k-steps) and zero (odd k-steps).
+        // Accumulators: Z_j^T (even k-steps; zero when composing the F maps)
+        // and zero (odd k-steps).
         float acc[2][2][4];
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt) {
-            acc[mt][0][0] = bf_lo(zf[2 * mt]);
-            acc[mt][0][1] = bf_hi(zf[2 * mt]);
-            acc[mt][0][2] = bf_lo(zf[2 * mt + 1]);
-            acc[mt][0][3] = bf_hi(zf[2 * mt + 1]);
+            acc[mt][0][0] = add_z ? bf_lo(zf[2 * mt]) : 0.f;
+            acc[mt][0][1] = add_z ? bf_hi(zf[2 * mt]) : 0.f;
+            acc[mt][0][2] = add_z ? bf_lo(zf[2 * mt + 1]) : 0.f;
+            acc[mt][0][3] = add_z ? bf_hi(zf[2 * mt + 1]) : 0.f;
             acc[mt][1][0] = acc[mt][1][1] = acc[mt][1][2] = acc[mt][1][3] = 0.f;
         }
 #pragma unroll
@@ -225,7 +265,7 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
             for (int mt = 0; mt < 2; ++mt) mma_bf16(acc[mt][kk & 1], af[mt][kk], b[kk], acc[mt][kk & 1]);
         // While the MMAs run: S_j out as this segment's incoming state, and
         // the next step's operands in.
-        copy_rows_out(xc, a.starts + (((first + j) * a.H + h) * kHeadDim + v0) * kHeadDim, tid);
+        copy_rows_out(xc, starts + (((first + j) * a.H + h) * kHeadDim + v0) * kHeadDim, tid);
         if (j + 1 < nseg && !load_step(j + 1)) ok = false;
 #pragma unroll
         for (int mt = 0; mt < 2; ++mt)
@@ -234,8 +274,144 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
         put_rows(xbuf + ((j + 1) & 1) * kScanXBytes, c, warp, g8, t4);
         ok = group_all<kScanWarps * 32>(1, ok);
     }
-    if (ok && a.final_state)
-        copy_rows_out(xbuf + (nseg & 1) * kScanXBytes, a.final_state + rows0 * kHeadDim, tid);
+    __nv_bfloat16* const fin = compose ? (part ? a.gmap[1] : a.gmap[0]) : a.final_state;
+    if (ok && fin) copy_rows_out(xbuf + (nseg & 1) * kScanXBytes, fin + rows0 * kHeadDim, tid);
+}
+
+// ---------------------------------------------------------------------------
+// Last level of a two-level chain: for segment s, the i-th of its group g,
+// the incoming state S_s = S_g P_F[s - 1] + P_Z[s - 1] (i >= 1; S_g itself for
+// i = 0), where S_g is the group's incoming state and (P_F, P_Z) the map of
+// the group's segments before s.  One CTA per (segment, head), all 128 value
+// rows: four warps each form 32 key columns of S_s^T = P_F^T S_g^T + P_Z^T
+// (warp MMA, BF16 operands, FP32 accumulation) from the three TMA-staged
+// states, and the rows leave through shared memory in 16-byte stores.
+// ---------------------------------------------------------------------------
+constexpr int kApplyWarps = 4;
+constexpr uint32_t kApplyTile = kHeadDim * kHeadDim * 2;   // one state, two SW128 slabs [128][64]
+constexpr uint32_t kApplyOut = 3 * kApplyTile;            // output rows, XOR-swizzled [128][128]
+constexpr uint32_t kApplyBar = 4 * kApplyTile;
+constexpr uint32_t kApplySmemBytes = kApplyBar + 8 + 1024;
+
+struct ApplyArgs {
+    const __nv_bfloat16* group_starts;   // S_g: [N groups][H][128][128]
+    __nv_bfloat16* starts;               // S_s: [N segs][H][128][128]
+    int64_t segs, groups, group_segs, H;
+    int* status;
+};
+
+__device__ __forceinline__ uint32_t out_off(uint32_t v, uint32_t ch) {
+    return v * (kHeadDim * 2) + ((ch ^ (v & 7u)) << 4);
+}
+
+__global__ void __launch_bounds__(kApplyWarps * 32, 1)
+    segment_apply_kernel(ApplyArgs a, const __grid_constant__ CUtensorMap pfmap,
+                         const __grid_constant__ CUtensorMap pzmap,
+                         const __grid_constant__ CUtensorMap sgmap) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    uint64_t* bar = reinterpret_cast<uint64_t*>(smem + kApplyBar);
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int tid = threadIdx.x;
+    const int64_t sh = blockIdx.x;
+    const int64_t seg = sh / a.H;
+    const int64_t h = sh - seg * a.H;
+    const int64_t sq = seg / a.segs;
+    const int64_t sl = seg - sq * a.segs;
+    const int64_t gi = sl / a.group_segs;
+    const int64_t i = sl - gi * a.group_segs;
+    const int64_t g = sq * a.groups + gi;
+    __nv_bfloat16* dst = a.starts + (seg * a.H + h) * kHeadDim * kHeadDim;
+    if (i == 0) {
+        // The group's first segment starts from the group's incoming state.
+        const uint4* src = reinterpret_cast<const uint4*>(a.group_starts + (g * a.H + h) * kHeadDim * kHeadDim);
+        for (int q = tid; q < static_cast<int>(kApplyTile / 16); q += kApplyWarps * 32)
+            reinterpret_cast<uint4*>(dst)[q] = src[q];
+        return;
+    }
+    if (tid == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+        const int32_t prow = static_cast<int32_t>(((seg - 1) * a.H + h) * kHeadDim);
+        const int32_t grow = static_cast<int32_t>((g * a.H + h) * kHeadDim);
+        mbar_arrive_expect_tx(bar, 3 * kApplyTile);
+        tma_load_2d(smem, &pfmap, 0, prow, bar);
+        tma_load_2d(smem + kApplyTile / 2, &pfmap, 64, prow, bar);
+        tma_load_2d(smem + kApplyTile, &pzmap, 0, prow, bar);
+        tma_load_2d(smem + kApplyTile + kApplyTile / 2, &pzmap, 64, prow, bar);
+        tma_load_2d(smem + 2 * kApplyTile, &sgmap, 0, grow, bar);
+        tma_load_2d(smem + 2 * kApplyTile + kApplyTile / 2, &sgmap, 64, grow, bar);
+    }
+    __syncthreads();
+    const bool ok = mbar_wait_warp(bar, 0, a.status);
+    if (!__all_sync(0xffffffffu, ok)) return;   // bounded wait ran out (status is set)
+
+    const uint8_t* tf = smem;                   // P_F rows (old key) x columns (new key)
+    const uint8_t* tz = smem + kApplyTile;      // P_Z rows (value) x columns (new key)
+    const uint8_t* ts = smem + 2 * kApplyTile;  // S_g rows (value) x columns (old key)
+    uint8_t* out = smem + kApplyOut;
+    const int g8 = lane >> 2, t4 = lane & 3;
+    const uint32_t mi = lane >> 3, r8 = lane & 7;
+
+    // Accumulators: P_Z^T tiles (m = new key 32 warp + 16 mt .., n = value 8 nt ..).
+    float acc[2][16][4];
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+            uint32_t z[4];
+            const uint32_t v = 8 * (2 * np + (mi >> 1)) + r8;
+            const uint32_t ch = 4 * warp + 2 * mt + (mi & 1);
+            ldsm_x4_trans(z, smem_u32(tz + sw128_off(kHeadDim, v, ch)));
+#pragma unroll
+            for (int e = 0; e < 2; ++e) {
+                acc[mt][2 * np + e][0] = bf_lo(z[2 * e]);
+                acc[mt][2 * np + e][1] = bf_hi(z[2 * e]);
+                acc[mt][2 * np + e][2] = bf_lo(z[2 * e + 1]);
+                acc[mt][2 * np + e][3] = bf_hi(z[2 * e + 1]);
+            }
+        }
+    // + P_F^T S_g^T over the 128 old keys.
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) {
+        uint32_t af[2][4];
+#pragma unroll
+        for (int mt = 0; mt < 2; ++mt) {
+            const uint32_t row = 16 * kk + r8 + 8 * (mi >> 1);
+            const uint32_t ch = 4 * warp + 2 * mt + (mi & 1);
+            ldsm_x4_trans(af[mt], smem_u32(tf + sw128_off(kHeadDim, row, ch)));
+        }
+#pragma unroll
+        for (int np = 0; np < 8; ++np) {
+            uint32_t b[4];   // S_g^T (k = old key, n = value) for value tiles 2 np, 2 np + 1
+            const uint32_t v = 8 * (2 * np + (mi >> 1)) + r8;
+            ldsm_x4(b, smem_u32(ts + sw128_off(kHeadDim, v, 2 * kk + (mi & 1))));
+#pragma unroll
+            for (int mt = 0; mt < 2; ++mt) {
+                mma_bf16(acc[mt][2 * np], af[mt], b, acc[mt][2 * np]);
+                mma_bf16(acc[mt][2 * np + 1], af[mt], b + 2, acc[mt][2 * np + 1]);
+            }
+        }
+    }
+    // S_s rows (value) x key, BF16, through shared memory.
+#pragma unroll
+    for (int mt = 0; mt < 2; ++mt)
+#pragma unroll
+        for (int nt = 0; nt < 16; ++nt) {
+            const uint32_t lo = movm_trans(pack_bf16(acc[mt][nt][0], acc[mt][nt][1]));
+            const uint32_t hi = movm_trans(pack_bf16(acc[mt][nt][2], acc[mt][nt][3]));
+            const uint32_t v = 8 * nt + g8;
+            const uint32_t base = 32 * warp + 16 * mt;
+            *reinterpret_cast<uint32_t*>(out + out_off(v, base / 8) + 4 * t4) = lo;
+            *reinterpret_cast<uint32_t*>(out + out_off(v, base / 8 + 1) + 4 * t4) = hi;
+        }
+    __syncthreads();
+    for (int q = tid; q < static_cast<int>(kApplyTile / 16); q += kApplyWarps * 32) {
+        const uint32_t v = q >> 4, ch = q & 15;
+        reinterpret_cast<uint4*>(dst)[q] = *reinterpret_cast<const uint4*>(out + out_off(v, ch));
+    }
 }
 
 // Segments of a packed batch (one block): sequence n, of c_n chunks, gets
@@ -343,6 +519,11 @@ cudaError_t launch_segment_scan(const void* init_state, void* final_state, const
     a.segs = segs;
     a.seg_begin = seg_begin;
     a.valid = valid;
+    a.groups = 0;
+    a.group_segs = 0;
+    a.src[0] = a.src[1] = nullptr;
+    a.prefix[0] = a.prefix[1] = nullptr;
+    a.gmap[0] = a.gmap[1] = nullptr;
     a.H = H;
     a.status = status;
     segment_scan_kernel<<<static_cast<unsigned>(blocks), (kScanWarps + 1) * 32, kScanSmemBytes,
@@ -358,6 +539,88 @@ cudaError_t launch_segment_meta(const int64_t* cu_seqlens, const int64_t* cu_chu
     segment_meta_kernel<<<1, kSegMetaThreads, 0, stream>>>(cu_seqlens, cu_chunks, valid, n_seqs,
                                                           seg_chunks_len, s_ub, seg_begin,
                                                           seg_chunks, seg_tokens, seg_seq, status);
+    return cudaGetLastError();
+}
+
+namespace {
+
+bool configure_scan(int dev) {
+    static bool configured[64] = {};
+    if (dev < 0 || dev >= 64) return false;
+    if (!configured[dev]) {
+        if (cudaFuncSetAttribute(segment_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kScanSmemBytes)) != cudaSuccess ||
+            cudaFuncSetAttribute(segment_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kApplySmemBytes)) != cudaSuccess)
+            return false;
+        configured[dev] = true;
+    }
+    return true;
+}
+
+}  // namespace
+
+cudaError_t launch_segment_compose(const void* transitions, const void* zero_start_states,
+                                   void* prefix_f, void* prefix_z, void* group_f, void* group_z,
+                                   int64_t n_seqs, int64_t segs, int64_t group_segs,
+                                   int64_t groups, int64_t H, int* status, cudaStream_t stream) {
+    const int64_t blocks = 2 * n_seqs * groups * H * (kHeadDim / kScanRows);
+    if (blocks <= 0) return cudaSuccess;
+    const int64_t rows = n_seqs * segs * H * kHeadDim;
+    if (rows >= (int64_t(1) << 31) || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || !configure_scan(dev)) return cudaErrorInvalidDevice;
+    CUtensorMap fmap, zmap;
+    cudaError_t e = encode_state_map(&fmap, transitions, rows, kHeadDim);
+    if (e == cudaSuccess) e = encode_state_map(&zmap, zero_start_states, rows, kScanRows);
+    if (e != cudaSuccess) return e;
+    ScanArgs a;
+    a.init_state = nullptr;
+    a.final_state = nullptr;
+    a.starts = nullptr;
+    a.seg_begin = nullptr;
+    a.valid = nullptr;
+    a.segs = segs;
+    a.H = H;
+    a.status = status;
+    a.groups = groups;
+    a.group_segs = group_segs;
+    a.src[0] = static_cast<const __nv_bfloat16*>(transitions);
+    a.src[1] = static_cast<const __nv_bfloat16*>(zero_start_states);
+    a.prefix[0] = static_cast<__nv_bfloat16*>(prefix_f);
+    a.prefix[1] = static_cast<__nv_bfloat16*>(prefix_z);
+    a.gmap[0] = static_cast<__nv_bfloat16*>(group_f);
+    a.gmap[1] = static_cast<__nv_bfloat16*>(group_z);
+    segment_scan_kernel<<<static_cast<unsigned>(blocks), (kScanWarps + 1) * 32, kScanSmemBytes,
+                          stream>>>(a, fmap, zmap);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_segment_apply(const void* group_starts, const void* prefix_f, const void* prefix_z,
+                                 void* starts, int64_t n_seqs, int64_t segs, int64_t group_segs,
+                                 int64_t groups, int64_t H, int* status, cudaStream_t stream) {
+    const int64_t blocks = n_seqs * segs * H;
+    if (blocks <= 0) return cudaSuccess;
+    const int64_t rows = n_seqs * segs * H * kHeadDim;
+    const int64_t grows = n_seqs * groups * H * kHeadDim;
+    if (rows >= (int64_t(1) << 31) || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || !configure_scan(dev)) return cudaErrorInvalidDevice;
+    CUtensorMap pfmap, pzmap, sgmap;
+    cudaError_t e = encode_state_map(&pfmap, prefix_f, rows, kHeadDim);
+    if (e == cudaSuccess) e = encode_state_map(&pzmap, prefix_z, rows, kHeadDim);
+    if (e == cudaSuccess) e = encode_state_map(&sgmap, group_starts, grows, kHeadDim);
+    if (e != cudaSuccess) return e;
+    ApplyArgs a;
+    a.group_starts = static_cast<const __nv_bfloat16*>(group_starts);
+    a.starts = static_cast<__nv_bfloat16*>(starts);
+    a.segs = segs;
+    a.groups = groups;
+    a.group_segs = group_segs;
+    a.H = H;
+    a.status = status;
+    segment_apply_kernel<<<static_cast<unsigned>(blocks), kApplyWarps * 32, kApplySmemBytes, stream>>>(
+        a, pfmap, pzmap, sgmap);
     return cudaGetLastError();
 }
 

@@ -285,3 +285,50 @@ def test_forced_checkpoints_packed(forced):
     plain = run(forced, inp)
     assert torch.equal(out, plain[0]) and torch.equal(fin, plain[1])
     _check_rows(inp, LENGTHS, every, starts, ck)
+
+
+# ----------------------------------------------------------------------------
+# Two-level chain (48 or more segments per sequence, fixed layout)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,T,H", [(1, 1024, 1), (2, 1000, 3), (1, 800, 2), (1, 912, 2)])
+def test_two_level_chain(forced, B, T, H):
+    """One-chunk segments: 50-64 per sequence, composed in groups of 8 (the
+    last group of 1000 tokens has 7 segments, of 800 two, of 912 one), chained
+    over the groups and applied; against the oracle and the serial chain."""
+    forced.set_segments(True, 1)
+    assert forced.plan_segments(B, T, H, False) == (T + 15) // 16
+    inp = synthetic.make_inputs(B, T, H, 7900 + T, init_std=0.02)
+    out, fin = run(forced, inp)
+    tu.check_against_oracle(inp, out, fin)
+    forced.set_segments(False)
+    out_s, fin_s = run(forced, inp)
+    for b in range(B):
+        tu.assert_within_tolerance(out[b].double().numpy(), out_s[b].double().numpy(), 1,
+                                   "two-level vs serial O")
+        tu.assert_within_tolerance(fin[b].double().numpy(), fin_s[b].double().numpy(), 0,
+                                   "two-level vs serial S")
+
+
+def test_two_level_chain_long_memory_and_checkpoints(forced):
+    """The correlated long-memory family carries state across every group, and
+    the rerun's checkpoints follow the applied incoming states."""
+    import oracle
+    inp = synthetic.stress_inputs("weak_decay_correlated", 1024, 2, 93)
+    o_ref, f_ref = oracle.kda_token(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"])
+    forced.set_segments(False)
+    out_s, fin_s = run(forced, inp)
+    forced.set_segments(True, 1)
+    out, fin = run(forced, inp)
+    for got, ser, ref, ax in ((out[0], out_s[0], o_ref[0], 1), (fin[0], fin_s[0], f_ref[0], 0)):
+        e_seg = tu.per_head_errors(got.double().numpy(), ref, ax)
+        e_ser = tu.per_head_errors(ser.double().numpy(), ref, ax)
+        for (rel, mx), (rel_s, _) in zip(e_seg, e_ser):
+            assert rel <= 3e-2 and mx <= tu.MAX_ABS_TOL
+            assert rel <= 1.15 * rel_s + 1e-3, (rel, rel_s)
+    ck_inp = synthetic.make_inputs(1, 1024, 2, 7950, init_std=0.02)
+    starts = _ck_starts([1024], 128)
+    o, f, ck = _ck_call(forced, ck_inp, 128, starts)
+    plain = run(forced, ck_inp)
+    assert torch.equal(o, plain[0]) and torch.equal(f, plain[1])
+    _check_rows(ck_inp, [1024], 128, starts, ck)
