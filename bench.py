@@ -71,18 +71,19 @@ PATH_BYTES_PER_HT = 2 * 256 + 512 + 2 + 256 + 256
 TRANSITION_BYTES_PER_HT = 2 * PACKET_PER_TOKEN + 256
 STATE_BYTES = 128 * 128 * 2
 
-# DRAM bytes (read + write) of one launch of the dominant kernel, from one ncu
-# capture each (summaries in profiles/).  A figure is reported only while the
+# DRAM bytes (read + write) of one launch of the dominant kernel (of the
+# segment chain: its launches in one call), from one ncu capture each
+# (summaries in profiles/).  A figure is reported only while the
 # kernel's sources still hash to the value they had when it was captured.
 REC_SOURCES = ("kda_recurrence.cu", "kda_rec_impl.cuh", "kda_common.cuh")
 PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
 SEG_SOURCES = ("kda_segments.cu", "kda_common.cuh")
 PROFILED_TRAFFIC = {
-    ("transition", "t8192_h6"): (55.514e6, REC_SOURCES, "703f5024d16930e2"),
-    ("chunk_prep", "t8192_h6"): (54.477e6, PREP_SOURCES, "983222c2baaef973"),
-    ("segment_chain", "t65536_h1"): (10.009e6, SEG_SOURCES, "469bcecb9ef0f87e"),
-    ("recurrence", "t8192_h96"): (1067.616e6, REC_SOURCES, "703f5024d16930e2"),
-    ("chunk_prep", "t8192_h96"): (1460.403e6, PREP_SOURCES, "983222c2baaef973"),
+    ("transition", "t8192_h6"): (55.574e6, REC_SOURCES, "07eabcbca4f1a1df"),
+    ("chunk_prep", "t8192_h6"): (53.492e6, PREP_SOURCES, "70ed937ba7aaa41b"),
+    ("segment_chain", "t65536_h1"): (20.306e6, SEG_SOURCES, "a574cabe1e495497"),
+    ("recurrence", "t8192_h96"): (1066.769e6, REC_SOURCES, "07eabcbca4f1a1df"),
+    ("chunk_prep", "t8192_h96"): (1457.915e6, PREP_SOURCES, "70ed937ba7aaa41b"),
 }
 
 
@@ -396,7 +397,10 @@ def critical_path(kda, inp, ht, state_io, us_per_call, segs):
         plan_chain = 2 * L * t_step / 1e3
         plan_bound = max(hbm_us, tensor_us, plan_chain)
         res.update({"plan_segment_chunks": L, "plan_chain_bound_us": plan_chain,
-                    "plan_bound_us": plan_bound, "plan_frac": plan_bound / us_per_call})
+                    "plan_bound_us": plan_bound, "plan_frac": plan_bound / us_per_call,
+                    "note": "bound/frac: a serial walk's bounds, which a segmented call is not "
+                            "held to (frac > 1 when it beats the serial chain); plan_*: the "
+                            "bounds of the segmented plan that ran"})
     return res
 
 

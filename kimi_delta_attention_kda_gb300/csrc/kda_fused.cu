@@ -104,13 +104,7 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
         return cudaErrorInvalidValue;
 
     FusedArgs f;
-    f.p.beta = static_cast<const __nv_bfloat16*>(beta);
-    f.p.packets = packets;
-    f.p.geo = geo;
-    f.p.geo.status = status;
-    f.p.H = H;
-    f.p.n_chunk_heads = geo.chunk_ub * H;
-    f.p.scale = scale;
+    if (!prep::make_prep_args(&f.p, beta, packets, geo, H, scale, status)) return cudaErrorInvalidValue;
     f.r.v = static_cast<const __nv_bfloat16*>(v);
     f.r.out = static_cast<__nv_bfloat16*>(out);
     f.r.init_state = static_cast<const __nv_bfloat16*>(init_state);

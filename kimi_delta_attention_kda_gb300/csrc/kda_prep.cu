@@ -111,16 +111,10 @@ using namespace prep;
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const void* beta,
                         uint8_t* packets, const SeqGeometry& geo, int64_t H, float scale,
                         int* status, cudaStream_t stream) {
-    PrepArgs a;
-    a.beta = static_cast<const __nv_bfloat16*>(beta);
-    a.packets = packets;
-    a.geo = geo;
-    a.geo.status = status;
-    a.H = H;
-    a.n_chunk_heads = geo.chunk_ub * H;
-    a.scale = scale;
-    if (a.n_chunk_heads <= 0 || geo.tokens <= 0) return cudaSuccess;
+    if (geo.chunk_ub * H <= 0 || geo.tokens <= 0) return cudaSuccess;
     if (geo.tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // TMA coordinates are int32
+    PrepArgs a;
+    if (!make_prep_args(&a, beta, packets, geo, H, scale, status)) return cudaErrorInvalidValue;
     PrepMaps maps;
     cudaError_t e = encode_maps(&maps, q, k, g, geo.tokens, H);
     if (e != cudaSuccess) return e;

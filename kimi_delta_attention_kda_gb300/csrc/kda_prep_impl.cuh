@@ -11,6 +11,29 @@
 namespace kda {
 namespace prep {
 
+// Division by a divisor fixed for a launch, as a multiply-high, an add and a
+// shift: the round-up multiplier of Granlund and Montgomery ("Division by
+// invariant integers using multiplication", 1994, section 4).  For d in
+// [1, 2^31): s = ceil(log2 d), m = floor(2^32 (2^s - d) / d) + 1 (< 2^32),
+// and floor(n / d) = (mulhi(n, m) + n) >> s for every n in [0, 2^31), where
+// mulhi(n, m) + n < 2 n cannot overflow 32 bits.
+struct FastDiv {
+    uint32_t d, m, s;
+};
+inline FastDiv make_fastdiv(uint32_t d) {
+    uint32_t s = 0;
+    while ((uint64_t(1) << s) < d) ++s;
+    const uint64_t m = ((uint64_t(1) << 32) * ((uint64_t(1) << s) - d)) / d + 1;
+    return FastDiv{d, static_cast<uint32_t>(m), s};
+}
+__host__ __device__ __forceinline__ uint32_t fast_div(uint32_t n, const FastDiv& f) {
+#ifdef __CUDA_ARCH__
+    return (__umulhi(n, f.m) + n) >> f.s;
+#else
+    return static_cast<uint32_t>(((static_cast<uint64_t>(n) * f.m >> 32) + n) >> f.s);
+#endif
+}
+
 // A CTA has 8 warps: 4 pairs.  Each (chunk, head) is prepared by one pair:
 // warp h (0 or 1) of the pair builds the operands of tokens 8 h .. 8 h + 7,
 // and the pair splits the rest (step comments below).  The pair synchronises on its own
@@ -48,9 +71,30 @@ struct PrepArgs {
     uint8_t* packets;
     SeqGeometry geo;
     int64_t H;
-    int64_t n_chunk_heads;
+    int64_t n_chunk_heads;   // < 2^31, so item, chunk and head indices fit 32 bits
     float scale;
+    FastDiv div_h;           // by H
+    FastDiv div_cps;         // by geo.chunks_per_seq (fixed layout)
 };
+
+// The preparation's arguments for `geo` and H heads; false when the item
+// count leaves the 32-bit range of the item arithmetic.
+inline bool make_prep_args(PrepArgs* a, const void* beta, uint8_t* packets, const SeqGeometry& geo,
+                           int64_t H, float scale, int* status) {
+    a->beta = static_cast<const __nv_bfloat16*>(beta);
+    a->packets = packets;
+    a->geo = geo;
+    a->geo.status = status;
+    a->H = H;
+    a->n_chunk_heads = geo.chunk_ub * H;
+    a->scale = scale;
+    if (H <= 0 || H >= (int64_t(1) << 31) || a->n_chunk_heads >= (int64_t(1) << 31)) return false;
+    const int64_t cps = geo.cu_chunks ? 1 : geo.chunks_per_seq;
+    if (cps <= 0 || cps >= (int64_t(1) << 31)) return false;
+    a->div_h = make_fastdiv(static_cast<uint32_t>(H));
+    a->div_cps = make_fastdiv(static_cast<uint32_t>(cps));
+    return true;
+}
 
 struct PrepMaps {
     CUtensorMap q, k, g;   // [tokens][H * 128] views, boxes of 16 tokens x 128 channels
@@ -109,16 +153,20 @@ __device__ __forceinline__ void st_row4_split(uint8_t* hi, uint8_t* lo, int t, i
 // does not exist (past the last chunk of a packed batch, or invalid offsets).
 __device__ __forceinline__ bool item_range(const PrepArgs& a, int64_t item, int64_t* t0,
                                            int64_t* len, int64_t* c_out, int64_t* h_out) {
-    const int64_t c = item / a.H;
-    const int64_t h = item - c * a.H;
+    // item < n_chunk_heads < 2^31: 32-bit quotients by the launch's divisors.
+    const uint32_t it = static_cast<uint32_t>(item);
+    const uint32_t c32 = fast_div(it, a.div_h);
+    const int64_t c = c32;
+    const int64_t h = it - c32 * a.div_h.d;
     if (a.geo.cu_chunks) {
         if (c >= a.geo.cu_chunks[a.geo.n_seqs]) return false;
         const int64_t n = find_sequence(a.geo.cu_chunks, a.geo.n_seqs, c);
         *t0 = a.geo.cu_seqlens[n] + kChunk * (c - a.geo.cu_chunks[n]);
         *len = a.geo.cu_seqlens[n + 1] - *t0;
     } else {
-        const int64_t n = c / a.geo.chunks_per_seq;
-        const int64_t ci = c - n * a.geo.chunks_per_seq;
+        const uint32_t n32 = fast_div(c32, a.div_cps);
+        const int64_t n = n32;
+        const int64_t ci = c32 - n32 * a.div_cps.d;
         *t0 = n * a.geo.tokens_per_seq + kChunk * ci;
         *len = a.geo.tokens_per_seq - kChunk * ci;
     }
@@ -150,10 +198,23 @@ __device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, floa
     float* tR = reinterpret_cast<float*>(sc + kPrepOffR);
     const int tb = 8 * hw;   // this warp's tokens in steps 1-3: tb .. tb + 7
 
+    // ---- 0. A ragged last chunk: the tile rows past the end of the sequence
+    // (the next sequence's tokens, or the tensor map's zero fill) are set to
+    // zero, so that the steps below read all 16 rows unconditionally.
+    if (len < kChunk) {
+        for (int t = static_cast<int>(len) + hw; t < kChunk; t += 2) {
+            *reinterpret_cast<float4*>(region + kInG + t * 512 + 16 * lane) =
+                make_float4(0.f, 0.f, 0.f, 0.f);
+            *reinterpret_cast<uint2*>(region + kInQ + t * 256 + 8 * lane) = make_uint2(0u, 0u);
+            *reinterpret_cast<uint2*>(region + kInK + t * 256 + 8 * lane) = make_uint2(0u, 0u);
+        }
+        pair_sync(bid);
+    }
+
     // ---- 1. Lane l owns key channels 4 l .. 4 l + 3.  g's running sum (G, in
     // base-2 units so that each exponential below is one ex2) over all 16
     // tokens, keeping this warp's 8 tokens and G_15; q and k of this warp's 8
-    // tokens.  Tokens past the end of the sequence read as zero.
+    // tokens.
     uint2 qv[8], kv[8];
     float G[8][4];
     float gl[4];             // G_15
@@ -163,31 +224,27 @@ __device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, floa
         if (hw == 1) {
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
-                const bool live = t < len;
                 const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
-                r0 += live ? gg.x * kLog2e : 0.f;
-                r1 += live ? gg.y * kLog2e : 0.f;
-                r2 += live ? gg.z * kLog2e : 0.f;
-                r3 += live ? gg.w * kLog2e : 0.f;
+                r0 = fmaf(gg.x, kLog2e, r0);
+                r1 = fmaf(gg.y, kLog2e, r1);
+                r2 = fmaf(gg.z, kLog2e, r2);
+                r3 = fmaf(gg.w, kLog2e, r3);
             }
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int t = tb + j;
-            const bool live = t < len;
             const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
-            r0 += live ? gg.x * kLog2e : 0.f;
-            r1 += live ? gg.y * kLog2e : 0.f;
-            r2 += live ? gg.z * kLog2e : 0.f;
-            r3 += live ? gg.w * kLog2e : 0.f;
+            r0 = fmaf(gg.x, kLog2e, r0);
+            r1 = fmaf(gg.y, kLog2e, r1);
+            r2 = fmaf(gg.z, kLog2e, r2);
+            r3 = fmaf(gg.w, kLog2e, r3);
             G[j][0] = r0;
             G[j][1] = r1;
             G[j][2] = r2;
             G[j][3] = r3;
-            const uint2 qq = *reinterpret_cast<const uint2*>(in + kInQ + t * 256 + 8 * lane);
-            const uint2 kq = *reinterpret_cast<const uint2*>(in + kInK + t * 256 + 8 * lane);
-            qv[j] = live ? qq : make_uint2(0u, 0u);
-            kv[j] = live ? kq : make_uint2(0u, 0u);
+            qv[j] = *reinterpret_cast<const uint2*>(in + kInQ + t * 256 + 8 * lane);
+            kv[j] = *reinterpret_cast<const uint2*>(in + kInK + t * 256 + 8 * lane);
             const float q0 = bf16_lo(qv[j].x), q1 = bf16_hi(qv[j].x), q2 = bf16_lo(qv[j].y),
                         q3 = bf16_hi(qv[j].y);
             const float k0 = bf16_lo(kv[j].x), k1 = bf16_hi(kv[j].x), k2 = bf16_lo(kv[j].y),
@@ -198,12 +255,11 @@ __device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, floa
         if (hw == 0) {
 #pragma unroll
             for (int t = 8; t < kChunk; ++t) {
-                const bool live = t < len;
                 const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
-                r0 += live ? gg.x * kLog2e : 0.f;
-                r1 += live ? gg.y * kLog2e : 0.f;
-                r2 += live ? gg.z * kLog2e : 0.f;
-                r3 += live ? gg.w * kLog2e : 0.f;
+                r0 = fmaf(gg.x, kLog2e, r0);
+                r1 = fmaf(gg.y, kLog2e, r1);
+                r2 = fmaf(gg.z, kLog2e, r2);
+                r3 = fmaf(gg.w, kLog2e, r3);
             }
         }
         gl[0] = r0;

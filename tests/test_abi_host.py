@@ -9,6 +9,8 @@ dereferenced: validation runs before the library touches the device.
 import ctypes
 import os
 import re
+import shutil
+import subprocess
 
 import pytest
 
@@ -169,3 +171,19 @@ def test_checkpoint_arguments(lib):
     assert call_ck(lib, states=A + 5 * GB) == -4                  # out
     assert call_ck(lib, states=A + 10 * GB - 1024) == -4          # the offsets
     assert call_ck(lib, B=0) == -2                                # ordinary shape checks still apply
+
+
+def test_fast_divider_matches_integer_division(tmp_path):
+    """The launch-time divider of the preparation's item decoding (a
+    multiply-high division, kda_prep_impl.cuh) against exact integer division at
+    its hardest numerators, through its host instantiation."""
+    nvcc = shutil.which("nvcc") or "/usr/local/cuda/bin/nvcc"
+    if not os.path.exists(nvcc):
+        pytest.skip("nvcc not found")
+    exe = str(tmp_path / "fastdiv_check")
+    src = os.path.join(ROOT, "tests", "fastdiv_check.cu")
+    inc = os.path.join(ROOT, "kimi_delta_attention_kda_gb300", "csrc")
+    subprocess.run([nvcc, "-std=c++17", "-O2", "-I", inc, src, "-o", exe], check=True,
+                   capture_output=True, timeout=300)
+    r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout
