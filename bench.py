@@ -12,9 +12,10 @@ H=96, T=8192 the same way.  Between timed steps a 512 MiB buffer is written
 to flush the 129 MB L2.
 
 Reported: `value` = head-tokens/s over the timed steps (device time, CUDA
-events on the launching stream); `e2e` = the same metric with the inputs
-copied host->device from pinned memory and the outputs copied back inside
-every timed step (eager calls); `roofline` for the dominant kernel (events
+events on the launching stream); `e2e` = the same metric through the host-buffer
+entry point kda_prefill_host (pinned host tensors; the library copies the
+inputs in and O and the final state out inside every timed step, overlapped
+with the computation); `roofline` for the dominant kernel (events
 recorded by the library between its kernels in a separate pass of eager
 calls) and `roofline.critical_path` (HBM, tensor and serial-chain bounds of
 the call); `cpu_baseline` = the FP64 oracle timed on this host's cores.  `--impl reference` times that oracle
@@ -80,10 +81,11 @@ PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
 SEG_SOURCES = ("kda_segments.cu", "kda_common.cuh")
 PROFILED_TRAFFIC = {
     ("transition", "t8192_h6"): (55.574e6, REC_SOURCES, "07eabcbca4f1a1df"),
-    ("chunk_prep", "t8192_h6"): (53.492e6, PREP_SOURCES, "70ed937ba7aaa41b"),
+    ("chunk_prep", "t8192_h6"): (53.496e6, PREP_SOURCES, "3e9deecd5eb41b6e"),
+    ("transition", "t65536_h1"): (75.742e6, REC_SOURCES, "07eabcbca4f1a1df"),
     ("segment_chain", "t65536_h1"): (20.306e6, SEG_SOURCES, "a574cabe1e495497"),
     ("recurrence", "t8192_h96"): (1066.769e6, REC_SOURCES, "07eabcbca4f1a1df"),
-    ("chunk_prep", "t8192_h96"): (1457.915e6, PREP_SOURCES, "70ed937ba7aaa41b"),
+    ("chunk_prep", "t8192_h96"): (1452.671e6, PREP_SOURCES, "3e9deecd5eb41b6e"),
 }
 
 
@@ -193,6 +195,7 @@ def time_kernel_steps(kda, d, steps, warmup, flush, stream, profile=False, graph
             flush.zero_()
             eager()
         stream.synchronize()
+        launches = kda._lib.last_call_launches()   # kernels one call enqueues
         if graph:
             g = torch.cuda.CUDAGraph()
             with torch.cuda.graph(g, stream=stream):
@@ -211,32 +214,27 @@ def time_kernel_steps(kda, d, steps, warmup, flush, stream, profile=False, graph
         stream.synchronize()
         prof = kda._lib.profile_end_detail() if profile else None
     ms = [s.elapsed_time(e) for s, e in zip(starts, ends)]
-    return ms, prof
+    return ms, prof, launches
 
 
 def time_e2e_steps(kda, inp, steps, warmup, flush, stream, device):
-    """Same metric through the public API with host buffers: every step copies
-    its inputs host->device (pinned) and its outputs device->host."""
+    """Same metric through the public API with host buffers: every step is one
+    kda_prefill_host call on pinned host tensors, which copies the inputs to
+    the device, computes, and copies O and the final state back (the library
+    overlaps those copies with the computation)."""
     host = {k: (None if inp[k] is None else inp[k].pin_memory())
             for k in ("q", "k", "v", "g", "beta", "init_state", "cu_seqlens")}
-    dev = {k: (None if v is None else torch.empty_like(v, device=device)) for k, v in host.items()}
     H = inp["q"].shape[2]
     N = inp["N"]
-    out_d = torch.empty_like(dev["v"])
-    fin_d = torch.empty((N, H, 128, 128), dtype=torch.bfloat16, device=device)
-    out_h = torch.empty(out_d.shape, dtype=out_d.dtype).pin_memory()
-    fin_h = torch.empty(fin_d.shape, dtype=fin_d.dtype).pin_memory()
+    out_h = torch.empty(host["v"].shape, dtype=torch.bfloat16).pin_memory()
+    fin_h = torch.empty((N, H, 128, 128), dtype=torch.bfloat16).pin_memory()
     h2d = sum(t.numel() * t.element_size() for t in host.values() if t is not None)
     d2h = out_h.numel() * 2 + fin_h.numel() * 2
 
     def step():
-        for k, t in host.items():
-            if t is not None:
-                dev[k].copy_(t, non_blocking=True)
-        kda.kda_prefill(dev["q"], dev["k"], dev["v"], dev["g"], dev["beta"], dev["init_state"],
-                        cu_seqlens=dev["cu_seqlens"], out=out_d, final_state=fin_d, stream=stream)
-        out_h.copy_(out_d, non_blocking=True)
-        fin_h.copy_(fin_d, non_blocking=True)
+        kda.kda_prefill_host(host["q"], host["k"], host["v"], host["g"], host["beta"],
+                             host["init_state"], cu_seqlens=host["cu_seqlens"], out=out_h,
+                             final_state=fin_h, stream=stream)
 
     with torch.cuda.stream(stream):
         for _ in range(warmup):
@@ -446,10 +444,10 @@ def run_ours(args):
         # between each pair of kernels adds a few microseconds per call); a
         # second, shorter pass of eager calls records them for the per-kernel
         # split, and a third times eager calls without them.
-        ms, _ = time_kernel_steps(kda, d, args.steps, args.warmup, flush, stream,
-                                  graph=bool(args.graph))
-        _, prof = time_kernel_steps(kda, d, prof_steps, 3, flush, stream, profile=True)
-        eager_ms, _ = time_kernel_steps(kda, d, prof_steps, 3, flush, stream)
+        ms, _, launches_per_call = time_kernel_steps(kda, d, args.steps, args.warmup, flush,
+                                                     stream, graph=bool(args.graph))
+        _, prof, _ = time_kernel_steps(kda, d, prof_steps, 3, flush, stream, profile=True)
+        eager_ms, _, _ = time_kernel_steps(kda, d, prof_steps, 3, flush, stream)
         e2e_ms, h2d, d2h = time_e2e_steps(kda, inp, args.steps, min(args.warmup, 3), flush, stream,
                                           device)
     torch.cuda.synchronize(device)
@@ -514,8 +512,7 @@ def run_ours(args):
                                    "events between the kernels" % prof_steps,
                    "cuda_graph": bool(args.graph)},
         "eager_us_per_call": 1e3 * sum(eager_ms) / len(eager_ms),
-        "gpu_launches": (1 if fused else 4 if segs else
-                         (3 + (1 if long_split else 0) if packed else 2)) * args.steps,
+        "gpu_launches": launches_per_call * args.steps,
         "e2e": {"value": e2e_value, "unit": UNIT, "h2d_bytes_per_step": h2d,
                 "d2h_bytes_per_step": d2h, "us_per_call": 1e3 * total_e2e / args.steps},
         "roofline": roofline,
@@ -530,9 +527,9 @@ def run_ours(args):
     if not args.no_secondary and args.workload != "t8192_h96":
         sec = synthetic.make_workload("t8192_h96")
         ds = device_inputs(sec, device)
-        ms2, _ = time_kernel_steps(kda, ds, max(10, args.steps // 10), 3, flush, stream,
+        ms2, _, _ = time_kernel_steps(kda, ds, max(10, args.steps // 10), 3, flush, stream,
                                    graph=bool(args.graph))
-        _, prof2 = time_kernel_steps(kda, ds, 10, 3, flush, stream, profile=True)
+        _, prof2, _ = time_kernel_steps(kda, ds, 10, 3, flush, stream, profile=True)
         ht2 = head_tokens(sec)
         t2 = sum(ms2) / len(ms2)
         line["secondary"] = {"workload": sec["workload"].name, "us_per_call": 1e3 * t2,

@@ -41,6 +41,7 @@ extern "C" {
 #define KDA_ERR_CUDA (-6)      /* a CUDA call (allocation, launch) failed */
 #define KDA_ERR_ARG (-7)       /* an option value is out of range */
 #define KDA_ERR_SCRATCH (-8)   /* shape too large for kda_prefill_noalloc's fixed scratch */
+#define KDA_ERR_SEQLENS (-9)   /* kda_prefill_host: the host cu_seqlens break their contract */
 
 /* Device-side status bits, reported by kda_device_status(). */
 #define KDA_DEV_BAD_SEQLENS 1  /* cu_seqlens broke its contract; out/final_state untouched */
@@ -81,6 +82,60 @@ extern "C" {
 int kda_prefill(const void* q, const void* k, const void* v, const float* g, const void* beta,
                 const void* init_state, void* out, void* final_state, int64_t B, int64_t T,
                 int64_t H, const int64_t* cu_seqlens, void* stream);
+
+/*
+ * kda_prefill on HOST buffers: the same operation, arguments and layouts as
+ * kda_prefill, except that q, k, v, g, beta, init_state, out, final_state and
+ * cu_seqlens are HOST pointers (cu_seqlens: host int64 [B + 1] or NULL).  The
+ * library copies the inputs to the device, runs the device path and copies
+ * out and final_state back, overlapping the copies with the computation: the
+ * batch is cut into at most 8 pieces, each a contiguous range of every tensor
+ * (token ranges of whole chunks for a single fixed-length sequence, groups of
+ * batch rows, or groups of whole packed sequences); while the caller's stream
+ * computes one piece, a library stream copies the next one in and another
+ * copies the previous piece's outputs back.  A single sequence cut into token
+ * ranges carries its state from piece to piece as a BF16 state, as two
+ * kda_prefill calls chained through final_state -> init_state would, so its
+ * results can differ from one device call by that rounding (within the
+ * operation's tolerance); batches cut between sequences give each sequence
+ * the results of a device call on its group.
+ *
+ * Host memory: page-locked buffers (cudaHostAlloc, cudaHostRegister, or a
+ * pinned framework tensor) let the copies run asynchronously and overlap;
+ * pageable buffers are accepted, but the driver then stages each copy and the
+ * overlap is lost (and a CUDA-graph capture of the call fails).
+ * Asynchronous on `stream`: the call returns once everything is enqueued; the
+ * inputs must stay unchanged and the outputs unread until `stream` has passed
+ * the call.  Device memory: images of every tensor, taken from the library's
+ * stream-ordered pool for the duration of the call, plus kda_prefill's
+ * workspace per piece.  The copy streams are the library's, one pair per
+ * device: calls from several host threads enqueue one after another.
+ *
+ * Returns KDA_OK, kda_prefill's argument codes (shape, NULL, overlap of the
+ * host ranges; no alignment rule), KDA_ERR_SEQLENS when the host cu_seqlens
+ * break the contract of kda_prefill (nothing is enqueued then), or
+ * KDA_ERR_CUDA when a copy or launch could not be enqueued (the copies already
+ * enqueued are joined back into `stream` before the call returns).
+ */
+int kda_prefill_host(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                     const void* init_state, void* out, void* final_state, int64_t B, int64_t T,
+                     int64_t H, const int64_t* cu_seqlens, void* stream);
+
+/*
+ * How many pieces kda_prefill_host cuts a call into: 0 (the default) chooses
+ * automatically, 1 .. 8 sets the number (fewer when the batch has fewer
+ * chunks, rows or sequences).  Process-wide, for comparing the choices;
+ * KDA_ERR_ARG for other values.
+ */
+int kda_set_host_pieces(int n);
+
+/*
+ * Number of kernels (HOST out) that the last kda_prefill, kda_prefill_checkpointed
+ * or kda_prefill_host call made on this host thread enqueued (memsets and copies
+ * are not counted; after a call that returned an error the count may include
+ * the launch that failed).
+ */
+int kda_last_call_launches(int64_t* n);
 
 /* Human-readable text for a KDA_* status code (static storage). */
 const char* kda_error_string(int status);

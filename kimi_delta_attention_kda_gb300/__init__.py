@@ -15,7 +15,7 @@ from ._lib import (KdaError, auto_split, device_status, packet_bytes, plan_fused
 
 HEAD_DIM = 128
 
-__all__ = ["kda_prefill", "prep_only", "KdaError", "device_status", "set_split", "set_engine",
+__all__ = ["kda_prefill", "kda_prefill_host", "prep_only", "KdaError", "device_status", "set_split", "set_engine",
            "set_fusion", "plan_fused", "plan_long_split", "set_segments", "plan_segments",
            "auto_split",
            "workspace_bytes", "packet_bytes", "HEAD_DIM"]
@@ -110,6 +110,56 @@ def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
     if rc != 0:
         raise KdaError(rc, "kda_prefill_checkpointed")
     return out, final_state, state_checkpoints
+
+
+def kda_prefill_host(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
+                     final_state=None, output_final_state=True, stream=None):
+    """KDA prefill on CPU (host) tensors through ``kda_prefill_host``: the
+    library copies the inputs to the current CUDA device, computes, and copies
+    ``out`` and ``final_state`` back, overlapping the copies with the work.
+    Shapes and dtypes as ``kda_prefill``; every tensor (cu_seqlens included)
+    is a contiguous CPU tensor, pinned for asynchronous, overlapped copies
+    (``tensor.pin_memory()``).  New outputs are allocated pinned.  The call is
+    asynchronous on ``stream``: synchronise it before reading the outputs.
+    Returns ``(out, final_state)``."""
+    import torch
+    _require(q.dim() == 4 and q.shape[-1] == HEAD_DIM, "q must be [B, T, H, 128]")
+    B, T, H, _ = q.shape
+    for name, t, dt in (("q", q, torch.bfloat16), ("k", k, torch.bfloat16),
+                        ("v", v, torch.bfloat16), ("g", g, torch.float32),
+                        ("beta", beta, torch.bfloat16)):
+        _require(not t.is_cuda and t.dtype == dt and t.is_contiguous(),
+                 "%s must be a contiguous %s CPU tensor" % (name, dt))
+    for name, t in (("k", k), ("v", v), ("g", g)):
+        _require(t.shape == q.shape, "%s must have the shape of q" % name)
+    _require(beta.shape == q.shape[:3], "beta must be [B, T, H]")
+    if cu_seqlens is not None:
+        _require(B == 1, "packed input needs B == 1")
+        _require(not cu_seqlens.is_cuda and cu_seqlens.dtype == torch.int64
+                 and cu_seqlens.dim() == 1 and cu_seqlens.is_contiguous(),
+                 "cu_seqlens must be a contiguous int64 CPU vector")
+        N = n_arg = cu_seqlens.numel() - 1
+    else:
+        N = n_arg = B
+    if init_state is not None:
+        _require(not init_state.is_cuda and init_state.dtype == torch.bfloat16
+                 and init_state.is_contiguous()
+                 and tuple(init_state.shape) == (N, H, HEAD_DIM, HEAD_DIM),
+                 "init_state must be a contiguous bf16 [N, H, 128, 128] CPU tensor")
+    if out is None:
+        out = torch.empty(v.shape, dtype=torch.bfloat16).pin_memory()
+    if final_state is None and output_final_state:
+        final_state = torch.empty((N, H, HEAD_DIM, HEAD_DIM), dtype=torch.bfloat16).pin_memory()
+    for name, t in (("out", out), ("final_state", final_state)):
+        if t is not None:
+            _require(not t.is_cuda and t.dtype == torch.bfloat16 and t.is_contiguous(),
+                     "%s must be a contiguous bf16 CPU tensor" % name)
+    rc = _lib.prefill_host_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                               _ptr(out), _ptr(final_state), n_arg, T, H, _ptr(cu_seqlens),
+                               _stream_handle(stream))
+    if rc != 0:
+        raise KdaError(rc, "kda_prefill_host")
+    return out, final_state
 
 
 def prep_only(q, k, g, beta, cu_seqlens=None, stream=None):

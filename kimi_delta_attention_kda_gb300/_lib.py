@@ -78,6 +78,12 @@ def load():
         lib.kda_profile_end_detail.restype = I
         lib.kda_chain_step_ns.argtypes = [ctypes.POINTER(ctypes.c_double)]
         lib.kda_chain_step_ns.restype = I
+        lib.kda_set_host_pieces.argtypes = [I]
+        lib.kda_set_host_pieces.restype = I
+        lib.kda_last_call_launches.argtypes = [ctypes.POINTER(I64)]
+        lib.kda_last_call_launches.restype = I
+        lib.kda_prefill_host.argtypes = [P] * 8 + [I64] * 3 + [P, P]
+        lib.kda_prefill_host.restype = I
         lib.kda_prefill_noalloc.argtypes = [P] * 8 + [I64] * 3 + [P, P]
         lib.kda_prefill_noalloc.restype = I
         lib.kda_noalloc_scratch_bytes.argtypes = []
@@ -103,6 +109,29 @@ def prefill_raw(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seql
     return load().kda_prefill(q or None, k or None, v or None, g or None, beta or None,
                               init_state or None, out or None, final_state or None,
                               int(B), int(T), int(H), cu_seqlens or None, stream or None)
+
+
+def set_host_pieces(n):
+    """Pieces kda_prefill_host cuts a call into (0: automatic)."""
+    rc = load().kda_set_host_pieces(int(n))
+    if rc != 0:
+        raise KdaError(rc, "kda_set_host_pieces")
+
+
+def last_call_launches():
+    """Kernels the last kda_prefill / kda_prefill_host call of this thread enqueued."""
+    n = ctypes.c_int64(0)
+    rc = load().kda_last_call_launches(ctypes.byref(n))
+    if rc != 0:
+        raise KdaError(rc, "kda_last_call_launches")
+    return n.value
+
+
+def prefill_host_raw(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens, stream):
+    """Call ``kda_prefill_host`` with integer HOST addresses (0 for NULL); returns the status."""
+    return load().kda_prefill_host(q or None, k or None, v or None, g or None, beta or None,
+                                   init_state or None, out or None, final_state or None,
+                                   int(B), int(T), int(H), cu_seqlens or None, stream or None)
 
 
 def prefill_checkpointed_raw(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,

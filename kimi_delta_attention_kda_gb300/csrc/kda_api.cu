@@ -5,6 +5,7 @@
 // recurrence) on the caller's stream.  No host <-> device synchronisation and
 // no host reads of device data happen here (flashinfer kda_prefill, "Optimized
 // Blackwell prefill subset": cu_seqlens is never inspected on the host).
+#include <algorithm>
 #include <cmath>
 #include <mutex>
 
@@ -29,15 +30,22 @@ struct DeviceState {
     // launch (long packed sequences at split 2); created on first use.
     cudaStream_t side = nullptr;
     cudaEvent_t fork = nullptr, join = nullptr;
+    // Copy streams and events of kda_prefill_host (host -> device, device ->
+    // host); created on first use.
+    cudaStream_t h2d = nullptr, d2h = nullptr;
+    cudaEvent_t h_start = nullptr, h_in = nullptr, h_done = nullptr, h_out = nullptr;
 };
 
 std::mutex g_mu;
 DeviceState g_dev[kMaxDevices];
+// Kernels enqueued by the current (or last) entry-point call of this host thread.
+thread_local int64_t t_launches = 0;
 int g_split_override = 0;
 int g_engine = 0;
 int g_fusion = 1;
 int g_segments = 1;
 int64_t g_seg_chunks = 0;   // > 0: forced segment length (kda_set_segments)
+int g_host_pieces = 0;      // > 0: kda_prefill_host cuts into at most this many pieces
 
 // Optional per-kernel timing: when active, each kda_prefill call records three
 // events on its stream (before the preparation kernels, between preparation
@@ -307,6 +315,23 @@ bool ensure_side(DeviceState* d) {
     return true;
 }
 
+// The copy streams and events of kda_prefill_host (under g_mu).
+bool ensure_host_streams(DeviceState* d) {
+    if (d->h2d) return true;
+    // Default (timing) events, as for the side stream's fork and join.
+    if (cudaStreamCreateWithFlags(&d->h2d, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaStreamCreateWithFlags(&d->d2h, cudaStreamNonBlocking) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d->h_start, cudaEventDefault) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d->h_in, cudaEventDefault) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d->h_done, cudaEventDefault) != cudaSuccess ||
+        cudaEventCreateWithFlags(&d->h_out, cudaEventDefault) != cudaSuccess) {
+        cudaGetLastError();
+        d->h2d = nullptr;
+        return false;
+    }
+    return true;
+}
+
 bool use_fusion(const Plan& pl, int64_t H, int nsplit, int sms) {
     if (!g_fusion || g_engine != 0 || pl.packed || pl.tokens <= 0) return false;
     if (!fused_supported(pl.N, H, nsplit, sms)) return false;
@@ -330,6 +355,7 @@ int run_prep(const Plan& pl, const void* q, const void* k, const float* g, const
         if (launch_varlen_meta(cu_seqlens, pl.N, pl.tokens, valid, cu_chunks, order, d->status,
                                stream) != cudaSuccess)
             return KDA_ERR_CUDA;
+        ++t_launches;
         geo.cu_seqlens = cu_seqlens;
         geo.cu_chunks = cu_chunks;
         geo.valid = valid;
@@ -337,6 +363,7 @@ int run_prep(const Plan& pl, const void* q, const void* k, const float* g, const
     }
     if (launch_prep(q, k, g, beta, packets, geo, H, kScale, d->status, stream) != cudaSuccess)
         return KDA_ERR_CUDA;
+    ++t_launches;
     *geo_out = geo;
     return KDA_OK;
 }
@@ -433,8 +460,10 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         prof_record(3, stream);
         if (rc == KDA_OK) {
             if (launch_fused(q, k, g, beta, v, out, init_state, final_state, ws + pl.meta_bytes,
-                             ready, pl.geo, H, nsplit, kScale, d->status, stream, ck) == cudaSuccess)
+                             ready, pl.geo, H, nsplit, kScale, d->status, stream, ck) == cudaSuccess) {
                 done = true;
+                ++t_launches;
+            }
             else
                 cudaGetLastError();
         }
@@ -459,6 +488,7 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
                                     sc.seg_chunks, sc.segs, seg_begin, seg_chunk0, seg_tok0, seg_seq,
                                     d->status, stream) != cudaSuccess)
                 rc = KDA_ERR_CUDA;
+            ++t_launches;
             sg.n_seqs = sc.segs;
             sg.cu_seqlens = seg_tok0;
             sg.cu_chunks = seg_chunk0;
@@ -474,6 +504,7 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         if (rc == KDA_OK &&
             launch_transition(v, packets, sg, H, zstates, maps, d->status, stream) != cudaSuccess)
             rc = KDA_ERR_CUDA;
+        ++t_launches;
         prof_record(2, stream);
         if (rc == KDA_OK && sc.groups > 0) {
             // Two levels: compose inside groups, chain over the groups, apply.
@@ -490,17 +521,21 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
                 launch_segment_apply(gs, pf, pz, starts, pl.N, sc.segs, sc.group_segs, sc.groups, H,
                                      d->status, stream) != cudaSuccess)
                 rc = KDA_ERR_CUDA;
+            t_launches += 3;
         } else if (rc == KDA_OK &&
                    launch_segment_scan(init_state, final_state, maps, zstates, starts, pl.N,
                                        sc.segs, seg_begin, pl.packed ? geo.valid : nullptr, H,
                                        d->status, stream) != cudaSuccess) {
             rc = KDA_ERR_CUDA;
+        } else {
+            ++t_launches;
         }
         prof_record(3, stream);
         if (rc == KDA_OK &&
             launch_recurrence(v, out, starts, nullptr, packets, sg, H, 1, d->status, stream, ck) !=
                 cudaSuccess)
             rc = KDA_ERR_CUDA;
+        ++t_launches;
         done = true;
     }
     if (rc == KDA_OK && !done) {
@@ -531,15 +566,240 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
                 cudaEventRecord(d->join, d->side) != cudaSuccess ||
                 cudaStreamWaitEvent(stream, d->join, 0) != cudaSuccess)
                 rc = KDA_ERR_CUDA;
+            t_launches += 2;
         } else if (rc == KDA_OK &&
                    launch_recurrence(v, out, init_state, final_state, ws + pl.meta_bytes, geo, H,
                                      nsplit, d->status, stream, ck) != cudaSuccess) {
             rc = KDA_ERR_CUDA;
+        } else if (rc == KDA_OK) {
+            ++t_launches;
         }
     }
     prof_record(4, stream);
     if (g_prof.active && g_prof.calls < g_prof.max_calls) g_prof.calls += 1;
     if (ws) cudaFreeAsync(ws, stream);
+    if (rc != KDA_OK) cudaGetLastError();
+    return rc;
+}
+
+// ---------------------------------------------------------------------------
+// kda_prefill_host: the operation on HOST buffers, with the host <-> device
+// copies overlapped with the computation.  The batch is cut into at most
+// kMaxSeqGroups pieces, each a contiguous byte range of every tensor: token
+// ranges (whole chunks) of a single fixed-length sequence, whose state passes
+// from piece to piece through a BF16 state buffer on the device (as a
+// final_state -> init_state hand-off of two calls); groups of batch rows of a
+// fixed-length batch; or groups of whole sequences of a packed batch.  The
+// library's host -> device stream copies piece p + 1 while the caller's stream
+// computes piece p with the device path, and its device -> host stream
+// returns piece p's outputs meanwhile.
+// ---------------------------------------------------------------------------
+constexpr int64_t kHostInBytesPerHT = 3 * kHeadDim * 2 + kHeadDim * 4 + 2;   // q, k, v, g, beta
+// About this many input bytes per piece (the nearest count, 1 to 8): measured
+// on GB300, fewer, larger pieces win where a piece's computation is
+// latency-bound (few heads), and up to 8 pieces where it is not (B=1,
+// T=8192: H=6 best at 3 pieces, H=96 at 6 to 8; B=1, T=65,536, H=1 at 3).
+constexpr int64_t kHostPieceBytes = int64_t(24) << 20;
+std::mutex g_host_mu;   // one kda_prefill_host enqueues on the copy streams at a time
+
+struct HostPieces {
+    int n = 1;
+    int kind = 0;                        // 0 token ranges, 1 batch rows, 2 packed sequences
+    int64_t first[kMaxSeqGroups + 1];    // bounds in tokens (kind 0), rows or sequences
+};
+
+HostPieces plan_host_pieces(const Plan& pl, int64_t T, int64_t H, const int64_t* cu) {
+    HostPieces hp;
+    const int64_t bytes = pl.tokens * H * kHostInBytesPerHT;
+    int64_t want = (bytes + kHostPieceBytes / 2) / kHostPieceBytes;
+    want = want < 1 ? 1 : (want > kMaxSeqGroups ? kMaxSeqGroups : want);
+    if (g_host_pieces > 0) want = g_host_pieces;
+    if (cu) {
+        hp.kind = 2;
+        const int64_t N = pl.N;
+        if (want > N) want = N;
+        hp.first[0] = 0;
+        for (int64_t j = 1; j < want; ++j) {
+            const int64_t target = T * j / want;
+            int64_t s = std::lower_bound(cu, cu + N + 1, target) - cu;
+            if (s < hp.first[j - 1] + 1) s = hp.first[j - 1] + 1;
+            if (s > N - (want - j)) s = N - (want - j);
+            hp.first[j] = s;
+        }
+        hp.first[want] = N;
+        hp.n = static_cast<int>(want);
+    } else if (pl.N == 1) {
+        hp.kind = 0;
+        const int64_t chunks = (T + kChunk - 1) / kChunk;
+        if (want > chunks) want = chunks > 0 ? chunks : 1;
+        const int64_t per = ((chunks + want - 1) / want) * kChunk;   // tokens per piece
+        hp.n = T > 0 ? static_cast<int>((T + per - 1) / per) : 1;
+        for (int j = 0; j <= hp.n; ++j) hp.first[j] = std::min<int64_t>(j * per, T);
+        hp.first[hp.n] = T;
+    } else {
+        hp.kind = 1;
+        if (want > pl.N) want = pl.N;
+        for (int64_t j = 0; j <= want; ++j) hp.first[j] = pl.N * j / want;
+        hp.n = static_cast<int>(want);
+    }
+    return hp;
+}
+
+// Byte offset into a host buffer that may be NULL (then nothing is copied).
+void* at(void* p, int64_t bytes) { return p ? static_cast<char*>(p) + bytes : nullptr; }
+const void* at(const void* p, int64_t bytes) {
+    return p ? static_cast<const char*>(p) + bytes : nullptr;
+}
+
+int prefill_host_impl(const void* q, const void* k, const void* v, const float* g,
+                      const void* beta, const void* init_state, void* out, void* final_state,
+                      int64_t B, int64_t T, int64_t H, const int64_t* cu, void* stream_ptr) {
+    const bool packed = cu != nullptr;
+    Plan pl;
+    int rc = make_plan(B, T, H, packed, &pl);
+    if (rc != KDA_OK) return rc;
+    if (pl.tokens > 0 && (!q || !k || !v || !g || !beta || !out)) return KDA_ERR_NULL;
+    if (packed) {
+        if (cu[0] != 0 || cu[pl.N] != T) return KDA_ERR_SEQLENS;
+        for (int64_t n = 0; n < pl.N; ++n)
+            if (cu[n + 1] < cu[n]) return KDA_ERR_SEQLENS;
+    }
+    const int64_t xb = pl.tokens * H * kHeadDim * 2, gb = pl.tokens * H * kHeadDim * 4;
+    const int64_t bb = pl.tokens * H * 2, sb = pl.N * H * kHeadDim * kHeadDim * 2;
+    {
+        const Range rq = range(q, xb), rk = range(k, xb), rv = range(v, xb), rg = range(g, gb);
+        const Range rb = range(beta, bb), ro = range(out, xb);
+        const Range ri = range(init_state, init_state ? sb : 0);
+        const Range rf = range(final_state, final_state ? sb : 0);
+        const Range rc_ = range(cu, packed ? 8 * (pl.N + 1) : 0);
+        for (Range in : {rq, rk, rv, rg, rb, ri, rf, rc_})
+            if (overlap(ro, in)) return KDA_ERR_OVERLAP;
+        for (Range in : {rq, rk, rv, rg, rb, rc_})
+            if (overlap(rf, in)) return KDA_ERR_OVERLAP;
+        if (final_state && init_state && final_state != init_state && overlap(rf, ri))
+            return KDA_ERR_OVERLAP;
+    }
+    DeviceState* d = nullptr;
+    rc = device_state(&d);
+    if (rc != KDA_OK) return rc;
+    {
+        std::lock_guard<std::mutex> lock(g_mu);
+        if (!ensure_host_streams(d)) return KDA_ERR_CUDA;
+    }
+    const HostPieces hp = plan_host_pieces(pl, T, H, cu);
+    // Device images of the tensors (one allocation, 256-byte aligned parts).
+    int64_t off = 0;
+    auto part = [&off](int64_t bytes) {
+        const int64_t at = off;
+        off += align256(bytes);
+        return at;
+    };
+    const int64_t oq = part(xb), ok_ = part(xb), ov = part(xb), og = part(gb), ob = part(bb);
+    const int64_t oo = part(xb), os = part(sb);
+    const int64_t ocu = part(packed ? 8 * (pl.N + 1) : 0);
+    const int64_t orb = part(packed ? 8 * (pl.N + hp.n) : 0);
+    cudaStream_t S = static_cast<cudaStream_t>(stream_ptr);
+    std::lock_guard<std::mutex> hold(g_host_mu);
+    uint8_t* buf = nullptr;
+    if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&buf), static_cast<size_t>(off), d->pool,
+                                S) != cudaSuccess) {
+        cudaGetLastError();
+        return KDA_ERR_CUDA;
+    }
+    auto* qd = buf + oq;
+    auto* kd = buf + ok_;
+    auto* vd = buf + ov;
+    auto* gd = reinterpret_cast<float*>(buf + og);
+    auto* bd = buf + ob;
+    auto* od = buf + oo;
+    auto* sd = buf + os;
+    auto* cud = reinterpret_cast<int64_t*>(buf + ocu);
+    auto* rbd = reinterpret_cast<int64_t*>(buf + orb);
+    const int64_t xrow = H * kHeadDim * 2, grow = H * kHeadDim * 4, brow = H * 2;
+    const int64_t srow = H * kHeadDim * kHeadDim * 2;
+
+    // One piece: nothing to overlap, so every copy goes on the caller's
+    // stream (no cross-stream hand-offs).
+    const bool one = hp.n == 1;
+    cudaStream_t in_st = one ? S : d->h2d, out_st = one ? S : d->d2h;
+    cudaError_t e = cudaSuccess;
+    if (!one) {
+        e = cudaEventRecord(d->h_start, S);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(d->h2d, d->h_start, 0);
+        if (e == cudaSuccess) e = cudaStreamWaitEvent(d->d2h, d->h_start, 0);
+    }
+    auto copy = [&e](void* dst, const void* src, int64_t n, cudaMemcpyKind kind, cudaStream_t st) {
+        if (e == cudaSuccess && n > 0) e = cudaMemcpyAsync(dst, src, static_cast<size_t>(n), kind, st);
+    };
+    const cudaMemcpyKind H2D = cudaMemcpyHostToDevice, D2H = cudaMemcpyDeviceToHost;
+    if (packed) copy(cud, cu, 8 * (pl.N + 1), H2D, in_st);
+    rc = KDA_OK;
+    for (int p = 0; p < hp.n && e == cudaSuccess && rc == KDA_OK; ++p) {
+        // Tokens [ta, tb) of the tensors and state rows [na, nb) of this piece.
+        int64_t ta, tb, na = 0, nb = 1;
+        if (hp.kind == 0) {
+            ta = hp.first[p];
+            tb = hp.first[p + 1];
+        } else if (hp.kind == 1) {
+            na = hp.first[p];
+            nb = hp.first[p + 1];
+            ta = na * T;
+            tb = nb * T;
+        } else {
+            na = hp.first[p];
+            nb = hp.first[p + 1];
+            ta = cu[na];
+            tb = cu[nb];
+        }
+        const int64_t nt = tb - ta;
+        copy(qd + ta * xrow, at(q, ta * xrow), nt * xrow, H2D, in_st);
+        copy(kd + ta * xrow, at(k, ta * xrow), nt * xrow, H2D, in_st);
+        copy(gd + ta * H * kHeadDim, at(g, ta * grow), nt * grow, H2D, in_st);
+        copy(bd + ta * brow, at(beta, ta * brow), nt * brow, H2D, in_st);
+        copy(vd + ta * xrow, at(v, ta * xrow), nt * xrow, H2D, in_st);
+        if (init_state && (hp.kind != 0 || p == 0))
+            copy(sd + na * srow, at(init_state, na * srow), (nb - na) * srow, H2D, in_st);
+        if (!one && e == cudaSuccess) e = cudaEventRecord(d->h_in, d->h2d);
+        if (!one && e == cudaSuccess) e = cudaStreamWaitEvent(S, d->h_in, 0);
+        if (e != cudaSuccess) break;
+        if (packed && p == 0) {
+            SeqGroups groups;
+            groups.n = hp.n;
+            for (int j = 0; j <= hp.n; ++j) groups.first[j] = hp.first[j];
+            e = launch_rebase_offsets(cud, groups, rbd, S);
+            if (e != cudaSuccess) break;
+            ++t_launches;
+        }
+        const void* init_p;
+        if (hp.kind == 0)
+            init_p = (p == 0 && !init_state) ? nullptr : sd;
+        else
+            init_p = init_state ? sd + na * srow : nullptr;
+        rc = prefill_impl(qd + ta * xrow, kd + ta * xrow, vd + ta * xrow, gd + ta * H * kHeadDim,
+                          bd + ta * brow, init_p, od + ta * xrow, sd + na * srow,
+                          hp.kind == 0 ? 1 : nb - na, hp.kind == 1 ? T : nt, H,
+                          packed ? rbd + na + p : nullptr, S, nullptr, nullptr);
+        if (rc != KDA_OK) break;
+        if (!one) {
+            e = cudaEventRecord(d->h_done, S);
+            if (e == cudaSuccess) e = cudaStreamWaitEvent(d->d2h, d->h_done, 0);
+        }
+        copy(at(out, ta * xrow), od + ta * xrow, nt * xrow, D2H, out_st);
+        if (final_state && hp.kind != 0)
+            copy(at(final_state, na * srow), sd + na * srow, (nb - na) * srow, D2H, out_st);
+    }
+    if (rc == KDA_OK && e == cudaSuccess && final_state && hp.kind == 0)
+        copy(final_state, sd, srow, D2H, out_st);
+    // Join both copy streams back into the caller's stream (also after an
+    // error, so that the buffer is freed only after every copy issued so far),
+    // then free the device images in stream order.
+    bool joined = one || (cudaEventRecord(d->h_in, d->h2d) == cudaSuccess &&
+                          cudaStreamWaitEvent(S, d->h_in, 0) == cudaSuccess &&
+                          cudaEventRecord(d->h_out, d->d2h) == cudaSuccess &&
+                          cudaStreamWaitEvent(S, d->h_out, 0) == cudaSuccess);
+    if (!joined && e == cudaSuccess) e = cudaErrorUnknown;
+    cudaFreeAsync(buf, S);
+    if (rc == KDA_OK && e != cudaSuccess) rc = KDA_ERR_CUDA;
     if (rc != KDA_OK) cudaGetLastError();
     return rc;
 }
@@ -551,8 +811,18 @@ extern "C" int kda_prefill(const void* q, const void* k, const void* v, const fl
                            const void* beta, const void* init_state, void* out,
                            void* final_state, int64_t B, int64_t T, int64_t H,
                            const int64_t* cu_seqlens, void* stream_ptr) {
+    t_launches = 0;
     return prefill_impl(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,
                         stream_ptr, nullptr, nullptr);
+}
+
+extern "C" int kda_prefill_host(const void* q, const void* k, const void* v, const float* g,
+                                const void* beta, const void* init_state, void* out,
+                                void* final_state, int64_t B, int64_t T, int64_t H,
+                                const int64_t* cu_seqlens, void* stream_ptr) {
+    t_launches = 0;
+    return prefill_host_impl(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,
+                             stream_ptr);
 }
 
 extern "C" int kda_prefill_checkpointed(const void* q, const void* k, const void* v,
@@ -573,6 +843,7 @@ extern "C" int kda_prefill_checkpointed(const void* q, const void* k, const void
     ck.cu_starts = checkpoint_cu_starts;
     ck.every = checkpoint_every_n_tokens / kChunk;
     ck.rows = checkpoint_rows;
+    t_launches = 0;
     return prefill_impl(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,
                         stream_ptr, &ck, checkpoint_cu_starts);
 }
@@ -609,6 +880,18 @@ extern "C" int kda_prep_only(const void* q, const void* k, const float* g, const
     return rc;
 }
 
+extern "C" int kda_set_host_pieces(int n) {
+    if (n < 0 || n > kMaxSeqGroups) return KDA_ERR_ARG;
+    g_host_pieces = n;
+    return KDA_OK;
+}
+
+extern "C" int kda_last_call_launches(int64_t* n) {
+    if (!n) return KDA_ERR_NULL;
+    *n = t_launches;
+    return KDA_OK;
+}
+
 extern "C" const char* kda_error_string(int status) {
     switch (status) {
         case KDA_OK: return "success";
@@ -621,6 +904,7 @@ extern "C" const char* kda_error_string(int status) {
         case KDA_ERR_ARG: return "an option value is out of range";
         case KDA_ERR_SCRATCH:
             return "the shape needs more scratch than the fixed no-allocation buffer holds";
+        case KDA_ERR_SEQLENS: return "host cu_seqlens break their contract";
         default: return "unknown KDA status";
     }
 }

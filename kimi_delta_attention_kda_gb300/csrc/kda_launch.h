@@ -47,6 +47,19 @@ cudaError_t launch_varlen_meta(const int64_t* cu_seqlens, int64_t n_seqs, int64_
                                int32_t* valid, int64_t* cu_chunks, int32_t* order, int* status,
                                cudaStream_t stream);
 
+// Consecutive groups of the sequences of a packed batch: group j is
+// sequences first[j] .. first[j + 1] - 1 (first[0] = 0, first[n] = N).
+constexpr int kMaxSeqGroups = 8;
+struct SeqGroups {
+    int64_t first[kMaxSeqGroups + 1];
+    int n;
+};
+// Each group's offsets rebased to zero: out[first[j] + j + i] =
+// cu_seqlens[first[j] + i] - cu_seqlens[first[j]] for i = 0 .. its sequence count
+// (N + n entries in all).
+cudaError_t launch_rebase_offsets(const int64_t* cu_seqlens, const SeqGroups& groups, int64_t* out,
+                                  cudaStream_t stream);
+
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const void* beta,
                         uint8_t* packets, const SeqGeometry& geo, int64_t H, float scale,
                         int* status, cudaStream_t stream);

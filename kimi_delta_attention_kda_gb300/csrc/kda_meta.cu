@@ -89,7 +89,24 @@ varlen_meta_kernel(const int64_t* cu, int64_t N, int64_t total, int32_t* valid,
     }
 }
 
+// Group j of a packed batch (sequences first[j] .. first[j + 1] - 1) gets its
+// offsets rebased to start at zero, at out[first[j] + j ..
+// first[j + 1] + j]: a packed batch of its own over the group's tokens.
+__global__ void rebase_offsets_kernel(const int64_t* cu, SeqGroups groups, int64_t* out) {
+    const int j = blockIdx.x;
+    const int64_t s0 = groups.first[j], s1 = groups.first[j + 1];
+    const int64_t base = cu[s0];
+    for (int64_t i = threadIdx.x; i <= s1 - s0; i += blockDim.x) out[s0 + j + i] = cu[s0 + i] - base;
+}
+
 }  // namespace
+
+cudaError_t launch_rebase_offsets(const int64_t* cu_seqlens, const SeqGroups& groups, int64_t* out,
+                                  cudaStream_t stream) {
+    if (groups.n < 1 || groups.n > kMaxSeqGroups) return cudaErrorInvalidValue;
+    rebase_offsets_kernel<<<groups.n, 256, 0, stream>>>(cu_seqlens, groups, out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_varlen_meta(const int64_t* cu_seqlens, int64_t n_seqs, int64_t total_tokens,
                                int32_t* valid, int64_t* cu_chunks, int32_t* order, int* status,

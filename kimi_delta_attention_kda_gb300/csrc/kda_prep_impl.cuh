@@ -116,6 +116,18 @@ __device__ __forceinline__ int64_t find_sequence(const int64_t* cu_chunks, int64
 
 constexpr float kLog2e = 1.4426950408889634f;
 
+// (acc0, acc1) += (x0, x1) * (y0, y1) as one packed FP32x2 fused multiply-add
+// (each lane rounded as fmaf).
+__device__ __forceinline__ void fma2(float& acc0, float& acc1, float x0, float x1, float y0,
+                                     float y1) {
+    uint64_t a, x, y;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(a) : "f"(acc0), "f"(acc1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(x) : "f"(x0), "f"(x1));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(y) : "f"(y0), "f"(y1));
+    asm("fma.rn.f32x2 %0, %1, %2, %0;" : "+l"(a) : "l"(x), "l"(y));
+    asm("mov.b64 {%0, %1}, %2;" : "=f"(acc0), "=f"(acc1) : "l"(a));
+}
+
 // 2^x by the hardware's approximate base-2 exponential (relative error about
 // 2^-22 over the range used here, |x| <= 16 * 5 * log2(e)).
 __device__ __forceinline__ float ex2_approx(float x) {
@@ -225,20 +237,16 @@ __device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, floa
 #pragma unroll
             for (int t = 0; t < 8; ++t) {
                 const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
-                r0 = fmaf(gg.x, kLog2e, r0);
-                r1 = fmaf(gg.y, kLog2e, r1);
-                r2 = fmaf(gg.z, kLog2e, r2);
-                r3 = fmaf(gg.w, kLog2e, r3);
+                fma2(r0, r1, gg.x, gg.y, kLog2e, kLog2e);
+                fma2(r2, r3, gg.z, gg.w, kLog2e, kLog2e);
             }
         }
 #pragma unroll
         for (int j = 0; j < 8; ++j) {
             const int t = tb + j;
             const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
-            r0 = fmaf(gg.x, kLog2e, r0);
-            r1 = fmaf(gg.y, kLog2e, r1);
-            r2 = fmaf(gg.z, kLog2e, r2);
-            r3 = fmaf(gg.w, kLog2e, r3);
+            fma2(r0, r1, gg.x, gg.y, kLog2e, kLog2e);
+            fma2(r2, r3, gg.z, gg.w, kLog2e, kLog2e);
             G[j][0] = r0;
             G[j][1] = r1;
             G[j][2] = r2;
@@ -256,10 +264,8 @@ __device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, floa
 #pragma unroll
             for (int t = 8; t < kChunk; ++t) {
                 const float4 gg = *reinterpret_cast<const float4*>(in + kInG + t * 512 + 16 * lane);
-                r0 = fmaf(gg.x, kLog2e, r0);
-                r1 = fmaf(gg.y, kLog2e, r1);
-                r2 = fmaf(gg.z, kLog2e, r2);
-                r3 = fmaf(gg.w, kLog2e, r3);
+                fma2(r0, r1, gg.x, gg.y, kLog2e, kLog2e);
+                fma2(r2, r3, gg.z, gg.w, kLog2e, kLog2e);
             }
         }
         gl[0] = r0;

@@ -45,7 +45,7 @@ def test_library_exports_every_declared_symbol(lib):
 
 
 def test_error_strings(lib):
-    for code in range(0, -8, -1):
+    for code in range(0, -10, -1):
         s = lib.kda_error_string(code).decode()
         assert s and s != "unknown KDA status"
     assert lib.kda_error_string(-99).decode() == "unknown KDA status"
@@ -187,3 +187,29 @@ def test_fast_divider_matches_integer_division(tmp_path):
                    capture_output=True, timeout=300)
     r = subprocess.run([exe], capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == "ok", r.stdout
+
+
+def call_host(lib, cu=None, B=1, T=16, H=1, q=A, out=A + 5 * GB, final=0, init=0):
+    """kda_prefill_host with fake host addresses (never dereferenced before
+    the device query) and, for the packed layout, a real host offsets array."""
+    import numpy as np
+    cu_arr = None if cu is None else np.ascontiguousarray(np.asarray(cu, dtype=np.int64))
+    cu_ptr = 0 if cu_arr is None else cu_arr.ctypes.data
+    return _lib.prefill_host_raw(q, A + GB, A + 2 * GB, A + 3 * GB, A + 4 * GB, init, out, final,
+                                 B, T, H, cu_ptr, 0)
+
+
+def test_host_entry_checks_offsets_on_the_host(lib):
+    """kda_prefill_host reads its HOST cu_seqlens before anything else and
+    refuses a broken contract with KDA_ERR_SEQLENS (-9)."""
+    assert call_host(lib, cu=[1, 16], B=1, T=16) == -9        # cu[0] != 0
+    assert call_host(lib, cu=[0, 32, 16], B=2, T=16) == -9    # decreasing
+    assert call_host(lib, cu=[0, 16, 40], B=2, T=48) == -9    # cu[N] != T
+    assert call_host(lib, B=0) == -2
+    assert call_host(lib, q=0) == -1
+    assert call_host(lib, out=A + 64) == -4                   # host out overlaps host q
+    import torch
+    if not torch.cuda.is_available():
+        # valid arguments (no alignment rule for host buffers) reach the device query
+        assert call_host(lib, cu=[0, 0, 16, 48], B=3, T=48) == -5
+        assert call_host(lib, q=A + 2) == -5
