@@ -79,6 +79,7 @@ STATE_BYTES = 128 * 128 * 2
 REC_SOURCES = ("kda_recurrence.cu", "kda_rec_impl.cuh", "kda_common.cuh")
 PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
 SEG_SOURCES = ("kda_segments.cu", "kda_common.cuh")
+FUSED_SOURCES = ("kda_fused.cu", "kda_prep_impl.cuh", "kda_rec_impl.cuh", "kda_common.cuh")
 PROFILED_TRAFFIC = {
     ("transition", "t8192_h6"): (55.574e6, REC_SOURCES, "07eabcbca4f1a1df"),
     ("chunk_prep", "t8192_h6"): (53.496e6, PREP_SOURCES, "3e9deecd5eb41b6e"),
@@ -86,6 +87,8 @@ PROFILED_TRAFFIC = {
     ("segment_chain", "t65536_h1"): (20.306e6, SEG_SOURCES, "a574cabe1e495497"),
     ("recurrence", "t8192_h96"): (1066.769e6, REC_SOURCES, "07eabcbca4f1a1df"),
     ("chunk_prep", "t8192_h96"): (1452.671e6, PREP_SOURCES, "3e9deecd5eb41b6e"),
+    ("recurrence", "varlen8_h12"): (380.516e6, REC_SOURCES, "07eabcbca4f1a1df"),
+    ("fused", "t256_h1"): (0.390e6, FUSED_SOURCES, "ef37c449dd467f86"),
 }
 
 
