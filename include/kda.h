@@ -109,7 +109,10 @@ int kda_prefill(const void* q, const void* k, const void* v, const float* g, con
  * the call.  Device memory: images of every tensor, taken from the library's
  * stream-ordered pool for the duration of the call, plus kda_prefill's
  * workspace per piece.  The copy streams are the library's, one pair per
- * device: calls from several host threads enqueue one after another.
+ * device: calls from several host threads enqueue one after another, and
+ * while a CUDA-graph capture that contains a kda_prefill_host call is open,
+ * those streams belong to it: no other thread may call kda_prefill_host on
+ * the device until the capture ends.
  *
  * Returns KDA_OK, kda_prefill's argument codes (shape, NULL, overlap of the
  * host ranges; no alignment rule), KDA_ERR_SEQLENS when the host cu_seqlens
