@@ -598,8 +598,8 @@ constexpr int64_t kHostInBytesPerHT = 3 * kHeadDim * 2 + kHeadDim * 4 + 2;   // 
 // About this many input bytes per piece (the nearest count, 1 to 8): measured
 // on GB300, fewer, larger pieces win where a piece's computation is
 // latency-bound (few heads), and up to 8 pieces where it is not (B=1,
-// T=8192: H=6 best at 3 pieces, H=96 at 6 to 8; B=1, T=65,536, H=1 at 3).
-constexpr int64_t kHostPieceBytes = int64_t(24) << 20;
+// T=8192: H=6 best at 2 pieces, H=96 at 6 to 8; B=1, T=65,536, H=1 at 2).
+constexpr int64_t kHostPieceBytes = int64_t(40) << 20;
 std::mutex g_host_mu;   // one kda_prefill_host enqueues on the copy streams at a time
 
 struct HostPieces {
@@ -632,9 +632,16 @@ HostPieces plan_host_pieces(const Plan& pl, int64_t T, int64_t H, const int64_t*
         hp.kind = 0;
         const int64_t chunks = (T + kChunk - 1) / kChunk;
         if (want > chunks) want = chunks > 0 ? chunks : 1;
-        const int64_t per = ((chunks + want - 1) / want) * kChunk;   // tokens per piece
-        hp.n = T > 0 ? static_cast<int>((T + per - 1) / per) : 1;
-        for (int j = 0; j <= hp.n; ++j) hp.first[j] = std::min<int64_t>(j * per, T);
+        // The last piece's call and outbound copy are not overlapped with
+        // anything, so it gets about half the chunks of the others.
+        const int64_t per = want > 1 ? (2 * chunks + 2 * want - 2) / (2 * want - 1) : chunks;
+        hp.n = 0;
+        hp.first[0] = 0;
+        for (int64_t c = 0; c < chunks && hp.n < want; ++hp.n) {
+            c = hp.n + 1 == want ? chunks : std::min(chunks, c + per);
+            hp.first[hp.n + 1] = std::min<int64_t>(c * kChunk, T);
+        }
+        if (hp.n == 0) hp.n = 1;
         hp.first[hp.n] = T;
     } else {
         hp.kind = 1;
