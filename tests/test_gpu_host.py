@@ -88,7 +88,7 @@ def test_host_matches_oracle_and_device(kda, pieces, case):
 
 
 def test_host_full_workload(kda):
-    """B=1, T=8192, H=6 (automatic: three token ranges) through the host path,
+    """B=1, T=8192, H=6 (automatic: two token ranges) through the host path,
     against the device call (all heads) and the oracle (head 0)."""
     inp = synthetic.make_workload("t8192_h6")
     out, fin = _host(kda, inp)
