@@ -124,6 +124,7 @@ bool overlap(Range a, Range b) {
     return a.lo < b.hi && b.lo < a.hi;
 }
 
+
 int choose_split(int64_t units, int sms) {
     if (g_split_override) return g_split_override;
     // The widest split whose grid still fits on the SMs: with few heads the
@@ -300,6 +301,35 @@ SegChoice plan_segments(const Plan& pl, int64_t H, int sms, bool checkpoints) {
     return sc;
 }
 
+// Whether the outputs of a call stay clear of its inputs and of each other
+// (final_state == init_state, the in-place update, is allowed): the byte
+// ranges of the tensors of `pl` with H heads, device or host alike.
+bool io_disjoint(const Plan& pl, int64_t H, const void* q, const void* k, const void* v,
+                 const void* g, const void* beta, const void* init_state, const void* out,
+                 const void* final_state, const void* cu_seqlens, const Checkpoints* ck,
+                 const void* ck_cu_starts) {
+    const int64_t x_bytes = pl.tokens * H * kHeadDim * 2;
+    const int64_t s_bytes = pl.N * H * kHeadDim * kHeadDim * 2;
+    const Range rq = range(q, x_bytes), rk = range(k, x_bytes), rv = range(v, x_bytes);
+    const Range rg = range(g, pl.tokens * H * kHeadDim * 4), rb = range(beta, pl.tokens * H * 2);
+    const Range ro = range(out, x_bytes);
+    const Range ri = range(init_state, init_state ? s_bytes : 0);
+    const Range rf = range(final_state, final_state ? s_bytes : 0);
+    const Range rc = range(cu_seqlens, cu_seqlens ? 8 * (pl.N + 1) : 0);
+    for (Range in : {rq, rk, rv, rg, rb, ri, rf, rc})
+        if (overlap(ro, in)) return false;
+    for (Range in : {rq, rk, rv, rg, rb, rc})
+        if (overlap(rf, in)) return false;
+    if (final_state && init_state && final_state != init_state && overlap(rf, ri)) return false;
+    if (ck) {
+        const Range rs = range(ck->states, ck->rows * H * kHeadDim * kHeadDim * 2);
+        const Range rcs = range(ck_cu_starts, 8 * (pl.N + 1));
+        for (Range in : {rq, rk, rv, rg, rb, ro, ri, rf, rc, rcs})
+            if (overlap(rs, in)) return false;
+    }
+    return true;
+}
+
 // The side stream and events of device state d (under g_mu).
 bool ensure_side(DeviceState* d) {
     if (d->side) return true;
@@ -406,26 +436,9 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         (final_state && !aligned(final_state, 16)) || (cu_seqlens && !aligned(cu_seqlens, 8)))
         return KDA_ERR_ALIGN;
 
-    const int64_t x_bytes = pl.tokens * H * kHeadDim * 2;
-    const int64_t s_bytes = pl.N * H * kHeadDim * kHeadDim * 2;
-    const Range rq = range(q, x_bytes), rk = range(k, x_bytes), rv = range(v, x_bytes);
-    const Range rg = range(g, pl.tokens * H * kHeadDim * 4), rb = range(beta, pl.tokens * H * 2);
-    const Range ro = range(out, x_bytes);
-    const Range ri = range(init_state, init_state ? s_bytes : 0);
-    const Range rf = range(final_state, final_state ? s_bytes : 0);
-    const Range rc_ = range(cu_seqlens, cu_seqlens ? 8 * (pl.N + 1) : 0);
-    for (Range in : {rq, rk, rv, rg, rb, ri, rf, rc_})
-        if (overlap(ro, in)) return KDA_ERR_OVERLAP;
-    for (Range in : {rq, rk, rv, rg, rb, rc_})
-        if (overlap(rf, in)) return KDA_ERR_OVERLAP;
-    if (final_state && init_state && final_state != init_state && overlap(rf, ri))
+    if (!io_disjoint(pl, H, q, k, v, g, beta, init_state, out, final_state, cu_seqlens, ck,
+                     ck_cu_starts))
         return KDA_ERR_OVERLAP;
-    if (ck) {
-        const Range rs = range(ck->states, ck->rows * H * kHeadDim * kHeadDim * 2);
-        const Range rcs = range(ck_cu_starts, 8 * (pl.N + 1));
-        for (Range in : {rq, rk, rv, rg, rb, ro, ri, rf, rc_, rcs})
-            if (overlap(rs, in)) return KDA_ERR_OVERLAP;
-    }
 
     DeviceState* d = nullptr;
     rc = device_state(&d);
@@ -673,19 +686,8 @@ int prefill_host_impl(const void* q, const void* k, const void* v, const float* 
     }
     const int64_t xb = pl.tokens * H * kHeadDim * 2, gb = pl.tokens * H * kHeadDim * 4;
     const int64_t bb = pl.tokens * H * 2, sb = pl.N * H * kHeadDim * kHeadDim * 2;
-    {
-        const Range rq = range(q, xb), rk = range(k, xb), rv = range(v, xb), rg = range(g, gb);
-        const Range rb = range(beta, bb), ro = range(out, xb);
-        const Range ri = range(init_state, init_state ? sb : 0);
-        const Range rf = range(final_state, final_state ? sb : 0);
-        const Range rc_ = range(cu, packed ? 8 * (pl.N + 1) : 0);
-        for (Range in : {rq, rk, rv, rg, rb, ri, rf, rc_})
-            if (overlap(ro, in)) return KDA_ERR_OVERLAP;
-        for (Range in : {rq, rk, rv, rg, rb, rc_})
-            if (overlap(rf, in)) return KDA_ERR_OVERLAP;
-        if (final_state && init_state && final_state != init_state && overlap(rf, ri))
-            return KDA_ERR_OVERLAP;
-    }
+    if (!io_disjoint(pl, H, q, k, v, g, beta, init_state, out, final_state, cu, nullptr, nullptr))
+        return KDA_ERR_OVERLAP;
     DeviceState* d = nullptr;
     rc = device_state(&d);
     if (rc != KDA_OK) return rc;
