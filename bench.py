@@ -51,7 +51,7 @@ FLASHKDA_B200_US = {"t8192_h6": 731.7, "t8192_h96": 1032.6}
 COLUMN_SPLIT_B200_US = {"t8192_h6": 283.4, "t8192_h96": 914.7}
 L2_FLUSH_BYTES = 512 << 20
 
-# Algorithmic bytes per head-token of each kernel (see DESIGN.md):
+# Algorithmic bytes per head-token of each kernel:
 #   preparation: reads q, k (2 x 256 B), g (512 B), beta (2 B); writes one
 #                13,824-byte packet per 16 tokens (864 B per head-token).
 #   recurrence:  reads the packets (864 B) and v (256 B); writes O (256 B);
