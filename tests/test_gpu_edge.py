@@ -83,3 +83,19 @@ def test_packed_sub_chunk_sequences(kda):
                                 lengths=[1, 15, 7, 0, 3, 16, 9, 2, 11, 5])
     out, fin = run(kda, inp)
     tu.check_against_oracle(inp, out, fin)
+
+
+@pytest.mark.parametrize("T", [16, 500])
+def test_read_back_closed_form(kda, T):
+    """No decay (g = 0), beta = 1 and q = k: after token t's write
+    S khat_t = v_t exactly (khat has unit norm), so o_t = s v_t whatever the
+    initial state: a closed form that needs no oracle."""
+    inp = synthetic.make_inputs(1, T, 2, 9930 + T, init_std=0.5)
+    inp["q"] = inp["k"].clone()
+    inp["g"] = torch.zeros_like(inp["g"])
+    inp["beta"] = torch.ones_like(inp["beta"])
+    out, fin = run(kda, inp)
+    ref = inp["v"].double().numpy()[0] / np.sqrt(128.0)             # [T, H, 128]
+    got = out.double().numpy()[0]
+    tu.assert_within_tolerance(got, ref, 1, "O against s v")
+    tu.check_against_oracle(inp, out, fin)
