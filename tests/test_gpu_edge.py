@@ -72,8 +72,11 @@ def test_multi_wave_fixed_batch(kda):
     tu.check_against_oracle(inp, out, fin)
 
 
-def test_many_heads_few_tokens(kda):
-    inp = synthetic.make_inputs(1, 33, 160, 9910, init_std=0.02)
+@pytest.mark.parametrize("B,T,H", [(1, 33, 160), (2, 48, 512)])
+def test_many_heads_few_tokens(kda, B, T, H):
+    """Recurrence grids of several waves (up to 1,024 CTAs) and preparation
+    grids with more items than pairs."""
+    inp = synthetic.make_inputs(B, T, H, 9910 + H, init_std=0.02)
     out, fin = run(kda, inp)
     tu.check_against_oracle(inp, out, fin)
 
