@@ -240,8 +240,9 @@ int kda_plan_long_split(int64_t n_seqs, int64_t T, int64_t H, int64_t* k);
  * Whether kda_prefill may use the segmented scan over chunks (1, the default)
  * or always runs each (sequence, head) as one serial chain of chunk steps (0).
  * The chunkwise state update is affine in the incoming state, so over a run
- * of chunks it is S -> S F + Z ("Kimi Linear" technical report, chunkwise
- * KDA: S_{c+1} = S_c D_c + U_c K^end_c with U_c affine in S_c).  When there
+ * of chunks it is S -> S F + Z (the chunk equations of "FlashKDA column
+ * split", section 1: S_{c+1} = S_c D_{0:15} + U_c K^end_c with
+ * U_c = (V_c - S_c K^start_c) B_c (A^kk_c)^T affine in S_c).  When there
  * are too few (sequence, head) chains to fill the GPU (engine 0, automatic
  * split; fixed or packed layout; with or without checkpoints, which the last
  * pass writes), each sequence is cut into
@@ -333,8 +334,13 @@ int kda_chain_step_ns(double* ns);
  * allocations on their hot path, or processes that have already handed out
  * nearly all HBM.
  *
- * Arguments, results, alignment and overlap rules and error codes are those
- * of kda_prefill; the caller still passes every input and output.  The
+ * Arguments, alignment and overlap rules and error codes are those of
+ * kda_prefill; the caller still passes every input and output.  It runs the
+ * plain plan -- the preparation kernel, then one recurrence launch at the
+ * split kda_prefill would pick (kda_set_split and kda_set_engine apply) --
+ * and never the one-launch form, the segmented scan or the longest-first
+ * scheduling of packed sequences, so its results agree with kda_prefill's
+ * within the operation's tolerance, not bit for bit.  The
  * scratch kda_prefill would take from its pool lives instead in one fixed
  * device array of kda_noalloc_scratch_bytes() bytes (48 MiB) inside this
  * library, which every GPU that loads the library holds until the process

@@ -150,6 +150,9 @@ struct Plan {
 
 int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
     if (B < 1 || T < 0 || H < 1) return KDA_ERR_SHAPE;
+    // H first: every bound below divides by a multiple of H, which must not
+    // overflow (H * 128 * 128 wraps to 0 for H = 2^50).
+    if (H > kMaxElems / (kHeadDim * kHeadDim)) return KDA_ERR_SHAPE;
     p->packed = packed;
     p->N = B;
     p->tokens = packed ? T : B * T;
@@ -846,7 +849,8 @@ extern "C" int kda_prefill_checkpointed(const void* q, const void* k, const void
         return KDA_ERR_ARG;
     if (!checkpoint_cu_starts || !state_checkpoints) return KDA_ERR_NULL;
     if (!aligned(state_checkpoints, 16) || !aligned(checkpoint_cu_starts, 8)) return KDA_ERR_ALIGN;
-    if (H > 0 && checkpoint_rows > kMaxElems / (H * kHeadDim * kHeadDim)) return KDA_ERR_SHAPE;
+    if (H < 1 || H > kMaxElems / (kHeadDim * kHeadDim)) return KDA_ERR_SHAPE;
+    if (checkpoint_rows > kMaxElems / (H * kHeadDim * kHeadDim)) return KDA_ERR_SHAPE;
     Checkpoints ck;
     ck.states = static_cast<__nv_bfloat16*>(state_checkpoints);
     ck.cu_starts = checkpoint_cu_starts;

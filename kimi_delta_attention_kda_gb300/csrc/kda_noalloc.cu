@@ -9,8 +9,16 @@
 // processes that have already given nearly all HBM away.  This entry point
 // serves them: its scratch is a fixed array in this file, created when the
 // library's device code is loaded, so a call never allocates or frees
-// anything.  The operation, its arguments and its results are those of
-// kda_prefill (the same kernels run); only where the scratch lives differs.
+// anything.  The operation and its arguments are those of kda_prefill, but
+// the launch plan is the plain one: the preparation kernel, then one
+// recurrence launch at the split kda_prefill would pick (kda_set_split and
+// kda_set_engine apply).  It never takes kda_prefill's other plans -- the
+// one-launch form, the segmented scan, the longest-first order of packed
+// sequences or their concurrent split-2 launch -- whose extra buffers would
+// not fit the fixed scratch, so its results agree with kda_prefill's within
+// the operation's tolerance rather than bit for bit, and its speed on shapes
+// that kda_prefill segments (few heads, long sequences) is that of the serial
+// chain.
 #include <mutex>
 
 #include "../../include/kda.h"
@@ -80,6 +88,7 @@ extern "C" int kda_prefill_noalloc(const void* q, const void* k, const void* v, 
     constexpr int64_t kMaxElems = int64_t(1) << 56;
     const bool packed = cu_seqlens != nullptr;
     if (B < 1 || T < 0 || H < 1) return KDA_ERR_SHAPE;
+    if (H > kMaxElems / (kHeadDim * kHeadDim)) return KDA_ERR_SHAPE;   // before dividing by H
     if (!packed && T > 0 && B > kMaxElems / T) return KDA_ERR_SHAPE;
     const int64_t tokens = packed ? T : B * T;
     if (tokens > kMaxElems / (H * kHeadDim) || B > kMaxElems / (H * kHeadDim * kHeadDim))

@@ -1,9 +1,10 @@
 // kda_segments.cu -- the middle pass of the segmented scan over chunks.
 //
-// The chunkwise recurrence ("Kimi Linear" technical report, section on the
-// chunkwise KDA algorithm) maps the state of one chunk to the next by
-//     S_{c+1} = S_c D_c + U_c K^end_c,   U_c = V_c (A^kk B)^T + S_c K'_c^T,
-// which is affine in S_c.  Over a segment of consecutive chunks the map is
+// The chunk equations of "FlashKDA column split", section 1, map the state of
+// one chunk to the next by
+//     S_{c+1} = S_c D_{0:15} + U_c K^end_c,   U_c = V_c (A^kk B)^T + S_c K'_c^T
+// (U_c = (V_c - S_c K^start_c) B_c (A^kk_c)^T with K' = -(A^kk B) K^start^T),
+// which is affine in S_c: S_{c+1} = S_c (D_{0:15} + K'^T K^end) + V_c (A^kk B)^T K^end.  Over a segment of consecutive chunks the map is
 // therefore S -> S F + Z, with F the state the segment's chunks lead to from
 // the identity with V taken as zero and Z the state they lead to from zero.
 // The first pass (launch_transition) forms F and Z for every segment at

@@ -213,3 +213,56 @@ def test_host_entry_checks_offsets_on_the_host(lib):
         # valid arguments (no alignment rule for host buffers) reach the device query
         assert call_host(lib, cu=[0, 0, 16, 48], B=3, T=48) == -5
         assert call_host(lib, q=A + 2) == -5
+
+
+def test_huge_head_count_is_a_shape_error_not_a_crash(lib):
+    """With no tokens and H = 2^50, H * 128 * 128 wraps to zero in 64 bits; every
+    entry point must refuse the shape (KDA_ERR_SHAPE) before dividing by it."""
+    H = 1 << 50
+    assert call(lib, T=0, H=H) == -2
+    assert call(lib, T=0, H=H, cu=A + 7 * GB) == -2
+    assert call_ck(lib, T=0, H=H) == -2
+    assert call_host(lib, T=0, H=H) == -2
+    assert _lib.prefill_noalloc_raw(A, A + GB, A + 2 * GB, A + 3 * GB, A + 4 * GB, 0,
+                                    A + 5 * GB, 0, 1, 0, H, 0, 0) == -2
+    assert _lib.prep_only_raw(A, A + GB, A + 3 * GB, A + 4 * GB, 1, 0, H, 0, A + 5 * GB,
+                              1 << 40, 0) == -2
+    n = ctypes.c_int64(0)
+    flag = ctypes.c_int(0)
+    assert lib.kda_workspace_bytes(1, 0, H, 0, ctypes.byref(n)) == -2
+    assert lib.kda_plan_segments(1, 0, H, 0, ctypes.byref(n)) == -2
+    assert lib.kda_plan_fused(1, 0, H, 0, ctypes.byref(flag)) == -2
+    assert lib.kda_plan_long_split(1, 0, H, ctypes.byref(n)) == -2
+
+
+def call_noalloc(lib, B=1, T=16, H=1, cu=0):
+    return _lib.prefill_noalloc_raw(A, A + GB, A + 2 * GB, A + 3 * GB, A + 4 * GB, 0,
+                                    A + 5 * GB, 0, B, T, H, cu, 0)
+
+
+def test_noalloc_scratch_boundary(lib):
+    """kda_prefill_noalloc's fixed 48 MiB scratch holds 3,640 packets of 13,824
+    bytes plus 12,288 bytes.  The refusal (KDA_ERR_SCRATCH) is decided on the
+    host before any device work; a shape that fits goes on to the device
+    query (KDA_ERR_DEVICE here, with no GPU)."""
+    import torch
+    if torch.cuda.is_available():
+        pytest.skip("a GPU is present: shapes that fit would launch on fake pointers")
+    cap = 48 << 20
+    assert _lib.noalloc_scratch_bytes() == cap
+    assert cap // 13824 == 3640 and cap - 3640 * 13824 == 12288
+    # fixed layout: 3,640 chunks of one head fit exactly, one more does not
+    assert call_noalloc(lib, T=3640 * 16) == -5
+    assert call_noalloc(lib, T=3640 * 16 + 1) == -8
+    assert call_noalloc(lib, T=1820 * 16, H=2) == -5
+    assert call_noalloc(lib, T=1820 * 16 + 1, H=2) == -8
+    # packed: chunk bound (T + 15 N) // 16 and 256 + ceil(8 (N + 1) / 256) * 256
+    # bytes of metadata.  N = 1503 sequences: 3,640 packets + 12,288 bytes of
+    # metadata fill the array to the byte; N = 1504: the packets still fit but
+    # the metadata (12,544 bytes) does not.
+    def need(N, T):
+        return 256 + -(-8 * (N + 1) // 256) * 256 + (T + 15 * N) // 16 * 13824
+    assert need(1503, 35695) == cap
+    assert call_noalloc(lib, B=1503, T=35695, cu=A + 7 * GB) == -5
+    assert (35695 + 15 * 1504) // 16 * 13824 <= cap < need(1504, 35695)
+    assert call_noalloc(lib, B=1504, T=35695, cu=A + 7 * GB) == -8

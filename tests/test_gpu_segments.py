@@ -1,8 +1,9 @@
 """The segmented scan over chunks (kda_set_segments): each sequence cut into
 segments, every segment's zero-start state and state map formed at once, a
 short chain over the segments, and every segment rerun from its incoming
-state.  The chunkwise update is affine in the incoming state ("Kimi Linear"
-technical report, chunkwise KDA), so the results must match the FP64 oracle
+state.  The chunk update of "FlashKDA column split", section 1, is affine in
+the incoming state (U_c is affine in S_c, and S_{c+1} = S_c D_{0:15} + U_c
+K^end_c), so the results must match the FP64 oracle
 within the same tolerance as the serial chain, and the serial chain itself to
 rounding.  Forced segment lengths exercise ragged tails, one-segment
 sequences and several sequences; the long-memory stress families check that

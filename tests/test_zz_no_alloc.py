@@ -4,10 +4,11 @@ path where driver allocations are forbidden).  It runs the same operation as
 kda_prefill with its scratch in a fixed array inside the library.
 
 These tests call it through the C ABI and compare it with kda_prefill on the
-same inputs, within the tolerance of the other GPU tests (per sequence and
-head: rel-Frobenius <= 1e-2, max-abs <= 3e-2), over two calls in a row with
-different shapes, so that what the first call leaves in the shared scratch
-cannot leak into the second.  This file is collected last.
+same inputs, and both with the FP64 oracle, within the tolerance of the other
+GPU tests (per sequence and head: rel-Frobenius <= 1e-2, max-abs <= 3e-2),
+over two calls in a row with different shapes, so that what the first call
+leaves in the shared scratch cannot leak into the second.  This file is
+collected last.
 """
 
 import pytest
@@ -79,6 +80,9 @@ def test_noalloc_matches_prefill_on_two_calls_in_a_row(lib):
     ref2 = _run(_lib.prefill_raw, second)
     _compare(first, got1, ref1)
     _compare(second, got2, ref2)
+    # Both calls against the FP64 oracle as well (every head of both shapes).
+    tu.check_against_oracle(first, *got1)
+    tu.check_against_oracle(second, *got2)
 
 
 def test_noalloc_refuses_shapes_beyond_its_scratch(lib):
