@@ -19,6 +19,8 @@ Functions (see ``kda_oracle.c`` for the equations and their sources):
 * ``chunk_intermediates`` -- per-chunk K^start, Q^start, K^end, D_{0:C-1},
   A^kk and A^qk.
 * ``unitri_inverse`` -- (I + L)^{-1} alone.
+* ``sigmoid`` -- beta from a logit (flashinfer kda_prefill, beta_is_logit);
+  ``kda_token`` and ``kda_chunk`` apply it with ``beta_is_logit=True``.
 
 Conventions: q, k, g are ``[B, T, H, dk]``, v is ``[B, T, H, dv]``, beta is
 ``[B, T, H]``, states are ``[N, H, dv, dk]`` (rows = value channels).  Packed
@@ -72,6 +74,8 @@ def _bind(path):
     lib.kda_oracle_chunk_intermediates.restype = I
     lib.kda_oracle_unitri_inverse.argtypes = [P, P, I64, I]
     lib.kda_oracle_unitri_inverse.restype = I
+    lib.kda_oracle_sigmoid.argtypes = [P, P, I64]
+    lib.kda_oracle_sigmoid.restype = I
     lib.kda_oracle_num_threads.argtypes = []
     lib.kda_oracle_num_threads.restype = I
     return lib
@@ -103,6 +107,9 @@ class Variant:
 
     def unitri_inverse(self, *a, **kw):
         return unitri_inverse(*a, _lib=self._lib, **kw)
+
+    def sigmoid(self, *a, **kw):
+        return sigmoid(*a, _lib=self._lib, **kw)
 
 
 def num_threads() -> int:
@@ -141,10 +148,14 @@ def _check(rc, name):
 
 
 def kda_token(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=None,
-              eps=L2NORM_EPS, l2norm=True, want_final=True, _lib=None):
-    """Per-token recurrence; returns ``(out [B,T,H,dv], final [N,H,dv,dk])``."""
+              eps=L2NORM_EPS, l2norm=True, want_final=True, beta_is_logit=False, _lib=None):
+    """Per-token recurrence; returns ``(out [B,T,H,dv], final [N,H,dv,dk])``.
+    With ``beta_is_logit`` the beta argument holds logits and the operation
+    uses sigmoid(beta) (:func:`sigmoid`)."""
     lib = _lib or _load()
     q, k, v, g, beta = map(_f64, (q, k, v, g, beta))
+    if beta_is_logit:
+        beta = sigmoid(beta, _lib=lib)
     init = _f64(init_state)
     N, T, H, dk, dv, cu = _geometry(q, v, cu_seqlens)
     if scale is None:
@@ -160,10 +171,13 @@ def kda_token(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=None,
 
 
 def kda_chunk(q, k, v, g, beta, init_state=None, cu_seqlens=None, scale=None,
-              eps=L2NORM_EPS, l2norm=True, chunk=16, inverse="forward", _lib=None):
+              eps=L2NORM_EPS, l2norm=True, chunk=16, inverse="forward", beta_is_logit=False,
+              _lib=None):
     """Chunkwise form; returns ``(out, final)`` like :func:`kda_token`."""
     lib = _lib or _load()
     q, k, v, g, beta = map(_f64, (q, k, v, g, beta))
+    if beta_is_logit:
+        beta = sigmoid(beta, _lib=lib)
     init = _f64(init_state)
     N, T, H, dk, dv, cu = _geometry(q, v, cu_seqlens)
     if scale is None:
@@ -235,3 +249,13 @@ def unitri_inverse(L, mode="forward", _lib=None):
     rc = lib.kda_oracle_unitri_inverse(_ptr(L), _ptr(X), C, {"forward": 0, "neumann": 1}[mode])
     _check(rc, "kda_oracle_unitri_inverse")
     return X
+
+
+def sigmoid(x, _lib=None):
+    """Elementwise 1 / (1 + exp(-x)) in FP64 (beta from a logit, flashinfer
+    kda_prefill "Optimized Blackwell prefill subset", beta_is_logit)."""
+    lib = _lib or _load()
+    x = _f64(x)
+    y = np.zeros_like(x)
+    _check(lib.kda_oracle_sigmoid(_ptr(x), _ptr(y), int(x.size)), "kda_oracle_sigmoid")
+    return y

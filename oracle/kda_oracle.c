@@ -516,3 +516,25 @@ int kda_oracle_unitri_inverse(const double* L, double* X, int64_t C, int mode) {
     inverse_forward(L, X, C);
     return KDA_ORACLE_OK;
 }
+
+/*
+ * beta from a logit: beta = sigmoid(x) = 1 / (1 + exp(-x)), elementwise, n
+ * values.  The flashinfer kda_prefill page ("Optimized Blackwell prefill
+ * subset": beta_is_logit=True, and the N16 schedule's list of rounding points,
+ * which names "sigmoid beta") takes beta as a logit and applies the sigmoid
+ * inside the operation; the page gives no other formula, so this is the plain
+ * logistic function, in FP64.  For x < 0 it is evaluated as exp(x) / (1 +
+ * exp(x)), the same function, so that exp never overflows.
+ */
+int kda_oracle_sigmoid(const double* x, double* y, int64_t n) {
+    if (n < 0 || (n > 0 && (!x || !y))) return KDA_ORACLE_EBADARG;
+    for (int64_t i = 0; i < n; ++i) {
+        if (x[i] >= 0.0) {
+            y[i] = 1.0 / (1.0 + exp(-x[i]));
+        } else {
+            const double e = exp(x[i]);
+            y[i] = e / (1.0 + e);
+        }
+    }
+    return KDA_ORACLE_OK;
+}

@@ -54,6 +54,8 @@ MUTATIONS = [
      "X[i * C + j] = ((i == j) ? 1.0 : 0.0) + L[i * C + j];"),
     ("neumann_one_factor_short", "for (int64_t e = 2; e < C; e *= 2) {",
      "for (int64_t e = 2; e < C / 2; e *= 2) {"),
+    ("sigmoid_sign", "y[i] = 1.0 / (1.0 + exp(-x[i]));", "y[i] = 1.0 / (1.0 + exp(x[i]));"),
+    ("sigmoid_negative_branch", "y[i] = e / (1.0 + e);", "y[i] = 1.0 / (1.0 + e);"),
 ]
 
 
@@ -74,6 +76,8 @@ def _pin_suite(o):
         ("inverse16", lambda: pins.test_unitri_inverse(o, 16)),
         ("inverse32", lambda: pins.test_unitri_inverse(o, 32)),
         ("split_exponent", lambda: pins.test_chunk_quantities_split_exponent(o)),
+        ("sigmoid", lambda: pins.test_sigmoid_values(o)),
+        ("beta_logit", lambda: pins.test_beta_logit_path(o)),
     ]
     for name, fn in checks:
         try:

@@ -353,3 +353,53 @@ def test_chunk_quantities_split_exponent(oracle_mod):
             if Cc < 16:
                 assert np.all(im["Kst"][ch, h, Cc:] == 0)
                 np.testing.assert_array_equal(im["Akk"][ch, h, Cc:, Cc:], np.eye(16 - Cc))
+
+
+def test_sigmoid_values(oracle_mod):
+    """beta from a logit: the logistic function's fixed points and identities
+    (sigmoid(0) = 1/2, sigmoid(ln 3) = 3/4, sigmoid(-x) = 1 - sigmoid(x),
+    saturation without overflow) and scipy's expit on a spread of logits."""
+    scipy_special = pytest.importorskip("scipy.special")
+    y = oracle_mod.sigmoid(np.array([0.0, math.log(3.0), -math.log(3.0), -800.0, 800.0]))
+    assert y[0] == 0.5
+    assert abs(y[1] - 0.75) < 1e-15 and abs(y[2] - 0.25) < 1e-15
+    assert y[3] == 0.0 and y[4] == 1.0
+    x = np.random.default_rng(5).normal(0.0, 4.0, size=1000)
+    y = oracle_mod.sigmoid(x)
+    np.testing.assert_allclose(y, scipy_special.expit(x), rtol=1e-14, atol=0)
+    np.testing.assert_allclose(oracle_mod.sigmoid(-x), 1.0 - y, rtol=0, atol=1e-15)
+
+
+def test_beta_logit_path(oracle_mod):
+    """beta_is_logit: the operation on logits equals the operation on
+    sigmoid(logits) computed by scipy; logit 0 is beta = 1/2; a logit of -60
+    (beta ~ 9e-27) is the beta = 0 closed form (pure decay) to rounding."""
+    scipy_special = pytest.importorskip("scipy.special")
+    inp = small_inputs(B=2, T=23, H=2, d=8, seed=11)
+    q, k, v, g = map(f64, (inp["q"], inp["k"], inp["v"], inp["g"]))
+    init = f64(inp["init_state"])
+    logit = np.random.default_rng(2).normal(0.0, 2.0, size=(2, 23, 2))
+    for form in ("kda_token", "kda_chunk"):
+        fn = getattr(oracle_mod, form)
+        o1, f1 = fn(q, k, v, g, logit, init, beta_is_logit=True)
+        o2, f2 = fn(q, k, v, g, scipy_special.expit(logit), init)
+        assert rel_fro(o1, o2) < 1e-13 and rel_fro(f1, f2) < 1e-13
+    o1, f1 = oracle_mod.kda_token(q, k, v, g, np.zeros((2, 23, 2)), init, beta_is_logit=True)
+    o2, f2 = oracle_mod.kda_token(q, k, v, g, np.full((2, 23, 2), 0.5), init)
+    np.testing.assert_array_equal(o1, o2)
+    np.testing.assert_array_equal(f1, f2)
+    # -60: beta = 8.8e-27, so the state is S_0 Diag(exp(G_t)) to ~1e-25 of its
+    # size (weak decay, so that the state stays of order one)
+    g = 0.02 * g
+    o1, f1 = oracle_mod.kda_token(q, k, v, g, np.full((2, 23, 2), -60.0), init,
+                                  beta_is_logit=True)
+    G = np.cumsum(g, axis=1)                                   # [B, T, H, dk]
+    s = 1 / math.sqrt(8)
+    qh = _normalise(q)
+    for b in range(2):
+        for h in range(2):
+            S0 = init[b, h]
+            expect = np.stack([s * (S0 * np.exp(G[b, t, h])[None, :]) @ qh[b, t, h]
+                               for t in range(23)])
+            assert rel_fro(o1[b, :, h], expect) < 1e-13
+            assert rel_fro(f1[b, h], S0 * np.exp(G[b, -1, h])[None, :]) < 1e-13
