@@ -15,10 +15,12 @@ Reported: `value` = head-tokens/s over the timed steps (device time, CUDA
 events on the launching stream); `e2e` = the same metric through the host-buffer
 entry point kda_prefill_host (pinned host tensors; the library copies the
 inputs in and O and the final state out inside every timed step, overlapped
-with the computation); `roofline` for the dominant kernel (events
-recorded by the library between its kernels in a separate pass of eager
-calls) and `roofline.critical_path` (HBM, tensor and serial-chain bounds of
-the call); `cpu_baseline` = the FP64 oracle timed on this host's cores.  `--impl reference` times that oracle
+with the computation); `roofline`: the whole call against its algorithmic
+bytes (1,538 B per head-token plus the states) at the measured copy
+bandwidth, the tensor fraction of its algorithmic FLOPs, per-kernel times
+(events recorded by the library between its kernels in a separate pass of
+eager calls) with each kernel's method and workspace bytes, and
+`roofline.critical_path` (HBM, tensor and serial-chain bounds of the call); `cpu_baseline` = the FP64 oracle timed on this host's cores.  `--impl reference` times that oracle
 alone on a bounded sample of the same workload (the pages name no runnable
 reference implementation).  Under torchrun every rank runs its own replica of
 the workload on its own GPU (weak scaling, no collective in the data path).
@@ -51,25 +53,13 @@ FLASHKDA_B200_US = {"t8192_h6": 731.7, "t8192_h96": 1032.6}
 COLUMN_SPLIT_B200_US = {"t8192_h6": 283.4, "t8192_h96": 914.7}
 L2_FLUSH_BYTES = 512 << 20
 
-# Algorithmic bytes per head-token of each kernel:
-#   preparation: reads q, k (2 x 256 B), g (512 B), beta (2 B); writes one
-#                13,824-byte packet per 16 tokens (864 B per head-token).
-#   recurrence:  reads the packets (864 B) and v (256 B); writes O (256 B);
-#                plus 32 KB per (sequence, head) for each state read or written.
-#   one launch (preparation and recurrence fused): the inputs and outputs of
-#                the whole path, q, k, g, beta, v in and O out (1,538 B per
-#                head-token) plus the states; the packets pass between the two
-#                halves of the launch and are not counted.
-#   segmented scan: the transition pass reads the packets twice and v once
-#                (1,984 B per head-token) and writes two states per (segment,
-#                head); the segment chain reads two states and writes one per
-#                (segment, head); the rerun is the recurrence above plus one
-#                state read per (segment, head).
+# Algorithmic bytes per head-token of the path (the method's own inputs and
+# outputs, nothing the implementation adds): q, k, v 256 B each, g 512 B,
+# beta 2 B, O 256 B; plus 32 KB per (sequence, head) per state read or
+# written.  The 13,824-byte packet per 16 tokens (864 B per head-token) that
+# the preparation writes and the recurrence reads is workspace.
 PACKET_PER_TOKEN = 13824 / 16
-PREP_BYTES_PER_HT = 2 * 256 + 512 + 2 + PACKET_PER_TOKEN
-REC_BYTES_PER_HT = PACKET_PER_TOKEN + 256 + 256
 PATH_BYTES_PER_HT = 2 * 256 + 512 + 2 + 256 + 256
-TRANSITION_BYTES_PER_HT = 2 * PACKET_PER_TOKEN + 256
 STATE_BYTES = 128 * 128 * 2
 
 # DRAM bytes (read + write) of one launch of the dominant kernel (of the
@@ -405,6 +395,70 @@ def critical_path(kda, inp, ht, state_io, us_per_call, segs):
     return res
 
 
+def call_roofline(inp, ht, H, segs, fused, us_call, prof_ms, peak, peak_kind, tpeak,
+                  tpeak_kind, workload, engine):
+    """Roofline of one call against the path's algorithmic bytes and FLOPs.
+
+    Algorithmic bytes are the method's own inputs and outputs: q, k, v (256 B
+    per head-token each), g (512 B), beta (2 B) and O (256 B), 1,538 B per
+    head-token, plus 32 KB per (sequence, head) for each state read or
+    written.  The packets that pass from the preparation to the recurrence,
+    and the segmented scan's intermediate states, are workspace: they are
+    counted separately and never in `achieved`.  `frac` = achieved / the
+    measured copy bandwidth over the whole call; per kernel, `method_frac`
+    counts only the method bytes that kernel reads or writes.  `traffic` is
+    the DRAM bytes ncu measured for every kernel of one call (null unless all
+    of the call's kernels have a current capture)."""
+    prep_ms, trans_ms, chain_ms, rec_ms = prof_ms
+    n_states = inp["N"] * H
+    state_io = (2 if inp["init_state"] is not None else 1) * n_states * STATE_BYTES
+    seg_states = n_states * segs * STATE_BYTES
+    path_bytes = PATH_BYTES_PER_HT * ht + state_io
+    flops = FLOP_PER_HT * ht
+    pkt = PACKET_PER_TOKEN * ht
+    in_qkgb = (2 * 256 + 512 + 2) * ht
+    vo = 2 * 256 * ht
+    # name: (mean ms, method bytes, workspace bytes)
+    if fused:
+        kernels = {"fused": (rec_ms, path_bytes, 0.0)}
+    elif segs:
+        kernels = {"chunk_prep": (prep_ms, in_qkgb, pkt),
+                   "transition": (trans_ms, 256 * ht, pkt + 2 * seg_states),
+                   "segment_chain": (chain_ms, state_io, 3 * seg_states),
+                   "recurrence": (rec_ms, vo, pkt + seg_states)}
+    else:
+        kernels = {"chunk_prep": (prep_ms, in_qkgb, pkt),
+                   "recurrence": (rec_ms, vo + state_io, pkt)}
+    total_ms = sum(k[0] for k in kernels.values())
+    per = {}
+    traffic = 0.0
+    for name, (ms, mb, wb) in kernels.items():
+        tr = profiled_traffic(name, workload, engine)
+        per[name] = {"us": 1e3 * ms, "share": ms / total_ms if total_ms > 0 else None,
+                     "method_bytes": mb, "workspace_bytes": wb,
+                     "method_frac": mb / (ms * 1e-3) / 1e9 / peak if ms > 0 else None,
+                     "traffic": tr}
+        traffic = None if (traffic is None or tr is None) else traffic + tr
+    dom = max(kernels, key=lambda k: kernels[k][0])
+    achieved = path_bytes / (us_call * 1e-6) / 1e9
+    tflops = flops / (us_call * 1e-6) / 1e12
+    return {
+        "bound": "hbm", "scope": "whole call (every kernel of one kda_prefill)",
+        "achieved": achieved, "peak": peak, "unit": "GB/s", "frac": achieved / peak,
+        "peak_kind": peak_kind, "algorithmic_bytes": path_bytes,
+        "algorithmic_state_bytes": state_io,
+        "traffic": traffic,
+        "workspace_traffic": None if traffic is None else traffic - path_bytes,
+        "tensor": {"flops": flops, "achieved_tflops": tflops, "peak_tflops": tpeak,
+                   "frac": tflops / tpeak, "peak_kind": tpeak_kind},
+        "dominant_kernel": dom,
+        "dominant_kernel_path_frac": path_bytes / (kernels[dom][0] * 1e-3) / 1e9 / peak,
+        "kernels": per,
+        "chain_steps": int(math.ceil(inp["q"].shape[1] / 16)) if inp["cu_seqlens"] is None
+        else None,
+    }
+
+
 def run_ours(args):
     import kimi_delta_attention_kda_gb300 as kda
     ws, rank, local = dist_env()
@@ -467,39 +521,16 @@ def run_ours(args):
     intervals, calls = prof
     prep_avg, trans_avg, chain_avg, rec_avg = (t / calls for t in intervals)
     peak, peak_kind = measured_peaks()
+    tpeak, tpeak_kind = measured_tensor_peak()
     H = inp["q"].shape[2]
-    n_states = inp["N"] * H
-    state_io = (2 if inp["init_state"] is not None else 1) * n_states * STATE_BYTES
-    seg_states = n_states * segs * STATE_BYTES
-    prep_bytes = PREP_BYTES_PER_HT * ht
-    if fused:
-        # The profile's first interval is the reset of the ready flags, the
-        # last the one launch.
-        kernels = {"fused": (PATH_BYTES_PER_HT * ht + state_io, rec_avg)}
-    elif segs:
-        kernels = {"chunk_prep": (prep_bytes, prep_avg),
-                   "transition": (TRANSITION_BYTES_PER_HT * ht + 2 * seg_states, trans_avg),
-                   "segment_chain": (3 * seg_states + state_io, chain_avg),
-                   "recurrence": (REC_BYTES_PER_HT * ht + seg_states, rec_avg)}
-    else:
-        kernels = {"chunk_prep": (prep_bytes, prep_avg),
-                   "recurrence": (REC_BYTES_PER_HT * ht + state_io, rec_avg)}
-    dom = max(kernels, key=lambda k: kernels[k][1])
-    dom_bytes, dom_ms = kernels[dom]
-    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
-    roofline = {"bound": "hbm", "kernel": dom, "achieved": achieved, "peak": peak,
-                "unit": "GB/s", "frac": achieved / peak, "peak_kind": peak_kind,
-                "traffic": profiled_traffic(dom, args.workload, args.engine),
-                "chain_steps": int(math.ceil(inp["q"].shape[1] / 16)) if inp["cu_seqlens"] is None
-                else None}
-    if fused:
-        roofline.update({"fused_us": 1e3 * rec_avg, "flag_reset_us": 1e3 * prep_avg})
-    else:
-        roofline.update({"prep_us": 1e3 * prep_avg, "recurrence_us": 1e3 * rec_avg})
-    if segs:
-        roofline.update({"transition_us": 1e3 * trans_avg, "segment_chain_us": 1e3 * chain_avg})
-    roofline["critical_path"] = critical_path(kda, inp, ht, state_io, 1e3 * total_ms / args.steps,
-                                              segs)
+    us_call = 1e3 * total_ms / args.steps
+    roofline = call_roofline(inp, ht, H, segs, fused, us_call,
+                             (prep_avg, trans_avg, chain_avg, rec_avg), peak, peak_kind,
+                             tpeak, tpeak_kind, args.workload, args.engine)
+    state_io = roofline["algorithmic_state_bytes"]
+    roofline["critical_path"] = critical_path(kda, inp, ht, state_io, us_call, segs)
+    if "plan_frac" in roofline["critical_path"]:
+        roofline["plan_frac"] = roofline["critical_path"]["plan_frac"]
 
     line = {
         "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
@@ -526,11 +557,11 @@ def run_ours(args):
         "clocks": clk.summary(),
     }
     if args.workload in FLASHKDA_B200_US:
-        ref_value = ht / (FLASHKDA_B200_US[args.workload] * 1e-6)
-        line["vs_baseline"] = value / ref_value
-        line["baseline"] = {"what": "FlashKDA prep + recurrence on a B200, %.1f us (pages, "
-                                    "FlashKDA column split section 4)" % FLASHKDA_B200_US[args.workload],
-                            "column_split_b200_us": COLUMN_SPLIT_B200_US[args.workload]}
+        # Another machine's number: context only, never the target (vs_baseline stays null).
+        line["context_b200"] = {
+            "what": "FlashKDA prep + recurrence on a B200, %.1f us (pages, FlashKDA column split "
+                    "section 4); not measured here" % FLASHKDA_B200_US[args.workload],
+            "column_split_b200_us": COLUMN_SPLIT_B200_US[args.workload]}
     if not args.no_secondary and args.workload != "t8192_h96":
         sec = synthetic.make_workload("t8192_h96")
         ds = device_inputs(sec, device)
@@ -543,9 +574,15 @@ def run_ours(args):
                              "value": ht2 / (t2 * 1e-3), "unit": UNIT,
                              "prep_us": 1e3 * prof2[0][0] / prof2[1],
                              "recurrence_us": 1e3 * sum(prof2[0][1:]) / prof2[1],
-                             "recurrence_split": kda.auto_split(1, 96),
-                             "vs_flashkda_b200": (ht2 / (t2 * 1e-3)) /
-                             (ht2 / (FLASHKDA_B200_US["t8192_h96"] * 1e-6))}
+                             "recurrence_split": kda.auto_split(1, 96)}
+        sec_state = sec["N"] * 96 * STATE_BYTES * (2 if sec["init_state"] is not None else 1)
+        sec_path = PATH_BYTES_PER_HT * ht2 + sec_state
+        peak2, _ = measured_peaks()
+        line["secondary"]["roofline"] = {
+            "bound": "hbm", "scope": "whole call", "algorithmic_bytes": sec_path,
+            "achieved": sec_path / (t2 * 1e-3) / 1e9, "peak": peak2, "unit": "GB/s",
+            "frac": sec_path / (t2 * 1e-3) / 1e9 / peak2,
+            "tensor_frac": FLOP_PER_HT * ht2 / (t2 * 1e-3) / 1e12 / measured_tensor_peak()[0]}
         del ds
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
         line["cpu_baseline"] = cpu_baseline(args.workload, args.cpu_seconds)

@@ -77,3 +77,32 @@ def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     bench.run_reference(_Args())
     assert capsys.readouterr().out == ""
+
+
+def test_call_roofline_counts_only_algorithmic_bytes():
+    """The headline fraction divides the path's algorithmic bytes (1,538 B per
+    head-token plus the states) by the whole call's time; packets and
+    segment states appear only as workspace bytes."""
+    T, H = 8192, 6
+    inp = {"N": 1, "q": torch.empty((1, T, H, 1)), "cu_seqlens": None,
+           "init_state": torch.empty((1, H, 1, 1))}
+    ht = T * H
+    r = bench.call_roofline(inp, ht, H, 25, False, 100.0, (0.03, 0.03, 0.015, 0.025), 6673.8,
+                            "measured", 1925.9, "measured", "t8192_h6", 0)
+    path = 1538 * ht + 2 * H * 128 * 128 * 2
+    assert r["algorithmic_bytes"] == path
+    assert abs(r["achieved"] - path / 100e-6 / 1e9) < 1e-6
+    assert abs(r["frac"] - r["achieved"] / 6673.8) < 1e-12
+    assert 0.11 < r["frac"] < 0.12
+    assert abs(r["tensor"]["frac"] - 117760 * ht / 100e-6 / 1e12 / 1925.9) < 1e-12
+    assert r["dominant_kernel"] == "chunk_prep"   # first of the two 30-us kernels
+    assert set(r["kernels"]) == {"chunk_prep", "transition", "segment_chain", "recurrence"}
+    # each kernel counts the method bytes it touches: v is read by the
+    # transition pass and again by the rerun, everything else once
+    assert sum(k["method_bytes"] for k in r["kernels"].values()) == path + 256 * ht
+    assert r["kernels"]["recurrence"]["workspace_bytes"] >= 864 * ht
+    # serial plan: preparation and recurrence split the path's bytes exactly
+    r = bench.call_roofline(inp, ht, H, 0, False, 700.0, (0.3, 0.0, 0.0, 0.4), 6673.8,
+                            "measured", 1925.9, "measured", "t8192_h6", 0)
+    assert sum(k["method_bytes"] for k in r["kernels"].values()) == path
+    assert r["dominant_kernel"] == "recurrence"
