@@ -43,6 +43,9 @@ extern "C" {
 #define KDA_ERR_SCRATCH (-8)   /* shape too large for kda_prefill_noalloc's fixed scratch */
 #define KDA_ERR_SEQLENS (-9)   /* kda_prefill_host: the host cu_seqlens break their contract */
 
+/* Flags of kda_prefill_ex. */
+#define KDA_FLAG_BETA_LOGIT 1u /* beta holds logits; the operation uses sigmoid(beta) */
+
 /* Device-side status bits, reported by kda_device_status(). */
 #define KDA_DEV_BAD_SEQLENS 1  /* cu_seqlens broke its contract; out/final_state untouched */
 #define KDA_DEV_PIPE_TIMEOUT 2 /* an internal pipeline wait hit its bound; results incomplete */
@@ -206,6 +209,24 @@ int kda_prefill_checkpointed(const void* q, const void* k, const void* v, const 
                              const int64_t* cu_seqlens, int64_t checkpoint_every_n_tokens,
                              void* state_checkpoints, const int64_t* checkpoint_cu_starts,
                              int64_t checkpoint_rows, void* stream);
+
+/*
+ * kda_prefill with options: the same operation, arguments, layouts, results
+ * and errors, plus
+ *   flags  0, or KDA_FLAG_BETA_LOGIT: beta (BF16 [B, T, H]) holds logits x and
+ *          the operation uses beta = sigmoid(x) = 1 / (1 + exp(-x)), formed in
+ *          FP32 inside the chunk preparation ("flashinfer kda_prefill",
+ *          "Optimized Blackwell prefill subset": beta_is_logit=True).  Other
+ *          bits: KDA_ERR_ARG.
+ *   checkpoint_every_n_tokens, state_checkpoints, checkpoint_cu_starts,
+ *   checkpoint_rows: native checkpoints exactly as kda_prefill_checkpointed;
+ *          state_checkpoints NULL for none (the other three are then ignored).
+ */
+int kda_prefill_ex(const void* q, const void* k, const void* v, const float* g, const void* beta,
+                   const void* init_state, void* out, void* final_state, int64_t B, int64_t T,
+                   int64_t H, const int64_t* cu_seqlens, uint32_t flags,
+                   int64_t checkpoint_every_n_tokens, void* state_checkpoints,
+                   const int64_t* checkpoint_cu_starts, int64_t checkpoint_rows, void* stream);
 
 /*
  * Whether kda_prefill may run preparation and recurrence as one cooperative

@@ -40,7 +40,7 @@ def _stream_handle(stream):
 def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
                 final_state=None, output_final_state=True, stream=None,
                 checkpoint_every_n_tokens=None, state_checkpoints=None,
-                checkpoint_cu_starts=None):
+                checkpoint_cu_starts=None, beta_is_logit=False):
     """KDA prefill on CUDA tensors; returns ``(out, final_state)``, or
     ``(out, final_state, state_checkpoints)`` with checkpoints.
 
@@ -52,8 +52,9 @@ def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
     ``state_checkpoints`` (bf16 ``[C, H, 128, 128]``) receives the state before
     every interval of each sequence at rows ``checkpoint_cu_starts[n]`` ..
     (int64 ``[N + 1]`` on the device; see ``kda_prefill_checkpointed`` in
-    include/kda.h).  The call is asynchronous on ``stream`` (default: the
-    current PyTorch stream).
+    include/kda.h).  With ``beta_is_logit`` beta holds logits and the
+    operation uses sigmoid(beta) (``kda_prefill_ex``).  The call is
+    asynchronous on ``stream`` (default: the current PyTorch stream).
     """
     import torch
     _require(q.dim() == 4 and q.shape[-1] == HEAD_DIM, "q must be [B, T, H, 128]")
@@ -86,6 +87,14 @@ def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
     if final_state is None and output_final_state:
         final_state = torch.empty((N, H, HEAD_DIM, HEAD_DIM), dtype=torch.bfloat16,
                                   device=q.device)
+    flags = _lib.FLAG_BETA_LOGIT if beta_is_logit else 0
+    if checkpoint_every_n_tokens is None and flags:
+        rc = _lib.prefill_ex_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
+                                 _ptr(out), _ptr(final_state), n_arg, T, H, _ptr(cu_seqlens),
+                                 flags, 0, 0, 0, 0, _stream_handle(stream))
+        if rc != 0:
+            raise KdaError(rc, "kda_prefill_ex")
+        return out, final_state
     if checkpoint_every_n_tokens is None:
         rc = _lib.prefill_raw(_ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state),
                               _ptr(out), _ptr(final_state), n_arg, T, H, _ptr(cu_seqlens),
@@ -102,13 +111,20 @@ def kda_prefill(q, k, v, g, beta, init_state=None, cu_seqlens=None, out=None,
     _require(checkpoint_cu_starts.is_cuda and checkpoint_cu_starts.dtype == torch.int64
              and checkpoint_cu_starts.is_contiguous() and checkpoint_cu_starts.numel() == N + 1,
              "checkpoint_cu_starts must be a contiguous int64 [N + 1] CUDA vector")
-    rc = _lib.prefill_checkpointed_raw(
-        _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(out),
-        _ptr(final_state), n_arg, T, H, _ptr(cu_seqlens), checkpoint_every_n_tokens,
-        _ptr(state_checkpoints), _ptr(checkpoint_cu_starts), state_checkpoints.shape[0],
-        _stream_handle(stream))
+    if flags:
+        rc = _lib.prefill_ex_raw(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(out),
+            _ptr(final_state), n_arg, T, H, _ptr(cu_seqlens), flags, checkpoint_every_n_tokens,
+            _ptr(state_checkpoints), _ptr(checkpoint_cu_starts), state_checkpoints.shape[0],
+            _stream_handle(stream))
+    else:
+        rc = _lib.prefill_checkpointed_raw(
+            _ptr(q), _ptr(k), _ptr(v), _ptr(g), _ptr(beta), _ptr(init_state), _ptr(out),
+            _ptr(final_state), n_arg, T, H, _ptr(cu_seqlens), checkpoint_every_n_tokens,
+            _ptr(state_checkpoints), _ptr(checkpoint_cu_starts), state_checkpoints.shape[0],
+            _stream_handle(stream))
     if rc != 0:
-        raise KdaError(rc, "kda_prefill_checkpointed")
+        raise KdaError(rc, "kda_prefill_ex" if flags else "kda_prefill_checkpointed")
     return out, final_state, state_checkpoints
 
 

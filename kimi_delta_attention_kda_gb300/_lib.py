@@ -43,6 +43,8 @@ def load():
         lib.kda_prefill.restype = I
         lib.kda_prefill_checkpointed.argtypes = [P] * 8 + [I64] * 3 + [P, I64, P, P, I64, P]
         lib.kda_prefill_checkpointed.restype = I
+        lib.kda_prefill_ex.argtypes = [P] * 8 + [I64] * 3 + [P, ctypes.c_uint32, I64, P, P, I64, P]
+        lib.kda_prefill_ex.restype = I
         lib.kda_error_string.argtypes = [I]
         lib.kda_error_string.restype = ctypes.c_char_p
         lib.kda_device_status.argtypes = [P, ctypes.POINTER(I)]
@@ -140,6 +142,18 @@ def prefill_checkpointed_raw(q, k, v, g, beta, init_state, out, final_state, B, 
     return load().kda_prefill_checkpointed(
         q or None, k or None, v or None, g or None, beta or None, init_state or None, out or None,
         final_state or None, int(B), int(T), int(H), cu_seqlens or None, int(every),
+        states or None, cu_starts or None, int(rows), stream or None)
+
+
+FLAG_BETA_LOGIT = 1
+
+
+def prefill_ex_raw(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens, flags,
+                   every, states, cu_starts, rows, stream):
+    """Call ``kda_prefill_ex`` with integer device addresses (0 for NULL)."""
+    return load().kda_prefill_ex(
+        q or None, k or None, v or None, g or None, beta or None, init_state or None, out or None,
+        final_state or None, int(B), int(T), int(H), cu_seqlens or None, int(flags), int(every),
         states or None, cu_starts or None, int(rows), stream or None)
 
 

@@ -85,6 +85,28 @@ def build(force: bool = False, verbose: bool = False, ptxas_info: bool = False) 
     return LIB_PATH
 
 
+TEST_HOOKS_LIB = os.path.join(HERE, "libkda_testhooks.so")
+TEST_WAIT_BOUND_CYCLES = 100000
+
+
+def build_test_hooks(force: bool = False) -> str:
+    """Compile the test-only library ``libkda_testhooks.so``: the hooks of
+    ``csrc/kda_test_hooks.cu`` with the library's wait bound cut to 10^5
+    cycles, so that a test can make a bounded wait run out.  Never linked
+    into ``libkda.so``."""
+    src = os.path.join(CSRC, "kda_test_hooks.cu")
+    if force or _stale(TEST_HOOKS_LIB, [src] + _headers()):
+        tmp = TEST_HOOKS_LIB + ".tmp.%d" % os.getpid()
+        cmd = ([nvcc()] + NVCC_FLAGS + ARCH_FLAGS +
+               ["-DKDA_TEST_HOOKS", "-DKDA_WAIT_BOUND_CYCLES=%dLL" % TEST_WAIT_BOUND_CYCLES,
+                "-shared", "-o", tmp, src])
+        r = subprocess.run(cmd, capture_output=True, text=True)
+        if r.returncode != 0:
+            raise RuntimeError("nvcc failed for the test hooks:\n" + r.stdout + r.stderr)
+        os.replace(tmp, TEST_HOOKS_LIB)
+    return TEST_HOOKS_LIB
+
+
 if __name__ == "__main__":
     build(force="--force" in sys.argv, verbose=True, ptxas_info="--ptxas-info" in sys.argv)
     print(LIB_PATH)

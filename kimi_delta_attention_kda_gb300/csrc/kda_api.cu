@@ -377,7 +377,8 @@ bool use_fusion(const Plan& pl, int64_t H, int nsplit, int sms) {
 // `ordered`: also have the metadata kernel order the sequences longest-first.
 int run_prep(const Plan& pl, const void* q, const void* k, const float* g, const void* beta,
              int64_t H, const int64_t* cu_seqlens, uint8_t* meta, uint8_t* packets,
-             DeviceState* d, cudaStream_t stream, SeqGeometry* geo_out, bool ordered = false) {
+             DeviceState* d, cudaStream_t stream, SeqGeometry* geo_out, bool ordered = false,
+             bool beta_logit = false) {
     SeqGeometry geo = pl.geo;
     if (pl.packed) {
         int32_t* valid = reinterpret_cast<int32_t*>(meta);
@@ -394,7 +395,8 @@ int run_prep(const Plan& pl, const void* q, const void* k, const float* g, const
         geo.valid = valid;
         geo.order = order;
     }
-    if (launch_prep(q, k, g, beta, packets, geo, H, kScale, d->status, stream) != cudaSuccess)
+    if (launch_prep(q, k, g, beta, packets, geo, H, kScale, d->status, stream, beta_logit) !=
+        cudaSuccess)
         return KDA_ERR_CUDA;
     ++t_launches;
     *geo_out = geo;
@@ -427,8 +429,10 @@ namespace {
 int prefill_impl(const void* q, const void* k, const void* v, const float* g, const void* beta,
                  const void* init_state, void* out, void* final_state, int64_t B, int64_t T,
                  int64_t H, const int64_t* cu_seqlens, void* stream_ptr, const Checkpoints* ck,
-                 const void* ck_cu_starts) {
+                 const void* ck_cu_starts, uint32_t flags = 0) {
     const bool packed = cu_seqlens != nullptr;
+    if (flags & ~static_cast<uint32_t>(KDA_FLAG_BETA_LOGIT)) return KDA_ERR_ARG;
+    const bool beta_logit = (flags & KDA_FLAG_BETA_LOGIT) != 0;
     Plan pl;
     int rc = make_plan(B, T, H, packed, &pl);
     if (rc != KDA_OK) return rc;
@@ -476,7 +480,8 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         prof_record(3, stream);
         if (rc == KDA_OK) {
             if (launch_fused(q, k, g, beta, v, out, init_state, final_state, ws + pl.meta_bytes,
-                             ready, pl.geo, H, nsplit, kScale, d->status, stream, ck) == cudaSuccess) {
+                             ready, pl.geo, H, nsplit, kScale, d->status, stream, ck,
+                             beta_logit) == cudaSuccess) {
                 done = true;
                 ++t_launches;
             }
@@ -490,7 +495,8 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         uint8_t* zstates = packets + pl.packet_bytes;
         uint8_t* maps = zstates + sc.state_bytes;
         uint8_t* starts = maps + sc.state_bytes;
-        rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, packets, d, stream, &geo);
+        rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, packets, d, stream, &geo, false,
+                      beta_logit);
         SeqGeometry sg = geo;
         int64_t* seg_begin = nullptr;
         if (pl.packed) {
@@ -561,7 +567,7 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         const int64_t k_long = long_split_count(pl, H, nsplit, d->sms);
         const bool ordered = pl.packed && (pl.N * H * nsplit > d->sms || k_long > 0);
         rc = run_prep(pl, q, k, g, beta, H, cu_seqlens, ws, ws + pl.meta_bytes, d, stream, &geo,
-                      ordered);
+                      ordered, beta_logit);
         prof_record(1, stream);
         prof_record(2, stream);
         prof_record(3, stream);
@@ -861,6 +867,32 @@ extern "C" int kda_prefill_checkpointed(const void* q, const void* k, const void
                         stream_ptr, &ck, checkpoint_cu_starts);
 }
 
+extern "C" int kda_prefill_ex(const void* q, const void* k, const void* v, const float* g,
+                              const void* beta, const void* init_state, void* out,
+                              void* final_state, int64_t B, int64_t T, int64_t H,
+                              const int64_t* cu_seqlens, uint32_t flags,
+                              int64_t checkpoint_every_n_tokens, void* state_checkpoints,
+                              const int64_t* checkpoint_cu_starts, int64_t checkpoint_rows,
+                              void* stream_ptr) {
+    t_launches = 0;
+    if (!state_checkpoints)
+        return prefill_impl(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,
+                            stream_ptr, nullptr, nullptr, flags);
+    if (checkpoint_every_n_tokens <= 0 || checkpoint_every_n_tokens % kChunk != 0 ||
+        checkpoint_rows < 0)
+        return KDA_ERR_ARG;
+    if (!checkpoint_cu_starts) return KDA_ERR_NULL;
+    if (!aligned(state_checkpoints, 16) || !aligned(checkpoint_cu_starts, 8)) return KDA_ERR_ALIGN;
+    if (H < 1 || H > kMaxElems / (kHeadDim * kHeadDim)) return KDA_ERR_SHAPE;
+    if (checkpoint_rows > kMaxElems / (H * kHeadDim * kHeadDim)) return KDA_ERR_SHAPE;
+    Checkpoints ck;
+    ck.states = static_cast<__nv_bfloat16*>(state_checkpoints);
+    ck.cu_starts = checkpoint_cu_starts;
+    ck.every = checkpoint_every_n_tokens / kChunk;
+    ck.rows = checkpoint_rows;
+    return prefill_impl(q, k, v, g, beta, init_state, out, final_state, B, T, H, cu_seqlens,
+                        stream_ptr, &ck, checkpoint_cu_starts, flags);
+}
 
 extern "C" int kda_prep_only(const void* q, const void* k, const float* g, const void* beta,
                              int64_t B, int64_t T, int64_t H, const int64_t* cu_seqlens,

@@ -144,7 +144,13 @@ __device__ __forceinline__ bool mbar_try_wait_sleep(uint64_t* bar, uint32_t pari
 // Wait for phase `parity` of an mbarrier with an upper bound on elapsed clock
 // cycles.  Returns false (and ORs kDevPipeTimeout into *status) when the bound
 // runs out, so that no wait can hang the GPU.
+// A test build (tests/test_gpu_wait_bound.py) compiles the wait-bound hooks
+// with KDA_WAIT_BOUND_CYCLES set to 10^5 cycles to make a wait run out.
+#ifdef KDA_WAIT_BOUND_CYCLES
+constexpr long long kWaitBoundCycles = KDA_WAIT_BOUND_CYCLES;
+#else
 constexpr long long kWaitBoundCycles = 4000000000LL;   // about 2 s at 2 GHz
+#endif
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, int* status) {
     if (mbar_try_wait(bar, parity)) return true;
     long long t0 = clock64();
@@ -239,6 +245,27 @@ __device__ __forceinline__ uint32_t ld_acquire_gpu(const uint32_t* p) {
     return v;
 }
 
+
+// Wait, with the whole warp, until the ready flag flags[0] is set, polling
+// the flags flags[i * stride] of the next 32 items at once (lane i: item i,
+// for i < count; a release store of 1 sets a flag).  Returns true with
+// *mask = the items seen ready (bit i), or false after kWaitBoundCycles with
+// kDevPipeTimeout ORed into *status; warp-uniform either way.
+__device__ __forceinline__ bool wait_ready_flags(const uint32_t* flags, int64_t stride,
+                                                 int64_t count, uint32_t* mask, int* status) {
+    const int lane = threadIdx.x & 31;
+    const long long t0 = clock64();
+    for (;;) {
+        const uint32_t flag = lane < count ? ld_acquire_gpu(flags + lane * stride) : 0u;
+        *mask = __ballot_sync(0xffffffffu, flag != 0u);
+        if (*mask & 1u) return true;
+        if (__shfl_sync(0xffffffffu, clock64() - t0 > kWaitBoundCycles, 0)) {
+            if (lane == 0) atomicOr(status, kDevPipeTimeout);
+            return false;
+        }
+        __nanosleep(256);
+    }
+}
 
 // Named barrier of a warp pair (64 threads).
 __device__ __forceinline__ void pair_sync(int id) {

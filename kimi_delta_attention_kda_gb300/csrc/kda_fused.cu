@@ -94,7 +94,7 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
                          const void* v, void* out, const void* init_state, void* final_state,
                          uint8_t* packets, uint32_t* ready, const SeqGeometry& geo, int64_t H,
                          int nsplit, float scale, int* status, cudaStream_t stream,
-                         const Checkpoints* ck) {
+                         const Checkpoints* ck, bool beta_logit) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return cudaErrorInvalidDevice;
     cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -104,7 +104,8 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
         return cudaErrorInvalidValue;
 
     FusedArgs f;
-    if (!prep::make_prep_args(&f.p, beta, packets, geo, H, scale, status)) return cudaErrorInvalidValue;
+    if (!prep::make_prep_args(&f.p, beta, packets, geo, H, scale, status, beta_logit))
+        return cudaErrorInvalidValue;
     f.r.v = static_cast<const __nv_bfloat16*>(v);
     f.r.out = static_cast<__nv_bfloat16*>(out);
     f.r.init_state = static_cast<const __nv_bfloat16*>(init_state);

@@ -60,9 +60,11 @@ struct SeqGroups {
 cudaError_t launch_rebase_offsets(const int64_t* cu_seqlens, const SeqGroups& groups, int64_t* out,
                                   cudaStream_t stream);
 
+// beta_logit: the beta tensor holds logits and the preparation applies
+// beta = sigmoid(logit) ("flashinfer kda_prefill", beta_is_logit).
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const void* beta,
                         uint8_t* packets, const SeqGeometry& geo, int64_t H, float scale,
-                        int* status, cudaStream_t stream);
+                        int* status, cudaStream_t stream, bool beta_logit = false);
 
 // Native state checkpoints: the state before every `every`-chunk interval of
 // each sequence (its initial state first), in rows cu_starts[n] ..
@@ -141,7 +143,7 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
                          const void* v, void* out, const void* init_state, void* final_state,
                          uint8_t* packets, uint32_t* ready, const SeqGeometry& geo, int64_t H,
                          int nsplit, float scale, int* status, cudaStream_t stream,
-                         const Checkpoints* ck = nullptr);
+                         const Checkpoints* ck = nullptr, bool beta_logit = false);
 
 // Tensor map of v viewed as a 2-D BF16 array [tokens][H * 128], boxes of
 // 16 tokens x `cols` value columns.

@@ -110,11 +110,12 @@ using namespace prep;
 
 cudaError_t launch_prep(const void* q, const void* k, const float* g, const void* beta,
                         uint8_t* packets, const SeqGeometry& geo, int64_t H, float scale,
-                        int* status, cudaStream_t stream) {
+                        int* status, cudaStream_t stream, bool beta_logit) {
     if (geo.chunk_ub * H <= 0 || geo.tokens <= 0) return cudaSuccess;
     if (geo.tokens >= (int64_t(1) << 31)) return cudaErrorInvalidValue;   // TMA coordinates are int32
     PrepArgs a;
-    if (!make_prep_args(&a, beta, packets, geo, H, scale, status)) return cudaErrorInvalidValue;
+    if (!make_prep_args(&a, beta, packets, geo, H, scale, status, beta_logit))
+        return cudaErrorInvalidValue;
     PrepMaps maps;
     cudaError_t e = encode_maps(&maps, q, k, g, geo.tokens, H);
     if (e != cudaSuccess) return e;

@@ -73,6 +73,7 @@ struct PrepArgs {
     int64_t H;
     int64_t n_chunk_heads;   // < 2^31, so item, chunk and head indices fit 32 bits
     float scale;
+    int beta_logit;          // 1: the beta tensor holds logits, beta = sigmoid(logit)
     FastDiv div_h;           // by H
     FastDiv div_cps;         // by geo.chunks_per_seq (fixed layout)
 };
@@ -80,8 +81,9 @@ struct PrepArgs {
 // The preparation's arguments for `geo` and H heads; false when the item
 // count leaves the 32-bit range of the item arithmetic.
 inline bool make_prep_args(PrepArgs* a, const void* beta, uint8_t* packets, const SeqGeometry& geo,
-                           int64_t H, float scale, int* status) {
+                           int64_t H, float scale, int* status, bool beta_logit = false) {
     a->beta = static_cast<const __nv_bfloat16*>(beta);
+    a->beta_logit = beta_logit ? 1 : 0;
     a->packets = packets;
     a->geo = geo;
     a->geo.status = status;
@@ -563,7 +565,11 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
                 pending = -1;
             }
         }
-        const float beta_f = lane < len ? __bfloat162float(a.beta[(t0 + lane) * a.H + h]) : 0.f;
+        float beta_f = lane < len ? __bfloat162float(a.beta[(t0 + lane) * a.H + h]) : 0.f;
+        // beta from a logit ("flashinfer kda_prefill", beta_is_logit):
+        // sigmoid(x) = 1 / (1 + e^-x) in FP32; e^-x = inf for very negative x
+        // gives 0, as it should.  Padding lanes stay 0.
+        if (a.beta_logit && lane < len) beta_f = 1.f / (1.f + __expf(-beta_f));
         const bool got = mbar_wait_warp_sleep(bar, phase, a.geo.status);
         if (!pair_all(bid, got)) {
             // The loads may still land: wait for them (bounded) before leaving.

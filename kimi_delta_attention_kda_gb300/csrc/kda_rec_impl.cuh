@@ -236,20 +236,8 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
                 // c + i) until chunk c's is set; one proxy fence then orders
                 // every copy of a chunk seen ready here after its packet.
                 ready_base = c;
-                const long long t0 = clock64();
-                for (;;) {
-                    const int64_t cc = c + lane;
-                    const uint32_t flag =
-                        cc < nch ? ld_acquire_gpu(ready + (c_begin + cc) * a.H + h) : 0u;
-                    ready_mask = __ballot_sync(0xffffffffu, flag != 0u);
-                    if (ready_mask & 1u) break;
-                    if (__shfl_sync(0xffffffffu, clock64() - t0 > kWaitBoundCycles, 0)) {
-                        if (lane == 0) atomicOr(a.status, kDevPipeTimeout);
-                        ok = false;
-                        break;
-                    }
-                    __nanosleep(256);
-                }
+                ok = wait_ready_flags(ready + (c_begin + c) * a.H + h, a.H, nch - c, &ready_mask,
+                                      a.status);
                 if (!ok) break;
                 if (lane == 0) fence_proxy_async_global();
             }

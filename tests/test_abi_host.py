@@ -266,3 +266,27 @@ def test_noalloc_scratch_boundary(lib):
     assert call_noalloc(lib, B=1503, T=35695, cu=A + 7 * GB) == -5
     assert (35695 + 15 * 1504) // 16 * 13824 <= cap < need(1504, 35695)
     assert call_noalloc(lib, B=1504, T=35695, cu=A + 7 * GB) == -8
+
+
+def test_prefill_ex_arguments(lib):
+    """kda_prefill_ex: unknown flag bits are KDA_ERR_ARG; its checkpoint
+    arguments are checked like kda_prefill_checkpointed's (host only)."""
+    def ex(flags=1, every=0, states=0, cu_starts=0, rows=0, **kw):
+        a = dict(q=A, k=A + GB, v=A + 2 * GB, g=A + 3 * GB, beta=A + 4 * GB, init=0,
+                 out=A + 5 * GB, final=0, B=1, T=16, H=1, cu=0)
+        a.update(kw)
+        return _lib.prefill_ex_raw(a["q"], a["k"], a["v"], a["g"], a["beta"], a["init"], a["out"],
+                                   a["final"], a["B"], a["T"], a["H"], a["cu"], flags, every,
+                                   states, cu_starts, rows, 0)
+    for flags in (2, 4, 3, 1 << 31):
+        assert ex(flags=flags) == -7
+    assert ex(flags=1, B=0) == -2
+    assert ex(flags=1, q=0) == -1
+    assert ex(flags=1, states=A + 9 * GB, cu_starts=A + 10 * GB, every=8, rows=4) == -7
+    assert ex(flags=1, states=A + 9 * GB, cu_starts=0, every=16, rows=4) == -1
+    assert ex(flags=1, states=A + 9 * GB + 8, cu_starts=A + 10 * GB, every=16, rows=4) == -3
+    assert ex(flags=1, states=A + 64, cu_starts=A + 10 * GB, every=16, rows=4) == -4
+    import torch
+    if not torch.cuda.is_available():
+        assert ex(flags=1) == -5
+        assert ex(flags=0) == -5
