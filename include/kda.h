@@ -338,7 +338,7 @@ int kda_profile_end_detail(double* intervals_ms, int* calls);
  * one chunk step on the current device (HOST out), for the critical-path
  * bound of a serial walk over the chunks ("FlashKDA column split" section 1:
  * chunk c + 1 needs chunk c's state).  One warp runs, 4,096 times, U^T = K'
- * S^T over 128 keys (two interleaved MMA accumulators and an add), the BF16
+ * S^T over 128 keys (two interleaved MMA accumulators and an add), the FP16
  * conversion and transpose of U^T, S^T <- D S^T + (K^end)^T U^T and the BF16
  * conversion and transpose of the new state, with operands in registers.
  * Synchronises the device; not for use on a hot path.  KDA_ERR_DEVICE

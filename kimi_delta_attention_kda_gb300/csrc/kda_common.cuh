@@ -11,6 +11,7 @@
 #pragma once
 
 #include <cuda_bf16.h>
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -23,16 +24,17 @@ constexpr int kChunk = 16;      // C = 16 tokens per chunk
 // Per-(chunk, head) packet written by the preparation kernel and read by the
 // recurrence kernel.  The byte image is exactly the shared-memory image the
 // recurrence consumes, so one bulk copy moves a whole packet.  Matrix tiles
-// are BF16 and "K-major" (the contraction index is contiguous in a row) with
+// are BF16 (KE and AQK: FP16, the operands of the state update and of the
+// output's U term, see mma_f16) and "K-major" (the contraction index is contiguous in a row) with
 // the 128-byte or 32-byte XOR swizzle that both ldmatrix (conflict-free rows)
 // and tcgen05 shared-memory descriptors understand:
 //
 //  [    0,  4096)  KS   : K' = -(A^kk B_c) K^start^T, 16 token rows x 128 key
 //                         channels, SW128, two 64-channel slabs of 16 x 128 B
 //  [ 4096,  8192)  QS   : s * Q^start^T, same layout (the scale s is folded in)
-//  [ 8192, 12288)  KE   : K^end^T, 128 key rows x 16 tokens (32 B rows), SW32
+//  [ 8192, 12288)  KE   : K^end^T, 128 key rows x 16 tokens (32 B rows), SW32, FP16
 //  [12288, 12800)  AKB  : A^kk B_c (A^kk with column j scaled by beta_j), 16 x 16, SW32
-//  [12800, 13312)  AQK  : A^qk (includes s), 16 x 16, SW32
+//  [12800, 13312)  AQK  : A^qk (includes s), 16 x 16, SW32, FP16
 //  [13312, 13824)  DTOT : D_{0:15}, 128 FP32, permuted: key c = 16 m + r + 8 h
 //                         (m < 8, r < 8, h < 2) sits at index 16 r + 2 m + h, so
 //                         the recurrence thread that owns key rows r and r + 8 of
@@ -347,6 +349,36 @@ __device__ __forceinline__ void mma_bf16(float* d, const uint32_t* a, const uint
         : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "f"(c[0]),
           "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+// D = A * B + C for one m16n8k16 FP16 tile with FP32 accumulation.  The state
+// update S <- S D + U K^end and the output term U (A^qk)^T take their
+// operands in FP16 (10 significand bits against BF16's 7): the delta rule only
+// ever corrects the state along the keys it sees, so rounding error that the
+// K^end operand leaves in other directions is never removed, and FP16 keeps
+// it eight times smaller.  K^end (|x| <= 1), A^qk (|x| <= 1/sqrt(128)) and U
+// fit FP16's range; U is converted with saturation (pack_f16_sat).
+__device__ __forceinline__ void mma_f16(float* d, const uint32_t* a, const uint32_t* b,
+                                        const float* c) {
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, "
+        "{%4,%5,%6,%7}, {%8,%9}, {%10,%11,%12,%13};\n"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b[0]), "r"(b[1]), "f"(c[0]),
+          "f"(c[1]), "f"(c[2]), "f"(c[3]));
+}
+
+// Two floats -> packed FP16x2, round to nearest even, finite values beyond
+// FP16's range saturated to +-65504; `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16_sat(float lo, float hi) {
+    uint32_t r;
+    asm("cvt.rn.satfinite.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+// Two floats -> packed FP16x2 (round to nearest even); `lo` in the low half.
+__device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
+    __half2 v = __floats2half2_rn(lo, hi);
+    return *reinterpret_cast<uint32_t*>(&v);
 }
 
 // Two floats -> packed BF16x2 (round to nearest even); `lo` in the low half.

@@ -148,6 +148,11 @@ __device__ __forceinline__ void st_row4(uint8_t* tile, int t, int lane, float a,
                                         float d) {
     *reinterpret_cast<uint2*>(tile + row4_off(t, lane)) = make_uint2(pack_bf16(a, b), pack_bf16(c, d));
 }
+// Same in FP16 (the K^end rows: the state update's operand is FP16).
+__device__ __forceinline__ void st_row4_f16(uint8_t* tile, int t, int lane, float a, float b,
+                                            float c, float d) {
+    *reinterpret_cast<uint2*>(tile + row4_off(t, lane)) = make_uint2(pack_f16(a, b), pack_f16(c, d));
+}
 // Same, storing the BF16 rounding in `hi` and the BF16 rounding of what it
 // left out in `lo`, so that hi + lo carries about 16 significant bits.
 __device__ __forceinline__ void st_row4_split(uint8_t* hi, uint8_t* lo, int t, int lane, float a,
@@ -335,7 +340,7 @@ __device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, floa
         st_row4_split(tKS, tKsLo, t, lane, ks0, ks1, ks2, ks3);
         st_row4_split(tQS, tQsLo, t, lane, qs0, qs1, qs2, qs3);
         st_row4_split(tKinv, tKinvLo, t, lane, kv0, kv1, kv2, kv3);
-        st_row4(tKen, t, lane, ke0, ke1, ke2, ke3);
+        st_row4_f16(tKen, t, lane, ke0, ke1, ke2, ke3);
     }
     // Every operand tile is complete.
     pair_sync(bid);
@@ -397,7 +402,7 @@ __device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, floa
                 const int i = gq + 8 * hh;
                 const float q0 = (j0 <= i) ? acc[nt][2 * hh] : 0.f;
                 const float q1 = (j0 + 1 <= i) ? acc[nt][2 * hh + 1] : 0.f;
-                *reinterpret_cast<uint32_t*>(tAQK + sw32_off(i, nt) + 4 * tq) = pack_bf16(q0, q1);
+                *reinterpret_cast<uint32_t*>(tAQK + sw32_off(i, nt) + 4 * tq) = pack_f16(q0, q1);
             }
         }
     }

@@ -5,8 +5,8 @@
 // contraction folded as U = V (A^kk B)^T + S K'^T) cannot start the
 // state-dependent part of chunk c + 1 before chunk c's state exists.  For one
 // warp's 8 value columns that part is at least: U^T = K' S^T over the 128 keys
-// (8 m16n8k16 MMAs as two interleaved accumulators, then one add), U^T to a
-// BF16 operand (convert, 8x8 transpose), S^T <- D S^T + (K^end)^T U^T (one
+// (8 m16n8k16 MMAs as two interleaved accumulators, then one add), U^T to an
+// FP16 operand (convert, 8x8 transpose), S^T <- D S^T + (K^end)^T U^T (one
 // MMA per 16-key tile, independent across tiles), and the new S^T to BF16
 // operands (convert, transpose).  The probe runs exactly that chain `iters`
 // times in one warp, with operand fragments held in registers (no memory
@@ -42,7 +42,7 @@ __global__ void __launch_bounds__(32, 1) chain_probe_kernel(int iters, float sca
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             ks[i][j] = pack_bf16(a * (i + 1), -a * (j + 1));
-            ke[i][j] = pack_bf16(-a * (j + 2), a * (i + 2));
+            ke[i][j] = pack_f16(-a * (j + 2), a * (i + 2));
             Sf[i][j] = a * (i - j);
         }
         Sb[i][0] = movm_trans(pack_bf16(Sf[i][0], Sf[i][1]));
@@ -59,13 +59,13 @@ __global__ void __launch_bounds__(32, 1) chain_probe_kernel(int iters, float sca
             mma_bf16(ub, ks[i + 1], Sb[i + 1], ub);
         }
         uint32_t Ub[2];
-        Ub[0] = movm_trans(pack_bf16(ua[0] + ub[0], ua[1] + ub[1]));
-        Ub[1] = movm_trans(pack_bf16(ua[2] + ub[2], ua[3] + ub[3]));
+        Ub[0] = movm_trans(pack_f16_sat(ua[0] + ub[0], ua[1] + ub[1]));
+        Ub[1] = movm_trans(pack_f16_sat(ua[2] + ub[2], ua[3] + ub[3]));
 #pragma unroll
         for (int i = 0; i < 8; ++i) {
 #pragma unroll
             for (int j = 0; j < 4; ++j) Sf[i][j] *= d;
-            mma_bf16(Sf[i], ke[i], Ub, Sf[i]);
+            mma_f16(Sf[i], ke[i], Ub, Sf[i]);
         }
 #pragma unroll
         for (int i = 0; i < 8; ++i) {

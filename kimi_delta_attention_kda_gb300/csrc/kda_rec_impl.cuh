@@ -375,13 +375,13 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
             pp[3] = kh == 0 ? 0.f : pr.y;
         }
         uint32_t Ub[2];
-        Ub[0] = movm_t(pack_bf16(u[0], u[1]));
-        Ub[1] = movm_t(pack_bf16(u[2], u[3]));
+        Ub[0] = movm_t(pack_f16_sat(u[0], u[1]));   // FP16 (mma_f16)
+        Ub[1] = movm_t(pack_f16_sat(u[2], u[3]));
         // S^T <- D S^T + (K^end)^T U^T for this half.
 #pragma unroll
-        for (int i = 0; i < 4; ++i) mma_bf16(Sf[i], f.ke[i], Ub, Sf[i]);
+        for (int i = 0; i < 4; ++i) mma_f16(Sf[i], f.ke[i], Ub, Sf[i]);
         float o[4];
-        mma_bf16(o, f.aqk, Ub, pp);
+        mma_f16(o, f.aqk, Ub, pp);
         if (has_next && ok) ks_load_rest(stage1, L::kVRowBytes, cg, kh, lane, f);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {

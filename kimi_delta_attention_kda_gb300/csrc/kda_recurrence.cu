@@ -146,12 +146,12 @@ __device__ __forceinline__ void chunk_step(const ChunkFrags& f, float (&Sf)[8][4
         mul2(Sf[mt][0], Sf[mt][1], d0);
         mul2(Sf[mt][2], Sf[mt][3], d1);
     }
-    uint32_t Ub[2];
-    Ub[0] = movm_t(pack_bf16(u0[0] + u1[0], u0[1] + u1[1]));
-    Ub[1] = movm_t(pack_bf16(u0[2] + u1[2], u0[3] + u1[3]));
+    uint32_t Ub[2];   // U^T as the FP16 B operand of the update and the output term
+    Ub[0] = movm_t(pack_f16_sat(u0[0] + u1[0], u0[1] + u1[1]));
+    Ub[1] = movm_t(pack_f16_sat(u0[2] + u1[2], u0[3] + u1[3]));
     // S^T <- D S^T + (K^end)^T U^T.
 #pragma unroll
-    for (int mt = 0; mt < 8; ++mt) mma_bf16(Sf[mt], f.ke[mt], Ub, Sf[mt]);
+    for (int mt = 0; mt < 8; ++mt) mma_f16(Sf[mt], f.ke[mt], Ub, Sf[mt]);
     // P^T = s (Q^start)^T S^T, off the state chain.
     float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -161,7 +161,7 @@ __device__ __forceinline__ void chunk_step(const ChunkFrags& f, float (&Sf)[8][4
     }
     // O^T = P^T + A^qk U^T.
     float pin[4] = {p0[0] + p1[0], p0[1] + p1[1], p0[2] + p1[2], p0[3] + p1[3]};
-    mma_bf16(o, f.aqk, Ub, pin);
+    mma_f16(o, f.aqk, Ub, pin);
 }
 
 // A warp's slice of a state (all 128 keys of 8 value columns), BF16, into a
@@ -335,11 +335,11 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                 else
                     ok = false;
             }
-            uint32_t Ub[2];
-            Ub[0] = movm_t(pack_bf16(u0[0] + u1[0], u0[1] + u1[1]));
-            Ub[1] = movm_t(pack_bf16(u0[2] + u1[2], u0[3] + u1[3]));
+            uint32_t Ub[2];   // FP16 (see mma_f16)
+            Ub[0] = movm_t(pack_f16_sat(u0[0] + u1[0], u0[1] + u1[1]));
+            Ub[1] = movm_t(pack_f16_sat(u0[2] + u1[2], u0[3] + u1[3]));
 #pragma unroll
-            for (int mt = 0; mt < 8; ++mt) mma_bf16(Sf[mt], f.ke[mt], Ub, Sf[mt]);
+            for (int mt = 0; mt < 8; ++mt) mma_f16(Sf[mt], f.ke[mt], Ub, Sf[mt]);
             if (has_next && ok) load_frags_ke(stage1, lane, f);
             float p0[4] = {0.f, 0.f, 0.f, 0.f}, p1[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
@@ -350,7 +350,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
             float o[4];
             {
                 float pin[4] = {p0[0] + p1[0], p0[1] + p1[1], p0[2] + p1[2], p0[3] + p1[3]};
-                mma_bf16(o, f.aqk, Ub, pin);
+                mma_f16(o, f.aqk, Ub, pin);
             }
             if (has_next && ok) load_frags_o(stage1, lane, f);
 #pragma unroll
@@ -627,8 +627,8 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
         for (int nt = 0; nt < 4; ++nt) {
             add2(u[0][nt][0], u[0][nt][1], u[1][nt][0], u[1][nt][1]);
             add2(u[0][nt][2], u[0][nt][3], u[1][nt][2], u[1][nt][3]);
-            Ub[nt][0] = movm_t(pack_bf16(u[0][nt][0], u[0][nt][1]));
-            Ub[nt][1] = movm_t(pack_bf16(u[0][nt][2], u[0][nt][3]));
+            Ub[nt][0] = movm_t(pack_f16_sat(u[0][nt][0], u[0][nt][1]));   // FP16 (mma_f16)
+            Ub[nt][1] = movm_t(pack_f16_sat(u[0][nt][2], u[0][nt][3]));
         }
         // S^T <- D S^T + (K^end)^T U^T.
 #pragma unroll
@@ -636,7 +636,7 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
             uint32_t af[4];
             ldsm_x4(af, sKE + sw32_off(16 * mt + rowA, hiA));
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) mma_bf16(Sf[mt][nt], af, Ub[nt], Sf[mt][nt]);
+            for (int nt = 0; nt < 4; ++nt) mma_f16(Sf[mt][nt], af, Ub[nt], Sf[mt][nt]);
         }
         // O^T = P^T + A^qk U^T.
         float o[4][4];
@@ -647,7 +647,7 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
             for (int nt = 0; nt < 4; ++nt) {
                 add2(p[0][nt][0], p[0][nt][1], p[1][nt][0], p[1][nt][1]);
                 add2(p[0][nt][2], p[0][nt][3], p[1][nt][2], p[1][nt][3]);
-                mma_bf16(o[nt], aq, Ub[nt], p[0][nt]);
+                mma_f16(o[nt], aq, Ub[nt], p[0][nt]);
             }
         }
         __syncwarp();
@@ -823,8 +823,8 @@ __global__ void __launch_bounds__(kTransWarps * 32, 1)
         for (int nt = 0; nt < 4; ++nt) {
             add2(u[0][nt][0], u[0][nt][1], u[1][nt][0], u[1][nt][1]);
             add2(u[0][nt][2], u[0][nt][3], u[1][nt][2], u[1][nt][3]);
-            Ub[nt][0] = movm_t(pack_bf16(u[0][nt][0], u[0][nt][1]));
-            Ub[nt][1] = movm_t(pack_bf16(u[0][nt][2], u[0][nt][3]));
+            Ub[nt][0] = movm_t(pack_f16_sat(u[0][nt][0], u[0][nt][1]));   // FP16 (mma_f16)
+            Ub[nt][1] = movm_t(pack_f16_sat(u[0][nt][2], u[0][nt][3]));
         }
         // S^T <- D S^T + (K^end)^T U^T.
 #pragma unroll
@@ -832,7 +832,7 @@ __global__ void __launch_bounds__(kTransWarps * 32, 1)
             uint32_t af[4];
             ldsm_x4(af, sKE + sw32_off(16 * mt + rowA, hiA));
 #pragma unroll
-            for (int nt = 0; nt < 4; ++nt) mma_bf16(Sf[mt][nt], af, Ub[nt], Sf[mt][nt]);
+            for (int nt = 0; nt < 4; ++nt) mma_f16(Sf[mt][nt], af, Ub[nt], Sf[mt][nt]);
         }
         __syncwarp();
         mbar_arrive_if(&empty[s], lane == 0);

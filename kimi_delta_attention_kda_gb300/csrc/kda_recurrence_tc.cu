@@ -35,7 +35,7 @@ constexpr int kTcStages = 6;
 constexpr uint32_t kTcVTileBytes = kChunk * kHeadDim * 2;                                  // 4096
 constexpr uint32_t kTcStageBytes = ((kPacketBytes + kTcVTileBytes + 1023) / 1024) * 1024;   // 18432
 constexpr uint32_t kTcOffSA = kTcStages * kTcStageBytes;      // S (BF16), 128 x 128, SW128
-constexpr uint32_t kTcOffUA = kTcOffSA + 32768;                // U (BF16), 128 x 16, SW32
+constexpr uint32_t kTcOffUA = kTcOffSA + 32768;                // U (FP16), 128 x 16, SW32
 constexpr uint32_t kTcOffVT = kTcOffUA + 4096;                 // V^T (BF16), 128 x 16, SW32
 constexpr uint32_t kTcOffBar = kTcOffVT + 4096;
 constexpr int kTcNumBars = 2 * kTcStages + 7;
@@ -164,7 +164,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 if (filled >> s & 1u) mbar_wait_bounded(&full[s], (fill_parity >> s) & 1u, a.status);
     } else if (warp == kMmaWarp) {
         // ---------------------------------------------------------- MMA issuer
-        const uint32_t id16 = tc::idesc_bf16(128, 16), id128 = tc::idesc_bf16(128, 128);
+        const uint32_t id16 = tc::idesc_bf16(128, 16);
+        // U is FP16 in shared memory, and so are A^qk and K^end (see mma_f16).
+        const uint32_t ih16 = tc::idesc_f16(128, 16), ih128 = tc::idesc_f16(128, 128);
         const uint64_t dVT = tc::smem_desc(vT, 256, tc::kSwizzle32B);
         const uint64_t dUA = tc::smem_desc(uA, 256, tc::kSwizzle32B);
         for (int64_t c = 0; c < nch; ++c) {
@@ -214,9 +216,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             if (lane == 0) {
                 // O += U (A^qk)^T;  S update = U K^end
                 tc::mma_bf16(tmem + kColO, dUA, tc::smem_desc(stage + kOffAQK, 256, tc::kSwizzle32B),
-                             id16, 1);
+                             ih16, 1);
                 tc::mma_bf16(tmem + kColS, dUA, tc::smem_desc(stage + kOffKE, 256, tc::kSwizzle32B),
-                             id128, 0);
+                             ih128, 0);
                 tc::commit(bar_s);
             }
             __syncwarp();
@@ -282,10 +284,10 @@ __global__ void __launch_bounds__(kTcThreads, 1)
                 tc::ld_x8(trow + kColU + 8 * hf, u);
                 tc::wait_ld();
                 st_shared_v4(uA + sw32_off(r, hf),
-                             pack_bf16(__uint_as_float(u[0]), __uint_as_float(u[1])),
-                             pack_bf16(__uint_as_float(u[2]), __uint_as_float(u[3])),
-                             pack_bf16(__uint_as_float(u[4]), __uint_as_float(u[5])),
-                             pack_bf16(__uint_as_float(u[6]), __uint_as_float(u[7])));
+                             pack_f16_sat(__uint_as_float(u[0]), __uint_as_float(u[1])),
+                             pack_f16_sat(__uint_as_float(u[2]), __uint_as_float(u[3])),
+                             pack_f16_sat(__uint_as_float(u[4]), __uint_as_float(u[5])),
+                             pack_f16_sat(__uint_as_float(u[6]), __uint_as_float(u[7])));
             }
             fence_proxy_async_smem();
             tc::fence_before_sync();

@@ -45,6 +45,13 @@ def _bf16_at(buf, base, idx):
     return bits.view(np.float32).astype(np.float64)
 
 
+def _f16_at(buf, base, idx):
+    """Gather FP16 values at byte offsets base + idx from a uint8 array [..., bytes]."""
+    lo = buf[..., base + idx].astype(np.uint16)
+    hi = buf[..., base + idx + 1].astype(np.uint16)
+    return (lo | (hi << 8)).view(np.float16).astype(np.float64)
+
+
 def unpack_packets(packets):
     """Decode packets (uint8 [..., PACKET_BYTES]) into float64 arrays."""
     p = np.ascontiguousarray(packets)
@@ -56,9 +63,9 @@ def unpack_packets(packets):
     return {
         "Kprime": _bf16_at(p, OFF_KS, i128),       # -(A^kk B) K^start^T [..., 16 tokens, 128 keys]
         "Qst_s": _bf16_at(p, OFF_QS, i128),        # s * Q^start rows
-        "KendT": _bf16_at(p, OFF_KE, iKE),         # [..., 128 keys, 16 tokens]
+        "KendT": _f16_at(p, OFF_KE, iKE),          # [..., 128 keys, 16 tokens], FP16
         "AkkB": _bf16_at(p, OFF_AKB, i32),         # A^kk with column j scaled by beta_j
-        "Aqk": _bf16_at(p, OFF_AQK, i32),
+        "Aqk": _f16_at(p, OFF_AQK, i32),           # FP16
         "D": d,
     }
 

@@ -53,12 +53,16 @@ def _check_prep(kda, inp):
     nch = im["Akk"].shape[0]
     s = 1 / np.sqrt(128)
     beta = inp["beta"].double().numpy()
-    # Elementwise BF16 quantities: relative error of one BF16 rounding (2^-9)
-    # plus FP32 arithmetic and the fast exponential.
-    for key, ref in (("Qst_s", s * im["Qst"]), ("KendT", np.swapaxes(im["Kend"], -1, -2))):
-        got = P[key][:nch]
-        err = np.abs(got - ref)
-        assert np.all(err <= 2.0 ** -8 * np.abs(ref) + 1e-30), key
+    # Elementwise quantities: relative error of one BF16 rounding (2^-9) for
+    # Q^start, of one FP16 rounding (2^-11, and half the subnormal spacing,
+    # 2^-25, below 2^-14) for K^end, plus FP32 arithmetic and the fast
+    # exponential.
+    got = P["Qst_s"][:nch]
+    ref = s * im["Qst"]
+    assert np.all(np.abs(got - ref) <= 2.0 ** -8 * np.abs(ref) + 1e-30), "Qst_s"
+    got = P["KendT"][:nch]
+    ref = np.swapaxes(im["Kend"], -1, -2)
+    assert np.all(np.abs(got - ref) <= 2.0 ** -10 * np.abs(ref) + 2.0 ** -24), "KendT"
     np.testing.assert_allclose(P["D"][:nch], im["D"], rtol=2e-5, atol=1e-37)
     # Scores come from BF16 operands with FP32 accumulation.
     assert np.abs(P["Aqk"][:nch] - im["Aqk"]).max() < 2e-3
@@ -143,22 +147,23 @@ def test_stress_families_end_to_end(kda, family):
     tu.check_against_oracle(inp, out, fin)
 
 
-def test_correlated_keys_end_to_end(kda):
+@pytest.mark.parametrize("split", [0, 1, 2, 4])
+def test_correlated_keys_end_to_end(kda, split):
     """Every key points the same way (g = -0.01, beta = 0.5).  The delta rule
-    only ever corrects the state along that one direction, so the BF16
-    rounding of the K^end / K^start operands leaves state error orthogonal to
-    it that is never removed (only decayed, with a time constant of ~100
-    tokens), and the read-out with a random q amplifies it by 1 / (khat . qhat)
-    (about 11).  An emulation of the kernel's rounding points in FP64 gives
-    1.3e-2 for O and 1.4e-2 for the state on this input, so the bound here is
-    3e-2 (max-abs bound unchanged)."""
+    only ever corrects the state along that one direction, so rounding error
+    that the K^end operand of the state update leaves in other directions is
+    never removed (only decayed, with a time constant of ~100 tokens), and the
+    read-out with a random q amplifies it by 1 / (khat . qhat) (about 11).
+    With BF16 operands the kernels measured 1.3e-2 (O) and 1.4e-2 (state)
+    here; with the update's operands in FP16 they measure 3.8e-3 for both on
+    GB300 (every split), so the ordinary tolerance holds."""
     inp = synthetic.stress_inputs("weak_decay_correlated", 300, 2, 9)
-    out, fin = run(kda, inp)
-    o_ref, f_ref = oracle.kda_token(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"])
-    for rel, mx in tu.per_head_errors(out[0].double().numpy(), o_ref[0], 1):
-        assert rel <= 3e-2 and mx <= tu.MAX_ABS_TOL
-    for rel, mx in tu.per_head_errors(fin[0].double().numpy(), f_ref[0], 0):
-        assert rel <= 3e-2 and mx <= tu.MAX_ABS_TOL
+    kda.set_split(split)
+    try:
+        out, fin = run(kda, inp)
+    finally:
+        kda.set_split(0)
+    tu.check_against_oracle(inp, out, fin)
 
 
 def test_split_factors_bitwise_identical(kda):

@@ -87,10 +87,11 @@ def test_forced_long_memory(forced, family):
     """Long memory: with g = -0.01 and every key the same direction the state
     lasts for hundreds of tokens, so a wrong incoming state of any segment
     would show.  The segmented scan rounds each segment's incoming state and
-    map to BF16, so its error against the oracle may exceed the serial
-    chain's by a little, not more.  (On the correlated family the serial
-    chain itself is at ~1.3e-2 against the oracle, which the end-to-end test
-    of that family bounds by 3e-2; see there.)"""
+    map to BF16 (relative error 2^-9 per boundary, which the serial chain's
+    FP32 state does not have), so its error against the oracle may exceed
+    the serial chain's by that much, not more; both stay within the
+    ordinary tolerance (measured on GB300: serial 3.8e-3, segments of one
+    chunk 5.4e-3 on the correlated family)."""
     import oracle
     inp = synthetic.stress_inputs(family, 1024, 2, 91)
     o_ref, f_ref = oracle.kda_token(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"])
@@ -98,13 +99,13 @@ def test_forced_long_memory(forced, family):
     out_s, fin_s = run(forced, inp)
     forced.set_segments(True, 5)
     out, fin = run(forced, inp)
-    bound = 3e-2 if family == "weak_decay_correlated" else tu.REL_FRO_TOL
+    bound = tu.REL_FRO_TOL
     for got, ser, ref, ax in ((out[0], out_s[0], o_ref[0], 1), (fin[0], fin_s[0], f_ref[0], 0)):
         e_seg = tu.per_head_errors(got.double().numpy(), ref, ax)
         e_ser = tu.per_head_errors(ser.double().numpy(), ref, ax)
         for (rel, mx), (rel_s, _) in zip(e_seg, e_ser):
             assert rel <= bound and mx <= tu.MAX_ABS_TOL
-            assert rel <= 1.15 * rel_s + 1e-3, (rel, rel_s)
+            assert rel <= 1.15 * rel_s + 2e-3, (rel, rel_s)
 
 
 def test_forced_deterministic_in_place_and_optional_states(forced):
@@ -325,8 +326,8 @@ def test_two_level_chain_long_memory_and_checkpoints(forced):
         e_seg = tu.per_head_errors(got.double().numpy(), ref, ax)
         e_ser = tu.per_head_errors(ser.double().numpy(), ref, ax)
         for (rel, mx), (rel_s, _) in zip(e_seg, e_ser):
-            assert rel <= 3e-2 and mx <= tu.MAX_ABS_TOL
-            assert rel <= 1.15 * rel_s + 1e-3, (rel, rel_s)
+            assert rel <= tu.REL_FRO_TOL and mx <= tu.MAX_ABS_TOL
+            assert rel <= 1.15 * rel_s + 2e-3, (rel, rel_s)
     ck_inp = synthetic.make_inputs(1, 1024, 2, 7950, init_std=0.02)
     starts = _ck_starts([1024], 128)
     o, f, ck = _ck_call(forced, ck_inp, 128, starts)
