@@ -231,10 +231,16 @@ int kda_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
 /*
  * Whether kda_prefill may run preparation and recurrence as one cooperative
  * launch (1, the default) or always as two kernels (0).  One launch is used
- * for fixed-length batches (cu_seqlens NULL) under engine 0 whose recurrence
- * takes a split of 8 or 16 and leaves at least 16 SMs free: those SMs prepare
- * packets while the recurrence consumes them, each packet behind a ready flag
- * in the workspace.  The results are bit for bit those of the two-kernel path.
+ * for fixed-length batches (cu_seqlens NULL) under engine 0 in two forms, each
+ * packet behind a ready flag in the workspace: (a) few heads, whose
+ * recurrence takes a split of 8 or 16 and leaves at least 16 SMs free: those
+ * SMs prepare packets while the recurrence consumes them; (b) many heads, one
+ * recurrence CTA per (sequence, head) and N * H <= the SM count, when a cost
+ * estimate favours it, and never with checkpoints: one CTA per SM, the first
+ * N * H of them each run a head's recurrence and prepare packets on three warp
+ * pairs, the others prepare on eight; the preparation walks the chunks in
+ * order across all heads so that each head's recurrence starts on its first
+ * packets at once.  The results are bit for bit those of the two-kernel path.
  * Process-wide; returns KDA_ERR_ARG for other values.
  */
 int kda_set_fusion(int on);

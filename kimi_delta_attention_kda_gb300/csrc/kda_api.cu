@@ -373,6 +373,25 @@ bool use_fusion(const Plan& pl, int64_t H, int nsplit, int sms) {
     return pl.geo.chunk_ub * H <= free_sms * pl.geo.chunks_per_seq / 4;
 }
 
+// Whether kda_prefill runs a fixed-length batch of one recurrence CTA per
+// (sequence, head) as the many-head one-launch form (kda_fused.cu): every SM
+// holds one CTA, the first N*H of them each run one head's recurrence while
+// four warp pairs on each of them and eight on every other SM prepare the
+// packets just ahead of it.  Sharing an SM slows both (measured on GB300, B=1,
+// T=8192, H=96: a recurrence chunk step 0.84 -> 1.22 us, a preparation item
+// on one pair 7.2 -> 8.8 us), so the form gains only while enough SMs are left
+// to the preparation alone: measured, one launch against two kernels at
+// T=8192, H=80 679 vs 698 us, H=96 716 vs 732, H=112 765 vs 778, H=128 874 vs
+// 809, H=144 1,048 vs 862; T=2048, H=96 198 vs 202; B=2, T=4096, H=48 370 vs
+// 379.  Hence the rule: at most three quarters of the SMs run a recurrence.
+bool use_fusion_heads(const Plan& pl, int64_t H, int nsplit, int sms, bool checkpoints) {
+    if (!g_fusion || g_engine != 0 || g_split_override || pl.packed || pl.tokens <= 0 ||
+        checkpoints || nsplit != 1)
+        return false;
+    if (!fused_heads_supported(pl.N, H, sms)) return false;
+    return 4 * pl.N * H <= 3 * static_cast<int64_t>(sms) && pl.geo.chunks_per_seq >= 64;
+}
+
 // Launch metadata (packed) and preparation into `ws` (meta) and `packets`.
 // `ordered`: also have the metadata kernel order the sequences longest-first.
 int run_prep(const Plan& pl, const void* q, const void* k, const float* g, const void* beta,
@@ -454,7 +473,10 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
 
     const int nsplit = choose_split(pl.N * H, d->sms);
     const SegChoice sc = plan_segments(pl, H, d->sms, ck != nullptr);
-    const bool fused = sc.segs == 0 && use_fusion(pl, H, nsplit, d->sms);
+    const bool fused_few = sc.segs == 0 && use_fusion(pl, H, nsplit, d->sms);
+    const bool fused_many =
+        !fused_few && sc.segs == 0 && use_fusion_heads(pl, H, nsplit, d->sms, ck != nullptr);
+    const bool fused = fused_few || fused_many;
     const int64_t ws_bytes = pl.meta_bytes + pl.packet_bytes + (fused ? pl.ready_bytes : 0) +
                              3 * sc.state_bytes + sc.meta_bytes + sc.group_bytes;
     uint8_t* ws = nullptr;
@@ -479,9 +501,15 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         prof_record(2, stream);
         prof_record(3, stream);
         if (rc == KDA_OK) {
-            if (launch_fused(q, k, g, beta, v, out, init_state, final_state, ws + pl.meta_bytes,
-                             ready, pl.geo, H, nsplit, kScale, d->status, stream, ck,
-                             beta_logit) == cudaSuccess) {
+            const cudaError_t e =
+                fused_many
+                    ? launch_fused_heads(q, k, g, beta, v, out, init_state, final_state,
+                                         ws + pl.meta_bytes, ready, pl.geo, H, kScale, d->status,
+                                         stream, beta_logit)
+                    : launch_fused(q, k, g, beta, v, out, init_state, final_state,
+                                   ws + pl.meta_bytes, ready, pl.geo, H, nsplit, kScale, d->status,
+                                   stream, ck, beta_logit);
+            if (e == cudaSuccess) {
                 done = true;
                 ++t_launches;
             }
@@ -988,8 +1016,10 @@ extern "C" int kda_plan_fused(int64_t B, int64_t T, int64_t H, int packed, int* 
     DeviceState* d = nullptr;
     rc = device_state(&d);
     if (rc != KDA_OK) return rc;
+    const int nsplit = choose_split(pl.N * H, d->sms);
     *fused = plan_segments(pl, H, d->sms, false).segs == 0 &&
-                     use_fusion(pl, H, choose_split(pl.N * H, d->sms), d->sms)
+                     (use_fusion(pl, H, nsplit, d->sms) ||
+                      use_fusion_heads(pl, H, nsplit, d->sms, false))
                  ? 1
                  : 0;
     return KDA_OK;

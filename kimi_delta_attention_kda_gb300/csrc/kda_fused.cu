@@ -82,7 +82,174 @@ cudaError_t launch_fused_ncg(FusedArgs& f, const prep::PrepMaps& maps, const CUt
                                        smem, stream);
 }
 
+// ---------------------------------------------------------------------------
+// The one-launch form for many (sequence, head) units (fixed layout, one
+// recurrence CTA per unit, N*H <= SMs): every SM holds one 16-warp CTA,
+// launched at 128 registers a thread.  CTAs 0 .. R-1 (R = N*H) each run a
+// whole head's recurrence: warpgroup 0 (warps 0-3) is the quad form (32 value
+// columns a warp, kda_rec_impl.cuh) and takes 232 registers a thread with
+// setmaxnreg, which warpgroup 1 gives up (down to 24: warp 4 is the producer,
+// which waits for each packet's ready flag, warps 5-7 leave); warpgroups 2
+// and 3 prepare packets (four warp pairs, 128 registers).  The other CTAs
+// prepare packets on all 16 warps (eight pairs).  The shares add up to the
+// launch's 512 x 128 registers exactly (128 x (232 + 24 + 128 + 128)).  Every
+// pair of the grid walks one strided list of items numbered chunk first (the
+// preparation's interleaved order), so the packets of each chunk index appear
+// for every head at about the same time and the recurrences stay close behind
+// them; the packets are read back soon after they are written, from L2.  The
+// preparation never waits on the recurrence, and the cooperative launch keeps
+// every CTA resident, so every wait (bounded) ends.  The arithmetic is that of
+// the preparation and quad kernels: the results are bit for bit those of the
+// two-kernel path.
+// ---------------------------------------------------------------------------
+constexpr int kFhWarps = 16;
+constexpr int kFhThreads = kFhWarps * 32;
+constexpr int kFhRecWarps = 4;    // warpgroup 0
+constexpr int kFhProdWarp = 4;    // first warp of warpgroup 1
+constexpr int kFhRecPairs = 4;    // warpgroups 2 and 3
+constexpr int kFhPrepPairs = 8;   // all warps of a preparing CTA
+constexpr int kFhStages = 6;
+constexpr uint32_t kFhRecRegs = 232, kFhProdRegs = 24;
+static_assert(128 * (kFhRecRegs + kFhProdRegs + 2 * 128) == kFhThreads * 128,
+              "register shares must add up to the launch's registers");
+constexpr uint32_t kFhRingBytes = kFhStages * kWideStageBytes;
+constexpr uint32_t kFhRecPrepOff = kFhRingBytes + 1024;   // ring barriers in between
+constexpr uint32_t kFhRecPairBarOff = kFhRecPrepOff + kFhRecPairs * prep::kPrepRegion;
+constexpr uint32_t kFhPrepPairBarOff = kFhPrepPairs * prep::kPrepRegion;
+constexpr uint32_t kFhRecBytes = kFhRecPairBarOff + 8 * kFhRecPairs;
+constexpr uint32_t kFhPrepBytes = kFhPrepPairBarOff + 8 * kFhPrepPairs;
+constexpr uint32_t kFhSmemBytes = (kFhRecBytes > kFhPrepBytes ? kFhRecBytes : kFhPrepBytes) + 1024;
+static_assert(kFhSmemBytes <= 227 * 1024, "one-launch CTA exceeds shared memory");
+static_assert(2 * kFhStages * 8 <= 1024, "ring barriers overflow their slot");
+
+struct FusedHeadsArgs {
+    prep::PrepArgs p;
+    RecArgs r;
+    int64_t rec_blocks;
+    uint32_t* ready;
+};
+
+// The mbarrier of pair `pair` (at bars[pair]), initialised by the pair's
+// first thread, then the pair's named barrier.
+__device__ __forceinline__ uint64_t* fh_pair_barrier(uint64_t* bars, int pair, int hw, int lane,
+                                                     int bid) {
+    uint64_t* bar = bars + pair;
+    if (hw == 0 && lane == 0) {
+        mbar_init(bar, 1);
+        fence_barrier_init();
+    }
+    pair_sync(bid);
+    return bar;
+}
+
+__global__ void __launch_bounds__(kFhThreads, 1)
+    fused_heads_kernel(FusedHeadsArgs f, const __grid_constant__ prep::PrepMaps maps,
+                       const __grid_constant__ CUtensorMap vmap) {
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>(
+        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+    const int warp = threadIdx.x >> 5;
+    const int lane = threadIdx.x & 31;
+    const int64_t rec = f.rec_blocks;
+    const int64_t pairs = rec * kFhRecPairs + (static_cast<int64_t>(gridDim.x) - rec) * kFhPrepPairs;
+    if (blockIdx.x < rec) {
+        const RecArgs& a = f.r;
+        const int64_t n = blockIdx.x / a.H;
+        const int64_t h = blockIdx.x - n * a.H;
+        int64_t c_begin, nch, tok0, seqlen;
+        seq_span(a.geo, n, c_begin, nch, tok0, seqlen);   // fixed layout: always valid
+        uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFhRingBytes);
+        uint64_t* empty = full + kFhStages;
+        if (threadIdx.x == 0) {
+            for (int s = 0; s < kFhStages; ++s) {
+                mbar_init(&full[s], 1);
+                mbar_init(&empty[s], kFhRecWarps);
+            }
+            fence_barrier_init();
+        }
+        __syncthreads();
+        if (warp < kFhRecWarps) {
+            asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;\n" ::"n"(kFhRecRegs) : "memory");
+            wide_consume<4, kFhStages, false>(a, smem, full, empty, warp, lane, n, h, c_begin, nch,
+                                              tok0, seqlen);
+        } else if (warp < 2 * kFhRecWarps) {
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kFhProdRegs) : "memory");
+            if (warp == kFhProdWarp)
+                wide_produce<kFhStages>(a, &vmap, smem, full, empty, lane, h, c_begin, nch, tok0,
+                                        f.ready);
+        } else {
+            const int pair = (warp - 2 * kFhRecWarps) >> 1, hw = warp & 1;
+            const int bid = 1 + pair;
+            uint64_t* bar = fh_pair_barrier(reinterpret_cast<uint64_t*>(smem + kFhRecPairBarOff),
+                                            pair, hw, lane, bid);
+            prep::run_items(f.p, maps, smem + kFhRecPrepOff + pair * prep::kPrepRegion, bar, bid, hw,
+                            lane, static_cast<int64_t>(blockIdx.x) * kFhRecPairs + pair, pairs,
+                            f.ready);
+        }
+    } else {
+        const int pair = warp >> 1, hw = warp & 1, bid = 1 + pair;
+        uint64_t* bar = fh_pair_barrier(reinterpret_cast<uint64_t*>(smem + kFhPrepPairBarOff), pair,
+                                        hw, lane, bid);
+        prep::run_items(f.p, maps, smem + pair * prep::kPrepRegion, bar, bid, hw, lane,
+                        rec * kFhRecPairs + (static_cast<int64_t>(blockIdx.x) - rec) * kFhPrepPairs +
+                            pair,
+                        pairs, f.ready);
+    }
+}
+
 }  // namespace
+
+bool fused_heads_supported(int64_t n_seqs, int64_t H, int sms) {
+    const int64_t units = n_seqs * H;
+    return units >= 1 && units <= sms;
+}
+
+cudaError_t launch_fused_heads(const void* q, const void* k, const float* g, const void* beta,
+                               const void* v, void* out, const void* init_state, void* final_state,
+                               uint8_t* packets, uint32_t* ready, const SeqGeometry& geo, int64_t H,
+                               float scale, int* status, cudaStream_t stream, bool beta_logit) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+    cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+    if (e != cudaSuccess) return e;
+    if (geo.cu_chunks || geo.seg_chunks || geo.tokens <= 0 || geo.tokens >= (int64_t(1) << 31) ||
+        !fused_heads_supported(geo.n_seqs, H, sms))
+        return cudaErrorInvalidValue;
+    FusedHeadsArgs f;
+    if (!prep::make_prep_args(&f.p, beta, packets, geo, H, scale, status, beta_logit))
+        return cudaErrorInvalidValue;
+    f.p.interleave = 1;
+    f.r.v = static_cast<const __nv_bfloat16*>(v);
+    f.r.out = static_cast<__nv_bfloat16*>(out);
+    f.r.init_state = static_cast<const __nv_bfloat16*>(init_state);
+    f.r.final_state = static_cast<__nv_bfloat16*>(final_state);
+    f.r.packets = packets;
+    f.r.geo = geo;
+    f.r.H = H;
+    f.r.nsplit = 1;
+    f.r.status = status;
+    f.r.ck = Checkpoints{nullptr, nullptr, 1, 0};
+    f.r.final_ident = nullptr;
+    f.rec_blocks = geo.n_seqs * H;
+    f.ready = ready;
+    prep::PrepMaps maps;
+    e = prep::encode_maps(&maps, q, k, g, geo.tokens, H);
+    if (e != cudaSuccess) return e;
+    CUtensorMap vmap;
+    e = encode_v_map_sw128(&vmap, v, geo.tokens, H);
+    if (e != cudaSuccess) return e;
+    static bool configured[64] = {};
+    if (!configured[dev]) {
+        e = cudaFuncSetAttribute(fused_heads_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                 static_cast<int>(kFhSmemBytes));
+        if (e != cudaSuccess) return e;
+        configured[dev] = true;
+    }
+    void* args[] = {&f, &maps, &vmap};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(fused_heads_kernel),
+                                       dim3(static_cast<unsigned>(sms)), dim3(kFhThreads), args,
+                                       kFhSmemBytes, stream);
+}
 
 bool fused_supported(int64_t n_seqs, int64_t H, int nsplit, int sms) {
     if (nsplit != 8 && nsplit != 16) return false;

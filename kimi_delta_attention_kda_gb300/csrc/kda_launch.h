@@ -145,6 +145,15 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
                          int nsplit, float scale, int* status, cudaStream_t stream,
                          const Checkpoints* ck = nullptr, bool beta_logit = false);
 
+// Preparation and the wide one-CTA-per-head recurrence as one cooperative
+// launch of one 16-warp CTA per SM, for fixed-length batches of at most one
+// (sequence, head) unit per SM (kda_fused.cu).  `ready` as for launch_fused.
+bool fused_heads_supported(int64_t n_seqs, int64_t H, int sms);
+cudaError_t launch_fused_heads(const void* q, const void* k, const float* g, const void* beta,
+                               const void* v, void* out, const void* init_state, void* final_state,
+                               uint8_t* packets, uint32_t* ready, const SeqGeometry& geo, int64_t H,
+                               float scale, int* status, cudaStream_t stream, bool beta_logit);
+
 // Tensor map of v viewed as a 2-D BF16 array [tokens][H * 128], boxes of
 // 16 tokens x `cols` value columns.
 cudaError_t encode_v_map(CUtensorMap* map, const void* v, int64_t tokens, int64_t H, int cols);

@@ -74,8 +74,14 @@ struct PrepArgs {
     int64_t n_chunk_heads;   // < 2^31, so item, chunk and head indices fit 32 bits
     float scale;
     int beta_logit;          // 1: the beta tensor holds logits, beta = sigmoid(logit)
+    // Fixed layout only: 1 numbers the items chunk index first, sequence
+    // second ((chunk-in-sequence * N + sequence) * H + head), so that a
+    // launch whose recurrence consumes every sequence at once gets each
+    // sequence's first chunks first; 0: sequence by sequence.
+    int interleave;
     FastDiv div_h;           // by H
     FastDiv div_cps;         // by geo.chunks_per_seq (fixed layout)
+    FastDiv div_n;           // by geo.n_seqs (fixed layout, interleave)
 };
 
 // The preparation's arguments for `geo` and H heads; false when the item
@@ -84,6 +90,7 @@ inline bool make_prep_args(PrepArgs* a, const void* beta, uint8_t* packets, cons
                            int64_t H, float scale, int* status, bool beta_logit = false) {
     a->beta = static_cast<const __nv_bfloat16*>(beta);
     a->beta_logit = beta_logit ? 1 : 0;
+    a->interleave = 0;
     a->packets = packets;
     a->geo = geo;
     a->geo.status = status;
@@ -95,6 +102,8 @@ inline bool make_prep_args(PrepArgs* a, const void* beta, uint8_t* packets, cons
     if (cps <= 0 || cps >= (int64_t(1) << 31)) return false;
     a->div_h = make_fastdiv(static_cast<uint32_t>(H));
     a->div_cps = make_fastdiv(static_cast<uint32_t>(cps));
+    if (geo.n_seqs <= 0 || geo.n_seqs >= (int64_t(1) << 31)) return false;
+    a->div_n = make_fastdiv(static_cast<uint32_t>(geo.n_seqs));
     return true;
 }
 
@@ -182,6 +191,18 @@ __device__ __forceinline__ bool item_range(const PrepArgs& a, int64_t item, int6
         const int64_t n = find_sequence(a.geo.cu_chunks, a.geo.n_seqs, c);
         *t0 = a.geo.cu_seqlens[n] + kChunk * (c - a.geo.cu_chunks[n]);
         *len = a.geo.cu_seqlens[n + 1] - *t0;
+    } else if (a.interleave) {
+        // c32 = chunk-in-sequence * N + sequence; the packet goes to the
+        // sequence-by-sequence chunk number.
+        const uint32_t ci32 = fast_div(c32, a.div_n);
+        const int64_t n = c32 - ci32 * a.div_n.d;
+        const int64_t ci = ci32;
+        *t0 = n * a.geo.tokens_per_seq + kChunk * ci;
+        *len = a.geo.tokens_per_seq - kChunk * ci;
+        if (*len > kChunk) *len = kChunk;
+        *c_out = n * a.geo.chunks_per_seq + ci;
+        *h_out = h;
+        return true;
     } else {
         const uint32_t n32 = fast_div(c32, a.div_cps);
         const int64_t n = n32;
@@ -529,9 +550,9 @@ __device__ __forceinline__ uint64_t* pair_barrier(uint8_t* smem, int pair, int h
 
 // A pair's share of the items: items first, first + stride, ... .  Both warps
 // run this loop; warp 0's lane 0 issues the copies.  With `ready` set,
-// ready[item] becomes 1 (release, GPU scope) once the item's packet is in
-// global memory; the flag of an item is published when the pair has issued
-// the next item's loads, or at the end.
+// ready[chunk * H + head] (the packet's index) becomes 1 (release, GPU scope)
+// once the item's packet is in global memory; the flag of an item is
+// published when the pair has issued the next item's loads, or at the end.
 __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& maps, uint8_t* region,
                                           uint64_t* bar, int bid, int hw, int lane, int64_t first,
                                           int64_t stride, uint32_t* ready) {
@@ -589,7 +610,7 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
             bulk_s2g(a.packets + (c * a.H + h) * static_cast<int64_t>(kPacketBytes), region,
                      kPacketBytes);
             bulk_commit();
-            pending = item;
+            pending = c * a.H + h;   // the packet's index (the item's, unless interleaved)
         }
     }
     if (issuer) {

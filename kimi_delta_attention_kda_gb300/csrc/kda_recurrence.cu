@@ -406,57 +406,14 @@ __global__ void __launch_bounds__((NW + 1) * 32)
 }
 
 // ---------------------------------------------------------------------------
-// Quad-width variant for one CTA per head: 4 consumer warps of 32 value
-// columns (four 8-column n-tiles sharing every A fragment), so the CTA reads
-// each chunk's K', Q^start and K^end fragments from shared memory 4 times
-// rather than once per 8 columns (with 16 warps of 8 columns the
-// shared-memory pipe, not the tensor pipe, limits a chunk step).  The BF16
-// copy of the state is not kept: each k-step converts its slice of the
-// incoming FP32 state just before the U and P MMAs that use it (the same
-// conversions as the other variants, so the results are bitwise theirs).
+// Quad-width variant for one CTA per head (kda_rec_impl.cuh, wide_consume
+// with four n-tiles per warp): 4 consumer warps of 32 value columns and a
+// producer warp.
 // ---------------------------------------------------------------------------
-constexpr uint32_t kQuadVRowBytes = kHeadDim * 2;
-// The V tile sits 1024-aligned after the packet as two [16][64] slabs with
-// the 128-byte swizzle (rows 256 bytes apart would put the eight rows of
-// each transposing load in the same banks).
-constexpr uint32_t kQuadVOff = ((kPacketBytes + 1023) / 1024) * 1024;
-constexpr uint32_t kQuadStageBytes = ((kQuadVOff + kChunk * kQuadVRowBytes + 1023) / 1024) * 1024;
 constexpr int kQuadWarps = 4;
 constexpr int kQuadStages = 8;
-constexpr uint32_t kQuadBarOff = kQuadStages * kQuadStageBytes;
+constexpr uint32_t kQuadBarOff = kQuadStages * kWideStageBytes;
 constexpr uint32_t kQuadSmemBytes = kQuadBarOff + 2 * kQuadStages * 8 + 1024;
-
-// V rows tok .. tok + 15 of head h into the stage's two swizzled slabs.
-__device__ __forceinline__ void quad_load_v(uint8_t* stage, const CUtensorMap* vmap, int64_t h,
-                                            int64_t tok, uint64_t* bar) {
-    tma_load_2d(stage + kQuadVOff, vmap, static_cast<int32_t>(h * kHeadDim), static_cast<int32_t>(tok),
-                bar);
-    tma_load_2d(stage + kQuadVOff + kChunk * 128, vmap, static_cast<int32_t>(h * kHeadDim + 64),
-                static_cast<int32_t>(tok), bar);
-}
-
-// A warp's slice of a state (all 128 keys of 32 value columns), BF16, into a
-// [128 value][128 key] state at dst.
-__device__ __forceinline__ void quad_store_state(__nv_bfloat16* dst, const float (&Sf)[8][4][4],
-                                                 int vcol, int g8, int t4) {
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            const int key = 16 * mt + g8;
-            const int val = vcol + 8 * nt + 2 * t4;
-            dst[(int64_t)val * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][nt][0]);
-            dst[(int64_t)(val + 1) * kHeadDim + key] = __float2bfloat16_rn(Sf[mt][nt][1]);
-            dst[(int64_t)val * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][nt][2]);
-            dst[(int64_t)(val + 1) * kHeadDim + key + 8] = __float2bfloat16_rn(Sf[mt][nt][3]);
-        }
-}
-
-// Modes of the quad kernel: kQuadPlain; kQuadCkpt writes checkpoints (a
-// separate instantiation keeps the check out of the loop of the plain call,
-// which is at the register limit).
-constexpr int kQuadPlain = 0;
-constexpr int kQuadCkpt = 1;
 
 template <int kMode>
 __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
@@ -468,7 +425,6 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
     uint64_t* empty = full + kQuadStages;
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
-    constexpr bool kCkpt = kMode == kQuadCkpt;
     const int64_t n_slot = blockIdx.x / a.H;
     const int64_t h = blockIdx.x - n_slot * a.H;
     if (n_slot < a.geo.first_slot) return;   // runs in the other launch
@@ -484,183 +440,11 @@ __global__ void __launch_bounds__((kQuadWarps + 1) * 32, 1)
         fence_barrier_init();
     }
     __syncthreads();
-
-    if (warp == kQuadWarps) {
-        // ------------------------------------------------------------ producer
-        uint32_t fill_parity = 0, filled = 0;
-        bool ok = true;
-        for (int64_t c = 0; c < nch && ok; ++c) {
-            const int s = static_cast<int>(c % kQuadStages);
-            if (c >= kQuadStages)
-                ok = mbar_wait_warp_sleep(&empty[s], ((c / kQuadStages) - 1) & 1, a.status);
-            if (!ok) break;
-            uint8_t* stage = smem + s * kQuadStageBytes;
-            if (lane == 0) {
-                mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * kQuadVRowBytes);
-                bulk_g2s(stage, a.packets + ((c_begin + c) * a.H + h) * static_cast<int64_t>(kPacketBytes),
-                         kPacketBytes, &full[s]);
-                quad_load_v(stage, &vmap, h, tok0 + kChunk * c, &full[s]);
-            }
-            __syncwarp();
-            fill_parity ^= (filled >> s & 1u) << s;
-            filled |= 1u << s;
-        }
-        if (!ok)
-            for (int s = 0; s < kQuadStages; ++s)
-                if (filled >> s & 1u) mbar_wait_bounded(&full[s], (fill_parity >> s) & 1u, a.status);
-        return;
-    }
-
-    // ---------------------------------------------------------------- consumers
-    const int g8 = lane >> 2, t4 = lane & 3;
-    const int vcol = 32 * warp;   // first of this warp's 32 value columns
-    const int64_t state_base = (n * a.H + h) * kHeadDim * kHeadDim;
-    const uint32_t rowA = (lane & 7) + ((lane >> 3) & 1) * 8;
-    const uint32_t hiA = lane >> 4;
-
-    float Sf[8][4][4];
-#pragma unroll
-    for (int mt = 0; mt < 8; ++mt)
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            if (a.init_state) {
-                const __nv_bfloat16* src = a.init_state + state_base;
-                const int key = 16 * mt + g8;
-                const int val = vcol + 8 * nt + 2 * t4;
-                Sf[mt][nt][0] = __bfloat162float(src[(int64_t)val * kHeadDim + key]);
-                Sf[mt][nt][1] = __bfloat162float(src[(int64_t)(val + 1) * kHeadDim + key]);
-                Sf[mt][nt][2] = __bfloat162float(src[(int64_t)val * kHeadDim + key + 8]);
-                Sf[mt][nt][3] = __bfloat162float(src[(int64_t)(val + 1) * kHeadDim + key + 8]);
-            } else {
-                Sf[mt][nt][0] = Sf[mt][nt][1] = Sf[mt][nt][2] = Sf[mt][nt][3] = 0.f;
-            }
-        }
-
-    bool ok = true;
-    // Checkpoints are numbered per sequence: a segment's chunks start at
-    // chunk c_off of sequence n_ck.
-    int64_t n_ck = n, c_off = 0;
-    if (kCkpt) {
-        if (a.geo.seg_chunks) {
-            n_ck = n / a.geo.segs_per_seq;
-            c_off = (n - n_ck * a.geo.segs_per_seq) * a.geo.seg_chunks;
-        } else if (a.geo.seg_seq) {
-            n_ck = a.geo.seg_seq[n];
-            c_off = c_begin - a.geo.seq_chunks[n_ck];
-        }
-    }
-    // next chunk whose incoming state is a checkpoint
-    int64_t ck_next = kCkpt ? ((c_off + a.ck.every - 1) / a.ck.every) * a.ck.every - c_off : 0;
-    for (int64_t c = 0; c < nch; ++c) {
-        if (kCkpt && c == ck_next) {
-            ck_next += a.ck.every;
-            __nv_bfloat16* dst = checkpoint_dst(a, n_ck, h, (c_off + c) / a.ck.every);
-            if (dst) quad_store_state(dst, Sf, vcol, g8, t4);
-        }
-        const int s = static_cast<int>(c % kQuadStages);
-        if (!mbar_wait_warp(&full[s], (c / kQuadStages) & 1, a.status)) {
-            ok = false;
-            break;
-        }
-        const uint8_t* stage = smem + s * kQuadStageBytes;
-        const uint32_t sKS = smem_u32(stage + kOffKS);
-        const uint32_t sQS = smem_u32(stage + kOffQS);
-        const uint32_t sKE = smem_u32(stage + kOffKE);
-        int64_t len = seqlen - kChunk * c;
-        if (len > kChunk) len = kChunk;
-
-        // U^T = (A^kk B) V^T + K' S^T and P^T = s (Q^start)^T S^T from the
-        // incoming state, four n-tiles, two accumulators each.
-        float u[2][4][4], p[2][4][4];
-#pragma unroll
-        for (int x = 0; x < 2; ++x)
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt)
-#pragma unroll
-                for (int j = 0; j < 4; ++j) u[x][nt][j] = p[x][nt][j] = 0.f;
-        {
-            uint32_t akb[4];
-            ldsm_x4(akb, smem_u32(stage + kOffAKB + sw32_off(rowA, hiA)));
-#pragma unroll
-            for (int hp = 0; hp < 2; ++hp) {
-                // lanes 0-15: tokens of columns vcol + 16 hp .. + 7; lanes 16-31: + 8.
-                uint32_t vb[4];
-                const uint8_t* sV = stage + kQuadVOff +
-                                    sw128_off(kChunk, lane & 15, (vcol + 16 * hp) / 8 + (lane >> 4));
-                asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
-                             : "=r"(vb[0]), "=r"(vb[1]), "=r"(vb[2]), "=r"(vb[3])
-                             : "r"(smem_u32(sV)));
-                mma_bf16(u[0][2 * hp], akb, vb, u[0][2 * hp]);
-                mma_bf16(u[0][2 * hp + 1], akb, vb + 2, u[0][2 * hp + 1]);
-            }
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk) {
-            uint32_t kf[4], qf[4];
-            ldsm_x4(kf, sKS + sw128_off(16, rowA, 2 * kk + hiA));
-            ldsm_x4(qf, sQS + sw128_off(16, rowA, 2 * kk + hiA));
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                const uint32_t sb[2] = {movm_t(pack_bf16(Sf[kk][nt][0], Sf[kk][nt][1])),
-                                        movm_t(pack_bf16(Sf[kk][nt][2], Sf[kk][nt][3]))};
-                mma_bf16(u[kk & 1][nt], kf, sb, u[kk & 1][nt]);
-                mma_bf16(p[kk & 1][nt], qf, sb, p[kk & 1][nt]);
-            }
-        }
-        // D S^T in place.
-        {
-            const float4* dp = reinterpret_cast<const float4*>(stage + kOffD) + 4 * g8;
-#pragma unroll
-            for (int j = 0; j < 4; ++j) {
-                const float4 d = dp[j];
-#pragma unroll
-                for (int nt = 0; nt < 4; ++nt) {
-                    mul2(Sf[2 * j][nt][0], Sf[2 * j][nt][1], d.x);
-                    mul2(Sf[2 * j][nt][2], Sf[2 * j][nt][3], d.y);
-                    mul2(Sf[2 * j + 1][nt][0], Sf[2 * j + 1][nt][1], d.z);
-                    mul2(Sf[2 * j + 1][nt][2], Sf[2 * j + 1][nt][3], d.w);
-                }
-            }
-        }
-        uint32_t Ub[4][2];
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            add2(u[0][nt][0], u[0][nt][1], u[1][nt][0], u[1][nt][1]);
-            add2(u[0][nt][2], u[0][nt][3], u[1][nt][2], u[1][nt][3]);
-            Ub[nt][0] = movm_t(pack_f16_sat(u[0][nt][0], u[0][nt][1]));   // FP16 (mma_f16)
-            Ub[nt][1] = movm_t(pack_f16_sat(u[0][nt][2], u[0][nt][3]));
-        }
-        // S^T <- D S^T + (K^end)^T U^T.
-#pragma unroll
-        for (int mt = 0; mt < 8; ++mt) {
-            uint32_t af[4];
-            ldsm_x4(af, sKE + sw32_off(16 * mt + rowA, hiA));
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) mma_f16(Sf[mt][nt], af, Ub[nt], Sf[mt][nt]);
-        }
-        // O^T = P^T + A^qk U^T.
-        float o[4][4];
-        {
-            uint32_t aq[4];
-            ldsm_x4(aq, smem_u32(stage + kOffAQK + sw32_off(rowA, hiA)));
-#pragma unroll
-            for (int nt = 0; nt < 4; ++nt) {
-                add2(p[0][nt][0], p[0][nt][1], p[1][nt][0], p[1][nt][1]);
-                add2(p[0][nt][2], p[0][nt][3], p[1][nt][2], p[1][nt][3]);
-                mma_f16(o[nt], aq, Ub[nt], p[0][nt]);
-            }
-        }
-        __syncwarp();
-        mbar_arrive_if(&empty[s], lane == 0);
-        __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + g8) * a.H + h) * kHeadDim + vcol + 2 * t4;
-#pragma unroll
-        for (int nt = 0; nt < 4; ++nt) {
-            st_global_u32_if(orow + 8 * nt, pack_bf16(o[nt][0], o[nt][1]), g8 < len);
-            st_global_u32_if(orow + 8 * a.H * kHeadDim + 8 * nt, pack_bf16(o[nt][2], o[nt][3]), g8 + 8 < len);
-        }
-    }
-
-    if (ok && a.final_state) quad_store_state(a.final_state + state_base, Sf, vcol, g8, t4);
+    if (warp == kQuadWarps)
+        wide_produce<kQuadStages>(a, &vmap, smem, full, empty, lane, h, c_begin, nch, tok0, nullptr);
+    else
+        wide_consume<4, kQuadStages, kMode == kWideCkpt>(a, smem, full, empty, warp, lane, n, h,
+                                                         c_begin, nch, tok0, seqlen);
 }
 
 template <int kMode>
@@ -686,8 +470,8 @@ cudaError_t launch_quad_t(const RecArgs& a, int64_t blocks, cudaStream_t stream)
 }
 
 cudaError_t launch_quad(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
-    return a.ck.states ? launch_quad_t<kQuadCkpt>(a, blocks, stream)
-                       : launch_quad_t<kQuadPlain>(a, blocks, stream);
+    return a.ck.states ? launch_quad_t<kWideCkpt>(a, blocks, stream)
+                       : launch_quad_t<kWidePlain>(a, blocks, stream);
 }
 
 // ---------------------------------------------------------------------------
@@ -727,11 +511,11 @@ __global__ void __launch_bounds__(kTransWarps * 32, 1)
     // Chunk c's packet and V tile into its stage (warp 0, lane 0).
     auto load = [&](int64_t c) {
         const int s = static_cast<int>(c % kQuadStages);
-        uint8_t* stage = smem + s * kQuadStageBytes;
-        mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * kQuadVRowBytes);
+        uint8_t* stage = smem + s * kWideStageBytes;
+        mbar_arrive_expect_tx(&full[s], kPacketBytes + kChunk * kWideVRowBytes);
         bulk_g2s(stage, a.packets + ((c_begin + c) * a.H + h) * static_cast<int64_t>(kPacketBytes),
                  kPacketBytes, &full[s]);
-        quad_load_v(stage, &vmap, h, tok0 + kChunk * c, &full[s]);
+        wide_load_v(stage, &vmap, h, tok0 + kChunk * c, &full[s]);
     };
     int64_t issued = nch < kQuadStages ? nch : kQuadStages;
     if (warp == 0 && lane == 0)
@@ -765,7 +549,7 @@ __global__ void __launch_bounds__(kTransWarps * 32, 1)
             ok = false;
             break;
         }
-        const uint8_t* stage = smem + s * kQuadStageBytes;
+        const uint8_t* stage = smem + s * kWideStageBytes;
         const uint32_t sKS = smem_u32(stage + kOffKS);
         const uint32_t sKE = smem_u32(stage + kOffKE);
 
@@ -783,7 +567,7 @@ __global__ void __launch_bounds__(kTransWarps * 32, 1)
 #pragma unroll
             for (int hp = 0; hp < 2; ++hp) {
                 uint32_t vb[4];
-                const uint8_t* sV = stage + kQuadVOff +
+                const uint8_t* sV = stage + kWideVOff +
                                     sw128_off(kChunk, lane & 15, (vcol + 16 * hp) / 8 + (lane >> 4));
                 asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0,%1,%2,%3}, [%4];"
                              : "=r"(vb[0]), "=r"(vb[1]), "=r"(vb[2]), "=r"(vb[3])
@@ -855,7 +639,7 @@ __global__ void __launch_bounds__(kTransWarps * 32, 1)
             mbar_wait_bounded(&full[cc % kQuadStages], (cc / kQuadStages) & 1, a.status);
     }
     __nv_bfloat16* dst = ident ? a.final_ident : a.final_state;
-    if (ok && dst) quad_store_state(dst + state_base, Sf, vcol, g8, t4);
+    if (ok && dst) wide_store_state<4>(dst + state_base, Sf, vcol, g8, t4);
 }
 
 template <int NCG>

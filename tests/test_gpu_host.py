@@ -152,11 +152,12 @@ def test_host_graph_capture(kda, pieces):
 
 def test_launch_counts(kda):
     """kda_last_call_launches reports the kernels one call enqueued: the
-    preparation and the recurrence; one cooperative launch; the segmented
+    preparation and the recurrence (more heads than SMs); one cooperative
+    launch (many heads, or few heads and a short sequence); the segmented
     scan's four kernels (six with the two-level chain)."""
     from kimi_delta_attention_kda_gb300 import _lib
-    for (B, T, H), want in (((1, 2048, 96), 2), ((1, 256, 1), 1), ((1, 8192, 6), 4),
-                            ((1, 65536, 1), 6)):
+    for (B, T, H), want in (((2, 2048, 96), 2), ((1, 2048, 96), 1), ((1, 256, 1), 1),
+                            ((1, 8192, 6), 4), ((1, 65536, 1), 6)):
         d = tu.to_device(synthetic.make_inputs(B, T, H, 9600, init_std=0.02))
         kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"])
         torch.cuda.synchronize()

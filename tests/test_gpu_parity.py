@@ -417,9 +417,57 @@ def test_fused_matches_two_kernels_bitwise(fusion_toggle, B, T, H):
 
 
 def test_fused_not_planned_where_it_cannot_run(kda):
-    assert not kda.plan_fused(1, 8192, 96, False)   # one CTA per head fills the SMs
+    assert not kda.plan_fused(2, 8192, 96, False)   # 192 recurrence CTAs: more than the SMs
+    assert not kda.plan_fused(1, 8192, 128, False)  # too few SMs left to the preparation
+    assert not kda.plan_fused(1, 512, 96, False)    # too short to pay
     assert not kda.plan_fused(1, 8192, 6, True)      # packed layout
     assert not kda.plan_fused(1, 0, 6, False)        # no tokens
+
+
+# ----------------------------------------------------------------------------
+# The many-head one-launch form: one recurrence CTA per (sequence, head) and
+# the preparation in the same launch (warp pairs on every SM)
+# ----------------------------------------------------------------------------
+
+@pytest.mark.parametrize("B,T,H", [(1, 8192, 96), (2, 1024, 48), (1, 1033, 100), (1, 2048, 80)])
+def test_fused_many_heads_matches_two_kernels_bitwise(fusion_toggle, B, T, H):
+    """Bit for bit the preparation followed by the one-CTA-per-head recurrence
+    (the same arithmetic), checked twice so that the second call meets the
+    first call's stale ready flags in reused pool memory; a sample of heads
+    against the oracle."""
+    kda = fusion_toggle
+    assert kda.auto_split(B, H) == 1
+    assert kda.plan_fused(B, T, H, False)
+    inp = synthetic.make_inputs(B, T, H, 4200 + T, init_std=0.02)
+    kda.set_fusion(True)
+    fused = run(kda, inp)
+    again = run(kda, inp)
+    kda.set_fusion(False)
+    assert not kda.plan_fused(B, T, H, False)
+    split = run(kda, inp)
+    for a, b in ((fused, split), (again, split)):
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    tu.check_against_oracle(inp, fused[0], fused[1], heads=[0, H // 2, H - 1])
+
+
+def test_fused_many_heads_in_place_and_no_states(fusion_toggle):
+    kda = fusion_toggle
+    inp = synthetic.make_inputs(1, 1024, 96, 4300, init_std=0.02)
+    assert kda.plan_fused(1, 1024, 96, False)
+    ref = run(kda, inp)
+    d = tu.to_device(inp)
+    state = d["init_state"].clone()
+    out, fin = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], state, final_state=state)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    assert torch.equal(out.cpu(), ref[0]) and torch.equal(state.cpu(), ref[1])
+    out, fin = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], None,
+                               output_final_state=False)
+    torch.cuda.synchronize()
+    assert fin is None and kda.device_status() == 0
+    zero = dict(inp)
+    zero["init_state"] = None
+    tu.check_against_oracle(zero, out.cpu(), run(kda, zero)[1], heads=[5])
 
 
 def test_fused_repeated_calls_and_in_place(fusion_toggle):
