@@ -176,7 +176,8 @@ int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
     }
     if (g.chunk_ub > kMaxElems / (H * kPacketBytes)) return KDA_ERR_SHAPE;
     p->packet_bytes = g.chunk_ub * H * static_cast<int64_t>(kPacketBytes);
-    p->ready_bytes = ((g.chunk_ub * H * 4 + 255) / 256) * 256;
+    // One flag per packet, then the many-head one-launch form's item counter.
+    p->ready_bytes = g.chunk_ub > 0 ? ((g.chunk_ub * H * 4 + 4 + 255) / 256) * 256 : 0;
     return KDA_OK;
 }
 

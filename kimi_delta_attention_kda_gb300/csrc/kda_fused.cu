@@ -96,7 +96,8 @@ cudaError_t launch_fused_ncg(FusedArgs& f, const prep::PrepMaps& maps, const CUt
 // pair of the grid walks one strided list of items numbered chunk first (the
 // preparation's interleaved order), so the packets of each chunk index appear
 // for every head at about the same time and the recurrences stay close behind
-// them; the packets are read back soon after they are written, from L2.  The
+// them.  The pairs take items in order from a counter, so that the pairs that
+// share an SM with a recurrence (slower) take fewer than the others.  The
 // preparation never waits on the recurrence, and the cooperative launch keeps
 // every CTA resident, so every wait (bounded) ends.  The arithmetic is that of
 // the preparation and quad kernels: the results are bit for bit those of the
@@ -116,8 +117,9 @@ constexpr uint32_t kFhRingBytes = kFhStages * kWideStageBytes;
 constexpr uint32_t kFhRecPrepOff = kFhRingBytes + 1024;   // ring barriers in between
 constexpr uint32_t kFhRecPairBarOff = kFhRecPrepOff + kFhRecPairs * prep::kPrepRegion;
 constexpr uint32_t kFhPrepPairBarOff = kFhPrepPairs * prep::kPrepRegion;
-constexpr uint32_t kFhRecBytes = kFhRecPairBarOff + 8 * kFhRecPairs;
-constexpr uint32_t kFhPrepBytes = kFhPrepPairBarOff + 8 * kFhPrepPairs;
+// Each pair's mbarrier and its item slot (run_items' counter mode) follow the regions.
+constexpr uint32_t kFhRecBytes = kFhRecPairBarOff + 16 * kFhRecPairs;
+constexpr uint32_t kFhPrepBytes = kFhPrepPairBarOff + 16 * kFhPrepPairs;
 constexpr uint32_t kFhSmemBytes = (kFhRecBytes > kFhPrepBytes ? kFhRecBytes : kFhPrepBytes) + 1024;
 static_assert(kFhSmemBytes <= 227 * 1024, "one-launch CTA exceeds shared memory");
 static_assert(2 * kFhStages * 8 <= 1024, "ring barriers overflow their slot");
@@ -126,7 +128,8 @@ struct FusedHeadsArgs {
     prep::PrepArgs p;
     RecArgs r;
     int64_t rec_blocks;
-    uint32_t* ready;
+    uint32_t* ready;     // one flag per packet, then the item counter (all zero at launch)
+    uint32_t* counter;
 };
 
 // The mbarrier of pair `pair` (at bars[pair]), initialised by the pair's
@@ -180,20 +183,18 @@ __global__ void __launch_bounds__(kFhThreads, 1)
         } else {
             const int pair = (warp - 2 * kFhRecWarps) >> 1, hw = warp & 1;
             const int bid = 1 + pair;
-            uint64_t* bar = fh_pair_barrier(reinterpret_cast<uint64_t*>(smem + kFhRecPairBarOff),
-                                            pair, hw, lane, bid);
+            uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFhRecPairBarOff);
+            uint64_t* bar = fh_pair_barrier(bars, pair, hw, lane, bid);
             prep::run_items(f.p, maps, smem + kFhRecPrepOff + pair * prep::kPrepRegion, bar, bid, hw,
-                            lane, static_cast<int64_t>(blockIdx.x) * kFhRecPairs + pair, pairs,
-                            f.ready);
+                            lane, 0, pairs, f.ready, f.counter,
+                            reinterpret_cast<int64_t*>(bars + kFhRecPairs) + pair);
         }
     } else {
         const int pair = warp >> 1, hw = warp & 1, bid = 1 + pair;
-        uint64_t* bar = fh_pair_barrier(reinterpret_cast<uint64_t*>(smem + kFhPrepPairBarOff), pair,
-                                        hw, lane, bid);
-        prep::run_items(f.p, maps, smem + pair * prep::kPrepRegion, bar, bid, hw, lane,
-                        rec * kFhRecPairs + (static_cast<int64_t>(blockIdx.x) - rec) * kFhPrepPairs +
-                            pair,
-                        pairs, f.ready);
+        uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFhPrepPairBarOff);
+        uint64_t* bar = fh_pair_barrier(bars, pair, hw, lane, bid);
+        prep::run_items(f.p, maps, smem + pair * prep::kPrepRegion, bar, bid, hw, lane, 0, pairs,
+                        f.ready, f.counter, reinterpret_cast<int64_t*>(bars + kFhPrepPairs) + pair);
     }
 }
 
@@ -232,6 +233,7 @@ cudaError_t launch_fused_heads(const void* q, const void* k, const float* g, con
     f.r.final_ident = nullptr;
     f.rec_blocks = geo.n_seqs * H;
     f.ready = ready;
+    f.counter = ready + geo.chunk_ub * H;
     prep::PrepMaps maps;
     e = prep::encode_maps(&maps, q, k, g, geo.tokens, H);
     if (e != cudaSuccess) return e;

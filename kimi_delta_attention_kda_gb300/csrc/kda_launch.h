@@ -147,7 +147,8 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
 
 // Preparation and the wide one-CTA-per-head recurrence as one cooperative
 // launch of one 16-warp CTA per SM, for fixed-length batches of at most one
-// (sequence, head) unit per SM (kda_fused.cu).  `ready` as for launch_fused.
+// (sequence, head) unit per SM (kda_fused.cu).  `ready` as for launch_fused,
+// followed by one more zeroed word (the preparation's item counter).
 bool fused_heads_supported(int64_t n_seqs, int64_t H, int sms);
 cudaError_t launch_fused_heads(const void* q, const void* k, const float* g, const void* beta,
                                const void* v, void* out, const void* init_state, void* final_state,

@@ -553,18 +553,35 @@ __device__ __forceinline__ uint64_t* pair_barrier(uint8_t* smem, int pair, int h
 // ready[chunk * H + head] (the packet's index) becomes 1 (release, GPU scope)
 // once the item's packet is in global memory; the flag of an item is
 // published when the pair has issued the next item's loads, or at the end.
+// With `counter` (a zeroed global word) the pairs instead take items in
+// order from it (atomicAdd by the pair's issuing thread, handed to the other
+// warp through `slot`, a shared word of the pair), so that faster pairs take
+// more items; `first` and `stride` are then unused.
 __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& maps, uint8_t* region,
                                           uint64_t* bar, int bid, int hw, int lane, int64_t first,
-                                          int64_t stride, uint32_t* ready) {
+                                          int64_t stride, uint32_t* ready,
+                                          uint32_t* counter = nullptr,
+                                          volatile int64_t* slot = nullptr) {
     int64_t pending = -1;   // item whose packet store is in flight, not yet published
     if (a.geo.cu_chunks && !*a.geo.valid) return;
     const bool issuer = hw == 0 && lane == 0;
 
     uint32_t phase = 0;
-    for (int64_t item = first; item < a.n_chunk_heads; item += stride) {
+    int64_t item = first;
+    if (counter) {
+        if (issuer) *slot = static_cast<int64_t>(atomicAdd(counter, 1u));
+        pair_sync(bid);
+        item = *slot;
+    }
+    while (item < a.n_chunk_heads) {
         int64_t t0, len, c, h;
         if (!item_range(a, item, &t0, &len, &c, &h)) break;   // items only grow past the end
+        int64_t next = item + stride;
         if (issuer) {
+            if (counter) {
+                next = static_cast<int64_t>(atomicAdd(counter, 1u));
+                *slot = next;   // read by the other warp after the barrier below
+            }
             // The previous packet store must have read the region before TMA
             // overwrites it; the region's generic-proxy writes were fenced
             // (fence.proxy.async) before that store.
@@ -577,7 +594,7 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
             // This pair's next item: its tiles on their way to L2 while this
             // item is worked on, so that its loads above find them there.
             int64_t nt0, nlen, nc, nh;
-            if (item + stride < a.n_chunk_heads && item_range(a, item + stride, &nt0, &nlen, &nc, &nh)) {
+            if (next < a.n_chunk_heads && item_range(a, next, &nt0, &nlen, &nc, &nh)) {
                 const int32_t nx = static_cast<int32_t>(nh * kHeadDim), ny = static_cast<int32_t>(nt0);
                 tma_prefetch_l2_2d(&maps.q, nx, ny);
                 tma_prefetch_l2_2d(&maps.k, nx, ny);
@@ -602,6 +619,7 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
             if (!got) mbar_wait_bounded_sleep(bar, phase, a.geo.status);
             break;
         }
+        if (counter) next = *slot;   // the issuer's write precedes the barrier above
         phase ^= 1u;
         prep_item(region, bid, hw, beta_f, len, a.scale, lane);
 
@@ -612,6 +630,7 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
             bulk_commit();
             pending = c * a.H + h;   // the packet's index (the item's, unless interleaved)
         }
+        item = next;
     }
     if (issuer) {
         bulk_wait_all();

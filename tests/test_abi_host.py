@@ -128,7 +128,8 @@ def test_workspace_bytes(lib):
     pb = _lib.packet_bytes()
     assert pb == 13824
     # fixed: ceil(T/16) chunks per sequence
-    # packets, plus 256-aligned ready flags (one per chunk and head) for a fused launch
+    # packets, plus 256-aligned ready flags (one per chunk and head, and one word
+    # more: the item counter of the many-head form) for a fused launch
     assert _lib.workspace_bytes(2, 40, 3, False) == 2 * 3 * 3 * pb + 256
     assert _lib.workspace_bytes(1, 0, 5, False) == 0
     # packed: (T + 15 N) // 16 chunks at most, plus the metadata block (valid
@@ -141,9 +142,9 @@ def test_workspace_bytes(lib):
     import torch
     if not torch.cuda.is_available():
         st = 25 * 6 * 128 * 128 * 2
-        assert _lib.workspace_bytes(1, 8192, 6, False) == 512 * 6 * pb + 12288 + 3 * st
+        assert _lib.workspace_bytes(1, 8192, 6, False) == 512 * 6 * pb + 12544 + 3 * st
         lib.kda_set_segments(0, 0)
-        assert _lib.workspace_bytes(1, 8192, 6, False) == 512 * 6 * pb + 12288
+        assert _lib.workspace_bytes(1, 8192, 6, False) == 512 * 6 * pb + 12544
         lib.kda_set_segments(1, 0)
 
 
