@@ -62,23 +62,27 @@ PACKET_PER_TOKEN = 13824 / 16
 PATH_BYTES_PER_HT = 2 * 256 + 512 + 2 + 256 + 256
 STATE_BYTES = 128 * 128 * 2
 
-# DRAM bytes (read + write) of one launch of the dominant kernel (of the
-# segment chain: its launches in one call), from one ncu capture each
-# (summaries in profiles/).  A figure is reported only while the
-# kernel's sources still hash to the value they had when it was captured.
+# DRAM bytes (read + write) of one launch of each kernel (of the segment
+# chain: its launches in one call; of the packed recurrence: both concurrent
+# launches), from one ncu capture each (summaries in profiles/).  A figure is
+# reported only while the kernel's sources still hash to the value they had
+# when it was captured.
 REC_SOURCES = ("kda_recurrence.cu", "kda_rec_impl.cuh", "kda_common.cuh")
 PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
 SEG_SOURCES = ("kda_segments.cu", "kda_common.cuh")
 FUSED_SOURCES = ("kda_fused.cu", "kda_prep_impl.cuh", "kda_rec_impl.cuh", "kda_common.cuh")
 PROFILED_TRAFFIC = {
-    ("transition", "t8192_h6"): (55.574e6, REC_SOURCES, "07eabcbca4f1a1df"),
-    ("chunk_prep", "t8192_h6"): (53.496e6, PREP_SOURCES, "3e9deecd5eb41b6e"),
-    ("transition", "t65536_h1"): (75.742e6, REC_SOURCES, "07eabcbca4f1a1df"),
-    ("segment_chain", "t65536_h1"): (20.306e6, SEG_SOURCES, "a574cabe1e495497"),
-    ("recurrence", "t8192_h96"): (1066.769e6, REC_SOURCES, "07eabcbca4f1a1df"),
-    ("chunk_prep", "t8192_h96"): (1452.671e6, PREP_SOURCES, "3e9deecd5eb41b6e"),
-    ("recurrence", "varlen8_h12"): (380.516e6, REC_SOURCES, "07eabcbca4f1a1df"),
-    ("fused", "t256_h1"): (0.390e6, FUSED_SOURCES, "ef37c449dd467f86"),
+    ("chunk_prep", "t8192_h6"): (53.8e6, PREP_SOURCES, "a415e4e83a7553c7"),
+    ("transition", "t8192_h6"): (55.6e6, REC_SOURCES, "8e95600d539bd31e"),
+    ("segment_chain", "t8192_h6"): (10.0e6, SEG_SOURCES, "4f030b91dec9e1c5"),
+    ("recurrence", "t8192_h6"): (60.9e6, REC_SOURCES, "8e95600d539bd31e"),
+    ("fused", "t8192_h96"): (2548.6e6, FUSED_SOURCES, "15d22163cf8072c8"),
+    ("chunk_prep", "t8192_h96"): (1457.3e6, PREP_SOURCES, "a415e4e83a7553c7"),
+    ("recurrence", "t8192_h96"): (1066.6e6, REC_SOURCES, "8e95600d539bd31e"),
+    ("transition", "t65536_h1"): (75.6e6, REC_SOURCES, "8e95600d539bd31e"),
+    ("segment_chain", "t65536_h1"): (20.3e6, SEG_SOURCES, "4f030b91dec9e1c5"),
+    ("recurrence", "varlen8_h12"): (380.9e6, REC_SOURCES, "8e95600d539bd31e"),
+    ("fused", "t256_h1"): (0.4e6, FUSED_SOURCES, "15d22163cf8072c8"),
 }
 
 
