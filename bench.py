@@ -76,13 +76,13 @@ PROFILED_TRAFFIC = {
     ("transition", "t8192_h6"): (55.6e6, REC_SOURCES, "8e95600d539bd31e"),
     ("segment_chain", "t8192_h6"): (10.0e6, SEG_SOURCES, "4f030b91dec9e1c5"),
     ("recurrence", "t8192_h6"): (60.9e6, REC_SOURCES, "8e95600d539bd31e"),
-    ("fused", "t8192_h96"): (2548.6e6, FUSED_SOURCES, "15d22163cf8072c8"),
+    ("fused", "t8192_h96"): (1857.4e6, FUSED_SOURCES, "3632681e83b98871"),
     ("chunk_prep", "t8192_h96"): (1457.3e6, PREP_SOURCES, "a415e4e83a7553c7"),
     ("recurrence", "t8192_h96"): (1066.6e6, REC_SOURCES, "8e95600d539bd31e"),
     ("transition", "t65536_h1"): (75.6e6, REC_SOURCES, "8e95600d539bd31e"),
     ("segment_chain", "t65536_h1"): (20.3e6, SEG_SOURCES, "4f030b91dec9e1c5"),
     ("recurrence", "varlen8_h12"): (380.9e6, REC_SOURCES, "8e95600d539bd31e"),
-    ("fused", "t256_h1"): (0.4e6, FUSED_SOURCES, "15d22163cf8072c8"),
+    ("fused", "t256_h1"): (0.4e6, FUSED_SOURCES, "3632681e83b98871"),
 }
 
 

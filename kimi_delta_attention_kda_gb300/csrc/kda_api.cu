@@ -377,20 +377,19 @@ bool use_fusion(const Plan& pl, int64_t H, int nsplit, int sms) {
 // Whether kda_prefill runs a fixed-length batch of one recurrence CTA per
 // (sequence, head) as the many-head one-launch form (kda_fused.cu): every SM
 // holds one CTA, the first N*H of them each run one head's recurrence while
-// four warp pairs on each of them and eight on every other SM prepare the
-// packets just ahead of it.  Sharing an SM slows both (measured on GB300, B=1,
-// T=8192, H=96: a recurrence chunk step 0.84 -> 1.22 us, a preparation item
-// on one pair 7.2 -> 8.8 us), so the form gains only while enough SMs are left
-// to the preparation alone: measured, one launch against two kernels at
-// T=8192, H=80 679 vs 698 us, H=96 716 vs 732, H=112 765 vs 778, H=128 874 vs
-// 809, H=144 1,048 vs 862; T=2048, H=96 198 vs 202; B=2, T=4096, H=48 370 vs
-// 379.  Hence the rule: at most three quarters of the SMs run a recurrence.
+// two warp pairs on each of them and eight on every other SM prepare the
+// packets just ahead of it.  The preparation then has fewer pairs than alone
+// (1,216 on 152 SMs), so the form gains while enough SMs are left to it.
+// Measured on GB300, one launch against two kernels (eager, L2 flushed),
+// T=8192: H=80 579 vs 703 us, H=96 664 vs 741, H=112 874 vs 782; T=2048,
+// H=96 188 vs 203; B=2, T=4096, H=48 345 vs 383.  Hence the rule: at most two
+// thirds of the SMs run a recurrence, and at least 64 chunks per sequence.
 bool use_fusion_heads(const Plan& pl, int64_t H, int nsplit, int sms, bool checkpoints) {
     if (!g_fusion || g_engine != 0 || g_split_override || pl.packed || pl.tokens <= 0 ||
         checkpoints || nsplit != 1)
         return false;
     if (!fused_heads_supported(pl.N, H, sms)) return false;
-    return 4 * pl.N * H <= 3 * static_cast<int64_t>(sms) && pl.geo.chunks_per_seq >= 64;
+    return 3 * pl.N * H <= 2 * static_cast<int64_t>(sms) && pl.geo.chunks_per_seq >= 64;
 }
 
 // Launch metadata (packed) and preparation into `ws` (meta) and `packets`.

@@ -87,32 +87,31 @@ cudaError_t launch_fused_ncg(FusedArgs& f, const prep::PrepMaps& maps, const CUt
 // recurrence CTA per unit, N*H <= SMs): every SM holds one 16-warp CTA,
 // launched at 128 registers a thread.  CTAs 0 .. R-1 (R = N*H) each run a
 // whole head's recurrence: warpgroup 0 (warps 0-3) is the quad form (32 value
-// columns a warp, kda_rec_impl.cuh) and takes 232 registers a thread with
-// setmaxnreg, which warpgroup 1 gives up (down to 24: warp 4 is the producer,
-// which waits for each packet's ready flag, warps 5-7 leave); warpgroups 2
-// and 3 prepare packets (four warp pairs, 128 registers).  The other CTAs
-// prepare packets on all 16 warps (eight pairs).  The shares add up to the
-// launch's 512 x 128 registers exactly (128 x (232 + 24 + 128 + 128)).  Every
-// pair of the grid walks one strided list of items numbered chunk first (the
+// columns a warp, kda_rec_impl.cuh) and takes 256 registers a thread with
+// setmaxnreg, which warpgroups 1 and 3 give up (down to 24: warp 4 is the
+// producer, which waits for each packet's ready flag; warps 5-7 and 12-15
+// leave); warpgroup 2 prepares packets (two warp pairs, 128 registers).  The
+// other CTAs prepare packets on all 16 warps (eight pairs).  The shares,
+// 128 x (256 + 24 + 128 + 24), stay within the launch's 512 x 128 registers.
+// Every pair takes items in order from a counter, numbered chunk first (the
 // preparation's interleaved order), so the packets of each chunk index appear
 // for every head at about the same time and the recurrences stay close behind
-// them.  The pairs take items in order from a counter, so that the pairs that
-// share an SM with a recurrence (slower) take fewer than the others.  The
-// preparation never waits on the recurrence, and the cooperative launch keeps
-// every CTA resident, so every wait (bounded) ends.  The arithmetic is that of
-// the preparation and quad kernels: the results are bit for bit those of the
-// two-kernel path.
+// them, and the pairs that share an SM with a recurrence (slower) take fewer
+// items than the others.  The preparation never waits on the recurrence, and
+// the cooperative launch keeps every CTA resident, so every wait (bounded)
+// ends.  The arithmetic is that of the preparation and quad kernels: the
+// results are bit for bit those of the two-kernel path.
 // ---------------------------------------------------------------------------
 constexpr int kFhWarps = 16;
 constexpr int kFhThreads = kFhWarps * 32;
 constexpr int kFhRecWarps = 4;    // warpgroup 0
 constexpr int kFhProdWarp = 4;    // first warp of warpgroup 1
-constexpr int kFhRecPairs = 4;    // warpgroups 2 and 3
+constexpr int kFhRecPairs = 2;    // warpgroup 2 (warpgroup 3 gives its registers away)
 constexpr int kFhPrepPairs = 8;   // all warps of a preparing CTA
-constexpr int kFhStages = 6;
-constexpr uint32_t kFhRecRegs = 232, kFhProdRegs = 24;
-static_assert(128 * (kFhRecRegs + kFhProdRegs + 2 * 128) == kFhThreads * 128,
-              "register shares must add up to the launch's registers");
+constexpr int kFhStages = 8;
+constexpr uint32_t kFhRecRegs = 256, kFhIdleRegs = 24;
+static_assert(128 * (kFhRecRegs + 2 * kFhIdleRegs + 128) <= kFhThreads * 128,
+              "register shares must fit the launch's registers");
 constexpr uint32_t kFhRingBytes = kFhStages * kWideStageBytes;
 constexpr uint32_t kFhRecPrepOff = kFhRingBytes + 1024;   // ring barriers in between
 constexpr uint32_t kFhRecPairBarOff = kFhRecPrepOff + kFhRecPairs * prep::kPrepRegion;
@@ -176,10 +175,13 @@ __global__ void __launch_bounds__(kFhThreads, 1)
             wide_consume<4, kFhStages, false>(a, smem, full, empty, warp, lane, n, h, c_begin, nch,
                                               tok0, seqlen);
         } else if (warp < 2 * kFhRecWarps) {
-            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kFhProdRegs) : "memory");
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kFhIdleRegs) : "memory");
             if (warp == kFhProdWarp)
                 wide_produce<kFhStages>(a, &vmap, smem, full, empty, lane, h, c_begin, nch, tok0,
                                         f.ready);
+        } else if (warp >= 3 * kFhRecWarps) {
+            // Warpgroup 3 gives its registers to warpgroup 0 and leaves.
+            asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kFhIdleRegs) : "memory");
         } else {
             const int pair = (warp - 2 * kFhRecWarps) >> 1, hw = warp & 1;
             const int bid = 1 + pair;
