@@ -233,6 +233,18 @@ __device__ __forceinline__ void bulk_wait_all() {
 __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
+// Release of a shared-memory stage that this warp read through the generic
+// proxy (ld.shared, ldmatrix) and that a bulk copy (the async proxy) will
+// overwrite once every consumer has released it.  The memory model orders
+// the copy after those reads only through a proxy fence (generic and async
+// proxies); without it, a ring of this kind on GB300 (two CTAs per SM) gave
+// results that varied from run to run in single chunks, and with it they
+// were bit-identical.  Every lane fences its own reads, then lane 0 arrives.
+__device__ __forceinline__ void stage_release(uint64_t* bar, int lane) {
+    fence_proxy_async_smem();
+    __syncwarp();
+    mbar_arrive_if(bar, lane == 0);
+}
 // Orders global-memory accesses of the async proxy (bulk copies) with those
 // of the generic proxy made by the same thread.
 __device__ __forceinline__ void fence_proxy_async_global() {

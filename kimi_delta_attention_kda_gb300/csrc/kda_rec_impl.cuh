@@ -348,6 +348,10 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
             mul2(Sf[i][0], Sf[i][1], d0);
             mul2(Sf[i][2], Sf[i][3], d1);
         }
+        // Every read of this chunk's stage was issued during the previous
+        // chunk (or before the loop): hand it back before the next chunk's
+        // loads, so that the proxy fence finds nothing in flight.
+        stage_release(&empty[s], lane);
         // The K' and Q^start fragments are dead: load the next chunk's.
         if (has_next) {
             if (!__all_sync(0xffffffffu, next_ready))
@@ -388,8 +392,6 @@ __device__ __forceinline__ void ks_run(const RecArgs& a, const CUtensorMap* vmap
             Sb[i][0] = movm_t(pack_bf16(Sf[i][0], Sf[i][1]));
             Sb[i][1] = movm_t(pack_bf16(Sf[i][2], Sf[i][3]));
         }
-        __syncwarp();
-        mbar_arrive_if(&empty[s], lane == 0);
         // Key half 0 stores tokens 0-7 of O, key half 1 tokens 8-15.
         const int tok = 8 * kh + g8;
         __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + tok) * a.H + h) * kHeadDim + vcol + 2 * t4;
@@ -636,8 +638,7 @@ __device__ __forceinline__ void wide_consume(const RecArgs& a, const uint8_t* sm
                 mma_f16(o[nt], aq, Ub[nt], p[0][nt]);
             }
         }
-        __syncwarp();
-        mbar_arrive_if(&empty[s], lane == 0);
+        stage_release(&empty[s], lane);
         __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + g8) * a.H + h) * kHeadDim + vcol + 2 * t4;
 #pragma unroll
         for (int nt = 0; nt < NT; ++nt) {

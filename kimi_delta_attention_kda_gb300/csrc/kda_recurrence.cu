@@ -327,6 +327,10 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                 mul2(Sf[mt][0], Sf[mt][1], d0);
                 mul2(Sf[mt][2], Sf[mt][3], d1);
             }
+            // Every read of this chunk's stage was issued during the previous
+            // chunk (or before the loop): hand it back before the next
+            // chunk's loads, so that the proxy fence finds nothing in flight.
+            stage_release(&empty[s], lane);
             if (has_next) {
                 if (!__all_sync(0xffffffffu, next_ready))
                     next_ready = mbar_wait_warp(&full[s1], par1, a.status);
@@ -358,8 +362,6 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                 Sb[mt][0] = movm_t(pack_bf16(Sf[mt][0], Sf[mt][1]));
                 Sb[mt][1] = movm_t(pack_bf16(Sf[mt][2], Sf[mt][3]));
             }
-            __syncwarp();
-            mbar_arrive_if(&empty[s], lane == 0);
             __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + g8) * a.H + h) * kHeadDim + vcol + 2 * t4;
             st_global_u32_if(orow, pack_bf16(o[0], o[1]), g8 < len);
             st_global_u32_if(orow + 8 * a.H * kHeadDim, pack_bf16(o[2], o[3]), g8 + 8 < len);
@@ -392,8 +394,7 @@ __global__ void __launch_bounds__((NW + 1) * 32)
                 Sb[mt][1] = movm_t(pack_bf16(Sf[mt][2], Sf[mt][3]));
             }
             // Every read of this stage is done: hand it back to the producer.
-            __syncwarp();
-            mbar_arrive_if(&empty[s], lane == 0);
+            stage_release(&empty[s], lane);
 
             // Store O (tokens g8 and g8 + 8, values vcol + 2 t4 .. + 1), predicated.
             __nv_bfloat16* orow = a.out + ((tok0 + kChunk * c + g8) * a.H + h) * kHeadDim + vcol + 2 * t4;
@@ -618,8 +619,7 @@ __global__ void __launch_bounds__(kTransWarps * 32, 1)
 #pragma unroll
             for (int nt = 0; nt < 4; ++nt) mma_f16(Sf[mt][nt], af, Ub[nt], Sf[mt][nt]);
         }
-        __syncwarp();
-        mbar_arrive_if(&empty[s], lane == 0);
+        stage_release(&empty[s], lane);
         // Refill the stage of chunk c - 1 once every warp has released it.
         if (warp == 0 && c >= 1 && issued < nch) {
             const int64_t cp = c - 1;

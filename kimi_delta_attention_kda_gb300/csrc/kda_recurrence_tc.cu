@@ -348,8 +348,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
             for (int i = 0; i < 8; ++i)
                 if (8 * hf + i < len) orow[i * a.H * kHeadDim] = __float2bfloat16_rn(__uint_as_float(o[i]));
             // This stage's V tile and D have been read.
-            __syncwarp();
-            mbar_arrive_if(&empty[s], lane == 0);
+            stage_release(&empty[s], lane);
         }
         if (ok && a.final_state) {
             uint4* dst = reinterpret_cast<uint4*>(a.final_state + state_row);
