@@ -72,17 +72,17 @@ PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
 SEG_SOURCES = ("kda_segments.cu", "kda_common.cuh")
 FUSED_SOURCES = ("kda_fused.cu", "kda_prep_impl.cuh", "kda_rec_impl.cuh", "kda_common.cuh")
 PROFILED_TRAFFIC = {
-    ("chunk_prep", "t8192_h6"): (53.8e6, PREP_SOURCES, "a415e4e83a7553c7"),
-    ("transition", "t8192_h6"): (55.6e6, REC_SOURCES, "8e95600d539bd31e"),
-    ("segment_chain", "t8192_h6"): (10.0e6, SEG_SOURCES, "4f030b91dec9e1c5"),
-    ("recurrence", "t8192_h6"): (60.9e6, REC_SOURCES, "8e95600d539bd31e"),
-    ("fused", "t8192_h96"): (1857.4e6, FUSED_SOURCES, "3632681e83b98871"),
-    ("chunk_prep", "t8192_h96"): (1457.3e6, PREP_SOURCES, "a415e4e83a7553c7"),
-    ("recurrence", "t8192_h96"): (1066.6e6, REC_SOURCES, "8e95600d539bd31e"),
-    ("transition", "t65536_h1"): (75.6e6, REC_SOURCES, "8e95600d539bd31e"),
-    ("segment_chain", "t65536_h1"): (20.3e6, SEG_SOURCES, "4f030b91dec9e1c5"),
-    ("recurrence", "varlen8_h12"): (380.9e6, REC_SOURCES, "8e95600d539bd31e"),
-    ("fused", "t256_h1"): (0.4e6, FUSED_SOURCES, "3632681e83b98871"),
+    ("chunk_prep", "t8192_h6"): (53.7e6, PREP_SOURCES, "b3d01d8fb20878cf"),
+    ("transition", "t8192_h6"): (55.6e6, REC_SOURCES, "694d11e96e58d88a"),
+    ("segment_chain", "t8192_h6"): (10.0e6, SEG_SOURCES, "f91a7d7fb3238b25"),
+    ("recurrence", "t8192_h6"): (61.0e6, REC_SOURCES, "694d11e96e58d88a"),
+    ("fused", "t8192_h96"): (1857.3e6, FUSED_SOURCES, "a40697bab4233f67"),
+    ("chunk_prep", "t8192_h96"): (1456.0e6, PREP_SOURCES, "b3d01d8fb20878cf"),
+    ("recurrence", "t8192_h96"): (1067.0e6, REC_SOURCES, "694d11e96e58d88a"),
+    ("transition", "t65536_h1"): (75.7e6, REC_SOURCES, "694d11e96e58d88a"),
+    ("segment_chain", "t65536_h1"): (20.3e6, SEG_SOURCES, "f91a7d7fb3238b25"),
+    ("recurrence", "varlen8_h12"): (381.3e6, REC_SOURCES, "694d11e96e58d88a"),
+    ("fused", "t256_h1"): (0.4e6, FUSED_SOURCES, "a40697bab4233f67"),
 }
 
 
