@@ -271,23 +271,43 @@ def cpu_baseline(name, min_seconds=10.0):
 
 
 def run_reference(args):
-    """The oracle as the reference arm: each step a bounded sample of the workload."""
+    """The oracle as the reference arm, on this arm's workload: every step the
+    whole workload (the default, reference_tokens 0), or with reference_tokens
+    > 0 the first that many tokens of every sequence (a quicker sample)."""
     import oracle
     ws, rank, _ = dist_env()
     if ws > 1 and rank != 0:
         return
     inp = synthetic.make_workload(args.workload)
-    tokens = min(inp["q"].shape[1], args.reference_tokens)
-    sl = {k: inp[k][:, :tokens].contiguous() for k in ("q", "k", "v", "g", "beta")}
-    if inp["cu_seqlens"] is not None:
-        sl = {k: inp[k][:, :tokens].contiguous() for k in ("q", "k", "v", "g", "beta")}
-        cu = None
-        init = inp["init_state"][:1] if inp["init_state"] is not None else None
-    else:
-        cu = None
-        init = inp["init_state"]
     H = inp["q"].shape[2]
-    ht = sl["q"].shape[0] * tokens * H
+    init = inp["init_state"]
+    if args.reference_tokens <= 0:
+        sl = {k: inp[k] for k in ("q", "k", "v", "g", "beta")}
+        cu = None if inp["cu_seqlens"] is None else inp["cu_seqlens"].numpy()
+        ht = head_tokens(inp)
+        sample = "the whole workload %s every step (%d head-tokens), FP64 token recurrence" % (
+            inp["workload"].name, ht)
+        tokens = inp["q"].shape[1]
+    else:
+        # The first `tokens` of every sequence (packed: of each sequence's span).
+        tokens = min(inp["q"].shape[1], args.reference_tokens)
+        if inp["cu_seqlens"] is None:
+            sl = {k: inp[k][:, :tokens].contiguous() for k in ("q", "k", "v", "g", "beta")}
+            cu = None
+        else:
+            c = inp["cu_seqlens"].tolist()
+            spans = [(c[n], min(c[n + 1], c[n] + tokens)) for n in range(len(c) - 1)]
+            sl = {k: torch.cat([inp[k][:, a:b] for a, b in spans], 1).contiguous()
+                  for k in ("q", "k", "v", "g", "beta")}
+            lens = [b - a for a, b in spans]
+            cu = [0]
+            for n in lens:
+                cu.append(cu[-1] + n)
+            import numpy as np
+            cu = np.asarray(cu, dtype=np.int64)
+        ht = int(sl["q"].shape[0] * sl["q"].shape[1] * H)
+        sample = ("first %d tokens of every sequence of %s (%d head-tokens per step), FP64 token "
+                  "recurrence" % (tokens, inp["workload"].name, ht))
 
     def step():
         oracle.kda_token(sl["q"], sl["k"], sl["v"], sl["g"], sl["beta"], init, cu_seqlens=cu)
@@ -301,14 +321,13 @@ def run_reference(args):
         times.append(time.perf_counter() - t0)
     total = sum(times)
     value = ht * args.steps / total
-    sample = ("first %d tokens of every sequence of %s (%d head-tokens per step), FP64 token "
-              "recurrence" % (tokens, inp["workload"].name, ht))
     line = {
         "impl": "reference", "metric": METRIC, "value": value, "unit": UNIT, "n_gpus": ws,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic",
-        "config": {"workload": inp["workload"].name, "sample_tokens": tokens},
+        "config": {"workload": inp["workload"].name,
+                   "sample_tokens": None if args.reference_tokens <= 0 else tokens},
         "cpu_baseline": {"value": value, "unit": UNIT, "cores": oracle.num_threads(),
                          "kind": "oracle", "sample": sample},
         "e2e": {"value": value, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -611,7 +630,9 @@ def main():
     ap.add_argument("--no-secondary", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--cpu-seconds", type=float, default=10.0)
-    ap.add_argument("--reference-tokens", type=int, default=1024)
+    ap.add_argument("--reference-tokens", type=int, default=0,
+                    help="reference arm: 0 (default) runs the whole workload every step; "
+                         "n > 0 the first n tokens of every sequence")
     ap.add_argument("--split", type=int, default=0,
                     help="CTAs per (sequence, head) in the recurrence (0 = automatic)")
     ap.add_argument("--engine", type=int, default=0,

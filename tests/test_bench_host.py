@@ -72,6 +72,35 @@ def test_reference_arm_rank0_line(monkeypatch, capsys):
     assert line["e2e"]["h2d_bytes_per_step"] == 0 and line["config"]["sample_tokens"] == 64
 
 
+def test_reference_arm_whole_workload(monkeypatch, capsys):
+    """By default the oracle runs the arm's whole workload every step."""
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    args = _Args()
+    args.reference_tokens = 0
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["config"]["sample_tokens"] is None
+    assert "whole workload" in line["cpu_baseline"]["sample"]
+    assert line["value"] > 0
+
+
+def test_reference_arm_packed_sample_keeps_sequences(monkeypatch, capsys):
+    """A packed workload's sample keeps every sequence apart (its first
+    tokens), with the offsets of the sample."""
+    monkeypatch.setenv("WORLD_SIZE", "1")
+    monkeypatch.setenv("RANK", "0")
+    args = _Args()
+    args.workload = "varlen8_h12"
+    args.reference_tokens = 16
+    args.steps = 1
+    args.warmup = 0
+    bench.run_reference(args)
+    line = json.loads(capsys.readouterr().out.strip())
+    assert line["config"]["sample_tokens"] == 16
+    assert "first 16 tokens" in line["cpu_baseline"]["sample"]
+
+
 def test_reference_arm_other_ranks_do_nothing(monkeypatch, capsys):
     monkeypatch.setenv("WORLD_SIZE", "2")
     monkeypatch.setenv("RANK", "1")
