@@ -199,6 +199,11 @@ def time_kernel_steps(kda, d, steps, warmup, flush, stream, profile=False, graph
                 eager()
             stream.synchronize()
             call = g.replay
+            # Untimed replays: the first launches of a new graph upload it.
+            for _ in range(min(warmup, 3)):
+                flush.zero_()
+                call()
+            stream.synchronize()
         starts = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         ends = [torch.cuda.Event(enable_timing=True) for _ in range(steps)]
         if profile:
@@ -588,7 +593,7 @@ def run_ours(args):
     if not args.no_secondary and args.workload != "t8192_h96":
         sec = synthetic.make_workload("t8192_h96")
         ds = device_inputs(sec, device)
-        ms2, _, _ = time_kernel_steps(kda, ds, max(10, args.steps // 10), 3, flush, stream,
+        ms2, _, _ = time_kernel_steps(kda, ds, max(20, args.steps // 10), 5, flush, stream,
                                    graph=bool(args.graph))
         _, prof2, _ = time_kernel_steps(kda, ds, 10, 3, flush, stream, profile=True)
         ht2 = head_tokens(sec)

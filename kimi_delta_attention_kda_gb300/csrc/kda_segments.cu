@@ -215,8 +215,8 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
     const uint32_t mi = lane >> 3, r8 = lane & 7;
     // Step j's operands from its stage into registers: F_j^T (m = new key,
     // k = old key) by transposing loads of F_j's rows (old key), and the C
-    // fragments of Z_j^T.  The stage is released at the end of the step that
-    // loads it, once those loads have had the step's MMAs to complete.
+    // fragments of Z_j^T.  The stage is released after the step that loads
+    // it, once those loads have had the step's MMAs and barrier to complete.
     uint32_t af[2][8][4], zf[4];
     auto load_step = [&](int64_t j) -> bool {
         const int s = static_cast<int>(j % kScanStages);
@@ -275,8 +275,9 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
 #pragma unroll
             for (int e = 0; e < 4; ++e) c[mt][e] = acc[mt][0][e] + acc[mt][1][e];
         put_rows(xbuf + ((j + 1) & 1) * kScanXBytes, c, warp, g8, t4);
-        if (j + 1 < nseg && ok) stage_release(&empty[(j + 1) % kScanStages], lane);
         ok = group_all<kScanWarps * 32>(1, ok);
+        // Past the barrier the next step's loads have had time to complete.
+        if (j + 1 < nseg && ok) stage_release(&empty[(j + 1) % kScanStages], lane);
     }
     __nv_bfloat16* const fin = compose ? (part ? a.gmap[1] : a.gmap[0]) : a.final_state;
     if (ok && fin) copy_rows_out(xbuf + (nseg & 1) * kScanXBytes, fin + rows0 * kHeadDim, tid);
