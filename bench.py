@@ -74,13 +74,13 @@ FUSED_SOURCES = ("kda_fused.cu", "kda_prep_impl.cuh", "kda_rec_impl.cuh", "kda_c
 PROFILED_TRAFFIC = {
     ("chunk_prep", "t8192_h6"): (53.7e6, PREP_SOURCES, "b3d01d8fb20878cf"),
     ("transition", "t8192_h6"): (55.6e6, REC_SOURCES, "694d11e96e58d88a"),
-    ("segment_chain", "t8192_h6"): (10.0e6, SEG_SOURCES, "f91a7d7fb3238b25"),
+    ("segment_chain", "t8192_h6"): (10.0e6, SEG_SOURCES, "1b0f3949273b91b6"),
     ("recurrence", "t8192_h6"): (61.0e6, REC_SOURCES, "694d11e96e58d88a"),
     ("fused", "t8192_h96"): (1857.3e6, FUSED_SOURCES, "a40697bab4233f67"),
     ("chunk_prep", "t8192_h96"): (1456.0e6, PREP_SOURCES, "b3d01d8fb20878cf"),
     ("recurrence", "t8192_h96"): (1067.0e6, REC_SOURCES, "694d11e96e58d88a"),
     ("transition", "t65536_h1"): (75.7e6, REC_SOURCES, "694d11e96e58d88a"),
-    ("segment_chain", "t65536_h1"): (20.3e6, SEG_SOURCES, "f91a7d7fb3238b25"),
+    ("segment_chain", "t65536_h1"): (20.3e6, SEG_SOURCES, "1b0f3949273b91b6"),
     ("recurrence", "varlen8_h12"): (381.3e6, REC_SOURCES, "694d11e96e58d88a"),
     ("fused", "t256_h1"): (0.4e6, FUSED_SOURCES, "a40697bab4233f67"),
 }
