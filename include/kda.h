@@ -231,16 +231,20 @@ int kda_prefill_ex(const void* q, const void* k, const void* v, const float* g, 
 /*
  * Whether kda_prefill may run preparation and recurrence as one cooperative
  * launch (1, the default) or always as two kernels (0).  One launch is used
- * for fixed-length batches (cu_seqlens NULL) under engine 0 in two forms, each
- * packet behind a ready flag in the workspace: (a) few heads, whose
+ * under engine 0 in two forms, each packet behind a ready flag in the
+ * workspace: (a) fixed-length batches (cu_seqlens NULL) with few heads, whose
  * recurrence takes a split of 8 or 16 and leaves at least 16 SMs free: those
  * SMs prepare packets while the recurrence consumes them; (b) many heads, one
- * recurrence CTA per (sequence, head) and N * H <= the SM count, when a cost
- * estimate favours it, and never with checkpoints: one CTA per SM, the first
- * N * H of them each run a head's recurrence and prepare packets on three warp
- * pairs, the others prepare on eight; the preparation walks the chunks in
- * order across all heads so that each head's recurrence starts on its first
- * packets at once.  The results are bit for bit those of the two-kernel path.
+ * recurrence CTA per (sequence, head) and 3 N H <= 2 x the SM count, at
+ * least 64 chunks per sequence (packed: on average), never with checkpoints:
+ * one CTA per SM, the first N * H of them each run a head's recurrence and
+ * prepare packets on two warp pairs, the others prepare on eight.  The
+ * preparation walks the chunks in the order the recurrences consume them:
+ * chunk index first across all heads (fixed layout), or, for a packed batch,
+ * by each chunk's position relative to its sequence's length (a small kernel
+ * ranks the chunks on the device after the offsets are checked), so that
+ * every sequence's recurrence gets its packets at the pace its length needs.
+ * The results are bit for bit those of the two-kernel path.
  * Process-wide; returns KDA_ERR_ARG for other values.
  */
 int kda_set_fusion(int on);
@@ -257,9 +261,10 @@ int kda_plan_fused(int64_t B, int64_t T, int64_t H, int packed, int* fused);
  * For a packed call of n_seqs sequences (T tokens in all) and H heads: how
  * many of its longest sequences kda_prefill runs at split 2 in a second,
  * concurrent recurrence launch on a library-owned stream (HOST out; 0 when
- * the call uses a single launch).  That happens under engine 0 with the
- * automatic split when the one-CTA-per-head grid leaves SMs free and
- * n_seqs <= 1024; the results are bitwise those of split 1.
+ * the call uses a single recurrence launch or the many-head one-launch form).
+ * That happens under engine 0 with the automatic split when the
+ * one-CTA-per-head grid leaves SMs free and n_seqs <= 1024; the results are
+ * bitwise those of split 1.
  */
 int kda_plan_long_split(int64_t n_seqs, int64_t T, int64_t H, int64_t* k);
 
@@ -299,9 +304,11 @@ int kda_auto_split(int64_t n_seqs, int64_t H, int* nsplit);
 /*
  * Bytes of scratch kda_prefill takes for a given shape at most (HOST out);
  * `packed` is nonzero for the packed layout.  The ready flags of a fused
- * launch (kda_set_fusion) are counted whether or not the call fuses; the
- * segmented scan's three state buffers (kda_set_segments) when the current
- * device (a 152-SM one when there is none) would use it.
+ * launch (kda_set_fusion) are counted whether or not a fixed-length call
+ * fuses, and for a packed call, with its chunk order (4 bytes a chunk), when
+ * the current device (a 152-SM one when there is none) would run it as the
+ * many-head one-launch form; the segmented scan's three state buffers
+ * (kda_set_segments) when that device would use it.
  */
 int kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int packed, int64_t* bytes);
 

@@ -200,7 +200,8 @@ def plan_fused(B: int, T: int, H: int, packed: bool) -> bool:
 
 
 def plan_long_split(n_seqs: int, T: int, H: int) -> int:
-    """How many longest sequences of a packed call run at split 2 in a second launch."""
+    """How many longest sequences of a packed call run at split 2 in a second
+    launch (0 under the many-head one-launch form)."""
     out = ctypes.c_int64(0)
     _check(load().kda_plan_long_split(int(n_seqs), int(T), int(H), ctypes.byref(out)),
            "kda_plan_long_split")

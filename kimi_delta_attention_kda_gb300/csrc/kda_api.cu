@@ -146,6 +146,7 @@ struct Plan {
     int64_t meta_bytes;      // valid flag + cu_chunks + order (packed only), 256-aligned
     int64_t packet_bytes;    // chunk_ub * H * kPacketBytes
     int64_t ready_bytes;     // chunk_ub * H flags of the fused launch, 256-aligned
+    int64_t order_bytes;     // packed: chunk_ub ranks of the many-head one-launch form, 256-aligned
 };
 
 int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
@@ -178,6 +179,7 @@ int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
     p->packet_bytes = g.chunk_ub * H * static_cast<int64_t>(kPacketBytes);
     // One flag per packet, then the many-head one-launch form's item counter.
     p->ready_bytes = g.chunk_ub > 0 ? ((g.chunk_ub * H * 4 + 4 + 255) / 256) * 256 : 0;
+    p->order_bytes = packed && g.chunk_ub > 0 ? ((g.chunk_ub * 4 + 255) / 256) * 256 : 0;
     return KDA_OK;
 }
 
@@ -384,12 +386,17 @@ bool use_fusion(const Plan& pl, int64_t H, int nsplit, int sms) {
 // T=8192: H=80 579 vs 703 us, H=96 664 vs 741, H=112 874 vs 782; T=2048,
 // H=96 188 vs 203; B=2, T=4096, H=48 345 vs 383.  Hence the rule: at most two
 // thirds of the SMs run a recurrence, and at least 64 chunks per sequence.
+// Packed batches (their lengths are on the device only) qualify by the same
+// rule on the mean length; their packets are made in the order of the chunks'
+// positions relative to their sequence's length (launch_chunk_order).
 bool use_fusion_heads(const Plan& pl, int64_t H, int nsplit, int sms, bool checkpoints) {
-    if (!g_fusion || g_engine != 0 || g_split_override || pl.packed || pl.tokens <= 0 ||
-        checkpoints || nsplit != 1)
+    if (!g_fusion || g_engine != 0 || g_split_override || pl.tokens <= 0 || checkpoints ||
+        nsplit != 1)
         return false;
     if (!fused_heads_supported(pl.N, H, sms)) return false;
-    return 3 * pl.N * H <= 2 * static_cast<int64_t>(sms) && pl.geo.chunks_per_seq >= 64;
+    if (3 * pl.N * H > 2 * static_cast<int64_t>(sms)) return false;
+    if (pl.packed) return pl.N <= kMaxOrdered && pl.tokens >= 64 * kChunk * pl.N;
+    return pl.geo.chunks_per_seq >= 64;
 }
 
 // Launch metadata (packed) and preparation into `ws` (meta) and `packets`.
@@ -478,7 +485,8 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         !fused_few && sc.segs == 0 && use_fusion_heads(pl, H, nsplit, d->sms, ck != nullptr);
     const bool fused = fused_few || fused_many;
     const int64_t ws_bytes = pl.meta_bytes + pl.packet_bytes + (fused ? pl.ready_bytes : 0) +
-                             3 * sc.state_bytes + sc.meta_bytes + sc.group_bytes;
+                             (fused_many ? pl.order_bytes : 0) + 3 * sc.state_bytes +
+                             sc.meta_bytes + sc.group_bytes;
     uint8_t* ws = nullptr;
     if (ws_bytes > 0) {
         if (cudaMallocFromPoolAsync(reinterpret_cast<void**>(&ws), static_cast<size_t>(ws_bytes),
@@ -495,7 +503,29 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         // refuses the cooperative launch (fewer SMs available to this
         // context), fall through to the two-kernel path.
         uint32_t* ready = reinterpret_cast<uint32_t*>(ws + pl.meta_bytes + pl.packet_bytes);
-        if (cudaMemsetAsync(ready, 0, static_cast<size_t>(pl.ready_bytes), stream) != cudaSuccess)
+        int32_t* chunk_order = nullptr;
+        geo = pl.geo;
+        if (pl.packed) {
+            // Offsets checked and chunk offsets on the device, then the
+            // preparation's chunk order.
+            int32_t* valid = reinterpret_cast<int32_t*>(ws);
+            int64_t* cu_chunks = reinterpret_cast<int64_t*>(ws + 256);
+            chunk_order = reinterpret_cast<int32_t*>(ws + pl.meta_bytes + pl.packet_bytes +
+                                                     pl.ready_bytes);
+            if (launch_varlen_meta(cu_seqlens, pl.N, pl.tokens, valid, cu_chunks, nullptr,
+                                   d->status, stream) != cudaSuccess)
+                rc = KDA_ERR_CUDA;
+            ++t_launches;
+            if (rc == KDA_OK && launch_chunk_order(cu_chunks, valid, pl.N, pl.geo.chunk_ub,
+                                                   chunk_order, stream) != cudaSuccess)
+                rc = KDA_ERR_CUDA;
+            ++t_launches;
+            geo.cu_seqlens = cu_seqlens;
+            geo.cu_chunks = cu_chunks;
+            geo.valid = valid;
+        }
+        if (rc == KDA_OK &&
+            cudaMemsetAsync(ready, 0, static_cast<size_t>(pl.ready_bytes), stream) != cudaSuccess)
             rc = KDA_ERR_CUDA;
         prof_record(1, stream);
         prof_record(2, stream);
@@ -504,8 +534,8 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
             const cudaError_t e =
                 fused_many
                     ? launch_fused_heads(q, k, g, beta, v, out, init_state, final_state,
-                                         ws + pl.meta_bytes, ready, pl.geo, H, kScale, d->status,
-                                         stream, beta_logit)
+                                         ws + pl.meta_bytes, ready, chunk_order, geo, H, kScale,
+                                         d->status, stream, beta_logit)
                     : launch_fused(q, k, g, beta, v, out, init_state, final_state,
                                    ws + pl.meta_bytes, ready, pl.geo, H, nsplit, kScale, d->status,
                                    stream, ck, beta_logit);
@@ -1033,7 +1063,11 @@ extern "C" int kda_plan_long_split(int64_t n_seqs, int64_t T, int64_t H, int64_t
     DeviceState* d = nullptr;
     rc = device_state(&d);
     if (rc != KDA_OK) return rc;
-    *k = long_split_count(pl, H, choose_split(pl.N * H, d->sms), d->sms);
+    const int nsplit = choose_split(pl.N * H, d->sms);
+    // None when the call runs as the many-head one-launch form.
+    const bool many = plan_segments(pl, H, d->sms, false).segs == 0 &&
+                      use_fusion_heads(pl, H, nsplit, d->sms, false);
+    *k = many ? 0 : long_split_count(pl, H, nsplit, d->sms);
     return KDA_OK;
 }
 
@@ -1089,7 +1123,12 @@ extern "C" int kda_workspace_bytes(int64_t B, int64_t T, int64_t H, int packed, 
     DeviceState* d = nullptr;
     if (device_state(&d) == KDA_OK) sms = d->sms;
     const SegChoice sc = plan_segments(pl, H, sms, false);
-    *bytes = pl.meta_bytes + pl.packet_bytes + (pl.packed ? 0 : pl.ready_bytes) +
+    // Fixed layout: the ready flags of a one-launch form are always counted;
+    // packed: the flags and the chunk order when the many-head form is planned.
+    const bool packed_fused =
+        pl.packed && sc.segs == 0 && use_fusion_heads(pl, H, choose_split(pl.N * H, sms), sms, false);
+    *bytes = pl.meta_bytes + pl.packet_bytes +
+             (pl.packed ? (packed_fused ? pl.ready_bytes + pl.order_bytes : 0) : pl.ready_bytes) +
              3 * sc.state_bytes + sc.meta_bytes + sc.group_bytes;
     return KDA_OK;
 }

@@ -83,8 +83,8 @@ cudaError_t launch_fused_ncg(FusedArgs& f, const prep::PrepMaps& maps, const CUt
 }
 
 // ---------------------------------------------------------------------------
-// The one-launch form for many (sequence, head) units (fixed layout, one
-// recurrence CTA per unit, N*H <= SMs): every SM holds one 16-warp CTA,
+// The one-launch form for many (sequence, head) units (fixed or packed
+// layout, one recurrence CTA per unit, N*H <= SMs): every SM holds one 16-warp CTA,
 // launched at 128 registers a thread.  CTAs 0 .. R-1 (R = N*H) each run a
 // whole head's recurrence: warpgroup 0 (warps 0-3) is the quad form (32 value
 // columns a warp, kda_rec_impl.cuh) and takes 256 registers a thread with
@@ -94,10 +94,11 @@ cudaError_t launch_fused_ncg(FusedArgs& f, const prep::PrepMaps& maps, const CUt
 // other CTAs prepare packets on all 16 warps (eight pairs).  The shares,
 // 128 x (256 + 24 + 128 + 24), stay within the launch's 512 x 128 registers.
 // Every pair takes items in order from a counter, numbered chunk first (the
-// preparation's interleaved order), so the packets of each chunk index appear
-// for every head at about the same time and the recurrences stay close behind
-// them, and the pairs that share an SM with a recurrence (slower) take fewer
-// items than the others.  The preparation never waits on the recurrence, and
+// preparation's interleaved order; packed batches by the chunks' positions
+// relative to their sequence's length), so the packets of each chunk index
+// appear for every head at about the same time and the recurrences stay close
+// behind them, and the pairs that share an SM with a recurrence (slower) take
+// fewer items than the others.  The preparation never waits on the recurrence, and
 // the cooperative launch keeps every CTA resident, so every wait (bounded)
 // ends.  The arithmetic is that of the preparation and quad kernels: the
 // results are bit for bit those of the two-kernel path.
@@ -159,7 +160,9 @@ __global__ void __launch_bounds__(kFhThreads, 1)
         const int64_t n = blockIdx.x / a.H;
         const int64_t h = blockIdx.x - n * a.H;
         int64_t c_begin, nch, tok0, seqlen;
-        seq_span(a.geo, n, c_begin, nch, tok0, seqlen);   // fixed layout: always valid
+        // Packed offsets found invalid: the whole CTA leaves before any
+        // register setting (every warp reads the same flag).
+        if (!seq_span(a.geo, n, c_begin, nch, tok0, seqlen)) return;
         uint64_t* full = reinterpret_cast<uint64_t*>(smem + kFhRingBytes);
         uint64_t* empty = full + kFhStages;
         if (threadIdx.x == 0) {
@@ -209,19 +212,26 @@ bool fused_heads_supported(int64_t n_seqs, int64_t H, int sms) {
 
 cudaError_t launch_fused_heads(const void* q, const void* k, const float* g, const void* beta,
                                const void* v, void* out, const void* init_state, void* final_state,
-                               uint8_t* packets, uint32_t* ready, const SeqGeometry& geo, int64_t H,
-                               float scale, int* status, cudaStream_t stream, bool beta_logit) {
+                               uint8_t* packets, uint32_t* ready, const int32_t* chunk_order,
+                               const SeqGeometry& geo, int64_t H, float scale, int* status,
+                               cudaStream_t stream, bool beta_logit) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
     if (e != cudaSuccess) return e;
-    if (geo.cu_chunks || geo.seg_chunks || geo.tokens <= 0 || geo.tokens >= (int64_t(1) << 31) ||
+    if (geo.seg_chunks || geo.tokens <= 0 || geo.tokens >= (int64_t(1) << 31) ||
+        (geo.cu_chunks && (!chunk_order || !geo.valid || !geo.cu_seqlens)) ||
         !fused_heads_supported(geo.n_seqs, H, sms))
         return cudaErrorInvalidValue;
     FusedHeadsArgs f;
     if (!prep::make_prep_args(&f.p, beta, packets, geo, H, scale, status, beta_logit))
         return cudaErrorInvalidValue;
-    f.p.interleave = 1;
+    // Items in the order the recurrences consume them: fixed layout chunk
+    // index first; packed by the chunks' relative positions.
+    if (geo.cu_chunks)
+        f.p.chunk_order = chunk_order;
+    else
+        f.p.interleave = 1;
     f.r.v = static_cast<const __nv_bfloat16*>(v);
     f.r.out = static_cast<__nv_bfloat16*>(out);
     f.r.init_state = static_cast<const __nv_bfloat16*>(init_state);

@@ -47,6 +47,11 @@ cudaError_t launch_varlen_meta(const int64_t* cu_seqlens, int64_t n_seqs, int64_
                                int32_t* valid, int64_t* cu_chunks, int32_t* order, int* status,
                                cudaStream_t stream);
 
+// order[r] = the chunk of rank r when the chunks of a packed batch are ranked
+// by their position relative to their sequence's length (kda_meta.cu).
+cudaError_t launch_chunk_order(const int64_t* cu_chunks, const int32_t* valid, int64_t n_seqs,
+                               int64_t chunk_ub, int32_t* order, cudaStream_t stream);
+
 // Consecutive groups of the sequences of a packed batch: group j is
 // sequences first[j] .. first[j + 1] - 1 (first[0] = 0, first[n] = N).
 constexpr int kMaxSeqGroups = 8;
@@ -152,8 +157,9 @@ cudaError_t launch_fused(const void* q, const void* k, const float* g, const voi
 bool fused_heads_supported(int64_t n_seqs, int64_t H, int sms);
 cudaError_t launch_fused_heads(const void* q, const void* k, const float* g, const void* beta,
                                const void* v, void* out, const void* init_state, void* final_state,
-                               uint8_t* packets, uint32_t* ready, const SeqGeometry& geo, int64_t H,
-                               float scale, int* status, cudaStream_t stream, bool beta_logit);
+                               uint8_t* packets, uint32_t* ready, const int32_t* chunk_order,
+                               const SeqGeometry& geo, int64_t H, float scale, int* status,
+                               cudaStream_t stream, bool beta_logit);
 
 // Tensor map of v viewed as a 2-D BF16 array [tokens][H * 128], boxes of
 // 16 tokens x `cols` value columns.

@@ -89,6 +89,50 @@ varlen_meta_kernel(const int64_t* cu, int64_t N, int64_t total, int32_t* valid,
     }
 }
 
+// The chunks of a packed batch in the order of their position relative to
+// their sequence's length: chunk i of a sequence of n chunks has the key
+// (2i + 1) / 2n, ties going to the lower sequence index.  order[r] is the
+// global index of the chunk of rank r.  A preparation that produces the
+// packets in this order brings every sequence along at the pace its length
+// needs, so the longest sequence's recurrence gets its packets about as fast
+// as it consumes them while the short ones are still being prepared.  The
+// rank of a chunk is the number of chunks with a smaller key (or an equal key
+// and a lower sequence index), counted per sequence in closed form: for
+// sequence m with n_m chunks, chunk i' has a smaller key than chunk i of
+// sequence n iff (2i' + 1) n < X with X = (2i + 1) n_m, i.e. for
+// i' < ceil(X / n) / 2, and an equal key iff n divides X with an odd
+// quotient.  The ranks of all chunks form a permutation of 0 .. total - 1.
+__global__ void chunk_order_kernel(const int64_t* cu_chunks, const int32_t* valid, int64_t N,
+                                   int64_t chunk_ub, int32_t* order) {
+    const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
+    if (c >= chunk_ub || !*valid || c >= cu_chunks[N]) return;
+    // The sequence of chunk c: the largest n with cu_chunks[n] <= c.
+    int64_t lo = 0, hi = N;
+    while (hi - lo > 1) {
+        const int64_t mid = (lo + hi) >> 1;
+        if (cu_chunks[mid] <= c)
+            lo = mid;
+        else
+            hi = mid;
+    }
+    const int64_t n = lo;
+    const int64_t nn = cu_chunks[n + 1] - cu_chunks[n];   // >= 1: chunk c is in it
+    const int64_t i = c - cu_chunks[n];
+    int64_t rank = i;
+    for (int64_t m = 0; m < N; ++m) {
+        if (m == n) continue;
+        const int64_t nm = cu_chunks[m + 1] - cu_chunks[m];
+        if (nm <= 0) continue;
+        const int64_t X = (2 * i + 1) * nm;
+        const int64_t q = (X + nn - 1) / nn;   // ceil(X / n)
+        int64_t less = q / 2;
+        if (less > nm) less = nm;
+        rank += less;
+        if (m < n && X % nn == 0 && ((X / nn) & 1)) rank += 1;
+    }
+    order[rank] = static_cast<int32_t>(c);
+}
+
 // Group j of a packed batch (sequences first[j] .. first[j + 1] - 1) gets its
 // offsets rebased to start at zero, at out[first[j] + j ..
 // first[j + 1] + j]: a packed batch of its own over the group's tokens.
@@ -105,6 +149,16 @@ cudaError_t launch_rebase_offsets(const int64_t* cu_seqlens, const SeqGroups& gr
                                   cudaStream_t stream) {
     if (groups.n < 1 || groups.n > kMaxSeqGroups) return cudaErrorInvalidValue;
     rebase_offsets_kernel<<<groups.n, 256, 0, stream>>>(cu_seqlens, groups, out);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_chunk_order(const int64_t* cu_chunks, const int32_t* valid, int64_t n_seqs,
+                               int64_t chunk_ub, int32_t* order, cudaStream_t stream) {
+    if (chunk_ub <= 0) return cudaSuccess;
+    if (chunk_ub >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    const int64_t blocks = (chunk_ub + 255) / 256;
+    chunk_order_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(cu_chunks, valid, n_seqs,
+                                                                         chunk_ub, order);
     return cudaGetLastError();
 }
 

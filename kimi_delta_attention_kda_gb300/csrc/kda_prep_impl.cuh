@@ -79,6 +79,9 @@ struct PrepArgs {
     // launch whose recurrence consumes every sequence at once gets each
     // sequence's first chunks first; 0: sequence by sequence.
     int interleave;
+    // Packed layout, may be null: the items are numbered by chunk rank
+    // (rank * H + head), and chunk_order[rank] is the chunk (launch_chunk_order).
+    const int32_t* chunk_order;
     FastDiv div_h;           // by H
     FastDiv div_cps;         // by geo.chunks_per_seq (fixed layout)
     FastDiv div_n;           // by geo.n_seqs (fixed layout, interleave)
@@ -91,6 +94,7 @@ inline bool make_prep_args(PrepArgs* a, const void* beta, uint8_t* packets, cons
     a->beta = static_cast<const __nv_bfloat16*>(beta);
     a->beta_logit = beta_logit ? 1 : 0;
     a->interleave = 0;
+    a->chunk_order = nullptr;
     a->packets = packets;
     a->geo = geo;
     a->geo.status = status;
@@ -184,10 +188,11 @@ __device__ __forceinline__ bool item_range(const PrepArgs& a, int64_t item, int6
     // item < n_chunk_heads < 2^31: 32-bit quotients by the launch's divisors.
     const uint32_t it = static_cast<uint32_t>(item);
     const uint32_t c32 = fast_div(it, a.div_h);
-    const int64_t c = c32;
+    int64_t c = c32;
     const int64_t h = it - c32 * a.div_h.d;
     if (a.geo.cu_chunks) {
         if (c >= a.geo.cu_chunks[a.geo.n_seqs]) return false;
+        if (a.chunk_order) c = a.chunk_order[c];
         const int64_t n = find_sequence(a.geo.cu_chunks, a.geo.n_seqs, c);
         *t0 = a.geo.cu_seqlens[n] + kChunk * (c - a.geo.cu_chunks[n]);
         *len = a.geo.cu_seqlens[n + 1] - *t0;

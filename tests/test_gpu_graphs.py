@@ -32,7 +32,10 @@ def kda():
 CASES = {
     "segmented_fixed": dict(B=1, T=8192, H=6, lengths=None),
     "one_launch": dict(B=1, T=1024, H=6, lengths=None),
-    "packed_long_split": dict(B=0, T=0, H=12, lengths=[4096, 512, 1024, 2048, 256, 3072, 768, 1536]),
+    # mean below 64 chunks: the two-kernel path, the longest four at split 2
+    "packed_long_split": dict(B=0, T=0, H=12, lengths=[3072, 256, 512, 1024, 128, 1536, 384, 768]),
+    # the many-head one-launch form (metadata, chunk order, one cooperative launch)
+    "packed_one_launch": dict(B=0, T=0, H=12, lengths=[4096, 512, 1024, 2048, 256, 3072, 768, 1536]),
     "segmented_packed": dict(B=0, T=0, H=6, lengths=[8192, 6000]),
     "one_cta_per_head": dict(B=1, T=2048, H=96, lengths=None),
 }
@@ -49,6 +52,10 @@ def test_graph_replay_equals_eager(kda, case):
     second = tu.to_device(_inputs(case, 8200))
     H = first["q"].shape[2]
     N = first["init_state"].shape[0]
+    if case.startswith("packed"):
+        T = first["q"].shape[1]
+        assert kda.plan_fused(N, T, H, True) == (case == "packed_one_launch")
+        assert (kda.plan_long_split(N, T, H) > 0) == (case == "packed_long_split")
     # Static buffers the graph reads and writes.
     static = {k: (None if v is None else v.clone()) for k, v in first.items()}
     out = torch.empty_like(static["v"])

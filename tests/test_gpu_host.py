@@ -154,7 +154,9 @@ def test_launch_counts(kda):
     """kda_last_call_launches reports the kernels one call enqueued: the
     preparation and the recurrence (more heads than SMs); one cooperative
     launch (many heads, or few heads and a short sequence); the segmented
-    scan's four kernels (six with the two-level chain)."""
+    scan's four kernels (six with the two-level chain); a packed batch in the
+    many-head form: the offsets' metadata, the chunk order and one
+    cooperative launch."""
     from kimi_delta_attention_kda_gb300 import _lib
     for (B, T, H), want in (((2, 2048, 96), 2), ((1, 2048, 96), 1), ((1, 256, 1), 1),
                             ((1, 8192, 6), 4), ((1, 65536, 1), 6)):
@@ -162,3 +164,8 @@ def test_launch_counts(kda):
         kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"])
         torch.cuda.synchronize()
         assert _lib.last_call_launches() == want, (B, T, H)
+    d = tu.to_device(synthetic.make_workload("varlen8_h12"))
+    kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                    cu_seqlens=d["cu_seqlens"])
+    torch.cuda.synchronize()
+    assert _lib.last_call_launches() == 3

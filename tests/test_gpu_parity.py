@@ -420,7 +420,8 @@ def test_fused_not_planned_where_it_cannot_run(kda):
     assert not kda.plan_fused(2, 8192, 96, False)   # 192 recurrence CTAs: more than the SMs
     assert not kda.plan_fused(1, 8192, 128, False)  # too few SMs left to the preparation
     assert not kda.plan_fused(1, 512, 96, False)    # too short to pay
-    assert not kda.plan_fused(1, 8192, 6, True)      # packed layout
+    assert not kda.plan_fused(1, 8192, 6, True)      # packed, few heads: the segmented scan
+    assert not kda.plan_fused(8, 8000, 12, True)     # packed, mean length below 64 chunks
     assert not kda.plan_fused(1, 0, 6, False)        # no tokens
 
 
@@ -487,6 +488,75 @@ def test_fused_repeated_calls_and_in_place(fusion_toggle):
     assert torch.equal(out.cpu(), a[0]) and torch.equal(state.cpu(), a[1])
 
 
+# Packed batches in the many-head one-launch form: the preparation makes each
+# sequence's packets in the order of their positions relative to the
+# sequence's length (launch_chunk_order), so every sequence's recurrence gets
+# them at its pace; the recurrence is the quad form (split 1), which sums in
+# the order of the split-1/split-2 launches of the two-kernel path.
+PACKED_MANY = {
+    "varlen8_h12": None,
+    "n4_h24": ([5131, 8000, 613, 2900], 24),
+    "n6_h16_ragged": ([4101, 1029, 7, 3333, 2048, 6000], 16),
+    "empty_and_short": ([0, 3000, 1, 0, 4100, 17, 2500, 600], 12),
+}
+
+
+def _packed_many_inputs(name, seed):
+    spec = PACKED_MANY[name]
+    if spec is None:
+        return synthetic.make_workload(name)
+    lengths, H = spec
+    return synthetic.make_inputs(0, 0, H, seed, init_std=0.02, lengths=lengths)
+
+
+@pytest.mark.parametrize("name", list(PACKED_MANY))
+def test_fused_many_heads_packed_matches_two_kernels_bitwise(fusion_toggle, name):
+    """Bit for bit the metadata, preparation and split-1/split-2 recurrence
+    launches, twice (the second call meets stale ready flags in reused pool
+    memory); the longest, shortest and an empty sequence's heads against the
+    oracle."""
+    kda = fusion_toggle
+    inp = _packed_many_inputs(name, 4400 + len(name))
+    N, T, H = inp["N"], inp["q"].shape[1], inp["q"].shape[2]
+    assert kda.plan_fused(N, T, H, True)
+    assert kda.plan_long_split(N, T, H) == 0
+    kda.set_fusion(True)
+    fused = run(kda, inp)
+    again = run(kda, inp)
+    kda.set_fusion(False)
+    assert not kda.plan_fused(N, T, H, True)
+    split = run(kda, inp)
+    for a, b in ((fused, split), (again, split)):
+        assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    tu.check_against_oracle(inp, fused[0], fused[1], heads=[0, H - 1])
+
+
+def test_fused_many_heads_packed_bad_offsets_and_in_place(fusion_toggle):
+    """Invalid offsets under the packed one-launch plan: the status bit, and
+    the outputs untouched; then an in-place call equals the out-of-place one."""
+    kda = fusion_toggle
+    inp = _packed_many_inputs("n4_h24", 4500)
+    d = tu.to_device(inp)
+    N, H = inp["N"], inp["q"].shape[2]
+    assert kda.plan_fused(N, inp["q"].shape[1], H, True)
+    cu = d["cu_seqlens"].clone()
+    cu[2] = cu[1] - 16
+    out = torch.full_like(d["v"], 7.0)
+    fin = torch.full((N, H, 128, 128), 7.0, dtype=torch.bfloat16, device="cuda")
+    kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"], cu_seqlens=cu,
+                    out=out, final_state=fin)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 1
+    assert bool((out == 7.0).all()) and bool((fin == 7.0).all())
+    ref = run(kda, inp)
+    state = d["init_state"].clone()
+    out, _ = kda.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], state,
+                             cu_seqlens=d["cu_seqlens"], final_state=state)
+    torch.cuda.synchronize()
+    assert kda.device_status() == 0
+    assert torch.equal(out.cpu(), ref[0]) and torch.equal(state.cpu(), ref[1])
+
+
 def test_packed_many_sequences_longest_first(kda):
     """300 packed sequences (0-400 tokens) at H=2 and split 1: 600 one-CTA-per-head
     units are more than one wave, so the recurrence takes the sequences longest
@@ -515,14 +585,18 @@ def test_packed_many_sequences_longest_first(kda):
     tu.check_against_oracle(inp, out, fin)
 
 
-def test_long_sequences_at_split_two_bitwise(kda):
+def test_long_sequences_at_split_two_bitwise(fusion_toggle):
     """The packed 12-head workload (8 sequences, 96 one-CTA-per-head units on
-    152 SMs): its 4 longest sequences run at split 2 in a second, concurrent
-    launch.  Splits 1 and 2 sum in the same order, so the call equals the
-    single-launch split-1 call bit for bit."""
+    152 SMs) without the one-launch form: its 4 longest sequences run at
+    split 2 in a second, concurrent launch.  Splits 1 and 2 sum in the same
+    order, so the call equals the single-launch split-1 call, and the
+    one-launch form, bit for bit."""
+    kda = fusion_toggle
     inp = synthetic.make_workload("varlen8_h12")
     N, T = inp["N"], inp["q"].shape[1]
     props = torch.cuda.get_device_properties(0)
+    fused = run(kda, inp)
+    kda.set_fusion(False)
     assert kda.plan_long_split(N, T, 12) == min(N, (props.multi_processor_count - N * 12) // 12)
     a = run(kda, inp)
     kda.set_split(1)
@@ -532,6 +606,7 @@ def test_long_sequences_at_split_two_bitwise(kda):
     finally:
         kda.set_split(0)
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
+    assert torch.equal(a[0], fused[0]) and torch.equal(a[1], fused[1])
 
 
 def test_chain_step_probe(kda):
