@@ -146,7 +146,7 @@ struct Plan {
     int64_t meta_bytes;      // valid flag + cu_chunks + order (packed only), 256-aligned
     int64_t packet_bytes;    // chunk_ub * H * kPacketBytes
     int64_t ready_bytes;     // chunk_ub * H flags of the fused launch, 256-aligned
-    int64_t order_bytes;     // packed: chunk_ub ranks of the many-head one-launch form, 256-aligned
+    int64_t order_bytes;     // packed: chunk order and alone flags of the many-head one-launch form
 };
 
 int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
@@ -179,7 +179,9 @@ int make_plan(int64_t B, int64_t T, int64_t H, bool packed, Plan* p) {
     p->packet_bytes = g.chunk_ub * H * static_cast<int64_t>(kPacketBytes);
     // One flag per packet, then the many-head one-launch form's item counter.
     p->ready_bytes = g.chunk_ub > 0 ? ((g.chunk_ub * H * 4 + 4 + 255) / 256) * 256 : 0;
-    p->order_bytes = packed && g.chunk_ub > 0 ? ((g.chunk_ub * 4 + 255) / 256) * 256 : 0;
+    p->order_bytes =
+        packed && g.chunk_ub > 0 ? ((g.chunk_ub * 4 + 255) / 256) * 256 + ((B * 4 + 255) / 256) * 256
+                                 : 0;
     return KDA_OK;
 }
 
@@ -504,6 +506,7 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
         // context), fall through to the two-kernel path.
         uint32_t* ready = reinterpret_cast<uint32_t*>(ws + pl.meta_bytes + pl.packet_bytes);
         int32_t* chunk_order = nullptr;
+        int32_t* alone = nullptr;
         geo = pl.geo;
         if (pl.packed) {
             // Offsets checked and chunk offsets on the device, then the
@@ -512,12 +515,14 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
             int64_t* cu_chunks = reinterpret_cast<int64_t*>(ws + 256);
             chunk_order = reinterpret_cast<int32_t*>(ws + pl.meta_bytes + pl.packet_bytes +
                                                      pl.ready_bytes);
+            alone = chunk_order + ((pl.geo.chunk_ub + 63) / 64) * 64;
             if (launch_varlen_meta(cu_seqlens, pl.N, pl.tokens, valid, cu_chunks, nullptr,
                                    d->status, stream) != cudaSuccess)
                 rc = KDA_ERR_CUDA;
             ++t_launches;
             if (rc == KDA_OK && launch_chunk_order(cu_chunks, valid, pl.N, pl.geo.chunk_ub,
-                                                   chunk_order, stream) != cudaSuccess)
+                                                   chunk_order, alone, H, d->sms,
+                                                   stream) != cudaSuccess)
                 rc = KDA_ERR_CUDA;
             ++t_launches;
             geo.cu_seqlens = cu_seqlens;
@@ -534,8 +539,8 @@ int prefill_impl(const void* q, const void* k, const void* v, const float* g, co
             const cudaError_t e =
                 fused_many
                     ? launch_fused_heads(q, k, g, beta, v, out, init_state, final_state,
-                                         ws + pl.meta_bytes, ready, chunk_order, geo, H, kScale,
-                                         d->status, stream, beta_logit)
+                                         ws + pl.meta_bytes, ready, chunk_order, alone, geo, H,
+                                         kScale, d->status, stream, beta_logit)
                     : launch_fused(q, k, g, beta, v, out, init_state, final_state,
                                    ws + pl.meta_bytes, ready, pl.geo, H, nsplit, kScale, d->status,
                                    stream, ck, beta_logit);

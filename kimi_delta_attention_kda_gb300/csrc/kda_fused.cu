@@ -130,6 +130,7 @@ struct FusedHeadsArgs {
     int64_t rec_blocks;
     uint32_t* ready;     // one flag per packet, then the item counter (all zero at launch)
     uint32_t* counter;
+    const int32_t* alone;   // packed, may be null: alone[n] = 1, no preparing pairs beside n's heads
 };
 
 // The mbarrier of pair `pair` (at bars[pair]), initialised by the pair's
@@ -186,6 +187,9 @@ __global__ void __launch_bounds__(kFhThreads, 1)
             // Warpgroup 3 gives its registers to warpgroup 0 and leaves.
             asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;\n" ::"n"(kFhIdleRegs) : "memory");
         } else {
+            // A long sequence's recurrence runs alone on its SM (its step is
+            // the critical chain); both warps of every pair read the same flag.
+            if (f.alone && f.alone[n]) return;
             const int pair = (warp - 2 * kFhRecWarps) >> 1, hw = warp & 1;
             const int bid = 1 + pair;
             uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFhRecPairBarOff);
@@ -213,8 +217,8 @@ bool fused_heads_supported(int64_t n_seqs, int64_t H, int sms) {
 cudaError_t launch_fused_heads(const void* q, const void* k, const float* g, const void* beta,
                                const void* v, void* out, const void* init_state, void* final_state,
                                uint8_t* packets, uint32_t* ready, const int32_t* chunk_order,
-                               const SeqGeometry& geo, int64_t H, float scale, int* status,
-                               cudaStream_t stream, bool beta_logit) {
+                               const int32_t* alone, const SeqGeometry& geo, int64_t H,
+                               float scale, int* status, cudaStream_t stream, bool beta_logit) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
     cudaError_t e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -246,6 +250,7 @@ cudaError_t launch_fused_heads(const void* q, const void* k, const float* g, con
     f.rec_blocks = geo.n_seqs * H;
     f.ready = ready;
     f.counter = ready + geo.chunk_ub * H;
+    f.alone = geo.cu_chunks ? alone : nullptr;
     prep::PrepMaps maps;
     e = prep::encode_maps(&maps, q, k, g, geo.tokens, H);
     if (e != cudaSuccess) return e;

@@ -48,9 +48,12 @@ cudaError_t launch_varlen_meta(const int64_t* cu_seqlens, int64_t n_seqs, int64_
                                cudaStream_t stream);
 
 // order[r] = the chunk of rank r when the chunks of a packed batch are ranked
-// by their position relative to their sequence's length (kda_meta.cu).
+// by their position relative to their sequence's length, and alone[n] = 1 for
+// the sequences whose recurrences run without preparing pairs on their SMs in
+// the many-head one-launch form of H heads on `grid` SMs (kda_meta.cu).
 cudaError_t launch_chunk_order(const int64_t* cu_chunks, const int32_t* valid, int64_t n_seqs,
-                               int64_t chunk_ub, int32_t* order, cudaStream_t stream);
+                               int64_t chunk_ub, int32_t* order, int32_t* alone, int64_t H,
+                               int64_t grid, cudaStream_t stream);
 
 // Consecutive groups of the sequences of a packed batch: group j is
 // sequences first[j] .. first[j + 1] - 1 (first[0] = 0, first[n] = N).
@@ -158,8 +161,8 @@ bool fused_heads_supported(int64_t n_seqs, int64_t H, int sms);
 cudaError_t launch_fused_heads(const void* q, const void* k, const float* g, const void* beta,
                                const void* v, void* out, const void* init_state, void* final_state,
                                uint8_t* packets, uint32_t* ready, const int32_t* chunk_order,
-                               const SeqGeometry& geo, int64_t H, float scale, int* status,
-                               cudaStream_t stream, bool beta_logit);
+                               const int32_t* alone, const SeqGeometry& geo, int64_t H,
+                               float scale, int* status, cudaStream_t stream, bool beta_logit);
 
 // Tensor map of v viewed as a 2-D BF16 array [tokens][H * 128], boxes of
 // 16 tokens x `cols` value columns.

@@ -102,8 +102,62 @@ varlen_meta_kernel(const int64_t* cu, int64_t N, int64_t total, int32_t* valid,
 // sequence n iff (2i' + 1) n < X with X = (2i + 1) n_m, i.e. for
 // i' < ceil(X / n) / 2, and an equal key iff n divides X with an odd
 // quotient.  The ranks of all chunks form a permutation of 0 .. total - 1.
+//
+// Block 0 also picks which sequences' recurrences run without preparing
+// pairs beside them (alone[n] = 1): the k longest, with k minimising the
+// larger of the preparation's time on the pairs that remain and the longest
+// chain, a recurrence alone on its SM taking kAloneStepUs per chunk and one
+// beside two pairs kSharedStepUs (the preparation rate and both step times
+// measured on GB300 in the many-head one-launch form of a packed 8-sequence,
+// 12-head batch).  Equal lengths give k = 0.
+constexpr int kAloneMaxSeqs = 256;
+constexpr double kPairItemsPerUs = 0.108;
+constexpr double kAloneStepUs = 1.02;
+constexpr double kSharedStepUs = 1.12;
+
 __global__ void chunk_order_kernel(const int64_t* cu_chunks, const int32_t* valid, int64_t N,
-                                   int64_t chunk_ub, int32_t* order) {
+                                   int64_t chunk_ub, int32_t* order, int32_t* alone, int64_t H,
+                                   int64_t grid) {
+    if (blockIdx.x == 0 && alone) {
+        __shared__ int64_t sorted[kAloneMaxSeqs];
+        __shared__ int64_t best_k;
+        const bool ok = *valid && N <= kAloneMaxSeqs;
+        int64_t rank[kAloneMaxSeqs / 256];
+        for (int64_t n = threadIdx.x, j = 0; ok && n < N; n += blockDim.x, ++j) {
+            const int64_t cn = cu_chunks[n + 1] - cu_chunks[n];
+            int64_t r = 0;
+            for (int64_t m = 0; m < N; ++m) {
+                const int64_t cm = cu_chunks[m + 1] - cu_chunks[m];
+                r += (cm > cn || (cm == cn && m < n)) ? 1 : 0;
+            }
+            rank[j] = r;
+            sorted[r] = cn;
+        }
+        __syncthreads();
+        if (threadIdx.x == 0) {
+            best_k = 0;
+            if (ok) {
+                const double items = static_cast<double>(cu_chunks[N]) * H;
+                const int64_t units = N * H;
+                const double pairs0 = 2.0 * units + 8.0 * (grid - units);
+                double best = 0.0;
+                for (int64_t k = 0; k < N; ++k) {
+                    const double pairs = pairs0 - 2.0 * H * k;
+                    if (pairs <= 0.0) break;
+                    double t = items / (kPairItemsPerUs * pairs);
+                    if (k > 0 && sorted[0] * kAloneStepUs > t) t = sorted[0] * kAloneStepUs;
+                    if (sorted[k] * kSharedStepUs > t) t = sorted[k] * kSharedStepUs;
+                    if (k == 0 || t < best) {
+                        best = t;
+                        best_k = k;
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        for (int64_t n = threadIdx.x, j = 0; n < N; n += blockDim.x, ++j)
+            alone[n] = ok && rank[j] < best_k ? 1 : 0;
+    }
     const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (c >= chunk_ub || !*valid || c >= cu_chunks[N]) return;
     // The sequence of chunk c: the largest n with cu_chunks[n] <= c.
@@ -153,12 +207,14 @@ cudaError_t launch_rebase_offsets(const int64_t* cu_seqlens, const SeqGroups& gr
 }
 
 cudaError_t launch_chunk_order(const int64_t* cu_chunks, const int32_t* valid, int64_t n_seqs,
-                               int64_t chunk_ub, int32_t* order, cudaStream_t stream) {
+                               int64_t chunk_ub, int32_t* order, int32_t* alone, int64_t H,
+                               int64_t grid, cudaStream_t stream) {
     if (chunk_ub <= 0) return cudaSuccess;
-    if (chunk_ub >= (int64_t(1) << 31)) return cudaErrorInvalidValue;
+    if (chunk_ub >= (int64_t(1) << 31) || n_seqs < 1 || H < 1 || grid < 1)
+        return cudaErrorInvalidValue;
     const int64_t blocks = (chunk_ub + 255) / 256;
-    chunk_order_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(cu_chunks, valid, n_seqs,
-                                                                         chunk_ub, order);
+    chunk_order_kernel<<<static_cast<unsigned>(blocks), 256, 0, stream>>>(
+        cu_chunks, valid, n_seqs, chunk_ub, order, alone, H, grid);
     return cudaGetLastError();
 }
 

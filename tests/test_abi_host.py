@@ -147,13 +147,13 @@ def test_workspace_bytes(lib):
         assert _lib.workspace_bytes(1, 8192, 6, False) == 512 * 6 * pb + 12544
         lib.kda_set_segments(1, 0)
         # packed, 8 sequences, 24,672 tokens, 12 heads: the many-head one-launch
-        # form, so also the ready flags (and the item counter) and the chunk
-        # order, 4 bytes a chunk (1,549 chunks at most)
+        # form, so also the ready flags (and the item counter), the chunk
+        # order, 4 bytes a chunk (1,549 chunks at most), and a flag a sequence
         n, T, H = 8, 24672, 12
         meta = 256 + 256 + 256
         cub = (T + 15 * n) // 16
         ready = ((cub * H * 4 + 4 + 255) // 256) * 256
-        order = ((cub * 4 + 255) // 256) * 256
+        order = ((cub * 4 + 255) // 256) * 256 + 256
         assert _lib.workspace_bytes(n, T, H, True) == meta + cub * H * pb + ready + order
         lib.kda_set_fusion(0)
         assert _lib.workspace_bytes(n, T, H, True) == meta + cub * H * pb
