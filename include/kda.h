@@ -170,9 +170,10 @@ int kda_set_split(int nsplit);
  * (their partial sums over keys are added in a fixed order, so results agree
  * with the other variants to rounding, not bit for bit).  Engine 1 gives each
  * warp 8 columns and all 128 keys at every split.  2: the tcgen05
- * kernel (one CTA per (sequence, head); the value rows are the MMA's M = 128,
- * operands are read by the tensor cores straight from shared memory,
- * accumulators live in tensor memory; the split setting is ignored).
+ * kernel (one CTA per (sequence, head); the value rows are the MMA's M = 128;
+ * the FP32 state, its BF16 operand copy and every accumulator live in tensor
+ * memory, the packets are read by the tensor cores from shared memory; the
+ * split setting is ignored).
  * Process-wide; returns KDA_ERR_ARG for other values.
  */
 int kda_set_engine(int engine);
