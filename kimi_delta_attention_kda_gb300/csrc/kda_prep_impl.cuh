@@ -561,9 +561,10 @@ __device__ __forceinline__ uint64_t* pair_barrier(uint8_t* smem, int pair, int h
 // once the item's packet is in global memory; the flag of an item is
 // published when the pair has issued the next item's loads, or at the end.
 // With `counter` (a zeroed global word) the pairs instead take items in
-// order from it (atomicAdd by the pair's issuing thread, handed to the other
-// warp through `slot`, a shared word of the pair), so that faster pairs take
-// more items; `first` and `stride` are then unused.
+// order from it (atomicAdd by the pair's issuing thread once the item's loads
+// are issued, handed to the other warp through `slot`, a shared word of the
+// pair), so that faster pairs take more items; `first` and `stride` are then
+// unused.
 __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& maps, uint8_t* region,
                                           uint64_t* bar, int bid, int hw, int lane, int64_t first,
                                           int64_t stride, uint32_t* ready,
@@ -585,10 +586,6 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
         if (!item_range(a, item, &t0, &len, &c, &h)) break;   // items only grow past the end
         int64_t next = item + stride;
         if (issuer) {
-            if (counter) {
-                next = static_cast<int64_t>(atomicAdd(counter, 1u));
-                *slot = next;   // read by the other warp after the barrier below
-            }
             // The previous packet store must have read the region before TMA
             // overwrites it; the region's generic-proxy writes were fenced
             // (fence.proxy.async) before that store.
@@ -598,6 +595,12 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
             tma_load_2d(region + kInQ, &maps.q, x, y, bar);
             tma_load_2d(region + kInK, &maps.k, x, y, bar);
             tma_load_2d(region + kInG, &maps.g, x, y, bar);
+            // The next item's number, once this item's loads are on their way
+            // (the atomic's round trip then overlaps them).
+            if (counter) {
+                next = static_cast<int64_t>(atomicAdd(counter, 1u));
+                *slot = next;   // read by the other warp after the barrier below
+            }
             // This pair's next item: its tiles on their way to L2 while this
             // item is worked on, so that its loads above find them there.
             int64_t nt0, nlen, nc, nh;
