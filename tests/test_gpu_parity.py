@@ -337,6 +337,47 @@ def test_tcgen05_deterministic(tc_engine):
     assert torch.equal(a[0], b[0]) and torch.equal(a[1], b[1])
 
 
+def test_tcgen05_packed_beta_logit(tc_engine):
+    """beta as a logit through the tcgen05 engine: packed, with empty, one-token
+    and ragged sequences, against the oracle run with the same option."""
+    import oracle
+    inp = synthetic.make_inputs(0, 0, 3, 61, init_std=0.02, lengths=[40, 0, 1, 17, 300])
+    gen = torch.Generator(device="cpu")
+    gen.manual_seed(62)
+    inp["beta"] = (2.0 * torch.randn(inp["beta"].shape, generator=gen)).to(torch.bfloat16)
+    d = tu.to_device(inp)
+    out, fin = tc_engine.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], d["init_state"],
+                                     cu_seqlens=d["cu_seqlens"], beta_is_logit=True)
+    torch.cuda.synchronize()
+    assert tc_engine.device_status() == 0
+    o_ref, f_ref = oracle.kda_token(inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                    inp["init_state"], cu_seqlens=inp["cu_seqlens"].numpy(),
+                                    beta_is_logit=True)
+    o, f = out.cpu().double().numpy(), fin.cpu().double().numpy()
+    c = inp["cu_seqlens"].numpy()
+    for n in range(len(c) - 1):
+        if c[n + 1] > c[n]:
+            tu.assert_within_tolerance(o[0, c[n]:c[n + 1]], o_ref[0, c[n]:c[n + 1]], 1,
+                                       "O seq %d" % n)
+        tu.assert_within_tolerance(f[n], f_ref[n], 0, "final seq %d" % n)
+
+
+def test_tcgen05_bad_cu_seqlens_leaves_outputs(tc_engine):
+    """Invalid offsets: the tcgen05 CTAs leave before they allocate tensor
+    memory; the status bit is set and neither output is touched."""
+    inp = synthetic.make_inputs(1, 20, 2, 4, init_std=0.02)
+    d = tu.to_device(inp)
+    cu_t = torch.tensor([0, 10, 5, 20], dtype=torch.int64, device="cuda")
+    init = torch.randn((3, 2, 128, 128), device="cuda").to(torch.bfloat16)
+    out = torch.full_like(d["v"], 7.0)
+    fin = torch.full_like(init, 3.0)
+    tc_engine.kda_prefill(d["q"], d["k"], d["v"], d["g"], d["beta"], init, cu_seqlens=cu_t,
+                          out=out, final_state=fin)
+    torch.cuda.synchronize()
+    assert tc_engine.device_status() & 1
+    assert torch.all(out == 7.0) and torch.all(fin == 3.0)
+
+
 @pytest.mark.parametrize("name", ["t8192_h6", "t65536_h1", "varlen8_h12"])
 def test_tcgen05_full_workload(tc_engine, name):
     inp = synthetic.make_workload(name)
