@@ -10,7 +10,7 @@
 namespace kda {
 namespace {
 
-constexpr int kTcStages = 6;
+constexpr int kTcStages = 4;
 constexpr uint32_t kTcOffUA = kTcStages * tcr::kStageBytes;   // U (FP16), 128 x 16, SW32
 constexpr uint32_t kTcOffVT = kTcOffUA + 4096;                 // V^T (BF16), 128 x 16, SW32
 constexpr uint32_t kTcOffBar = kTcOffVT + 4096;
@@ -31,7 +31,7 @@ struct TcArgs {
     int* status;
 };
 
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(kTcThreads, 2)
     recurrence_tc_kernel(TcArgs a, const __grid_constant__ CUtensorMap vmap) {
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>(

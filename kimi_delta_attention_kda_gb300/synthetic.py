@@ -57,6 +57,9 @@ WORKLOADS = {
     "t8192_h6": Workload("B=1,H=6,T=8192,d=128", B=1, H=6, T=8192, seed=1, init_std=0.02),
     # Full head count at 8,192 tokens.
     "t8192_h96": Workload("B=1,H=96,T=8192,d=128", B=1, H=96, T=8192, seed=2),
+    # Full head count, a batch of two sequences: more (sequence, head) chains
+    # than the GPU has SMs (a measurement case beside the five above).
+    "t8192_h96_b2": Workload("B=2,H=96,T=8192,d=128", B=2, H=96, T=8192, seed=5),
     # Packed: 8 sequences, lengths uniform in [512, 8192] rounded to multiples of 16.
     "varlen8_h12": Workload("packed B=1,H=12,d=128,N=8", B=1, H=12, T=0, seed=3,
                             init_std=0.02, packed_n=8),
