@@ -111,17 +111,31 @@ varlen_meta_kernel(const int64_t* cu, int64_t N, int64_t total, int32_t* valid,
 // measured on GB300 in the many-head one-launch form of a packed 8-sequence,
 // 12-head batch).  Equal lengths give k = 0.
 constexpr int kAloneMaxSeqs = 256;
-constexpr double kPairItemsPerUs = 0.108;
-constexpr double kAloneStepUs = 1.02;
-constexpr double kSharedStepUs = 1.12;
+// (FP32: an estimate, and FP64 arithmetic is slow on this GPU.)
+constexpr float kPairItemsPerUs = 0.108f;
+constexpr float kAloneStepUs = 1.02f;
+constexpr float kSharedStepUs = 1.12f;
 
-__global__ void chunk_order_kernel(const int64_t* cu_chunks, const int32_t* valid, int64_t N,
+constexpr int64_t kOrderSmemSeqs = 1024;   // offsets staged in shared memory up to this many
+
+__global__ void chunk_order_kernel(const int64_t* cu_chunks_g, const int32_t* valid, int64_t N,
                                    int64_t chunk_ub, int32_t* order, int32_t* alone, int64_t H,
                                    int64_t grid) {
+    // The chunk offsets are read many times by every thread: stage them in
+    // shared memory once per block (short chains of dependent global loads
+    // were most of this kernel's time).
+    __shared__ int64_t cu_s[kOrderSmemSeqs + 1];
+    __shared__ int32_t valid_s;
+    const bool staged = N <= kOrderSmemSeqs;
+    if (staged)
+        for (int64_t n = threadIdx.x; n <= N; n += blockDim.x) cu_s[n] = cu_chunks_g[n];
+    if (threadIdx.x == 0) valid_s = *valid;
+    __syncthreads();
+    const int64_t* cu_chunks = staged ? cu_s : cu_chunks_g;
     if (blockIdx.x == 0 && alone) {
         __shared__ int64_t sorted[kAloneMaxSeqs];
         __shared__ int64_t best_k;
-        const bool ok = *valid && N <= kAloneMaxSeqs;
+        const bool ok = valid_s && N <= kAloneMaxSeqs;
         int64_t rank[kAloneMaxSeqs / 256];
         for (int64_t n = threadIdx.x, j = 0; ok && n < N; n += blockDim.x, ++j) {
             const int64_t cn = cu_chunks[n + 1] - cu_chunks[n];
@@ -137,16 +151,18 @@ __global__ void chunk_order_kernel(const int64_t* cu_chunks, const int32_t* vali
         if (threadIdx.x == 0) {
             best_k = 0;
             if (ok) {
-                const double items = static_cast<double>(cu_chunks[N]) * H;
+                const float items = static_cast<float>(cu_chunks[N]) * static_cast<float>(H);
                 const int64_t units = N * H;
-                const double pairs0 = 2.0 * units + 8.0 * (grid - units);
-                double best = 0.0;
+                const float pairs0 = 2.f * static_cast<float>(units) + 8.f * static_cast<float>(grid - units);
+                float best = 0.f;
                 for (int64_t k = 0; k < N; ++k) {
-                    const double pairs = pairs0 - 2.0 * H * k;
-                    if (pairs <= 0.0) break;
-                    double t = items / (kPairItemsPerUs * pairs);
-                    if (k > 0 && sorted[0] * kAloneStepUs > t) t = sorted[0] * kAloneStepUs;
-                    if (sorted[k] * kSharedStepUs > t) t = sorted[k] * kSharedStepUs;
+                    const float pairs = pairs0 - 2.f * static_cast<float>(H * k);
+                    if (pairs <= 0.f) break;
+                    float t = items / (kPairItemsPerUs * pairs);
+                    const float alone_t = static_cast<float>(sorted[0]) * kAloneStepUs;
+                    const float shared_t = static_cast<float>(sorted[k]) * kSharedStepUs;
+                    if (k > 0 && alone_t > t) t = alone_t;
+                    if (shared_t > t) t = shared_t;
                     if (k == 0 || t < best) {
                         best = t;
                         best_k = k;
@@ -159,7 +175,7 @@ __global__ void chunk_order_kernel(const int64_t* cu_chunks, const int32_t* vali
             alone[n] = ok && rank[j] < best_k ? 1 : 0;
     }
     const int64_t c = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
-    if (c >= chunk_ub || !*valid || c >= cu_chunks[N]) return;
+    if (c >= chunk_ub || !valid_s || c >= cu_chunks[N]) return;
     // The sequence of chunk c: the largest n with cu_chunks[n] <= c.
     int64_t lo = 0, hi = N;
     while (hi - lo > 1) {
@@ -178,11 +194,23 @@ __global__ void chunk_order_kernel(const int64_t* cu_chunks, const int32_t* vali
         const int64_t nm = cu_chunks[m + 1] - cu_chunks[m];
         if (nm <= 0) continue;
         const int64_t X = (2 * i + 1) * nm;
-        const int64_t q = (X + nn - 1) / nn;   // ceil(X / n)
-        int64_t less = q / 2;
+        // q = floor(X / n), r = X mod n: in 32 bits when X fits (every batch
+        // of fewer than about 46,000 chunks per sequence), exact either way.
+        int64_t q, r;
+        if (X < (int64_t(1) << 32)) {
+            const uint32_t x32 = static_cast<uint32_t>(X), n32 = static_cast<uint32_t>(nn);
+            const uint32_t q32 = x32 / n32;
+            q = q32;
+            r = x32 - q32 * n32;
+        } else {
+            q = X / nn;
+            r = X - q * nn;
+        }
+        // Chunks of m with (2 i' + 1) n < (2 i + 1) nm: i' < ceil(X / n) / 2.
+        int64_t less = (q + (r != 0 ? 1 : 0)) / 2;
         if (less > nm) less = nm;
         rank += less;
-        if (m < n && X % nn == 0 && ((X / nn) & 1)) rank += 1;
+        if (m < n && r == 0 && (q & 1)) rank += 1;
     }
     order[rank] = static_cast<int32_t>(c);
 }
