@@ -1,7 +1,7 @@
 """Helpers shared by the tests: tolerance metrics, packet decoding, and oracle
 runs on a subset of heads.
 
-The tolerance is the one the task fixes for BF16 I/O with FP32 accumulation:
+The tolerance for BF16 inputs and outputs with FP32 accumulation:
 per (sequence, head), relative Frobenius error <= 1e-2 and max-abs error
 <= 3e-2, for the output O (T_n x 128) and the final state (128 x 128); when
 the reference is all zeros only the max-abs bound applies.
