@@ -34,8 +34,8 @@ struct FusedArgs {
 
 template <int NCG>
 constexpr uint32_t fused_smem_bytes() {
-    return KsLayout<NCG>::kSmemBytes > prep::kPrepSmemBytes ? KsLayout<NCG>::kSmemBytes
-                                                            : prep::kPrepSmemBytes;
+    return KsLayout<NCG>::kSmemBytes > prep::kPrepSmemBytes + 32 ? KsLayout<NCG>::kSmemBytes
+                                                                 : prep::kPrepSmemBytes + 32;
 }
 
 template <int NCG>
@@ -57,8 +57,15 @@ __global__ void __launch_bounds__(kFusedThreads, 1)
         uint64_t* bar = prep::pair_barrier(smem, pair, hw, lane, bid);
         const int64_t pb = static_cast<int64_t>(blockIdx.x) - f.rec_blocks;
         const int64_t pgrid = static_cast<int64_t>(gridDim.x) - f.rec_blocks;
+        prep::PairCtl* ctl = reinterpret_cast<prep::PairCtl*>(
+            smem + prep::kPrepPairs * prep::kPrepRegion + 8 * prep::kPrepPairs);
+        if (threadIdx.x == 0) {
+            ctl->ready = f.ready;
+            ctl->counter = nullptr;
+        }
+        __syncthreads();
         prep::run_items(f.p, maps, smem + pair * prep::kPrepRegion, bar, bid, hw, lane,
-                        pb * prep::kPrepPairs + pair, pgrid * prep::kPrepPairs, f.ready);
+                        pb * prep::kPrepPairs + pair, pgrid * prep::kPrepPairs, ctl);
     }
 }
 
@@ -118,8 +125,8 @@ constexpr uint32_t kFhRecPrepOff = kFhRingBytes + 1024;   // ring barriers in be
 constexpr uint32_t kFhRecPairBarOff = kFhRecPrepOff + kFhRecPairs * prep::kPrepRegion;
 constexpr uint32_t kFhPrepPairBarOff = kFhPrepPairs * prep::kPrepRegion;
 // Each pair's mbarrier and its item slot (run_items' counter mode) follow the regions.
-constexpr uint32_t kFhRecBytes = kFhRecPairBarOff + 16 * kFhRecPairs;
-constexpr uint32_t kFhPrepBytes = kFhPrepPairBarOff + 16 * kFhPrepPairs;
+constexpr uint32_t kFhRecBytes = kFhRecPairBarOff + (8 + sizeof(prep::PairCtl)) * kFhRecPairs;
+constexpr uint32_t kFhPrepBytes = kFhPrepPairBarOff + (8 + sizeof(prep::PairCtl)) * kFhPrepPairs;
 constexpr uint32_t kFhSmemBytes = (kFhRecBytes > kFhPrepBytes ? kFhRecBytes : kFhPrepBytes) + 1024;
 static_assert(kFhSmemBytes <= 227 * 1024, "one-launch CTA exceeds shared memory");
 static_assert(2 * kFhStages * 8 <= 1024, "ring barriers overflow their slot");
@@ -194,16 +201,26 @@ __global__ void __launch_bounds__(kFhThreads, 1)
             const int bid = 1 + pair;
             uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFhRecPairBarOff);
             uint64_t* bar = fh_pair_barrier(bars, pair, hw, lane, bid);
+            prep::PairCtl* ctl = reinterpret_cast<prep::PairCtl*>(bars + kFhRecPairs) + pair;
+            if (hw == 0 && lane == 0) {
+                ctl->ready = f.ready;
+                ctl->counter = f.counter;
+            }
+            pair_sync(bid);
             prep::run_items(f.p, maps, smem + kFhRecPrepOff + pair * prep::kPrepRegion, bar, bid, hw,
-                            lane, 0, pairs, f.ready, f.counter,
-                            reinterpret_cast<int64_t*>(bars + kFhRecPairs) + pair);
+                            lane, 0, pairs, ctl);
         }
     } else {
         const int pair = warp >> 1, hw = warp & 1, bid = 1 + pair;
         uint64_t* bars = reinterpret_cast<uint64_t*>(smem + kFhPrepPairBarOff);
         uint64_t* bar = fh_pair_barrier(bars, pair, hw, lane, bid);
-        prep::run_items(f.p, maps, smem + pair * prep::kPrepRegion, bar, bid, hw, lane, 0, pairs,
-                        f.ready, f.counter, reinterpret_cast<int64_t*>(bars + kFhPrepPairs) + pair);
+        prep::PairCtl* ctl = reinterpret_cast<prep::PairCtl*>(bars + kFhPrepPairs) + pair;
+        if (hw == 0 && lane == 0) {
+            ctl->ready = f.ready;
+            ctl->counter = f.counter;
+        }
+        pair_sync(bid);
+        prep::run_items(f.p, maps, smem + pair * prep::kPrepRegion, bar, bid, hw, lane, 0, pairs, ctl);
     }
 }
 

@@ -183,39 +183,39 @@ __device__ __forceinline__ void st_row4_split(uint8_t* hi, uint8_t* lo, int t, i
 
 // Token range [t0, t0 + len) of item (chunk c, head h); false when the item
 // does not exist (past the last chunk of a packed batch, or invalid offsets).
-__device__ __forceinline__ bool item_range(const PrepArgs& a, int64_t item, int64_t* t0,
-                                           int64_t* len, int64_t* c_out, int64_t* h_out) {
-    // item < n_chunk_heads < 2^31: 32-bit quotients by the launch's divisors.
-    const uint32_t it = static_cast<uint32_t>(item);
-    const uint32_t c32 = fast_div(it, a.div_h);
-    int64_t c = c32;
-    const int64_t h = it - c32 * a.div_h.d;
+// Every quantity fits 32 bits: items < 2^31 (make_prep_args) and tokens
+// < 2^31 (the C ABI's shape check), so the item loop keeps 32-bit
+// bookkeeping (64-bit values there cost registers the item code needs).
+__device__ __forceinline__ bool item_range(const PrepArgs& a, uint32_t item, int32_t* t0,
+                                           int32_t* len, int32_t* c_out, int32_t* h_out) {
+    const uint32_t c32 = fast_div(item, a.div_h);
+    int32_t c = static_cast<int32_t>(c32);
+    const int32_t h = static_cast<int32_t>(item - c32 * a.div_h.d);
+    int64_t ln;
     if (a.geo.cu_chunks) {
         if (c >= a.geo.cu_chunks[a.geo.n_seqs]) return false;
         if (a.chunk_order) c = a.chunk_order[c];
         const int64_t n = find_sequence(a.geo.cu_chunks, a.geo.n_seqs, c);
-        *t0 = a.geo.cu_seqlens[n] + kChunk * (c - a.geo.cu_chunks[n]);
-        *len = a.geo.cu_seqlens[n + 1] - *t0;
+        const int64_t t = a.geo.cu_seqlens[n] + kChunk * (c - a.geo.cu_chunks[n]);
+        *t0 = static_cast<int32_t>(t);
+        ln = a.geo.cu_seqlens[n + 1] - t;
     } else if (a.interleave) {
         // c32 = chunk-in-sequence * N + sequence; the packet goes to the
         // sequence-by-sequence chunk number.
         const uint32_t ci32 = fast_div(c32, a.div_n);
         const int64_t n = c32 - ci32 * a.div_n.d;
         const int64_t ci = ci32;
-        *t0 = n * a.geo.tokens_per_seq + kChunk * ci;
-        *len = a.geo.tokens_per_seq - kChunk * ci;
-        if (*len > kChunk) *len = kChunk;
-        *c_out = n * a.geo.chunks_per_seq + ci;
-        *h_out = h;
-        return true;
+        *t0 = static_cast<int32_t>(n * a.geo.tokens_per_seq + kChunk * ci);
+        ln = a.geo.tokens_per_seq - kChunk * ci;
+        c = static_cast<int32_t>(n * a.geo.chunks_per_seq + ci);
     } else {
         const uint32_t n32 = fast_div(c32, a.div_cps);
         const int64_t n = n32;
         const int64_t ci = c32 - n32 * a.div_cps.d;
-        *t0 = n * a.geo.tokens_per_seq + kChunk * ci;
-        *len = a.geo.tokens_per_seq - kChunk * ci;
+        *t0 = static_cast<int32_t>(n * a.geo.tokens_per_seq + kChunk * ci);
+        ln = a.geo.tokens_per_seq - kChunk * ci;
     }
-    if (*len > kChunk) *len = kChunk;
+    *len = static_cast<int32_t>(ln > kChunk ? kChunk : ln);
     *c_out = c;
     *h_out = h;
     return true;
@@ -225,7 +225,7 @@ __device__ __forceinline__ bool item_range(const PrepArgs& a, int64_t item, int6
 // the TMA tiles in `region`, scratch in `region` once the inputs are in
 // registers, packet image in `region` at the end.
 __device__ __forceinline__ void prep_item(uint8_t* region, int bid, int hw, float beta_f,
-                                          int64_t len, float scale, int lane) {
+                                          int32_t len, float scale, int lane) {
     const uint8_t* in = region;
     uint8_t* ws = region;
     uint8_t* sc = region;
@@ -555,70 +555,80 @@ __device__ __forceinline__ uint64_t* pair_barrier(uint8_t* smem, int pair, int h
     return bar;
 }
 
+// What a pair needs beside its items when it runs in a one-launch kernel,
+// kept in the pair's shared memory and read by its issuing thread where it is
+// used (held in registers across an item, these values made the item code
+// spill).
+struct PairCtl {
+    uint32_t* ready;     // ready[chunk * H + head] = 1 once that packet is in global memory
+    uint32_t* counter;   // a zeroed global word the pairs take item numbers from, or null
+    int64_t slot;        // counter mode: the next item's number, from the issuing thread
+};
+
 // A pair's share of the items: items first, first + stride, ... .  Both warps
-// run this loop; warp 0's lane 0 issues the copies.  With `ready` set,
-// ready[chunk * H + head] (the packet's index) becomes 1 (release, GPU scope)
-// once the item's packet is in global memory; the flag of an item is
-// published when the pair has issued the next item's loads, or at the end.
-// With `counter` (a zeroed global word) the pairs instead take items in
-// order from it (atomicAdd by the pair's issuing thread once the item's loads
-// are issued, handed to the other warp through `slot`, a shared word of the
-// pair), so that faster pairs take more items; `first` and `stride` are then
-// unused.
+// run this loop; warp 0's lane 0 issues the copies.  With `ctl` (one-launch
+// kernels), ctl->ready[chunk * H + head] (the packet's index) becomes 1
+// (release, GPU scope) once the item's packet is in global memory; the flag
+// of an item is published when the pair has issued the next item's loads, or
+// at the end.  With ctl->counter the pairs instead take items in order from
+// it (atomicAdd by the pair's issuing thread once the item's loads are
+// issued, handed to the other warp through ctl->slot), so that faster pairs
+// take more items; `first` and `stride` are then unused.
 __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& maps, uint8_t* region,
                                           uint64_t* bar, int bid, int hw, int lane, int64_t first,
-                                          int64_t stride, uint32_t* ready,
-                                          uint32_t* counter = nullptr,
-                                          volatile int64_t* slot = nullptr) {
-    int64_t pending = -1;   // item whose packet store is in flight, not yet published
+                                          int64_t stride, volatile PairCtl* ctl) {
+    int32_t pending = -1;   // packet whose store is in flight, not yet published
     if (a.geo.cu_chunks && !*a.geo.valid) return;
     const bool issuer = hw == 0 && lane == 0;
+    const uint32_t n_items = static_cast<uint32_t>(a.n_chunk_heads);
+    const bool counted = ctl && ctl->counter;
 
     uint32_t phase = 0;
-    int64_t item = first;
-    if (counter) {
-        if (issuer) *slot = static_cast<int64_t>(atomicAdd(counter, 1u));
+    uint32_t item = static_cast<uint32_t>(first);
+    const uint32_t step = static_cast<uint32_t>(stride);
+    if (counted) {
+        if (issuer) ctl->slot = static_cast<int64_t>(atomicAdd(ctl->counter, 1u));
         pair_sync(bid);
-        item = *slot;
+        item = static_cast<uint32_t>(ctl->slot);
     }
-    while (item < a.n_chunk_heads) {
-        int64_t t0, len, c, h;
+    while (item < n_items) {
+        int32_t t0, len, c, h;
         if (!item_range(a, item, &t0, &len, &c, &h)) break;   // items only grow past the end
-        int64_t next = item + stride;
+        // (item + step cannot wrap: items < 2^31 and the pairs number far fewer.)
+        uint32_t next = item + step;
         if (issuer) {
             // The previous packet store must have read the region before TMA
             // overwrites it; the region's generic-proxy writes were fenced
             // (fence.proxy.async) before that store.
             bulk_wait_read_all();
             mbar_arrive_expect_tx(bar, kInBytes);
-            const int32_t x = static_cast<int32_t>(h * kHeadDim), y = static_cast<int32_t>(t0);
+            const int32_t x = h * kHeadDim, y = t0;
             tma_load_2d(region + kInQ, &maps.q, x, y, bar);
             tma_load_2d(region + kInK, &maps.k, x, y, bar);
             tma_load_2d(region + kInG, &maps.g, x, y, bar);
             // The next item's number, once this item's loads are on their way
             // (the atomic's round trip then overlaps them).
-            if (counter) {
-                next = static_cast<int64_t>(atomicAdd(counter, 1u));
-                *slot = next;   // read by the other warp after the barrier below
+            if (counted) {
+                next = atomicAdd(ctl->counter, 1u);
+                ctl->slot = static_cast<int64_t>(next);   // read by the other warp after the barrier below
             }
             // This pair's next item: its tiles on their way to L2 while this
             // item is worked on, so that its loads above find them there.
-            int64_t nt0, nlen, nc, nh;
-            if (next < a.n_chunk_heads && item_range(a, next, &nt0, &nlen, &nc, &nh)) {
-                const int32_t nx = static_cast<int32_t>(nh * kHeadDim), ny = static_cast<int32_t>(nt0);
-                tma_prefetch_l2_2d(&maps.q, nx, ny);
-                tma_prefetch_l2_2d(&maps.k, nx, ny);
-                tma_prefetch_l2_2d(&maps.g, nx, ny);
+            int32_t nt0, nlen, nc, nh;
+            if (next < n_items && item_range(a, next, &nt0, &nlen, &nc, &nh)) {
+                tma_prefetch_l2_2d(&maps.q, nh * kHeadDim, nt0);
+                tma_prefetch_l2_2d(&maps.k, nh * kHeadDim, nt0);
+                tma_prefetch_l2_2d(&maps.g, nh * kHeadDim, nt0);
             }
-            if (ready && pending >= 0) {
+            if (ctl && pending >= 0) {
                 // The previous packet is complete in global memory: publish it.
                 bulk_wait_all();
                 fence_proxy_async_global();
-                st_release_gpu(ready + pending, 1u);
+                st_release_gpu(ctl->ready + pending, 1u);
                 pending = -1;
             }
         }
-        float beta_f = lane < len ? __bfloat162float(a.beta[(t0 + lane) * a.H + h]) : 0.f;
+        float beta_f = lane < len ? __bfloat162float(a.beta[(static_cast<int64_t>(t0) + lane) * a.H + h]) : 0.f;
         // beta from a logit ("flashinfer kda_prefill", beta_is_logit):
         // sigmoid(x) = 1 / (1 + e^-x) in FP32; e^-x = inf for very negative x
         // gives 0, as it should.  Padding lanes stay 0.
@@ -629,24 +639,24 @@ __device__ __forceinline__ void run_items(const PrepArgs& a, const PrepMaps& map
             if (!got) mbar_wait_bounded_sleep(bar, phase, a.geo.status);
             break;
         }
-        if (counter) next = *slot;   // the issuer's write precedes the barrier above
+        if (counted) next = static_cast<uint32_t>(ctl->slot);   // the issuer's write precedes the barrier above
         phase ^= 1u;
         prep_item(region, bid, hw, beta_f, len, a.scale, lane);
 
         // Publish the packet with one bulk copy.
         if (issuer) {
-            bulk_s2g(a.packets + (c * a.H + h) * static_cast<int64_t>(kPacketBytes), region,
-                     kPacketBytes);
+            const int32_t pk = c * static_cast<int32_t>(a.H) + h;   // the packet's index
+            bulk_s2g(a.packets + static_cast<int64_t>(pk) * kPacketBytes, region, kPacketBytes);
             bulk_commit();
-            pending = c * a.H + h;   // the packet's index (the item's, unless interleaved)
+            pending = pk;
         }
         item = next;
     }
     if (issuer) {
         bulk_wait_all();
-        if (ready && pending >= 0) {
+        if (ctl && pending >= 0) {
             fence_proxy_async_global();
-            st_release_gpu(ready + pending, 1u);
+            st_release_gpu(ctl->ready + pending, 1u);
         }
     }
     __syncwarp();
