@@ -72,17 +72,17 @@ PREP_SOURCES = ("kda_prep.cu", "kda_prep_impl.cuh", "kda_common.cuh")
 SEG_SOURCES = ("kda_segments.cu", "kda_common.cuh")
 FUSED_SOURCES = ("kda_fused.cu", "kda_prep_impl.cuh", "kda_rec_impl.cuh", "kda_common.cuh")
 PROFILED_TRAFFIC = {
-    ("chunk_prep", "t8192_h6"): (52.8e6, PREP_SOURCES, "5d2fede34bf3ae58"),
+    ("chunk_prep", "t8192_h6"): (52.8e6, PREP_SOURCES, "49c80c6456fccd98"),
     ("transition", "t8192_h6"): (55.6e6, REC_SOURCES, "694d11e96e58d88a"),
     ("segment_chain", "t8192_h6"): (10.0e6, SEG_SOURCES, "1b0f3949273b91b6"),
     ("recurrence", "t8192_h6"): (61.0e6, REC_SOURCES, "694d11e96e58d88a"),
-    ("fused", "t8192_h96"): (1854.0e6, FUSED_SOURCES, "6aa575badb9dd439"),
-    ("chunk_prep", "t8192_h96"): (1454.9e6, PREP_SOURCES, "5d2fede34bf3ae58"),
+    ("fused", "t8192_h96"): (1854.1e6, FUSED_SOURCES, "e007fafac3c3037e"),
+    ("chunk_prep", "t8192_h96"): (1454.6e6, PREP_SOURCES, "49c80c6456fccd98"),
     ("recurrence", "t8192_h96"): (1067.0e6, REC_SOURCES, "694d11e96e58d88a"),
     ("transition", "t65536_h1"): (75.7e6, REC_SOURCES, "694d11e96e58d88a"),
     ("segment_chain", "t65536_h1"): (20.3e6, SEG_SOURCES, "1b0f3949273b91b6"),
-    ("fused", "t256_h1"): (0.4e6, FUSED_SOURCES, "6aa575badb9dd439"),
-    ("fused", "varlen8_h12"): (681.1e6, FUSED_SOURCES, "6aa575badb9dd439"),
+    ("fused", "t256_h1"): (0.4e6, FUSED_SOURCES, "e007fafac3c3037e"),
+    ("fused", "varlen8_h12"): (681.3e6, FUSED_SOURCES, "e007fafac3c3037e"),
 }
 
 
