@@ -638,8 +638,33 @@ __global__ void __launch_bounds__(kTransWarps * 32, 1)
         for (int64_t cc = c; cc < issued; ++cc)
             mbar_wait_bounded(&full[cc % kQuadStages], (cc / kQuadStages) & 1, a.status);
     }
+    // F and Z leave in the segment chain's fragment order (fmap_frag_off,
+    // zmap_frag_off): this warp's value tiles are 4 (warp % 4) + nt.
     __nv_bfloat16* dst = ident ? a.final_ident : a.final_state;
-    if (ok && dst) wide_store_state<4>(dst + state_base, Sf, vcol, g8, t4);
+    if (ok && dst) {
+        uint8_t* base = reinterpret_cast<uint8_t*>(dst + state_base);
+        const uint32_t q = static_cast<uint32_t>(warp % kQuadWarps);
+#pragma unroll
+        for (int mt = 0; mt < 8; ++mt) {
+            if (ident) {
+#pragma unroll
+                for (int p = 0; p < 2; ++p) {
+                    const uint4 r = make_uint4(pack_bf16(Sf[mt][2 * p][0], Sf[mt][2 * p][1]),
+                                               pack_bf16(Sf[mt][2 * p][2], Sf[mt][2 * p][3]),
+                                               pack_bf16(Sf[mt][2 * p + 1][0], Sf[mt][2 * p + 1][1]),
+                                               pack_bf16(Sf[mt][2 * p + 1][2], Sf[mt][2 * p + 1][3]));
+                    *reinterpret_cast<uint4*>(base + fmap_frag_off(mt, 2 * q + p, lane)) = r;
+                }
+            } else {
+#pragma unroll
+                for (int nt = 0; nt < 4; ++nt) {
+                    const uint2 r = make_uint2(pack_bf16(Sf[mt][nt][0], Sf[mt][nt][1]),
+                                               pack_bf16(Sf[mt][nt][2], Sf[mt][nt][3]));
+                    *reinterpret_cast<uint2*>(base + zmap_frag_off(4 * q + nt, mt, lane)) = r;
+                }
+            }
+        }
+    }
 }
 
 template <int NCG>

@@ -15,11 +15,15 @@
 // chains of one segment's chunks plus this short chain of segment steps.
 //
 // One CTA per (sequence, head, 8 value rows of S): the rows of S update
-// independently.  Four consumer warps each form 32 key columns of the new
-// rows as (S_{j+1})^T = F_j^T S_j^T + Z_j^T on the warp MMA (BF16 operands,
-// FP32 accumulation; the FP32 rows stay in registers), and swap their BF16
-// slices through shared memory for the next step's operand.  A producer warp
-// streams F_j and the CTA's rows of Z_j through a TMA ring.
+// independently.  Eight warps each form 16 key columns of the new rows as
+// (S_{j+1})^T = F_j^T S_j^T + Z_j^T on the warp MMA (BF16 operands, FP32
+// accumulation; the FP32 rows stay in registers), and swap their BF16 slices
+// through shared memory for the next step's operand.  The transition pass
+// stores F and Z in the MMA's fragment order (kda_common.cuh), so each warp
+// loads its A tiles of F_j^T and its C tile of Z_j^T straight into registers,
+// two steps ahead, with one coalesced load per tile: every CTA needs all of
+// F_j each step, and staging it through shared memory (a TMA copy in, a
+// transposing ldmatrix out) made that traffic the step's bound.
 #include <cuda.h>
 
 #include "kda_common.cuh"
@@ -29,15 +33,10 @@ namespace kda {
 namespace {
 
 constexpr int kScanRows = 8;     // value rows of the state per CTA
-constexpr int kScanWarps = 4;    // consumer warps, 32 keys each
-constexpr int kScanStages = 3;
-constexpr uint32_t kScanFBytes = kHeadDim * kHeadDim * 2;      // F: two SW128 slabs [128][64]
-constexpr uint32_t kScanZBytes = kScanRows * kHeadDim * 2;     // Z rows: two SW128 slabs [8][64]
-constexpr uint32_t kScanStageBytes = ((kScanFBytes + kScanZBytes + 1023) / 1024) * 1024;
+constexpr int kScanWarps = 8;    // warps, 16 keys (one m tile) each
+constexpr int kScanThreads = kScanWarps * 32;
 constexpr uint32_t kScanXBytes = kScanRows * kHeadDim * 2;     // one BF16 copy of the CTA's rows
-constexpr uint32_t kScanXOff = kScanStages * kScanStageBytes;
-constexpr uint32_t kScanBarOff = kScanXOff + 2 * kScanXBytes;
-constexpr uint32_t kScanSmemBytes = kScanBarOff + 2 * kScanStages * 8 + 1024;
+constexpr int64_t kMapElems = int64_t(kHeadDim) * kHeadDim;    // one map or state
 
 // Byte offset of (row v, keys 8 ch .. 8 ch + 7) in a [8][128] BF16 copy of
 // the CTA's rows; the 16-byte chunks of row v are XOR-swizzled by v so that
@@ -61,10 +60,29 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t* r, uint32_t addr) {
 __device__ __forceinline__ float bf_lo(uint32_t x) { return __uint_as_float(x << 16); }
 __device__ __forceinline__ float bf_hi(uint32_t x) { return __uint_as_float(x & 0xffff0000u); }
 
+// Read-only loads of map fragments (the maps are written by an earlier launch).
+__device__ __forceinline__ uint4 ld_map16(const uint8_t* p) {
+    uint4 r;
+    asm volatile("ld.global.nc.v4.u32 {%0,%1,%2,%3}, [%4];"
+                 : "=r"(r.x), "=r"(r.y), "=r"(r.z), "=r"(r.w)
+                 : "l"(p));
+    return r;
+}
+__device__ __forceinline__ uint2 ld_map8(const uint8_t* p) {
+    uint2 r;
+    asm volatile("ld.global.nc.v2.u32 {%0,%1}, [%2];" : "=r"(r.x), "=r"(r.y) : "l"(p));
+    return r;
+}
+
 struct ScanArgs {
     const __nv_bfloat16* init_state;   // [N][H][128][128] or null
     __nv_bfloat16* final_state;        // [N][H][128][128] or null
     __nv_bfloat16* starts;             // [segments][H][128][128]
+    // F maps (fmap_frag_off order) and Z states (zmap_frag_off order),
+    // [total][H] of 32 KB each.
+    const uint8_t* fmaps;
+    const uint8_t* zmaps;
+    int64_t total;
     // Sequence n's segments: seg_begin[n] .. seg_begin[n + 1] - 1 (packed
     // layout), or n segs .. n segs + segs - 1 (seg_begin null: fixed layout).
     const int64_t* seg_begin;
@@ -75,46 +93,45 @@ struct ScanArgs {
     // groups 0: off).  CTA sequence n is group n % groups of sequence
     // n / groups: segments gs = (n / groups) segs + (n % groups) group_segs
     // and on, up to group_segs of them.  The grid's first half composes the
-    // F maps (src[0], no Z), the second half the Z maps (src[1], adding Z):
-    // state_0 = src[gs], state_j = state_{j-1} F_{gs+j} (+ Z_{gs+j}); state_j
-    // goes to prefix[p][gs + j] and the last one to gmap[p][n].
+    // F maps (no Z), the second half the Z maps (adding Z):
+    // state_0 = map gs, state_j = state_{j-1} F_{gs+j} (+ Z_{gs+j}); state_j
+    // goes to prefix[p][gs + j] (rows) and the last one to gmap[p][n], in the
+    // fragment order of its kind so that the chain over the groups reads it
+    // like the segment maps.
     int64_t groups, group_segs;
-    const __nv_bfloat16* src[2];
     __nv_bfloat16* prefix[2];
     __nv_bfloat16* gmap[2];
 };
 
-// Warp w's slice (keys 32 w .. 32 w + 31 of the CTA's 8 rows) of a state in
+// Warp w's slice (keys 16 w .. 16 w + 15 of the CTA's 8 rows) of a state in
 // C-fragment form (m = key, n = value row), rounded to BF16, into the copy at x.
-__device__ __forceinline__ void put_rows(uint8_t* x, const float (&c)[2][4], int w, int g8, int t4) {
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-        const uint32_t lo = movm_trans(pack_bf16(c[mt][0], c[mt][1]));   // row g8, keys base + 2 t4
-        const uint32_t hi = movm_trans(pack_bf16(c[mt][2], c[mt][3]));   // keys base + 8 + 2 t4
-        const uint32_t base = 32 * w + 16 * mt;
-        *reinterpret_cast<uint32_t*>(x + x_off(g8, base / 8) + 4 * t4) = lo;
-        *reinterpret_cast<uint32_t*>(x + x_off(g8, base / 8 + 1) + 4 * t4) = hi;
-    }
+__device__ __forceinline__ void put_rows(uint8_t* x, const float (&c)[4], int w, int g8, int t4) {
+    const uint32_t lo = movm_trans(pack_bf16(c[0], c[1]));   // row g8, keys 16 w + 2 t4
+    const uint32_t hi = movm_trans(pack_bf16(c[2], c[3]));   // keys 16 w + 8 + 2 t4
+    *reinterpret_cast<uint32_t*>(x + x_off(g8, 2 * w) + 4 * t4) = lo;
+    *reinterpret_cast<uint32_t*>(x + x_off(g8, 2 * w + 1) + 4 * t4) = hi;
 }
 
 // The CTA's 8 rows from the copy at x into rows [8][128] at dst (thread tid
-// of the 128 consumers copies 16 bytes).
+// < 128 copies 16 bytes).
 __device__ __forceinline__ void copy_rows_out(const uint8_t* x, __nv_bfloat16* dst, int tid) {
     const int v = tid >> 4, ch = tid & 15;
     const uint4 val = *reinterpret_cast<const uint4*>(x + x_off(v, ch));
     *reinterpret_cast<uint4*>(dst + v * kHeadDim + 8 * ch) = val;
 }
 
-__global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
-    segment_scan_kernel(ScanArgs a, const __grid_constant__ CUtensorMap fmap,
-                        const __grid_constant__ CUtensorMap zmap) {
-    extern __shared__ uint8_t smem_raw[];
-    uint8_t* smem = reinterpret_cast<uint8_t*>(
-        (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kScanBarOff);
-    uint64_t* empty = full + kScanStages;
+// Byte offset, within one map, of this lane's 8 bytes of C-fragment data for
+// m tile mt and value tile nt: in an F map the half of A tile (mt, nt / 2)
+// that holds value tile nt; in a Z map C tile (nt, mt).
+__device__ __forceinline__ uint32_t cfrag_off(bool fmap, uint32_t mt, uint32_t nt, uint32_t lane) {
+    return fmap ? fmap_frag_off(mt, nt >> 1, lane) + 8 * (nt & 1) : zmap_frag_off(nt, mt, lane);
+}
+
+__global__ void __launch_bounds__(kScanThreads, 2) segment_scan_kernel(ScanArgs a) {
+    __shared__ __align__(128) uint8_t xbuf[2 * kScanXBytes];
     const int warp = threadIdx.x >> 5;
     const int lane = threadIdx.x & 31;
+    const int tid = threadIdx.x;
     constexpr int kGroups = kHeadDim / kScanRows;
     const bool compose = a.groups > 0;
     int part = 0;
@@ -125,7 +142,8 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
         blk -= part * half;
     }
     const int64_t nh = blk / kGroups;
-    const int v0 = kScanRows * static_cast<int>(blk - nh * kGroups);
+    const int vt = static_cast<int>(blk - nh * kGroups);   // value tile: rows 8 vt .. 8 vt + 7
+    const int v0 = kScanRows * vt;
     const int64_t n = nh / a.H;
     const int64_t h = nh - n * a.H;
     if (a.valid && !*a.valid) return;
@@ -145,142 +163,107 @@ __global__ void __launch_bounds__((kScanWarps + 1) * 32, 1)
         nseg = a.seg_begin ? a.seg_begin[n + 1] - first : a.segs;
         step0 = first;
     }
-    const bool add_z = !compose || part == 1;
-    __nv_bfloat16* const starts = compose ? (part ? a.prefix[1] : a.prefix[0]) : a.starts;
-    if (threadIdx.x == 0) {
-        for (int s = 0; s < kScanStages; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], kScanWarps);
-        }
-        fence_barrier_init();
-    }
-    __syncthreads();
-
-    if (warp == kScanWarps) {
-        // ------------------------------------------------------------ producer
-        uint32_t fill_parity = 0, filled = 0;
-        bool ok = true;
-        for (int64_t j = 0; j < nseg && ok; ++j) {
-            const int s = static_cast<int>(j % kScanStages);
-            if (j >= kScanStages)
-                ok = mbar_wait_warp_sleep(&empty[s], ((j / kScanStages) - 1) & 1, a.status);
-            if (!ok) break;
-            uint8_t* stage = smem + s * kScanStageBytes;
-            if (lane == 0) {
-                const int32_t row = static_cast<int32_t>(((step0 + j) * a.H + h) * kHeadDim);
-                mbar_arrive_expect_tx(&full[s], kScanFBytes + kScanZBytes);
-                tma_load_2d(stage, &fmap, 0, row, &full[s]);
-                tma_load_2d(stage + kScanFBytes / 2, &fmap, 64, row, &full[s]);
-                tma_load_2d(stage + kScanFBytes, &zmap, 0, row + v0, &full[s]);
-                tma_load_2d(stage + kScanFBytes + kScanZBytes / 2, &zmap, 64, row + v0, &full[s]);
-            }
-            __syncwarp();
-            fill_parity ^= (filled >> s & 1u) << s;
-            filled |= 1u << s;
-        }
-        if (!ok)
-            for (int s = 0; s < kScanStages; ++s)
-                if (filled >> s & 1u) mbar_wait_bounded(&full[s], (fill_parity >> s) & 1u, a.status);
+    // Every map read below lies inside the [total][H] arrays.
+    if (first < 0 || nseg < 0 || step0 + nseg > a.total) {
+        if (tid == 0) atomicOr(a.status, kDevBadSeqlens);
         return;
     }
-
-    // ---------------------------------------------------------------- consumers
+    const bool add_z = !compose || part == 1;
+    __nv_bfloat16* const starts = compose ? (part ? a.prefix[1] : a.prefix[0]) : a.starts;
     const int g8 = lane >> 2, t4 = lane & 3;
-    const int tid = threadIdx.x;   // 0 .. 127
-    uint8_t* xbuf = smem + kScanXOff;
     const int64_t rows0 = (n * a.H + h) * kHeadDim + v0;   // first row of this CTA in [N][H][128]
-    // The initial state: the caller's (per sequence), or when composing the
-    // group's first segment map.
-    const __nv_bfloat16* init = compose ? (part ? a.src[1] : a.src[0]) + ((first * a.H + h) * kHeadDim + v0) * kHeadDim
-                                        : (a.init_state ? a.init_state + rows0 * kHeadDim : nullptr);
 
-    // S_0^T for keys 32 warp + 16 mt + {g8, g8 + 8}, rows v0 + 2 t4 + {0, 1}.
-    float c[2][4];
-#pragma unroll
-    for (int mt = 0; mt < 2; ++mt) {
-        const int key = 32 * warp + 16 * mt + g8;
-        if (init) {
-            const __nv_bfloat16* src = init + 2 * t4 * kHeadDim;
-            c[mt][0] = __bfloat162float(src[key]);
-            c[mt][1] = __bfloat162float(src[kHeadDim + key]);
-            c[mt][2] = __bfloat162float(src[key + 8]);
-            c[mt][3] = __bfloat162float(src[kHeadDim + key + 8]);
-        } else {
-            c[mt][0] = c[mt][1] = c[mt][2] = c[mt][3] = 0.f;
-        }
+    // S_0^T for keys 16 warp + {g8, g8 + 8}, rows v0 + 2 t4 + {0, 1}: the
+    // caller's initial state (rows), or when composing the group's first
+    // segment map (fragment order).
+    float c[4];
+    if (compose) {
+        const uint8_t* src = (part ? a.zmaps : a.fmaps) + (first * a.H + h) * kMapElems * 2;
+        const uint2 p = ld_map8(src + cfrag_off(part == 0, warp, vt, lane));
+        c[0] = bf_lo(p.x);
+        c[1] = bf_hi(p.x);
+        c[2] = bf_lo(p.y);
+        c[3] = bf_hi(p.y);
+    } else if (a.init_state) {
+        const __nv_bfloat16* src = a.init_state + (rows0 + 2 * t4) * kHeadDim + 16 * warp + g8;
+        c[0] = __bfloat162float(src[0]);
+        c[1] = __bfloat162float(src[kHeadDim]);
+        c[2] = __bfloat162float(src[8]);
+        c[3] = __bfloat162float(src[kHeadDim + 8]);
+    } else {
+        c[0] = c[1] = c[2] = c[3] = 0.f;
     }
     put_rows(xbuf, c, warp, g8, t4);
-    bool ok = true;
+
+    // Step j's operands straight into registers: this warp's eight A tiles of
+    // F_j^T (m tile = warp) and its C tile of Z_j^T.  Two register sets: the
+    // loads of step j + 2 go out as soon as step j's MMAs have taken theirs.
+    uint32_t af[2][8][4], zf[2][2];
+    const int64_t map_stride = a.H * kMapElems * 2;   // bytes from one segment's map to the next
+    const uint8_t* fcur = a.fmaps + (step0 * a.H + h) * kMapElems * 2 + fmap_frag_off(warp, 0, lane);
+    const uint8_t* zcur = a.zmaps + (step0 * a.H + h) * kMapElems * 2 + zmap_frag_off(vt, warp, lane);
+    auto load_step = [&](int buf, int64_t j) {
+        const uint8_t* fp = fcur + j * map_stride;
+#pragma unroll
+        for (int kt = 0; kt < 8; ++kt) {
+            const uint4 r = ld_map16(fp + kt * 512);
+            af[buf][kt][0] = r.x;
+            af[buf][kt][1] = r.y;
+            af[buf][kt][2] = r.z;
+            af[buf][kt][3] = r.w;
+        }
+        if (add_z) {
+            const uint2 r = ld_map8(zcur + j * map_stride);
+            zf[buf][0] = r.x;
+            zf[buf][1] = r.y;
+        } else {
+            zf[buf][0] = zf[buf][1] = 0u;
+        }
+    };
+    if (nseg > 0) load_step(0, 0);
+    if (nseg > 1) load_step(1, 1);
+    __syncthreads();
 
     const uint32_t mi = lane >> 3, r8 = lane & 7;
-    // Step j's operands from its stage into registers: F_j^T (m = new key,
-    // k = old key) by transposing loads of F_j's rows (old key), and the C
-    // fragments of Z_j^T.  The stage is released after the step that loads
-    // it, once those loads have had the step's MMAs and barrier to complete.
-    uint32_t af[2][8][4], zf[4];
-    auto load_step = [&](int64_t j) -> bool {
-        const int s = static_cast<int>(j % kScanStages);
-        if (!mbar_wait_warp(&full[s], (j / kScanStages) & 1, a.status)) return false;
-        const uint8_t* stage = smem + s * kScanStageBytes;
-        ldsm_x4_trans(zf, smem_u32(stage + kScanFBytes + sw128_off(8, r8, 4 * warp + mi)));
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) {
-                const uint32_t row = 16 * kk + r8 + 8 * (mi >> 1);
-                const uint32_t ch = 4 * warp + 2 * mt + (mi & 1);
-                ldsm_x4_trans(af[mt][kk], smem_u32(stage + sw128_off(kHeadDim, row, ch)));
-            }
-        return true;
-    };
-    if (nseg > 0 && ok) {
-        ok = load_step(0);
-        if (ok) stage_release(&empty[0], lane);
-    }
-    ok = group_all<kScanWarps * 32>(1, ok);
-    for (int64_t j = 0; j < nseg && ok; ++j) {
+    // One step with register set `buf`.
+    auto step = [&](int buf, int64_t j) {
         const uint8_t* xc = xbuf + (j & 1) * kScanXBytes;
-        // B operand: S_j^T (k = key of S_j, n = value row), all 8 k-steps.
-        uint32_t b[8][2];
+        // Accumulators: Z_j^T (even k tiles; zero when composing the F maps)
+        // and zero (odd k tiles).
+        float acc[2][4];
+        acc[0][0] = bf_lo(zf[buf][0]);
+        acc[0][1] = bf_hi(zf[buf][0]);
+        acc[0][2] = bf_lo(zf[buf][1]);
+        acc[0][3] = bf_hi(zf[buf][1]);
+        acc[1][0] = acc[1][1] = acc[1][2] = acc[1][3] = 0.f;
+        // B operand: S_j^T (k = key of S_j, n = value row), two k tiles per load.
 #pragma unroll
         for (int kp = 0; kp < 4; ++kp) {
             uint32_t r[4];
             ldsm_x4(r, smem_u32(xc + x_off(r8, 4 * kp + mi)));
-            b[2 * kp][0] = r[0];
-            b[2 * kp][1] = r[1];
-            b[2 * kp + 1][0] = r[2];
-            b[2 * kp + 1][1] = r[3];
+            mma_bf16(acc[0], af[buf][2 * kp], r, acc[0]);
+            mma_bf16(acc[1], af[buf][2 * kp + 1], r + 2, acc[1]);
         }
-        // Accumulators: Z_j^T (even k-steps; zero when composing the F maps)
-        // and zero (odd k-steps).
-        float acc[2][2][4];
+        if (j + 2 < nseg) load_step(buf, j + 2);
+        // S_j out as this segment's incoming state.
+        if (tid < 128) copy_rows_out(xc, starts + (((first + j) * a.H + h) * kHeadDim + v0) * kHeadDim, tid);
 #pragma unroll
-        for (int mt = 0; mt < 2; ++mt) {
-            acc[mt][0][0] = add_z ? bf_lo(zf[2 * mt]) : 0.f;
-            acc[mt][0][1] = add_z ? bf_hi(zf[2 * mt]) : 0.f;
-            acc[mt][0][2] = add_z ? bf_lo(zf[2 * mt + 1]) : 0.f;
-            acc[mt][0][3] = add_z ? bf_hi(zf[2 * mt + 1]) : 0.f;
-            acc[mt][1][0] = acc[mt][1][1] = acc[mt][1][2] = acc[mt][1][3] = 0.f;
-        }
-#pragma unroll
-        for (int kk = 0; kk < 8; ++kk)
-#pragma unroll
-            for (int mt = 0; mt < 2; ++mt) mma_bf16(acc[mt][kk & 1], af[mt][kk], b[kk], acc[mt][kk & 1]);
-        // While the MMAs run: S_j out as this segment's incoming state, and
-        // the next step's operands in.
-        copy_rows_out(xc, starts + (((first + j) * a.H + h) * kHeadDim + v0) * kHeadDim, tid);
-        if (j + 1 < nseg && !load_step(j + 1)) ok = false;
-#pragma unroll
-        for (int mt = 0; mt < 2; ++mt)
-#pragma unroll
-            for (int e = 0; e < 4; ++e) c[mt][e] = acc[mt][0][e] + acc[mt][1][e];
+        for (int e = 0; e < 4; ++e) c[e] = acc[0][e] + acc[1][e];
         put_rows(xbuf + ((j + 1) & 1) * kScanXBytes, c, warp, g8, t4);
-        ok = group_all<kScanWarps * 32>(1, ok);
-        // Past the barrier the next step's loads have had time to complete.
-        if (j + 1 < nseg && ok) stage_release(&empty[(j + 1) % kScanStages], lane);
+        __syncthreads();
+    };
+    for (int64_t j = 0; j < nseg; j += 2) {
+        step(0, j);
+        if (j + 1 < nseg) step(1, j + 1);
     }
-    __nv_bfloat16* const fin = compose ? (part ? a.gmap[1] : a.gmap[0]) : a.final_state;
-    if (ok && fin) copy_rows_out(xbuf + (nseg & 1) * kScanXBytes, fin + rows0 * kHeadDim, tid);
+    if (compose) {
+        // The group's map, in the fragment order of its kind.
+        uint8_t* dst = reinterpret_cast<uint8_t*>(part ? a.gmap[1] : a.gmap[0]) + (n * a.H + h) * kMapElems * 2;
+        *reinterpret_cast<uint2*>(dst + cfrag_off(part == 0, warp, vt, lane)) =
+            make_uint2(pack_bf16(c[0], c[1]), pack_bf16(c[2], c[3]));
+    } else if (a.final_state && tid < 128) {
+        copy_rows_out(xbuf + (nseg & 1) * kScanXBytes, a.final_state + rows0 * kHeadDim, tid);
+    }
 }
 
 // ---------------------------------------------------------------------------
@@ -501,38 +484,25 @@ cudaError_t launch_segment_scan(const void* init_state, void* final_state, const
     const int64_t blocks = n_seqs * H * (kHeadDim / kScanRows);
     if (blocks <= 0) return cudaSuccess;
     const int64_t total_segs = seg_begin ? segs : n_seqs * segs;
-    const int64_t rows = (total_segs > 0 ? total_segs : 1) * H * kHeadDim;
-    if (rows >= (int64_t(1) << 31) || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    static bool configured[64] = {};
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-    if (!configured[dev]) {
-        cudaError_t e = cudaFuncSetAttribute(segment_scan_kernel,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(kScanSmemBytes));
-        if (e != cudaSuccess) return e;
-        configured[dev] = true;
-    }
-    CUtensorMap fmap, zmap;
-    cudaError_t e = encode_state_map(&fmap, transitions, rows, kHeadDim);
-    if (e == cudaSuccess) e = encode_state_map(&zmap, zero_start_states, rows, kScanRows);
-    if (e != cudaSuccess) return e;
+    if (total_segs * H * kHeadDim >= (int64_t(1) << 31) || blocks > 0x7fffffffLL)
+        return cudaErrorInvalidValue;
     ScanArgs a;
     a.init_state = static_cast<const __nv_bfloat16*>(init_state);
     a.final_state = static_cast<__nv_bfloat16*>(final_state);
     a.starts = static_cast<__nv_bfloat16*>(starts);
+    a.fmaps = static_cast<const uint8_t*>(transitions);
+    a.zmaps = static_cast<const uint8_t*>(zero_start_states);
+    a.total = total_segs;
     a.segs = segs;
     a.seg_begin = seg_begin;
     a.valid = valid;
     a.groups = 0;
     a.group_segs = 0;
-    a.src[0] = a.src[1] = nullptr;
     a.prefix[0] = a.prefix[1] = nullptr;
     a.gmap[0] = a.gmap[1] = nullptr;
     a.H = H;
     a.status = status;
-    segment_scan_kernel<<<static_cast<unsigned>(blocks), (kScanWarps + 1) * 32, kScanSmemBytes,
-                          stream>>>(a, fmap, zmap);
+    segment_scan_kernel<<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
@@ -553,9 +523,7 @@ bool configure_scan(int dev) {
     static bool configured[64] = {};
     if (dev < 0 || dev >= 64) return false;
     if (!configured[dev]) {
-        if (cudaFuncSetAttribute(segment_scan_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                 static_cast<int>(kScanSmemBytes)) != cudaSuccess ||
-            cudaFuncSetAttribute(segment_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        if (cudaFuncSetAttribute(segment_apply_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  static_cast<int>(kApplySmemBytes)) != cudaSuccess)
             return false;
         configured[dev] = true;
@@ -573,16 +541,13 @@ cudaError_t launch_segment_compose(const void* transitions, const void* zero_sta
     if (blocks <= 0) return cudaSuccess;
     const int64_t rows = n_seqs * segs * H * kHeadDim;
     if (rows >= (int64_t(1) << 31) || blocks > 0x7fffffffLL) return cudaErrorInvalidValue;
-    int dev = 0;
-    if (cudaGetDevice(&dev) != cudaSuccess || !configure_scan(dev)) return cudaErrorInvalidDevice;
-    CUtensorMap fmap, zmap;
-    cudaError_t e = encode_state_map(&fmap, transitions, rows, kHeadDim);
-    if (e == cudaSuccess) e = encode_state_map(&zmap, zero_start_states, rows, kScanRows);
-    if (e != cudaSuccess) return e;
     ScanArgs a;
     a.init_state = nullptr;
     a.final_state = nullptr;
     a.starts = nullptr;
+    a.fmaps = static_cast<const uint8_t*>(transitions);
+    a.zmaps = static_cast<const uint8_t*>(zero_start_states);
+    a.total = n_seqs * segs;
     a.seg_begin = nullptr;
     a.valid = nullptr;
     a.segs = segs;
@@ -590,14 +555,11 @@ cudaError_t launch_segment_compose(const void* transitions, const void* zero_sta
     a.status = status;
     a.groups = groups;
     a.group_segs = group_segs;
-    a.src[0] = static_cast<const __nv_bfloat16*>(transitions);
-    a.src[1] = static_cast<const __nv_bfloat16*>(zero_start_states);
     a.prefix[0] = static_cast<__nv_bfloat16*>(prefix_f);
     a.prefix[1] = static_cast<__nv_bfloat16*>(prefix_z);
     a.gmap[0] = static_cast<__nv_bfloat16*>(group_f);
     a.gmap[1] = static_cast<__nv_bfloat16*>(group_z);
-    segment_scan_kernel<<<static_cast<unsigned>(blocks), (kScanWarps + 1) * 32, kScanSmemBytes,
-                          stream>>>(a, fmap, zmap);
+    segment_scan_kernel<<<static_cast<unsigned>(blocks), kScanThreads, 0, stream>>>(a);
     return cudaGetLastError();
 }
 
