@@ -94,7 +94,9 @@ cudaError_t launch_recurrence(const void* v, void* out, const void* init_state,
 // First pass of the segmented scan (geo: a fixed layout with seg_chunks set):
 // for every segment and head, the BF16 state the segment's chunks lead to
 // from a zero state (zero_start_states) and from the identity with V taken as
-// zero (transitions: the segment's state map S -> S F), each [segments][H][128][128].
+// zero (transitions: the segment's state map S -> S F), each [segments][H] of
+// 32 KB: F in fmap_frag_off order, the zero-start state in zmap_frag_off
+// order (kda_segmap.cuh), the layouts the segment chain's MMA loads.
 cudaError_t launch_transition(const void* v, const uint8_t* packets, const SeqGeometry& geo,
                               int64_t H, void* zero_start_states, void* transitions, int* status,
                               cudaStream_t stream);
@@ -113,9 +115,10 @@ cudaError_t launch_segment_scan(const void* init_state, void* final_state, const
 
 // Two-level chain (fixed layout, segs segments per sequence in groups of
 // group_segs): first the composition inside each group — prefix maps
-// (prefix_f, prefix_z: [segments][H][128][128], entry s = the map of the
-// group's segments up to s) and the group maps (group_f, group_z:
-// [groups][H][128][128]); then launch_segment_scan over the group maps gives
+// (prefix_f, prefix_z: [segments][H][128][128] rows, entry s = the map of
+// the group's segments up to s) and the group maps (group_f, group_z:
+// [groups][H] in the fragment orders of transitions and zero_start_states);
+// then launch_segment_scan over the group maps gives
 // each group's incoming state; then launch_segment_apply forms every
 // segment's incoming state from its group's and the prefix before it.
 cudaError_t launch_segment_compose(const void* transitions, const void* zero_start_states,

@@ -26,6 +26,7 @@
 #include <mutex>
 
 #include "kda_common.cuh"
+#include "kda_segmap.cuh"
 #include "kda_launch.h"
 #include "kda_rec_impl.cuh"
 
@@ -483,7 +484,8 @@ cudaError_t launch_quad(const RecArgs& a, int64_t blocks, cudaStream_t stream) {
 // packets; each warp holds 32 value columns of its state over all 128 keys as
 // in the quad kernel and runs the U^T and S^T updates only (no P^T, no O).
 // Under the state's registers eight warps leave no room for a producer warp,
-// so warp 0 refills each stage once every warp has released it.
+// so warp 0 refills each stage once every warp has released it.  Z and F
+// leave in the segment chain's fragment order.
 // ---------------------------------------------------------------------------
 constexpr int kTransWarps = 2 * kQuadWarps;
 

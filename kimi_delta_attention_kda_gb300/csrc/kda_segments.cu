@@ -19,7 +19,7 @@
 // (S_{j+1})^T = F_j^T S_j^T + Z_j^T on the warp MMA (BF16 operands, FP32
 // accumulation; the FP32 rows stay in registers), and swap their BF16 slices
 // through shared memory for the next step's operand.  The transition pass
-// stores F and Z in the MMA's fragment order (kda_common.cuh), so each warp
+// stores F and Z in the MMA's fragment order (kda_segmap.cuh), so each warp
 // loads its A tiles of F_j^T and its C tile of Z_j^T straight into registers,
 // two steps ahead, with one coalesced load per tile: every CTA needs all of
 // F_j each step, and staging it through shared memory (a TMA copy in, a
@@ -27,6 +27,7 @@
 #include <cuda.h>
 
 #include "kda_common.cuh"
+#include "kda_segmap.cuh"
 #include "kda_launch.h"
 
 namespace kda {
