@@ -9,7 +9,8 @@ operand) fails at least one of them:
 * closed forms: pure decay (beta = 0), exact read-back (alpha = 1, beta = 1,
   q = k), orthonormal keys;
 * structure: linearity in (V, S_0), channel permutations, scale invariance of
-  the normalised q and k, packed = separate, split-and-continue;
+  the normalised q and k, packed = separate, split-and-continue, the affine
+  segment maps S -> S F + Z and their composition;
 * the second, chunkwise implementation (no shared code) for several chunk
   lengths and both inverse methods;
 * (I + R)^{-1} against a library inverse and its defining residual;
@@ -214,6 +215,46 @@ def test_split_and_continue(oracle_mod):
                                       beta[:, t0:], fa)
         assert rel_fro(np.concatenate([oa, ob], axis=1), o) < 1e-12
         assert rel_fro(fb, f) < 1e-12
+
+
+def test_segment_maps_compose(oracle_mod):
+    """With the keys, decays and betas fixed, a run of tokens maps the state
+    affinely, S_end = S_0 F + Z: F is the end state from S_0 = I with V = 0
+    (each value row evolves on its own, S <- S Diag(alpha)(I - beta k k^T)),
+    Z the end state from zero.  Consecutive runs compose, (F1, Z1) then
+    (F2, Z2) = (F1 F2, Z1 F2 + Z2), which is what a scan over segments of
+    chunks, and over groups of segments, relies on."""
+    d, H = 16, 2
+    # Weak decay, so that F keeps the incoming state (with g down to -5 it
+    # would be close to zero after a few tokens and pin nothing).
+    inp = small_inputs(B=1, T=48, H=H, d=d, seed=13, g_low=-0.05)
+    q, k, v, g, beta, s0 = map(f64, (inp["q"], inp["k"], inp["v"], inp["g"], inp["beta"],
+                                     inp["init_state"]))
+    eye = np.broadcast_to(np.eye(d), (1, H, d, d)).copy()
+    cuts = [0, 7, 23, 30, 48]
+    maps = []
+    for a, b in zip(cuts[:-1], cuts[1:]):
+        part = (q[:, a:b], k[:, a:b])
+        _, f = oracle_mod.kda_token(*part, np.zeros_like(v[:, a:b]), g[:, a:b], beta[:, a:b], eye)
+        _, z = oracle_mod.kda_token(*part, v[:, a:b], g[:, a:b], beta[:, a:b], None)
+        maps.append((f, z))
+    _, ref = oracle_mod.kda_token(q, k, v, g, beta, s0)
+    s = s0
+    for f, z in maps:
+        s = s @ f + z
+    assert rel_fro(s, ref) < 1e-12
+    # The first two segments' maps composed into one, then the rest.
+    (f1, z1), (f2, z2) = maps[0], maps[1]
+    s = s0 @ (f1 @ f2) + (z1 @ f2 + z2)
+    for f, z in maps[2:]:
+        s = s @ f + z
+    assert rel_fro(s, ref) < 1e-12
+    # Planted mistakes are caught: the map applied from the left, or transposed.
+    for wrong in (lambda s, f: f @ s, lambda s, f: s @ np.swapaxes(f, -1, -2)):
+        s = s0
+        for f, z in maps:
+            s = wrong(s, f) + z
+        assert rel_fro(s, ref) > 1e-2
 
 
 def test_empty_sequences(oracle_mod):
