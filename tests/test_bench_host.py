@@ -135,3 +135,15 @@ def test_call_roofline_counts_only_algorithmic_bytes():
                             "measured", 1925.9, "measured", "t8192_h6", 0)
     assert sum(k["method_bytes"] for k in r["kernels"].values()) == path
     assert r["dominant_kernel"] == "recurrence"
+
+
+def test_profiled_traffic_entries_match_sources():
+    """Every measured-traffic entry still matches the sources it was captured
+    from (a changed kernel needs a new capture or loses its entry), and the
+    figures are reported for the default engine only."""
+    for (kernel, workload), (nbytes, files, _digest) in bench.PROFILED_TRAFFIC.items():
+        for f in files:
+            assert os.path.exists(os.path.join(ROOT, "kimi_delta_attention_kda_gb300", "csrc", f)), f
+        assert bench.profiled_traffic(kernel, workload, 0) == nbytes, (kernel, workload)
+        assert bench.profiled_traffic(kernel, workload, 2) is None
+    assert bench.profiled_traffic("chunk_prep", "no_such_workload", 0) is None
